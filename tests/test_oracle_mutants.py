@@ -1,0 +1,57 @@
+"""Planted mistakes: each mutant is a copy of the oracle's C source with one plausible error (a
+dropped term, a wrong sign, a shifted bit, a transposed index).  The pin suite must reject every
+one of them, which shows the pins constrain each part of the oracle and not only its happy path.
+The mistakes are planted in a temporary copy of the oracle, on the CPU; nothing here touches a GPU.
+"""
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "tmap_oracle.c")
+
+MUTANTS = {
+    "swizzle_row_bits_shifted": ("(off >> 7)", "(off >> 8)"),
+    "swizzle_sector_bits_shifted": ("return off ^ (line << 4);", "return off ^ (line << 5);"),
+    "oob_upper_off_by_one": ("(uint64_t)g[i] >= m->dim[i]", "(uint64_t)g[i] > m->dim[i]"),
+    "oob_negative_dropped": ("if (g[i] < 0 || (uint64_t)g[i]", "if ((uint64_t)g[i] + 0 == 0 && (uint64_t)g[i]"),
+    "image_axes_transposed": (
+        "    for (uint32_t e1 = 0; e1 < box_of(m, 1); e1++)\n"
+        "    for (uint32_t e0 = 0; e0 < box_of(m, 0); e0++) {",
+        "    for (uint32_t e0 = 0; e0 < box_of(m, 0); e0++)\n"
+        "    for (uint32_t e1 = 0; e1 < box_of(m, 1); e1++) {"),
+    "grid_floor_not_ceil": ("return (m->dim[i] + m->box[i] - 1) / m->box[i];",
+                            "return m->dim[i] / m->box[i] + (m->dim[i] < m->box[i]);"),
+    "stride_index_transposed": ("off += g[i] * m->stride[i];",
+                                "off += g[i] * m->stride[m->rank - 1 - i];"),
+    "reduce_wrong_sign": ("d = d + a;", "d = d - a;"),
+    "checksum_tree_halves": ("sums[i] = sums[2 * i] + sums[2 * i + 1];",
+                             "sums[i] = sums[i] + sums[i + n / 2];"),
+    "mbar_ignores_tx": ("if (b->pending == 0 && b->tx == 0) {", "if (b->pending == 0) {"),
+    "store_writes_oob": ("    if (!in_bounds(m, g)) return;\n    uint8_t* dst = element_address(m, g);\n    for",
+                         "    uint8_t* dst = element_address(m, g);\n    if (!in_bounds(m, g)) dst = dst + 0;\n    for"),
+    "checksum_bits_dropped_high_byte": ("(img[orc_swz(off + 1, span)] << 8)",
+                                        "(img[orc_swz(off + 1, span)] << 0)"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not unique"
+    d = tmp_path / "oracle"
+    d.mkdir()
+    shutil.copy(os.path.join(ROOT, "oracle", "tmap_oracle.h"), d)
+    (d / "tmap_oracle.c").write_text(src.replace(old, new))
+    lib = d / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                    "-o", str(lib), str(d / "tmap_oracle.c")], check=True)
+    env = dict(os.environ, TMAP_ORACLE_LIB=str(lib))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"

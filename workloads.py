@@ -1,0 +1,148 @@
+"""Seeded synthetic inputs for descriptor-driven tiled tensor movement.
+
+This module only makes input bytes and describes the workloads' shapes; it holds none of the
+method's arithmetic (no swizzle, no box addressing, no reduction).  Both the CPU oracle's tests
+and the GPU path's tests and benchmark draw their inputs from here, so that both sides see the same
+bytes.
+
+Shapes follow the pages' examples ([MLSys-TMA] = mlc.ai "Modern GPU Programming for MLSys",
+chapter "异步数据搬运：TMA"):
+  W1  fp16 16 x 128, element (r, c) holds the bit pattern r*128 + c; one 8 x 64 box at (0, 0) and
+      at column 64 / row 8 (§"异步数据搬运：TMA", the interactive figure's 16 x 128 tensor and 8 x 64
+      tile).
+  W2  fp16 16 x 256 viewed as (group, row, col) slices of 128 columns (§"用 3D TMA 搬运多个 swizzle
+      atoms"), seeded random bit patterns that are never NaN or Inf.
+  W3  bf16 8192 x 8192, normal(0, 1) rounded to bf16, 128 x 64 boxes, 128-byte swizzle.
+  W4  bf16 16 x 4095 x 1000 stored with a padded row of 1024 elements (2048 bytes); the padding
+      holds the sentinel 0xDEAD.  Ragged 64 x 64 / 64 x 32 boxes and a rank-5 view
+      4 x 4 x 4095 x 10 x 100 whose 200-byte stride no tensor-map hardware can take.
+  W5a fp32 16384 x 16384 destination normal(0, 1) and source uniform(-1, 1), 128 x 32 boxes.
+  W5b bf16 A 8192 x 4096 and B 4096 x 8192, 128 x 64 tiles streamed through a 4-stage ring.
+
+Every shape list in this module is outermost first (how a user writes a matrix); the maps built
+from them list dims innermost first, as the tensor-map encoder wants.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+SENTINEL_U16 = 0xDEAD
+
+SEEDS = {"w2": 2, "w3": 3, "w4": 4, "w5a_dst": 51, "w5a_src": 52, "w5b_a": 53, "w5b_b": 54}
+
+
+def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """Round float32 values to bfloat16 (round to nearest, ties to even); returns uint16 bits.
+    Inputs are finite by construction."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    bias = np.uint32(0x7FFF) + ((u >> np.uint32(16)) & np.uint32(1))
+    return ((u + bias) >> np.uint32(16)).astype(np.uint16)
+
+
+def normal_bf16(shape, seed: int) -> np.ndarray:
+    """bf16 bit patterns of normal(0, 1) draws, shape outermost first."""
+    rng = np.random.default_rng(seed)
+    out = np.empty(int(np.prod(shape)), dtype=np.uint16)
+    chunk = 1 << 24
+    for i in range(0, out.size, chunk):
+        n = min(chunk, out.size - i)
+        out[i:i + n] = f32_to_bf16_bits(rng.standard_normal(n, dtype=np.float32))
+    return out.reshape(shape)
+
+
+def finite_f16_bits(shape, seed: int) -> np.ndarray:
+    """Uniform 16-bit patterns, redrawn wherever the fp16 exponent field is all ones (NaN / Inf)."""
+    rng = np.random.default_rng(seed)
+    x = rng.integers(0, 1 << 16, size=shape, dtype=np.uint32).astype(np.uint16)
+    while True:
+        bad = (x & 0x7C00) == 0x7C00
+        if not bad.any():
+            return x
+        x[bad] = rng.integers(0, 1 << 16, size=int(bad.sum()), dtype=np.uint32).astype(np.uint16)
+
+
+def w1_tensor() -> np.ndarray:
+    """fp16 16 x 128 whose element (r, c) carries the bit pattern r*128 + c."""
+    r = np.arange(16, dtype=np.uint32)[:, None]
+    c = np.arange(128, dtype=np.uint32)[None, :]
+    return (r * 128 + c).astype(np.uint16)
+
+
+def w2_tensor(seed: int = SEEDS["w2"]) -> np.ndarray:
+    return finite_f16_bits((16, 256), seed)
+
+
+def w3_tensor(rows: int = 8192, cols: int = 8192, seed: int = SEEDS["w3"]) -> np.ndarray:
+    return normal_bf16((rows, cols), seed)
+
+
+def w4_tensor(batch: int = 16, rows: int = 4095, cols: int = 1000, pitch: int = 1024,
+              seed: int = SEEDS["w4"]) -> np.ndarray:
+    """bf16 batch x rows x cols stored with a row pitch of `pitch` elements; the padding columns
+    cols..pitch-1 hold the sentinel."""
+    x = np.full((batch, rows, pitch), SENTINEL_U16, dtype=np.uint16)
+    x[:, :, :cols] = normal_bf16((batch, rows, cols), seed)
+    return x
+
+
+TINY_F32 = np.float32(2.0 ** -126)  # smallest normal binary32
+
+
+def w5a_tensors(rows: int = 16384, cols: int = 16384, seed_dst: int = SEEDS["w5a_dst"],
+                seed_src: int = SEEDS["w5a_src"]):
+    """fp32 destination normal(0, 1) and source uniform(-1, 1).  Pairs whose operands or exact sum
+    would be subnormal are redrawn, so flush-to-zero can never decide a result."""
+    rd = np.random.default_rng(seed_dst)
+    rs = np.random.default_rng(seed_src)
+    dst = rd.standard_normal((rows, cols), dtype=np.float32)
+    src = rs.uniform(-1.0, 1.0, size=(rows, cols)).astype(np.float32)
+    fd = dst.reshape(-1)
+    fs = src.reshape(-1)
+    chunk = 1 << 24
+    for i in range(0, fd.size, chunk):
+        d = fd[i:i + chunk]
+        s = fs[i:i + chunk]
+        while True:
+            exact = d.astype(np.float64) + s.astype(np.float64)
+            bad = (((np.abs(d) < TINY_F32) & (d != 0)) | ((np.abs(s) < TINY_F32) & (s != 0))
+                   | ((np.abs(exact) < float(TINY_F32)) & (exact != 0)))
+            if not bad.any():
+                break
+            s[bad] = rs.uniform(-1.0, 1.0, size=int(bad.sum())).astype(np.float32)
+            d[bad] = rd.standard_normal(int(bad.sum()), dtype=np.float32)
+    return dst, src
+
+
+def w5b_tensors(m: int = 8192, k: int = 4096, n: int = 8192, seed_a: int = SEEDS["w5b_a"],
+                seed_b: int = SEEDS["w5b_b"]):
+    """bf16 A (m x k) and B (k x n)."""
+    return normal_bf16((m, k), seed_a), normal_bf16((k, n), seed_b)
+
+
+# Map recipes, dims innermost first: (dims, byte strides of dims 1.., box, swizzle span)
+def w3_map(rows: int = 8192, cols: int = 8192, span: int = 128):
+    return dict(dims=[cols, rows], strides=[cols * 2], box=[64, 128], span=span, esize=2)
+
+
+def w4_rank3_map(box_cols: int, batch=16, rows=4095, cols=1000, pitch=1024, span=128):
+    return dict(dims=[cols, rows, batch], strides=[pitch * 2, rows * pitch * 2],
+                box=[box_cols, 64, 1], span=span, esize=2)
+
+
+def w4_rank5_map(batch=16, rows=4095, cols=1000, pitch=1024, span=0):
+    """The 4 x 4 x rows x 10 x 100 view: batch split 4 x 4, each row's first 1000 columns split
+    into 10 groups of 100 (a 200-byte group stride)."""
+    assert batch == 16 and cols == 1000
+    return dict(dims=[100, 10, rows, 4, 4],
+                strides=[200, pitch * 2, rows * pitch * 2, 4 * rows * pitch * 2],
+                box=[64, 10, 32, 1, 1], span=span, esize=2)
+
+
+def w5a_map(rows=16384, cols=16384, span=128):
+    return dict(dims=[cols, rows], strides=[cols * 4], box=[32, 128], span=span, esize=4)
+
+
+def w5b_maps(m=8192, k=4096, n=8192, span=128):
+    a = dict(dims=[k, m], strides=[k * 2], box=[64, 128], span=span, esize=2)
+    b = dict(dims=[n, k], strides=[n * 2], box=[64, 128], span=span, esize=2)
+    return a, b
