@@ -1,0 +1,188 @@
+// k_ring.cu -- the multi-stage producer/consumer ring that streams GEMM-operand-shaped tiles.
+//
+// [MLSys-TMA] = mlc.ai "Modern GPU Programming for MLSys", chapter "异步数据搬运：TMA".
+// §"把 TMA 放进 pipeline": while the consumer reads stage s the TMA engine fills the next stage; the
+// consumer waits for the load of a stage before reading it, and the producer waits until the
+// consumer is done with a stage before overwriting it.  §"如何等待 TMA load 完成": the two operand
+// tiles of a stage complete on ONE mbarrier whose expected byte count is their sum (2 x 2048 bytes
+// there, 2 x 16 KiB for 128 x 64 bf16 tiles).
+//
+// CTA = 3 warps.  Warp 0: producer, one elected lane.  Warp 1 consumes the A tile of each stage,
+// warp 2 the B tile.  full[s] (count 1) completes when both tiles' bytes have landed; empty[s]
+// (count 2) completes when both consumer warps have read the stage.
+//
+// Consumer reads follow [MLSys-TMA] §"128-byte swizzle 的分组要求": lane l reads image rows l, l+32,
+// ...; at any instant eight neighbouring lanes read the same logical sector c of eight consecutive
+// rows, which the 128B swizzle has spread over physical sectors c XOR (row % 8): eight distinct
+// bank sectors, no conflict.  With swizzle NONE the same reads all hit sector c (8-way conflict).
+//
+// What the consumer computes (the pages leave it open): per tile, each row is summed in fp32 in
+// logical element order starting from its first element; rows are combined by a pairwise-adjacent
+// tree (xor-shuffles 1, 2, 4, 8, 16 inside each 32-row block, then pairs of blocks); plus the exact
+// integer sum of the 16-bit patterns.
+#include "tm_ptx.cuh"
+
+namespace tmk {
+
+constexpr uint32_t kRingMaxStages = 8;
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+__global__ void __launch_bounds__(96, 1)
+    k_ring(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
+           const __grid_constant__ RingArgs r)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kRingMaxStages];
+    __shared__ __align__(8) uint64_t empty_bar[kRingMaxStages];
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + (kStageAlign - 1)) & ~(kStageAlign - 1);
+    const uint8_t* const stage0 = smem_raw + (base - raw);
+    const uint32_t S = r.stages;
+    const uint32_t tile = r.tile_bytes;  // multiple of 1024
+
+    const uint64_t first = blockIdx.x;
+    if (r.ntiles <= first) return;
+    const uint64_t n_local = (r.ntiles - 1 - first) / gridDim.x + 1;
+    const uint32_t warp = threadIdx.x >> 5;
+    const uint32_t lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < S; s++) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 2);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ---------------- producer ----------------
+        if (!elect_one()) return;
+        prefetch_tmap(&ma);
+        prefetch_tmap(&mb);
+        uint64_t i = 0;
+        for (; i < n_local; i++) {
+            const uint32_t s = (uint32_t)(i % S);
+            const uint64_t k = i / S;
+            if (k > 0) {
+                const uint32_t parity = (uint32_t)((k - 1) & 1);
+                if (!mbar_wait(smem_u32(&empty_bar[s]), parity, r.timeout_ns)) {
+                    record_timeout(r.status, K_STREAM, s, parity, first + i * gridDim.x);
+                    break;
+                }
+            }
+            const uint64_t t = first + i * gridDim.x;
+            const uint32_t bar = smem_u32(&full_bar[s]);
+            const int32_t ca[2] = {(int32_t)((t % r.a_nb0) * 64), (int32_t)((t / r.a_nb0) * r.rows)};
+            const int32_t cb[2] = {(int32_t)((t % r.b_nb0) * 64), (int32_t)((t / r.b_nb0) * r.rows)};
+            mbar_arrive_expect_tx(bar, 2 * tile);
+            tma_load<2>(base + s * 2 * tile, &ma, ca, bar);
+            tma_load<2>(base + s * 2 * tile + tile, &mb, cb, bar);
+        }
+        // Loads still landing (only after a failure): wait for them, bounded, before leaving.
+        const uint64_t lo = i > S ? i - S : 0;
+        for (uint64_t j = lo; j < i && i < n_local; j++) {
+            mbar_wait(smem_u32(&full_bar[j % S]), (uint32_t)((j / S) & 1), r.timeout_ns);
+        }
+        return;
+    }
+
+    // ---------------- consumers: warp 1 -> A, warp 2 -> B ----------------
+    const uint32_t which = warp - 1;
+    const uint32_t rpl = r.rows >> 5;  // rows per lane
+    float* const cs_out = which == 0 ? r.cs_a : r.cs_b;
+    unsigned long long* const bits_out = which == 0 ? r.bits_a : r.bits_b;
+    const uint32_t xr = r.swizzled ? 7u : 0u;
+
+    for (uint64_t i = 0; i < n_local; i++) {
+        const uint32_t s = (uint32_t)(i % S);
+        const uint32_t parity = (uint32_t)((i / S) & 1);
+        const bool ok = __all_sync(0xffffffffu,
+                                   mbar_wait(smem_u32(&full_bar[s]), parity, r.timeout_ns));
+        if (!ok) {
+            if (lane == 0) record_timeout(r.status, K_STREAM, s, parity, first + i * gridDim.x);
+            break;
+        }
+        const uint8_t* const t_img = stage0 + s * 2 * tile + which * tile;
+
+        float blk[8];
+        uint32_t bits = 0;
+#pragma unroll
+        for (uint32_t q = 0; q < 8; q++) {
+            if (q < rpl) {
+                const uint32_t row = lane + 32 * q;
+                const uint8_t* const rp = t_img + row * 128;
+                float acc = 0.f;
+#pragma unroll
+                for (uint32_t c = 0; c < 8; c++) {
+                    const uint4 v = *reinterpret_cast<const uint4*>(rp + ((c ^ (row & xr)) << 4));
+                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int h = 0; h < 4; h++) {
+                        acc = (c == 0 && h == 0) ? bf16lo(w[h]) : __fadd_rn(acc, bf16lo(w[h]));
+                        acc = __fadd_rn(acc, bf16hi(w[h]));
+                        bits += (w[h] & 0xffffu) + (w[h] >> 16);
+                    }
+                }
+                blk[q] = acc;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));  // stage read: release it
+
+        // pairwise tree: inside each 32-row block by xor-shuffles, then across blocks
+#pragma unroll
+        for (uint32_t q = 0; q < 8; q++) {
+            if (q < rpl) {
+                float v = blk[q];
+#pragma unroll
+                for (int m = 1; m < 32; m <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, m));
+                blk[q] = v;
+            }
+        }
+        for (uint32_t n = rpl; n > 1; n >>= 1) {
+#pragma unroll
+            for (uint32_t q = 0; q < 4; q++) {
+                if (q < n / 2) blk[q] = __fadd_rn(blk[2 * q], blk[2 * q + 1]);
+            }
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) bits += __shfl_xor_sync(0xffffffffu, bits, m);
+        if (lane == 0) {
+            const uint64_t t = first + i * gridDim.x;
+            cs_out[t] = blk[0];
+            bits_out[t] = (unsigned long long)bits;
+        }
+    }
+}
+
+__global__ void k_selftest(uint64_t timeout_ns, StatusBlock* st)
+{
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x != 0) return;
+    mbar_init(smem_u32(&bar), 1);
+    fence_barrier_init();
+    // Nothing ever arrives on `bar`: the wait must give up and report.
+    if (!mbar_wait(smem_u32(&bar), 0, timeout_ns)) record_timeout(st, K_SELFTEST, 0, 0, 0);
+}
+
+cudaError_t launch_ring(const CUtensorMap* a, const CUtensorMap* b, const RingArgs& r,
+                        uint32_t grid, size_t smem, cudaStream_t s)
+{
+    cudaError_t e =
+        cudaFuncSetAttribute(k_ring, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_ring<<<grid, 96, smem, s>>>(*a, *b, r);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_selftest(uint64_t timeout_ns, StatusBlock* status, cudaStream_t s)
+{
+    k_selftest<<<1, 32, 0, s>>>(timeout_ns, status);
+    return cudaGetLastError();
+}
+
+}  // namespace tmk

@@ -1,0 +1,106 @@
+// tm_internal.h -- launch parameters shared by the host side (tmap_host.cpp) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "tmap.h"
+
+namespace tmk {
+
+constexpr uint32_t kInlineBoxes = 8;   // explicit box lists up to this size travel in parameters
+constexpr uint32_t kStageAlign = 1024; // 128B swizzle is computed on smem address bits 4..9
+
+// Kernel ids recorded with a timeout.
+enum KernelId : uint32_t {
+    K_COPY = 1, K_ROUNDTRIP = 2, K_REDUCE = 3, K_STREAM = 4, K_FB_COPY = 5, K_FB_STORE = 6,
+    K_FB_REDUCE = 7, K_SELFTEST = 8
+};
+
+// Per-device status word written by a kernel whose bounded wait gave up.
+struct StatusBlock {
+    int code;          // 0 or TM_ETIMEOUT; first failure wins (atomicCAS)
+    uint32_t kernel;   // KernelId
+    uint32_t block;    // blockIdx.x
+    uint32_t stage;    // ring stage
+    uint64_t box;      // box (or tile) index
+    uint32_t phase;    // parity waited for
+    uint32_t pad[9];
+};
+static_assert(sizeof(StatusBlock) == 64, "status block is 64 bytes");
+
+// How a launch enumerates its boxes: the whole grid, a device list, or a short inline list.
+enum WalkMode : uint32_t { WALK_GRID = 0, WALK_LIST = 1, WALK_INLINE = 2 };
+
+struct BoxWalk {
+    uint64_t nbox;         // boxes handled by the launch
+    uint64_t grid_nb[5];   // boxes along each dim (grid mode)
+    uint32_t box[5];       // box shape (unused dims 1)
+    uint32_t rank;
+    uint32_t mode;         // WalkMode
+    const int32_t* list;   // nbox * rank coordinates (WALK_LIST)
+    int32_t inl[kInlineBoxes * 5];
+};
+
+// TMA-path streaming kernels (copy, round trip, reduce).
+struct StreamArgs {
+    BoxWalk walk;
+    uint64_t images;       // copy: destination images; round trip: source images
+    uint32_t box_bytes;
+    uint32_t stage_bytes;  // box_bytes rounded up to kStageAlign
+    uint32_t stages;
+    uint32_t pad;
+    uint64_t timeout_ns;
+    StatusBlock* status;
+};
+
+// Generic fallback kernels.
+struct FbArgs {
+    BoxWalk walk;
+    uint64_t base;         // tensor (destination for store / reduce) base address
+    uint64_t src_base;     // reduce: source tensor base
+    uint64_t dim[5];
+    int64_t stride[5];     // bytes, destination / tensor
+    int64_t src_stride[5]; // bytes, reduce source
+    uint64_t images;
+    uint32_t esize;
+    uint32_t span;         // swizzle span in bytes, 0 = none
+    uint32_t inner_bytes;  // box[0] * esize
+    uint32_t box_bytes;
+    uint32_t stage_bytes;
+    uint32_t rows;         // image rows = box_bytes / inner_bytes
+    uint64_t timeout_ns;
+    StatusBlock* status;
+};
+
+// Ring consumer (stream_tiles).
+struct RingArgs {
+    uint64_t ntiles;
+    uint64_t a_nb0, b_nb0;   // boxes along dim 0 of A and B
+    uint32_t rows;           // tile rows R (box[1]); rows are 128 bytes
+    uint32_t stages;
+    uint32_t tile_bytes;     // R * 128
+    uint32_t swizzled;       // 1 = 128B, 0 = none
+    float* cs_a;
+    float* cs_b;
+    unsigned long long* bits_a;
+    unsigned long long* bits_b;
+    uint64_t timeout_ns;
+    StatusBlock* status;
+};
+
+// Launchers (defined next to their kernels).  Return a cudaError_t.
+enum StreamKind : int { KIND_COPY = 0, KIND_ROUNDTRIP = 1, KIND_REDUCE = 2 };
+cudaError_t launch_tma_stream(int kind, uint32_t rank, const CUtensorMap* in_map,
+                              const CUtensorMap* out_map, const StreamArgs& a, uint32_t grid,
+                              size_t smem, cudaStream_t s);
+size_t tma_stream_kernel_max_smem();
+cudaError_t launch_fb_copy(const FbArgs& a, uint32_t grid, size_t smem, cudaStream_t s);
+cudaError_t launch_fb_store(const FbArgs& a, uint32_t grid, size_t smem, cudaStream_t s);
+cudaError_t launch_fb_reduce(const FbArgs& a, uint32_t grid, cudaStream_t s);
+cudaError_t launch_ring(const CUtensorMap* a, const CUtensorMap* b, const RingArgs& r,
+                        uint32_t grid, size_t smem, cudaStream_t s);
+cudaError_t launch_selftest(uint64_t timeout_ns, StatusBlock* status, cudaStream_t s);
+
+}  // namespace tmk

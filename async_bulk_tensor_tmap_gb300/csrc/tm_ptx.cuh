@@ -1,0 +1,285 @@
+// tm_ptx.cuh -- the asynchronous-copy primitives of the path, as inline PTX for sm_103a.
+//
+// Written from the PTX ISA semantics the pages describe:
+//   [MLSys-TMA] mlc.ai "Modern GPU Programming for MLSys", chapter "异步数据搬运：TMA"
+//   [Book-TMA]  fangpin "gpu-hpc-book", chapter 08 "Cuda TMA （Tensor Memory Accelerator）"
+//   [H200-TMA]  coolgpu "H200 · TMA · Tensor Memory Accelerator" feature card
+//
+// Every wait on an mbarrier here is bounded by a %globaltimer deadline: a wait that runs out
+// returns false and the caller records TM_ETIMEOUT instead of spinning forever.
+#pragma once
+
+#include <cuda.h>
+#include <stdint.h>
+
+#include "tm_internal.h"
+
+namespace tmk {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t gtimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// One thread of a full warp is chosen to issue ([MLSys-TMA] §"一个 thread 如何描述整个 tile": the
+// other lanes are masked while the request is submitted; [H200-TMA] §03: one issuing thread).
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t pred = 0;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "elect.sync _|P, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(pred));
+    return pred != 0;
+}
+
+// ---- mbarrier ([MLSys-TMA] §"如何等待 TMA load 完成", [Book-TMA] §"TMA 完成异步数据搬运") ------
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Makes initialised barriers visible to the async proxy (the TMA engine) before first use.
+__device__ __forceinline__ void fence_barrier_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy reads of them.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// One arrival plus `bytes` expected transaction bytes for the current phase.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+                 ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 P, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Waits until the phase with parity `parity` has completed or `limit_ns` has passed.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = gtimer_ns();
+    for (;;) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (gtimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// Records the first failure of the launch set in the device status word.
+__device__ __forceinline__ void record_timeout(StatusBlock* st, uint32_t kernel, uint32_t stage,
+                                               uint32_t phase, uint64_t box)
+{
+    if (atomicCAS(&st->code, 0, TM_ETIMEOUT) == 0) {
+        st->kernel = kernel;
+        st->block = blockIdx.x;
+        st->stage = stage;
+        st->phase = phase;
+        st->box = box;
+        __threadfence();
+    }
+}
+
+// ---- tensor-map copies ([Book-TMA] §"单 block、单 lane、单 tile 的 TMA load", §"TMA store",
+//      §"TMA reduce，把“搬运”和“归约”合并"; [H200-TMA] §04 ②) ----------------------------------
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
+}
+
+// Global -> shared box load completing `box_bytes` on mbarrier `bar`.
+template <int R>
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* m, const int32_t* c,
+                                         uint32_t bar)
+{
+    const uint64_t mp = reinterpret_cast<uint64_t>(m);
+    if constexpr (R == 1) {
+        asm volatile(
+            "cp.async.bulk.tensor.1d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2}], [%3];" ::"r"(dst), "l"(mp), "r"(c[0]), "r"(bar) : "memory");
+    } else if constexpr (R == 2) {
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst), "l"(mp), "r"(c[0]), "r"(c[1]), "r"(bar)
+            : "memory");
+    } else if constexpr (R == 3) {
+        asm volatile(
+            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst), "l"(mp), "r"(c[0]), "r"(c[1]),
+            "r"(c[2]), "r"(bar) : "memory");
+    } else if constexpr (R == 4) {
+        asm volatile(
+            "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst), "l"(mp), "r"(c[0]), "r"(c[1]),
+            "r"(c[2]), "r"(c[3]), "r"(bar) : "memory");
+    } else {
+        asm volatile(
+            "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+            " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst), "l"(mp), "r"(c[0]),
+            "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(bar) : "memory");
+    }
+}
+
+// Shared -> global box store (only in-bounds elements are written), tracked by a bulk group.
+template <int R>
+__device__ __forceinline__ void tma_store(const CUtensorMap* m, const int32_t* c, uint32_t src)
+{
+    const uint64_t mp = reinterpret_cast<uint64_t>(m);
+    if constexpr (R == 1) {
+        asm volatile("cp.async.bulk.tensor.1d.global.shared::cta.tile.bulk_group [%0, {%2}], [%1];"
+                     ::"l"(mp), "r"(src), "r"(c[0]) : "memory");
+    } else if constexpr (R == 2) {
+        asm volatile(
+            "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];"
+            ::"l"(mp), "r"(src), "r"(c[0]), "r"(c[1]) : "memory");
+    } else if constexpr (R == 3) {
+        asm volatile(
+            "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
+            ::"l"(mp), "r"(src), "r"(c[0]), "r"(c[1]), "r"(c[2]) : "memory");
+    } else if constexpr (R == 4) {
+        asm volatile(
+            "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group"
+            " [%0, {%2, %3, %4, %5}], [%1];"
+            ::"l"(mp), "r"(src), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]) : "memory");
+    } else {
+        asm volatile(
+            "cp.async.bulk.tensor.5d.global.shared::cta.tile.bulk_group"
+            " [%0, {%2, %3, %4, %5, %6}], [%1];"
+            ::"l"(mp), "r"(src), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4])
+            : "memory");
+    }
+}
+
+// Shared -> global element-wise add into the tensor (the map's type decides the add: fp32 here).
+template <int R>
+__device__ __forceinline__ void tma_reduce_add(const CUtensorMap* m, const int32_t* c,
+                                               uint32_t src)
+{
+    const uint64_t mp = reinterpret_cast<uint64_t>(m);
+    if constexpr (R == 1) {
+        asm volatile(
+            "cp.reduce.async.bulk.tensor.1d.global.shared::cta.add.tile.bulk_group [%0, {%2}], [%1];"
+            ::"l"(mp), "r"(src), "r"(c[0]) : "memory");
+    } else if constexpr (R == 2) {
+        asm volatile(
+            "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group"
+            " [%0, {%2, %3}], [%1];"
+            ::"l"(mp), "r"(src), "r"(c[0]), "r"(c[1]) : "memory");
+    } else if constexpr (R == 3) {
+        asm volatile(
+            "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+            " [%0, {%2, %3, %4}], [%1];"
+            ::"l"(mp), "r"(src), "r"(c[0]), "r"(c[1]), "r"(c[2]) : "memory");
+    } else if constexpr (R == 4) {
+        asm volatile(
+            "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group"
+            " [%0, {%2, %3, %4, %5}], [%1];"
+            ::"l"(mp), "r"(src), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]) : "memory");
+    } else {
+        asm volatile(
+            "cp.reduce.async.bulk.tensor.5d.global.shared::cta.add.tile.bulk_group"
+            " [%0, {%2, %3, %4, %5, %6}], [%1];"
+            ::"l"(mp), "r"(src), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4])
+            : "memory");
+    }
+}
+
+// ---- untiled bulk copies (contiguous bytes; both addresses 16-byte aligned, size % 16 == 0) ---
+__device__ __forceinline__ void bulk_load(uint32_t dst, uint64_t src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void bulk_store(uint64_t dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(dst), "r"(src), "r"(bytes) : "memory");
+}
+
+// ---- bulk async groups ([MLSys-TMA] §"如何等待 TMA store 完成": commit, then wait until the
+//      source buffer may be reused) ---------------------------------------------------------------
+__device__ __forceinline__ void bulk_commit()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// At most N committed groups may still be READING their shared-memory source.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// At most N committed groups may still be in flight (writes included).
+template <int N>
+__device__ __forceinline__ void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// ---- swizzle of an image byte offset (the hardware's placement; stages are 1024-byte aligned
+//      so the image offset and the shared-memory address agree on bits 4..9).
+//      [MLSys-TMA] §"用 3D TMA 搬运多个 swizzle atoms": 16-byte sector XOR (row % 8) in 128-byte rows;
+//      64B / 32B use two / one row bits. ----------------------------------------------------------
+__device__ __forceinline__ uint32_t swizzle_offset(uint32_t off, uint32_t span)
+{
+    const uint32_t bits = span == 128 ? 7u : span == 64 ? 3u : span == 32 ? 1u : 0u;
+    return off ^ (((off >> 7) & bits) << 4);
+}
+
+// ---- box addressing ------------------------------------------------------------------------
+// Start coordinates of the launch's box `b` (grid: k[i] * box[i] with dim 0 fastest).
+__device__ __forceinline__ void box_start(const BoxWalk& w, uint64_t b, int32_t* c)
+{
+    if (w.mode == WALK_GRID) {
+#pragma unroll
+        for (int i = 0; i < 5; i++) {
+            if (i < (int)w.rank) {
+                const uint64_t nb = w.grid_nb[i];
+                const uint64_t q = b / nb;
+                c[i] = (int32_t)((b - q * nb) * w.box[i]);
+                b = q;
+            } else {
+                c[i] = 0;
+            }
+        }
+    } else {
+        const int32_t* src = (w.mode == WALK_LIST) ? (w.list + b * w.rank) : (w.inl + b * w.rank);
+#pragma unroll
+        for (int i = 0; i < 5; i++) c[i] = i < (int)w.rank ? src[i] : 0;
+    }
+}
+
+}  // namespace tmk

@@ -1,0 +1,678 @@
+// tmap_host.cpp -- the C ABI of include/tmap.h: descriptor validation and encoding, path
+// selection, launch geometry, coordinate staging and the per-device status word.
+//
+// [MLSys-TMA] mlc.ai "Modern GPU Programming for MLSys", chapter "异步数据搬运：TMA"
+// [H200-TMA]  coolgpu "H200 · TMA · Tensor Memory Accelerator" feature card
+// [Book-TMA]  fangpin "gpu-hpc-book", chapter 08 "Cuda TMA （Tensor Memory Accelerator）"
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstddef>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "tm_internal.h"
+#include "tmap.h"
+
+using namespace tmk;
+
+static_assert(sizeof(tm_desc) == 384, "tm_desc is 384 bytes");
+static_assert(alignof(tm_desc) == 64, "tm_desc is 64-byte aligned");
+static_assert(offsetof(tm_desc, base) == 32, "tm_desc layout");
+static_assert(offsetof(tm_desc, box) == 120, "tm_desc layout");
+static_assert(offsetof(tm_desc, nbox) == 160, "tm_desc layout");
+static_assert(offsetof(tm_desc, box_bytes) == 200, "tm_desc layout");
+static_assert(offsetof(tm_desc, tmap) == 256, "tm_desc layout");
+static_assert(sizeof(CUtensorMap) == 128, "CUtensorMap is 128 bytes");
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what)
+{
+    return fail(TM_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+uint32_t esize_of(int dt)
+{
+    switch (dt) {
+        case TM_U8: return 1;
+        case TM_U16: case TM_F16: case TM_BF16: return 2;
+        case TM_U32: case TM_S32: case TM_F32: return 4;
+        case TM_U64: case TM_S64: case TM_F64: return 8;
+        default: return 0;
+    }
+}
+
+uint32_t span_of(uint32_t sw)
+{
+    return sw == TM_SWIZZLE_128B ? 128u : sw == TM_SWIZZLE_64B ? 64u : sw == TM_SWIZZLE_32B ? 32u : 0u;
+}
+
+uint64_t env_u64(const char* name, uint64_t dflt)
+{
+    const char* v = getenv(name);
+    if (!v || !*v) return dflt;
+    char* end = nullptr;
+    unsigned long long x = strtoull(v, &end, 10);
+    return (end && *end == 0) ? (uint64_t)x : dflt;
+}
+
+bool valid_desc(const tm_desc* d) { return d && d->magic == TM_DESC_MAGIC; }
+
+// ---- driver entry points (no link-time dependency on libcuda) ---------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+using ReplaceAddressFn = CUresult (*)(CUtensorMap*, void*);
+
+void* driver_symbol(const char* name)
+{
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    cudaError_t e = cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return p;
+}
+
+EncodeTiledFn encode_fn()
+{
+    static std::once_flag once;
+    static EncodeTiledFn fn = nullptr;
+    std::call_once(once, [] { fn = (EncodeTiledFn)driver_symbol("cuTensorMapEncodeTiled"); });
+    return fn;
+}
+
+ReplaceAddressFn replace_fn()
+{
+    static std::once_flag once;
+    static ReplaceAddressFn fn = nullptr;
+    std::call_once(once, [] { fn = (ReplaceAddressFn)driver_symbol("cuTensorMapReplaceAddress"); });
+    return fn;
+}
+
+// ---- per-device state ---------------------------------------------------------------------------
+struct DevState {
+    bool ready = false;
+    int sms = 0;
+    int smem_per_sm = 0;
+    int smem_optin = 0;
+    StatusBlock* status = nullptr;
+};
+
+std::mutex g_mu;
+DevState g_dev[64];
+
+int device_state(DevState** out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= 64) return fail(TM_EUNSUPPORTED, "device ordinal %d above 63", dev);
+    std::lock_guard<std::mutex> lk(g_mu);
+    DevState& d = g_dev[dev];
+    if (!d.ready) {
+        if ((e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev)) ||
+            (e = cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                        dev)) ||
+            (e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                        dev)))
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        if ((e = cudaMalloc((void**)&d.status, sizeof(StatusBlock))) != cudaSuccess)
+            return cuda_fail(e, "cudaMalloc(status word)");
+        if ((e = cudaMemset(d.status, 0, sizeof(StatusBlock))) != cudaSuccess)
+            return cuda_fail(e, "cudaMemset(status word)");
+        d.ready = true;
+    }
+    *out = &d;
+    return TM_OK;
+}
+
+uint64_t wait_limit_ns() { return env_u64("TM_WAIT_TIMEOUT_NS", 1000000000ull); }
+
+// ---- launch geometry ------------------------------------------------------------------------
+// Shared memory a CTA may use when `per_sm` CTAs share an SM (1 KiB per CTA is reserved by the
+// hardware; 1 KiB more lets the kernel align its stages to 1024 bytes; 256 bytes of barriers).
+size_t cta_budget(const DevState& ds, uint32_t per_sm)
+{
+    const size_t share = (size_t)ds.smem_per_sm / per_sm;
+    const size_t cap = std::min<size_t>((size_t)ds.smem_optin, share > 1024 ? share - 1024 : 0);
+    return cap > 2048 + 256 ? cap - 1024 - 256 : 0;
+}
+
+struct Geometry {
+    uint32_t grid, stages;
+    size_t smem;
+};
+
+// The TMA streaming kernels: `per_sm` one-warp CTAs per SM (TM_CTAS_PER_SM, default 2), each with
+// as many stages as fit (TM_STAGES caps it).
+Geometry tma_geometry(const DevState& ds, uint64_t nbox, uint32_t stage_bytes)
+{
+    uint32_t per_sm = (uint32_t)std::min<uint64_t>(std::max<uint64_t>(env_u64("TM_CTAS_PER_SM", 2), 1), 16);
+    size_t budget = cta_budget(ds, per_sm);
+    while (per_sm > 1 && budget < stage_bytes) budget = cta_budget(ds, --per_sm);
+    uint32_t stages = (uint32_t)std::min<size_t>(budget / stage_bytes, TM_MAX_STAGES);
+    const uint64_t cap = env_u64("TM_STAGES", 0);
+    if (cap > 0) stages = (uint32_t)std::min<uint64_t>(stages, cap);
+    stages = std::max<uint32_t>(stages, 1);
+    const uint64_t ctas = (uint64_t)ds.sms * per_sm;
+    Geometry g;
+    g.grid = (uint32_t)std::min<uint64_t>(nbox, ctas);
+    g.stages = stages;
+    g.smem = (size_t)stages * stage_bytes + kStageAlign;
+    return g;
+}
+
+// The fallback kernels: two stages per CTA, as many CTAs per SM as fit (at most 4).
+Geometry fb_geometry(const DevState& ds, uint64_t nbox, uint32_t stage_bytes)
+{
+    uint32_t per_sm = 4;
+    while (per_sm > 1 && cta_budget(ds, per_sm) < 2ull * stage_bytes) per_sm--;
+    Geometry g;
+    g.grid = (uint32_t)std::min<uint64_t>(nbox, (uint64_t)ds.sms * per_sm);
+    g.stages = 2;
+    g.smem = 2ull * stage_bytes + kStageAlign;
+    return g;
+}
+
+uint32_t stage_bytes_of(uint64_t box_bytes)
+{
+    return (uint32_t)((box_bytes + kStageAlign - 1) / kStageAlign * kStageAlign);
+}
+
+// ---- box lists --------------------------------------------------------------------------------
+// Whether the TMA path may be given every box of an explicit list.  The tensor-map copies need the
+// box's innermost start coordinate times the element size to be a multiple of 16 bytes.  Loads
+// accept starts outside the tensor as long as part of the box is inside; stores and reduces are
+// only given boxes that start inside the tensor.  Anything else runs on the fallback path, which
+// gives the same bytes.
+bool list_fits_tma(const tm_desc* d, const int32_t* coords, size_t n, bool store)
+{
+    for (size_t b = 0; b < n; b++) {
+        const int32_t* c = coords + b * d->rank;
+        if (((int64_t)c[0] * d->esize) % 16 != 0) return false;
+        for (uint32_t i = 0; i < d->rank; i++) {
+            const int64_t s = c[i];
+            if (store && s < 0) return false;
+            if (s >= (int64_t)d->dim[i] || s + (int64_t)d->box[i] <= 0) return false;
+        }
+    }
+    return true;
+}
+
+// Fills the walk; a list longer than the inline capacity is copied to device memory allocated on
+// `st` (freed by release_walk after the launch).
+int make_walk(const tm_desc* d, const int32_t* coords, size_t n, cudaStream_t st, BoxWalk& w)
+{
+    memset(&w, 0, sizeof(w));
+    w.nbox = coords ? n : d->num_boxes;
+    w.rank = d->rank;
+    for (int i = 0; i < 5; i++) {
+        w.box[i] = d->box[i];
+        w.grid_nb[i] = d->nbox[i];
+    }
+    if (!coords) {
+        w.mode = WALK_GRID;
+    } else if (n <= kInlineBoxes) {
+        w.mode = WALK_INLINE;
+        memcpy(w.inl, coords, n * d->rank * sizeof(int32_t));
+    } else {
+        w.mode = WALK_LIST;
+        int32_t* dev = nullptr;
+        const size_t bytes = n * d->rank * sizeof(int32_t);
+        cudaError_t e = cudaMallocAsync((void**)&dev, bytes, st);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaMallocAsync(box list)");
+        e = cudaMemcpyAsync(dev, coords, bytes, cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) {
+            cudaFreeAsync(dev, st);
+            return cuda_fail(e, "cudaMemcpyAsync(box list)");
+        }
+        w.list = dev;
+    }
+    return TM_OK;
+}
+
+void release_walk(const BoxWalk& w, cudaStream_t st)
+{
+    if (w.mode == WALK_LIST && w.list) cudaFreeAsync((void*)w.list, st);
+}
+
+FbArgs fb_args(const tm_desc* d, const BoxWalk& w, uint64_t images, const DevState& ds)
+{
+    FbArgs a;
+    memset(&a, 0, sizeof(a));
+    a.walk = w;
+    a.base = d->base;
+    for (int i = 0; i < 5; i++) {
+        a.dim[i] = d->dim[i];
+        a.stride[i] = (int64_t)d->stride[i];
+    }
+    a.images = images;
+    a.esize = d->esize;
+    a.span = span_of(d->swizzle);
+    a.inner_bytes = d->box[0] * d->esize;
+    a.box_bytes = (uint32_t)d->box_bytes;
+    a.stage_bytes = stage_bytes_of(d->box_bytes);
+    a.rows = (uint32_t)(d->box_bytes / a.inner_bytes);
+    a.timeout_ns = wait_limit_ns();
+    a.status = ds.status;
+    return a;
+}
+
+StreamArgs stream_args(const tm_desc* d, const BoxWalk& w, uint64_t images, uint32_t stages,
+                       const DevState& ds)
+{
+    StreamArgs a;
+    memset(&a, 0, sizeof(a));
+    a.walk = w;
+    a.images = images;
+    a.box_bytes = (uint32_t)d->box_bytes;
+    a.stage_bytes = stage_bytes_of(d->box_bytes);
+    a.stages = stages;
+    a.timeout_ns = wait_limit_ns();
+    a.status = ds.status;
+    return a;
+}
+
+int check_launch(cudaError_t e, const char* what)
+{
+    return e == cudaSuccess ? TM_OK : cuda_fail(e, what);
+}
+
+// Box copy in the load direction (tile_load_image, tiled_copy).
+int copy_boxes(const tm_desc* src, const int32_t* coords, size_t nbox, void* images, void* stream)
+{
+    if (!valid_desc(src)) return fail(TM_EINVAL, "source descriptor is not filled");
+    if (!images) return fail(TM_EINVAL, "images is NULL");
+    if ((uintptr_t)images % 16) return fail(TM_EALIGN, "images must be 16-byte aligned");
+    if (!coords && nbox != 0 && nbox != src->num_boxes)
+        return fail(TM_EINVAL, "nbox %zu is neither 0 nor the grid's %llu boxes", nbox,
+                    (unsigned long long)src->num_boxes);
+    const uint64_t n = coords ? nbox : src->num_boxes;
+    if (n == 0) return TM_OK;
+    DevState* ds = nullptr;
+    int rc = device_state(&ds);
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool tma = src->path == TM_PATH_TMA && (!coords || list_fits_tma(src, coords, n, false));
+    BoxWalk w;
+    if ((rc = make_walk(src, coords, n, st, w))) return rc;
+    if (tma) {
+        const Geometry g = tma_geometry(*ds, n, stage_bytes_of(src->box_bytes));
+        const StreamArgs a = stream_args(src, w, (uint64_t)images, g.stages, *ds);
+        const CUtensorMap* m = (const CUtensorMap*)src->tmap;
+        rc = check_launch(launch_tma_stream(KIND_COPY, src->rank, m, m, a, g.grid, g.smem, st),
+                          "tensor copy launch");
+    } else {
+        const Geometry g = fb_geometry(*ds, n, stage_bytes_of(src->box_bytes));
+        rc = check_launch(launch_fb_copy(fb_args(src, w, (uint64_t)images, *ds), g.grid, g.smem, st),
+                          "fallback copy launch");
+    }
+    release_walk(w, st);
+    return rc;
+}
+
+int plan_impl(tm_desc* out, int dtype, uint32_t rank, void* base, const uint64_t* gdim,
+              const uint64_t* gstr, const uint32_t* box, const uint32_t* estr, int sw, int oob)
+{
+    if (!out) return fail(TM_EINVAL, "descriptor pointer is NULL");
+    memset(out, 0, sizeof(*out));
+    const uint32_t es = esize_of(dtype);
+    if (!es) return fail(TM_EINVAL, "unknown dtype %d", dtype);
+    if (rank < 1 || rank > 5) return fail(TM_EINVAL, "rank %u outside 1..5", rank);
+    if (!base) return fail(TM_EINVAL, "base is NULL");
+    if (!gdim || !box || (rank > 1 && !gstr)) return fail(TM_EINVAL, "dims / strides / box NULL");
+    if (sw < TM_SWIZZLE_NONE || sw > TM_SWIZZLE_128B) return fail(TM_EINVAL, "bad swizzle %d", sw);
+    if (oob == TM_OOB_NAN) return fail(TM_EUNSUPPORTED, "NaN out-of-bounds fill is not supported");
+    if (oob != TM_OOB_ZERO) return fail(TM_EINVAL, "bad oob fill %d", oob);
+    for (uint32_t i = 0; i < rank; i++) {
+        if (gdim[i] < 1 || gdim[i] > (1ull << 32))
+            return fail(TM_ERANGE, "globalDim[%u] = %llu outside 1..2^32", i,
+                        (unsigned long long)gdim[i]);
+        if (box[i] < 1 || box[i] > 256)
+            return fail(TM_ERANGE, "boxDim[%u] = %u outside 1..256", i, box[i]);
+        if (estr && estr[i] != 1) {
+            if (estr[i] >= 1 && estr[i] <= 8)
+                return fail(TM_EUNSUPPORTED, "elementStrides[%u] = %u: only 1 is supported", i,
+                            estr[i]);
+            return fail(TM_EINVAL, "elementStrides[%u] = %u outside 1..8", i, estr[i]);
+        }
+    }
+    const uint64_t inner = (uint64_t)box[0] * es;
+    if (inner % 16)
+        return fail(TM_EALIGN, "boxDim[0] * element size = %llu bytes is not a multiple of 16",
+                    (unsigned long long)inner);
+    const uint32_t span = span_of((uint32_t)sw);
+    if (span && inner != span)
+        return fail(TM_EUNSUPPORTED, "swizzle %u B needs an inner box row of exactly %u bytes, got %llu",
+                    span, span, (unsigned long long)inner);
+    uint64_t bb = es;
+    for (uint32_t i = 0; i < rank; i++) bb *= box[i];
+    if (bb > TM_MAX_BOX_BYTES)
+        return fail(TM_ERANGE, "box of %llu bytes exceeds %u", (unsigned long long)bb,
+                    TM_MAX_BOX_BYTES);
+    const uint64_t b = (uint64_t)(uintptr_t)base;
+    if (b % es) return fail(TM_EALIGN, "base is not a multiple of the element size");
+    uint32_t why = (b % 16) ? TM_WHY_BASE : 0u;
+    for (uint32_t i = 1; i < rank; i++) {
+        const uint64_t s = gstr[i - 1];
+        if (s == 0 || s >= (1ull << 40))
+            return fail(TM_ERANGE, "globalStrides[%u] = %llu outside 1..2^40-1", i - 1,
+                        (unsigned long long)s);
+        if (s % es) return fail(TM_EALIGN, "globalStrides[%u] is not a multiple of the element size", i - 1);
+        if (s % 16) why |= TM_WHY_STRIDE;
+    }
+    out->dtype = (uint32_t)dtype;
+    out->esize = es;
+    out->rank = rank;
+    out->swizzle = (uint32_t)sw;
+    out->oob = (uint32_t)oob;
+    out->path = why ? TM_PATH_FALLBACK : TM_PATH_TMA;
+    out->why_fallback = why;
+    out->base = b;
+    uint64_t nb_total = 1;
+    for (uint32_t i = 0; i < 5; i++) {
+        const bool used = i < rank;
+        out->dim[i] = used ? gdim[i] : 1;
+        out->stride[i] = !used ? 0 : (i == 0 ? es : gstr[i - 1]);
+        out->box[i] = used ? box[i] : 1;
+        out->estride[i] = 1;
+        out->nbox[i] = used ? (gdim[i] + box[i] - 1) / box[i] : 1;
+        if (__builtin_mul_overflow(nb_total, out->nbox[i], &nb_total))
+            return fail(TM_ERANGE, "box count overflows 64 bits");
+    }
+    out->box_bytes = bb;
+    out->num_boxes = nb_total;
+    out->magic = TM_DESC_MAGIC;
+    return TM_OK;
+}
+
+int encode_into(tm_desc* d)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) {
+        d->magic = 0;
+        return fail(TM_ECUDA, "the CUDA driver's cuTensorMapEncodeTiled is not reachable");
+    }
+    cuuint64_t dims[5], strides[4];
+    cuuint32_t boxd[5], estr[5];
+    for (uint32_t i = 0; i < d->rank; i++) {
+        dims[i] = d->dim[i];
+        boxd[i] = d->box[i];
+        estr[i] = 1;
+        if (i > 0) strides[i - 1] = d->stride[i];
+    }
+    const CUtensorMapL2promotion promo =
+        (CUtensorMapL2promotion)std::min<uint64_t>(env_u64("TM_L2_PROMOTION", 2), 3);
+    const CUresult r = enc((CUtensorMap*)d->tmap, (CUtensorMapDataType)d->dtype, d->rank,
+                           (void*)(uintptr_t)d->base, dims, strides, boxd, estr,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, (CUtensorMapSwizzle)d->swizzle, promo,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        memset(d->tmap, 0, sizeof(d->tmap));
+        d->path = TM_PATH_FALLBACK;
+        d->why_fallback |= TM_WHY_DRIVER;
+    }
+    return TM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tmap_plan(tm_desc* out, tm_dtype dtype, uint32_t rank, void* base, const uint64_t* globalDim,
+              const uint64_t* globalStrides, const uint32_t* boxDim,
+              const uint32_t* elementStrides, tm_swizzle swizzle, tm_oob oob)
+{
+    return plan_impl(out, dtype, rank, base, globalDim, globalStrides, boxDim, elementStrides,
+                     swizzle, oob);
+}
+
+int tmap_encode(tm_desc* out, tm_dtype dtype, uint32_t rank, void* base,
+                const uint64_t* globalDim, const uint64_t* globalStrides, const uint32_t* boxDim,
+                const uint32_t* elementStrides, tm_swizzle swizzle, tm_oob oob)
+{
+    int rc = plan_impl(out, dtype, rank, base, globalDim, globalStrides, boxDim, elementStrides,
+                       swizzle, oob);
+    if (rc) return rc;
+    if (out->path != TM_PATH_TMA) return TM_OK;
+    return encode_into(out);
+}
+
+int tmap_replace_address(tm_desc* d, void* new_base)
+{
+    if (!valid_desc(d)) return fail(TM_EINVAL, "descriptor is not filled");
+    const uint64_t nb = (uint64_t)(uintptr_t)new_base;
+    if (!nb) return fail(TM_EINVAL, "new base is NULL");
+    if (nb % d->esize) return fail(TM_EALIGN, "new base is not a multiple of the element size");
+    const bool forced = (d->why_fallback & TM_WHY_FORCED) != 0;
+    if (d->path == TM_PATH_TMA && nb % 16 == 0) {
+        ReplaceAddressFn rep = replace_fn();
+        if (!rep) return fail(TM_ECUDA, "the CUDA driver's cuTensorMapReplaceAddress is not reachable");
+        if (rep((CUtensorMap*)d->tmap, new_base) != CUDA_SUCCESS)
+            return fail(TM_ECUDA, "cuTensorMapReplaceAddress refused the new base");
+        d->base = nb;
+        return TM_OK;
+    }
+    // The path may change: rebuild from the stored fields.
+    uint64_t gdim[5], gstr[4];
+    uint32_t box[5];
+    for (uint32_t i = 0; i < d->rank; i++) {
+        gdim[i] = d->dim[i];
+        box[i] = d->box[i];
+        if (i > 0) gstr[i - 1] = d->stride[i];
+    }
+    tm_desc t;
+    int rc = tmap_encode(&t, (tm_dtype)d->dtype, d->rank, new_base, gdim, gstr, box, nullptr,
+                         (tm_swizzle)d->swizzle, (tm_oob)d->oob);
+    if (rc) return rc;
+    if (forced) {
+        t.path = TM_PATH_FALLBACK;
+        t.why_fallback |= TM_WHY_FORCED;
+    }
+    *d = t;
+    return TM_OK;
+}
+
+int tmap_force_fallback(tm_desc* d)
+{
+    if (!valid_desc(d)) return fail(TM_EINVAL, "descriptor is not filled");
+    d->path = TM_PATH_FALLBACK;
+    d->why_fallback |= TM_WHY_FORCED;
+    return TM_OK;
+}
+
+int tile_load_image(const tm_desc* src, const int32_t* coords, void* image, void* stream)
+{
+    if (!coords) return fail(TM_EINVAL, "coords is NULL");
+    return copy_boxes(src, coords, 1, image, stream);
+}
+
+int tiled_copy(const tm_desc* src, const int32_t* coords, size_t nbox, void* images, void* stream)
+{
+    return copy_boxes(src, coords, nbox, images, stream);
+}
+
+int tiled_roundtrip(const tm_desc* dst, const int32_t* coords, size_t nbox, const void* images,
+                    void* stream)
+{
+    if (!valid_desc(dst)) return fail(TM_EINVAL, "destination descriptor is not filled");
+    if (!images) return fail(TM_EINVAL, "images is NULL");
+    if ((uintptr_t)images % 16) return fail(TM_EALIGN, "images must be 16-byte aligned");
+    if (!coords && nbox != 0 && nbox != dst->num_boxes)
+        return fail(TM_EINVAL, "nbox %zu is neither 0 nor the grid's %llu boxes", nbox,
+                    (unsigned long long)dst->num_boxes);
+    const uint64_t n = coords ? nbox : dst->num_boxes;
+    if (n == 0) return TM_OK;
+    DevState* ds = nullptr;
+    int rc = device_state(&ds);
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    const bool tma = dst->path == TM_PATH_TMA && (!coords || list_fits_tma(dst, coords, n, true));
+    BoxWalk w;
+    if ((rc = make_walk(dst, coords, n, st, w))) return rc;
+    if (tma) {
+        const Geometry g = tma_geometry(*ds, n, stage_bytes_of(dst->box_bytes));
+        const StreamArgs a = stream_args(dst, w, (uint64_t)images, g.stages, *ds);
+        const CUtensorMap* m = (const CUtensorMap*)dst->tmap;
+        rc = check_launch(launch_tma_stream(KIND_ROUNDTRIP, dst->rank, m, m, a, g.grid, g.smem, st),
+                          "tensor store launch");
+    } else {
+        const Geometry g = fb_geometry(*ds, n, stage_bytes_of(dst->box_bytes));
+        rc = check_launch(launch_fb_store(fb_args(dst, w, (uint64_t)images, *ds), g.grid, g.smem, st),
+                          "fallback store launch");
+    }
+    release_walk(w, st);
+    return rc;
+}
+
+int tile_reduce_add(const tm_desc* dst, const tm_desc* src, void* stream)
+{
+    if (!valid_desc(dst) || !valid_desc(src)) return fail(TM_EINVAL, "descriptor is not filled");
+    if (dst->dtype != TM_F32 || src->dtype != TM_F32)
+        return fail(TM_EUNSUPPORTED, "reduce-add supports TM_F32 maps only");
+    if (dst->rank != src->rank || dst->swizzle != src->swizzle)
+        return fail(TM_EINVAL, "dst and src differ in rank or swizzle");
+    for (uint32_t i = 0; i < dst->rank; i++) {
+        if (dst->dim[i] != src->dim[i] || dst->box[i] != src->box[i])
+            return fail(TM_EINVAL, "dst and src differ in dims or box (dim %u)", i);
+    }
+    DevState* ds = nullptr;
+    int rc = device_state(&ds);
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    BoxWalk w;
+    if ((rc = make_walk(dst, nullptr, 0, st, w))) return rc;
+    const uint64_t n = dst->num_boxes;
+    if (dst->path == TM_PATH_TMA && src->path == TM_PATH_TMA) {
+        const Geometry g = tma_geometry(*ds, n, stage_bytes_of(dst->box_bytes));
+        const StreamArgs a = stream_args(dst, w, 0, g.stages, *ds);
+        rc = check_launch(launch_tma_stream(KIND_REDUCE, dst->rank, (const CUtensorMap*)src->tmap,
+                                            (const CUtensorMap*)dst->tmap, a, g.grid, g.smem, st),
+                          "tensor reduce launch");
+    } else {
+        FbArgs a = fb_args(dst, w, 0, *ds);
+        a.src_base = src->base;
+        for (int i = 0; i < 5; i++) a.src_stride[i] = (int64_t)src->stride[i];
+        const uint64_t rows = n * a.rows;
+        const uint32_t grid = (uint32_t)std::min<uint64_t>((rows + 7) / 8, (uint64_t)ds->sms * 8);
+        rc = check_launch(launch_fb_reduce(a, std::max<uint32_t>(grid, 1), st),
+                          "fallback reduce launch");
+    }
+    return rc;
+}
+
+int stream_tiles(const tm_desc* a, const tm_desc* b, uint32_t stages, float* cs_a, float* cs_b,
+                 uint64_t* bits_a, uint64_t* bits_b, void* stream)
+{
+    if (!valid_desc(a) || !valid_desc(b)) return fail(TM_EINVAL, "descriptor is not filled");
+    if (!cs_a || !cs_b || !bits_a || !bits_b) return fail(TM_EINVAL, "an output array is NULL");
+    if ((uintptr_t)cs_a % 4 || (uintptr_t)cs_b % 4 || (uintptr_t)bits_a % 8 || (uintptr_t)bits_b % 8)
+        return fail(TM_EALIGN, "output arrays must be naturally aligned");
+    for (const tm_desc* d : {a, b}) {
+        if (d->dtype != TM_BF16 || d->rank != 2)
+            return fail(TM_EUNSUPPORTED, "stream_tiles needs rank-2 TM_BF16 maps");
+        const uint32_t rows = d->box[1];
+        if (d->box[0] != 64 || !(rows == 32 || rows == 64 || rows == 128 || rows == 256))
+            return fail(TM_EUNSUPPORTED, "stream_tiles needs boxes {64, R}, R in 32/64/128/256");
+        if (d->swizzle != TM_SWIZZLE_128B && d->swizzle != TM_SWIZZLE_NONE)
+            return fail(TM_EUNSUPPORTED, "stream_tiles reads 128B-swizzled or unswizzled tiles");
+        if (d->path != TM_PATH_TMA) return fail(TM_EUNSUPPORTED, "stream_tiles needs TMA-path maps");
+    }
+    if (a->box[1] != b->box[1] || a->swizzle != b->swizzle)
+        return fail(TM_EINVAL, "A and B differ in tile rows or swizzle");
+    if (a->num_boxes != b->num_boxes)
+        return fail(TM_EINVAL, "A has %llu tiles, B has %llu", (unsigned long long)a->num_boxes,
+                    (unsigned long long)b->num_boxes);
+    if (stages < 2 || stages > 8) return fail(TM_ERANGE, "stages %u outside 2..8", stages);
+    DevState* ds = nullptr;
+    int rc = device_state(&ds);
+    if (rc) return rc;
+    RingArgs r;
+    memset(&r, 0, sizeof(r));
+    r.ntiles = a->num_boxes;
+    r.a_nb0 = a->nbox[0];
+    r.b_nb0 = b->nbox[0];
+    r.rows = a->box[1];
+    r.stages = stages;
+    r.tile_bytes = (uint32_t)a->box_bytes;
+    r.swizzled = a->swizzle == TM_SWIZZLE_128B ? 1u : 0u;
+    r.cs_a = cs_a;
+    r.cs_b = cs_b;
+    r.bits_a = (unsigned long long*)bits_a;
+    r.bits_b = (unsigned long long*)bits_b;
+    r.timeout_ns = wait_limit_ns();
+    r.status = ds->status;
+    const size_t smem = (size_t)stages * 2 * r.tile_bytes + kStageAlign;
+    if (smem > cta_budget(*ds, 1)) return fail(TM_ERANGE, "%u stages of two tiles exceed shared memory", stages);
+    uint32_t per_sm = 1;
+    while (per_sm < 4 && cta_budget(*ds, per_sm + 1) >= smem) per_sm++;
+    const uint32_t grid = (uint32_t)std::min<uint64_t>(r.ntiles, (uint64_t)ds->sms * per_sm);
+    return check_launch(launch_ring((const CUtensorMap*)a->tmap, (const CUtensorMap*)b->tmap, r, grid,
+                                    smem, (cudaStream_t)stream),
+                        "ring launch");
+}
+
+int tm_stream_check(void* stream)
+{
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    DevState* ds = nullptr;
+    int rc = device_state(&ds);
+    if (rc) return rc;
+    StatusBlock sb;
+    if ((e = cudaMemcpy(&sb, ds->status, sizeof(sb), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e, "reading the status word");
+    if (sb.code == 0) return TM_OK;
+    if ((e = cudaMemset(ds->status, 0, sizeof(sb))) != cudaSuccess)
+        return cuda_fail(e, "clearing the status word");
+    static const char* names[] = {"?", "tiled copy", "round trip", "reduce-add", "ring",
+                                  "fallback copy", "fallback store", "fallback reduce", "self-test"};
+    const char* kn = sb.kernel < 9 ? names[sb.kernel] : "?";
+    return fail(sb.code, "%s kernel: wait gave up in block %u, stage %u, parity %u, box %llu", kn,
+                sb.block, sb.stage, sb.phase, (unsigned long long)sb.box);
+}
+
+int tm_selftest_wait_timeout(uint64_t timeout_ns, void* stream)
+{
+    DevState* ds = nullptr;
+    int rc = device_state(&ds);
+    if (rc) return rc;
+    return check_launch(launch_selftest(timeout_ns, ds->status, (cudaStream_t)stream),
+                        "self-test launch");
+}
+
+const char* tm_last_error(void) { return g_err; }
+size_t tm_box_bytes(const tm_desc* d) { return valid_desc(d) ? (size_t)d->box_bytes : 0; }
+size_t tm_num_boxes(const tm_desc* d) { return valid_desc(d) ? (size_t)d->num_boxes : 0; }
+int tm_path(const tm_desc* d) { return valid_desc(d) ? (int)d->path : 0; }
+size_t tm_desc_size(void) { return sizeof(tm_desc); }
+
+int tm_pick_swizzle(uint32_t inner_bytes)
+{
+    return inner_bytes == 128 ? TM_SWIZZLE_128B
+           : inner_bytes == 64 ? TM_SWIZZLE_64B
+           : inner_bytes == 32 ? TM_SWIZZLE_32B
+                               : TM_SWIZZLE_NONE;
+}
+
+}  // extern "C"

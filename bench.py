@@ -1,0 +1,517 @@
+"""Benchmark of the tiled tensor movement hot path on one GB300 (or N, one process per GPU).
+
+One step = one pass of every kernel of the path over one batch of synthetic input, each kernel
+preceded by an L2 flush (a 512 MiB device write, not timed):
+  w3.copy       bf16 8192 x 8192, 128 x 64 boxes, 128B swizzle -> 8192 tile-major images
+  w3.roundtrip  the images stored back through the map into a second tensor
+  w4r3.copy / .roundtrip      bf16 16 x 4095 x 1000 (row pitch 1024), 1 x 64 x 64 boxes, 128B
+  w4r3n.copy / .roundtrip     same tensor, 1 x 64 x 32 boxes, 64B
+  w4r5.copy / .roundtrip      rank-5 view 4 x 4 x 4095 x 10 x 100, box 1 x 1 x 32 x 10 x 64,
+                              200-byte stride: the vector fallback path
+  w5a.reduce    fp32 16384 x 16384: dst += src, 128 x 32 boxes, 128B swizzle
+  w5b.ring      bf16 A 8192 x 4096 and B 4096 x 8192, 128 x 64 tiles, 4-stage ring + checksums
+
+value = algorithmic bytes of the step / device time of its kernels (CUDA events on the launching
+stream), in GB/s; under torchrun every rank runs the same per-GPU workload (weak scaling) and the
+step time is the max over ranks.  The JSON line also carries the roofline of the dominant kernel
+(the reduce-add), an end-to-end figure with host buffers, the CPU oracle baseline, clocks sampled
+during the timed region, and a per-kernel breakdown.
+
+--impl reference times the CPU oracle (the reference of this build) on a bounded sample of the
+same workload on the host's cores and prints the same kind of line.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "tiled copy / round-trip / reduce-add HBM GB/s on 1 GB300 and % of HBM peak"
+GB = 1e9
+FLUSH_BYTES = 512 << 20
+WORKLOAD = ("tmap hot path: W3 bf16 8192x8192 copy+roundtrip (128x64, 128B); W4 bf16 "
+            "16x4095x1000 pitch 1024 rank-3 (1x64x64 128B, 1x64x32 64B) and rank-5 fallback view "
+            "copy+roundtrip; W5a fp32 16384x16384 reduce-add (128x32, 128B); W5b bf16 "
+            "8192x4096 + 4096x8192 4-stage ring")
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", default="tmap", choices=["tmap", "reference"])
+    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--ops", default="", help="comma list of op names to run (default: all)")
+    return p.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+# ------------------------------------------------------------------------------------------------
+# Workload: host arrays (numpy, the bytes both the GPU and the oracle see) and maps
+# ------------------------------------------------------------------------------------------------
+class HostWorkload:
+    def __init__(self):
+        t0 = time.time()
+        self.w3 = workloads.w3_tensor()
+        self.w4 = workloads.w4_tensor()
+        self.w5a_dst, self.w5a_src = workloads.w5a_tensors()
+        self.w5b_a, self.w5b_b = workloads.w5b_tensors()
+        self.gen_s = time.time() - t0
+        self.r3 = workloads.w3_map()
+        self.r4_128 = workloads.w4_rank3_map(64, span=128)
+        self.r4_64 = workloads.w4_rank3_map(32, span=64)
+        self.r4_r5 = workloads.w4_rank5_map(span=128)
+        self.r5a = workloads.w5a_map()
+        self.r5b_a, self.r5b_b = workloads.w5b_maps()
+
+
+def box_count(r):
+    n = 1
+    for d, b in zip(r["dims"], r["box"]):
+        n *= -(-d // b)
+    return n
+
+
+def box_bytes(r):
+    n = r["esize"]
+    for b in r["box"]:
+        n *= b
+    return n
+
+
+def inbounds_bytes(r):
+    n = r["esize"]
+    for d in r["dims"]:
+        n *= d
+    return n
+
+
+def op_table(h: HostWorkload):
+    """(name, algorithmic bytes) per op: bytes read + bytes written, counting in-bounds tensor bytes
+    and whole images."""
+    t = []
+    for name, r in (("w3", h.r3), ("w4r3", h.r4_128), ("w4r3n", h.r4_64), ("w4r5", h.r4_r5)):
+        img = box_count(r) * box_bytes(r)
+        ten = inbounds_bytes(r)
+        t.append((f"{name}.copy", ten + img))
+        t.append((f"{name}.roundtrip", img + ten))
+    t.append(("w5a.reduce", 3 * inbounds_bytes(h.r5a)))
+    t.append(("w5b.ring", inbounds_bytes(h.r5b_a) + inbounds_bytes(h.r5b_b)))
+    return t
+
+
+# ------------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------------
+class GpuWorkload:
+    def __init__(self, h: HostWorkload, stream):
+        import torch
+
+        import async_bulk_tensor_tmap_gb300 as tm
+        self.tm, self.torch, self.stream = tm, torch, stream
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).reshape(-1).view(np.uint8)).cuda()
+        self.t = {
+            "w3": dev(h.w3), "w4": dev(h.w4), "w5a_dst": dev(h.w5a_dst),
+            "w5a_src": dev(h.w5a_src), "w5b_a": dev(h.w5b_a), "w5b_b": dev(h.w5b_b),
+        }
+        self.t["w3_out"] = torch.empty_like(self.t["w3"])
+        self.t["w4_out"] = self.t["w4"].clone()
+        sw = {0: 0, 32: 1, 64: 2, 128: 3}
+
+        def enc(dtype, buf, r):
+            return tm.tmap_encode(dtype, buf, r["dims"], r["strides"], r["box"], swizzle=sw[r["span"]])
+
+        bf, f32 = tm.TM_BF16, tm.TM_F32
+        self.maps = {
+            "w3": enc(bf, self.t["w3"], h.r3), "w3_out": enc(bf, self.t["w3_out"], h.r3),
+            "w4r3": enc(bf, self.t["w4"], h.r4_128), "w4r3_out": enc(bf, self.t["w4_out"], h.r4_128),
+            "w4r3n": enc(bf, self.t["w4"], h.r4_64), "w4r3n_out": enc(bf, self.t["w4_out"], h.r4_64),
+            "w4r5": enc(bf, self.t["w4"], h.r4_r5), "w4r5_out": enc(bf, self.t["w4_out"], h.r4_r5),
+            "w5a_dst": enc(f32, self.t["w5a_dst"], h.r5a), "w5a_src": enc(f32, self.t["w5a_src"], h.r5a),
+            "w5b_a": enc(bf, self.t["w5b_a"], h.r5b_a), "w5b_b": enc(bf, self.t["w5b_b"], h.r5b_b),
+        }
+        for k in ("w3", "w4r3", "w4r3n", "w4r5"):
+            m = self.maps[k]
+            self.t[f"{k}_img"] = torch.empty(m.num_boxes * m.box_bytes, dtype=torch.uint8,
+                                             device="cuda")
+        n = self.maps["w5b_a"].num_boxes
+        self.t["cs_a"] = torch.zeros(n, dtype=torch.float32, device="cuda")
+        self.t["cs_b"] = torch.zeros(n, dtype=torch.float32, device="cuda")
+        self.t["bits_a"] = torch.zeros(n, dtype=torch.int64, device="cuda")
+        self.t["bits_b"] = torch.zeros(n, dtype=torch.int64, device="cuda")
+        self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        self.paths = {k: m.path for k, m in self.maps.items()}
+
+    def run_op(self, name):
+        tm, t, m, s = self.tm, self.t, self.maps, self.stream
+        base, kind = name.split(".")
+        if kind == "copy":
+            tm.tiled_copy(m[base], None, t[f"{base}_img"], s)
+        elif kind == "roundtrip":
+            tm.tiled_roundtrip(m[f"{base}_out"], None, t[f"{base}_img"], s)
+        elif kind == "reduce":
+            tm.tile_reduce_add(m["w5a_dst"], m["w5a_src"], s)
+        elif kind == "ring":
+            tm.stream_tiles(m["w5b_a"], m["w5b_b"], 4, t["cs_a"], t["cs_b"], t["bits_a"],
+                            t["bits_b"], s)
+
+    def flush_l2(self):
+        with self.torch.cuda.stream(self.stream):
+            self.flush.fill_(1)
+
+
+class ClockSampler:
+    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu, self.rows, self.proc = gpu_index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in self.rows for n, v in zip(names, r[4:8]) if v == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(self.rows)}
+
+
+def time_steps(g: GpuWorkload, ops, steps, warmup):
+    """Per-op device ms for each timed step (events on the launching stream)."""
+    torch = g.torch
+    for _ in range(warmup):
+        for name, _ in ops:
+            g.flush_l2()
+            g.run_op(name)
+    torch.cuda.synchronize()
+    rc = g.tm.tm_stream_check(g.stream)
+    if rc != g.tm.TM_OK:
+        raise RuntimeError(g.tm.tm_last_error())
+    per = {name: [] for name, _ in ops}
+    ev = []
+    for _ in range(steps):
+        for name, _ in ops:
+            g.flush_l2()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(g.stream)
+            g.run_op(name)
+            e1.record(g.stream)
+            ev.append((name, e0, e1))
+    return per, ev
+
+
+def collect(per, ev):
+    for name, e0, e1 in ev:
+        per[name].append(e0.elapsed_time(e1))
+    return per
+
+
+def e2e_run(g: GpuWorkload, h: HostWorkload, ops, steps):
+    """Same step through the public API with HOST buffers: every step copies its inputs from
+    pinned host memory and its results back, inside the timed region."""
+    torch = g.torch
+    names = [n for n, _ in ops]
+    ins, outs = [], []
+    want_w3 = any(n.startswith("w3") for n in names)
+    want_w4 = any(n.startswith("w4") for n in names)
+    if want_w3:
+        ins.append("w3")
+        outs.append("w3_out")
+    if want_w4:
+        ins.append("w4")
+        outs.append("w4_out")
+    if "w5a.reduce" in names:
+        ins += ["w5a_dst", "w5a_src"]
+        outs.append("w5a_dst")
+    if "w5b.ring" in names:
+        ins += ["w5b_a", "w5b_b"]
+        outs += ["cs_a", "cs_b", "bits_a", "bits_b"]
+    pin_in = {k: torch.empty_like(g.t[k], device="cpu").pin_memory() for k in ins}
+    src = {"w3": h.w3, "w4": h.w4, "w5a_dst": h.w5a_dst, "w5a_src": h.w5a_src,
+           "w5b_a": h.w5b_a, "w5b_b": h.w5b_b}
+    for k in ins:
+        pin_in[k].copy_(torch.from_numpy(np.ascontiguousarray(src[k]).reshape(-1).view(np.uint8)))
+    pin_out = {k: torch.empty_like(g.t[k], device="cpu").pin_memory() for k in outs}
+    bi = sum(v.numel() * v.element_size() for v in pin_in.values())
+    bo = sum(v.numel() * v.element_size() for v in pin_out.values())
+
+    def step():
+        with torch.cuda.stream(g.stream):
+            for k in ins:
+                g.t[k].copy_(pin_in[k], non_blocking=True)
+        for name in names:
+            g.run_op(name)
+        with torch.cuda.stream(g.stream):
+            for k in outs:
+                pin_out[k].copy_(g.t[k], non_blocking=True)
+
+    step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(g.stream)
+    for _ in range(steps):
+        step()
+    e1.record(g.stream)
+    torch.cuda.synchronize()
+    if g.tm.tm_stream_check(g.stream) != g.tm.TM_OK:
+        raise RuntimeError(g.tm.tm_last_error())
+    return e0.elapsed_time(e1) / steps, bi, bo
+
+
+# ------------------------------------------------------------------------------------------------
+# CPU arm: the oracle as it stands, on a bounded sample of the same workload
+# ------------------------------------------------------------------------------------------------
+def oracle_sample(h: HostWorkload, ops, fraction: float, threads: int):
+    """Runs the oracle over the first `fraction` of the boxes of every op; returns (seconds,
+    algorithmic bytes covered)."""
+    import oracle
+
+    def om(arr, r):
+        return oracle.Map(arr, r["esize"], r["dims"], r["strides"], r["box"], r["span"])
+
+    spent, covered = 0.0, 0
+    if not hasattr(h, "scratch3"):  # destinations of the sampled round trips, made once
+        h.scratch3 = np.empty_like(h.w3)
+        h.scratch4 = h.w4.copy()
+    scratch3, scratch4 = h.scratch3, h.scratch4
+    for name, nbytes in ops:
+        base, kind = name.split(".")
+        if base in ("w3", "w4r3", "w4r3n", "w4r5"):
+            r = {"w3": h.r3, "w4r3": h.r4_128, "w4r3n": h.r4_64, "w4r5": h.r4_r5}[base]
+            src = h.w3 if base == "w3" else h.w4
+            dst = scratch3 if base == "w3" else scratch4
+            n = box_count(r)
+            k = max(1, int(n * fraction))
+            imgs = np.empty(k * box_bytes(r), np.uint8)
+            if kind == "copy":
+                t0 = time.perf_counter()
+                oracle.tiled_copy(om(src, r), threads=threads, b0=0, b1=k, out=imgs, nbox=k)
+                spent += time.perf_counter() - t0
+            else:
+                oracle.tiled_copy(om(src, r), threads=threads, b0=0, b1=k, out=imgs, nbox=k)
+                t0 = time.perf_counter()
+                oracle.tiled_roundtrip(om(dst, r), imgs, threads=threads, b0=0, b1=k)
+                spent += time.perf_counter() - t0
+            covered += nbytes * k // n
+        elif kind == "reduce":
+            n = box_count(h.r5a)
+            k = max(1, int(n * fraction))
+            d = h.w5a_dst  # the oracle adds in place into the host copy (a sample of boxes)
+            t0 = time.perf_counter()
+            oracle.tile_reduce_add(om(d, h.r5a), om(h.w5a_src, h.r5a), threads=threads, b0=0, b1=k)
+            spent += time.perf_counter() - t0
+            covered += nbytes * k // n
+        elif kind == "ring":
+            n = box_count(h.r5b_a)
+            k = max(1, int(n * fraction))
+            t0 = time.perf_counter()
+            oracle.stream_checksums(om(h.w5b_a, h.r5b_a), om(h.w5b_b, h.r5b_b), threads=threads,
+                                    t0=0, t1=k)
+            spent += time.perf_counter() - t0
+            covered += nbytes * k // n
+    return spent, covered
+
+
+def calibrated_fraction(h: HostWorkload, ops, threads: int, target_s: float) -> float:
+    """Fraction of every op's boxes that keeps one oracle sample near `target_s` seconds."""
+    frac = 0.005
+    oracle_sample(h, ops, frac, threads)
+    spent, _ = oracle_sample(h, ops, frac, threads)
+    return min(1.0, frac * target_s / max(spent, 1e-3))
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ------------------------------------------------------------------------------------------------
+def measured_hbm_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def select_ops(h, spec):
+    ops = op_table(h)
+    if spec:
+        keep = set(spec.split(","))
+        ops = [o for o in ops if o[0] in keep]
+    return ops
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    h = HostWorkload()
+    ops = select_ops(h, args.ops)
+    cores = cpu_cores()
+    frac = calibrated_fraction(h, ops, cores, target_s=2.0)
+    for _ in range(args.warmup):
+        oracle_sample(h, ops, frac / 4, cores)
+    spent, covered = 0.0, 0
+    for _ in range(args.steps):
+        s, c = oracle_sample(h, ops, frac, cores)
+        spent += s
+        covered += c
+    value = covered / spent / GB
+    sample = (f"first {frac:.2%} of the boxes of every op per step "
+              f"({covered // max(args.steps, 1)} algorithmic bytes)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": spent / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": WORKLOAD, "sample": sample},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    h = HostWorkload()
+    ops = select_ops(h, args.ops)
+    stream = torch.cuda.Stream()
+    g = GpuWorkload(h, stream)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    barrier()
+    with ClockSampler(local) as clk:
+        per, ev = time_steps(g, ops, args.steps, args.warmup)
+        torch.cuda.synchronize()
+    per = collect(per, ev)
+    barrier()
+    rc = g.tm.tm_stream_check(stream)
+    if rc != g.tm.TM_OK:
+        raise RuntimeError(g.tm.tm_last_error())
+    step_ms = sum(sum(v) for v in per.values()) / args.steps
+    if world > 1:
+        t = torch.tensor([step_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+    step_bytes = sum(b for _, b in ops)
+    value = world * step_bytes / (step_ms * 1e-3) / GB
+    peak, peak_kind = measured_hbm_peak()
+    breakdown = {}
+    for name, nbytes in ops:
+        ms = statistics.mean(per[name])
+        breakdown[name] = {"ms": round(ms, 4), "GB/s": round(nbytes / ms / 1e6, 1),
+                           "frac_of_peak": round(nbytes / ms / 1e6 / peak, 3),
+                           "bytes": nbytes}
+    dom = max(ops, key=lambda o: statistics.mean(per[o[0]]))
+    dom_name, dom_bytes = dom
+    dom_ms = statistics.mean(per[dom_name])
+    achieved = dom_bytes / dom_ms / 1e6
+    e2e_ms, bi, bo = e2e_run(g, h, ops, args.e2e_steps)
+    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / GB
+    if rank != 0:
+        return
+    cpu = None
+    if not args.no_cpu_baseline:
+        cores = cpu_cores()
+        frac = calibrated_fraction(h, ops, cores, target_s=2.0)
+        spent, covered = oracle_sample(h, ops, frac, cores)
+        cpu = {"value": covered / spent / GB, "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": f"first {frac:.2%} of the boxes of every op ({covered} algorithmic "
+                         f"bytes, {spent:.1f} s on {cores} threads)"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "step_bytes": step_bytes,
+                   "l2": "flushed by a 512 MiB device write before every kernel (not timed)",
+                   "hbm_frac_of_peak": round(value / world / peak, 3),
+                   "paths": {k: ("tma" if p == 1 else "fallback") for k, p in g.paths.items()
+                             if not k.endswith("_out")}},
+        "roofline": {"kernel": dom_name, "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo},
+        "cpu_baseline": cpu,
+        "gpu_launches": len(ops) * args.steps,
+        "clocks": clk.summary(),
+        "breakdown": breakdown,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,212 @@
+/*
+ * tmap.h -- C ABI of the GB300 (sm_103a) tiled tensor movement library (libtmap_gb300.so).
+ *
+ * A tensor map describes how a global tensor is cut into boxes; each box is moved between global
+ * memory and a (possibly swizzled) shared-memory image by the Tensor Memory Accelerator, then
+ * written out, stored back through a map, reduce-added, or consumed from a multi-stage ring.
+ *
+ * Sources (cited below by tag and section):
+ *   [MLSys-TMA]  mlc.ai "Modern GPU Programming for MLSys", chapter "异步数据搬运：TMA"
+ *   [H200-TMA]   coolgpu "H200 · TMA · Tensor Memory Accelerator" feature card
+ *   [Book-TMA]   fangpin "gpu-hpc-book", chapter 08 "Cuda TMA （Tensor Memory Accelerator）"
+ *
+ * Conventions shared by every call
+ *   - Every call returns an int status (TM_OK = 0 or a TM_E* code); tm_last_error() returns a
+ *     thread-local description of the last failure.  No C++ exception or abort crosses the ABI.
+ *   - The caller owns all memory.  Tensor bases, image buffers and checksum arrays are DEVICE
+ *     pointers on the current CUDA device; coordinate lists and dimension arrays are HOST pointers
+ *     read before the call returns.  The library never frees a caller's buffer.
+ *   - Dimension, stride, box and coordinate arrays are innermost first (index 0 is the contiguous
+ *     dimension), as in the encoder of [H200-TMA] §04 ① and the launcher of [Book-TMA]
+ *     §"单 block、单 lane、单 tile 的 TMA load".
+ *   - Launching calls are asynchronous on `stream` (a cudaStream_t passed as void*, NULL = the
+ *     legacy default stream).  Argument errors are reported synchronously.  A wait that gives up
+ *     inside a kernel (every mbarrier wait is bounded, default 1 s, TM_WAIT_TIMEOUT_NS overrides)
+ *     is recorded in a per-device status word and reported by tm_stream_check().
+ *   - The first call that launches work on a device allocates that device's 64-byte status word
+ *     (cudaMalloc) and reads its attributes; make that first call before capturing a stream.
+ *     A call given an explicit list of more than 8 boxes stages the list in device memory with
+ *     cudaMallocAsync/cudaFreeAsync on `stream`.
+ */
+#ifndef TMAP_GB300_H
+#define TMAP_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes --------------------------------------------------------------------------- */
+#define TM_OK 0
+#define TM_EINVAL 1        /* malformed argument: NULL pointer, bad enum, rank, count mismatch   */
+#define TM_EALIGN 2        /* an address, stride or inner box row breaks an alignment rule       */
+#define TM_ERANGE 3        /* a size is out of range: dim, box, stride, or box too large for smem */
+#define TM_EUNSUPPORTED 4  /* legal for the hardware but not supported by this library           */
+#define TM_ECUDA 5         /* the CUDA runtime or driver reported an error                       */
+#define TM_ETIMEOUT 6      /* a bounded wait inside a kernel gave up                             */
+
+/* ---- element types (numerically equal to CUtensorMapDataType) ----------------------------- */
+typedef enum tm_dtype {
+    TM_U8 = 0, TM_U16 = 1, TM_U32 = 2, TM_S32 = 3, TM_U64 = 4, TM_S64 = 5,
+    TM_F16 = 6, TM_F32 = 7, TM_F64 = 8, TM_BF16 = 9
+} tm_dtype;
+
+/* ---- swizzle modes (numerically equal to CUtensorMapSwizzle) -------------------------------
+ * [MLSys-TMA] §"TMA 如何写入 swizzled layout" and §"用 3D TMA 搬运多个 swizzle atoms": with 128B,
+ * inside each atom of 8 rows x 128 bytes the 16-byte sector c of image row r is written to sector
+ * c XOR (r % 8).  64B / 32B are the narrower atoms of §"128-byte swizzle 的分组要求" (8 rows x 64 /
+ * 32 bytes, XOR of the row bits 7..8 / 7 into the chunk bits 4..5 / 4).  With any swizzle the inner
+ * box row must be exactly the atom width (boxDim[0] * element size == 32, 64 or 128 bytes). */
+typedef enum tm_swizzle {
+    TM_SWIZZLE_NONE = 0, TM_SWIZZLE_32B = 1, TM_SWIZZLE_64B = 2, TM_SWIZZLE_128B = 3
+} tm_swizzle;
+
+/* ---- out-of-bounds fill, [H200-TMA] §02 (out-of-bounds row: the hardware fills with 0 / NaN) - */
+typedef enum tm_oob { TM_OOB_ZERO = 0, TM_OOB_NAN = 1 /* not supported: TM_EUNSUPPORTED */ } tm_oob;
+
+/* ---- execution paths ------------------------------------------------------------------------ */
+#define TM_PATH_TMA 1      /* cp.async.bulk.tensor with a driver-encoded tensor map               */
+#define TM_PATH_FALLBACK 2 /* 16-byte vector loads/stores + warp shuffles where TMA cannot go     */
+/* why a descriptor is on the fallback path (bit set in tm_desc.why_fallback) */
+#define TM_WHY_STRIDE 1u   /* a global stride is not a multiple of 16 bytes ([H200-TMA] §03)     */
+#define TM_WHY_BASE 2u     /* the base address is not 16-byte aligned ([H200-TMA] §03)           */
+#define TM_WHY_DRIVER 4u   /* the driver's encoder refused the map                               */
+#define TM_WHY_FORCED 8u   /* tmap_force_fallback() was called                                   */
+
+/* ---- the descriptor -------------------------------------------------------------------------
+ * [MLSys-TMA] §"一个 thread 如何描述整个 tile": the descriptor says how the whole tensor is laid
+ * out (type, shape, strides, box, swizzle); each copy only adds a start coordinate and a
+ * shared-memory address.  [Book-TMA] §"Tensor descriptor：CUtensorMap" lists its fields.
+ * A caller-allocated plain struct, 64-byte aligned ([H200-TMA] §03: the CUtensorMap object itself
+ * is 64-byte aligned), filled by tmap_encode() or tmap_plan() and passed by pointer; the library
+ * copies the embedded CUtensorMap into kernel parameter space (__grid_constant__, [H200-TMA] §03).
+ * Field offsets are part of the ABI (static-asserted in the library). */
+typedef struct __attribute__((aligned(64))) tm_desc {
+    uint32_t magic;         /* TM_DESC_MAGIC once filled                                        */
+    uint32_t dtype;         /* tm_dtype                                                         */
+    uint32_t esize;         /* element size in bytes                                            */
+    uint32_t rank;          /* 1..5                                                             */
+    uint32_t swizzle;       /* tm_swizzle                                                       */
+    uint32_t oob;           /* tm_oob                                                           */
+    uint32_t path;          /* TM_PATH_TMA or TM_PATH_FALLBACK                                  */
+    uint32_t why_fallback;  /* TM_WHY_* bits when path == TM_PATH_FALLBACK                      */
+    uint64_t base;          /* device address of element (0, ..., 0)                           */
+    uint64_t dim[5];        /* globalDim, innermost first (unused entries 1)                    */
+    uint64_t stride[5];     /* byte stride of each dim; stride[0] = esize (unused entries 0)    */
+    uint32_t box[5];        /* boxDim (unused entries 1)                                        */
+    uint32_t estride[5];    /* elementStrides (always 1 here)                                   */
+    uint64_t nbox[5];       /* boxes along each dim: ceil(dim / box)                           */
+    uint64_t box_bytes;     /* bytes of one box image: esize * prod(box)                       */
+    uint64_t num_boxes;     /* prod(nbox)                                                       */
+    uint8_t reserved[40];
+    uint8_t tmap[128];      /* CUtensorMap (driver-encoded) when path == TM_PATH_TMA            */
+} tm_desc;
+
+#define TM_DESC_MAGIC 0x544d4150u /* "TMAP" */
+#define TM_MAX_BOX_BYTES 229376u  /* 224 KiB: one image must fit a CTA's shared memory          */
+#define TM_MAX_STAGES 16u
+
+/* tmap_plan -- validate a tensor map and fill `out` without touching the GPU or the driver.
+ *   [H200-TMA] §03 rules: 1 <= rank <= 5 (else TM_EINVAL); 1 <= globalDim[i] <= 2^32 and
+ *   1 <= boxDim[i] <= 256 (else TM_ERANGE); boxDim[0] * esize a multiple of 16 bytes (else
+ *   TM_EALIGN); globalStrides below 2^40 (else TM_ERANGE).  [MLSys-TMA] §"用 3D TMA 搬运多个
+ *   swizzle atoms" and §"128-byte swizzle 的分组要求": with a swizzle, boxDim[0] * esize equals the
+ *   atom width (else TM_EUNSUPPORTED).  elementStrides (NULL = all 1) must be all 1 and oob must be
+ *   TM_OOB_ZERO (else TM_EUNSUPPORTED).  box_bytes above TM_MAX_BOX_BYTES gives TM_ERANGE.
+ *   A base or stride that is a multiple of the element size but not of 16 bytes is NOT an error:
+ *   the map goes to the fallback path (why_fallback says which).  A base or stride that is not a
+ *   multiple of the element size gives TM_EALIGN.
+ *   dtype, rank, base: element type, number of dims, device address of element (0,...,0).
+ *   globalDim[rank]: elements per dim.  globalStrides[rank-1]: bytes between neighbours along dims
+ *   1..rank-1 (any order, strides need not grow with the dim index: [MLSys-TMA] §"用 3D TMA 搬运多个
+ *   swizzle atoms" regroups a row with a smaller outer stride).  boxDim[rank]: box shape. */
+int tmap_plan(tm_desc* out, tm_dtype dtype, uint32_t rank, void* base, const uint64_t* globalDim,
+              const uint64_t* globalStrides, const uint32_t* boxDim,
+              const uint32_t* elementStrides, tm_swizzle swizzle, tm_oob oob);
+
+/* tmap_encode -- tmap_plan(), then, for a TMA-path map, encode the CUtensorMap with the driver's
+ *   cuTensorMapEncodeTiled ([H200-TMA] §04 ①, [Book-TMA] §"单 block、单 lane、单 tile 的 TMA load";
+ *   the map is created on the host, [H200-TMA] §05).  If the driver refuses a map that passed
+ *   validation, the map goes to the fallback path with TM_WHY_DRIVER.  TM_ECUDA if no driver is
+ *   reachable.  Same arguments as tmap_plan(). */
+int tmap_encode(tm_desc* out, tm_dtype dtype, uint32_t rank, void* base,
+                const uint64_t* globalDim, const uint64_t* globalStrides, const uint32_t* boxDim,
+                const uint32_t* elementStrides, tm_swizzle swizzle, tm_oob oob);
+
+/* tmap_replace_address -- move an encoded map to another base address of the same layout
+ *   ([H200-TMA] §03 and §05: rebase with cuTensorMapReplaceAddress rather than rebuilding on the
+ *   device).  A new base that is not 16-byte aligned moves the map to the fallback path; one that
+ *   is not a multiple of the element size gives TM_EALIGN. */
+int tmap_replace_address(tm_desc* d, void* new_base);
+
+/* tmap_force_fallback -- put a valid map on the fallback path (why_fallback |= TM_WHY_FORCED).
+ *   Used to check that both paths produce identical bytes. */
+int tmap_force_fallback(tm_desc* d);
+
+/* tile_load_image -- one box to its shared-memory image, written to `image` (device, box_bytes,
+ *   16-byte aligned).  [Book-TMA] §"单 block、单 lane、单 tile 的 TMA load" (one block, one lane,
+ *   one tile) and [MLSys-TMA] §"TMA 如何写入 swizzled layout": image element e (box coordinates,
+ *   dim 0 fastest) sits at swizzle(lin(e) * esize); elements outside the tensor are zero bytes.
+ *   coords[rank] (host): signed start of the box; may lie partly or wholly outside the tensor. */
+int tile_load_image(const tm_desc* src, const int32_t* coords, void* image, void* stream);
+
+/* tiled_copy -- images of many boxes, image b written at images + b * box_bytes (tile-major).
+ *   coords == NULL: the whole box grid, box b = k0 + nbox0 * (k1 + nbox1 * (...)) starting at
+ *   k[i] * box[i]; nbox must be 0 or num_boxes.  Otherwise coords holds nbox * rank int32 (host).
+ *   Each box is one TMA load completed through an mbarrier byte count ([MLSys-TMA] §"如何等待 TMA
+ *   load 完成") and one bulk store of the image completed through a bulk async group.  `images`:
+ *   device, nbox * box_bytes, 16-byte aligned. */
+int tiled_copy(const tm_desc* src, const int32_t* coords, size_t nbox, void* images,
+               void* stream);
+
+/* tiled_roundtrip -- the reverse of tiled_copy: image b (device, tile-major as above) is stored
+ *   through `dst` at box b's coordinates.  Only in-bounds elements are written; padding and
+ *   everything else in dst keeps its bytes.  Completion of each store is tracked with
+ *   commit_group / wait_group ([MLSys-TMA] §"如何等待 TMA store 完成", [Book-TMA] §"TMA store"). */
+int tiled_roundtrip(const tm_desc* dst, const int32_t* coords, size_t nbox, const void* images,
+                    void* stream);
+
+/* tile_reduce_add -- dst += src over the whole box grid, fp32, one IEEE binary32 add (round to
+ *   nearest) per in-bounds element, performed by the bulk tensor reduce ([Book-TMA] §"TMA reduce，
+ *   把“搬运”和“归约”合并").  Both maps TM_F32 with equal dims, box and swizzle (else TM_EINVAL /
+ *   TM_EUNSUPPORTED); strides and bases may differ.  dst and src must not overlap. */
+int tile_reduce_add(const tm_desc* dst, const tm_desc* src, void* stream);
+
+/* stream_tiles -- a `stages`-deep producer/consumer ring ([MLSys-TMA] §"把 TMA 放进 pipeline"):
+ *   one elected producer thread fills stage s with tile t of A and tile t of B (one mbarrier,
+ *   expect_tx = 2 * box_bytes), consumer warps read the stage through the swizzle and release it.
+ *   A and B: TM_BF16, rank 2, box {64, R} with R in {32, 64, 128, 256}, swizzle 128B or NONE,
+ *   TMA path, equal num_boxes; tiles are walked in box-grid order.  Per tile t (device outputs,
+ *   num_boxes entries each): cs = fp32 checksum (each row summed in order from its first element,
+ *   then a pairwise-adjacent tree over the rows), bits = sum of the 16-bit patterns.
+ *   stages: 2..8. */
+int stream_tiles(const tm_desc* a, const tm_desc* b, uint32_t stages, float* cs_a, float* cs_b,
+                 uint64_t* bits_a, uint64_t* bits_b, void* stream);
+
+/* tm_stream_check -- synchronise `stream`, then read and clear the current device's status word:
+ *   TM_ETIMEOUT if a kernel's bounded wait gave up since the last check (tm_last_error() names the
+ *   kernel, block, stage, phase and box), TM_ECUDA on a CUDA error, else TM_OK.  Kernels on
+ *   different streams share the word: the first failure is kept. */
+int tm_stream_check(void* stream);
+
+/* tm_selftest_wait_timeout -- launch one block that waits, with the given limit, on an mbarrier
+ *   nothing will complete; the wait gives up, records TM_ETIMEOUT and the kernel returns.  Lets a
+ *   caller check that failure reporting works without faulting anything. */
+int tm_selftest_wait_timeout(uint64_t timeout_ns, void* stream);
+
+const char* tm_last_error(void);
+size_t tm_box_bytes(const tm_desc* d);   /* 0 for an unfilled descriptor */
+size_t tm_num_boxes(const tm_desc* d);   /* 0 for an unfilled descriptor */
+int tm_path(const tm_desc* d);           /* TM_PATH_* or 0 */
+size_t tm_desc_size(void);               /* sizeof(tm_desc) == 384 */
+/* The widest swizzle whose atom row fits `inner_bytes` exactly, [MLSys-TMA] §"128-byte swizzle 的
+ * 分组要求" (choose the widest swizzle the tile allows, else 64 or 32 bytes): 128 -> 128B,
+ * 64 -> 64B, 32 -> 32B, anything else -> NONE. */
+int tm_pick_swizzle(uint32_t inner_bytes);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* TMAP_GB300_H */

@@ -1,0 +1,36 @@
+"""Helpers for the GPU parity tests: one map recipe, built on both sides (the C-ABI library over a
+device buffer, the oracle over the same bytes on the host)."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+
+SPAN_TO_SW = {0: 0, 32: 1, 64: 2, 128: 3}
+ESIZE_TO_DTYPE = {1: 0, 2: 9, 4: 7, 8: 4}  # u8, bf16, f32, u64: copies are bitwise
+
+
+def to_dev(arr: np.ndarray):
+    import torch
+    flat = np.ascontiguousarray(arr).reshape(-1).view(np.uint8)
+    return torch.from_numpy(flat.copy()).cuda()
+
+
+def to_host(t) -> np.ndarray:
+    return t.cpu().numpy()
+
+
+def dev_map(tm, buf, r, offset=0, dtype=None):
+    dt = ESIZE_TO_DTYPE[r["esize"]] if dtype is None else dtype
+    return tm.tmap_encode(dt, buf.data_ptr() + offset, r["dims"], r["strides"], r["box"],
+                          swizzle=SPAN_TO_SW[r["span"]])
+
+
+def host_map(arr: np.ndarray, r, offset=0):
+    return oracle.Map(arr, r["esize"], r["dims"], r["strides"], r["box"], r["span"],
+                      offset=offset)
+
+
+def empty_images(n_boxes: int, box_bytes: int, fill: int = 0x5A):
+    import torch
+    return torch.full((n_boxes * box_bytes,), fill, dtype=torch.uint8, device="cuda")

@@ -1,0 +1,323 @@
+"""GPU parity: every result of the CUDA path, through the C ABI, equals the CPU oracle's bit for
+bit, on the pages' example shapes and on reduced copies of the large workloads that still span
+several boxes and a ragged tail.
+
+Page tags: [MLSys-TMA] mlc.ai "Modern GPU Programming for MLSys", chapter "异步数据搬运：TMA";
+[Book-TMA] fangpin "gpu-hpc-book" ch. 08 "Cuda TMA"; [H200-TMA] coolgpu H200 TMA feature card.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from gpu_util import dev_map, empty_images, host_map, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def tm():
+    import async_bulk_tensor_tmap_gb300 as m  # raises if the CUDA library is missing
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return m
+
+
+def check(tm):
+    torch.cuda.synchronize()
+    rc = tm.tm_stream_check()
+    assert rc == tm.TM_OK, tm.tm_last_error()
+
+
+def w1_recipe(span):
+    return dict(dims=[128, 16], strides=[256], box=[64, 8], span=span, esize=2)
+
+
+# ---- W1: [MLSys-TMA] §"TMA 如何写入 swizzled layout", 16 x 128 fp16, one 8 x 64 box --------------
+@pytest.mark.parametrize("span", [0, 128])
+@pytest.mark.parametrize("start", [(0, 0), (64, 8)])
+def test_w1_image_and_roundtrip(tm, span, start):
+    x = workloads.w1_tensor()
+    r = w1_recipe(span)
+    xd = to_dev(x)
+    m = dev_map(tm, xd, r, dtype=tm.TM_F16)
+    assert m.path == tm.TM_PATH_TMA
+    img = empty_images(1, 1024)
+    tm.tile_load_image(m, list(start), img)
+    check(tm)
+    want = oracle.image(host_map(x, r), start)
+    np.testing.assert_array_equal(to_host(img), want)
+    # round trip into a sentinel-filled tensor: only the box's elements change
+    dst = torch.full((16 * 128 * 2,), 0xEE, dtype=torch.uint8, device="cuda")
+    md = dev_map(tm, dst, r, dtype=tm.TM_F16)
+    tm.tiled_roundtrip(md, [list(start)], img)
+    check(tm)
+    host_dst = np.full(16 * 128 * 2, 0xEE, dtype=np.uint8)
+    oracle.store(host_map(host_dst, r), start, want)
+    np.testing.assert_array_equal(to_host(dst), host_dst)
+
+
+# ---- W2: [MLSys-TMA] §"用 3D TMA 搬运多个 swizzle atoms", 3-D regrouped views --------------------
+W2_VIEWS = {128: (64, [0, 0, 0], [0, 0, 2]), 64: (32, [0, 0, 0], [0, 0, 4]),
+            32: (16, [0, 0, 0], [0, 0, 8])}
+
+
+@pytest.mark.parametrize("span", [128, 64, 32])
+def test_w2_regrouped_views(tm, span):
+    x = workloads.w2_tensor()
+    gcols, c0, c1 = W2_VIEWS[span]
+    r = dict(dims=[gcols, 16, 256 // gcols], strides=[512, gcols * 2], box=[gcols, 16, 128 // gcols],
+             span=span, esize=2)
+    xd = to_dev(x)
+    m = dev_map(tm, xd, r, dtype=tm.TM_F16)
+    imgs = empty_images(2, 4096)
+    tm.tiled_copy(m, [c0, c1], imgs)
+    check(tm)
+    want = oracle.tiled_copy(host_map(x, r), coords=[c0, c1])
+    np.testing.assert_array_equal(to_host(imgs), want)
+    print(f"W2 {span}B view path={m.path} why={m.why_fallback}")
+    if span == 128:  # the per-slice map (base moved to column 128) gives the same second image
+        rs = dict(dims=[64, 16, 2], strides=[512, 128], box=[64, 16, 2], span=128, esize=2)
+        ms = dev_map(tm, xd, rs, offset=256, dtype=tm.TM_F16)
+        one = empty_images(1, 4096)
+        tm.tile_load_image(ms, [0, 0, 0], one)
+        check(tm)
+        np.testing.assert_array_equal(to_host(one), want[4096:])
+
+
+# ---- W3 (reduced): bf16 matrix, 128 x 64 boxes, 128B, ragged in both dims -------------------------
+def w3_small(span=128, rows=1000, cols=776):
+    x = workloads.w3_tensor(rows, cols, seed=31)
+    return x, workloads.w3_map(rows, cols, span=span)
+
+
+@pytest.mark.parametrize("span", [128, 0])
+@pytest.mark.parametrize("force_fallback", [False, True])
+def test_w3_copy_and_roundtrip(tm, span, force_fallback):
+    x, r = w3_small(span)
+    xd = to_dev(x)
+    m = dev_map(tm, xd, r)
+    if force_fallback:
+        tm.tmap_force_fallback(m)
+    n, bb = m.num_boxes, m.box_bytes
+    assert n == 8 * 13
+    imgs = empty_images(n, bb)
+    tm.tiled_copy(m, None, imgs)
+    check(tm)
+    want = oracle.tiled_copy(host_map(x, r), threads=8)
+    np.testing.assert_array_equal(to_host(imgs), want)
+    dst = torch.full_like(xd, 0x77)
+    md = dev_map(tm, dst, r)
+    if force_fallback:
+        tm.tmap_force_fallback(md)
+    tm.tiled_roundtrip(md, None, imgs)
+    check(tm)
+    assert torch.equal(dst, xd)
+
+
+def test_w3_fallback_and_tma_images_identical(tm):
+    x, r = w3_small(128, rows=520, cols=392)
+    xd = to_dev(x)
+    a, b = dev_map(tm, xd, r), dev_map(tm, xd, r)
+    tm.tmap_force_fallback(b)
+    ia, ib = empty_images(a.num_boxes, a.box_bytes, 1), empty_images(b.num_boxes, b.box_bytes, 2)
+    tm.tiled_copy(a, None, ia)
+    tm.tiled_copy(b, None, ib)
+    check(tm)
+    assert torch.equal(ia, ib)
+
+
+def test_unaligned_base_takes_fallback(tm):
+    x, r = w3_small(0, rows=300, cols=200)
+    raw = np.zeros(x.size * 2 + 64, np.uint8)
+    raw[8:8 + x.size * 2] = x.reshape(-1).view(np.uint8)
+    rd = to_dev(raw)
+    m = dev_map(tm, rd, r, offset=8)
+    assert m.path == tm.TM_PATH_FALLBACK and m.why_fallback == tm.TM_WHY_BASE
+    imgs = empty_images(m.num_boxes, m.box_bytes)
+    tm.tiled_copy(m, None, imgs)
+    check(tm)
+    want = oracle.tiled_copy(host_map(raw, r, offset=8))
+    np.testing.assert_array_equal(to_host(imgs), want)
+    out = torch.full_like(rd, 0x33)
+    mo = dev_map(tm, out, r, offset=8)
+    tm.tiled_roundtrip(mo, None, imgs)
+    check(tm)
+    host_out = np.full_like(raw, 0x33)
+    oracle.tiled_roundtrip(host_map(host_out, r, offset=8), want)
+    np.testing.assert_array_equal(to_host(out), host_out)
+
+
+# ---- explicit box lists: inline (<= 8) and staged in device memory; odd starts go to fallback ---
+@pytest.mark.parametrize("nbox", [5, 40])
+@pytest.mark.parametrize("kind", ["grid_shuffled", "odd_starts"])
+def test_box_lists(tm, nbox, kind):
+    x, r = w3_small(128, rows=700, cols=520)
+    xd = to_dev(x)
+    m = dev_map(tm, xd, r)
+    rng = np.random.default_rng(nbox)
+    if kind == "grid_shuffled":
+        starts = [m_ for m_ in (oracle.Map(x, 2, r["dims"], r["strides"], r["box"], 128)
+                                .box_start(b) for b in range(m.num_boxes))]
+        coords = [starts[i] for i in rng.permutation(len(starts))[:nbox]]
+    else:  # x starts 3 elements off the 16-byte grid, first box partly before the tensor
+        coords = [[-3 + 64 * (k % 9), 128 * (k // 9) - (5 if k == 0 else 0)] for k in range(nbox)]
+    imgs = empty_images(nbox, m.box_bytes)
+    tm.tiled_copy(m, coords, imgs)
+    check(tm)
+    want = oracle.tiled_copy(host_map(x, r), coords=coords)
+    np.testing.assert_array_equal(to_host(imgs), want)
+    # write the images back through the list into a sentinel tensor (boxes do not overlap)
+    dst = torch.full_like(xd, 0x44)
+    md = dev_map(tm, dst, r)
+    tm.tiled_roundtrip(md, coords, imgs)
+    check(tm)
+    host_dst = np.full(xd.numel(), 0x44, np.uint8)
+    oracle.tiled_roundtrip(host_map(host_dst, r), want, coords=coords)
+    np.testing.assert_array_equal(to_host(dst), host_dst)
+
+
+def test_wholly_outside_box_is_zero(tm):
+    x, r = w3_small(128, rows=300, cols=200)
+    m = dev_map(tm, to_dev(x), r)
+    coords = [[-64, 0], [256, 0], [0, 300], [0, -128]]
+    imgs = empty_images(4, m.box_bytes, 0xFF)
+    tm.tiled_copy(m, coords, imgs)
+    check(tm)
+    assert int(imgs.count_nonzero()) == 0
+
+
+# ---- W4 (reduced): padded rank-3 tensor, ragged boxes, sentinel padding, rank-5 fallback view ----
+W4_SMALL = dict(batch=16, rows=70, cols=1000, pitch=1024)
+
+
+@pytest.mark.parametrize("variant", ["r3_128B", "r3_64B", "r5_none", "r5_128B"])
+def test_w4_ragged_and_fallback(tm, variant):
+    x = workloads.w4_tensor(**W4_SMALL, seed=41)
+    if variant == "r3_128B":
+        r = workloads.w4_rank3_map(64, span=128, **W4_SMALL)
+    elif variant == "r3_64B":
+        r = workloads.w4_rank3_map(32, span=64, **W4_SMALL)
+    else:
+        r = workloads.w4_rank5_map(**W4_SMALL, span=0 if variant == "r5_none" else 128)
+    xd = to_dev(x)
+    m = dev_map(tm, xd, r)
+    assert m.path == (tm.TM_PATH_FALLBACK if variant.startswith("r5") else tm.TM_PATH_TMA)
+    imgs = empty_images(m.num_boxes, m.box_bytes)
+    tm.tiled_copy(m, None, imgs)
+    check(tm)
+    want = oracle.tiled_copy(host_map(x, r), threads=8)
+    np.testing.assert_array_equal(to_host(imgs), want)
+    # round trip into an all-sentinel tensor: the in-bounds elements come back, padding survives
+    dst = torch.from_numpy(np.full(x.size, workloads.SENTINEL_U16, np.uint16).view(np.uint8)).cuda()
+    md = dev_map(tm, dst, r)
+    tm.tiled_roundtrip(md, None, imgs)
+    check(tm)
+    assert torch.equal(dst, xd)
+
+
+# ---- W5a (reduced): fp32 reduce-add, [Book-TMA] §"TMA reduce，把“搬运”和“归约”合并" ----------------
+@pytest.mark.parametrize("span", [128, 0])
+@pytest.mark.parametrize("force_fallback", [False, True])
+def test_w5a_reduce_add(tm, span, force_fallback):
+    d, s = workloads.w5a_tensors(rows=300, cols=200, seed_dst=7, seed_src=8)
+    r = workloads.w5a_map(rows=300, cols=200, span=span)
+    dd, sd = to_dev(d), to_dev(s)
+    md, ms = dev_map(tm, dd, r), dev_map(tm, sd, r)
+    if force_fallback:
+        tm.tmap_force_fallback(md)
+    tm.tile_reduce_add(md, ms)
+    check(tm)
+    hd = d.copy()
+    oracle.tile_reduce_add(host_map(hd, r), host_map(s, r))
+    np.testing.assert_array_equal(to_host(dd).view(np.uint32), hd.reshape(-1).view(np.uint32))
+
+
+# ---- W5b (reduced): the ring, [MLSys-TMA] §"把 TMA 放进 pipeline" ---------------------------------
+@pytest.mark.parametrize("span", [128, 0])
+@pytest.mark.parametrize("stages", [2, 4, 8])
+def test_w5b_ring_checksums(tm, span, stages):
+    a, b = workloads.w5b_tensors(m=380, k=248, n=376, seed_a=9, seed_b=10)
+    ra, rb = workloads.w5b_maps(m=380, k=248, n=376, span=span)
+    ad, bd = to_dev(a), to_dev(b)
+    ma, mb = dev_map(tm, ad, ra), dev_map(tm, bd, rb)
+    n = ma.num_boxes
+    assert n == mb.num_boxes == 12
+    cs_a = torch.zeros(n, dtype=torch.float32, device="cuda")
+    cs_b = torch.zeros_like(cs_a)
+    bits_a = torch.zeros(n, dtype=torch.int64, device="cuda")
+    bits_b = torch.zeros_like(bits_a)
+    tm.stream_tiles(ma, mb, stages, cs_a, cs_b, bits_a, bits_b)
+    check(tm)
+    wa, wb, wba, wbb = oracle.stream_checksums(host_map(a, ra), host_map(b, rb))
+    np.testing.assert_array_equal(to_host(cs_a).view(np.uint32), wa.view(np.uint32))
+    np.testing.assert_array_equal(to_host(cs_b).view(np.uint32), wb.view(np.uint32))
+    np.testing.assert_array_equal(to_host(bits_a).astype(np.uint64), wba)
+    np.testing.assert_array_equal(to_host(bits_b).astype(np.uint64), wbb)
+
+
+# ---- brute force: random tiny maps of every rank, swizzle and element size ----------------------
+def random_recipe(rng, span, aligned):
+    rank = int(rng.integers(1, 6))
+    es = int(rng.choice([2, 4])) if span else int(rng.choice([1, 2, 4, 8]))
+    box = [int(rng.integers(1, 5)) for _ in range(rank)]
+    box[0] = span // es if span else (16 // es) * int(rng.integers(1, 3))
+    dims = [int(rng.integers(1, 6)) for _ in range(rank)]
+    dims[0] = int(rng.integers(1, box[0] + 7))
+    strides, step = [], dims[0] * es
+    order = rng.permutation(np.arange(1, rank))
+    st = [0] * rank
+    for dd in order:
+        pad = int(rng.integers(0, 3)) * es
+        if aligned:
+            step = (step + 15) // 16 * 16
+        st[dd] = step
+        step = step * dims[dd] + pad
+    strides = [st[i] for i in range(1, rank)]
+    return dict(dims=dims, strides=strides, box=box, span=span, esize=es), step + 64
+
+
+@pytest.mark.parametrize("span", [0, 32, 64, 128])
+@pytest.mark.parametrize("aligned", [True, False])
+def test_brute_force_tiny(tm, span, aligned):
+    rng = np.random.default_rng(500 + span + aligned)
+    for _ in range(25):
+        r, nbytes = random_recipe(rng, span, aligned)
+        x = rng.integers(0, 256, size=nbytes, dtype=np.uint16).astype(np.uint8)
+        xd = to_dev(x)
+        m = dev_map(tm, xd, r)
+        coords = [[int(rng.integers(-3, d + 4)) for d in r["dims"]] for _ in range(3)]
+        coords.append([0] * len(r["dims"]))
+        imgs = empty_images(len(coords), m.box_bytes)
+        tm.tiled_copy(m, coords, imgs)
+        check(tm)
+        want = oracle.tiled_copy(host_map(x, r), coords=coords)
+        np.testing.assert_array_equal(to_host(imgs), want, err_msg=f"{r} {coords} path={m.path}")
+        # whole grid, then back into a sentinel copy
+        g = empty_images(m.num_boxes, m.box_bytes)
+        tm.tiled_copy(m, None, g)
+        dst = torch.full_like(xd, 0xC3)
+        md = dev_map(tm, dst, r)
+        tm.tiled_roundtrip(md, None, g)
+        check(tm)
+        hg = oracle.tiled_copy(host_map(x, r))
+        np.testing.assert_array_equal(to_host(g), hg)
+        hdst = np.full_like(x, 0xC3)
+        oracle.tiled_roundtrip(host_map(hdst, r), hg)
+        np.testing.assert_array_equal(to_host(dst), hdst)
+
+
+# ---- bounded waits: a wait that nothing completes gives up and reports, the GPU stays usable -----
+def test_wait_timeout_is_reported_and_recoverable(tm):
+    tm.tm_selftest_wait_timeout(50_000_000)
+    rc = tm.tm_stream_check()
+    assert rc == tm.TM_ETIMEOUT
+    assert "self-test" in tm.tm_last_error()
+    assert tm.tm_stream_check() == tm.TM_OK  # the status word was cleared
+    x, r = w3_small(128, rows=256, cols=128)
+    m = dev_map(tm, to_dev(x), r)
+    imgs = empty_images(m.num_boxes, m.box_bytes)
+    tm.tiled_copy(m, None, imgs)
+    check(tm)
+    np.testing.assert_array_equal(to_host(imgs), oracle.tiled_copy(host_map(x, r)))

@@ -43,7 +43,7 @@ def normal_bf16(shape, seed: int) -> np.ndarray:
     """bf16 bit patterns of normal(0, 1) draws, shape outermost first."""
     rng = np.random.default_rng(seed)
     out = np.empty(int(np.prod(shape)), dtype=np.uint16)
-    chunk = 1 << 24
+    chunk = 1 << 22
     for i in range(0, out.size, chunk):
         n = min(chunk, out.size - i)
         out[i:i + n] = f32_to_bf16_bits(rng.standard_normal(n, dtype=np.float32))
@@ -90,26 +90,34 @@ TINY_F32 = np.float32(2.0 ** -126)  # smallest normal binary32
 
 def w5a_tensors(rows: int = 16384, cols: int = 16384, seed_dst: int = SEEDS["w5a_dst"],
                 seed_src: int = SEEDS["w5a_src"]):
-    """fp32 destination normal(0, 1) and source uniform(-1, 1).  Pairs whose operands or exact sum
-    would be subnormal are redrawn, so flush-to-zero can never decide a result."""
+    """fp32 destination normal(0, 1) and source uniform(-1, 1) (2u - 1 with u uniform on [0, 1),
+    exact in float32).  Pairs whose operands or exact sum would be subnormal are redrawn, so
+    flush-to-zero can never decide a result."""
     rd = np.random.default_rng(seed_dst)
     rs = np.random.default_rng(seed_src)
-    dst = rd.standard_normal((rows, cols), dtype=np.float32)
-    src = rs.uniform(-1.0, 1.0, size=(rows, cols)).astype(np.float32)
+    dst = np.empty((rows, cols), dtype=np.float32)
+    src = np.empty((rows, cols), dtype=np.float32)
     fd = dst.reshape(-1)
     fs = src.reshape(-1)
-    chunk = 1 << 24
+    chunk = 1 << 22
     for i in range(0, fd.size, chunk):
         d = fd[i:i + chunk]
         s = fs[i:i + chunk]
+        rd.standard_normal(d.size, dtype=np.float32, out=d)
+        rs.random(s.size, dtype=np.float32, out=s)
+        s *= 2
+        s -= 1
         while True:
-            exact = d.astype(np.float64) + s.astype(np.float64)
+            # Both operands are multiples of 2^-149, so a sum below 2^-126 in magnitude is exactly
+            # representable and the float32 sum equals the exact one there.
+            tot = d + s
             bad = (((np.abs(d) < TINY_F32) & (d != 0)) | ((np.abs(s) < TINY_F32) & (s != 0))
-                   | ((np.abs(exact) < float(TINY_F32)) & (exact != 0)))
+                   | ((np.abs(tot) < TINY_F32) & (tot != 0)))
             if not bad.any():
                 break
-            s[bad] = rs.uniform(-1.0, 1.0, size=int(bad.sum())).astype(np.float32)
-            d[bad] = rd.standard_normal(int(bad.sum()), dtype=np.float32)
+            nb = int(bad.sum())
+            s[bad] = rs.random(nb, dtype=np.float32) * np.float32(2) - np.float32(1)
+            d[bad] = rd.standard_normal(nb, dtype=np.float32)
     return dst, src
 
 
