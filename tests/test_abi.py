@@ -16,8 +16,8 @@ HEADER = os.path.join(ROOT, "include", "tmap.h")
 
 @pytest.fixture(scope="module")
 def tm():
-    from async_bulk_tensor_tmap_gb300.csrc import build as b
-    b.build()
+    import __graft_entry__
+    __graft_entry__._cuda_build_module().build()
     import async_bulk_tensor_tmap_gb300 as m
     return m
 
