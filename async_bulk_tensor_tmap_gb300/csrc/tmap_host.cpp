@@ -251,6 +251,15 @@ int make_walk(const tm_desc* d, const int32_t* coords, size_t n, cudaStream_t st
     return TM_OK;
 }
 
+// The tensor store and the tensor reduce write whole 16-byte units of the innermost dimension
+// (measured on GB300: with globalDim[0] * esize not a multiple of 16, the out-of-bounds tail of
+// the last unit of every row is overwritten with the image's zero fill).  Such maps store on the
+// vector path, which writes exactly the in-bounds bytes.
+bool store_fits_tma(const tm_desc* d)
+{
+    return d->path == TM_PATH_TMA && (d->dim[0] * d->esize) % 16 == 0;
+}
+
 void release_walk(const BoxWalk& w, cudaStream_t st)
 {
     if (w.mode == WALK_LIST && w.list) cudaFreeAsync((void*)w.list, st);
@@ -527,7 +536,7 @@ int tiled_roundtrip(const tm_desc* dst, const int32_t* coords, size_t nbox, cons
     int rc = device_state(&ds);
     if (rc) return rc;
     cudaStream_t st = (cudaStream_t)stream;
-    const bool tma = dst->path == TM_PATH_TMA && (!coords || list_fits_tma(dst, coords, n, true));
+    const bool tma = store_fits_tma(dst) && (!coords || list_fits_tma(dst, coords, n, true));
     BoxWalk w;
     if ((rc = make_walk(dst, coords, n, st, w))) return rc;
     if (tma) {
@@ -563,7 +572,7 @@ int tile_reduce_add(const tm_desc* dst, const tm_desc* src, void* stream)
     BoxWalk w;
     if ((rc = make_walk(dst, nullptr, 0, st, w))) return rc;
     const uint64_t n = dst->num_boxes;
-    if (dst->path == TM_PATH_TMA && src->path == TM_PATH_TMA) {
+    if (store_fits_tma(dst) && src->path == TM_PATH_TMA) {
         const Geometry g = tma_geometry(*ds, n, stage_bytes_of(dst->box_bytes));
         const StreamArgs a = stream_args(dst, w, 0, g.stages, *ds);
         rc = check_launch(launch_tma_stream(KIND_REDUCE, dst->rank, (const CUtensorMap*)src->tmap,

@@ -164,14 +164,20 @@ int tiled_copy(const tm_desc* src, const int32_t* coords, size_t nbox, void* ima
 /* tiled_roundtrip -- the reverse of tiled_copy: image b (device, tile-major as above) is stored
  *   through `dst` at box b's coordinates.  Only in-bounds elements are written; padding and
  *   everything else in dst keeps its bytes.  Completion of each store is tracked with
- *   commit_group / wait_group ([MLSys-TMA] §"如何等待 TMA store 完成", [Book-TMA] §"TMA store"). */
+ *   commit_group / wait_group ([MLSys-TMA] §"如何等待 TMA store 完成", [Book-TMA] §"TMA store").
+ *   The tensor store writes whole 16-byte units of the innermost dimension, so a map whose
+ *   globalDim[0] * esize is not a multiple of 16 (or a box list starting off the 16-byte grid or
+ *   outside the tensor) is stored by the vector path instead, which writes exactly the in-bounds
+ *   bytes. */
 int tiled_roundtrip(const tm_desc* dst, const int32_t* coords, size_t nbox, const void* images,
                     void* stream);
 
 /* tile_reduce_add -- dst += src over the whole box grid, fp32, one IEEE binary32 add (round to
  *   nearest) per in-bounds element, performed by the bulk tensor reduce ([Book-TMA] §"TMA reduce，
  *   把“搬运”和“归约”合并").  Both maps TM_F32 with equal dims, box and swizzle (else TM_EINVAL /
- *   TM_EUNSUPPORTED); strides and bases may differ.  dst and src must not overlap. */
+ *   TM_EUNSUPPORTED); strides and bases may differ.  dst and src must not overlap.  As for
+ *   tiled_roundtrip, a dst whose globalDim[0] * esize is not a multiple of 16 is reduced by the
+ *   vector path (one IEEE add per element, same result). */
 int tile_reduce_add(const tm_desc* dst, const tm_desc* src, void* stream);
 
 /* stream_tiles -- a `stages`-deep producer/consumer ring ([MLSys-TMA] §"把 TMA 放进 pipeline"):
