@@ -22,8 +22,10 @@ def to_host(t) -> np.ndarray:
 
 def dev_map(tm, buf, r, offset=0, dtype=None):
     dt = ESIZE_TO_DTYPE[r["esize"]] if dtype is None else dtype
-    return tm.tmap_encode(dt, buf.data_ptr() + offset, r["dims"], r["strides"], r["box"],
-                          swizzle=SPAN_TO_SW[r["span"]])
+    m = tm.tmap_encode(dt, buf.data_ptr() + offset, r["dims"], r["strides"], r["box"],
+                       swizzle=SPAN_TO_SW[r["span"]])
+    m.keepalive = buf  # the map holds a raw address: keep the tensor it points into alive
+    return m
 
 
 def host_map(arr: np.ndarray, r, offset=0):
