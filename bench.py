@@ -57,6 +57,10 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--ops", default="", help="comma list of op names to run (default: all)")
+    p.add_argument("--scale", type=int, default=1,
+                   help="divide every workload's row count by this (small cases for profiling)")
+    p.add_argument("--ring-swizzle", default="128", choices=["128", "none"],
+                   help="swizzle of the ring's tiles (none = the bank-conflict control)")
     return p.parse_args()
 
 
@@ -69,19 +73,21 @@ def dist_env():
 # Workload: host arrays (numpy, the bytes both the GPU and the oracle see) and maps
 # ------------------------------------------------------------------------------------------------
 class HostWorkload:
-    def __init__(self):
+    def __init__(self, scale: int = 1, ops=None, ring_span: int = 128):
         t0 = time.time()
-        self.w3 = workloads.w3_tensor()
-        self.w4 = workloads.w4_tensor()
-        self.w5a_dst, self.w5a_src = workloads.w5a_tensors()
-        self.w5b_a, self.w5b_b = workloads.w5b_tensors()
+        need = lambda prefix: ops is None or any(o.startswith(prefix) for o in ops)
+        r3, r4, r5a, m5b = 8192 // scale, 4095 // scale, 16384 // scale, 8192 // scale
+        self.w3 = workloads.w3_tensor(r3, 8192) if need("w3") else None
+        self.w4 = workloads.w4_tensor(rows=r4) if need("w4") else None
+        self.w5a_dst, self.w5a_src = workloads.w5a_tensors(r5a) if need("w5a") else (None, None)
+        self.w5b_a, self.w5b_b = workloads.w5b_tensors(m5b, 4096, m5b) if need("w5b") else (None, None)
         self.gen_s = time.time() - t0
-        self.r3 = workloads.w3_map()
-        self.r4_128 = workloads.w4_rank3_map(64, span=128)
-        self.r4_64 = workloads.w4_rank3_map(32, span=64)
-        self.r4_r5 = workloads.w4_rank5_map(span=128)
-        self.r5a = workloads.w5a_map()
-        self.r5b_a, self.r5b_b = workloads.w5b_maps()
+        self.r3 = workloads.w3_map(r3, 8192)
+        self.r4_128 = workloads.w4_rank3_map(64, rows=r4, span=128)
+        self.r4_64 = workloads.w4_rank3_map(32, rows=r4, span=64)
+        self.r4_r5 = workloads.w4_rank5_map(rows=r4, span=128)
+        self.r5a = workloads.w5a_map(r5a, 16384)
+        self.r5b_a, self.r5b_b = workloads.w5b_maps(m5b, 4096, m5b, span=ring_span)
 
 
 def box_count(r):
@@ -129,35 +135,40 @@ class GpuWorkload:
         import async_bulk_tensor_tmap_gb300 as tm
         self.tm, self.torch, self.stream = tm, torch, stream
         dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).reshape(-1).view(np.uint8)).cuda()
-        self.t = {
-            "w3": dev(h.w3), "w4": dev(h.w4), "w5a_dst": dev(h.w5a_dst),
-            "w5a_src": dev(h.w5a_src), "w5b_a": dev(h.w5b_a), "w5b_b": dev(h.w5b_b),
-        }
-        self.t["w3_out"] = torch.empty_like(self.t["w3"])
-        self.t["w4_out"] = self.t["w4"].clone()
+        self.t = {k: dev(getattr(h, k)) for k in ("w3", "w4", "w5a_dst", "w5a_src", "w5b_a",
+                                                  "w5b_b") if getattr(h, k) is not None}
         sw = {0: 0, 32: 1, 64: 2, 128: 3}
 
         def enc(dtype, buf, r):
             return tm.tmap_encode(dtype, buf, r["dims"], r["strides"], r["box"], swizzle=sw[r["span"]])
 
         bf, f32 = tm.TM_BF16, tm.TM_F32
-        self.maps = {
-            "w3": enc(bf, self.t["w3"], h.r3), "w3_out": enc(bf, self.t["w3_out"], h.r3),
-            "w4r3": enc(bf, self.t["w4"], h.r4_128), "w4r3_out": enc(bf, self.t["w4_out"], h.r4_128),
-            "w4r3n": enc(bf, self.t["w4"], h.r4_64), "w4r3n_out": enc(bf, self.t["w4_out"], h.r4_64),
-            "w4r5": enc(bf, self.t["w4"], h.r4_r5), "w4r5_out": enc(bf, self.t["w4_out"], h.r4_r5),
-            "w5a_dst": enc(f32, self.t["w5a_dst"], h.r5a), "w5a_src": enc(f32, self.t["w5a_src"], h.r5a),
-            "w5b_a": enc(bf, self.t["w5b_a"], h.r5b_a), "w5b_b": enc(bf, self.t["w5b_b"], h.r5b_b),
-        }
+        self.maps = {}
+        if "w3" in self.t:
+            self.t["w3_out"] = torch.empty_like(self.t["w3"])
+            self.maps["w3"] = enc(bf, self.t["w3"], h.r3)
+            self.maps["w3_out"] = enc(bf, self.t["w3_out"], h.r3)
+        if "w4" in self.t:
+            self.t["w4_out"] = self.t["w4"].clone()
+            for k, r in (("w4r3", h.r4_128), ("w4r3n", h.r4_64), ("w4r5", h.r4_r5)):
+                self.maps[k] = enc(bf, self.t["w4"], r)
+                self.maps[f"{k}_out"] = enc(bf, self.t["w4_out"], r)
+        if "w5a_dst" in self.t:
+            self.maps["w5a_dst"] = enc(f32, self.t["w5a_dst"], h.r5a)
+            self.maps["w5a_src"] = enc(f32, self.t["w5a_src"], h.r5a)
+        if "w5b_a" in self.t:
+            self.maps["w5b_a"] = enc(bf, self.t["w5b_a"], h.r5b_a)
+            self.maps["w5b_b"] = enc(bf, self.t["w5b_b"], h.r5b_b)
+            n = self.maps["w5b_a"].num_boxes
+            self.t["cs_a"] = torch.zeros(n, dtype=torch.float32, device="cuda")
+            self.t["cs_b"] = torch.zeros(n, dtype=torch.float32, device="cuda")
+            self.t["bits_a"] = torch.zeros(n, dtype=torch.int64, device="cuda")
+            self.t["bits_b"] = torch.zeros(n, dtype=torch.int64, device="cuda")
         for k in ("w3", "w4r3", "w4r3n", "w4r5"):
-            m = self.maps[k]
-            self.t[f"{k}_img"] = torch.empty(m.num_boxes * m.box_bytes, dtype=torch.uint8,
-                                             device="cuda")
-        n = self.maps["w5b_a"].num_boxes
-        self.t["cs_a"] = torch.zeros(n, dtype=torch.float32, device="cuda")
-        self.t["cs_b"] = torch.zeros(n, dtype=torch.float32, device="cuda")
-        self.t["bits_a"] = torch.zeros(n, dtype=torch.int64, device="cuda")
-        self.t["bits_b"] = torch.zeros(n, dtype=torch.int64, device="cuda")
+            if k in self.maps:
+                m = self.maps[k]
+                self.t[f"{k}_img"] = torch.empty(m.num_boxes * m.box_bytes, dtype=torch.uint8,
+                                                 device="cuda")
         self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
         self.paths = {k: m.path for k, m in self.maps.items()}
 
@@ -180,7 +191,8 @@ class GpuWorkload:
 
 
 class ClockSampler:
-    """nvidia-smi samples (every 200 ms) while the timed region runs."""
+    """nvidia-smi samples (every 100 ms) from the first warm-up step to the end of the timed
+    steps."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -193,7 +205,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.th = threading.Thread(target=self._read, daemon=True)
             self.th.start()
@@ -230,10 +242,14 @@ class ClockSampler:
 def time_steps(g: GpuWorkload, ops, steps, warmup):
     """Per-op device ms for each timed step (events on the launching stream)."""
     torch = g.torch
-    for _ in range(warmup):
+    t0, done = time.time(), 0
+    while done < warmup or time.time() - t0 < 1.0:
         for name, _ in ops:
             g.flush_l2()
             g.run_op(name)
+        done += 1
+        if done >= warmup:
+            torch.cuda.synchronize()
     torch.cuda.synchronize()
     rc = g.tm.tm_stream_check(g.stream)
     if rc != g.tm.TM_OK:
@@ -389,6 +405,26 @@ def measured_hbm_peak():
         return 6800.0, "fallback"
 
 
+def recorded_traffic(kernel: str):
+    """Per-launch DRAM traffic of `kernel` from profiles/roofline_traffic.txt, or None when the
+    kernel's source changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "roofline_traffic.txt")
+    try:
+        fields = dict(ln.split(":", 1) for ln in open(path) if ":" in ln and not ln.startswith("#"))
+    except OSError:
+        return None
+    fields = {k.strip(): v.strip() for k, v in fields.items()}
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "async_bulk_tensor_tmap_gb300", "csrc")
+    for f in ("k_tma.cu", "tm_ptx.cuh", "tm_internal.h"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    if fields.get("kernel") != kernel or fields.get("source_sha256") != h.hexdigest():
+        return None
+    return int(fields["traffic_bytes"])
+
+
 def select_ops(h, spec):
     ops = op_table(h)
     if spec:
@@ -401,7 +437,8 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    h = HostWorkload()
+    h = HostWorkload(args.scale, args.ops.split(",") if args.ops else None,
+                     0 if args.ring_swizzle == "none" else 128)
     ops = select_ops(h, args.ops)
     cores = cpu_cores()
     frac = calibrated_fraction(h, ops, cores, target_s=2.0)
@@ -439,7 +476,8 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     else:
         torch.cuda.set_device(0)
-    h = HostWorkload()
+    h = HostWorkload(args.scale, args.ops.split(",") if args.ops else None,
+                     0 if args.ring_swizzle == "none" else 128)
     ops = select_ops(h, args.ops)
     stream = torch.cuda.Stream()
     g = GpuWorkload(h, stream)
@@ -477,10 +515,16 @@ def main():
     dom_name, dom_bytes = dom
     dom_ms = statistics.mean(per[dom_name])
     achieved = dom_bytes / dom_ms / 1e6
-    e2e_ms, bi, bo = e2e_run(g, h, ops, args.e2e_steps)
-    e2e_value = world * step_bytes / (e2e_ms * 1e-3) / GB
+    if args.e2e_steps > 0:
+        e2e_ms, bi, bo = e2e_run(g, h, ops, args.e2e_steps)
+        e2e = {"value": world * step_bytes / (e2e_ms * 1e-3) / GB, "unit": "GB/s",
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
+    else:
+        e2e = None
     if rank != 0:
         return
+    if args.scale != 1:
+        args.no_cpu_baseline = True
     cpu = None
     if not args.no_cpu_baseline:
         cores = cpu_cores()
@@ -500,9 +544,8 @@ def main():
                              if not k.endswith("_out")}},
         "roofline": {"kernel": dom_name, "bound": "hbm", "achieved": achieved, "peak": peak,
                      "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None},
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": bi,
-                "d2h_bytes_per_step": bo},
+                     "traffic": recorded_traffic(dom_name) if args.scale == 1 else None},
+        "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": len(ops) * args.steps,
         "clocks": clk.summary(),
