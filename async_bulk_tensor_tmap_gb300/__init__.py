@@ -11,6 +11,7 @@ Function names and argument order follow the C ABI:
     tile_load_image(src, coords, image, stream=None)
     tiled_copy(src, coords, images, stream=None)            coords None = whole box grid
     tiled_roundtrip(dst, coords, images, stream=None)
+    tiled_copy_noalloc(src, coords, images, stream=None)  no device allocation, returns when done
     tile_reduce_add(dst, src, stream=None)
     stream_tiles(a, b, stages, cs_a, cs_b, bits_a, bits_b, stream=None)
     tm_stream_check(stream=None), tm_selftest_wait_timeout(timeout_ns, stream=None)
@@ -24,7 +25,8 @@ import os
 __all__ = [
     "TmapError", "TensorMap", "tmap_plan", "tmap_encode", "tmap_replace_address",
     "tmap_force_fallback", "tile_load_image", "tiled_copy", "tiled_roundtrip", "tile_reduce_add",
-    "stream_tiles", "tm_stream_check", "tm_selftest_wait_timeout", "tm_pick_swizzle",
+    "stream_tiles", "tiled_copy_noalloc", "TM_NOALLOC_MAX_BOXES", "tm_stream_check",
+    "tm_selftest_wait_timeout", "tm_pick_swizzle", "tm_last_error",
     "library_path", "TM_OK", "TM_EINVAL", "TM_EALIGN", "TM_ERANGE", "TM_EUNSUPPORTED",
     "TM_ECUDA", "TM_ETIMEOUT", "TM_U8", "TM_U16", "TM_U32", "TM_S32", "TM_U64", "TM_S64",
     "TM_F16", "TM_F32", "TM_F64", "TM_BF16", "TM_SWIZZLE_NONE", "TM_SWIZZLE_32B",
@@ -39,6 +41,7 @@ TM_OOB_ZERO, TM_OOB_NAN = 0, 1
 TM_PATH_TMA, TM_PATH_FALLBACK = 1, 2
 TM_WHY_STRIDE, TM_WHY_BASE, TM_WHY_DRIVER, TM_WHY_FORCED = 1, 2, 4, 8
 DESC_SIZE = 384
+TM_NOALLOC_MAX_BOXES = 16384
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libtmap_gb300.so")
@@ -64,6 +67,7 @@ _SIGS = {
     "tile_load_image": [_vp, _P(_i32), _vp, _vp],
     "tiled_copy": [_vp, _P(_i32), ctypes.c_size_t, _vp, _vp],
     "tiled_roundtrip": [_vp, _P(_i32), ctypes.c_size_t, _vp, _vp],
+    "tiled_copy_noalloc": [_vp, _P(_i32), ctypes.c_size_t, _vp, _vp],
     "tile_reduce_add": [_vp, _vp, _vp],
     "stream_tiles": [_vp, _vp, _u32, _vp, _vp, _vp, _vp, _vp],
     "tm_stream_check": [_vp],
@@ -232,6 +236,17 @@ def tiled_copy(src: TensorMap, coords, images, stream=None) -> None:
         c, n = _coords(coords, src.rank)
         rc = _L.tiled_copy(src.ptr, c, n, _addr(images), _stream(stream))
     _check(rc, "tiled_copy")
+
+
+def tiled_copy_noalloc(src: TensorMap, coords, images, stream=None) -> None:
+    """tiled_copy without any device allocation (fixed library-owned scratch; at most
+    TM_NOALLOC_MAX_BOXES listed boxes); returns once the copy has finished."""
+    if coords is None:
+        rc = _L.tiled_copy_noalloc(src.ptr, None, 0, _addr(images), _stream(stream))
+    else:
+        c, n = _coords(coords, src.rank)
+        rc = _L.tiled_copy_noalloc(src.ptr, c, n, _addr(images), _stream(stream))
+    _check(rc, "tiled_copy_noalloc")
 
 
 def tiled_roundtrip(dst: TensorMap, coords, images, stream=None) -> None:

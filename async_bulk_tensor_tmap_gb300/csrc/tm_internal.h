@@ -103,4 +103,7 @@ cudaError_t launch_ring(const CUtensorMap* a, const CUtensorMap* b, const RingAr
                         uint32_t grid, size_t smem, cudaStream_t s);
 cudaError_t launch_selftest(uint64_t timeout_ns, StatusBlock* status, cudaStream_t s);
 
+// Sets the thread's tm_last_error() text; returns `code`.
+int set_last_error(int code, const char* msg);
+
 }  // namespace tmk

@@ -446,6 +446,8 @@ int encode_into(tm_desc* d)
 
 }  // namespace
 
+int tmk::set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
 extern "C" {
 
 int tmap_plan(tm_desc* out, tm_dtype dtype, uint32_t rank, void* base, const uint64_t* globalDim,

@@ -191,6 +191,25 @@ int tile_reduce_add(const tm_desc* dst, const tm_desc* src, void* stream);
 int stream_tiles(const tm_desc* a, const tm_desc* b, uint32_t stages, float* cs_a, float* cs_b,
                  uint64_t* bits_a, uint64_t* bits_b, void* stream);
 
+/* tiled_copy_noalloc -- tiled_copy for callers that must not allocate device memory.  The pages
+ *   have no counterpart: it exists because tiled_copy allocates (its first launching call on a
+ *   device cudaMallocs the status word; a list of more than 8 boxes is staged with
+ *   cudaMallocAsync), and some callers cannot allow an allocation -- code running while another
+ *   allocator owns all device memory, processes under a hard device-memory cap where a late
+ *   allocation may fail, latency-critical loops that cannot afford an allocator call.
+ *   Same arguments and the same image bytes as tiled_copy.  All scratch (a status word and the
+ *   box list, at most TM_NOALLOC_MAX_BOXES boxes; a longer list gives TM_ERANGE) lives in one
+ *   fixed __device__ array of 327,936 bytes inside the library, held by every GPU that loads the
+ *   library until the process exits.  The first call on a device looks up that array's device
+ *   address (cudaGetSymbolAddress, with the device current); make that first call before any
+ *   stream capture.  The call returns when the copy has finished: it synchronises `stream` and
+ *   returns TM_ETIMEOUT itself if a wait inside the kernel gave up.  Every call shares the one
+ *   array and clears its status word first: calls that overlap on the GPU (other host threads,
+ *   other streams) race on it and must not be issued. */
+#define TM_NOALLOC_MAX_BOXES 16384u
+int tiled_copy_noalloc(const tm_desc* src, const int32_t* coords, size_t nbox, void* images,
+                       void* stream);
+
 /* tm_stream_check -- synchronise `stream`, then read and clear the current device's status word:
  *   TM_ETIMEOUT if a kernel's bounded wait gave up since the last check (tm_last_error() names the
  *   kernel, block, stage, phase and box), TM_ECUDA on a CUDA error, else TM_OK.  Kernels on
