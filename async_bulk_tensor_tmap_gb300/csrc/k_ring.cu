@@ -7,41 +7,61 @@
 // tiles of a stage complete on ONE mbarrier whose expected byte count is their sum (2 x 2048 bytes
 // there, 2 x 16 KiB for 128 x 64 bf16 tiles).
 //
-// CTA = 3 warps.  Warp 0: producer, one elected lane.  Warp 1 consumes the A tile of each stage,
-// warp 2 the B tile.  full[s] (count 1) completes when both tiles' bytes have landed; empty[s]
-// (count 2) completes when both consumer warps have read the stage.
+// The ring holds S stages of shared memory; to keep more bytes in flight than that, the producer
+// also prefetches tiles a few iterations ahead into L2 (cp.async.bulk.prefetch.tensor), so that
+// each stage's load finds its tiles in L2.
 //
-// Consumer reads follow [MLSys-TMA] §"128-byte swizzle 的分组要求": lane l reads image rows l, l+32,
-// ...; at any instant eight neighbouring lanes read the same logical sector c of eight consecutive
-// rows, which the 128B swizzle has spread over physical sectors c XOR (row % 8): eight distinct
-// bank sectors, no conflict.  With swizzle NONE the same reads all hit sector c (8-way conflict).
+// CTA = 9 warps.  Warp 0: producer, one elected lane.  Warps 1-4 consume the A tile of each stage,
+// warps 5-8 the B tile (fewer for tiles under 128 rows); each consumer warp takes whole 32-row
+// blocks.  full[s] (count 1) completes when both tiles' bytes have landed; empty[s] (one arrival
+// per consumer warp) when every consumer warp has read the stage.  The per-warp partial sums meet
+// in shared-memory slots guarded by one more mbarrier per slot (S + 1 slots: no warp can be S
+// iterations ahead of another, so a slot is never rewritten before it was read).  Every wait is
+// bounded; no named barrier is used, so a warp that gives up cannot leave the others hanging.
+//
+// Consumer reads follow [MLSys-TMA] §"128-byte swizzle 的分组要求": lane l reads row l of a 32-row
+// block; at any instant eight neighbouring lanes read the same logical sector c of eight
+// consecutive rows, which the 128B swizzle has spread over physical sectors c XOR (row % 8): eight
+// distinct bank sectors, no conflict.  With swizzle NONE the same reads all hit sector c (8-way
+// conflict).
 //
 // What the consumer computes (the pages leave it open): per tile, each row is summed in fp32 in
 // logical element order starting from its first element; rows are combined by a pairwise-adjacent
 // tree (xor-shuffles 1, 2, 4, 8, 16 inside each 32-row block, then pairs of blocks); plus the exact
-// integer sum of the 16-bit patterns.
+// integer sum of the 16-bit patterns.  (The warps hold contiguous 32-row blocks in order, so the
+// shuffle levels, the in-warp block pairs and the cross-warp pairs together form exactly the
+// pairwise-adjacent tree over all rows.)
 #include "tm_ptx.cuh"
 
 namespace tmk {
 
 constexpr uint32_t kRingMaxStages = 8;
+constexpr uint32_t kRingMaxWpt = 4;                 // consumer warps per tile
+constexpr uint32_t kRingSlots = kRingMaxStages + 1;  // reduction slots: one more than the stages
+constexpr uint32_t kRingThreads = 32 * (1 + 2 * kRingMaxWpt);
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-__global__ void __launch_bounds__(96, 1)
+__global__ void __launch_bounds__(kRingThreads, 1)
     k_ring(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
            const __grid_constant__ RingArgs r)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kRingMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kRingMaxStages];
+    __shared__ __align__(8) uint64_t red_bar[2][kRingSlots];
+    __shared__ float red_cs[2][kRingSlots][kRingMaxWpt];
+    __shared__ uint32_t red_bits[2][kRingSlots][kRingMaxWpt];
 
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + (kStageAlign - 1)) & ~(kStageAlign - 1);
     const uint8_t* const stage0 = smem_raw + (base - raw);
     const uint32_t S = r.stages;
+    const uint32_t NS = S + 1;
     const uint32_t tile = r.tile_bytes;  // multiple of 1024
+    const uint32_t wpt = r.rows >= 32 * kRingMaxWpt ? kRingMaxWpt : r.rows / 32;
+    const uint32_t rpl = r.rows / (32 * wpt);  // rows per lane
 
     const uint64_t first = blockIdx.x;
     if (r.ntiles <= first) return;
@@ -52,7 +72,11 @@ __global__ void __launch_bounds__(96, 1)
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < S; s++) {
             mbar_init(smem_u32(&full_bar[s]), 1);
-            mbar_init(smem_u32(&empty_bar[s]), 2);
+            mbar_init(smem_u32(&empty_bar[s]), 2 * wpt);
+        }
+        for (uint32_t s = 0; s < NS; s++) {
+            mbar_init(smem_u32(&red_bar[0][s]), wpt);
+            mbar_init(smem_u32(&red_bar[1][s]), wpt);
         }
         fence_barrier_init();
     }
@@ -63,6 +87,22 @@ __global__ void __launch_bounds__(96, 1)
         if (!elect_one()) return;
         prefetch_tmap(&ma);
         prefetch_tmap(&mb);
+        auto coords = [&](uint64_t i, int32_t* ca, int32_t* cb) {
+            const uint64_t t = first + i * gridDim.x;
+            ca[0] = (int32_t)((t % r.a_nb0) * 64);
+            ca[1] = (int32_t)((t / r.a_nb0) * r.rows);
+            cb[0] = (int32_t)((t % r.b_nb0) * 64);
+            cb[1] = (int32_t)((t / r.b_nb0) * r.rows);
+        };
+        // Optional L2 prefetch r.prefetch tiles ahead of the loads (no completion is tracked).
+        auto prefetch = [&](uint64_t i) {
+            if (i >= n_local) return;
+            int32_t ca[2], cb[2];
+            coords(i, ca, cb);
+            tma_prefetch_l2_2d(&ma, ca[0], ca[1]);
+            tma_prefetch_l2_2d(&mb, cb[0], cb[1]);
+        };
+        for (uint64_t j = S; j < r.prefetch; j++) prefetch(j);
         uint64_t i = 0;
         for (; i < n_local; i++) {
             const uint32_t s = (uint32_t)(i % S);
@@ -74,13 +114,13 @@ __global__ void __launch_bounds__(96, 1)
                     break;
                 }
             }
-            const uint64_t t = first + i * gridDim.x;
             const uint32_t bar = smem_u32(&full_bar[s]);
-            const int32_t ca[2] = {(int32_t)((t % r.a_nb0) * 64), (int32_t)((t / r.a_nb0) * r.rows)};
-            const int32_t cb[2] = {(int32_t)((t % r.b_nb0) * 64), (int32_t)((t / r.b_nb0) * r.rows)};
+            int32_t ca[2], cb[2];
+            coords(i, ca, cb);
             mbar_arrive_expect_tx(bar, 2 * tile);
             tma_load<2>(base + s * 2 * tile, &ma, ca, bar);
             tma_load<2>(base + s * 2 * tile + tile, &mb, cb, bar);
+            if (r.prefetch) prefetch(i + r.prefetch);
         }
         // Loads still landing (only after a failure): wait for them, bounded, before leaving.
         const uint64_t lo = i > S ? i - S : 0;
@@ -90,11 +130,13 @@ __global__ void __launch_bounds__(96, 1)
         return;
     }
 
-    // ---------------- consumers: warp 1 -> A, warp 2 -> B ----------------
-    const uint32_t which = warp - 1;
-    const uint32_t rpl = r.rows >> 5;  // rows per lane
-    float* const cs_out = which == 0 ? r.cs_a : r.cs_b;
-    unsigned long long* const bits_out = which == 0 ? r.bits_a : r.bits_b;
+    // ---------------- consumers: warps 1..wpt read A, the next wpt read B ----------------
+    const uint32_t cw = warp - 1;
+    if (cw >= 2 * wpt) return;  // launched but idle (small tiles)
+    const uint32_t grp = cw / wpt;   // 0 = A, 1 = B
+    const uint32_t wi = cw % wpt;    // warp index inside the tile
+    float* const cs_out = grp == 0 ? r.cs_a : r.cs_b;
+    unsigned long long* const bits_out = grp == 0 ? r.bits_a : r.bits_b;
     const uint32_t xr = r.swizzled ? 7u : 0u;
 
     for (uint64_t i = 0; i < n_local; i++) {
@@ -106,34 +148,58 @@ __global__ void __launch_bounds__(96, 1)
             if (lane == 0) record_timeout(r.status, K_STREAM, s, parity, first + i * gridDim.x);
             break;
         }
-        const uint8_t* const t_img = stage0 + s * 2 * tile + which * tile;
+        const uint8_t* const t_img = stage0 + s * 2 * tile + grp * tile;
 
+        // This warp's rows: 32-row blocks wi*rpl .. wi*rpl + rpl - 1, lane l row l of a block.
+        // All of them are read into registers first; the stage is released as soon as the reads
+        // are done (the arrive orders them before the producer's next write into the stage), and
+        // the sums are formed afterwards.
         float blk[8];
         uint32_t bits = 0;
 #pragma unroll
-        for (uint32_t q = 0; q < 8; q++) {
-            if (q < rpl) {
-                const uint32_t row = lane + 32 * q;
-                const uint8_t* const rp = t_img + row * 128;
-                float acc = 0.f;
+        for (uint32_t q0 = 0; q0 < 8; q0 += 2) {
+            if (q0 < rpl) {
+                uint4 v[2][8];
 #pragma unroll
-                for (uint32_t c = 0; c < 8; c++) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(rp + ((c ^ (row & xr)) << 4));
-                    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+                for (uint32_t u = 0; u < 2; u++) {
+                    const uint32_t row = 32 * (wi * rpl + q0 + u) + lane;
+                    const uint8_t* const rp = t_img + row * 128;
 #pragma unroll
-                    for (int h = 0; h < 4; h++) {
-                        acc = (c == 0 && h == 0) ? bf16lo(w[h]) : __fadd_rn(acc, bf16lo(w[h]));
-                        acc = __fadd_rn(acc, bf16hi(w[h]));
-                        bits += (w[h] & 0xffffu) + (w[h] >> 16);
+                    for (uint32_t c = 0; c < 8; c++) {
+                        v[u][c] = (q0 + u < rpl)
+                                      ? *reinterpret_cast<const uint4*>(rp + ((c ^ (row & xr)) << 4))
+                                      : make_uint4(0, 0, 0, 0);
                     }
                 }
-                blk[q] = acc;
+                if (q0 + 2 >= rpl) {  // last rows of this warp read: release the stage
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));
+                }
+#pragma unroll
+                for (uint32_t u = 0; u < 2; u++) {
+                    if (q0 + u < rpl) {
+                        float acc = 0.f;
+                        uint32_t lo16 = 0, hi16 = 0;
+#pragma unroll
+                        for (uint32_t c = 0; c < 8; c++) {
+                            const uint32_t w[4] = {v[u][c].x, v[u][c].y, v[u][c].z, v[u][c].w};
+#pragma unroll
+                            for (int h = 0; h < 4; h++) {
+                                acc = (c == 0 && h == 0) ? bf16lo(w[h])
+                                                         : __fadd_rn(acc, bf16lo(w[h]));
+                                acc = __fadd_rn(acc, bf16hi(w[h]));
+                                lo16 += w[h] & 0xffffu;
+                                hi16 += w[h] >> 16;
+                            }
+                        }
+                        bits += lo16 + hi16;
+                        blk[q0 + u] = acc;
+                    }
+                }
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty_bar[s]));  // stage read: release it
 
-        // pairwise tree: inside each 32-row block by xor-shuffles, then across blocks
+        // pairwise tree: inside each 32-row block by xor-shuffles, then across this warp's blocks
 #pragma unroll
         for (uint32_t q = 0; q < 8; q++) {
             if (q < rpl) {
@@ -151,10 +217,32 @@ __global__ void __launch_bounds__(96, 1)
         }
 #pragma unroll
         for (int m = 16; m >= 1; m >>= 1) bits += __shfl_xor_sync(0xffffffffu, bits, m);
+
+        // ... then across the tile's warps, in warp order (slots of iteration i % NS)
+        const uint32_t slot = (uint32_t)(i % NS);
         if (lane == 0) {
+            red_cs[grp][slot][wi] = blk[0];
+            red_bits[grp][slot][wi] = bits;
+            mbar_arrive(smem_u32(&red_bar[grp][slot]));
+        }
+        if (wi == 0 && lane == 0) {
+            const uint32_t rp = (uint32_t)((i / NS) & 1);
+            if (!mbar_wait(smem_u32(&red_bar[grp][slot]), rp, r.timeout_ns)) {
+                record_timeout(r.status, K_STREAM, slot, rp, first + i * gridDim.x);
+                break;
+            }
+            float part[kRingMaxWpt];
+            unsigned long long total = 0;
+            for (uint32_t w = 0; w < wpt; w++) {
+                part[w] = red_cs[grp][slot][w];
+                total += red_bits[grp][slot][w];
+            }
+            for (uint32_t n = wpt; n > 1; n >>= 1) {
+                for (uint32_t q = 0; q < n / 2; q++) part[q] = __fadd_rn(part[2 * q], part[2 * q + 1]);
+            }
             const uint64_t t = first + i * gridDim.x;
-            cs_out[t] = blk[0];
-            bits_out[t] = (unsigned long long)bits;
+            cs_out[t] = part[0];
+            bits_out[t] = total;
         }
     }
 }
@@ -175,7 +263,7 @@ cudaError_t launch_ring(const CUtensorMap* a, const CUtensorMap* b, const RingAr
     cudaError_t e =
         cudaFuncSetAttribute(k_ring, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_ring<<<grid, 96, smem, s>>>(*a, *b, r);
+    k_ring<<<grid, kRingThreads, smem, s>>>(*a, *b, r);
     return cudaGetLastError();
 }
 

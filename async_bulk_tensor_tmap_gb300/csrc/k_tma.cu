@@ -2,16 +2,22 @@
 //
 // One CTA is one warp; its elected lane issues everything ([MLSys-TMA] = mlc.ai "Modern GPU
 // Programming for MLSys", chapter "异步数据搬运：TMA", §"一个 thread 如何描述整个 tile": a single
-// thread submits the copy, the engine does the addressing).  The lane walks the launch's boxes
-// blockIdx.x, blockIdx.x + gridDim.x, ... through an S-stage ring of 1024-byte aligned shared-memory
-// stages:
+// thread submits the copy, the engine does the addressing).  Boxes are taken in groups of G
+// consecutive boxes (G > 1 only for small boxes whose size is a multiple of 1024 bytes, so that
+// each image in a stage keeps the swizzle phase it has in its own image); the lane walks the
+// groups blockIdx.x, blockIdx.x + gridDim.x, ... through an S-stage ring of 1024-byte aligned
+// shared-memory stages:
 //
-//   load   box i into stage i % S       (mbarrier arrive.expect_tx + complete_tx, §"如何等待 TMA
-//                                         load 完成")
+//   load   group i into stage i % S     (one mbarrier, arrive.expect_tx of the group's bytes, one
+//                                         complete_tx per box, §"如何等待 TMA load 完成")
 //   wait   full[i % S] for parity (i / S) & 1           -- bounded
 //   write  stage i % S out, commit a bulk group          (§"如何等待 TMA store 完成")
-//   refill stage (i - 1) % S with box i - 1 + S once the bulk group of box i - 1 has finished
-//          READING shared memory (wait_group.read 1): the write of box i stays in flight.
+//   refill stage (i - 1) % S with group i - 1 + S once the bulk group of group i - 1 has finished
+//          READING shared memory (wait_group.read 1): the write of group i stays in flight
+//          (with a single stage, the stage of group i once its own write has read it).
+//
+// Grid coordinates of consecutive boxes are stepped with an odometer rather than recomputed with
+// 64-bit divisions.
 //
 // The three kinds differ only in the two copy instructions:
 //   copy       load = tensor load of the box;  write = 1-D bulk store of the image (tile-major)
@@ -33,9 +39,13 @@ __global__ void __launch_bounds__(32, 1)
 
     if (!elect_one()) return;
 
+    // Work unit: a group of `a.group` consecutive boxes sharing one stage (their images are
+    // consecutive in the tile-major buffer as well).
+    const uint64_t G = a.group;
+    const uint64_t ngroups = (a.walk.nbox + G - 1) / G;
     const uint64_t first = blockIdx.x;
-    if (a.walk.nbox <= first) return;
-    const uint64_t n_local = (a.walk.nbox - 1 - first) / gridDim.x + 1;
+    if (ngroups <= first) return;
+    const uint64_t n_local = (ngroups - 1 - first) / gridDim.x + 1;
     const uint32_t S = a.stages;
     const uint32_t base = (smem_u32(smem_raw) + (kStageAlign - 1)) & ~(kStageAlign - 1);
 
@@ -44,43 +54,73 @@ __global__ void __launch_bounds__(32, 1)
     for (uint32_t s = 0; s < S; s++) mbar_init(smem_u32(&full_bar[s]), 1);
     fence_barrier_init();
 
-    auto box_of = [&](uint64_t i) -> uint64_t { return first + i * gridDim.x; };
+    auto group_of = [&](uint64_t i) -> uint64_t { return first + i * gridDim.x; };
+    auto count_of = [&](uint64_t g) -> uint32_t {
+        const uint64_t b0 = g * G;
+        return (uint32_t)(a.walk.nbox - b0 < G ? a.walk.nbox - b0 : G);
+    };
+
+    // Calls fn(k, coords) for the boxes of group g, in order.
+    auto for_boxes = [&](uint64_t g, auto&& fn) {
+        const uint64_t b0 = g * G;
+        const uint32_t cnt = count_of(g);
+        int32_t c[5];
+        if (a.walk.mode == WALK_GRID) {
+            uint32_t k[5];
+            grid_counters(a.walk, b0, k);
+            for (uint32_t j = 0; j < cnt; j++) {
+#pragma unroll
+                for (int i = 0; i < 5; i++) c[i] = (int32_t)(k[i] * a.walk.box[i]);
+                fn(j, c);
+                grid_next(a.walk, k);
+            }
+        } else {
+            for (uint32_t j = 0; j < cnt; j++) {
+                box_start(a.walk, b0 + j, c);
+                fn(j, c);
+            }
+        }
+    };
 
     auto issue = [&](uint64_t i) {
         const uint32_t s = (uint32_t)(i % S);
         const uint32_t bar = smem_u32(&full_bar[s]);
         const uint32_t dst = base + s * a.stage_bytes;
-        const uint64_t b = box_of(i);
-        mbar_arrive_expect_tx(bar, a.box_bytes);
+        const uint64_t g = group_of(i);
+        const uint32_t bytes = count_of(g) * a.box_bytes;
+        mbar_arrive_expect_tx(bar, bytes);
         if constexpr (KIND == KIND_ROUNDTRIP) {
-            bulk_load(dst, a.images + b * a.box_bytes, a.box_bytes, bar);
+            bulk_load(dst, a.images + g * G * a.box_bytes, bytes, bar);
         } else {
-            int32_t c[5];
-            box_start(a.walk, b, c);
-            tma_load<R>(dst, &in_map, c, bar);
+            for_boxes(g, [&](uint32_t j, const int32_t* c) {
+                tma_load<R>(dst + j * a.box_bytes, &in_map, c, bar);
+            });
         }
     };
 
     auto write_out = [&](uint64_t i) {
         const uint32_t s = (uint32_t)(i % S);
         const uint32_t src = base + s * a.stage_bytes;
-        const uint64_t b = box_of(i);
+        const uint64_t g = group_of(i);
         if constexpr (KIND == KIND_COPY) {
-            bulk_store(a.images + b * a.box_bytes, src, a.box_bytes);
+            bulk_store(a.images + g * G * a.box_bytes, src, count_of(g) * a.box_bytes);
         } else {
-            int32_t c[5];
-            box_start(a.walk, b, c);
-            if constexpr (KIND == KIND_ROUNDTRIP) {
-                tma_store<R>(&out_map, c, src);
-            } else {
-                tma_reduce_add<R>(&out_map, c, src);
-            }
+            for_boxes(g, [&](uint32_t j, const int32_t* c) {
+                if constexpr (KIND == KIND_ROUNDTRIP) {
+                    tma_store<R>(&out_map, c, src + j * a.box_bytes);
+                } else {
+                    tma_reduce_add<R>(&out_map, c, src + j * a.box_bytes);
+                }
+            });
         }
         bulk_commit();
     };
 
     uint64_t issued = 0;
     while (issued < n_local && issued < S) issue(issued++);
+    // Stage refilled after writing group i: the one group i - 1 used (its write may still be
+    // reading), or with a single stage the one just written.
+    const uint64_t lag = S > 1 ? 1 : 0;
 
     for (uint64_t i = 0; i < n_local; i++) {
         const uint32_t s = (uint32_t)(i % S);
@@ -88,7 +128,7 @@ __global__ void __launch_bounds__(32, 1)
         if (!mbar_wait(smem_u32(&full_bar[s]), parity, a.timeout_ns)) {
             const uint32_t kid = KIND == KIND_COPY ? K_COPY : KIND == KIND_ROUNDTRIP ? K_ROUNDTRIP
                                                                                     : K_REDUCE;
-            record_timeout(a.status, kid, s, parity, box_of(i));
+            record_timeout(a.status, kid, s, parity, group_of(i) * G);
             // Let every load still in flight land (bounded) before the stages go away.
             for (uint64_t j = i + 1; j < issued; j++) {
                 mbar_wait(smem_u32(&full_bar[j % S]), (uint32_t)((j / S) & 1), a.timeout_ns);
@@ -96,8 +136,12 @@ __global__ void __launch_bounds__(32, 1)
             break;
         }
         write_out(i);
-        if (i >= 1 && issued < n_local) {
-            bulk_wait_read<1>();  // box i - 1's write has read its stage
+        if (i >= lag && issued < n_local) {
+            if (lag) {
+                bulk_wait_read<1>();  // group i - 1's write has read its stage
+            } else {
+                bulk_wait_read<0>();  // the only stage: group i's write has read it
+            }
             issue(issued++);
         }
     }

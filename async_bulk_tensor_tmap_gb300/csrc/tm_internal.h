@@ -48,9 +48,9 @@ struct StreamArgs {
     BoxWalk walk;
     uint64_t images;       // copy: destination images; round trip: source images
     uint32_t box_bytes;
-    uint32_t stage_bytes;  // box_bytes rounded up to kStageAlign
+    uint32_t stage_bytes;  // group * box_bytes rounded up to kStageAlign
     uint32_t stages;
-    uint32_t pad;
+    uint32_t group;        // consecutive boxes per stage (1, or more when box_bytes % 1024 == 0)
     uint64_t timeout_ns;
     StatusBlock* status;
 };
@@ -70,9 +70,14 @@ struct FbArgs {
     uint32_t box_bytes;
     uint32_t stage_bytes;
     uint32_t rows;         // image rows = box_bytes / inner_bytes
+    uint32_t table_rows;   // rows whose offsets are tabulated in shared memory (0 or rows)
+    uint32_t stages;       // 1 or 2 image stages per CTA
     uint64_t timeout_ns;
     StatusBlock* status;
 };
+
+// Rows up to this count get a per-box table of row offsets in the fallback kernels' shared memory.
+constexpr uint32_t kFbTableRows = 4096;
 
 // Ring consumer (stream_tiles).
 struct RingArgs {
@@ -82,6 +87,8 @@ struct RingArgs {
     uint32_t stages;
     uint32_t tile_bytes;     // R * 128
     uint32_t swizzled;       // 1 = 128B, 0 = none
+    uint32_t prefetch;       // tiles ahead of the ring prefetched into L2 (0 = none)
+    uint32_t pad;
     float* cs_a;
     float* cs_b;
     unsigned long long* bits_a;

@@ -166,6 +166,7 @@ extern "C" int tiled_copy_noalloc(const tm_desc* src, const int32_t* coords, siz
         a.images = (uint64_t)images;
         a.box_bytes = (uint32_t)src->box_bytes;
         a.stage_bytes = stage;
+        a.group = 1;
         a.stages = (uint32_t)std::max<size_t>(1, std::min<size_t>(b / stage, TM_MAX_STAGES));
         a.timeout_ns = limit_ns();
         a.status = status;
@@ -174,10 +175,12 @@ extern "C" int tiled_copy_noalloc(const tm_desc* src, const int32_t* coords, siz
         e = launch_tma_stream(KIND_COPY, src->rank, m, m, a, grid,
                               (size_t)a.stages * stage + kStageAlign, st);
     } else {
+        const uint32_t fb_stages = budget(*d, 1) >= 2ull * stage ? 2u : 1u;
         uint32_t per_sm = 4;
-        while (per_sm > 1 && budget(*d, per_sm) < 2ull * stage) per_sm--;
+        while (per_sm > 1 && budget(*d, per_sm) < (size_t)fb_stages * stage) per_sm--;
         FbArgs a;
         memset(&a, 0, sizeof(a));
+        a.stages = fb_stages;
         a.walk = w;
         a.base = src->base;
         for (int i = 0; i < 5; i++) {
@@ -195,7 +198,7 @@ extern "C" int tiled_copy_noalloc(const tm_desc* src, const int32_t* coords, siz
         a.timeout_ns = limit_ns();
         a.status = status;
         const uint32_t grid = (uint32_t)std::min<uint64_t>(n, (uint64_t)d->sms * per_sm);
-        e = launch_fb_copy(a, grid, 2ull * stage + kStageAlign, st);
+        e = launch_fb_copy(a, grid, (size_t)fb_stages * stage + kStageAlign, st);
     }
     if (e != cudaSuccess) return cuda_err(e, "copy launch");
     // The status word is read back before returning, so the call completes the copy.

@@ -214,6 +214,13 @@ __device__ __forceinline__ void tma_reduce_add(const CUtensorMap* m, const int32
     }
 }
 
+// L2 prefetch of a 2-D box (no shared memory, no completion tracking).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int32_t c0, int32_t c1)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 ::"l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1) : "memory");
+}
+
 // ---- untiled bulk copies (contiguous bytes; both addresses 16-byte aligned, size % 16 == 0) ---
 __device__ __forceinline__ void bulk_load(uint32_t dst, uint64_t src, uint32_t bytes, uint32_t bar)
 {
@@ -260,6 +267,34 @@ __device__ __forceinline__ uint32_t swizzle_offset(uint32_t off, uint32_t span)
 }
 
 // ---- box addressing ------------------------------------------------------------------------
+// Grid box index -> per-dim box counters k[i] (dim 0 fastest).
+__device__ __forceinline__ void grid_counters(const BoxWalk& w, uint64_t b, uint32_t* k)
+{
+#pragma unroll
+    for (int i = 0; i < 5; i++) {
+        if (i < (int)w.rank) {
+            const uint64_t nb = w.grid_nb[i];
+            const uint64_t q = b / nb;
+            k[i] = (uint32_t)(b - q * nb);
+            b = q;
+        } else {
+            k[i] = 0;
+        }
+    }
+}
+
+// The next grid box (odometer step of the counters).
+__device__ __forceinline__ void grid_next(const BoxWalk& w, uint32_t* k)
+{
+#pragma unroll
+    for (int i = 0; i < 5; i++) {
+        if (i < (int)w.rank) {
+            if (++k[i] < w.grid_nb[i]) return;
+            k[i] = 0;
+        }
+    }
+}
+
 // Start coordinates of the launch's box `b` (grid: k[i] * box[i] with dim 0 fastest).
 __device__ __forceinline__ void box_start(const BoxWalk& w, uint64_t b, int32_t* c)
 {

@@ -163,13 +163,22 @@ struct Geometry {
     size_t smem;
 };
 
+// Boxes per stage of the TMA streaming kernels: small boxes whose images keep their swizzle phase
+// when packed (size a multiple of 1024 bytes) share a stage of about TM_GROUP_BYTES (32 KiB).
+uint32_t tma_group(uint64_t box_bytes)
+{
+    if (box_bytes % 1024 != 0) return 1;
+    const uint64_t target = std::max<uint64_t>(env_u64("TM_GROUP_BYTES", 32768), 1024);
+    return (uint32_t)std::min<uint64_t>(std::max<uint64_t>(target / box_bytes, 1), 16);
+}
+
 // The TMA streaming kernels: `per_sm` one-warp CTAs per SM (TM_CTAS_PER_SM, default 2), each with
-// as many stages as fit (TM_STAGES caps it).
+// as many stages as fit (TM_STAGES caps it); `nbox` counts work units (box groups).
 Geometry tma_geometry(const DevState& ds, uint64_t nbox, uint32_t stage_bytes)
 {
     uint32_t per_sm = (uint32_t)std::min<uint64_t>(std::max<uint64_t>(env_u64("TM_CTAS_PER_SM", 2), 1), 16);
     size_t budget = cta_budget(ds, per_sm);
-    while (per_sm > 1 && budget < stage_bytes) budget = cta_budget(ds, --per_sm);
+    while (per_sm > 1 && budget < 2ull * stage_bytes) budget = cta_budget(ds, --per_sm);
     uint32_t stages = (uint32_t)std::min<size_t>(budget / stage_bytes, TM_MAX_STAGES);
     const uint64_t cap = env_u64("TM_STAGES", 0);
     if (cap > 0) stages = (uint32_t)std::min<uint64_t>(stages, cap);
@@ -182,15 +191,21 @@ Geometry tma_geometry(const DevState& ds, uint64_t nbox, uint32_t stage_bytes)
     return g;
 }
 
-// The fallback kernels: two stages per CTA, as many CTAs per SM as fit (at most 4).
-Geometry fb_geometry(const DevState& ds, uint64_t nbox, uint32_t stage_bytes)
+// The fallback kernels: TM_FB_STAGES (default 2) image stages per CTA plus the per-box row table,
+// as many CTAs per SM as fit (at most 4); one stage, then no table, when a box is too big.
+// Sets a.stages and a.table_rows.
+Geometry fb_geometry(const DevState& ds, uint64_t nbox, FbArgs& a)
 {
+    a.stages = env_u64("TM_FB_STAGES", 2) == 1 ? 1u : 2u;
+    auto need = [&]() { return (size_t)a.stages * a.stage_bytes + 8ull * a.table_rows; };
+    if (need() > cta_budget(ds, 1)) a.stages = 1;
+    if (need() > cta_budget(ds, 1)) a.table_rows = 0;
     uint32_t per_sm = 4;
-    while (per_sm > 1 && cta_budget(ds, per_sm) < 2ull * stage_bytes) per_sm--;
+    while (per_sm > 1 && cta_budget(ds, per_sm) < need()) per_sm--;
     Geometry g;
     g.grid = (uint32_t)std::min<uint64_t>(nbox, (uint64_t)ds.sms * per_sm);
-    g.stages = 2;
-    g.smem = 2ull * stage_bytes + kStageAlign;
+    g.stages = a.stages;
+    g.smem = need() + kStageAlign;
     return g;
 }
 
@@ -282,21 +297,25 @@ FbArgs fb_args(const tm_desc* d, const BoxWalk& w, uint64_t images, const DevSta
     a.box_bytes = (uint32_t)d->box_bytes;
     a.stage_bytes = stage_bytes_of(d->box_bytes);
     a.rows = (uint32_t)(d->box_bytes / a.inner_bytes);
+    a.table_rows = a.rows <= kFbTableRows ? a.rows : 0;
     a.timeout_ns = wait_limit_ns();
     a.status = ds.status;
     return a;
 }
 
-StreamArgs stream_args(const tm_desc* d, const BoxWalk& w, uint64_t images, uint32_t stages,
-                       const DevState& ds)
+// Arguments and launch geometry of a TMA streaming kernel over the walk's boxes.
+StreamArgs stream_args(const tm_desc* d, const BoxWalk& w, uint64_t images, const DevState& ds,
+                       Geometry& g)
 {
     StreamArgs a;
     memset(&a, 0, sizeof(a));
     a.walk = w;
     a.images = images;
     a.box_bytes = (uint32_t)d->box_bytes;
-    a.stage_bytes = stage_bytes_of(d->box_bytes);
-    a.stages = stages;
+    a.group = tma_group(d->box_bytes);
+    a.stage_bytes = stage_bytes_of((uint64_t)a.group * d->box_bytes);
+    g = tma_geometry(ds, (w.nbox + a.group - 1) / a.group, a.stage_bytes);
+    a.stages = g.stages;
     a.timeout_ns = wait_limit_ns();
     a.status = ds.status;
     return a;
@@ -326,15 +345,15 @@ int copy_boxes(const tm_desc* src, const int32_t* coords, size_t nbox, void* ima
     BoxWalk w;
     if ((rc = make_walk(src, coords, n, st, w))) return rc;
     if (tma) {
-        const Geometry g = tma_geometry(*ds, n, stage_bytes_of(src->box_bytes));
-        const StreamArgs a = stream_args(src, w, (uint64_t)images, g.stages, *ds);
+        Geometry g;
+        const StreamArgs a = stream_args(src, w, (uint64_t)images, *ds, g);
         const CUtensorMap* m = (const CUtensorMap*)src->tmap;
         rc = check_launch(launch_tma_stream(KIND_COPY, src->rank, m, m, a, g.grid, g.smem, st),
                           "tensor copy launch");
     } else {
-        const Geometry g = fb_geometry(*ds, n, stage_bytes_of(src->box_bytes));
-        rc = check_launch(launch_fb_copy(fb_args(src, w, (uint64_t)images, *ds), g.grid, g.smem, st),
-                          "fallback copy launch");
+        FbArgs a = fb_args(src, w, (uint64_t)images, *ds);
+        const Geometry g = fb_geometry(*ds, n, a);
+        rc = check_launch(launch_fb_copy(a, g.grid, g.smem, st), "fallback copy launch");
     }
     release_walk(w, st);
     return rc;
@@ -542,15 +561,15 @@ int tiled_roundtrip(const tm_desc* dst, const int32_t* coords, size_t nbox, cons
     BoxWalk w;
     if ((rc = make_walk(dst, coords, n, st, w))) return rc;
     if (tma) {
-        const Geometry g = tma_geometry(*ds, n, stage_bytes_of(dst->box_bytes));
-        const StreamArgs a = stream_args(dst, w, (uint64_t)images, g.stages, *ds);
+        Geometry g;
+        const StreamArgs a = stream_args(dst, w, (uint64_t)images, *ds, g);
         const CUtensorMap* m = (const CUtensorMap*)dst->tmap;
         rc = check_launch(launch_tma_stream(KIND_ROUNDTRIP, dst->rank, m, m, a, g.grid, g.smem, st),
                           "tensor store launch");
     } else {
-        const Geometry g = fb_geometry(*ds, n, stage_bytes_of(dst->box_bytes));
-        rc = check_launch(launch_fb_store(fb_args(dst, w, (uint64_t)images, *ds), g.grid, g.smem, st),
-                          "fallback store launch");
+        FbArgs a = fb_args(dst, w, (uint64_t)images, *ds);
+        const Geometry g = fb_geometry(*ds, n, a);
+        rc = check_launch(launch_fb_store(a, g.grid, g.smem, st), "fallback store launch");
     }
     release_walk(w, st);
     return rc;
@@ -575,8 +594,8 @@ int tile_reduce_add(const tm_desc* dst, const tm_desc* src, void* stream)
     if ((rc = make_walk(dst, nullptr, 0, st, w))) return rc;
     const uint64_t n = dst->num_boxes;
     if (store_fits_tma(dst) && src->path == TM_PATH_TMA) {
-        const Geometry g = tma_geometry(*ds, n, stage_bytes_of(dst->box_bytes));
-        const StreamArgs a = stream_args(dst, w, 0, g.stages, *ds);
+        Geometry g;
+        const StreamArgs a = stream_args(dst, w, 0, *ds, g);
         rc = check_launch(launch_tma_stream(KIND_REDUCE, dst->rank, (const CUtensorMap*)src->tmap,
                                             (const CUtensorMap*)dst->tmap, a, g.grid, g.smem, st),
                           "tensor reduce launch");
@@ -627,6 +646,7 @@ int stream_tiles(const tm_desc* a, const tm_desc* b, uint32_t stages, float* cs_
     r.stages = stages;
     r.tile_bytes = (uint32_t)a->box_bytes;
     r.swizzled = a->swizzle == TM_SWIZZLE_128B ? 1u : 0u;
+    r.prefetch = (uint32_t)std::min<uint64_t>(env_u64("TM_RING_PREFETCH", 0), 64);
     r.cs_a = cs_a;
     r.cs_b = cs_b;
     r.bits_a = (unsigned long long*)bits_a;

@@ -57,8 +57,10 @@ def parse():
     p.add_argument("--e2e-steps", type=int, default=3)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--ops", default="", help="comma list of op names to run (default: all)")
-    p.add_argument("--scale", type=int, default=1,
-                   help="divide every workload's row count by this (small cases for profiling)")
+    p.add_argument("--scale", type=float, default=1.0,
+                   help="divide every workload's row count by this (small cases for profiling, "
+                        "below 1 for larger ones)")
+    p.add_argument("--ring-stages", type=int, default=4, help="stages of the W5b ring")
     p.add_argument("--ring-swizzle", default="128", choices=["128", "none"],
                    help="swizzle of the ring's tiles (none = the bank-conflict control)")
     return p.parse_args()
@@ -73,10 +75,11 @@ def dist_env():
 # Workload: host arrays (numpy, the bytes both the GPU and the oracle see) and maps
 # ------------------------------------------------------------------------------------------------
 class HostWorkload:
-    def __init__(self, scale: int = 1, ops=None, ring_span: int = 128):
+    def __init__(self, scale: float = 1.0, ops=None, ring_span: int = 128):
         t0 = time.time()
         need = lambda prefix: ops is None or any(o.startswith(prefix) for o in ops)
-        r3, r4, r5a, m5b = 8192 // scale, 4095 // scale, 16384 // scale, 8192 // scale
+        r3, r4, r5a, m5b = (int(8192 / scale), int(4095 / scale), int(16384 / scale),
+                            int(8192 / scale))
         self.w3 = workloads.w3_tensor(r3, 8192) if need("w3") else None
         self.w4 = workloads.w4_tensor(rows=r4) if need("w4") else None
         self.w5a_dst, self.w5a_src = workloads.w5a_tensors(r5a) if need("w5a") else (None, None)
@@ -129,11 +132,12 @@ def op_table(h: HostWorkload):
 # GPU arm
 # ------------------------------------------------------------------------------------------------
 class GpuWorkload:
-    def __init__(self, h: HostWorkload, stream):
+    def __init__(self, h: HostWorkload, stream, ring_stages: int = 4):
         import torch
 
         import async_bulk_tensor_tmap_gb300 as tm
         self.tm, self.torch, self.stream = tm, torch, stream
+        self.ring_stages = ring_stages
         dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).reshape(-1).view(np.uint8)).cuda()
         self.t = {k: dev(getattr(h, k)) for k in ("w3", "w4", "w5a_dst", "w5a_src", "w5b_a",
                                                   "w5b_b") if getattr(h, k) is not None}
@@ -182,8 +186,8 @@ class GpuWorkload:
         elif kind == "reduce":
             tm.tile_reduce_add(m["w5a_dst"], m["w5a_src"], s)
         elif kind == "ring":
-            tm.stream_tiles(m["w5b_a"], m["w5b_b"], 4, t["cs_a"], t["cs_b"], t["bits_a"],
-                            t["bits_b"], s)
+            tm.stream_tiles(m["w5b_a"], m["w5b_b"], self.ring_stages, t["cs_a"], t["cs_b"],
+                            t["bits_a"], t["bits_b"], s)
 
     def flush_l2(self):
         with self.torch.cuda.stream(self.stream):
@@ -480,7 +484,7 @@ def main():
                      0 if args.ring_swizzle == "none" else 128)
     ops = select_ops(h, args.ops)
     stream = torch.cuda.Stream()
-    g = GpuWorkload(h, stream)
+    g = GpuWorkload(h, stream, args.ring_stages)
 
     def barrier():
         torch.cuda.synchronize()

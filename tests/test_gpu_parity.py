@@ -342,6 +342,41 @@ def test_reduce_add_ragged_row_end(tm):
     np.testing.assert_array_equal(to_host(dd).view(np.uint32), hd.reshape(-1).view(np.uint32))
 
 
+@pytest.mark.parametrize("force_fallback", [False, True])
+def test_big_boxes_single_stage(tm, force_fallback):
+    """128 KiB boxes: one stage per CTA on the tensor-map path, one image stage on the vector path."""
+    x = workloads.normal_bf16((9, 300, 64), 21)
+    r = dict(dims=[64, 300, 9], strides=[128, 300 * 128], box=[64, 256, 4], span=128, esize=2)
+    xd = to_dev(x)
+    m = dev_map(tm, xd, r)
+    if force_fallback:
+        tm.tmap_force_fallback(m)
+    assert (m.num_boxes, m.box_bytes) == (6, 131072)
+    imgs = empty_images(m.num_boxes, m.box_bytes)
+    tm.tiled_copy(m, None, imgs)
+    check(tm)
+    want = oracle.tiled_copy(host_map(x, r))
+    np.testing.assert_array_equal(to_host(imgs), want)
+    dst = torch.full_like(xd, 0x66)
+    md = dev_map(tm, dst, r)
+    if force_fallback:
+        tm.tmap_force_fallback(md)
+    tm.tiled_roundtrip(md, None, imgs)
+    check(tm)
+    assert torch.equal(dst, xd)
+    d, s = workloads.w5a_tensors(rows=520, cols=32, seed_dst=13, seed_src=14)
+    rr = dict(dims=[32, 520], strides=[128], box=[32, 256], span=128, esize=4)
+    dd, sd = to_dev(d), to_dev(s)
+    mdd = dev_map(tm, dd, rr)
+    if force_fallback:
+        tm.tmap_force_fallback(mdd)
+    tm.tile_reduce_add(mdd, dev_map(tm, sd, rr))
+    check(tm)
+    hd = d.copy()
+    oracle.tile_reduce_add(host_map(hd, rr), host_map(s, rr))
+    np.testing.assert_array_equal(to_host(dd).view(np.uint32), hd.reshape(-1).view(np.uint32))
+
+
 # ---- bounded waits: a wait that nothing completes gives up and reports, the GPU stays usable -----
 def test_wait_timeout_is_reported_and_recoverable(tm):
     tm.tm_selftest_wait_timeout(50_000_000)
