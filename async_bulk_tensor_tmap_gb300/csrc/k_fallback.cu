@@ -2,16 +2,21 @@
 // that is a multiple of the element size but not of 16 bytes, e.g. a 200-byte group stride), and
 // for explicit box lists the hardware must not be given (see tmap_host.cpp).
 //
-// The image is built exactly as the TMA path builds it -- same swizzle, zero fill outside the
-// tensor -- but by the CTA's threads: each thread owns one 16-byte chunk of an image row, loads
-// the aligned 16-byte window under the chunk's first byte, takes the following window from its
-// neighbour lane with a warp shuffle (loading it itself only where the neighbour does not hold
-// it: the row's last chunk, the warp's last lane), realigns the 32 bytes with funnel shifts and
-// stores the chunk to its swizzled place with a 16-byte shared store ([H200-TMA] = coolgpu "H200 · TMA · Tensor Memory Accelerator" card, §02:
-// the per-thread cp.async style of addressing that TMA replaces).  A proxy fence then hands the
-// image to the same 1-D bulk store the TMA path uses.
+// Both directions produce exactly the bytes of the tensor-map path -- same swizzle, zero fill
+// outside the tensor, only in-bounds elements written -- with threads doing the addressing the
+// engine would do ([H200-TMA] = coolgpu "H200 · TMA · Tensor Memory Accelerator" card, §02: the
+// per-thread cp.async / LDGSTS style of copy that TMA replaces):
 //
-// A window is only loaded when it holds at least one in-bounds byte of the chunk; an aligned
+//   copy   16-byte cp.async copies of the aligned windows under each image row into shared
+//          memory, then a realign of each 16-byte chunk from two staged windows, then one
+//          16-byte global store of the chunk at its swizzled place in the image.  (A first
+//          design realigned in registers with warp shuffles; it was instruction-bound on GB300 at
+//          about 1.9 TB/s, and most of its time stayed even with its global loads removed.)
+//   store  the image is bulk-loaded into shared memory, then each thread writes its chunks'
+//          in-bounds bytes with the widest stores the destination alignment allows.
+//   reduce element-wise fp32 adds straight from global memory.
+//
+// A window is only loaded when it holds at least one in-bounds byte of the row; an aligned
 // 16-byte window never crosses a page, so no load can touch an unmapped address.
 #include "tm_ptx.cuh"
 
@@ -82,7 +87,6 @@ __device__ __forceinline__ void chunk_range(int64_t x0, uint32_t j, uint32_t epc
 }  // namespace
 
 constexpr int64_t kRowOutside = INT64_MIN;  // table entry of a row outside the tensor
-constexpr int kBatch = 4;                    // chunks per thread whose loads are in flight together
 
 // Per-box table of image-row offsets (relative to the tensor base; kRowOutside when an outer
 // coordinate is outside the tensor), shared by every chunk of the row.
@@ -111,124 +115,118 @@ __device__ __forceinline__ void split_item(uint32_t item, uint32_t cpr, uint32_t
     j = item - row * cpr;
 }
 
+// ---- load direction: staged copy ------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(uint32_t dst, uint64_t src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Image of each box, rows taken in blocks of a.block_rows.  Per block: the row offsets go to a
+// shared table; every thread issues 16-byte cp.async copies of the aligned windows under its
+// share of the rows (only windows holding an in-bounds byte), so a whole block of loads is in
+// flight without occupying registers; after one wait each thread realigns its 16-byte chunks from
+// the staged windows (two aligned shared loads and a word select), zeroes out-of-bounds elements,
+// and stores the chunk to its swizzled place in the global image with one 16-byte store (the
+// swizzle only permutes chunks inside a 128-byte row, so a warp's stores stay coalesced).
 __global__ void __launch_bounds__(kThreads) k_fb_copy(const __grid_constant__ FbArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + (kStageAlign - 1)) & ~(kStageAlign - 1);
-    uint8_t* const stage0 = smem_raw + (base - raw);
-    const uint32_t SB = a.stages;
-    int64_t* const tab = reinterpret_cast<int64_t*>(stage0 + SB * a.stage_bytes);
+    const uint32_t cpr = a.inner_bytes >> 4;      // 16-byte chunks per row
+    const uint32_t cpr_shift = (cpr & (cpr - 1)) == 0 ? (uint32_t)(__ffs(cpr) - 1) : 32u;
+    const uint32_t wpr = cpr + 1;                 // staged windows per row
+    const uint32_t RB = a.block_rows;
+    uint8_t* const stg = smem_raw;
+    const uint32_t stg_u32 = smem_u32(stg);
+    int64_t* const tab = reinterpret_cast<int64_t*>(smem_raw + (size_t)RB * wpr * 16);
 
     const uint64_t first = blockIdx.x;
     if (a.walk.nbox <= first) return;
     const uint64_t n_local = (a.walk.nbox - 1 - first) / gridDim.x + 1;
-
-    const uint32_t lane = threadIdx.x & 31;
-    const uint32_t warp = threadIdx.x >> 5;
-    const uint32_t cpr = a.inner_bytes >> 4;  // 16-byte chunks per row
-    const uint32_t cpr_shift = (cpr & (cpr - 1)) == 0 ? (uint32_t)(__ffs(cpr) - 1) : 32u;
-    const uint32_t nchunks = a.rows * cpr;
-    const uint32_t es = a.esize;
-    const uint32_t epc = 16 / es;             // elements per chunk
     const int64_t gbase = (int64_t)a.base;
+    const int64_t box0 = a.walk.box[0];
+    const int64_t dim0 = (int64_t)a.dim[0];
+    const int es = (int)a.esize;
+    const int inner = (int)a.inner_bytes;
 
     for (uint64_t i = 0; i < n_local; i++) {
         const uint64_t b = first + i * gridDim.x;
-        const uint32_t st = (uint32_t)(i % SB);
-        uint8_t* const stage = stage0 + st * a.stage_bytes;
         int32_t c[5];
         box_start(a.walk, b, c);
-        if (threadIdx.x == 0) {  // the write that last used this stage has read it
-            if (SB == 2 && i >= 2) bulk_wait_read<1>();
-            if (SB == 1 && i >= 1) bulk_wait_read<0>();
-        }
-        __syncthreads();  // also: every thread is done with the previous box's row table
-        fill_row_table(a, c, tab, a.stride);
-        __syncthreads();
+        // In-bounds bytes of every image row of this box (the same for all rows).
+        const int64_t e_lo = min(max(-(int64_t)c[0], (int64_t)0), box0);
+        const int64_t e_hi = min(max(dim0 - (int64_t)c[0], (int64_t)0), box0);
+        const int lo_byte = (int)e_lo * es, hi_byte = (int)e_hi * es;
+        const bool whole_x = lo_byte == 0 && hi_byte == inner;
+        uint8_t* const img = reinterpret_cast<uint8_t*>(a.images + b * a.box_bytes);
 
-        // Each warp takes 32 consecutive chunks per slot, kBatch slots per pass (trip count is
-        // warp-uniform); all of a pass's loads are issued before any is used.  Per slot the thread
-        // keeps its first window, the second window when no neighbour lane will hold it (the row's
-        // last chunk, the warp's last lane, or a neighbour whose chunk is outside the tensor), and
-        // one packed word: bits 0..3 d (misalignment), 4 need_lo, 5 need_hi, 6 valid, 7 own hi,
-        // 8..14 j, 15.. row.
-        for (uint32_t it = warp * 32; it < nchunks; it += kThreads * kBatch) {
-            uint4 lo[kBatch], own[kBatch];
-            uint32_t meta[kBatch];
-#pragma unroll
-            for (int k = 0; k < kBatch; k++) {
-                const uint32_t item = it + k * kThreads + lane;
-                const bool valid = item < nchunks;
-                uint32_t row = 0, j = 0;
-                if (valid) split_item(item, cpr, cpr_shift, row, j);
-                const int64_t off = valid ? row_offset(a, c, tab, row, a.stride) : kRowOutside;
-                int k0 = 0, k1 = 0;
-                chunk_range(c[0], j, epc, a.dim[0], k0, k1);
-                const bool any = off != kRowOutside && k0 < k1;
-                const int64_t addr = gbase + (any ? off : 0) + (int64_t)j * 16;
-                const uint32_t d = (uint32_t)addr & 15u;
-                const bool need_lo = any && k0 * (int)es < 16 - (int)d;
-                const bool need_hi = any && d != 0 && k1 * (int)es > 16 - (int)d;
-                // The neighbour (same row, next chunk) loads the second window exactly when its
-                // first element is inside the tensor.
-                const int64_t next_x = (int64_t)c[0] + (int64_t)(j + 1) * epc;
-                const bool nb_loads = lane < 31 && j + 1 < cpr && next_x >= 0 &&
-                                      next_x < (int64_t)a.dim[0];
-                const bool own_hi = need_hi && !nb_loads;
-                meta[k] = d | (need_lo ? 1u << 4 : 0u) | (need_hi ? 1u << 5 : 0u) |
-                          (valid ? 1u << 6 : 0u) | (own_hi ? 1u << 7 : 0u) | (j << 8) | (row << 15);
-                const uint4* w0 = reinterpret_cast<const uint4*>(addr - (int64_t)d);
-                lo[k] = need_lo ? __ldg(w0) : make_uint4(0, 0, 0, 0);
-                own[k] = own_hi ? __ldg(w0 + 1) : make_uint4(0, 0, 0, 0);
+        for (uint32_t r0 = 0; r0 < a.rows; r0 += RB) {
+            const uint32_t nr = min(RB, a.rows - r0);
+            __syncthreads();  // the previous block's windows and table are no longer read
+            for (uint32_t r = threadIdx.x; r < nr; r += kThreads) {
+                const RowPos p = row_position(a, c, r0 + r, a.stride);
+                tab[r] = (p.ok && lo_byte < hi_byte) ? p.off : kRowOutside;
             }
-#pragma unroll
-            for (int k = 0; k < kBatch; k++) {
-                const uint32_t d = meta[k] & 15u;
-                const bool need_lo = (meta[k] >> 4) & 1u, need_hi = (meta[k] >> 5) & 1u;
-                const bool valid = (meta[k] >> 6) & 1u, own_hi = (meta[k] >> 7) & 1u;
-                const uint32_t j = (meta[k] >> 8) & 127u, row = meta[k] >> 15;
-                uint4 nb;
-                nb.x = __shfl_down_sync(0xffffffffu, lo[k].x, 1);
-                nb.y = __shfl_down_sync(0xffffffffu, lo[k].y, 1);
-                nb.z = __shfl_down_sync(0xffffffffu, lo[k].z, 1);
-                nb.w = __shfl_down_sync(0xffffffffu, lo[k].w, 1);
-                if (!valid) continue;
-                const uint4 hi = !need_hi ? make_uint4(0, 0, 0, 0) : own_hi ? own[k] : nb;
+            __syncthreads();
+            const uint32_t nwin = nr * wpr;
+            for (uint32_t w = threadIdx.x; w < nwin; w += kThreads) {
+                const uint32_t r = w / wpr, k = w - r * wpr;
+                const int64_t off = tab[r];
+                if (off == kRowOutside) continue;
+                const int64_t row_addr = gbase + off;
+                const int d = (int)(row_addr & 15);
+                const int wlo = 16 * (int)k - d;  // window k holds row bytes [wlo, wlo + 16)
+                if (wlo + 16 <= lo_byte || wlo >= hi_byte) continue;
+                cp_async16(stg_u32 + w * 16, (uint64_t)(row_addr - d + 16 * (int64_t)k));
+            }
+            cp_async_wait_all();
+            __syncthreads();
+            const uint32_t nch = nr * cpr;
+            for (uint32_t it = threadIdx.x; it < nch; it += kThreads) {
+                uint32_t r, j;
+                split_item(it, cpr, cpr_shift, r, j);
+                const int64_t off = tab[r];
                 uint4 out = make_uint4(0, 0, 0, 0);
-                int k0 = 0, k1 = 0;
-                chunk_range(c[0], j, epc, a.dim[0], k0, k1);
-                const bool whole = k0 == 0 && k1 == (int)epc;
-                if (whole && d == 0) {  // aligned and inside: the window is the chunk
-                    out = lo[k];
-                } else if (whole && d == 8) {  // inside, 8-byte aligned: two words from each window
-                    out = make_uint4(lo[k].z, lo[k].w, hi.x, hi.y);
-                } else if (need_lo || need_hi) {
-                    const int lo_b = k0 * (int)es, hi_b = k1 * (int)es;
-                    const uint32_t q = d >> 2, sh = (d & 3u) * 8u;
-                    const uint32_t w[8] = {lo[k].x, lo[k].y, lo[k].z, lo[k].w,
-                                           hi.x, hi.y, hi.z, hi.w};
-                    uint32_t o[4];
+                if (off != kRowOutside) {
+                    const uint32_t d = (uint32_t)((gbase + off) & 15);
+                    const uint4* src = reinterpret_cast<const uint4*>(stg + (r * wpr + j) * 16);
+                    const uint4 lo = src[0];
+                    if (d == 0) {
+                        out = lo;
+                    } else {
+                        const uint4 hi = src[1];
+                        if (d == 8) {
+                            out = make_uint4(lo.z, lo.w, hi.x, hi.y);
+                        } else {
+                            const uint32_t q = d >> 2, sh = (d & 3u) * 8u;
+                            const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                            uint32_t o[4];
 #pragma unroll
-                    for (int t = 0; t < 4; t++) {
-                        const uint32_t x = sel4(q, w[t], w[t + 1], w[t + 2], w[t + 3]);
-                        const uint32_t y = sel4(q, w[t + 1], w[t + 2], w[t + 3], w[t + 4]);
-                        o[t] = __funnelshift_r(x, y, sh) & word_mask(lo_b, hi_b, t);
+                            for (int t = 0; t < 4; t++) {
+                                const uint32_t x = sel4(q, w[t], w[t + 1], w[t + 2], w[t + 3]);
+                                const uint32_t y = sel4(q, w[t + 1], w[t + 2], w[t + 3], w[t + 4]);
+                                o[t] = __funnelshift_r(x, y, sh);
+                            }
+                            out = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
                     }
-                    out = make_uint4(o[0], o[1], o[2], o[3]);
+                    if (!whole_x) {  // zero the elements outside the tensor along dim 0
+                        const int blo = lo_byte - 16 * (int)j, bhi = hi_byte - 16 * (int)j;
+                        out.x &= word_mask(blo, bhi, 0);
+                        out.y &= word_mask(blo, bhi, 1);
+                        out.z &= word_mask(blo, bhi, 2);
+                        out.w &= word_mask(blo, bhi, 3);
+                    }
                 }
-                *reinterpret_cast<uint4*>(stage + swizzle_offset(row * a.inner_bytes + j * 16,
-                                                                 a.span)) = out;
+                *reinterpret_cast<uint4*>(
+                    img + swizzle_offset((r0 + r) * a.inner_bytes + j * 16, a.span)) = out;
             }
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            bulk_store(a.images + b * a.box_bytes, base + st * a.stage_bytes, a.box_bytes);
-            bulk_commit();
         }
     }
-    if (threadIdx.x == 0) bulk_wait_all<0>();
 }
 
 // Writes bytes [pos, end) of a 16-byte chunk `v` to `dst` (the chunk's global address) with the

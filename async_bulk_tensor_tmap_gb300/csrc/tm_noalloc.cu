@@ -175,12 +175,8 @@ extern "C" int tiled_copy_noalloc(const tm_desc* src, const int32_t* coords, siz
         e = launch_tma_stream(KIND_COPY, src->rank, m, m, a, grid,
                               (size_t)a.stages * stage + kStageAlign, st);
     } else {
-        const uint32_t fb_stages = budget(*d, 1) >= 2ull * stage ? 2u : 1u;
-        uint32_t per_sm = 4;
-        while (per_sm > 1 && budget(*d, per_sm) < (size_t)fb_stages * stage) per_sm--;
         FbArgs a;
         memset(&a, 0, sizeof(a));
-        a.stages = fb_stages;
         a.walk = w;
         a.base = src->base;
         for (int i = 0; i < 5; i++) {
@@ -197,8 +193,11 @@ extern "C" int tiled_copy_noalloc(const tm_desc* src, const int32_t* coords, siz
         a.rows = (uint32_t)(src->box_bytes / a.inner_bytes);
         a.timeout_ns = limit_ns();
         a.status = status;
-        const uint32_t grid = (uint32_t)std::min<uint64_t>(n, (uint64_t)d->sms * per_sm);
-        e = launch_fb_copy(a, grid, (size_t)fb_stages * stage + kStageAlign, st);
+        uint32_t grid = 0;
+        size_t smem = 0;
+        fb_copy_shape(a, n, (uint32_t)d->sms, 8u, [&](uint32_t per_sm) { return budget(*d, per_sm); },
+                      grid, smem);
+        e = launch_fb_copy(a, grid, smem, st);
     }
     if (e != cudaSuccess) return cuda_err(e, "copy launch");
     // The status word is read back before returning, so the call completes the copy.

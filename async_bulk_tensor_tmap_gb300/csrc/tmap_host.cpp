@@ -191,16 +191,16 @@ Geometry tma_geometry(const DevState& ds, uint64_t nbox, uint32_t stage_bytes)
     return g;
 }
 
-// The fallback kernels: TM_FB_STAGES (default 2) image stages per CTA plus the per-box row table,
-// as many CTAs per SM as fit (at most 4); one stage, then no table, when a box is too big.
-// Sets a.stages and a.table_rows.
+// The fallback kernels: TM_FB_STAGES (default 1) image stages per CTA plus the per-box row table,
+// as many CTAs per SM as fit up to TM_FB_CTAS_PER_SM (default 6; the copy kernel's registers
+// allow 4); one stage, then no table, when a box is too big.  Sets a.stages and a.table_rows.
 Geometry fb_geometry(const DevState& ds, uint64_t nbox, FbArgs& a)
 {
-    a.stages = env_u64("TM_FB_STAGES", 2) == 1 ? 1u : 2u;
+    a.stages = env_u64("TM_FB_STAGES", 1) == 2 ? 2u : 1u;
     auto need = [&]() { return (size_t)a.stages * a.stage_bytes + 8ull * a.table_rows; };
     if (need() > cta_budget(ds, 1)) a.stages = 1;
     if (need() > cta_budget(ds, 1)) a.table_rows = 0;
-    uint32_t per_sm = 4;
+    uint32_t per_sm = (uint32_t)std::min<uint64_t>(std::max<uint64_t>(env_u64("TM_FB_CTAS_PER_SM", 6), 1), 16);
     while (per_sm > 1 && cta_budget(ds, per_sm) < need()) per_sm--;
     Geometry g;
     g.grid = (uint32_t)std::min<uint64_t>(nbox, (uint64_t)ds.sms * per_sm);
@@ -352,8 +352,12 @@ int copy_boxes(const tm_desc* src, const int32_t* coords, size_t nbox, void* ima
                           "tensor copy launch");
     } else {
         FbArgs a = fb_args(src, w, (uint64_t)images, *ds);
-        const Geometry g = fb_geometry(*ds, n, a);
-        rc = check_launch(launch_fb_copy(a, g.grid, g.smem, st), "fallback copy launch");
+        uint32_t grid = 0;
+        size_t smem = 0;
+        fb_copy_shape(a, n, (uint32_t)ds->sms,
+                      (uint32_t)std::min<uint64_t>(env_u64("TM_FB_COPY_CTAS_PER_SM", 8), 16),
+                      [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); }, grid, smem);
+        rc = check_launch(launch_fb_copy(a, grid, smem, st), "fallback copy launch");
     }
     release_walk(w, st);
     return rc;
