@@ -66,6 +66,23 @@ def parse():
     return p.parse_args()
 
 
+def max_over_ranks(x: float, world: int) -> float:
+    """The largest of every rank's x (the step time is the slowest rank's); the identity at N=1."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(step_bytes: int, step_ms: float, world: int) -> float:
+    """Whole-job GB/s: every rank moves step_bytes per step; the step lasts the slowest rank's time."""
+    return world * step_bytes / (step_ms * 1e-3) / GB
+
+
 def dist_env():
     return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
             int(os.environ.get("LOCAL_RANK", 0)))
@@ -501,13 +518,9 @@ def main():
     rc = g.tm.tm_stream_check(stream)
     if rc != g.tm.TM_OK:
         raise RuntimeError(g.tm.tm_last_error())
-    step_ms = sum(sum(v) for v in per.values()) / args.steps
-    if world > 1:
-        t = torch.tensor([step_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(sum(sum(v) for v in per.values()) / args.steps, world)
     step_bytes = sum(b for _, b in ops)
-    value = world * step_bytes / (step_ms * 1e-3) / GB
+    value = weak_scaling_value(step_bytes, step_ms, world)
     peak, peak_kind = measured_hbm_peak()
     breakdown = {}
     for name, nbytes in ops:
