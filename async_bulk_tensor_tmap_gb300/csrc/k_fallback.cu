@@ -12,7 +12,8 @@
 //          16-byte global store of the chunk at its swizzled place in the image.  (A first
 //          design realigned in registers with warp shuffles; it was instruction-bound on GB300 at
 //          about 1.9 TB/s, and most of its time stayed even with its global loads removed.)
-//   store  the image is bulk-loaded into shared memory, then each thread writes its chunks'
+//   store  each thread reads its 16-byte chunks of the image straight from global memory
+//          (coalesced: a swizzle only permutes chunks inside a 128-byte row) and writes their
 //          in-bounds bytes with the widest stores the destination alignment allows.
 //   reduce element-wise fp32 adds straight from global memory.
 //
@@ -87,25 +88,6 @@ __device__ __forceinline__ void chunk_range(int64_t x0, uint32_t j, uint32_t epc
 }  // namespace
 
 constexpr int64_t kRowOutside = INT64_MIN;  // table entry of a row outside the tensor
-
-// Per-box table of image-row offsets (relative to the tensor base; kRowOutside when an outer
-// coordinate is outside the tensor), shared by every chunk of the row.
-__device__ __forceinline__ void fill_row_table(const FbArgs& a, const int32_t* c, int64_t* tab,
-                                               const int64_t* stride)
-{
-    for (uint32_t r = threadIdx.x; r < a.table_rows; r += kThreads) {
-        const RowPos p = row_position(a, c, r, stride);
-        tab[r] = p.ok ? p.off : kRowOutside;
-    }
-}
-
-__device__ __forceinline__ int64_t row_offset(const FbArgs& a, const int32_t* c, const int64_t* tab,
-                                              uint32_t row, const int64_t* stride)
-{
-    if (a.table_rows) return tab[row];
-    const RowPos p = row_position(a, c, row, stride);
-    return p.ok ? p.off : kRowOutside;
-}
 
 // Image row and chunk of item `item` (chunks of a row are consecutive items).
 __device__ __forceinline__ void split_item(uint32_t item, uint32_t cpr, uint32_t cpr_shift,
@@ -257,90 +239,88 @@ __device__ __forceinline__ void store_chunk_bytes(uint8_t* dst, const uint4& v, 
     }
 }
 
-// Store direction: image b is bulk-loaded into a stage, then each thread writes the in-bounds
-// bytes of its chunks with the widest stores the destination alignment allows.
-__global__ void __launch_bounds__(kThreads) k_fb_store(const __grid_constant__ FbArgs a)
+// Store direction.  Image b is read straight from global memory: a warp's 32 chunks are 4
+// consecutive 128-byte image rows (a swizzle only permutes chunks inside a row), so the 16-byte
+// loads are coalesced; each thread keeps 4 in flight, then writes each chunk's in-bounds bytes
+// with the widest stores the destination alignment allows.  Only the row table lives in shared
+// memory; no wait on another thread's copy is involved.
+__global__ void __launch_bounds__(kThreads, 6) k_fb_store(const __grid_constant__ FbArgs a)
 {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ __align__(8) uint64_t full_bar[2];
-    __shared__ int wait_ok;
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + (kStageAlign - 1)) & ~(kStageAlign - 1);
-    uint8_t* const stage0 = smem_raw + (base - raw);
-    const uint32_t SB = a.stages;
-    int64_t* const tab = reinterpret_cast<int64_t*>(stage0 + SB * a.stage_bytes);
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    int64_t* const tab = reinterpret_cast<int64_t*>(smem_raw);
+    constexpr int kLoads = 4;
 
     const uint64_t first = blockIdx.x;
     if (a.walk.nbox <= first) return;
     const uint64_t n_local = (a.walk.nbox - 1 - first) / gridDim.x + 1;
     const uint32_t cpr = a.inner_bytes >> 4;
     const uint32_t cpr_shift = (cpr & (cpr - 1)) == 0 ? (uint32_t)(__ffs(cpr) - 1) : 32u;
-    const uint32_t nchunks = a.rows * cpr;
-    const uint32_t es = a.esize;
-    const uint32_t epc = 16 / es;
-
-    auto issue = [&](uint64_t i) {
-        const uint32_t st = (uint32_t)(i % SB);
-        const uint32_t bar = smem_u32(&full_bar[st]);
-        mbar_arrive_expect_tx(bar, a.box_bytes);
-        bulk_load(base + st * a.stage_bytes, a.images + (first + i * gridDim.x) * a.box_bytes,
-                  a.box_bytes, bar);
-    };
-
-    if (threadIdx.x == 0) {
-        mbar_init(smem_u32(&full_bar[0]), 1);
-        mbar_init(smem_u32(&full_bar[1]), 1);
-        fence_barrier_init();
-        issue(0);
-        if (SB == 2 && n_local > 1) issue(1);
-    }
+    const uint32_t RB = a.block_rows;
+    const int64_t box0 = a.walk.box[0];
+    const int64_t dim0 = (int64_t)a.dim[0];
+    const int es = (int)a.esize;
+    const int inner = (int)a.inner_bytes;
 
     for (uint64_t i = 0; i < n_local; i++) {
-        const uint32_t st = (uint32_t)(i % SB);
+        const uint64_t b = first + i * gridDim.x;
         int32_t c[5];
-        box_start(a.walk, first + i * gridDim.x, c);
-        fill_row_table(a, c, tab, a.stride);  // the previous box's table is no longer read
-        if (threadIdx.x == 0) {
-            const uint32_t parity = (uint32_t)((i / SB) & 1);
-            const bool ok = mbar_wait(smem_u32(&full_bar[st]), parity, a.timeout_ns);
-            if (!ok) {
-                record_timeout(a.status, K_FB_STORE, st, parity, first + i * gridDim.x);
-                if (SB == 2 && i + 1 < n_local) {  // the other stage's load may still be landing
-                    mbar_wait(smem_u32(&full_bar[st ^ 1]), (uint32_t)(((i + 1) >> 1) & 1),
-                              a.timeout_ns);
-                }
-            }
-            wait_ok = ok ? 1 : 0;
-        }
-        __syncthreads();
-        if (!wait_ok) break;
+        box_start(a.walk, b, c);
+        const int64_t e_lo = min(max(-(int64_t)c[0], (int64_t)0), box0);
+        const int64_t e_hi = min(max(dim0 - (int64_t)c[0], (int64_t)0), box0);
+        const int lo_byte = (int)e_lo * es, hi_byte = (int)e_hi * es;
+        const bool whole_x = lo_byte == 0 && hi_byte == inner;
+        const uint8_t* const img = reinterpret_cast<const uint8_t*>(a.images + b * a.box_bytes);
 
-        const uint8_t* const stage = stage0 + st * a.stage_bytes;
-        for (uint32_t item = threadIdx.x; item < nchunks; item += kThreads) {
-            uint32_t row, j;
-            split_item(item, cpr, cpr_shift, row, j);
-            const int64_t off = row_offset(a, c, tab, row, a.stride);
-            int k0 = 0, k1 = 0;
-            chunk_range(c[0], j, epc, a.dim[0], k0, k1);
-            if (off == kRowOutside || k0 >= k1) continue;
-            const uint4 v = *reinterpret_cast<const uint4*>(
-                stage + swizzle_offset(row * a.inner_bytes + j * 16, a.span));
-            uint8_t* const chunk = reinterpret_cast<uint8_t*>(a.base + off + (int64_t)j * 16);
-            const uintptr_t at = reinterpret_cast<uintptr_t>(chunk);
-            if (k0 == 0 && k1 == (int)epc && (at & 7) == 0) {  // whole chunk, 8-byte aligned
-                if ((at & 15) == 0) {
-                    *reinterpret_cast<uint4*>(chunk) = v;
-                } else {
-                    *reinterpret_cast<uint2*>(chunk) = make_uint2(v.x, v.y);
-                    *reinterpret_cast<uint2*>(chunk + 8) = make_uint2(v.z, v.w);
+        for (uint32_t r0 = 0; r0 < a.rows; r0 += RB) {
+            const uint32_t nr = min(RB, a.rows - r0);
+            __syncthreads();  // the previous block's table is no longer read
+            for (uint32_t r = threadIdx.x; r < nr; r += kThreads) {
+                const RowPos p = row_position(a, c, r0 + r, a.stride);
+                tab[r] = (p.ok && lo_byte < hi_byte) ? p.off : kRowOutside;
+            }
+            __syncthreads();
+            const uint32_t nch = nr * cpr;
+            for (uint32_t it = threadIdx.x; it < nch; it += kThreads * kLoads) {
+                uint4 v[kLoads];
+#pragma unroll
+                for (int k = 0; k < kLoads; k++) {
+                    const uint32_t item = it + k * kThreads;
+                    v[k] = make_uint4(0, 0, 0, 0);
+                    if (item < nch) {
+                        uint32_t r, j;
+                        split_item(item, cpr, cpr_shift, r, j);
+                        if (tab[r] != kRowOutside) {
+                            v[k] = __ldg(reinterpret_cast<const uint4*>(
+                                img + swizzle_offset((r0 + r) * a.inner_bytes + j * 16, a.span)));
+                        }
+                    }
                 }
-            } else {
-                store_chunk_bytes(chunk, v, k0 * (int)es, k1 * (int)es);
+#pragma unroll
+                for (int k = 0; k < kLoads; k++) {
+                    const uint32_t item = it + k * kThreads;
+                    if (item >= nch) continue;
+                    uint32_t r, j;
+                    split_item(item, cpr, cpr_shift, r, j);
+                    const int64_t off = tab[r];
+                    if (off == kRowOutside) continue;
+                    const int pos = whole_x ? 0 : max(lo_byte - 16 * (int)j, 0);
+                    const int end = whole_x ? 16 : min(hi_byte - 16 * (int)j, 16);
+                    if (pos >= end) continue;
+                    uint8_t* const chunk = reinterpret_cast<uint8_t*>(a.base + off + (int64_t)j * 16);
+                    const uintptr_t at = reinterpret_cast<uintptr_t>(chunk);
+                    if (pos == 0 && end == 16 && (at & 7) == 0) {  // whole chunk, 8-byte aligned
+                        if ((at & 15) == 0) {
+                            *reinterpret_cast<uint4*>(chunk) = v[k];
+                        } else {
+                            *reinterpret_cast<uint2*>(chunk) = make_uint2(v[k].x, v[k].y);
+                            *reinterpret_cast<uint2*>(chunk + 8) = make_uint2(v[k].z, v[k].w);
+                        }
+                    } else {
+                        store_chunk_bytes(chunk, v[k], pos, end);
+                    }
+                }
             }
         }
-        fence_proxy_async_smem();  // generic reads of the stage before the next async write to it
-        __syncthreads();
-        if (threadIdx.x == 0 && i + SB < n_local) issue(i + SB);
     }
 }
 

@@ -70,35 +70,30 @@ struct FbArgs {
     uint32_t box_bytes;
     uint32_t stage_bytes;
     uint32_t rows;         // image rows = box_bytes / inner_bytes
-    uint32_t table_rows;   // store: rows whose offsets are tabulated in shared memory (0 or rows)
-    uint32_t stages;       // store: 1 or 2 image stages per CTA
-    uint32_t block_rows;   // copy: image rows staged per block
+    uint32_t block_rows;   // image rows handled per block (shared-memory row table / staging)
     uint32_t pad;
     uint64_t timeout_ns;
     StatusBlock* status;
 };
 
-// Rows up to this count get a per-box table of row offsets in the fallback store's shared memory.
-constexpr uint32_t kFbTableRows = 4096;
-
-// The staged vector copy keeps, per image row, the aligned 16-byte windows under the row (one more
-// than its chunks) and the row's offset.
+// Shared memory per image row: the staged copy keeps the aligned 16-byte windows under the row
+// (one more than its chunks) and the row's offset; the store keeps the offset only.
 inline size_t fb_copy_row_bytes(uint32_t inner_bytes) { return (size_t)(inner_bytes / 16 + 1) * 16 + 8; }
+constexpr size_t kFbStoreRowBytes = 8;
 
-// Launch shape of the staged vector copy: the most CTAs per SM up to `want` (fewer when a block
-// of 32 rows or the whole box would not fit), rows per block, grid and dynamic shared memory.
-// budget(n) is the shared memory one of n CTAs on an SM may use.
+// Launch shape of a vector kernel that handles image rows in blocks: the most CTAs per SM up to
+// `want` (fewer when a block of 32 rows, or the whole box, would not fit), rows per block, grid
+// and dynamic shared memory.  budget(n) is the shared memory one of n CTAs on an SM may use.
 template <class Budget>
-inline void fb_copy_shape(FbArgs& a, uint64_t nbox, uint32_t sms, uint32_t want, Budget budget,
-                          uint32_t& grid, size_t& smem)
+inline void fb_shape(FbArgs& a, uint64_t nbox, uint32_t sms, uint32_t want, size_t row_bytes,
+                     Budget budget, uint32_t& grid, size_t& smem)
 {
-    const size_t rb = fb_copy_row_bytes(a.inner_bytes);
     const uint32_t min_rows = a.rows < 32 ? a.rows : 32;
     uint32_t per_sm = want < 1 ? 1 : want;
-    while (per_sm > 1 && budget(per_sm) / rb < min_rows) per_sm--;
-    const size_t fit = budget(per_sm) / rb;
+    while (per_sm > 1 && budget(per_sm) / row_bytes < min_rows) per_sm--;
+    const size_t fit = budget(per_sm) / row_bytes;
     a.block_rows = (uint32_t)(fit < a.rows ? (fit < 1 ? 1 : fit) : a.rows);
-    smem = (size_t)a.block_rows * rb;
+    smem = (size_t)a.block_rows * row_bytes;
     const uint64_t ctas = (uint64_t)sms * per_sm;
     grid = (uint32_t)(nbox < ctas ? nbox : ctas);
 }
@@ -126,7 +121,6 @@ enum StreamKind : int { KIND_COPY = 0, KIND_ROUNDTRIP = 1, KIND_REDUCE = 2 };
 cudaError_t launch_tma_stream(int kind, uint32_t rank, const CUtensorMap* in_map,
                               const CUtensorMap* out_map, const StreamArgs& a, uint32_t grid,
                               size_t smem, cudaStream_t s);
-size_t tma_stream_kernel_max_smem();
 cudaError_t launch_fb_copy(const FbArgs& a, uint32_t grid, size_t smem, cudaStream_t s);
 cudaError_t launch_fb_store(const FbArgs& a, uint32_t grid, size_t smem, cudaStream_t s);
 cudaError_t launch_fb_reduce(const FbArgs& a, uint32_t grid, cudaStream_t s);

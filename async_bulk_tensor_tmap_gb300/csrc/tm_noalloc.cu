@@ -195,8 +195,8 @@ extern "C" int tiled_copy_noalloc(const tm_desc* src, const int32_t* coords, siz
         a.status = status;
         uint32_t grid = 0;
         size_t smem = 0;
-        fb_copy_shape(a, n, (uint32_t)d->sms, 8u, [&](uint32_t per_sm) { return budget(*d, per_sm); },
-                      grid, smem);
+        fb_shape(a, n, (uint32_t)d->sms, 8u, fb_copy_row_bytes(a.inner_bytes),
+                 [&](uint32_t per_sm) { return budget(*d, per_sm); }, grid, smem);
         e = launch_fb_copy(a, grid, smem, st);
     }
     if (e != cudaSuccess) return cuda_err(e, "copy launch");

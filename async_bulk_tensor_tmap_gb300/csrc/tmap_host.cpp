@@ -191,24 +191,6 @@ Geometry tma_geometry(const DevState& ds, uint64_t nbox, uint32_t stage_bytes)
     return g;
 }
 
-// The fallback kernels: TM_FB_STAGES (default 1) image stages per CTA plus the per-box row table,
-// as many CTAs per SM as fit up to TM_FB_CTAS_PER_SM (default 6; the copy kernel's registers
-// allow 4); one stage, then no table, when a box is too big.  Sets a.stages and a.table_rows.
-Geometry fb_geometry(const DevState& ds, uint64_t nbox, FbArgs& a)
-{
-    a.stages = env_u64("TM_FB_STAGES", 1) == 2 ? 2u : 1u;
-    auto need = [&]() { return (size_t)a.stages * a.stage_bytes + 8ull * a.table_rows; };
-    if (need() > cta_budget(ds, 1)) a.stages = 1;
-    if (need() > cta_budget(ds, 1)) a.table_rows = 0;
-    uint32_t per_sm = (uint32_t)std::min<uint64_t>(std::max<uint64_t>(env_u64("TM_FB_CTAS_PER_SM", 6), 1), 16);
-    while (per_sm > 1 && cta_budget(ds, per_sm) < need()) per_sm--;
-    Geometry g;
-    g.grid = (uint32_t)std::min<uint64_t>(nbox, (uint64_t)ds.sms * per_sm);
-    g.stages = a.stages;
-    g.smem = need() + kStageAlign;
-    return g;
-}
-
 uint32_t stage_bytes_of(uint64_t box_bytes)
 {
     return (uint32_t)((box_bytes + kStageAlign - 1) / kStageAlign * kStageAlign);
@@ -297,7 +279,6 @@ FbArgs fb_args(const tm_desc* d, const BoxWalk& w, uint64_t images, const DevSta
     a.box_bytes = (uint32_t)d->box_bytes;
     a.stage_bytes = stage_bytes_of(d->box_bytes);
     a.rows = (uint32_t)(d->box_bytes / a.inner_bytes);
-    a.table_rows = a.rows <= kFbTableRows ? a.rows : 0;
     a.timeout_ns = wait_limit_ns();
     a.status = ds.status;
     return a;
@@ -354,9 +335,10 @@ int copy_boxes(const tm_desc* src, const int32_t* coords, size_t nbox, void* ima
         FbArgs a = fb_args(src, w, (uint64_t)images, *ds);
         uint32_t grid = 0;
         size_t smem = 0;
-        fb_copy_shape(a, n, (uint32_t)ds->sms,
-                      (uint32_t)std::min<uint64_t>(env_u64("TM_FB_COPY_CTAS_PER_SM", 8), 16),
-                      [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); }, grid, smem);
+        fb_shape(a, n, (uint32_t)ds->sms,
+                 (uint32_t)std::min<uint64_t>(env_u64("TM_FB_COPY_CTAS_PER_SM", 8), 16),
+                 fb_copy_row_bytes(a.inner_bytes),
+                 [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); }, grid, smem);
         rc = check_launch(launch_fb_copy(a, grid, smem, st), "fallback copy launch");
     }
     release_walk(w, st);
@@ -572,8 +554,13 @@ int tiled_roundtrip(const tm_desc* dst, const int32_t* coords, size_t nbox, cons
                           "tensor store launch");
     } else {
         FbArgs a = fb_args(dst, w, (uint64_t)images, *ds);
-        const Geometry g = fb_geometry(*ds, n, a);
-        rc = check_launch(launch_fb_store(a, g.grid, g.smem, st), "fallback store launch");
+        uint32_t grid = 0;
+        size_t smem = 0;
+        fb_shape(a, n, (uint32_t)ds->sms,
+                 (uint32_t)std::min<uint64_t>(env_u64("TM_FB_STORE_CTAS_PER_SM", 6), 16),
+                 kFbStoreRowBytes, [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); }, grid,
+                 smem);
+        rc = check_launch(launch_fb_store(a, grid, smem, st), "fallback store launch");
     }
     release_walk(w, st);
     return rc;
