@@ -155,15 +155,24 @@ __global__ void __launch_bounds__(kThreads) k_fb_copy(const __grid_constant__ Fb
             }
             __syncthreads();
             const uint32_t nwin = nr * wpr;
+            // Window w = r * wpr + k; the (r, k) pair is stepped along instead of divided out.
+            const uint32_t dr = kThreads / wpr, dk = kThreads - dr * wpr;
+            uint32_t r = threadIdx.x / wpr, k = threadIdx.x - r * wpr;
             for (uint32_t w = threadIdx.x; w < nwin; w += kThreads) {
-                const uint32_t r = w / wpr, k = w - r * wpr;
                 const int64_t off = tab[r];
-                if (off == kRowOutside) continue;
-                const int64_t row_addr = gbase + off;
-                const int d = (int)(row_addr & 15);
-                const int wlo = 16 * (int)k - d;  // window k holds row bytes [wlo, wlo + 16)
-                if (wlo + 16 <= lo_byte || wlo >= hi_byte) continue;
-                cp_async16(stg_u32 + w * 16, (uint64_t)(row_addr - d + 16 * (int64_t)k));
+                if (off != kRowOutside) {
+                    const int64_t row_addr = gbase + off;
+                    const int d = (int)(row_addr & 15);
+                    const int wlo = 16 * (int)k - d;  // window k holds row bytes [wlo, wlo + 16)
+                    if (wlo + 16 > lo_byte && wlo < hi_byte)
+                        cp_async16(stg_u32 + w * 16, (uint64_t)(row_addr - d + 16 * (int64_t)k));
+                }
+                r += dr;
+                k += dk;
+                if (k >= wpr) {
+                    k -= wpr;
+                    r++;
+                }
             }
             cp_async_wait_all();
             __syncthreads();

@@ -215,8 +215,7 @@ __global__ void __launch_bounds__(kRingThreads, 1)
                 if (q < n / 2) blk[q] = __fadd_rn(blk[2 * q], blk[2 * q + 1]);
             }
         }
-#pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) bits += __shfl_xor_sync(0xffffffffu, bits, m);
+        bits = __reduce_add_sync(0xffffffffu, bits);  // exact integer sum: order-free
 
         // ... then across the tile's warps, in warp order (slots of iteration i % NS)
         const uint32_t slot = (uint32_t)(i % NS);

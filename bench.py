@@ -193,8 +193,9 @@ class GpuWorkload:
         self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
         self.paths = {k: m.path for k, m in self.maps.items()}
 
-    def run_op(self, name):
-        tm, t, m, s = self.tm, self.t, self.maps, self.stream
+    def run_op(self, name, stream=None):
+        tm, t, m = self.tm, self.t, self.maps
+        s = self.stream if stream is None else stream
         base, kind = name.split(".")
         if kind == "copy":
             tm.tiled_copy(m[base], None, t[f"{base}_img"], s)
@@ -295,53 +296,80 @@ def collect(per, ev):
     return per
 
 
+# End-to-end groups: the ops that share input tensors, the tensors copied in, the results read back.
+E2E_GROUPS = (
+    ("w3", ("w3",), ("w3_out",)),
+    ("w4", ("w4",), ("w4_out",)),
+    ("w5a", ("w5a_dst", "w5a_src"), ("w5a_dst",)),
+    ("w5b", ("w5b_a", "w5b_b"), ("cs_a", "cs_b", "bits_a", "bits_b")),
+)
+
+
 def e2e_run(g: GpuWorkload, h: HostWorkload, ops, steps):
     """Same step through the public API with HOST buffers: every step copies its inputs from
-    pinned host memory and its results back, inside the timed region."""
+    pinned host memory and its results back, inside the timed region.  Three streams pipeline the
+    work group by group (inputs of group k+1 go in while group k computes and group k-1's results
+    come out); events keep each tensor's copies and kernels in order across steps."""
     torch = g.torch
     names = [n for n, _ in ops]
-    ins, outs = [], []
-    want_w3 = any(n.startswith("w3") for n in names)
-    want_w4 = any(n.startswith("w4") for n in names)
-    if want_w3:
-        ins.append("w3")
-        outs.append("w3_out")
-    if want_w4:
-        ins.append("w4")
-        outs.append("w4_out")
-    if "w5a.reduce" in names:
-        ins += ["w5a_dst", "w5a_src"]
-        outs.append("w5a_dst")
-    if "w5b.ring" in names:
-        ins += ["w5b_a", "w5b_b"]
-        outs += ["cs_a", "cs_b", "bits_a", "bits_b"]
-    pin_in = {k: torch.empty_like(g.t[k], device="cpu").pin_memory() for k in ins}
+    groups = [(gn, ins, outs, [n for n in names if n.split(".")[0].startswith(gn)])
+              for gn, ins, outs in E2E_GROUPS]
+    assert sum(len(x[3]) for x in groups) == len(names), "every op belongs to one group"
+    groups = [x for x in groups if x[3]]
     src = {"w3": h.w3, "w4": h.w4, "w5a_dst": h.w5a_dst, "w5a_src": h.w5a_src,
            "w5b_a": h.w5b_a, "w5b_b": h.w5b_b}
-    for k in ins:
-        pin_in[k].copy_(torch.from_numpy(np.ascontiguousarray(src[k]).reshape(-1).view(np.uint8)))
-    pin_out = {k: torch.empty_like(g.t[k], device="cpu").pin_memory() for k in outs}
+    pin_in, pin_out = {}, {}
+    for _, ins, outs, _ in groups:
+        for k in ins:
+            pin_in[k] = torch.empty_like(g.t[k], device="cpu").pin_memory()
+            pin_in[k].copy_(torch.from_numpy(np.ascontiguousarray(src[k]).reshape(-1).view(np.uint8)))
+        for k in outs:
+            pin_out[k] = torch.empty_like(g.t[k], device="cpu").pin_memory()
     bi = sum(v.numel() * v.element_size() for v in pin_in.values())
     bo = sum(v.numel() * v.element_size() for v in pin_out.values())
+    s_in, s_out, s_run = torch.cuda.Stream(), torch.cuda.Stream(), g.stream
+    outd = {gn: None for gn, *_ in groups}   # results copied out (previous step)
 
     def step():
-        with torch.cuda.stream(g.stream):
-            for k in ins:
-                g.t[k].copy_(pin_in[k], non_blocking=True)
-        for name in names:
-            g.run_op(name)
-        with torch.cuda.stream(g.stream):
-            for k in outs:
-                pin_out[k].copy_(g.t[k], non_blocking=True)
+        for gn, ins, outs, gops in groups:
+            ev_in = torch.cuda.Event()
+            with torch.cuda.stream(s_in):
+                if outd[gn] is not None:
+                    # last step's kernels and read-out are done with these tensors (an input of
+                    # one step may be the previous step's result, e.g. the reduce destination)
+                    s_in.wait_event(outd[gn])
+                for k in ins:
+                    g.t[k].copy_(pin_in[k], non_blocking=True)
+                ev_in.record(s_in)
+            s_run.wait_event(ev_in)
+            if outd[gn] is not None:
+                s_run.wait_event(outd[gn])  # last step's results were read out
+            for name in gops:
+                g.run_op(name, s_run)
+            ev_done = torch.cuda.Event()
+            ev_done.record(s_run)
+            ev_out = torch.cuda.Event()
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done)
+                for k in outs:
+                    pin_out[k].copy_(g.t[k], non_blocking=True)
+                ev_out.record(s_out)
+            outd[gn] = ev_out
 
     step()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(g.stream)
+    e0.record(s_run)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
     for _ in range(steps):
         step()
-    e1.record(g.stream)
+    for st in (s_in, s_out):
+        ev = torch.cuda.Event()
+        ev.record(st)
+        s_run.wait_event(ev)
+    e1.record(s_run)
     torch.cuda.synchronize()
     if g.tm.tm_stream_check(g.stream) != g.tm.TM_OK:
         raise RuntimeError(g.tm.tm_last_error())
@@ -426,6 +454,21 @@ def measured_hbm_peak():
         return 6800.0, "fallback"
 
 
+def tma_kernel_source() -> bytes:
+    """What defines the tensor-map streaming kernels: k_tma.cu, tm_ptx.cuh and the BoxWalk /
+    StreamArgs structs of tm_internal.h."""
+    csrc = os.path.join(ROOT, "async_bulk_tensor_tmap_gb300", "csrc")
+    out = b""
+    for f in ("k_tma.cu", "tm_ptx.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            out += fh.read()
+    with open(os.path.join(csrc, "tm_internal.h"), "rb") as fh:
+        hdr = fh.read()
+    i = hdr.index(b"struct BoxWalk")
+    j = hdr.index(b"};", hdr.index(b"struct StreamArgs")) + 2
+    return out + hdr[i:j]
+
+
 def recorded_traffic(kernel: str):
     """Per-launch DRAM traffic of `kernel` from profiles/roofline_traffic.txt, or None when the
     kernel's source changed since the counters were taken."""
@@ -437,10 +480,7 @@ def recorded_traffic(kernel: str):
         return None
     fields = {k.strip(): v.strip() for k, v in fields.items()}
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "async_bulk_tensor_tmap_gb300", "csrc")
-    for f in ("k_tma.cu", "tm_ptx.cuh", "tm_internal.h"):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+    h.update(tma_kernel_source())
     if fields.get("kernel") != kernel or fields.get("source_sha256") != h.hexdigest():
         return None
     return int(fields["traffic_bytes"])
