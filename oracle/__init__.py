@@ -71,6 +71,17 @@ def lib():
         L.orc_tiled_roundtrip.argtypes = [P(_OrcMap), P(ctypes.c_int32), ctypes.c_uint64,
                                           ctypes.c_uint64, u8p]
         L.orc_tile_reduce_add.argtypes = [P(_OrcMap), P(_OrcMap), ctypes.c_uint64, ctypes.c_uint64]
+        L.orc_combine.argtypes = [ctypes.c_uint32, ctypes.c_uint32, ctypes.c_int, ctypes.c_int]
+        L.orc_combine.restype = ctypes.c_uint32
+        L.orc_reduce_op.argtypes = [P(_OrcMap), P(ctypes.c_int32), u8p, ctypes.c_int, ctypes.c_int]
+        L.orc_tile_reduce.argtypes = [P(_OrcMap), P(_OrcMap), ctypes.c_uint64, ctypes.c_uint64,
+                                      ctypes.c_int, ctypes.c_int]
+        L.orc_f16_to_double.argtypes = [ctypes.c_uint16]
+        L.orc_f16_to_double.restype = ctypes.c_double
+        L.orc_f16_from_double.argtypes = [ctypes.c_double]
+        L.orc_f16_from_double.restype = ctypes.c_uint16
+        L.orc_bf16_from_double.argtypes = [ctypes.c_double]
+        L.orc_bf16_from_double.restype = ctypes.c_uint16
         L.orc_tile_checksum.argtypes = [u8p, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
                                         P(ctypes.c_float), P(ctypes.c_uint64)]
         L.orc_stream_checksums.argtypes = [P(_OrcMap), P(_OrcMap), ctypes.c_uint64,
@@ -209,6 +220,42 @@ def tile_reduce_add(dst: Map, src: Map, threads: int = 1, b0: int = 0,
     L = lib()
     _run(lambda x0, x1: L.orc_tile_reduce_add(ctypes.byref(dst.c), ctypes.byref(src.c),
                                               b0 + x0, b0 + x1), b1 - b0, threads)
+
+
+# element types and operations of the general reduce (values of the C enums)
+F32, F16, BF16, U32, S32 = 0, 1, 2, 3, 4
+ADD, MIN, MAX = 0, 1, 2
+TYPE_ESIZE = {F32: 4, F16: 2, BF16: 2, U32: 4, S32: 4}
+
+
+def combine(a: int, b: int, type_: int, op: int) -> int:
+    """Bit pattern of op(a, b) for one element (a from the destination, b from the source)."""
+    return int(lib().orc_combine(a, b, type_, op))
+
+
+def f16_from_double(v: float) -> int:
+    return int(lib().orc_f16_from_double(v))
+
+
+def bf16_from_double(v: float) -> int:
+    return int(lib().orc_bf16_from_double(v))
+
+
+def f16_to_double(h: int) -> float:
+    return float(lib().orc_f16_to_double(h))
+
+
+def tile_reduce(dst: Map, src: Map, type_: int, op: int, threads: int = 1, b0: int = 0,
+                b1: int | None = None) -> None:
+    """dst = op(dst, src) over boxes b0..b1-1 of dst's grid (src: same dims and box)."""
+    if dst.dims != src.dims or dst.box != src.box:
+        raise ValueError("reduce needs maps with equal dims and box")
+    if dst.esize != TYPE_ESIZE[type_] or src.esize != TYPE_ESIZE[type_]:
+        raise ValueError("element size does not match the reduce type")
+    b1 = dst.num_boxes if b1 is None else b1
+    L = lib()
+    _run(lambda x0, x1: L.orc_tile_reduce(ctypes.byref(dst.c), ctypes.byref(src.c), b0 + x0,
+                                          b0 + x1, type_, op), b1 - b0, threads)
 
 
 def tile_checksum(img: np.ndarray, rows: int, row_bytes: int, span: int):

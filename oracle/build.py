@@ -22,7 +22,7 @@ def build(force: bool = False) -> str:
             os.path.getmtime(LIB) >= os.path.getmtime(d) for d in deps):
         return LIB
     tmp = LIB + f".tmp{os.getpid()}"
-    subprocess.run(["gcc", *CFLAGS, "-o", tmp, SRC], check=True)
+    subprocess.run(["gcc", *CFLAGS, "-o", tmp, SRC, "-lm"], check=True)
     os.replace(tmp, LIB)
     return LIB
 

@@ -11,6 +11,7 @@
  */
 #include "tmap_oracle.h"
 
+#include <math.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -217,6 +218,135 @@ void orc_tile_reduce_add(const orc_map* dst, const orc_map* src, uint64_t b0, ui
         orc_box_start(dst, b, s);
         orc_image(src, s, img);
         orc_reduce_add_f32(dst, s, img);
+    }
+    free(img);
+}
+
+/* ---------------------------------------------------------------------------------------------
+ * General reduce: add / min / max over f32, f16, bf16, u32, s32.
+ * ------------------------------------------------------------------------------------------- */
+double orc_f16_to_double(uint16_t h)
+{
+    const double sign = (h & 0x8000u) ? -1.0 : 1.0;
+    const unsigned e = (h >> 10) & 0x1fu, m = h & 0x3ffu;
+    if (e == 0) return sign * ldexp((double)m, -24);              /* zero or subnormal */
+    if (e == 31) return m ? NAN : sign * INFINITY;
+    return sign * ldexp((double)(1024u + m), (int)e - 25);
+}
+
+/* The value v (finite) rounded to nearest, ties to even, in a binary format with `mbits` stored
+ * significand bits and `ebits` exponent bits (bias 2^(ebits-1) - 1, subnormals, overflow to
+ * infinity); returns the bits. */
+static uint32_t round_to_format(double v, int mbits, int ebits)
+{
+    const int emax = (1 << (ebits - 1)) - 1, emin = 1 - emax;
+    const uint32_t sign_bit = (signbit(v) ? 1u : 0u) << (mbits + ebits);
+    v = fabs(v);
+    if (v == 0.0) return sign_bit;
+    int e2;
+    frexp(v, &e2);
+    int E = e2 - 1;                              /* v in [2^E, 2^(E+1)) */
+    if (E < emin) E = emin;                      /* subnormal range: fixed quantum */
+    const double q = ldexp(1.0, E - mbits);      /* one unit in the last place at E */
+    double n = nearbyint(v / q);                 /* exact scaling, then round half to even */
+    const double one = ldexp(1.0, mbits);
+    if (n >= 2.0 * one) {                        /* rounded up into the next binade */
+        n /= 2.0;
+        E += 1;
+    }
+    if (E > emax) return sign_bit | (((1u << ebits) - 1u) << mbits);   /* infinity */
+    if (n < one) return sign_bit | (uint32_t)n;                        /* subnormal */
+    return sign_bit | ((uint32_t)(E + emax) << mbits) | (uint32_t)(n - one);
+}
+
+uint16_t orc_f16_from_double(double v) { return (uint16_t)round_to_format(v, 10, 5); }
+uint16_t orc_bf16_from_double(double v) { return (uint16_t)round_to_format(v, 7, 8); }
+
+static double bf16_to_double(uint16_t h)
+{
+    uint32_t w = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &w, 4);
+    return (double)f;
+}
+
+static double as_double(uint32_t bits, int type)
+{
+    if (type == ORC_F16) return orc_f16_to_double((uint16_t)bits);
+    if (type == ORC_BF16) return bf16_to_double((uint16_t)bits);
+    float f;
+    memcpy(&f, &bits, 4);
+    return (double)f;
+}
+
+uint32_t orc_combine(uint32_t a, uint32_t b, int type, int op)
+{
+    if (type == ORC_U32) {
+        if (op == ORC_ADD) return a + b;                    /* modulo 2^32 */
+        if (op == ORC_MIN) return a < b ? a : b;
+        return a > b ? a : b;
+    }
+    if (type == ORC_S32) {
+        const int32_t x = (int32_t)a, y = (int32_t)b;
+        if (op == ORC_ADD) return a + b;                    /* two's complement wrap */
+        if (op == ORC_MIN) return (uint32_t)(x < y ? x : y);
+        return (uint32_t)(x > y ? x : y);
+    }
+    const double x = as_double(a, type), y = as_double(b, type);
+    if (op == ORC_MIN) return x < y ? a : (y < x ? b : a);
+    if (op == ORC_MAX) return x > y ? a : (y > x ? b : a);
+    if (type == ORC_F32) {
+        float fx, fy;
+        memcpy(&fx, &a, 4);
+        memcpy(&fy, &b, 4);
+        const float r = fx + fy;                            /* one binary32 add, to nearest */
+        uint32_t out;
+        memcpy(&out, &r, 4);
+        return out;
+    }
+    /* f16 / bf16: round the exact sum.  For two f16 operands the double sum is exact (both are
+     * multiples of 2^-24 below 2^16).  For two bf16 operands it is exact when their exponents
+     * differ by at most 45; otherwise the smaller is below 2^-45 of the larger, the exact sum lies
+     * far from any bf16 rounding midpoint, and the double sum rounds to the same bf16 value. */
+    const double sum = x + y;
+    return type == ORC_F16 ? orc_f16_from_double(sum) : orc_bf16_from_double(sum);
+}
+
+typedef struct {
+    const uint8_t* img;
+    int type, op;
+} reduce_ctx;
+
+static void reduce_op_one(const orc_map* m, const int64_t* g, uint64_t lin, void* ctx)
+{
+    const reduce_ctx* rc = (const reduce_ctx*)ctx;
+    if (!in_bounds(m, g)) return;
+    uint8_t* dst = element_address(m, g);
+    uint32_t a = 0, b = 0;
+    for (uint32_t k = 0; k < m->esize; k++) {
+        a |= (uint32_t)dst[k] << (8 * k);
+        b |= (uint32_t)rc->img[orc_swz(lin * m->esize + k, m->span)] << (8 * k);
+    }
+    const uint32_t r = orc_combine(a, b, rc->type, rc->op);
+    for (uint32_t k = 0; k < m->esize; k++) dst[k] = (uint8_t)(r >> (8 * k));
+}
+
+void orc_reduce_op(const orc_map* dst, const int32_t* s, const uint8_t* img, int type, int op)
+{
+    reduce_ctx rc = {img, type, op};
+    for_each_element(dst, s, reduce_op_one, &rc);
+}
+
+void orc_tile_reduce(const orc_map* dst, const orc_map* src, uint64_t b0, uint64_t b1, int type,
+                     int op)
+{
+    uint8_t* img = (uint8_t*)malloc(orc_box_bytes(src));
+    if (!img) return;
+    for (uint64_t b = b0; b < b1; b++) {
+        int32_t s[5];
+        orc_box_start(dst, b, s);
+        orc_image(src, s, img);
+        orc_reduce_op(dst, s, img, type, op);
     }
     free(img);
 }

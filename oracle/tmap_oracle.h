@@ -29,6 +29,10 @@
  *                             tensor; 128B mode equals the page's sector-XOR-row rule applied to
  *                             that slice; store(image(x)) restores x with sentinels intact.
  *   orc_reduce_add_f32 ...... pinned: numpy float32 addition (IEEE binary32, round to nearest).
+ *   orc_combine ............. pinned: f16 add against numpy float16 of the (exact) double sum;
+ *                             bf16 add against an exact rational sum rounded half-to-even in
+ *                             Python; min / max / integer ops against numpy.  Rounding of f16 /
+ *                             bf16 adds is this library's reading (the pages do not state it).
  *   orc_tile_checksum ....... pinned: numpy sequential cumsum + pairwise tree, and an exact
  *                             integer bit-sum.  The checksum itself is this library's definition;
  *                             the pages are silent on what the ring's consumer computes.
@@ -88,6 +92,25 @@ void orc_tiled_roundtrip(const orc_map* m, const int32_t* coords, uint64_t b0, u
                          const uint8_t* images);
 /* Boxes b0..b1-1 of the box grid of dst (src has the same dims and box): dst += src. */
 void orc_tile_reduce_add(const orc_map* dst, const orc_map* src, uint64_t b0, uint64_t b1);
+
+/* The general reduce ([Book-TMA] §"TMA reduce，把“搬运”和“归约”合并": the write-back combines each
+ * element with the value in global memory, "add, min and the like").  Element types and ops: */
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2, ORC_U32 = 3, ORC_S32 = 4 };
+enum { ORC_ADD = 0, ORC_MIN = 1, ORC_MAX = 2 };
+/* One element: the bit pattern of op(a, b), a from dst and b from src, in the element type.
+ *   float add: the exact sum rounded to nearest, ties to even, in the element format (subnormal
+ *              results kept, overflow to infinity);  float min / max: the smaller / larger value;
+ *   u32 / s32 add: the sum modulo 2^32;  u32 / s32 min / max: unsigned / signed comparison. */
+uint32_t orc_combine(uint32_t a, uint32_t b, int type, int op);
+/* dst(element) = op(dst(element), image(element)) for each in-bounds element of the box. */
+void orc_reduce_op(const orc_map* dst, const int32_t* s, const uint8_t* img, int type, int op);
+/* Boxes b0..b1-1 of the grid of dst: load the src box into its image, reduce it into dst. */
+void orc_tile_reduce(const orc_map* dst, const orc_map* src, uint64_t b0, uint64_t b1, int type,
+                     int op);
+/* Exact conversions used by the above (exposed for the pins). */
+double orc_f16_to_double(uint16_t h);
+uint16_t orc_f16_from_double(double v);
+uint16_t orc_bf16_from_double(double v);
 
 /* Checksum of one bf16 tile image of `rows` rows of `row_bytes` bytes (rows a power of two):
  * rowsum_r is the sequential fp32 sum of the row's elements in logical order, the tile value is

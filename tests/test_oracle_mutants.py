@@ -35,6 +35,13 @@ MUTANTS = {
                          "    uint8_t* dst = element_address(m, g);\n    if (!in_bounds(m, g)) dst = dst + 0;\n    for"),
     "checksum_bits_dropped_high_byte": ("(img[orc_swz(off + 1, span)] << 8)",
                                         "(img[orc_swz(off + 1, span)] << 0)"),
+    "half_add_rounds_half_up": ("double n = nearbyint(v / q);", "double n = floor(v / q + 0.5);"),
+    "s32_min_compares_unsigned": ("        if (op == ORC_MIN) return (uint32_t)(x < y ? x : y);",
+                                  "        if (op == ORC_MIN) return a < b ? a : b;"),
+    "subnormals_flushed": ("if (E < emin) E = emin;", "if (E < emin) return sign_bit;"),
+    "float_max_picks_smaller": ("if (op == ORC_MAX) return x > y ? a : (y > x ? b : a);",
+                                "if (op == ORC_MAX) return x < y ? a : (y < x ? b : a);"),
+    "half_add_drops_operand": ("    const double sum = x + y;", "    const double sum = x + 0 * y;"),
 }
 
 
@@ -49,9 +56,10 @@ def test_pins_reject_mutant(name, tmp_path):
     (d / "tmap_oracle.c").write_text(src.replace(old, new))
     lib = d / "libmutant.so"
     subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
-                    "-o", str(lib), str(d / "tmap_oracle.c")], check=True)
+                    "-o", str(lib), str(d / "tmap_oracle.c"), "-lm"], check=True)
     env = dict(os.environ, TMAP_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_reduce_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
