@@ -12,7 +12,7 @@ Function names and argument order follow the C ABI:
     tiled_copy(src, coords, images, stream=None)            coords None = whole box grid
     tiled_roundtrip(dst, coords, images, stream=None)
     tiled_copy_noalloc(src, coords, images, stream=None)  no device allocation, returns when done
-    tile_reduce_add(dst, src, stream=None)
+    tile_reduce_add(dst, src, stream=None), tile_reduce(dst, src, op, stream=None)
     stream_tiles(a, b, stages, cs_a, cs_b, bits_a, bits_b, stream=None)
     tm_stream_check(stream=None), tm_selftest_wait_timeout(timeout_ns, stream=None)
 Dimension lists are innermost first, as in the C ABI.
@@ -25,6 +25,7 @@ import os
 __all__ = [
     "TmapError", "TensorMap", "tmap_plan", "tmap_encode", "tmap_replace_address",
     "tmap_force_fallback", "tile_load_image", "tiled_copy", "tiled_roundtrip", "tile_reduce_add",
+    "tile_reduce", "TM_RED_ADD", "TM_RED_MIN", "TM_RED_MAX",
     "stream_tiles", "tiled_copy_noalloc", "TM_NOALLOC_MAX_BOXES", "tm_stream_check",
     "tm_selftest_wait_timeout", "tm_pick_swizzle", "tm_last_error",
     "library_path", "TM_OK", "TM_EINVAL", "TM_EALIGN", "TM_ERANGE", "TM_EUNSUPPORTED",
@@ -39,6 +40,7 @@ TM_U8, TM_U16, TM_U32, TM_S32, TM_U64, TM_S64, TM_F16, TM_F32, TM_F64, TM_BF16 =
 TM_SWIZZLE_NONE, TM_SWIZZLE_32B, TM_SWIZZLE_64B, TM_SWIZZLE_128B = range(4)
 TM_OOB_ZERO, TM_OOB_NAN = 0, 1
 TM_PATH_TMA, TM_PATH_FALLBACK = 1, 2
+TM_RED_ADD, TM_RED_MIN, TM_RED_MAX = 0, 1, 2
 TM_WHY_STRIDE, TM_WHY_BASE, TM_WHY_DRIVER, TM_WHY_FORCED = 1, 2, 4, 8
 DESC_SIZE = 384
 TM_NOALLOC_MAX_BOXES = 16384
@@ -69,6 +71,7 @@ _SIGS = {
     "tiled_roundtrip": [_vp, _P(_i32), ctypes.c_size_t, _vp, _vp],
     "tiled_copy_noalloc": [_vp, _P(_i32), ctypes.c_size_t, _vp, _vp],
     "tile_reduce_add": [_vp, _vp, _vp],
+    "tile_reduce": [_vp, _vp, ctypes.c_int, _vp],
     "stream_tiles": [_vp, _vp, _u32, _vp, _vp, _vp, _vp, _vp],
     "tm_stream_check": [_vp],
     "tm_selftest_wait_timeout": [_u64, _vp],
@@ -260,6 +263,10 @@ def tiled_roundtrip(dst: TensorMap, coords, images, stream=None) -> None:
 
 def tile_reduce_add(dst: TensorMap, src: TensorMap, stream=None) -> None:
     _check(_L.tile_reduce_add(dst.ptr, src.ptr, _stream(stream)), "tile_reduce_add")
+
+
+def tile_reduce(dst: TensorMap, src: TensorMap, op, stream=None) -> None:
+    _check(_L.tile_reduce(dst.ptr, src.ptr, int(op), _stream(stream)), "tile_reduce")
 
 
 def stream_tiles(a: TensorMap, b: TensorMap, stages, cs_a, cs_b, bits_a, bits_b,

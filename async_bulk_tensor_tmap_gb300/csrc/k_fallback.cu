@@ -15,10 +15,15 @@
 //   store  each thread reads its 16-byte chunks of the image straight from global memory
 //          (coalesced: a swizzle only permutes chunks inside a 128-byte row) and writes their
 //          in-bounds bytes with the widest stores the destination alignment allows.
-//   reduce element-wise fp32 adds straight from global memory.
+//   reduce element-wise add / min / max (f32, f16, bf16, u32, s32) straight from global memory.
 //
 // A window is only loaded when it holds at least one in-bounds byte of the row; an aligned
 // 16-byte window never crosses a page, so no load can touch an unmapped address.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
 #include "tm_ptx.cuh"
 
 namespace tmk {
@@ -333,31 +338,140 @@ __global__ void __launch_bounds__(kThreads, 6) k_fb_store(const __grid_constant_
     }
 }
 
-// Reduce direction on the fallback path: dst += src element by element (the swizzle of the image
-// in between cancels between load and store, so the element read is src at the same coordinate).
-__global__ void __launch_bounds__(kThreads) k_fb_reduce(const __grid_constant__ FbArgs a)
+// ---- reduce direction -------------------------------------------------------------------------
+// op(a, b) for one element, a from dst, b from src (op 0 add, 1 min, 2 max).  Float adds: for two
+// f16 or bf16 operands the binary32 sum is exact, or else too far from any 16-bit rounding midpoint
+// to change the result, so rounding it to the element format gives the correctly rounded sum.
+// Min / max keep dst on a tie of equal values.
+template <int T>
+__device__ __forceinline__ float to_f32(uint32_t bits)
 {
-    const uint32_t lane = threadIdx.x & 31;
-    const uint64_t warps = (uint64_t)gridDim.x * (kThreads / 32);
-    const uint64_t total = a.walk.nbox * a.rows;
-    const uint32_t box0 = a.walk.box[0];
-    for (uint64_t rr = (uint64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); rr < total;
-         rr += warps) {
-        const uint64_t b = rr / a.rows;
-        const uint32_t row = (uint32_t)(rr - b * a.rows);
-        int32_t c[5];
-        box_start(a.walk, b, c);
-        const RowPos pd = row_position(a, c, row, a.stride);
-        if (!pd.ok) continue;
-        const RowPos ps = row_position(a, c, row, a.src_stride);
-        for (uint32_t k = lane; k < box0; k += 32) {
-            const int64_t x = (int64_t)c[0] + k;
-            if (x < 0 || (uint64_t)x >= a.dim[0]) continue;
-            float* d = reinterpret_cast<float*>(a.base + pd.off + (int64_t)k * 4);
-            const float* s = reinterpret_cast<const float*>(a.src_base + ps.off + (int64_t)k * 4);
-            *d = __fadd_rn(*d, *s);
+    if constexpr (T == 1) return __half2float(__ushort_as_half((unsigned short)bits));
+    if constexpr (T == 2) return __uint_as_float(bits << 16);
+    return __uint_as_float(bits);
+}
+
+template <int T>
+__device__ __forceinline__ uint32_t from_f32(float v)
+{
+    if constexpr (T == 1) return __half_as_ushort(__float2half_rn(v));
+    if constexpr (T == 2) return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    return __float_as_uint(v);
+}
+
+template <int T, int OP>
+__device__ __forceinline__ uint32_t combine(uint32_t a, uint32_t b)
+{
+    if constexpr (T == 3) {  // u32
+        return OP == 0 ? a + b : OP == 1 ? (b < a ? b : a) : (b > a ? b : a);
+    } else if constexpr (T == 4) {  // s32
+        const int32_t x = (int32_t)a, y = (int32_t)b;
+        return OP == 0 ? a + b : (uint32_t)(OP == 1 ? (y < x ? y : x) : (y > x ? y : x));
+    } else {
+        const float x = to_f32<T>(a), y = to_f32<T>(b);
+        if constexpr (OP == 1) return y < x ? b : a;
+        if constexpr (OP == 2) return y > x ? b : a;
+        return from_f32<T>(__fadd_rn(x, y));
+    }
+}
+
+// Applies op to the elements of a 16-byte vector pair (4 x 32-bit or 8 x 16-bit elements).
+template <int T, int OP>
+__device__ __forceinline__ uint4 combine_vec(uint4 d, const uint4& s)
+{
+    uint32_t* dw = reinterpret_cast<uint32_t*>(&d);
+    const uint32_t* sw = reinterpret_cast<const uint32_t*>(&s);
+#pragma unroll
+    for (int w = 0; w < 4; w++) {
+        if constexpr (T == 1 || T == 2) {
+            const uint32_t lo = combine<T, OP>(dw[w] & 0xffffu, sw[w] & 0xffffu);
+            const uint32_t hi = combine<T, OP>(dw[w] >> 16, sw[w] >> 16);
+            dw[w] = (lo & 0xffffu) | (hi << 16);
+        } else {
+            dw[w] = combine<T, OP>(dw[w], sw[w]);
         }
     }
+    return d;
+}
+
+// dst = op(dst, src) over the whole box grid.  The grid covers every in-bounds element exactly
+// once and the op is element-wise (the image's swizzle cancels between load and store), so the
+// kernel walks the tensor's rows (dim 0 runs) directly: work items are 16 KiB segments of a row;
+// rows whose dst and src start on the same 16-byte phase go with 16-byte vector loads and stores
+// (elements before the first and after the last full vector one by one), other rows element by
+// element.
+template <int T, int OP>
+__device__ void fb_reduce_rows(const FbArgs& a)
+{
+    using E = typename std::conditional<(T == 1 || T == 2), uint16_t, uint32_t>::type;
+    constexpr int es = (int)sizeof(E);
+    constexpr uint32_t kVecPerThread = 4;
+    constexpr uint64_t kSegBytes = (uint64_t)kThreads * kVecPerThread * 16;
+    const uint64_t row_bytes = a.dim[0] * es;
+    const uint64_t segs = (row_bytes + kSegBytes - 1) / kSegBytes;
+    uint64_t nrows = 1;
+    for (uint32_t i = 1; i < a.walk.rank; i++) nrows *= a.dim[i];
+    const uint64_t items = nrows * segs;
+    for (uint64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const uint64_t row = it / segs, seg = it - row * segs;
+        int64_t od = 0, os = 0;
+        uint64_t q = row;
+        for (uint32_t i = 1; i < a.walk.rank; i++) {
+            const uint64_t nxt = q / a.dim[i];
+            const int64_t g = (int64_t)(q - nxt * a.dim[i]);
+            q = nxt;
+            od += g * a.stride[i];
+            os += g * a.src_stride[i];
+        }
+        uint8_t* const d = reinterpret_cast<uint8_t*>(a.base + od);
+        const uint8_t* const sp = reinterpret_cast<const uint8_t*>(a.src_base + os);
+        const uint64_t b0 = seg * kSegBytes;
+        const uint64_t b1 = min(b0 + kSegBytes, row_bytes);
+        const uint32_t phase = (uint32_t)((uintptr_t)d & 15);
+        if (phase == ((uintptr_t)sp & 15)) {
+            // head [b0, vs) and tail [ve, b1) element by element, whole vectors in [vs, ve)
+            const uint64_t first_vec = ((uint64_t)((uintptr_t)d + b0) + 15) / 16 * 16 - (uintptr_t)d;
+            const uint64_t vs = min(first_vec, b1);
+            const uint64_t ve = vs + (b1 - vs) / 16 * 16;
+            for (uint64_t x = b0 + threadIdx.x * es; x < vs; x += kThreads * es) {
+                E* p = reinterpret_cast<E*>(d + x);
+                *p = (E)combine<T, OP>((uint32_t)*p, (uint32_t)*reinterpret_cast<const E*>(sp + x));
+            }
+            const uint64_t nv = (ve - vs) / 16;
+            for (uint64_t v = threadIdx.x; v < nv; v += kThreads * kVecPerThread) {
+                uint4 dv[kVecPerThread], sv[kVecPerThread];
+#pragma unroll
+                for (uint32_t u = 0; u < kVecPerThread; u++) {
+                    const uint64_t vi = v + u * kThreads;
+                    if (vi < nv) {
+                        dv[u] = *reinterpret_cast<const uint4*>(d + vs + vi * 16);
+                        sv[u] = __ldg(reinterpret_cast<const uint4*>(sp + vs + vi * 16));
+                    }
+                }
+#pragma unroll
+                for (uint32_t u = 0; u < kVecPerThread; u++) {
+                    const uint64_t vi = v + u * kThreads;
+                    if (vi < nv)
+                        *reinterpret_cast<uint4*>(d + vs + vi * 16) = combine_vec<T, OP>(dv[u], sv[u]);
+                }
+            }
+            for (uint64_t x = ve + threadIdx.x * es; x < b1; x += kThreads * es) {
+                E* p = reinterpret_cast<E*>(d + x);
+                *p = (E)combine<T, OP>((uint32_t)*p, (uint32_t)*reinterpret_cast<const E*>(sp + x));
+            }
+        } else {
+            for (uint64_t x = b0 + threadIdx.x * es; x < b1; x += kThreads * es) {
+                E* p = reinterpret_cast<E*>(d + x);
+                *p = (E)combine<T, OP>((uint32_t)*p, (uint32_t)*reinterpret_cast<const E*>(sp + x));
+            }
+        }
+    }
+}
+
+template <int T, int OP>
+__global__ void __launch_bounds__(kThreads, 3) k_fb_reduce(const __grid_constant__ FbArgs a)
+{
+    fb_reduce_rows<T, OP>(a);
 }
 
 cudaError_t launch_fb_copy(const FbArgs& a, uint32_t grid, size_t smem, cudaStream_t s)
@@ -380,7 +494,16 @@ cudaError_t launch_fb_store(const FbArgs& a, uint32_t grid, size_t smem, cudaStr
 
 cudaError_t launch_fb_reduce(const FbArgs& a, uint32_t grid, cudaStream_t s)
 {
-    k_fb_reduce<<<grid, kThreads, 0, s>>>(a);
+    using Fn = void (*)(const FbArgs);
+    static const Fn table[5][3] = {
+        {k_fb_reduce<0, 0>, k_fb_reduce<0, 1>, k_fb_reduce<0, 2>},
+        {k_fb_reduce<1, 0>, k_fb_reduce<1, 1>, k_fb_reduce<1, 2>},
+        {k_fb_reduce<2, 0>, k_fb_reduce<2, 1>, k_fb_reduce<2, 2>},
+        {k_fb_reduce<3, 0>, k_fb_reduce<3, 1>, k_fb_reduce<3, 2>},
+        {k_fb_reduce<4, 0>, k_fb_reduce<4, 1>, k_fb_reduce<4, 2>},
+    };
+    if (a.red_type > 4 || a.red_op > 2) return cudaErrorInvalidValue;
+    table[a.red_type][a.red_op]<<<grid, kThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -22,7 +22,7 @@
 // The three kinds differ only in the two copy instructions:
 //   copy       load = tensor load of the box;  write = 1-D bulk store of the image (tile-major)
 //   round trip load = 1-D bulk load of image b; write = tensor store through the map
-//   reduce     load = tensor load of src;      write = tensor reduce-add into dst
+//   reduce     load = tensor load of src;      write = tensor reduce (add, min or max) into dst
 // ([Book-TMA] = fangpin "gpu-hpc-book" ch. 08 "Cuda TMA", §"TMA store" and §"TMA reduce，把“搬运”
 // 和“归约”合并" show the single-tile forms of the last two.)
 #include "tm_ptx.cuh"
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(32, 1)
                 if constexpr (KIND == KIND_ROUNDTRIP) {
                     tma_store<R>(&out_map, c, src + j * a.box_bytes);
                 } else {
-                    tma_reduce_add<R>(&out_map, c, src + j * a.box_bytes);
+                    tma_reduce<R, KIND - KIND_REDUCE>(&out_map, c, src + j * a.box_bytes);
                 }
             });
         }
@@ -153,9 +153,11 @@ static cudaError_t launch_rank(int kind, const CUtensorMap* in_map, const CUtens
                                const StreamArgs& a, uint32_t grid, size_t smem, cudaStream_t s)
 {
     void (*fn)(const CUtensorMap, const CUtensorMap, const StreamArgs) =
-        kind == KIND_COPY        ? k_tma_stream<R, KIND_COPY>
-        : kind == KIND_ROUNDTRIP ? k_tma_stream<R, KIND_ROUNDTRIP>
-                                 : k_tma_stream<R, KIND_REDUCE>;
+        kind == KIND_COPY         ? k_tma_stream<R, KIND_COPY>
+        : kind == KIND_ROUNDTRIP  ? k_tma_stream<R, KIND_ROUNDTRIP>
+        : kind == KIND_REDUCE_MIN ? k_tma_stream<R, KIND_REDUCE_MIN>
+        : kind == KIND_REDUCE_MAX ? k_tma_stream<R, KIND_REDUCE_MAX>
+                                  : k_tma_stream<R, KIND_REDUCE>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;

@@ -71,7 +71,8 @@ struct FbArgs {
     uint32_t stage_bytes;
     uint32_t rows;         // image rows = box_bytes / inner_bytes
     uint32_t block_rows;   // image rows handled per block (shared-memory row table / staging)
-    uint32_t pad;
+    uint16_t red_type;     // reduce: 0 f32, 1 f16, 2 bf16, 3 u32, 4 s32
+    uint16_t red_op;       // reduce: 0 add, 1 min, 2 max
     uint64_t timeout_ns;
     StatusBlock* status;
 };
@@ -117,7 +118,10 @@ struct RingArgs {
 };
 
 // Launchers (defined next to their kernels).  Return a cudaError_t.
-enum StreamKind : int { KIND_COPY = 0, KIND_ROUNDTRIP = 1, KIND_REDUCE = 2 };
+// Reduce kinds: KIND_REDUCE + op, op 0 add, 1 min, 2 max.
+enum StreamKind : int {
+    KIND_COPY = 0, KIND_ROUNDTRIP = 1, KIND_REDUCE = 2, KIND_REDUCE_MIN = 3, KIND_REDUCE_MAX = 4
+};
 cudaError_t launch_tma_stream(int kind, uint32_t rank, const CUtensorMap* in_map,
                               const CUtensorMap* out_map, const StreamArgs& a, uint32_t grid,
                               size_t smem, cudaStream_t s);

@@ -180,39 +180,40 @@ __device__ __forceinline__ void tma_store(const CUtensorMap* m, const int32_t* c
     }
 }
 
-// Shared -> global element-wise add into the tensor (the map's type decides the add: fp32 here).
-template <int R>
-__device__ __forceinline__ void tma_reduce_add(const CUtensorMap* m, const int32_t* c,
-                                               uint32_t src)
+// Shared -> global element-wise reduction into the tensor, op OP = 0 add, 1 min, 2 max; the map's
+// element type decides the arithmetic.
+#define TMK_RED_ASM(RANK, OPS, COORDS)                                                           \
+    asm volatile("cp.reduce.async.bulk.tensor." RANK ".global.shared::cta." OPS                 \
+                 ".tile.bulk_group [%0, {" COORDS "}], [%1];"
+
+template <int R, int OP>
+__device__ __forceinline__ void tma_reduce(const CUtensorMap* m, const int32_t* c, uint32_t src)
 {
     const uint64_t mp = reinterpret_cast<uint64_t>(m);
-    if constexpr (R == 1) {
-        asm volatile(
-            "cp.reduce.async.bulk.tensor.1d.global.shared::cta.add.tile.bulk_group [%0, {%2}], [%1];"
-            ::"l"(mp), "r"(src), "r"(c[0]) : "memory");
-    } else if constexpr (R == 2) {
-        asm volatile(
-            "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group"
-            " [%0, {%2, %3}], [%1];"
-            ::"l"(mp), "r"(src), "r"(c[0]), "r"(c[1]) : "memory");
-    } else if constexpr (R == 3) {
-        asm volatile(
-            "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
-            " [%0, {%2, %3, %4}], [%1];"
-            ::"l"(mp), "r"(src), "r"(c[0]), "r"(c[1]), "r"(c[2]) : "memory");
-    } else if constexpr (R == 4) {
-        asm volatile(
-            "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group"
-            " [%0, {%2, %3, %4, %5}], [%1];"
-            ::"l"(mp), "r"(src), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]) : "memory");
-    } else {
-        asm volatile(
-            "cp.reduce.async.bulk.tensor.5d.global.shared::cta.add.tile.bulk_group"
-            " [%0, {%2, %3, %4, %5, %6}], [%1];"
-            ::"l"(mp), "r"(src), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4])
-            : "memory");
+    constexpr bool add = OP == 0, mn = OP == 1;
+#define TMK_RED_OP(RANK, COORDS, ...)                                                            \
+    if constexpr (add) {                                                                         \
+        TMK_RED_ASM(RANK, "add", COORDS)::"l"(mp), "r"(src), __VA_ARGS__ : "memory");           \
+    } else if constexpr (mn) {                                                                   \
+        TMK_RED_ASM(RANK, "min", COORDS)::"l"(mp), "r"(src), __VA_ARGS__ : "memory");           \
+    } else {                                                                                     \
+        TMK_RED_ASM(RANK, "max", COORDS)::"l"(mp), "r"(src), __VA_ARGS__ : "memory");           \
     }
+    if constexpr (R == 1) {
+        TMK_RED_OP("1d", "%2", "r"(c[0]))
+    } else if constexpr (R == 2) {
+        TMK_RED_OP("2d", "%2, %3", "r"(c[0]), "r"(c[1]))
+    } else if constexpr (R == 3) {
+        TMK_RED_OP("3d", "%2, %3, %4", "r"(c[0]), "r"(c[1]), "r"(c[2]))
+    } else if constexpr (R == 4) {
+        TMK_RED_OP("4d", "%2, %3, %4, %5", "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]))
+    } else {
+        TMK_RED_OP("5d", "%2, %3, %4, %5, %6", "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]),
+                   "r"(c[4]))
+    }
+#undef TMK_RED_OP
 }
+#undef TMK_RED_ASM
 
 // L2 prefetch of a 2-D box (no shared memory, no completion tracking).
 __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int32_t c0, int32_t c1)

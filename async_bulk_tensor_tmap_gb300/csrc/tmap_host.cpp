@@ -566,11 +566,22 @@ int tiled_roundtrip(const tm_desc* dst, const int32_t* coords, size_t nbox, cons
     return rc;
 }
 
-int tile_reduce_add(const tm_desc* dst, const tm_desc* src, void* stream)
+int tile_reduce(const tm_desc* dst, const tm_desc* src, tm_redop op, void* stream)
 {
     if (!valid_desc(dst) || !valid_desc(src)) return fail(TM_EINVAL, "descriptor is not filled");
-    if (dst->dtype != TM_F32 || src->dtype != TM_F32)
-        return fail(TM_EUNSUPPORTED, "reduce-add supports TM_F32 maps only");
+    if (op != TM_RED_ADD && op != TM_RED_MIN && op != TM_RED_MAX)
+        return fail(TM_EINVAL, "bad reduce op %d", (int)op);
+    int red_type = -1;
+    switch (dst->dtype) {
+        case TM_F32: red_type = 0; break;
+        case TM_F16: red_type = 1; break;
+        case TM_BF16: red_type = 2; break;
+        case TM_U32: red_type = 3; break;
+        case TM_S32: red_type = 4; break;
+        default: break;
+    }
+    if (red_type < 0) return fail(TM_EUNSUPPORTED, "reduce supports f32, f16, bf16, u32 and s32");
+    if (src->dtype != dst->dtype) return fail(TM_EINVAL, "dst and src differ in element type");
     if (dst->rank != src->rank || dst->swizzle != src->swizzle)
         return fail(TM_EINVAL, "dst and src differ in rank or swizzle");
     for (uint32_t i = 0; i < dst->rank; i++) {
@@ -583,23 +594,38 @@ int tile_reduce_add(const tm_desc* dst, const tm_desc* src, void* stream)
     cudaStream_t st = (cudaStream_t)stream;
     BoxWalk w;
     if ((rc = make_walk(dst, nullptr, 0, st, w))) return rc;
-    const uint64_t n = dst->num_boxes;
-    if (store_fits_tma(dst) && src->path == TM_PATH_TMA) {
+    // The tensor reduce is given add on every supported type and min / max on the integer types;
+    // float min / max run element-wise on the vector path.
+    const bool tma_op = op == TM_RED_ADD || red_type >= 3;
+    if (tma_op && store_fits_tma(dst) && src->path == TM_PATH_TMA) {
         Geometry g;
         const StreamArgs a = stream_args(dst, w, 0, *ds, g);
-        rc = check_launch(launch_tma_stream(KIND_REDUCE, dst->rank, (const CUtensorMap*)src->tmap,
+        rc = check_launch(launch_tma_stream(KIND_REDUCE + (int)op, dst->rank,
+                                            (const CUtensorMap*)src->tmap,
                                             (const CUtensorMap*)dst->tmap, a, g.grid, g.smem, st),
                           "tensor reduce launch");
     } else {
         FbArgs a = fb_args(dst, w, 0, *ds);
         a.src_base = src->base;
         for (int i = 0; i < 5; i++) a.src_stride[i] = (int64_t)src->stride[i];
-        const uint64_t rows = n * a.rows;
-        const uint32_t grid = (uint32_t)std::min<uint64_t>((rows + 7) / 8, (uint64_t)ds->sms * 8);
+        a.red_type = (uint16_t)red_type;
+        a.red_op = (uint16_t)op;
+        // work items of the element-wise kernel: 16 KiB segments of the tensor's rows
+        uint64_t items = (dst->dim[0] * dst->esize + 16383) / 16384;
+        for (uint32_t i = 1; i < dst->rank; i++) items *= dst->dim[i];
+        const uint32_t grid = (uint32_t)std::min<uint64_t>(items, (uint64_t)ds->sms * 3);
         rc = check_launch(launch_fb_reduce(a, std::max<uint32_t>(grid, 1), st),
                           "fallback reduce launch");
     }
     return rc;
+}
+
+int tile_reduce_add(const tm_desc* dst, const tm_desc* src, void* stream)
+{
+    if (!valid_desc(dst) || !valid_desc(src)) return fail(TM_EINVAL, "descriptor is not filled");
+    if (dst->dtype != TM_F32 || src->dtype != TM_F32)
+        return fail(TM_EUNSUPPORTED, "reduce-add supports TM_F32 maps only");
+    return tile_reduce(dst, src, TM_RED_ADD, stream);
 }
 
 int stream_tiles(const tm_desc* a, const tm_desc* b, uint32_t stages, float* cs_a, float* cs_b,

@@ -101,6 +101,15 @@ class HostWorkload:
         self.w4 = workloads.w4_tensor(rows=r4) if need("w4") else None
         self.w5a_dst, self.w5a_src = workloads.w5a_tensors(r5a) if need("w5a") else (None, None)
         self.w5b_a, self.w5b_b = workloads.w5b_tensors(m5b, 4096, m5b) if need("w5b") else (None, None)
+        # widened reduce ops (not in the default step): bf16 add on its own tensors; s32 min and
+        # f32 max over the W5a buffers
+        if ops is not None and need("w5c"):
+            if self.w5a_dst is None:
+                self.w5a_dst, self.w5a_src = workloads.w5a_tensors(r5a)
+            self.w5c_dst = workloads.normal_bf16((r5a, 16384), 55)
+            self.w5c_src = workloads.normal_bf16((r5a, 16384), 56)
+        else:
+            self.w5c_dst = self.w5c_src = None
         self.gen_s = time.time() - t0
         self.r3 = workloads.w3_map(r3, 8192)
         self.r4_128 = workloads.w4_rank3_map(64, rows=r4, span=128)
@@ -145,6 +154,12 @@ def op_table(h: HostWorkload):
     return t
 
 
+# Widened reduce ops, timed only when named with --ops: (name, algorithmic bytes per call).
+def extra_ops(h: HostWorkload):
+    n = inbounds_bytes(h.r5a) // 4  # elements
+    return [("w5c.add_bf16", 3 * 2 * n), ("w5c.min_s32", 3 * 4 * n), ("w5c.max_f32", 3 * 4 * n)]
+
+
 # ------------------------------------------------------------------------------------------------
 # GPU arm
 # ------------------------------------------------------------------------------------------------
@@ -185,6 +200,13 @@ class GpuWorkload:
             self.t["cs_b"] = torch.zeros(n, dtype=torch.float32, device="cuda")
             self.t["bits_a"] = torch.zeros(n, dtype=torch.int64, device="cuda")
             self.t["bits_b"] = torch.zeros(n, dtype=torch.int64, device="cuda")
+        if h.w5c_dst is not None:
+            self.t["w5c_dst"], self.t["w5c_src"] = dev(h.w5c_dst), dev(h.w5c_src)
+            rb = dict(h.r5a, box=[64, 128], esize=2, strides=[h.r5a["dims"][0] * 2])
+            self.maps["w5c_dst"] = enc(tm.TM_BF16, self.t["w5c_dst"], rb)
+            self.maps["w5c_src"] = enc(tm.TM_BF16, self.t["w5c_src"], rb)
+            self.maps["w5a_dst_s32"] = enc(tm.TM_S32, self.t["w5a_dst"], h.r5a)
+            self.maps["w5a_src_s32"] = enc(tm.TM_S32, self.t["w5a_src"], h.r5a)
         for k in ("w3", "w4r3", "w4r3n", "w4r5"):
             if k in self.maps:
                 m = self.maps[k]
@@ -203,6 +225,12 @@ class GpuWorkload:
             tm.tiled_roundtrip(m[f"{base}_out"], None, t[f"{base}_img"], s)
         elif kind == "reduce":
             tm.tile_reduce_add(m["w5a_dst"], m["w5a_src"], s)
+        elif kind == "add_bf16":
+            tm.tile_reduce(m["w5c_dst"], m["w5c_src"], tm.TM_RED_ADD, s)
+        elif kind == "min_s32":
+            tm.tile_reduce(m["w5a_dst_s32"], m["w5a_src_s32"], tm.TM_RED_MIN, s)
+        elif kind == "max_f32":
+            tm.tile_reduce(m["w5a_dst"], m["w5a_src"], tm.TM_RED_MAX, s)
         elif kind == "ring":
             tm.stream_tiles(m["w5b_a"], m["w5b_b"], self.ring_stages, t["cs_a"], t["cs_b"],
                             t["bits_a"], t["bits_b"], s)
@@ -419,6 +447,12 @@ def oracle_sample(h: HostWorkload, ops, fraction: float, threads: int):
             oracle.tile_reduce_add(om(d, h.r5a), om(h.w5a_src, h.r5a), threads=threads, b0=0, b1=k)
             spent += time.perf_counter() - t0
             covered += nbytes * k // n
+        elif kind == "add_bf16":
+            tm.tile_reduce(m["w5c_dst"], m["w5c_src"], tm.TM_RED_ADD, s)
+        elif kind == "min_s32":
+            tm.tile_reduce(m["w5a_dst_s32"], m["w5a_src_s32"], tm.TM_RED_MIN, s)
+        elif kind == "max_f32":
+            tm.tile_reduce(m["w5a_dst"], m["w5a_src"], tm.TM_RED_MAX, s)
         elif kind == "ring":
             n = box_count(h.r5b_a)
             k = max(1, int(n * fraction))
@@ -490,7 +524,7 @@ def select_ops(h, spec):
     ops = op_table(h)
     if spec:
         keep = set(spec.split(","))
-        ops = [o for o in ops if o[0] in keep]
+        ops = [o for o in ops + extra_ops(h) if o[0] in keep]
     return ops
 
 
@@ -572,6 +606,8 @@ def main():
     dom_name, dom_bytes = dom
     dom_ms = statistics.mean(per[dom_name])
     achieved = dom_bytes / dom_ms / 1e6
+    if any(n.startswith("w5c") for n, _ in ops):
+        args.e2e_steps = 0  # the widened ops have no end-to-end leg
     if args.e2e_steps > 0:
         e2e_ms, bi, bo = e2e_run(g, h, ops, args.e2e_steps)
         e2e = {"value": world * step_bytes / (e2e_ms * 1e-3) / GB, "unit": "GB/s",
@@ -587,7 +623,7 @@ def main():
         cores = cpu_cores()
         frac = calibrated_fraction(h, ops, cores, target_s=2.0)
         spent, covered = oracle_sample(h, ops, frac, cores)
-        cpu = {"value": covered / spent / GB, "unit": "GB/s", "cores": cores, "kind": "oracle",
+        cpu = None if covered == 0 else {"value": covered / spent / GB, "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"first {frac:.2%} of the boxes of every op ({covered} algorithmic "
                          f"bytes, {spent:.1f} s on {cores} threads)"}
     line = {

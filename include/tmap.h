@@ -180,6 +180,18 @@ int tiled_roundtrip(const tm_desc* dst, const int32_t* coords, size_t nbox, cons
  *   vector path (one IEEE add per element, same result). */
 int tile_reduce_add(const tm_desc* dst, const tm_desc* src, void* stream);
 
+/* tile_reduce -- dst = op(dst, src) over the whole box grid, one combine per in-bounds element
+ *   ([Book-TMA] §"TMA reduce，把“搬运”和“归约”合并": the write-back combines each element with the
+ *   value in global memory, "add, min and the like").  Types TM_F32, TM_F16, TM_BF16, TM_U32,
+ *   TM_S32 (else TM_EUNSUPPORTED); dst and src of one type with equal dims, box and swizzle (else
+ *   TM_EINVAL); they must not overlap.  Semantics: float add = the exact sum rounded to nearest,
+ *   ties to even, in the element type (a reading: the pages fix no rounding); min / max = the
+ *   smaller / larger value (dst kept on a tie); u32 / s32 add wraps modulo 2^32.  Add on every type
+ *   and min / max on u32 / s32 use the bulk tensor reduce; float min / max, and maps the tensor
+ *   store cannot take, run element-wise on the vector path (same results). */
+typedef enum tm_redop { TM_RED_ADD = 0, TM_RED_MIN = 1, TM_RED_MAX = 2 } tm_redop;
+int tile_reduce(const tm_desc* dst, const tm_desc* src, tm_redop op, void* stream);
+
 /* stream_tiles -- a `stages`-deep producer/consumer ring ([MLSys-TMA] §"把 TMA 放进 pipeline"):
  *   one elected producer thread fills stage s with tile t of A and tile t of B (one mbarrier,
  *   expect_tx = 2 * box_bytes), consumer warps read the stage through the swizzle and release it.

@@ -127,6 +127,43 @@ def w5b_tensors(m: int = 8192, k: int = 4096, n: int = 8192, seed_a: int = SEEDS
     return normal_bf16((m, k), seed_a), normal_bf16((k, n), seed_b)
 
 
+def reduce_operands(kind: str, rows: int, cols: int, seed: int):
+    """Destination and source bit patterns (rows x cols) for the general reduce, kind one of
+    f32, f16, bf16 (normal(0, 1) values, then no zeros and no pair whose exact sum is a nonzero
+    subnormal), u32, s32 (uniform 32-bit patterns)."""
+    rng = np.random.default_rng(seed)
+    if kind in ("u32", "s32"):
+        d = rng.integers(0, 1 << 32, size=(rows, cols), dtype=np.uint64).astype(np.uint32)
+        s = rng.integers(0, 1 << 32, size=(rows, cols), dtype=np.uint64).astype(np.uint32)
+        return (d, s) if kind == "u32" else (d.view(np.int32), s.view(np.int32))
+
+    def draw(n):
+        v = rng.standard_normal(n).astype(np.float32)
+        if kind == "f32":
+            return v.view(np.uint32)
+        if kind == "f16":
+            return v.astype(np.float16).view(np.uint16)
+        return f32_to_bf16_bits(v)
+
+    def value(bits):
+        if kind == "f32":
+            return bits.view(np.float32).astype(np.float64)
+        if kind == "f16":
+            return bits.view(np.float16).astype(np.float64)
+        return (bits.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+
+    tiny = {"f32": 2.0 ** -126, "f16": 2.0 ** -14, "bf16": 2.0 ** -126}[kind]
+    d, s = draw(rows * cols), draw(rows * cols)
+    while True:
+        vd, vs = value(d), value(s)
+        tot = vd + vs
+        bad = (vd == 0) | (vs == 0) | ((np.abs(tot) < tiny) & (tot != 0))
+        if not bad.any():
+            return d.reshape(rows, cols), s.reshape(rows, cols)
+        n = int(bad.sum())
+        d[bad], s[bad] = draw(n), draw(n)
+
+
 # Map recipes, dims innermost first: (dims, byte strides of dims 1.., box, swizzle span)
 def w3_map(rows: int = 8192, cols: int = 8192, span: int = 128):
     return dict(dims=[cols, rows], strides=[cols * 2], box=[64, 128], span=span, esize=2)
