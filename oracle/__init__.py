@@ -29,11 +29,12 @@ class _OrcMap(ctypes.Structure):
         ("esize", ctypes.c_uint32),
         ("rank", ctypes.c_uint32),
         ("span", ctypes.c_uint32),
-        ("reserved", ctypes.c_uint32),
+        ("fill", ctypes.c_uint32),
         ("base", ctypes.c_void_p),
         ("dim", ctypes.c_uint64 * 5),
         ("stride", ctypes.c_int64 * 5),
         ("box", ctypes.c_uint32 * 5),
+        ("estride", ctypes.c_uint32 * 5),
     ]
 
 
@@ -58,6 +59,8 @@ def lib():
         L.orc_map_check.argtypes = [P(_OrcMap)]
         L.orc_swz.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
         L.orc_swz.restype = ctypes.c_uint64
+        L.orc_extent.argtypes = [P(_OrcMap), ctypes.c_uint32]
+        L.orc_extent.restype = ctypes.c_uint32
         L.orc_box_bytes.argtypes = [P(_OrcMap)]
         L.orc_box_bytes.restype = ctypes.c_uint64
         L.orc_num_boxes.argtypes = [P(_OrcMap)]
@@ -101,26 +104,35 @@ def _ptr(a: np.ndarray) -> int:
     return a.ctypes.data
 
 
+# out-of-bounds fill (values of the C enum): zero bytes, or the NaN of a float format
+FILL_ZERO, FILL_NAN_F16, FILL_NAN_BF16, FILL_NAN_F32, FILL_NAN_F64 = 0, 1, 2, 3, 4
+
+
 class Map:
-    """A tensor map over a host numpy buffer, as the oracle sees it."""
+    """A tensor map over a host numpy buffer, as the oracle sees it.  `estrides` are the
+    elementStrides (default all 1); `fill` one of the FILL_* values."""
 
     def __init__(self, buf: np.ndarray, esize: int, dims, strides, box, span: int = 0,
-                 offset: int = 0):
+                 offset: int = 0, estrides=None, fill: int = FILL_ZERO):
         rank = len(dims)
-        if not (1 <= rank <= 5) or len(box) != rank or len(strides) != rank - 1:
-            raise ValueError("rank / dims / strides / box lengths disagree")
+        estrides = [1] * rank if estrides is None else list(estrides)
+        if not (1 <= rank <= 5) or len(box) != rank or len(strides) != rank - 1 \
+                or len(estrides) != rank:
+            raise ValueError("rank / dims / strides / box / estrides lengths disagree")
         if not buf.flags.c_contiguous:
             raise ValueError("buffer must be contiguous")
         self.buf = buf  # keep alive
         self.esize, self.dims, self.box, self.span = esize, list(dims), list(box), span
+        self.estrides, self.fill = estrides, fill
         self.strides = [esize] + list(strides)
         s = _OrcMap()
-        s.esize, s.rank, s.span = esize, rank, span
+        s.esize, s.rank, s.span, s.fill = esize, rank, span, fill
         s.base = _ptr(buf) + offset
         for i in range(5):
             s.dim[i] = dims[i] if i < rank else 1
             s.stride[i] = self.strides[i] if i < rank else 0
             s.box[i] = box[i] if i < rank else 1
+            s.estride[i] = estrides[i] if i < rank else 1
         self.c = s
         rc = lib().orc_map_check(ctypes.byref(s))
         if rc != 0:
@@ -129,6 +141,10 @@ class Map:
     @property
     def rank(self) -> int:
         return len(self.dims)
+
+    def extent(self, i: int) -> int:
+        """Image elements along dim i: ceil(box[i] / estride[i])."""
+        return int(lib().orc_extent(ctypes.byref(self.c), i))
 
     @property
     def box_bytes(self) -> int:

@@ -50,21 +50,36 @@ int orc_map_check(const orc_map* m)
     if (m->esize != 1 && m->esize != 2 && m->esize != 4 && m->esize != 8) return 2;
     for (uint32_t i = 0; i < m->rank; i++) {
         if (m->box[i] < 1) return 3;
+        if (m->estride[i] < 1 || m->estride[i] > 8) return 6;
     }
     if (m->span != 0 && m->span != 32 && m->span != 64 && m->span != 128) return 4;
     /* [MLSys-TMA] §"用 3D TMA 搬运多个 swizzle atoms": the inner box row may not exceed the atom
      * width; §"128-byte swizzle 的分组要求": an N-byte atom needs a row of at least N bytes.
-     * Together: with a swizzle the inner box row is exactly `span` bytes. */
-    if (m->span != 0 && (uint64_t)m->box[0] * m->esize != m->span) return 5;
+     * Together: with a swizzle the inner box row is exactly `span` bytes, and (so that the image
+     * row is that row) the innermost element stride is 1. */
+    if (m->span != 0 && ((uint64_t)m->box[0] * m->esize != m->span || m->estride[0] != 1)) return 5;
+    if (m->fill > ORC_FILL_NAN_F64) return 7;
+    if ((m->fill == ORC_FILL_NAN_F16 || m->fill == ORC_FILL_NAN_BF16) && m->esize != 2) return 7;
+    if (m->fill == ORC_FILL_NAN_F32 && m->esize != 4) return 7;
+    if (m->fill == ORC_FILL_NAN_F64 && m->esize != 8) return 7;
     return 0;
 }
 
-static uint32_t box_of(const orc_map* m, uint32_t i) { return i < m->rank ? m->box[i] : 1u; }
+/* [Book-TMA] §"Tensor descriptor：CUtensorMap": elementStrides is the step, in elements, between
+ * the elements taken along each dim when the box is written to shared memory.  Read here as: of
+ * the box's box[i] elements along dim i, every estride[i]-th one starting at the box's first is
+ * taken, so the image holds ceil(box[i] / estride[i]) of them, packed. */
+uint32_t orc_extent(const orc_map* m, uint32_t i)
+{
+    return i < m->rank ? (m->box[i] + m->estride[i] - 1) / m->estride[i] : 1u;
+}
+
+static int64_t step_of(const orc_map* m, uint32_t i) { return i < m->rank ? m->estride[i] : 1; }
 
 uint64_t orc_box_bytes(const orc_map* m)
 {
     uint64_t n = m->esize;
-    for (uint32_t i = 0; i < m->rank; i++) n *= m->box[i];
+    for (uint32_t i = 0; i < m->rank; i++) n *= orc_extent(m, i);
     return n;
 }
 
@@ -107,24 +122,39 @@ static uint8_t* element_address(const orc_map* m, const int64_t* g)
     return m->base + off;
 }
 
-/* Visits every element of the box starting at s, dim 0 fastest.  For each, `g` is its global
- * coordinate and `lin` its element index inside the (unswizzled) image. */
+/* Visits every element of the image of the box starting at s, dim 0 fastest.  For each, `g` is
+ * the global coordinate it comes from and `lin` its element index inside the (unswizzled) image. */
 typedef void (*element_fn)(const orc_map* m, const int64_t* g, uint64_t lin, void* ctx);
 
 static void for_each_element(const orc_map* m, const int32_t* s, element_fn fn, void* ctx)
 {
     int64_t g[5] = {0, 0, 0, 0, 0};
     uint64_t lin = 0;
-    for (uint32_t e4 = 0; e4 < box_of(m, 4); e4++)
-    for (uint32_t e3 = 0; e3 < box_of(m, 3); e3++)
-    for (uint32_t e2 = 0; e2 < box_of(m, 2); e2++)
-    for (uint32_t e1 = 0; e1 < box_of(m, 1); e1++)
-    for (uint32_t e0 = 0; e0 < box_of(m, 0); e0++) {
+    for (uint32_t e4 = 0; e4 < orc_extent(m, 4); e4++)
+    for (uint32_t e3 = 0; e3 < orc_extent(m, 3); e3++)
+    for (uint32_t e2 = 0; e2 < orc_extent(m, 2); e2++)
+    for (uint32_t e1 = 0; e1 < orc_extent(m, 1); e1++)
+    for (uint32_t e0 = 0; e0 < orc_extent(m, 0); e0++) {
         uint32_t e[5] = {e0, e1, e2, e3, e4};
-        for (uint32_t i = 0; i < 5; i++) g[i] = (i < m->rank ? (int64_t)s[i] : 0) + e[i];
+        for (uint32_t i = 0; i < 5; i++)
+            g[i] = (i < m->rank ? (int64_t)s[i] : 0) + (int64_t)e[i] * step_of(m, i);
         fn(m, g, lin, ctx);
         lin++;
     }
+}
+
+/* Byte k (little-endian) of the fill element. */
+static uint8_t fill_byte(const orc_map* m, uint32_t k)
+{
+    uint64_t v;
+    switch (m->fill) {
+        case ORC_FILL_NAN_F16: v = 0x7E00u; break;
+        case ORC_FILL_NAN_BF16: v = 0x7FC0u; break;
+        case ORC_FILL_NAN_F32: v = 0x7FC00000u; break;
+        case ORC_FILL_NAN_F64: v = 0x7FF8000000000000ull; break;
+        default: v = 0; break;
+    }
+    return (uint8_t)(v >> (8 * k));
 }
 
 static void image_one(const orc_map* m, const int64_t* g, uint64_t lin, void* ctx)
@@ -133,7 +163,7 @@ static void image_one(const orc_map* m, const int64_t* g, uint64_t lin, void* ct
     int inb = in_bounds(m, g);
     const uint8_t* src = inb ? element_address(m, g) : 0;
     for (uint32_t k = 0; k < m->esize; k++) {
-        img[orc_swz(lin * m->esize + k, m->span)] = inb ? src[k] : 0;
+        img[orc_swz(lin * m->esize + k, m->span)] = inb ? src[k] : fill_byte(m, k);
     }
 }
 
@@ -407,7 +437,8 @@ void orc_stream_checksums(const orc_map* a, const orc_map* b, uint64_t t0, uint6
             orc_image(m, s, img);
             float cs;
             uint64_t bits;
-            orc_tile_checksum(img, m->box[1], m->box[0] * m->esize, m->span, &cs, &bits);
+            orc_tile_checksum(img, orc_extent(m, 1), orc_extent(m, 0) * m->esize, m->span, &cs,
+                              &bits);
             if (w == 0) {
                 cs_a[t] = cs;
                 bits_a[t] = bits;

@@ -28,6 +28,13 @@
  *   orc_image / orc_store ... pinned: NONE mode equals numpy strided slicing of a zero-padded
  *                             tensor; 128B mode equals the page's sector-XOR-row rule applied to
  *                             that slice; store(image(x)) restores x with sentinels intact.
+ *   elementStrides .......... pinned: the image equals numpy slicing with step estride[i] of the
+ *                             zero-padded tensor ([Book-TMA] §"Tensor descriptor：CUtensorMap":
+ *                             the step between elements along each dim, counted in elements);
+ *                             the store writes exactly those positions.  Reading: the image keeps
+ *                             ceil(box / estride) elements along each dim, packed.
+ *   NaN fill ................ pinned: out-of-bounds image elements are NaN in the element's float
+ *                             format (numpy isnan), in-bounds ones unchanged, stores unaffected.
  *   orc_reduce_add_f32 ...... pinned: numpy float32 addition (IEEE binary32, round to nearest).
  *   orc_combine ............. pinned: f16 add against numpy float16 of the (exact) double sum;
  *                             bf16 add against an exact rational sum rounded half-to-even in
@@ -55,30 +62,42 @@ typedef struct orc_map {
     uint32_t esize;     /* element size in bytes (1, 2, 4 or 8)                              */
     uint32_t rank;      /* 1..5                                                              */
     uint32_t span;      /* swizzle span in bytes: 0 = none, 32, 64 or 128                    */
-    uint32_t reserved;
+    uint32_t fill;      /* out-of-bounds fill: ORC_FILL_ZERO or the NaN of a float format    */
     uint8_t* base;      /* host address of element (0, ..., 0)                               */
     uint64_t dim[5];    /* globalDim, innermost first                                        */
     int64_t  stride[5]; /* byte distance between neighbours along dim i; stride[0] = esize   */
     uint32_t box[5];    /* boxDim, innermost first                                           */
+    uint32_t estride[5];/* elementStrides, in elements (1..8)                                */
 } orc_map;
 
-/* 0 if the map is one the oracle defines (rank 1..5, box >= 1, span in {0,32,64,128}, and with a
- * span the inner box row is exactly `span` bytes), otherwise a nonzero code. */
+/* Out-of-bounds fill ([H200-TMA] §02: the hardware fills out-of-bounds elements with 0 or NaN).
+ * The pages name no NaN bit pattern; the oracle writes the quiet NaN with only the leading
+ * fraction bit set (f16 0x7E00, bf16 0x7FC0, f32 0x7FC00000, f64 0x7FF8000000000000), and the
+ * tests accept any NaN there. */
+enum { ORC_FILL_ZERO = 0, ORC_FILL_NAN_F16 = 1, ORC_FILL_NAN_BF16 = 2, ORC_FILL_NAN_F32 = 3,
+       ORC_FILL_NAN_F64 = 4 };
+
+/* 0 if the map is one the oracle defines (rank 1..5, box >= 1, elementStrides 1..8, span in
+ * {0,32,64,128}, with a span elementStrides[0] = 1 and the inner box row exactly `span` bytes, a
+ * NaN fill only in the format of the element size), otherwise a nonzero code. */
 int orc_map_check(const orc_map* m);
 
 /* Swizzled position of byte offset `off` of an image whose rows are `span` bytes wide. */
 uint64_t orc_swz(uint64_t off, uint32_t span);
 
+/* Image extent along dim i: ceil(box[i] / estride[i]) elements.  Image bytes: esize * prod. */
+uint32_t orc_extent(const orc_map* m, uint32_t i);
 uint64_t orc_box_bytes(const orc_map* m);
 uint64_t orc_num_boxes(const orc_map* m);
 /* Start coordinates of box number `b` of the box grid (dim 0 fastest): s[i] = k[i] * box[i]. */
 void orc_box_start(const orc_map* m, uint64_t b, int32_t* s);
 
-/* Shared-memory image of the box starting at s[0..rank-1]: every element e of the box is stored at
- * byte swz(lin(e) * esize); out-of-bounds elements are zero bytes. */
+/* Shared-memory image of the box starting at s[0..rank-1]: image element e (e[i] < extent i) is
+ * the tensor element at global coordinate g[i] = s[i] + e[i] * estride[i], stored at byte
+ * swz(lin(e) * esize); out-of-bounds elements are the fill (zero bytes or the NaN pattern). */
 void orc_image(const orc_map* m, const int32_t* s, uint8_t* img);
-/* Writes each in-bounds element of the box starting at s from the image back to global memory;
- * out-of-bounds elements are not written. */
+/* Writes each in-bounds element of the box starting at s from the image back to global memory
+ * (image element e to coordinate s + e * estride); out-of-bounds elements are not written. */
 void orc_store(const orc_map* m, const int32_t* s, const uint8_t* img);
 /* dst(element) = fl32(dst(element) + image(element)) for each in-bounds element of the box. */
 void orc_reduce_add_f32(const orc_map* dst, const int32_t* s, const uint8_t* img);

@@ -91,3 +91,18 @@ def checksum_reference(logical_rows: np.ndarray):
         sums = (sums[0::2] + sums[1::2]).astype(np.float32)
     bits = int(logical_rows.astype(np.uint64).sum())
     return np.float32(sums[0]), bits
+
+
+def box_stepped(view: np.ndarray, start, box, estrides, fill=0):
+    """Image elements of a box with element strides, outermost first: along dim i the elements
+    start[i], start[i] + estrides[i], ... below start[i] + box[i], taken with numpy basic slicing
+    (step estrides[i]) of the tensor padded by `fill` on every side; also returns the in-bounds
+    mask of the same shape."""
+    rank = len(box)
+    pad = [(max(box[i], 1) + abs(start[i]), max(box[i], 1) + abs(start[i]))
+           for i in reversed(range(rank))]
+    padded = np.pad(np.ascontiguousarray(view), pad, constant_values=fill)
+    inside = np.pad(np.ones(view.shape, dtype=bool), pad, constant_values=False)
+    sl = tuple(slice(start[i] + pad[rank - 1 - i][0], start[i] + pad[rank - 1 - i][0] + box[i],
+                     estrides[i]) for i in reversed(range(rank)))
+    return padded[sl].copy(), inside[sl].copy()

@@ -19,10 +19,19 @@ MUTANTS = {
     "oob_upper_off_by_one": ("(uint64_t)g[i] >= m->dim[i]", "(uint64_t)g[i] > m->dim[i]"),
     "oob_negative_dropped": ("if (g[i] < 0 || (uint64_t)g[i]", "if ((uint64_t)g[i] + 0 == 0 && (uint64_t)g[i]"),
     "image_axes_transposed": (
-        "    for (uint32_t e1 = 0; e1 < box_of(m, 1); e1++)\n"
-        "    for (uint32_t e0 = 0; e0 < box_of(m, 0); e0++) {",
-        "    for (uint32_t e0 = 0; e0 < box_of(m, 0); e0++)\n"
-        "    for (uint32_t e1 = 0; e1 < box_of(m, 1); e1++) {"),
+        "    for (uint32_t e1 = 0; e1 < orc_extent(m, 1); e1++)\n"
+        "    for (uint32_t e0 = 0; e0 < orc_extent(m, 0); e0++) {",
+        "    for (uint32_t e0 = 0; e0 < orc_extent(m, 0); e0++)\n"
+        "    for (uint32_t e1 = 0; e1 < orc_extent(m, 1); e1++) {"),
+    "element_stride_ignored": ("(int64_t)e[i] * step_of(m, i);", "(int64_t)e[i];"),
+    "element_stride_in_bytes": ("(int64_t)e[i] * step_of(m, i);",
+                                "(int64_t)e[i] * step_of(m, i) / (int64_t)m->esize;"),
+    "extent_floor_not_ceil": ("(m->box[i] + m->estride[i] - 1) / m->estride[i]",
+                              "m->box[i] / m->estride[i] + (m->box[i] < m->estride[i])"),
+    "f32_fill_is_infinity": ("case ORC_FILL_NAN_F32: v = 0x7FC00000u;",
+                             "case ORC_FILL_NAN_F32: v = 0x7F800000u;"),
+    "fill_bytes_reversed": ("return (uint8_t)(v >> (8 * k));",
+                            "return (uint8_t)(v >> (8 * (m->esize - 1 - k)));"),
     "grid_floor_not_ceil": ("return (m->dim[i] + m->box[i] - 1) / m->box[i];",
                             "return m->dim[i] / m->box[i] + (m->dim[i] < m->box[i]);"),
     "stride_index_transposed": ("off += g[i] * m->stride[i];",
@@ -60,6 +69,7 @@ def test_pins_reject_mutant(name, tmp_path):
     env = dict(os.environ, TMAP_ORACLE_LIB=str(lib))
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_reduce_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_reduce_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_stride_fill_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
