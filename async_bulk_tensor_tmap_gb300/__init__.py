@@ -32,7 +32,7 @@ __all__ = [
     "TM_ECUDA", "TM_ETIMEOUT", "TM_U8", "TM_U16", "TM_U32", "TM_S32", "TM_U64", "TM_S64",
     "TM_F16", "TM_F32", "TM_F64", "TM_BF16", "TM_SWIZZLE_NONE", "TM_SWIZZLE_32B",
     "TM_SWIZZLE_64B", "TM_SWIZZLE_128B", "TM_OOB_ZERO", "TM_OOB_NAN", "TM_PATH_TMA",
-    "TM_PATH_FALLBACK", "TM_WHY_STRIDE", "TM_WHY_BASE", "TM_WHY_DRIVER", "TM_WHY_FORCED",
+    "TM_PATH_FALLBACK", "TM_WHY_STRIDE", "TM_WHY_BASE", "TM_WHY_DRIVER", "TM_WHY_FORCED", "TM_WHY_STEP0",
 ]
 
 TM_OK, TM_EINVAL, TM_EALIGN, TM_ERANGE, TM_EUNSUPPORTED, TM_ECUDA, TM_ETIMEOUT = range(7)
@@ -41,7 +41,7 @@ TM_SWIZZLE_NONE, TM_SWIZZLE_32B, TM_SWIZZLE_64B, TM_SWIZZLE_128B = range(4)
 TM_OOB_ZERO, TM_OOB_NAN = 0, 1
 TM_PATH_TMA, TM_PATH_FALLBACK = 1, 2
 TM_RED_ADD, TM_RED_MIN, TM_RED_MAX = 0, 1, 2
-TM_WHY_STRIDE, TM_WHY_BASE, TM_WHY_DRIVER, TM_WHY_FORCED = 1, 2, 4, 8
+TM_WHY_STRIDE, TM_WHY_BASE, TM_WHY_DRIVER, TM_WHY_FORCED, TM_WHY_STEP0 = 1, 2, 4, 8, 16
 DESC_SIZE = 384
 TM_NOALLOC_MAX_BOXES = 16384
 

@@ -49,7 +49,8 @@ __device__ __forceinline__ uint32_t word_mask(int lo, int hi, int t)
 }
 
 // Image row `row` of a box -> global byte address of its element 0 (relative to base, may be
-// negative) and whether every outer coordinate (dims 1..) is inside the tensor.
+// negative) and whether every outer coordinate (dims 1..) is inside the tensor.  Image row
+// coordinate e[i] (0 <= e[i] < ibox[i]) comes from tensor coordinate c[i] + e[i] * estride[i].
 struct RowPos {
     int64_t off;
     bool ok;
@@ -63,15 +64,93 @@ __device__ __forceinline__ RowPos row_position(const FbArgs& a, const int32_t* c
 #pragma unroll
     for (int i = 1; i < 5; i++) {
         if (i < (int)a.walk.rank) {
-            const uint32_t bi = a.walk.box[i];
+            const uint32_t bi = a.ibox[i];
             const uint32_t q = r / bi;
-            const int64_t g = (int64_t)c[i] + (int64_t)(r - q * bi);
+            const int64_t g = (int64_t)c[i] + (int64_t)(r - q * bi) * a.estride[i];
             r = q;
             p.ok = p.ok && g >= 0 && (uint64_t)g < a.dim[i];
             p.off += g * stride[i];
         }
     }
     return p;
+}
+
+// In-bounds part of an image row of a box whose dim-0 start is c0: image elements [i_lo, i_hi)
+// (element k comes from tensor coordinate c0 + k * estride[0]), and the bytes [g_lo, g_hi) of
+// the tensor row segment under the image row, counted from element c0, that hold them.
+struct XRange {
+    int i_lo, i_hi, g_lo, g_hi;
+};
+
+__device__ __forceinline__ XRange x_range(const FbArgs& a, int32_t c0)
+{
+    const int64_t step = a.estride[0], n0 = a.ibox[0];
+    const int64_t lo = max(-(int64_t)c0, (int64_t)0);
+    const int64_t hi = max((int64_t)a.dim[0] - (int64_t)c0, (int64_t)0);
+    XRange x;
+    x.i_lo = (int)min((lo + step - 1) / step, n0);
+    x.i_hi = (int)min((hi + step - 1) / step, n0);
+    const int es = (int)a.esize;
+    x.g_lo = x.i_lo * (int)step * es;
+    x.g_hi = x.i_hi > x.i_lo ? ((x.i_hi - 1) * (int)step + 1) * es : x.g_lo;
+    return x;
+}
+
+// 16 bytes of the fill element, repeated (zero, or the NaN pattern of a TM_OOB_NAN map).
+__device__ __forceinline__ uint4 fill_vector(const FbArgs& a)
+{
+    if (!a.fill_nan) return make_uint4(0, 0, 0, 0);
+    uint32_t lo, hi;
+    if (a.esize == 2) {
+        lo = hi = (uint32_t)(a.fill & 0xffffu) * 0x10001u;
+    } else if (a.esize == 4) {
+        lo = hi = (uint32_t)a.fill;
+    } else {
+        lo = (uint32_t)a.fill;
+        hi = (uint32_t)(a.fill >> 32);
+    }
+    return make_uint4(lo, hi, lo, hi);
+}
+
+// Chunk j (16 bytes, 16 / sizeof(E) elements) of an image row whose dim-0 elements lie `step`
+// elements apart in the staged row segment `row`; elements outside [i_lo, i_hi) are the fill.
+template <typename E>
+__device__ __forceinline__ uint4 gather_chunk(const uint8_t* row, int j, const XRange& x, int step,
+                                              const uint4& fill)
+{
+    constexpr int n = 16 / (int)sizeof(E);
+    union {
+        uint4 v;
+        E e[n];
+    } u;
+    u.v = fill;
+#pragma unroll
+    for (int t = 0; t < n; t++) {
+        const int k = j * n + t;
+        if (k >= x.i_lo && k < x.i_hi)
+            u.e[t] = *reinterpret_cast<const E*>(row + (size_t)k * step * sizeof(E));
+    }
+    return u.v;
+}
+
+// Writes the in-bounds elements of chunk j of an image row to the tensor row at `row` (the
+// address of the box's dim-0 start), element k at k * step elements.
+template <typename E>
+__device__ __forceinline__ void scatter_chunk(uint8_t* row, const uint4& v, int j, const XRange& x,
+                                              int step)
+{
+    constexpr int n = 16 / (int)sizeof(E);
+    union {
+        uint4 v;
+        E e[n];
+    } u;
+    u.v = v;
+#pragma unroll
+    for (int t = 0; t < n; t++) {
+        const int k = j * n + t;
+        if (k >= x.i_lo && k < x.i_hi)
+            *reinterpret_cast<E*>(row + (size_t)k * step * sizeof(E)) = u.e[t];
+    }
 }
 
 // In-bounds element range [k0, k1) of chunk j of a row whose element 0 has dim-0 coordinate x0.
@@ -120,12 +199,16 @@ __device__ __forceinline__ void cp_async_wait_all()
 // the staged windows (two aligned shared loads and a word select), zeroes out-of-bounds elements,
 // and stores the chunk to its swizzled place in the global image with one 16-byte store (the
 // swizzle only permutes chunks inside a 128-byte row, so a warp's stores stay coalesced).
+//
+// kStep0: the map's elementStrides[0] is not 1.  The staged windows then cover the box's whole
+// tensor row segment (box[0] elements) and each chunk gathers its elements `estride[0]` apart.
+template <bool kStep0>
 __global__ void __launch_bounds__(kThreads) k_fb_copy(const __grid_constant__ FbArgs a)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    const uint32_t cpr = a.inner_bytes >> 4;      // 16-byte chunks per row
+    const uint32_t cpr = a.inner_bytes >> 4;      // 16-byte chunks per image row
     const uint32_t cpr_shift = (cpr & (cpr - 1)) == 0 ? (uint32_t)(__ffs(cpr) - 1) : 32u;
-    const uint32_t wpr = cpr + 1;                 // staged windows per row
+    const uint32_t wpr = (a.gspan0 >> 4) + 1;     // staged windows per row
     const uint32_t RB = a.block_rows;
     uint8_t* const stg = smem_raw;
     const uint32_t stg_u32 = smem_u32(stg);
@@ -135,19 +218,17 @@ __global__ void __launch_bounds__(kThreads) k_fb_copy(const __grid_constant__ Fb
     if (a.walk.nbox <= first) return;
     const uint64_t n_local = (a.walk.nbox - 1 - first) / gridDim.x + 1;
     const int64_t gbase = (int64_t)a.base;
-    const int64_t box0 = a.walk.box[0];
-    const int64_t dim0 = (int64_t)a.dim[0];
     const int es = (int)a.esize;
     const int inner = (int)a.inner_bytes;
+    const uint4 fillv = fill_vector(a);
 
     for (uint64_t i = 0; i < n_local; i++) {
         const uint64_t b = first + i * gridDim.x;
         int32_t c[5];
         box_start(a.walk, b, c);
-        // In-bounds bytes of every image row of this box (the same for all rows).
-        const int64_t e_lo = min(max(-(int64_t)c[0], (int64_t)0), box0);
-        const int64_t e_hi = min(max(dim0 - (int64_t)c[0], (int64_t)0), box0);
-        const int lo_byte = (int)e_lo * es, hi_byte = (int)e_hi * es;
+        // In-bounds part of every image row of this box (the same for all rows).
+        const XRange x = x_range(a, c[0]);
+        const int lo_byte = x.i_lo * es, hi_byte = x.i_hi * es;
         const bool whole_x = lo_byte == 0 && hi_byte == inner;
         uint8_t* const img = reinterpret_cast<uint8_t*>(a.images + b * a.box_bytes);
 
@@ -156,7 +237,7 @@ __global__ void __launch_bounds__(kThreads) k_fb_copy(const __grid_constant__ Fb
             __syncthreads();  // the previous block's windows and table are no longer read
             for (uint32_t r = threadIdx.x; r < nr; r += kThreads) {
                 const RowPos p = row_position(a, c, r0 + r, a.stride);
-                tab[r] = (p.ok && lo_byte < hi_byte) ? p.off : kRowOutside;
+                tab[r] = (p.ok && x.i_lo < x.i_hi) ? p.off : kRowOutside;
             }
             __syncthreads();
             const uint32_t nwin = nr * wpr;
@@ -169,7 +250,7 @@ __global__ void __launch_bounds__(kThreads) k_fb_copy(const __grid_constant__ Fb
                     const int64_t row_addr = gbase + off;
                     const int d = (int)(row_addr & 15);
                     const int wlo = 16 * (int)k - d;  // window k holds row bytes [wlo, wlo + 16)
-                    if (wlo + 16 > lo_byte && wlo < hi_byte)
+                    if (wlo + 16 > x.g_lo && wlo < x.g_hi)
                         cp_async16(stg_u32 + w * 16, (uint64_t)(row_addr - d + 16 * (int64_t)k));
                 }
                 r += dr;
@@ -186,8 +267,15 @@ __global__ void __launch_bounds__(kThreads) k_fb_copy(const __grid_constant__ Fb
                 uint32_t r, j;
                 split_item(it, cpr, cpr_shift, r, j);
                 const int64_t off = tab[r];
-                uint4 out = make_uint4(0, 0, 0, 0);
-                if (off != kRowOutside) {
+                uint4 out = fillv;
+                if (kStep0 && off != kRowOutside) {
+                    const uint8_t* row = stg + r * wpr * 16 + ((gbase + off) & 15);
+                    const int step = (int)a.estride[0];
+                    out = es == 1   ? gather_chunk<uint8_t>(row, (int)j, x, step, fillv)
+                          : es == 2 ? gather_chunk<uint16_t>(row, (int)j, x, step, fillv)
+                          : es == 4 ? gather_chunk<uint32_t>(row, (int)j, x, step, fillv)
+                                    : gather_chunk<unsigned long long>(row, (int)j, x, step, fillv);
+                } else if (off != kRowOutside) {
                     const uint32_t d = (uint32_t)((gbase + off) & 15);
                     const uint4* src = reinterpret_cast<const uint4*>(stg + (r * wpr + j) * 16);
                     const uint4 lo = src[0];
@@ -210,12 +298,16 @@ __global__ void __launch_bounds__(kThreads) k_fb_copy(const __grid_constant__ Fb
                             out = make_uint4(o[0], o[1], o[2], o[3]);
                         }
                     }
-                    if (!whole_x) {  // zero the elements outside the tensor along dim 0
+                    if (!whole_x) {  // fill the elements outside the tensor along dim 0
                         const int blo = lo_byte - 16 * (int)j, bhi = hi_byte - 16 * (int)j;
-                        out.x &= word_mask(blo, bhi, 0);
-                        out.y &= word_mask(blo, bhi, 1);
-                        out.z &= word_mask(blo, bhi, 2);
-                        out.w &= word_mask(blo, bhi, 3);
+                        uint32_t m = word_mask(blo, bhi, 0);
+                        out.x = (out.x & m) | (fillv.x & ~m);
+                        m = word_mask(blo, bhi, 1);
+                        out.y = (out.y & m) | (fillv.y & ~m);
+                        m = word_mask(blo, bhi, 2);
+                        out.z = (out.z & m) | (fillv.z & ~m);
+                        m = word_mask(blo, bhi, 3);
+                        out.w = (out.w & m) | (fillv.w & ~m);
                     }
                 }
                 *reinterpret_cast<uint4*>(
@@ -258,6 +350,9 @@ __device__ __forceinline__ void store_chunk_bytes(uint8_t* dst, const uint4& v, 
 // loads are coalesced; each thread keeps 4 in flight, then writes each chunk's in-bounds bytes
 // with the widest stores the destination alignment allows.  Only the row table lives in shared
 // memory; no wait on another thread's copy is involved.
+// kStep0: elementStrides[0] is not 1; each chunk's in-bounds elements are written one by one,
+// `estride[0]` elements apart.
+template <bool kStep0>
 __global__ void __launch_bounds__(kThreads, 6) k_fb_store(const __grid_constant__ FbArgs a)
 {
     extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -270,8 +365,6 @@ __global__ void __launch_bounds__(kThreads, 6) k_fb_store(const __grid_constant_
     const uint32_t cpr = a.inner_bytes >> 4;
     const uint32_t cpr_shift = (cpr & (cpr - 1)) == 0 ? (uint32_t)(__ffs(cpr) - 1) : 32u;
     const uint32_t RB = a.block_rows;
-    const int64_t box0 = a.walk.box[0];
-    const int64_t dim0 = (int64_t)a.dim[0];
     const int es = (int)a.esize;
     const int inner = (int)a.inner_bytes;
 
@@ -279,9 +372,8 @@ __global__ void __launch_bounds__(kThreads, 6) k_fb_store(const __grid_constant_
         const uint64_t b = first + i * gridDim.x;
         int32_t c[5];
         box_start(a.walk, b, c);
-        const int64_t e_lo = min(max(-(int64_t)c[0], (int64_t)0), box0);
-        const int64_t e_hi = min(max(dim0 - (int64_t)c[0], (int64_t)0), box0);
-        const int lo_byte = (int)e_lo * es, hi_byte = (int)e_hi * es;
+        const XRange x = x_range(a, c[0]);
+        const int lo_byte = x.i_lo * es, hi_byte = x.i_hi * es;
         const bool whole_x = lo_byte == 0 && hi_byte == inner;
         const uint8_t* const img = reinterpret_cast<const uint8_t*>(a.images + b * a.box_bytes);
 
@@ -290,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 6) k_fb_store(const __grid_constant_
             __syncthreads();  // the previous block's table is no longer read
             for (uint32_t r = threadIdx.x; r < nr; r += kThreads) {
                 const RowPos p = row_position(a, c, r0 + r, a.stride);
-                tab[r] = (p.ok && lo_byte < hi_byte) ? p.off : kRowOutside;
+                tab[r] = (p.ok && x.i_lo < x.i_hi) ? p.off : kRowOutside;
             }
             __syncthreads();
             const uint32_t nch = nr * cpr;
@@ -317,6 +409,15 @@ __global__ void __launch_bounds__(kThreads, 6) k_fb_store(const __grid_constant_
                     split_item(item, cpr, cpr_shift, r, j);
                     const int64_t off = tab[r];
                     if (off == kRowOutside) continue;
+                    if (kStep0) {
+                        uint8_t* const row = reinterpret_cast<uint8_t*>(a.base + off);
+                        const int step = (int)a.estride[0];
+                        if (es == 1) scatter_chunk<uint8_t>(row, v[k], (int)j, x, step);
+                        else if (es == 2) scatter_chunk<uint16_t>(row, v[k], (int)j, x, step);
+                        else if (es == 4) scatter_chunk<uint32_t>(row, v[k], (int)j, x, step);
+                        else scatter_chunk<unsigned long long>(row, v[k], (int)j, x, step);
+                        continue;
+                    }
                     const int pos = whole_x ? 0 : max(lo_byte - 16 * (int)j, 0);
                     const int end = whole_x ? 16 : min(hi_byte - 16 * (int)j, 16);
                     if (pos >= end) continue;
@@ -476,19 +577,19 @@ __global__ void __launch_bounds__(kThreads, 3) k_fb_reduce(const __grid_constant
 
 cudaError_t launch_fb_copy(const FbArgs& a, uint32_t grid, size_t smem, cudaStream_t s)
 {
-    cudaError_t e =
-        cudaFuncSetAttribute(k_fb_copy, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    void (*k)(const FbArgs) = a.estride[0] != 1 ? k_fb_copy<true> : k_fb_copy<false>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_fb_copy<<<grid, kThreads, smem, s>>>(a);
+    k<<<grid, kThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_fb_store(const FbArgs& a, uint32_t grid, size_t smem, cudaStream_t s)
 {
-    cudaError_t e =
-        cudaFuncSetAttribute(k_fb_store, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    void (*k)(const FbArgs) = a.estride[0] != 1 ? k_fb_store<true> : k_fb_store<false>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_fb_store<<<grid, kThreads, smem, s>>>(a);
+    k<<<grid, kThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 

@@ -66,20 +66,67 @@ struct FbArgs {
     uint64_t images;
     uint32_t esize;
     uint32_t span;         // swizzle span in bytes, 0 = none
-    uint32_t inner_bytes;  // box[0] * esize
+    uint32_t inner_bytes;  // image row: ibox[0] * esize
     uint32_t box_bytes;
     uint32_t stage_bytes;
     uint32_t rows;         // image rows = box_bytes / inner_bytes
     uint32_t block_rows;   // image rows handled per block (shared-memory row table / staging)
     uint16_t red_type;     // reduce: 0 f32, 1 f16, 2 bf16, 3 u32, 4 s32
     uint16_t red_op;       // reduce: 0 add, 1 min, 2 max
+    uint32_t gspan0;       // box[0] * esize: bytes of the tensor row under one image row
+    uint32_t fill_nan;     // 1: out-of-bounds image elements are `fill`; 0: zero bytes
+    uint64_t fill;         // out-of-bounds element bit pattern (low esize bytes)
+    uint32_t ibox[5];      // image extents ceil(box[i] / estride[i]) (unused dims 1)
+    uint32_t estride[5];   // elementStrides (unused dims 1)
     uint64_t timeout_ns;
     StatusBlock* status;
 };
 
-// Shared memory per image row: the staged copy keeps the aligned 16-byte windows under the row
-// (one more than its chunks) and the row's offset; the store keeps the offset only.
-inline size_t fb_copy_row_bytes(uint32_t inner_bytes) { return (size_t)(inner_bytes / 16 + 1) * 16 + 8; }
+// NaN written for out-of-bounds elements of a map with TM_OOB_NAN on the vector path: the pattern
+// GB300's tensor-map NaN-request fill was measured to write, 0x7FF7 repeated over the element.
+inline uint64_t nan_fill_bits(uint32_t dtype)
+{
+    switch (dtype) {
+        case TM_F16: case TM_BF16: return 0x7ff7ull;
+        case TM_F32: return 0x7ff77ff7ull;
+        case TM_F64: return 0x7ff77ff77ff77ff7ull;
+        default: return 0;
+    }
+}
+
+// Whether every elementStride of the map is 1.
+inline bool unit_steps(const tm_desc* d)
+{
+    for (uint32_t i = 0; i < d->rank; i++)
+        if (d->estride[i] != 1) return false;
+    return true;
+}
+
+// The map's part of the vector kernels' arguments (tensor, image shape, fill).
+inline void fb_from_desc(FbArgs& a, const tm_desc* d)
+{
+    a.base = d->base;
+    for (int i = 0; i < 5; i++) {
+        a.dim[i] = d->dim[i];
+        a.stride[i] = (int64_t)d->stride[i];
+        a.estride[i] = d->estride[i] ? d->estride[i] : 1u;
+        a.ibox[i] = (d->box[i] + a.estride[i] - 1) / a.estride[i];
+    }
+    a.esize = d->esize;
+    a.span = d->swizzle == TM_SWIZZLE_128B ? 128u : d->swizzle == TM_SWIZZLE_64B ? 64u
+             : d->swizzle == TM_SWIZZLE_32B ? 32u : 0u;
+    a.inner_bytes = a.ibox[0] * d->esize;
+    a.gspan0 = d->box[0] * d->esize;
+    a.box_bytes = (uint32_t)d->box_bytes;
+    a.rows = (uint32_t)(d->box_bytes / a.inner_bytes);
+    a.fill_nan = d->oob == TM_OOB_NAN ? 1u : 0u;
+    a.fill = d->oob == TM_OOB_NAN ? nan_fill_bits(d->dtype) : 0ull;
+}
+
+// Shared memory per image row: the staged copy keeps the aligned 16-byte windows under the
+// tensor row segment of `gspan0` bytes (one more window than 16-byte units) and the row's offset;
+// the store keeps the offset only.
+inline size_t fb_copy_row_bytes(uint32_t gspan0) { return (size_t)(gspan0 / 16 + 1) * 16 + 8; }
 constexpr size_t kFbStoreRowBytes = 8;
 
 // Launch shape of a vector kernel that handles image rows in blocks: the most CTAs per SM up to

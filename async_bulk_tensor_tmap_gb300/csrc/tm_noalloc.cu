@@ -178,24 +178,14 @@ extern "C" int tiled_copy_noalloc(const tm_desc* src, const int32_t* coords, siz
         FbArgs a;
         memset(&a, 0, sizeof(a));
         a.walk = w;
-        a.base = src->base;
-        for (int i = 0; i < 5; i++) {
-            a.dim[i] = src->dim[i];
-            a.stride[i] = (int64_t)src->stride[i];
-        }
+        fb_from_desc(a, src);
         a.images = (uint64_t)images;
-        a.esize = src->esize;
-        a.span = src->swizzle == TM_SWIZZLE_128B ? 128u : src->swizzle == TM_SWIZZLE_64B ? 64u
-                 : src->swizzle == TM_SWIZZLE_32B ? 32u : 0u;
-        a.inner_bytes = src->box[0] * src->esize;
-        a.box_bytes = (uint32_t)src->box_bytes;
-        a.stage_bytes = stage;
-        a.rows = (uint32_t)(src->box_bytes / a.inner_bytes);
+        a.stage_bytes = stage_of(src->box_bytes);
         a.timeout_ns = limit_ns();
         a.status = status;
         uint32_t grid = 0;
         size_t smem = 0;
-        fb_shape(a, n, (uint32_t)d->sms, 8u, fb_copy_row_bytes(a.inner_bytes),
+        fb_shape(a, n, (uint32_t)d->sms, 8u, fb_copy_row_bytes(a.gspan0),
                  [&](uint32_t per_sm) { return budget(*d, per_sm); }, grid, smem);
         e = launch_fb_copy(a, grid, smem, st);
     }

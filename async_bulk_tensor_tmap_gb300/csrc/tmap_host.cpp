@@ -251,10 +251,12 @@ int make_walk(const tm_desc* d, const int32_t* coords, size_t n, cudaStream_t st
 // The tensor store and the tensor reduce write whole 16-byte units of the innermost dimension
 // (measured on GB300: with globalDim[0] * esize not a multiple of 16, the out-of-bounds tail of
 // the last unit of every row is overwritten with the image's zero fill).  Such maps store on the
-// vector path, which writes exactly the in-bounds bytes.
+// vector path, which writes exactly the in-bounds bytes.  So do maps with element strides: the
+// pages define the strides for the load into shared memory only, and the vector path writes the
+// image back to exactly the positions the load took.
 bool store_fits_tma(const tm_desc* d)
 {
-    return d->path == TM_PATH_TMA && (d->dim[0] * d->esize) % 16 == 0;
+    return d->path == TM_PATH_TMA && (d->dim[0] * d->esize) % 16 == 0 && unit_steps(d);
 }
 
 void release_walk(const BoxWalk& w, cudaStream_t st)
@@ -267,18 +269,9 @@ FbArgs fb_args(const tm_desc* d, const BoxWalk& w, uint64_t images, const DevSta
     FbArgs a;
     memset(&a, 0, sizeof(a));
     a.walk = w;
-    a.base = d->base;
-    for (int i = 0; i < 5; i++) {
-        a.dim[i] = d->dim[i];
-        a.stride[i] = (int64_t)d->stride[i];
-    }
+    fb_from_desc(a, d);
     a.images = images;
-    a.esize = d->esize;
-    a.span = span_of(d->swizzle);
-    a.inner_bytes = d->box[0] * d->esize;
-    a.box_bytes = (uint32_t)d->box_bytes;
     a.stage_bytes = stage_bytes_of(d->box_bytes);
-    a.rows = (uint32_t)(d->box_bytes / a.inner_bytes);
     a.timeout_ns = wait_limit_ns();
     a.status = ds.status;
     return a;
@@ -337,7 +330,7 @@ int copy_boxes(const tm_desc* src, const int32_t* coords, size_t nbox, void* ima
         size_t smem = 0;
         fb_shape(a, n, (uint32_t)ds->sms,
                  (uint32_t)std::min<uint64_t>(env_u64("TM_FB_COPY_CTAS_PER_SM", 8), 16),
-                 fb_copy_row_bytes(a.inner_bytes),
+                 fb_copy_row_bytes(a.gspan0),
                  [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); }, grid, smem);
         rc = check_launch(launch_fb_copy(a, grid, smem, st), "fallback copy launch");
     }
@@ -356,37 +349,46 @@ int plan_impl(tm_desc* out, int dtype, uint32_t rank, void* base, const uint64_t
     if (!base) return fail(TM_EINVAL, "base is NULL");
     if (!gdim || !box || (rank > 1 && !gstr)) return fail(TM_EINVAL, "dims / strides / box NULL");
     if (sw < TM_SWIZZLE_NONE || sw > TM_SWIZZLE_128B) return fail(TM_EINVAL, "bad swizzle %d", sw);
-    if (oob == TM_OOB_NAN) return fail(TM_EUNSUPPORTED, "NaN out-of-bounds fill is not supported");
-    if (oob != TM_OOB_ZERO) return fail(TM_EINVAL, "bad oob fill %d", oob);
+    if (oob != TM_OOB_ZERO && oob != TM_OOB_NAN) return fail(TM_EINVAL, "bad oob fill %d", oob);
+    if (oob == TM_OOB_NAN && dtype != TM_F16 && dtype != TM_BF16 && dtype != TM_F32 &&
+        dtype != TM_F64)
+        return fail(TM_EINVAL, "NaN out-of-bounds fill needs a floating-point dtype");
+    uint32_t step[5] = {1, 1, 1, 1, 1};
     for (uint32_t i = 0; i < rank; i++) {
         if (gdim[i] < 1 || gdim[i] > (1ull << 32))
             return fail(TM_ERANGE, "globalDim[%u] = %llu outside 1..2^32", i,
                         (unsigned long long)gdim[i]);
         if (box[i] < 1 || box[i] > 256)
             return fail(TM_ERANGE, "boxDim[%u] = %u outside 1..256", i, box[i]);
-        if (estr && estr[i] != 1) {
-            if (estr[i] >= 1 && estr[i] <= 8)
-                return fail(TM_EUNSUPPORTED, "elementStrides[%u] = %u: only 1 is supported", i,
-                            estr[i]);
-            return fail(TM_EINVAL, "elementStrides[%u] = %u outside 1..8", i, estr[i]);
+        if (estr) {
+            if (estr[i] < 1 || estr[i] > 8)
+                return fail(TM_EINVAL, "elementStrides[%u] = %u outside 1..8", i, estr[i]);
+            step[i] = estr[i];
         }
     }
     const uint64_t inner = (uint64_t)box[0] * es;
     if (inner % 16)
         return fail(TM_EALIGN, "boxDim[0] * element size = %llu bytes is not a multiple of 16",
                     (unsigned long long)inner);
+    const uint64_t image_row = (uint64_t)((box[0] + step[0] - 1) / step[0]) * es;
+    if (image_row % 16)
+        return fail(TM_EALIGN, "the image row ceil(boxDim[0] / elementStrides[0]) * element size = "
+                    "%llu bytes is not a multiple of 16", (unsigned long long)image_row);
     const uint32_t span = span_of((uint32_t)sw);
+    if (span && step[0] != 1)
+        return fail(TM_EUNSUPPORTED, "a swizzled map needs elementStrides[0] = 1");
     if (span && inner != span)
         return fail(TM_EUNSUPPORTED, "swizzle %u B needs an inner box row of exactly %u bytes, got %llu",
                     span, span, (unsigned long long)inner);
     uint64_t bb = es;
-    for (uint32_t i = 0; i < rank; i++) bb *= box[i];
+    for (uint32_t i = 0; i < rank; i++) bb *= (box[i] + step[i] - 1) / step[i];
     if (bb > TM_MAX_BOX_BYTES)
         return fail(TM_ERANGE, "box of %llu bytes exceeds %u", (unsigned long long)bb,
                     TM_MAX_BOX_BYTES);
     const uint64_t b = (uint64_t)(uintptr_t)base;
     if (b % es) return fail(TM_EALIGN, "base is not a multiple of the element size");
     uint32_t why = (b % 16) ? TM_WHY_BASE : 0u;
+    if (step[0] != 1) why |= TM_WHY_STEP0;
     for (uint32_t i = 1; i < rank; i++) {
         const uint64_t s = gstr[i - 1];
         if (s == 0 || s >= (1ull << 40))
@@ -409,7 +411,7 @@ int plan_impl(tm_desc* out, int dtype, uint32_t rank, void* base, const uint64_t
         out->dim[i] = used ? gdim[i] : 1;
         out->stride[i] = !used ? 0 : (i == 0 ? es : gstr[i - 1]);
         out->box[i] = used ? box[i] : 1;
-        out->estride[i] = 1;
+        out->estride[i] = used ? step[i] : 1;
         out->nbox[i] = used ? (gdim[i] + box[i] - 1) / box[i] : 1;
         if (__builtin_mul_overflow(nb_total, out->nbox[i], &nb_total))
             return fail(TM_ERANGE, "box count overflows 64 bits");
@@ -432,7 +434,7 @@ int encode_into(tm_desc* d)
     for (uint32_t i = 0; i < d->rank; i++) {
         dims[i] = d->dim[i];
         boxd[i] = d->box[i];
-        estr[i] = 1;
+        estr[i] = d->estride[i];
         if (i > 0) strides[i - 1] = d->stride[i];
     }
     const CUtensorMapL2promotion promo =
@@ -440,7 +442,8 @@ int encode_into(tm_desc* d)
     const CUresult r = enc((CUtensorMap*)d->tmap, (CUtensorMapDataType)d->dtype, d->rank,
                            (void*)(uintptr_t)d->base, dims, strides, boxd, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, (CUtensorMapSwizzle)d->swizzle, promo,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                           d->oob == TM_OOB_NAN ? CU_TENSOR_MAP_FLOAT_OOB_FILL_NAN_REQUEST_ZERO_FMA
+                                                : CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) {
         memset(d->tmap, 0, sizeof(d->tmap));
         d->path = TM_PATH_FALLBACK;
@@ -491,14 +494,15 @@ int tmap_replace_address(tm_desc* d, void* new_base)
     }
     // The path may change: rebuild from the stored fields.
     uint64_t gdim[5], gstr[4];
-    uint32_t box[5];
+    uint32_t box[5], estr[5];
     for (uint32_t i = 0; i < d->rank; i++) {
         gdim[i] = d->dim[i];
         box[i] = d->box[i];
+        estr[i] = d->estride[i];
         if (i > 0) gstr[i - 1] = d->stride[i];
     }
     tm_desc t;
-    int rc = tmap_encode(&t, (tm_dtype)d->dtype, d->rank, new_base, gdim, gstr, box, nullptr,
+    int rc = tmap_encode(&t, (tm_dtype)d->dtype, d->rank, new_base, gdim, gstr, box, estr,
                          (tm_swizzle)d->swizzle, (tm_oob)d->oob);
     if (rc) return rc;
     if (forced) {
@@ -584,6 +588,8 @@ int tile_reduce(const tm_desc* dst, const tm_desc* src, tm_redop op, void* strea
     if (src->dtype != dst->dtype) return fail(TM_EINVAL, "dst and src differ in element type");
     if (dst->rank != src->rank || dst->swizzle != src->swizzle)
         return fail(TM_EINVAL, "dst and src differ in rank or swizzle");
+    if (!unit_steps(dst) || !unit_steps(src))
+        return fail(TM_EUNSUPPORTED, "reduce takes maps whose elementStrides are all 1");
     for (uint32_t i = 0; i < dst->rank; i++) {
         if (dst->dim[i] != src->dim[i] || dst->box[i] != src->box[i])
             return fail(TM_EINVAL, "dst and src differ in dims or box (dim %u)", i);
@@ -644,6 +650,8 @@ int stream_tiles(const tm_desc* a, const tm_desc* b, uint32_t stages, float* cs_
         if (d->swizzle != TM_SWIZZLE_128B && d->swizzle != TM_SWIZZLE_NONE)
             return fail(TM_EUNSUPPORTED, "stream_tiles reads 128B-swizzled or unswizzled tiles");
         if (d->path != TM_PATH_TMA) return fail(TM_EUNSUPPORTED, "stream_tiles needs TMA-path maps");
+        if (!unit_steps(d) || d->oob != TM_OOB_ZERO)
+            return fail(TM_EUNSUPPORTED, "stream_tiles needs unit elementStrides and zero fill");
     }
     if (a->box[1] != b->box[1] || a->swizzle != b->swizzle)
         return fail(TM_EINVAL, "A and B differ in tile rows or swizzle");

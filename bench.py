@@ -97,8 +97,8 @@ class HostWorkload:
         need = lambda prefix: ops is None or any(o.startswith(prefix) for o in ops)
         r3, r4, r5a, m5b = (int(8192 / scale), int(4095 / scale), int(16384 / scale),
                             int(8192 / scale))
-        self.w3 = workloads.w3_tensor(r3, 8192) if need("w3") else None
-        self.w4 = workloads.w4_tensor(rows=r4) if need("w4") else None
+        self.w3 = workloads.w3_tensor(r3, 8192) if need("w3") or need("w6") else None
+        self.w4 = workloads.w4_tensor(rows=r4) if need("w4") or need("w6") else None
         self.w5a_dst, self.w5a_src = workloads.w5a_tensors(r5a) if need("w5a") else (None, None)
         self.w5b_a, self.w5b_b = workloads.w5b_tensors(m5b, 4096, m5b) if need("w5b") else (None, None)
         # widened reduce ops (not in the default step): bf16 add on its own tensors; s32 min and
@@ -117,6 +117,12 @@ class HostWorkload:
         self.r4_r5 = workloads.w4_rank5_map(rows=r4, span=128)
         self.r5a = workloads.w5a_map(r5a, 16384)
         self.r5b_a, self.r5b_b = workloads.w5b_maps(m5b, 4096, m5b, span=ring_span)
+        self.r5c = dict(self.r5a, box=[64, 128], esize=2, strides=[self.r5a["dims"][0] * 2])
+        # descriptor features over the W3 and W4 tensors: every other row, every other column,
+        # NaN out-of-bounds fill
+        self.r6_rows2 = workloads.w6_rows2_map(r3, 8192)
+        self.r6_cols2 = workloads.w6_cols2_map(r3, 8192)
+        self.r6_nan = dict(self.r4_128, nan=True)
 
 
 def box_count(r):
@@ -127,9 +133,10 @@ def box_count(r):
 
 
 def box_bytes(r):
+    """Image bytes: esize * prod(ceil(box / elementStrides))."""
     n = r["esize"]
-    for b in r["box"]:
-        n *= b
+    for i, b in enumerate(r["box"]):
+        n *= -(-b // r.get("estrides", [1] * len(r["box"]))[i])
     return n
 
 
@@ -154,10 +161,23 @@ def op_table(h: HostWorkload):
     return t
 
 
-# Widened reduce ops, timed only when named with --ops: (name, algorithmic bytes per call).
+# Widened ops, timed only when named with --ops: (name, algorithmic bytes per call).
+#   w5c: reduces of other types and ops: dst read + src read + dst written.
+#   w6.rows2: the image takes every other row: the taken rows are read, the images written.
+#   w6.cols2: every other column (vector path: an innermost step above 1); the taken elements
+#     are 4 bytes apart, so every 32-byte sector of the tensor holds some and the whole tensor is
+#     read.
+#   w6.cols2_rt: those images stored back: images read, every sector of the tensor written.
+#   w6.nan: the W4 rank-3 copy with NaN out-of-bounds fill (bytes as w4r3.copy).
 def extra_ops(h: HostWorkload):
     n = inbounds_bytes(h.r5a) // 4  # elements
-    return [("w5c.add_bf16", 3 * 2 * n), ("w5c.min_s32", 3 * 4 * n), ("w5c.max_f32", 3 * 4 * n)]
+    rows2_img = box_count(h.r6_rows2) * box_bytes(h.r6_rows2)
+    cols2_img = box_count(h.r6_cols2) * box_bytes(h.r6_cols2)
+    w3 = inbounds_bytes(h.r3)
+    return [("w5c.add_bf16", 3 * 2 * n), ("w5c.min_s32", 3 * 4 * n), ("w5c.max_f32", 3 * 4 * n),
+            ("w6.rows2", 2 * rows2_img), ("w6.cols2", w3 + cols2_img),
+            ("w6.cols2_rt", cols2_img + w3),
+            ("w6.nan", inbounds_bytes(h.r6_nan) + box_count(h.r6_nan) * box_bytes(h.r6_nan))]
 
 
 # ------------------------------------------------------------------------------------------------
@@ -176,7 +196,9 @@ class GpuWorkload:
         sw = {0: 0, 32: 1, 64: 2, 128: 3}
 
         def enc(dtype, buf, r):
-            return tm.tmap_encode(dtype, buf, r["dims"], r["strides"], r["box"], swizzle=sw[r["span"]])
+            return tm.tmap_encode(dtype, buf, r["dims"], r["strides"], r["box"],
+                                  element_strides=r.get("estrides"), swizzle=sw[r["span"]],
+                                  oob=tm.TM_OOB_NAN if r.get("nan") else tm.TM_OOB_ZERO)
 
         bf, f32 = tm.TM_BF16, tm.TM_F32
         self.maps = {}
@@ -202,12 +224,16 @@ class GpuWorkload:
             self.t["bits_b"] = torch.zeros(n, dtype=torch.int64, device="cuda")
         if h.w5c_dst is not None:
             self.t["w5c_dst"], self.t["w5c_src"] = dev(h.w5c_dst), dev(h.w5c_src)
-            rb = dict(h.r5a, box=[64, 128], esize=2, strides=[h.r5a["dims"][0] * 2])
-            self.maps["w5c_dst"] = enc(tm.TM_BF16, self.t["w5c_dst"], rb)
-            self.maps["w5c_src"] = enc(tm.TM_BF16, self.t["w5c_src"], rb)
+            self.maps["w5c_dst"] = enc(tm.TM_BF16, self.t["w5c_dst"], h.r5c)
+            self.maps["w5c_src"] = enc(tm.TM_BF16, self.t["w5c_src"], h.r5c)
             self.maps["w5a_dst_s32"] = enc(tm.TM_S32, self.t["w5a_dst"], h.r5a)
             self.maps["w5a_src_s32"] = enc(tm.TM_S32, self.t["w5a_src"], h.r5a)
-        for k in ("w3", "w4r3", "w4r3n", "w4r5"):
+        if "w3" in self.t and "w4" in self.t:
+            self.maps["w6_rows2"] = enc(bf, self.t["w3"], h.r6_rows2)
+            self.maps["w6_cols2"] = enc(bf, self.t["w3"], h.r6_cols2)
+            self.maps["w6_cols2_out"] = enc(bf, self.t["w3_out"], h.r6_cols2)
+            self.maps["w6_nan"] = enc(bf, self.t["w4"], h.r6_nan)
+        for k in ("w3", "w4r3", "w4r3n", "w4r5", "w6_rows2", "w6_cols2", "w6_nan"):
             if k in self.maps:
                 m = self.maps[k]
                 self.t[f"{k}_img"] = torch.empty(m.num_boxes * m.box_bytes, dtype=torch.uint8,
@@ -234,6 +260,12 @@ class GpuWorkload:
         elif kind == "ring":
             tm.stream_tiles(m["w5b_a"], m["w5b_b"], self.ring_stages, t["cs_a"], t["cs_b"],
                             t["bits_a"], t["bits_b"], s)
+        elif kind in ("rows2", "cols2", "nan"):
+            tm.tiled_copy(m[f"w6_{kind}"], None, t[f"w6_{kind}_img"], s)
+        elif kind == "cols2_rt":
+            tm.tiled_roundtrip(m["w6_cols2_out"], None, t["w6_cols2_img"], s)
+        else:
+            raise ValueError(f"unknown op {name}")
 
     def flush_l2(self):
         with self.torch.cuda.stream(self.stream):
@@ -413,7 +445,20 @@ def oracle_sample(h: HostWorkload, ops, fraction: float, threads: int):
     import oracle
 
     def om(arr, r):
-        return oracle.Map(arr, r["esize"], r["dims"], r["strides"], r["box"], r["span"])
+        fill = oracle.FILL_NAN_BF16 if r.get("nan") else oracle.FILL_ZERO
+        return oracle.Map(arr, r["esize"], r["dims"], r["strides"], r["box"], r["span"],
+                          estrides=r.get("estrides"), fill=fill)
+
+    def sample(fn, r, nbytes):
+        """fn(k): oracle work over the first k boxes of map r; returns the seconds it took."""
+        n = box_count(r)
+        k = max(1, int(n * fraction))
+        return fn(k), nbytes * k // n
+
+    def timed(f, *a, **kw):
+        t0 = time.perf_counter()
+        f(*a, **kw)
+        return time.perf_counter() - t0
 
     spent, covered = 0.0, 0
     if not hasattr(h, "scratch3"):  # destinations of the sampled round trips, made once
@@ -447,12 +492,29 @@ def oracle_sample(h: HostWorkload, ops, fraction: float, threads: int):
             oracle.tile_reduce_add(om(d, h.r5a), om(h.w5a_src, h.r5a), threads=threads, b0=0, b1=k)
             spent += time.perf_counter() - t0
             covered += nbytes * k // n
-        elif kind == "add_bf16":
-            tm.tile_reduce(m["w5c_dst"], m["w5c_src"], tm.TM_RED_ADD, s)
-        elif kind == "min_s32":
-            tm.tile_reduce(m["w5a_dst_s32"], m["w5a_src_s32"], tm.TM_RED_MIN, s)
-        elif kind == "max_f32":
-            tm.tile_reduce(m["w5a_dst"], m["w5a_src"], tm.TM_RED_MAX, s)
+        elif base == "w5c":
+            if kind == "add_bf16":
+                d, sr, r, ty, op = h.w5c_dst, h.w5c_src, h.r5c, oracle.BF16, oracle.ADD
+            else:
+                d, sr, r = h.w5a_dst, h.w5a_src, h.r5a
+                ty, op = (oracle.S32, oracle.MIN) if kind == "min_s32" else (oracle.F32, oracle.MAX)
+            sec, cov = sample(lambda k: timed(oracle.tile_reduce, om(d, r), om(sr, r), ty, op,
+                                              threads=threads, b0=0, b1=k), r, nbytes)
+            spent, covered = spent + sec, covered + cov
+        elif base == "w6":
+            r = {"rows2": h.r6_rows2, "nan": h.r6_nan}.get(kind, h.r6_cols2)
+            src = h.w4 if kind == "nan" else h.w3
+
+            def run(k):
+                imgs = np.empty(k * box_bytes(r), np.uint8)
+                sec = timed(oracle.tiled_copy, om(src, r), threads=threads, b0=0, b1=k, out=imgs,
+                            nbox=k)
+                if kind == "cols2_rt":
+                    sec = timed(oracle.tiled_roundtrip, om(scratch3, r), imgs, threads=threads,
+                                b0=0, b1=k)
+                return sec
+            sec, cov = sample(run, r, nbytes)
+            spent, covered = spent + sec, covered + cov
         elif kind == "ring":
             n = box_count(h.r5b_a)
             k = max(1, int(n * fraction))
@@ -606,7 +668,7 @@ def main():
     dom_name, dom_bytes = dom
     dom_ms = statistics.mean(per[dom_name])
     achieved = dom_bytes / dom_ms / 1e6
-    if any(n.startswith("w5c") for n, _ in ops):
+    if any(n.startswith(("w5c", "w6")) for n, _ in ops):
         args.e2e_steps = 0  # the widened ops have no end-to-end leg
     if args.e2e_steps > 0:
         e2e_ms, bi, bo = e2e_run(g, h, ops, args.e2e_steps)

@@ -63,8 +63,13 @@ typedef enum tm_swizzle {
     TM_SWIZZLE_NONE = 0, TM_SWIZZLE_32B = 1, TM_SWIZZLE_64B = 2, TM_SWIZZLE_128B = 3
 } tm_swizzle;
 
-/* ---- out-of-bounds fill, [H200-TMA] §02 (out-of-bounds row: the hardware fills with 0 / NaN) - */
-typedef enum tm_oob { TM_OOB_ZERO = 0, TM_OOB_NAN = 1 /* not supported: TM_EUNSUPPORTED */ } tm_oob;
+/* ---- out-of-bounds fill, [H200-TMA] §02 (out-of-bounds row: the hardware fills with 0 / NaN) -
+ * TM_OOB_ZERO: out-of-bounds image elements are zero bytes.  TM_OOB_NAN (floating-point dtypes
+ * only): they are a NaN of the element's format.  The pages name no NaN bit pattern; both paths
+ * write the one GB300's NaN-request fill was measured to write, the 16-bit pattern 0x7FF7 repeated
+ * over the element (f16 / bf16 0x7FF7, f32 0x7FF77FF7, f64 0x7FF77FF77FF77FF7).  Stores and
+ * reduces never write out-of-bounds elements, so the fill only shows in images. */
+typedef enum tm_oob { TM_OOB_ZERO = 0, TM_OOB_NAN = 1 } tm_oob;
 
 /* ---- execution paths ------------------------------------------------------------------------ */
 #define TM_PATH_TMA 1      /* cp.async.bulk.tensor with a driver-encoded tensor map               */
@@ -74,6 +79,9 @@ typedef enum tm_oob { TM_OOB_ZERO = 0, TM_OOB_NAN = 1 /* not supported: TM_EUNSU
 #define TM_WHY_BASE 2u     /* the base address is not 16-byte aligned ([H200-TMA] §03)           */
 #define TM_WHY_DRIVER 4u   /* the driver's encoder refused the map                               */
 #define TM_WHY_FORCED 8u   /* tmap_force_fallback() was called                                   */
+#define TM_WHY_STEP0 16u   /* elementStrides[0] > 1: measured on GB300, a tensor-map load of such a
+                            * map does not deliver rows of ceil(boxDim[0] / elementStrides[0])
+                            * packed elements (its byte count never completes)                  */
 
 /* ---- the descriptor -------------------------------------------------------------------------
  * [MLSys-TMA] §"一个 thread 如何描述整个 tile": the descriptor says how the whole tensor is laid
@@ -96,9 +104,9 @@ typedef struct __attribute__((aligned(64))) tm_desc {
     uint64_t dim[5];        /* globalDim, innermost first (unused entries 1)                    */
     uint64_t stride[5];     /* byte stride of each dim; stride[0] = esize (unused entries 0)    */
     uint32_t box[5];        /* boxDim (unused entries 1)                                        */
-    uint32_t estride[5];    /* elementStrides (always 1 here)                                   */
+    uint32_t estride[5];    /* elementStrides, 1..8 (unused entries 1)                          */
     uint64_t nbox[5];       /* boxes along each dim: ceil(dim / box)                           */
-    uint64_t box_bytes;     /* bytes of one box image: esize * prod(box)                       */
+    uint64_t box_bytes;     /* bytes of one box image: esize * prod(ceil(box / estride))        */
     uint64_t num_boxes;     /* prod(nbox)                                                       */
     uint8_t reserved[40];
     uint8_t tmap[128];      /* CUtensorMap (driver-encoded) when path == TM_PATH_TMA            */
@@ -113,8 +121,15 @@ typedef struct __attribute__((aligned(64))) tm_desc {
  *   1 <= boxDim[i] <= 256 (else TM_ERANGE); boxDim[0] * esize a multiple of 16 bytes (else
  *   TM_EALIGN); globalStrides below 2^40 (else TM_ERANGE).  [MLSys-TMA] §"用 3D TMA 搬运多个
  *   swizzle atoms" and §"128-byte swizzle 的分组要求": with a swizzle, boxDim[0] * esize equals the
- *   atom width (else TM_EUNSUPPORTED).  elementStrides (NULL = all 1) must be all 1 and oob must be
- *   TM_OOB_ZERO (else TM_EUNSUPPORTED).  box_bytes above TM_MAX_BOX_BYTES gives TM_ERANGE.
+ *   atom width (else TM_EUNSUPPORTED).  box_bytes above TM_MAX_BOX_BYTES gives TM_ERANGE.
+ *   elementStrides (NULL = all 1; [Book-TMA] §"Tensor descriptor：CUtensorMap": the step, in
+ *   elements, between the elements taken along each dim): each 1..8 (else TM_EINVAL).  Along dim
+ *   i the image takes the box's elements start, start + es, ... below start + boxDim[i], i.e.
+ *   ceil(boxDim[i] / es) of them, packed; the box grid still steps by boxDim.  The image row,
+ *   ceil(boxDim[0] / es[0]) * esize bytes, must be a multiple of 16 (else TM_EALIGN), and a
+ *   swizzled map needs elementStrides[0] == 1 (else TM_EUNSUPPORTED).  A map with
+ *   elementStrides[0] > 1 goes to the fallback path (TM_WHY_STEP0).  oob: TM_OOB_NAN needs a
+ *   floating-point dtype (else TM_EINVAL).
  *   A base or stride that is a multiple of the element size but not of 16 bytes is NOT an error:
  *   the map goes to the fallback path (why_fallback says which).  A base or stride that is not a
  *   multiple of the element size gives TM_EALIGN.
@@ -148,7 +163,8 @@ int tmap_force_fallback(tm_desc* d);
 /* tile_load_image -- one box to its shared-memory image, written to `image` (device, box_bytes,
  *   16-byte aligned).  [Book-TMA] §"单 block、单 lane、单 tile 的 TMA load" (one block, one lane,
  *   one tile) and [MLSys-TMA] §"TMA 如何写入 swizzled layout": image element e (box coordinates,
- *   dim 0 fastest) sits at swizzle(lin(e) * esize); elements outside the tensor are zero bytes.
+ *   dim 0 fastest) sits at swizzle(lin(e) * esize) and comes from tensor coordinate
+ *   start + e * elementStrides; elements outside the tensor are the map's fill (tm_oob).
  *   coords[rank] (host): signed start of the box; may lie partly or wholly outside the tensor. */
 int tile_load_image(const tm_desc* src, const int32_t* coords, void* image, void* stream);
 
@@ -168,7 +184,8 @@ int tiled_copy(const tm_desc* src, const int32_t* coords, size_t nbox, void* ima
  *   The tensor store writes whole 16-byte units of the innermost dimension, so a map whose
  *   globalDim[0] * esize is not a multiple of 16 (or a box list starting off the 16-byte grid or
  *   outside the tensor) is stored by the vector path instead, which writes exactly the in-bounds
- *   bytes. */
+ *   bytes.  So is a map with an elementStride other than 1: image element e goes back to tensor
+ *   coordinate start + e * elementStrides, and no other element is written. */
 int tiled_roundtrip(const tm_desc* dst, const int32_t* coords, size_t nbox, const void* images,
                     void* stream);
 
@@ -184,7 +201,7 @@ int tile_reduce_add(const tm_desc* dst, const tm_desc* src, void* stream);
  *   ([Book-TMA] §"TMA reduce，把“搬运”和“归约”合并": the write-back combines each element with the
  *   value in global memory, "add, min and the like").  Types TM_F32, TM_F16, TM_BF16, TM_U32,
  *   TM_S32 (else TM_EUNSUPPORTED); dst and src of one type with equal dims, box and swizzle (else
- *   TM_EINVAL); they must not overlap.  Semantics: float add = the exact sum rounded to nearest,
+ *   TM_EINVAL), elementStrides all 1 (else TM_EUNSUPPORTED); they must not overlap.  Semantics: float add = the exact sum rounded to nearest,
  *   ties to even, in the element type (a reading: the pages fix no rounding); min / max = the
  *   smaller / larger value (dst kept on a tie); u32 / s32 add wraps modulo 2^32.  Add on every type
  *   and min / max on u32 / s32 use the bulk tensor reduce; float min / max, and maps the tensor
@@ -196,7 +213,8 @@ int tile_reduce(const tm_desc* dst, const tm_desc* src, tm_redop op, void* strea
  *   one elected producer thread fills stage s with tile t of A and tile t of B (one mbarrier,
  *   expect_tx = 2 * box_bytes), consumer warps read the stage through the swizzle and release it.
  *   A and B: TM_BF16, rank 2, box {64, R} with R in {32, 64, 128, 256}, swizzle 128B or NONE,
- *   TMA path, equal num_boxes; tiles are walked in box-grid order.  Per tile t (device outputs,
+ *   TMA path, elementStrides all 1 and TM_OOB_ZERO (else TM_EUNSUPPORTED), equal num_boxes; tiles
+ *   are walked in box-grid order.  Per tile t (device outputs,
  *   num_boxes entries each): cs = fp32 checksum (each row summed in order from its first element,
  *   then a pairwise-adjacent tree over the rows), bits = sum of the 16-bit patterns.
  *   stages: 2..8. */

@@ -20,17 +20,25 @@ def to_host(t) -> np.ndarray:
     return t.cpu().numpy()
 
 
+# library dtype code (TM_F16, TM_F32, TM_F64, TM_BF16) -> the oracle's NaN fill of that format
+DTYPE_TO_NAN_FILL = {6: oracle.FILL_NAN_F16, 7: oracle.FILL_NAN_F32, 8: oracle.FILL_NAN_F64,
+                     9: oracle.FILL_NAN_BF16}
+
+
 def dev_map(tm, buf, r, offset=0, dtype=None):
+    """Recipe keys: dims, strides, box, span, esize; optional estrides and nan (True: NaN fill)."""
     dt = ESIZE_TO_DTYPE[r["esize"]] if dtype is None else dtype
     m = tm.tmap_encode(dt, buf.data_ptr() + offset, r["dims"], r["strides"], r["box"],
-                       swizzle=SPAN_TO_SW[r["span"]])
+                       element_strides=r.get("estrides"), swizzle=SPAN_TO_SW[r["span"]],
+                       oob=tm.TM_OOB_NAN if r.get("nan") else tm.TM_OOB_ZERO)
     m.keepalive = buf  # the map holds a raw address: keep the tensor it points into alive
     return m
 
 
-def host_map(arr: np.ndarray, r, offset=0):
+def host_map(arr: np.ndarray, r, offset=0, dtype=None):
+    fill = DTYPE_TO_NAN_FILL[dtype] if r.get("nan") else oracle.FILL_ZERO
     return oracle.Map(arr, r["esize"], r["dims"], r["strides"], r["box"], r["span"],
-                      offset=offset)
+                      offset=offset, estrides=r.get("estrides"), fill=fill)
 
 
 def empty_images(n_boxes: int, box_bytes: int, fill: int = 0x5A):

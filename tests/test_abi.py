@@ -79,8 +79,12 @@ def test_plan_rejections(tm):
     assert code_of(tm, global_strides=[1 << 40]) == tm.TM_ERANGE                   # stride >= 2^40
     assert code_of(tm, global_strides=[16383]) == tm.TM_EALIGN                     # not % esize
     assert code_of(tm, base=FAKE + 1) == tm.TM_EALIGN
-    assert code_of(tm, element_strides=[2, 1]) == tm.TM_EUNSUPPORTED
-    assert code_of(tm, oob=tm.TM_OOB_NAN) == tm.TM_EUNSUPPORTED
+    assert code_of(tm, element_strides=[2, 1]) == tm.TM_EUNSUPPORTED              # swizzled
+    assert code_of(tm, element_strides=[1, 9]) == tm.TM_EINVAL
+    assert code_of(tm, element_strides=[1, 0]) == tm.TM_EINVAL
+    assert code_of(tm, element_strides=[3, 1], swizzle=0) == tm.TM_EALIGN  # 22 * 2 B image row
+    assert code_of(tm, oob=tm.TM_OOB_NAN, dtype=tm.TM_U16) == tm.TM_EINVAL
+    assert code_of(tm, oob=2) == tm.TM_EINVAL
     assert code_of(tm, dtype=42) == tm.TM_EINVAL
     assert code_of(tm, base=0) == tm.TM_EINVAL
     assert code_of(tm, box_dim=[256, 256, 4], global_dim=[256, 256, 4],
@@ -148,3 +152,36 @@ def test_calls_reject_unfilled_descriptors(tm):
     with pytest.raises(tm.TmapError) as e:
         tm.stream_tiles(m, m, 1, FAKE, FAKE, FAKE, FAKE, stream=0)
     assert e.value.code == tm.TM_ERANGE
+
+
+def test_plan_element_strides_and_nan_fill(tm):
+    """Image extents are ceil(box / elementStrides); the box grid keeps stepping by the box."""
+    m = plan(tm, element_strides=[1, 3], oob=tm.TM_OOB_NAN)
+    assert (m.box_bytes, m.num_boxes, m.path) == (128 * 43, 8192, tm.TM_PATH_TMA)
+    assert list(m.d.estride[:2]) == [1, 3] and m.d.oob == tm.TM_OOB_NAN
+    m = plan(tm, element_strides=[2, 8], box_dim=[128, 16], swizzle=0)
+    assert (m.box_bytes, m.num_boxes) == (64 * 2 * 2, 64 * 512)
+    assert (m.path, m.why_fallback) == (tm.TM_PATH_FALLBACK, tm.TM_WHY_STEP0)
+    for dt in (tm.TM_F16, tm.TM_BF16, tm.TM_F32, tm.TM_F64):
+        assert code_of(tm, dtype=dt, box_dim=[64 if dt in (tm.TM_F16, tm.TM_BF16) else
+                                             (32 if dt == tm.TM_F32 else 16), 8],
+                       oob=tm.TM_OOB_NAN) == tm.TM_OK
+
+
+def test_reduce_and_ring_refuse_strided_or_nan_maps(tm):
+    """Checked on the host before any device work (so this runs without a GPU)."""
+    f = dict(dtype=tm.TM_F32, box_dim=[32, 128])
+    a = plan(tm, **f)
+    s = plan(tm, element_strides=[1, 2], **f)
+    for dst, src in ((a, s), (s, a)):
+        with pytest.raises(tm.TmapError) as e:
+            tm.tile_reduce(dst, src, tm.TM_RED_ADD, stream=0)
+        assert e.value.code == tm.TM_EUNSUPPORTED
+    ring = dict(box_dim=[64, 128])
+    ok, nan, step = plan(tm, **ring), plan(tm, oob=tm.TM_OOB_NAN, **ring), \
+        plan(tm, element_strides=[1, 2], **ring)
+    out = 1 << 41  # never dereferenced: the call fails validation first
+    for x, y in ((ok, nan), (step, ok)):
+        with pytest.raises(tm.TmapError) as e:
+            tm.stream_tiles(x, y, 4, out, out, out, out, stream=0)
+        assert e.value.code == tm.TM_EUNSUPPORTED

@@ -191,3 +191,14 @@ def w5b_maps(m=8192, k=4096, n=8192, span=128):
     a = dict(dims=[k, m], strides=[k * 2], box=[64, 128], span=span, esize=2)
     b = dict(dims=[n, k], strides=[n * 2], box=[64, 128], span=span, esize=2)
     return a, b
+
+
+# Descriptor features over the W3 tensor (8192 x 8192 bf16): elementStrides take every other row
+# (box 64 x 128, steps {1, 2}: 64 x 64 images, 128B swizzle) or every other column (box 128 x 64,
+# steps {2, 1}: 64 x 64 images, no swizzle -- a swizzled map needs a unit innermost step).
+def w6_rows2_map(rows: int = 8192, cols: int = 8192):
+    return dict(w3_map(rows, cols, 128), estrides=[1, 2])
+
+
+def w6_cols2_map(rows: int = 8192, cols: int = 8192):
+    return dict(w3_map(rows, cols, 0), box=[128, 64], estrides=[2, 1])
