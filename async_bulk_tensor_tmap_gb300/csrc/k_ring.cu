@@ -103,24 +103,45 @@ __global__ void __launch_bounds__(kRingThreads, 1)
             tma_prefetch_l2_2d(&mb, cb[0], cb[1]);
         };
         for (uint64_t j = S; j < r.prefetch; j++) prefetch(j);
+        // Tile counters of A and B (box along dim 0, box along dim 1), stepped by gridDim.x tiles
+        // with a carry; the stage and the number of times the ring has wrapped are counted too.
+        const uint32_t a_d0 = (uint32_t)(gridDim.x % r.a_nb0), b_d0 = (uint32_t)(gridDim.x % r.b_nb0);
+        const uint64_t a_d1 = gridDim.x / r.a_nb0, b_d1 = gridDim.x / r.b_nb0;
+        uint64_t a_k0 = first % r.a_nb0, a_k1 = first / r.a_nb0;
+        uint64_t b_k0 = first % r.b_nb0, b_k1 = first / r.b_nb0;
+        uint32_t s = 0, wraps = 0;
         uint64_t i = 0;
         for (; i < n_local; i++) {
-            const uint32_t s = (uint32_t)(i % S);
-            const uint64_t k = i / S;
-            if (k > 0) {
-                const uint32_t parity = (uint32_t)((k - 1) & 1);
+            if (wraps > 0) {
+                const uint32_t parity = (wraps - 1) & 1u;
                 if (!mbar_wait(smem_u32(&empty_bar[s]), parity, r.timeout_ns)) {
                     record_timeout(r.status, K_STREAM, s, parity, first + i * gridDim.x);
                     break;
                 }
             }
             const uint32_t bar = smem_u32(&full_bar[s]);
-            int32_t ca[2], cb[2];
-            coords(i, ca, cb);
+            const int32_t ca[2] = {(int32_t)(a_k0 * 64), (int32_t)(a_k1 * r.rows)};
+            const int32_t cb[2] = {(int32_t)(b_k0 * 64), (int32_t)(b_k1 * r.rows)};
             mbar_arrive_expect_tx(bar, 2 * tile);
             tma_load<2>(base + s * 2 * tile, &ma, ca, bar);
             tma_load<2>(base + s * 2 * tile + tile, &mb, cb, bar);
             if (r.prefetch) prefetch(i + r.prefetch);
+            a_k0 += a_d0;
+            a_k1 += a_d1;
+            if (a_k0 >= r.a_nb0) {
+                a_k0 -= r.a_nb0;
+                a_k1++;
+            }
+            b_k0 += b_d0;
+            b_k1 += b_d1;
+            if (b_k0 >= r.b_nb0) {
+                b_k0 -= r.b_nb0;
+                b_k1++;
+            }
+            if (++s == S) {
+                s = 0;
+                wraps++;
+            }
         }
         // Loads still landing (only after a failure): wait for them, bounded, before leaving.
         const uint64_t lo = i > S ? i - S : 0;
@@ -139,9 +160,19 @@ __global__ void __launch_bounds__(kRingThreads, 1)
     unsigned long long* const bits_out = grp == 0 ? r.bits_a : r.bits_b;
     const uint32_t xr = r.swizzled ? 7u : 0u;
 
+    uint32_t s = 0, parity = 0;         // stage of tile i and its phase parity
+    uint32_t slot = 0, slot_parity = 0;  // reduction slot of tile i (NS slots) and its parity
     for (uint64_t i = 0; i < n_local; i++) {
-        const uint32_t s = (uint32_t)(i % S);
-        const uint32_t parity = (uint32_t)((i / S) & 1);
+        if (i) {
+            if (++s == S) {
+                s = 0;
+                parity ^= 1u;
+            }
+            if (++slot == NS) {
+                slot = 0;
+                slot_parity ^= 1u;
+            }
+        }
         const bool ok = __all_sync(0xffffffffu,
                                    mbar_wait(smem_u32(&full_bar[s]), parity, r.timeout_ns));
         if (!ok) {
@@ -218,16 +249,14 @@ __global__ void __launch_bounds__(kRingThreads, 1)
         bits = __reduce_add_sync(0xffffffffu, bits);  // exact integer sum: order-free
 
         // ... then across the tile's warps, in warp order (slots of iteration i % NS)
-        const uint32_t slot = (uint32_t)(i % NS);
         if (lane == 0) {
             red_cs[grp][slot][wi] = blk[0];
             red_bits[grp][slot][wi] = bits;
             mbar_arrive(smem_u32(&red_bar[grp][slot]));
         }
         if (wi == 0 && lane == 0) {
-            const uint32_t rp = (uint32_t)((i / NS) & 1);
-            if (!mbar_wait(smem_u32(&red_bar[grp][slot]), rp, r.timeout_ns)) {
-                record_timeout(r.status, K_STREAM, slot, rp, first + i * gridDim.x);
+            if (!mbar_wait(smem_u32(&red_bar[grp][slot]), slot_parity, r.timeout_ns)) {
+                record_timeout(r.status, K_STREAM, slot, slot_parity, first + i * gridDim.x);
                 break;
             }
             float part[kRingMaxWpt];

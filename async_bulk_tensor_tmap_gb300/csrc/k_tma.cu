@@ -16,8 +16,10 @@
 //          READING shared memory (wait_group.read 1): the write of group i stays in flight
 //          (with a single stage, the stage of group i once its own write has read it).
 //
-// Grid coordinates of consecutive boxes are stepped with an odometer rather than recomputed with
-// 64-bit divisions.
+// The lane keeps two cursors over its groups, one for loads (running up to S groups ahead) and
+// one for writes: each holds the stage, its phase parity and, for a grid walk, the box counters of
+// the group's first box, stepped by G * gridDim.x boxes with carries; the boxes inside a group are
+// stepped with an odometer.  No 64-bit division is left on the issue path.
 //
 // The three kinds differ only in the two copy instructions:
 //   copy       load = tensor load of the box;  write = 1-D bulk store of the image (tile-major)
@@ -54,95 +56,119 @@ __global__ void __launch_bounds__(32, 1)
     for (uint32_t s = 0; s < S; s++) mbar_init(smem_u32(&full_bar[s]), 1);
     fence_barrier_init();
 
+    const bool grid = a.walk.mode == WALK_GRID;
     auto group_of = [&](uint64_t i) -> uint64_t { return first + i * gridDim.x; };
     auto count_of = [&](uint64_t g) -> uint32_t {
         const uint64_t b0 = g * G;
         return (uint32_t)(a.walk.nbox - b0 < G ? a.walk.nbox - b0 : G);
     };
 
-    // Calls fn(k, coords) for the boxes of group g, in order.
-    auto for_boxes = [&](uint64_t g, auto&& fn) {
-        const uint64_t b0 = g * G;
+    // Group i of this CTA: its stage, the phase parity of that stage's barrier, and (grid walks)
+    // the counters of its first box.
+    struct Cursor {
+        uint64_t i;
+        uint32_t s, phase;
+        uint32_t k[5];
+    };
+    uint32_t dstep[5] = {0, 0, 0, 0, 0};  // digits of G * gridDim.x boxes
+    Cursor ld{0, 0, 0, {0, 0, 0, 0, 0}};
+    if (grid) {
+        grid_counters(a.walk, first * G, ld.k);
+        grid_counters(a.walk, (uint64_t)gridDim.x * G, dstep);
+    }
+    Cursor wr = ld;
+    auto advance = [&](Cursor& c) {
+        c.i++;
+        if (++c.s == S) {
+            c.s = 0;
+            c.phase ^= 1u;
+        }
+        if (grid) grid_add(a.walk, c.k, dstep);
+    };
+
+    // Calls fn(j, coords) for the boxes of the cursor's group, in order.
+    auto for_boxes = [&](const Cursor& c, auto&& fn) {
+        const uint64_t g = group_of(c.i);
         const uint32_t cnt = count_of(g);
-        int32_t c[5];
-        if (a.walk.mode == WALK_GRID) {
+        int32_t co[5];
+        if (grid) {
             uint32_t k[5];
-            grid_counters(a.walk, b0, k);
+#pragma unroll
+            for (int d = 0; d < 5; d++) k[d] = c.k[d];
             for (uint32_t j = 0; j < cnt; j++) {
 #pragma unroll
-                for (int i = 0; i < 5; i++) c[i] = (int32_t)(k[i] * a.walk.box[i]);
-                fn(j, c);
+                for (int d = 0; d < 5; d++) co[d] = (int32_t)(k[d] * a.walk.box[d]);
+                fn(j, co);
                 grid_next(a.walk, k);
             }
         } else {
             for (uint32_t j = 0; j < cnt; j++) {
-                box_start(a.walk, b0 + j, c);
-                fn(j, c);
+                box_start(a.walk, g * G + j, co);
+                fn(j, co);
             }
         }
     };
 
-    auto issue = [&](uint64_t i) {
-        const uint32_t s = (uint32_t)(i % S);
-        const uint32_t bar = smem_u32(&full_bar[s]);
-        const uint32_t dst = base + s * a.stage_bytes;
-        const uint64_t g = group_of(i);
+    auto issue = [&](const Cursor& c) {
+        const uint32_t bar = smem_u32(&full_bar[c.s]);
+        const uint32_t dst = base + c.s * a.stage_bytes;
+        const uint64_t g = group_of(c.i);
         const uint32_t bytes = count_of(g) * a.box_bytes;
         mbar_arrive_expect_tx(bar, bytes);
         if constexpr (KIND == KIND_ROUNDTRIP) {
             bulk_load(dst, a.images + g * G * a.box_bytes, bytes, bar);
         } else {
-            for_boxes(g, [&](uint32_t j, const int32_t* c) {
-                tma_load<R>(dst + j * a.box_bytes, &in_map, c, bar);
+            for_boxes(c, [&](uint32_t j, const int32_t* co) {
+                tma_load<R>(dst + j * a.box_bytes, &in_map, co, bar);
             });
         }
     };
 
-    auto write_out = [&](uint64_t i) {
-        const uint32_t s = (uint32_t)(i % S);
-        const uint32_t src = base + s * a.stage_bytes;
-        const uint64_t g = group_of(i);
+    auto write_out = [&](const Cursor& c) {
+        const uint32_t src = base + c.s * a.stage_bytes;
+        const uint64_t g = group_of(c.i);
         if constexpr (KIND == KIND_COPY) {
             bulk_store(a.images + g * G * a.box_bytes, src, count_of(g) * a.box_bytes);
         } else {
-            for_boxes(g, [&](uint32_t j, const int32_t* c) {
+            for_boxes(c, [&](uint32_t j, const int32_t* co) {
                 if constexpr (KIND == KIND_ROUNDTRIP) {
-                    tma_store<R>(&out_map, c, src + j * a.box_bytes);
+                    tma_store<R>(&out_map, co, src + j * a.box_bytes);
                 } else {
-                    tma_reduce<R, KIND - KIND_REDUCE>(&out_map, c, src + j * a.box_bytes);
+                    tma_reduce<R, KIND - KIND_REDUCE>(&out_map, co, src + j * a.box_bytes);
                 }
             });
         }
         bulk_commit();
     };
 
-    uint64_t issued = 0;
-    while (issued < n_local && issued < S) issue(issued++);
+    while (ld.i < n_local && ld.i < S) {
+        issue(ld);
+        advance(ld);
+    }
     // Stage refilled after writing group i: the one group i - 1 used (its write may still be
     // reading), or with a single stage the one just written.
     const uint64_t lag = S > 1 ? 1 : 0;
 
-    for (uint64_t i = 0; i < n_local; i++) {
-        const uint32_t s = (uint32_t)(i % S);
-        const uint32_t parity = (uint32_t)((i / S) & 1);
-        if (!mbar_wait(smem_u32(&full_bar[s]), parity, a.timeout_ns)) {
+    for (; wr.i < n_local; advance(wr)) {
+        if (!mbar_wait(smem_u32(&full_bar[wr.s]), wr.phase, a.timeout_ns)) {
             const uint32_t kid = KIND == KIND_COPY ? K_COPY : KIND == KIND_ROUNDTRIP ? K_ROUNDTRIP
                                                                                     : K_REDUCE;
-            record_timeout(a.status, kid, s, parity, group_of(i) * G);
+            record_timeout(a.status, kid, wr.s, wr.phase, group_of(wr.i) * G);
             // Let every load still in flight land (bounded) before the stages go away.
-            for (uint64_t j = i + 1; j < issued; j++) {
+            for (uint64_t j = wr.i + 1; j < ld.i; j++) {
                 mbar_wait(smem_u32(&full_bar[j % S]), (uint32_t)((j / S) & 1), a.timeout_ns);
             }
             break;
         }
-        write_out(i);
-        if (i >= lag && issued < n_local) {
+        write_out(wr);
+        if (wr.i >= lag && ld.i < n_local) {
             if (lag) {
                 bulk_wait_read<1>();  // group i - 1's write has read its stage
             } else {
                 bulk_wait_read<0>();  // the only stage: group i's write has read it
             }
-            issue(issued++);
+            issue(ld);
+            advance(ld);
         }
     }
     bulk_wait_all<0>();

@@ -296,6 +296,20 @@ __device__ __forceinline__ void grid_next(const BoxWalk& w, uint32_t* k)
     }
 }
 
+// Counters k += digits d, with carries (mixed radix: the grid's box counts).
+__device__ __forceinline__ void grid_add(const BoxWalk& w, uint32_t* k, const uint32_t* d)
+{
+    uint32_t carry = 0;
+#pragma unroll
+    for (int i = 0; i < 5; i++) {
+        if (i < (int)w.rank) {
+            const uint64_t v = (uint64_t)k[i] + d[i] + carry;
+            carry = v >= w.grid_nb[i] ? 1u : 0u;
+            k[i] = (uint32_t)(carry ? v - w.grid_nb[i] : v);
+        }
+    }
+}
+
 // Start coordinates of the launch's box `b` (grid: k[i] * box[i] with dim 0 fastest).
 __device__ __forceinline__ void box_start(const BoxWalk& w, uint64_t b, int32_t* c)
 {
