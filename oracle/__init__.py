@@ -85,6 +85,11 @@ def lib():
         L.orc_f16_from_double.restype = ctypes.c_uint16
         L.orc_bf16_from_double.argtypes = [ctypes.c_double]
         L.orc_bf16_from_double.restype = ctypes.c_uint16
+        u64 = ctypes.c_uint64
+        for name in ("orc_gemm_dot", "orc_gemm_dot_abs"):
+            getattr(L, name).argtypes = [u8p, u64, u8p, u64, u64, u64, u64]
+            getattr(L, name).restype = ctypes.c_double
+        L.orc_gemm_block.argtypes = [u8p, u64, u8p, u64, u64, u64, u64, u64, u64, u8p]
         L.orc_tile_checksum.argtypes = [u8p, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
                                         P(ctypes.c_float), P(ctypes.c_uint64)]
         L.orc_stream_checksums.argtypes = [P(_OrcMap), P(_OrcMap), ctypes.c_uint64,
@@ -272,6 +277,35 @@ def tile_reduce(dst: Map, src: Map, type_: int, op: int, threads: int = 1, b0: i
     L = lib()
     _run(lambda x0, x1: L.orc_tile_reduce(ctypes.byref(dst.c), ctypes.byref(src.c), b0 + x0,
                                           b0 + x1, type_, op), b1 - b0, threads)
+
+
+def _bf16_matrix(x: np.ndarray, name: str) -> np.ndarray:
+    if x.dtype != np.uint16 or x.ndim != 2 or not x.flags.c_contiguous:
+        raise ValueError(f"{name} must be a C-contiguous 2-D uint16 (bf16 bits) array")
+    return x
+
+
+def gemm(a: np.ndarray, b: np.ndarray, m0: int = 0, m1: int | None = None, n0: int = 0,
+         n1: int | None = None, k: int | None = None) -> np.ndarray:
+    """C[m][n] = sum_k A[m][k] * B[n][k] in double, for bf16 bit arrays A (M x K) and B (N x K);
+    the block [m0, m1) x [n0, n1)."""
+    a, b = _bf16_matrix(a, "a"), _bf16_matrix(b, "b")
+    k = a.shape[1] if k is None else k
+    if k > a.shape[1] or k > b.shape[1]:
+        raise ValueError("k exceeds a row")
+    m1 = a.shape[0] if m1 is None else m1
+    n1 = b.shape[0] if n1 is None else n1
+    out = np.zeros((m1 - m0, n1 - n0), np.float64)
+    lib().orc_gemm_block(_ptr(a), a.shape[1], _ptr(b), b.shape[1], k, m0, m1, n0, n1, _ptr(out))
+    return out
+
+
+def gemm_entry(a: np.ndarray, b: np.ndarray, m: int, n: int):
+    """(C[m][n], sum_k |A[m][k] * B[n][k]|), both in double."""
+    a, b = _bf16_matrix(a, "a"), _bf16_matrix(b, "b")
+    L = lib()
+    args = (_ptr(a), a.shape[1], _ptr(b), b.shape[1], a.shape[1], m, n)
+    return float(L.orc_gemm_dot(*args)), float(L.orc_gemm_dot_abs(*args))
 
 
 def tile_checksum(img: np.ndarray, rows: int, row_bytes: int, span: int):

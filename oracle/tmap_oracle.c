@@ -382,6 +382,39 @@ void orc_tile_reduce(const orc_map* dst, const orc_map* src, uint64_t b0, uint64
 }
 
 /* ---------------------------------------------------------------------------------------------
+ * GEMM consumer of the k-ordered ring: C = A * B^T, one output element at a time, k in order.
+ * ------------------------------------------------------------------------------------------- */
+double orc_gemm_dot(const uint16_t* a, uint64_t lda, const uint16_t* b, uint64_t ldb, uint64_t k,
+                    uint64_t m, uint64_t n)
+{
+    double acc = 0.0;
+    for (uint64_t i = 0; i < k; i++) {
+        acc += bf16_to_double(a[m * lda + i]) * bf16_to_double(b[n * ldb + i]);
+    }
+    return acc;
+}
+
+double orc_gemm_dot_abs(const uint16_t* a, uint64_t lda, const uint16_t* b, uint64_t ldb,
+                        uint64_t k, uint64_t m, uint64_t n)
+{
+    double acc = 0.0;
+    for (uint64_t i = 0; i < k; i++) {
+        acc += fabs(bf16_to_double(a[m * lda + i]) * bf16_to_double(b[n * ldb + i]));
+    }
+    return acc;
+}
+
+void orc_gemm_block(const uint16_t* a, uint64_t lda, const uint16_t* b, uint64_t ldb, uint64_t k,
+                    uint64_t m0, uint64_t m1, uint64_t n0, uint64_t n1, double* out)
+{
+    for (uint64_t m = m0; m < m1; m++) {
+        for (uint64_t n = n0; n < n1; n++) {
+            out[(m - m0) * (n1 - n0) + (n - n0)] = orc_gemm_dot(a, lda, b, ldb, k, m, n);
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------------------------------
  * Ring consumer checksum.  The pages' pipeline ([MLSys-TMA] §"把 TMA 放进 pipeline") hands each
  * stage to a consumer but leave what it computes open; this library's consumer reads every element
  * of the tile through the swizzle and reduces it to one fp32 value and one exact integer.

@@ -40,6 +40,9 @@
  *                             bf16 add against an exact rational sum rounded half-to-even in
  *                             Python; min / max / integer ops against numpy.  Rounding of f16 /
  *                             bf16 adds is this library's reading (the pages do not state it).
+ *   orc_gemm_* .............. pinned: small integer matrices against exact Python integer
+ *                             arithmetic, one-hot rows (C picks entries of B), random bf16 values
+ *                             against an exact rational sum, and C(A, B) = C(B, A) transposed.
  *   orc_tile_checksum ....... pinned: numpy sequential cumsum + pairwise tree, and an exact
  *                             integer bit-sum.  The checksum itself is this library's definition;
  *                             the pages are silent on what the ring's consumer computes.
@@ -130,6 +133,20 @@ void orc_tile_reduce(const orc_map* dst, const orc_map* src, uint64_t b0, uint64
 double orc_f16_to_double(uint16_t h);
 uint16_t orc_f16_from_double(double v);
 uint16_t orc_bf16_from_double(double v);
+
+/* The k-ordered ring's tensor-core consumer ([MLSys-TMA] overview and §"把 TMA 放进 pipeline": while
+ * the tensor cores work on the A and B tiles of step k, TMA loads those of step k + 1): for bf16 A
+ * (M x K, row m at a + m * lda elements) and B (N x K, row n at b + n * ldb), both with K
+ * contiguous, C[m][n] = sum over k of A[m][k] * B[n][k].  orc_gemm_dot returns that sum in double
+ * (each bf16 product is exact in double; the K-term sum is exact up to about K * 2^-53 relative),
+ * orc_gemm_dot_abs the sum of |A[m][k] * B[n][k]| (the scale of the fp32 tolerance). */
+double orc_gemm_dot(const uint16_t* a, uint64_t lda, const uint16_t* b, uint64_t ldb, uint64_t k,
+                    uint64_t m, uint64_t n);
+double orc_gemm_dot_abs(const uint16_t* a, uint64_t lda, const uint16_t* b, uint64_t ldb,
+                        uint64_t k, uint64_t m, uint64_t n);
+/* C[m][n] for m in [m0, m1), n in [n0, n1) into out (row-major, (n1 - n0) per row). */
+void orc_gemm_block(const uint16_t* a, uint64_t lda, const uint16_t* b, uint64_t ldb, uint64_t k,
+                    uint64_t m0, uint64_t m1, uint64_t n0, uint64_t n1, double* out);
 
 /* Checksum of one bf16 tile image of `rows` rows of `row_bytes` bytes (rows a power of two):
  * rowsum_r is the sequential fp32 sum of the row's elements in logical order, the tile value is

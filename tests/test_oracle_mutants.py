@@ -32,6 +32,14 @@ MUTANTS = {
                              "case ORC_FILL_NAN_F32: v = 0x7F800000u;"),
     "fill_bytes_reversed": ("return (uint8_t)(v >> (8 * k));",
                             "return (uint8_t)(v >> (8 * (m->esize - 1 - k)));"),
+    "gemm_drops_last_k": ("    for (uint64_t i = 0; i < k; i++) {\n        acc += bf16_to_double(a[m * lda + i]) * bf16_to_double(b[n * ldb + i]);",
+                          "    for (uint64_t i = 0; i + 1 < k; i++) {\n        acc += bf16_to_double(a[m * lda + i]) * bf16_to_double(b[n * ldb + i]);"),
+    "gemm_b_transposed": ("acc += bf16_to_double(a[m * lda + i]) * bf16_to_double(b[n * ldb + i]);",
+                          "acc += bf16_to_double(a[m * lda + i]) * bf16_to_double(b[i * ldb + n]);"),
+    "gemm_float_accumulator": ("    double acc = 0.0;\n    for (uint64_t i = 0; i < k; i++) {\n        acc += bf16_to_double(a[m * lda + i])",
+                               "    float acc = 0.0f;\n    for (uint64_t i = 0; i < k; i++) {\n        acc += bf16_to_double(a[m * lda + i])"),
+    "gemm_block_rows_swapped": ("out[(m - m0) * (n1 - n0) + (n - n0)] = orc_gemm_dot(a, lda, b, ldb, k, m, n);",
+                                "out[(m - m0) * (n1 - n0) + (n - n0)] = orc_gemm_dot(a, lda, b, ldb, k, n, m);"),
     "grid_floor_not_ceil": ("return (m->dim[i] + m->box[i] - 1) / m->box[i];",
                             "return m->dim[i] / m->box[i] + (m->dim[i] < m->box[i]);"),
     "stride_index_transposed": ("off += g[i] * m->stride[i];",
@@ -70,6 +78,7 @@ def test_pins_reject_mutant(name, tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(ROOT, "tests", "test_oracle_pins.py"),
                         os.path.join(ROOT, "tests", "test_oracle_reduce_pins.py"),
-                        os.path.join(ROOT, "tests", "test_oracle_stride_fill_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_stride_fill_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_gemm_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"
