@@ -26,7 +26,7 @@ __all__ = [
     "TmapError", "TensorMap", "tmap_plan", "tmap_encode", "tmap_replace_address",
     "tmap_force_fallback", "tile_load_image", "tiled_copy", "tiled_roundtrip", "tile_reduce_add",
     "tile_reduce", "TM_RED_ADD", "TM_RED_MIN", "TM_RED_MAX",
-    "stream_tiles", "tiled_copy_noalloc", "TM_NOALLOC_MAX_BOXES", "tm_stream_check",
+    "stream_tiles", "stream_gemm", "tiled_copy_noalloc", "TM_NOALLOC_MAX_BOXES", "tm_stream_check",
     "tm_selftest_wait_timeout", "tm_pick_swizzle", "tm_last_error",
     "library_path", "TM_OK", "TM_EINVAL", "TM_EALIGN", "TM_ERANGE", "TM_EUNSUPPORTED",
     "TM_ECUDA", "TM_ETIMEOUT", "TM_U8", "TM_U16", "TM_U32", "TM_S32", "TM_U64", "TM_S64",
@@ -73,6 +73,7 @@ _SIGS = {
     "tile_reduce_add": [_vp, _vp, _vp],
     "tile_reduce": [_vp, _vp, ctypes.c_int, _vp],
     "stream_tiles": [_vp, _vp, _u32, _vp, _vp, _vp, _vp, _vp],
+    "stream_gemm": [_vp, _vp, _vp, _u64, _u32, _vp],
     "tm_stream_check": [_vp],
     "tm_selftest_wait_timeout": [_u64, _vp],
     "tm_last_error": [],
@@ -273,6 +274,14 @@ def stream_tiles(a: TensorMap, b: TensorMap, stages, cs_a, cs_b, bits_a, bits_b,
                  stream=None) -> None:
     _check(_L.stream_tiles(a.ptr, b.ptr, int(stages), _addr(cs_a), _addr(cs_b), _addr(bits_a),
                            _addr(bits_b), _stream(stream)), "stream_tiles")
+
+
+def stream_gemm(a: TensorMap, b: TensorMap, c, ldc=None, stages: int = 4, stream=None) -> None:
+    """C = A * B^T on the tensor cores: A map {K, M} box {64, 128}, B map {K, N} box {64, 256},
+    c an fp32 device buffer of M rows, ldc elements apart (default N)."""
+    ldc = b.dims[1] if ldc is None else ldc
+    _check(_L.stream_gemm(a.ptr, b.ptr, _addr(c), int(ldc), int(stages), _stream(stream)),
+           "stream_gemm")
 
 
 def tm_stream_check(stream=None) -> int:

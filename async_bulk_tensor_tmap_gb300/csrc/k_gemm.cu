@@ -1,0 +1,252 @@
+// k_gemm.cu -- the k-ordered ring feeding the 5th-generation tensor cores: C = A * B^T.
+//
+// [MLSys-TMA] = mlc.ai "Modern GPU Programming for MLSys", chapter "异步数据搬运：TMA".  Overview:
+// while the tensor cores work on the A and B tiles of step k, the next tiles must already be on
+// their way into shared memory, and TMA writes them in the swizzled layout the MMA reads.
+// §"把 TMA 放进 pipeline": stages are handed between the TMA producer and the MMA consumer with
+// barriers -- the consumer waits for a stage's bytes, the producer for the consumer to be done
+// with a stage before refilling it.
+//
+// One CTA computes one 128 x 256 tile of C (fp32) from bf16 A (M x K) and B (N x K), both with K
+// contiguous, through an S-stage ring of 48 KiB stages (A 128 x 64 and B 256 x 64, 128-byte
+// swizzled, one mbarrier per stage counting both tiles' bytes):
+//   warp 0  elected lane: TMA loads of step k into stage k % S once the stage is empty
+//   warp 1  owns the tensor memory (tcgen05.alloc / dealloc); its elected lane waits for each stage,
+//           issues four tcgen05.mma (K = 16 each) accumulating into tensor memory, and commits them
+//           to the stage's empty barrier (the stage is free once those MMAs have read it); after the
+//           last step it commits to the done barrier
+//   warps 2-5 wait for done, read the accumulator with tcgen05.ld (each warp the 32 tensor-memory
+//           lanes of its quarter, one row of the tile per lane) and store the in-bounds part of C
+// Every wait is bounded; after one gives up the CTA still drains what it issued, reaches the final
+// barrier and frees its tensor memory.
+#include "tm_ptx.cuh"
+
+namespace tmk {
+
+namespace {
+
+constexpr uint32_t kBM = 128, kBN = 256, kBK = 64, kUK = 16;
+constexpr uint32_t kTileA = kBM * kBK * 2;         // 16 KiB
+constexpr uint32_t kTileB = kBN * kBK * 2;         // 32 KiB
+constexpr uint32_t kGemmStage = kTileA + kTileB;   // 48 KiB, a multiple of 1024
+constexpr uint32_t kGemmThreads = 192;
+constexpr uint32_t kTmemCols = kBN;                // fp32 accumulator: one column per N
+
+// Instruction descriptor of tcgen05.mma kind::f16: D f32 (bits 4-5 = 1), A and B bf16 (bits 7-9
+// and 10-12 = 1), both K-major (bits 15, 16 = 0), N >> 3 in bits 17-22, M >> 4 in bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((kBN >> 3) << 17) |
+                            ((kBM >> 4) << 24);
+
+// Shared-memory matrix descriptor of a K-major tile of 128-byte rows written by TMA with the
+// 128-byte swizzle: start address >> 4 in bits 0-13, leading-dimension offset (unused for this
+// layout) 16 bytes, stride between 8-row groups 1024 bytes >> 4 in bits 32-45, descriptor version 1
+// in bits 46-47, swizzle mode 2 (128-byte) in bits 61-63.  The tile base is 1024-byte aligned, so
+// the K = 16 steps inside a 128-byte row advance the start address by 32 bytes.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr)
+{
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot_saddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot_saddr),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D (tensor memory) = A * B^T (+ D when accumulate != 0), A and B from shared-memory descriptors.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                         uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives on the mbarrier once every tcgen05 operation this thread issued before has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar_saddr)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar_saddr)
+                 : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's tensor-memory lane (warp-wide, .32x32b shape).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r)
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+        "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+        "%30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_gemm(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
+           const __grid_constant__ GemmArgs g)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kGemmMaxStages];
+    __shared__ __align__(8) uint64_t empty_bar[kGemmMaxStages];
+    __shared__ __align__(8) uint64_t done_bar;
+    __shared__ uint32_t tmem_slot;
+
+    const uint32_t base = (smem_u32(smem_raw) + (kStageAlign - 1)) & ~(kStageAlign - 1);
+    const uint32_t S = g.stages;
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // consecutive CTAs take consecutive M tiles of one N tile, so a B tile is read from L2 by
+    // the CTAs that run together
+    const uint32_t mt = blockIdx.x % g.mtiles, nt = blockIdx.x / g.mtiles;
+
+    if (threadIdx.x == 0) {
+        for (uint32_t s = 0; s < S; s++) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        mbar_init(smem_u32(&done_bar), 1);
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+
+    if (warp == 0) {
+        // ---------------- producer ----------------
+        if (elect_one()) {
+            prefetch_tmap(&ma);
+            prefetch_tmap(&mb);
+            uint32_t s = 0, wraps = 0, kb = 0;
+            for (; kb < g.kblocks; kb++) {
+                if (wraps > 0) {
+                    const uint32_t parity = (wraps - 1) & 1u;
+                    if (!mbar_wait(smem_u32(&empty_bar[s]), parity, g.timeout_ns)) {
+                        record_timeout(g.status, K_GEMM, s, parity, blockIdx.x);
+                        break;
+                    }
+                }
+                const uint32_t bar = smem_u32(&full_bar[s]);
+                const int32_t ca[2] = {(int32_t)(kb * kBK), (int32_t)(mt * kBM)};
+                const int32_t cb[2] = {(int32_t)(kb * kBK), (int32_t)(nt * kBN)};
+                mbar_arrive_expect_tx(bar, kGemmStage);
+                tma_load<2>(base + s * kGemmStage, &ma, ca, bar);
+                tma_load<2>(base + s * kGemmStage + kTileA, &mb, cb, bar);
+                if (++s == S) {
+                    s = 0;
+                    wraps++;
+                }
+            }
+            if (kb < g.kblocks) {
+                // After a failure: the last loads issued may still be landing; wait for them.
+                for (uint32_t j = kb > S ? kb - S : 0; j < kb; j++)
+                    mbar_wait(smem_u32(&full_bar[j % S]), (j / S) & 1u, g.timeout_ns);
+            } else {
+                // The MMA warp's last releases of the stages must land before shared memory goes
+                // away: wait for the empty barriers of the last S steps (bounded).
+                for (uint32_t j = kb > S ? kb - S : 0; j < kb; j++)
+                    mbar_wait(smem_u32(&empty_bar[j % S]), (j / S) & 1u, g.timeout_ns);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (elect_one()) {
+            uint32_t s = 0, phase = 0;
+            for (uint32_t kb = 0; kb < g.kblocks; kb++) {
+                if (!mbar_wait(smem_u32(&full_bar[s]), phase, g.timeout_ns)) {
+                    record_timeout(g.status, K_GEMM, s, phase, blockIdx.x);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = base + s * kGemmStage, b0 = a0 + kTileA;
+#pragma unroll
+                for (uint32_t ks = 0; ks < kBK / kUK; ks++) {
+                    mma_bf16(tmem, sw128_desc(a0 + ks * kUK * 2), sw128_desc(b0 + ks * kUK * 2),
+                             kIdesc, (kb | ks) != 0 ? 1u : 0u);
+                }
+                tc_commit(smem_u32(&empty_bar[s]));  // the stage is free once these MMAs read it
+                if (++s == S) {
+                    s = 0;
+                    phase ^= 1u;
+                }
+            }
+            tc_commit(smem_u32(&done_bar));  // every MMA issued above has completed
+        }
+        __syncwarp();
+    } else {
+        // ---------------- epilogue: warps 2-5, tensor-memory lane quarter warp % 4 ----------------
+        const uint32_t q = warp & 3u;
+        const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&done_bar), 0, g.timeout_ns));
+        tc_fence_after();
+        if (!ok) {
+            if (lane == 0) record_timeout(g.status, K_GEMM, 0, 0, blockIdx.x);
+        } else {
+            const uint32_t row = mt * kBM + q * 32 + lane;
+            float* const crow = g.c + (uint64_t)row * g.ldc;
+            const uint32_t n0 = nt * kBN;
+            for (uint32_t c0 = 0; c0 < kBN; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((q * 32) << 16) + c0, r);
+                if (row < g.m) {
+                    const uint32_t n = n0 + c0;
+                    if (n + 32 <= g.n) {
+#pragma unroll
+                        for (int v = 0; v < 8; v++) {
+                            *reinterpret_cast<float4*>(crow + n + 4 * v) =
+                                make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                            __uint_as_float(r[4 * v + 2]),
+                                            __uint_as_float(r[4 * v + 3]));
+                        }
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < 32; v++) {
+                            if (n + v < g.n) crow[n + v] = __uint_as_float(r[v]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // Every tensor-memory read and every MMA has completed (the done barrier, tcgen05.wait::ld):
+    // free the accumulator.
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+cudaError_t launch_gemm(const CUtensorMap* a, const CUtensorMap* b, const GemmArgs& g,
+                        uint32_t grid, size_t smem, cudaStream_t s)
+{
+    cudaError_t e =
+        cudaFuncSetAttribute(k_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_gemm<<<grid, kGemmThreads, smem, s>>>(*a, *b, g);
+    return cudaGetLastError();
+}
+
+}  // namespace tmk

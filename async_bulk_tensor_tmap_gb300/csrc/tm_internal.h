@@ -15,7 +15,7 @@ constexpr uint32_t kStageAlign = 1024; // 128B swizzle is computed on smem addre
 // Kernel ids recorded with a timeout.
 enum KernelId : uint32_t {
     K_COPY = 1, K_ROUNDTRIP = 2, K_REDUCE = 3, K_STREAM = 4, K_FB_COPY = 5, K_FB_STORE = 6,
-    K_FB_REDUCE = 7, K_SELFTEST = 8
+    K_FB_REDUCE = 7, K_SELFTEST = 8, K_GEMM = 9
 };
 
 // Per-device status word written by a kernel whose bounded wait gave up.
@@ -171,6 +171,20 @@ struct RingArgs {
     StatusBlock* status;
 };
 
+// Tensor-core consumer of the k-ordered ring (stream_gemm): C = A * B^T.
+constexpr uint32_t kGemmMaxStages = 4;
+struct GemmArgs {
+    uint32_t m, n, k;        // C is m x n; A is m x k, B is n x k (bf16, k contiguous)
+    uint32_t mtiles, ntiles; // 128-row and 256-column tiles of C
+    uint32_t kblocks;        // 64-wide steps along k
+    uint32_t stages;         // 2..kGemmMaxStages
+    uint32_t pad;
+    float* c;                // fp32, row-major
+    uint64_t ldc;            // elements between rows of C
+    uint64_t timeout_ns;
+    StatusBlock* status;
+};
+
 // Launchers (defined next to their kernels).  Return a cudaError_t.
 // Reduce kinds: KIND_REDUCE + op, op 0 add, 1 min, 2 max.
 enum StreamKind : int {
@@ -185,6 +199,8 @@ cudaError_t launch_fb_reduce(const FbArgs& a, uint32_t grid, cudaStream_t s);
 cudaError_t launch_ring(const CUtensorMap* a, const CUtensorMap* b, const RingArgs& r,
                         uint32_t grid, size_t smem, cudaStream_t s);
 cudaError_t launch_selftest(uint64_t timeout_ns, StatusBlock* status, cudaStream_t s);
+cudaError_t launch_gemm(const CUtensorMap* a, const CUtensorMap* b, const GemmArgs& g,
+                        uint32_t grid, size_t smem, cudaStream_t s);
 
 // Sets the thread's tm_last_error() text; returns `code`.
 int set_last_error(int code, const char* msg);

@@ -688,6 +688,61 @@ int stream_tiles(const tm_desc* a, const tm_desc* b, uint32_t stages, float* cs_
                         "ring launch");
 }
 
+int stream_gemm(const tm_desc* a, const tm_desc* b, float* c, uint64_t ldc, uint32_t stages,
+                void* stream)
+{
+    if (!valid_desc(a) || !valid_desc(b)) return fail(TM_EINVAL, "descriptor is not filled");
+    if (!c) return fail(TM_EINVAL, "c is NULL");
+    const uint32_t want_box[2][2] = {{64, 128}, {64, 256}};
+    const tm_desc* ops[2] = {a, b};
+    for (int i = 0; i < 2; i++) {
+        const tm_desc* d = ops[i];
+        if (d->dtype != TM_BF16 || d->rank != 2)
+            return fail(TM_EUNSUPPORTED, "stream_gemm needs rank-2 TM_BF16 maps");
+        if (d->box[0] != want_box[i][0] || d->box[1] != want_box[i][1])
+            return fail(TM_EUNSUPPORTED, "stream_gemm needs boxes {64, 128} for A and {64, 256} for B");
+        if (d->swizzle != TM_SWIZZLE_128B)
+            return fail(TM_EUNSUPPORTED, "stream_gemm needs 128-byte swizzled maps");
+        if (d->path != TM_PATH_TMA || !unit_steps(d) || d->oob != TM_OOB_ZERO)
+            return fail(TM_EUNSUPPORTED, "stream_gemm needs TMA-path maps with unit steps and zero fill");
+    }
+    if (a->dim[0] != b->dim[0])
+        return fail(TM_EINVAL, "A has K = %llu, B has K = %llu", (unsigned long long)a->dim[0],
+                    (unsigned long long)b->dim[0]);
+    const uint64_t M = a->dim[1], N = b->dim[1], K = a->dim[0];
+    if (M >= (1ull << 31) || N >= (1ull << 31) || K >= (1ull << 31))
+        return fail(TM_ERANGE, "M, N and K must be below 2^31");
+    if (ldc < N) return fail(TM_EINVAL, "ldc %llu is below N = %llu", (unsigned long long)ldc,
+                             (unsigned long long)N);
+    if ((uintptr_t)c % 16 || ldc % 4)
+        return fail(TM_EALIGN, "c must be 16-byte aligned and ldc a multiple of 4");
+    if (stages < 2 || stages > kGemmMaxStages)
+        return fail(TM_ERANGE, "stages %u outside 2..%u", stages, kGemmMaxStages);
+    DevState* ds = nullptr;
+    int rc = device_state(&ds);
+    if (rc) return rc;
+    GemmArgs g;
+    memset(&g, 0, sizeof(g));
+    g.m = (uint32_t)M;
+    g.n = (uint32_t)N;
+    g.k = (uint32_t)K;
+    g.mtiles = (uint32_t)((M + 127) / 128);
+    g.ntiles = (uint32_t)((N + 255) / 256);
+    g.kblocks = (uint32_t)((K + 63) / 64);
+    g.stages = stages;
+    g.c = c;
+    g.ldc = ldc;
+    g.timeout_ns = wait_limit_ns();
+    g.status = ds->status;
+    const uint64_t grid = (uint64_t)g.mtiles * g.ntiles;
+    if (grid >= (1ull << 31)) return fail(TM_ERANGE, "too many tiles");
+    const size_t smem = (size_t)stages * (16384 + 32768) + kStageAlign;
+    if (smem > cta_budget(*ds, 1) + 1024) return fail(TM_ERANGE, "%u stages exceed shared memory", stages);
+    return check_launch(launch_gemm((const CUtensorMap*)a->tmap, (const CUtensorMap*)b->tmap, g,
+                                    (uint32_t)grid, smem, (cudaStream_t)stream),
+                        "gemm launch");
+}
+
 int tm_stream_check(void* stream)
 {
     cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
@@ -702,8 +757,9 @@ int tm_stream_check(void* stream)
     if ((e = cudaMemset(ds->status, 0, sizeof(sb))) != cudaSuccess)
         return cuda_fail(e, "clearing the status word");
     static const char* names[] = {"?", "tiled copy", "round trip", "reduce-add", "ring",
-                                  "fallback copy", "fallback store", "fallback reduce", "self-test"};
-    const char* kn = sb.kernel < 9 ? names[sb.kernel] : "?";
+                                  "fallback copy", "fallback store", "fallback reduce", "self-test",
+                                  "gemm"};
+    const char* kn = sb.kernel < 10 ? names[sb.kernel] : "?";
     return fail(sb.code, "%s kernel: wait gave up in block %u, stage %u, parity %u, box %llu", kn,
                 sb.block, sb.stage, sb.phase, (unsigned long long)sb.box);
 }

@@ -103,6 +103,9 @@ class HostWorkload:
         self.w5b_a, self.w5b_b = workloads.w5b_tensors(m5b, 4096, m5b) if need("w5b") else (None, None)
         # widened reduce ops (not in the default step): bf16 add on its own tensors; s32 min and
         # f32 max over the W5a buffers
+        # the ring in GEMM order with its tensor-core consumer (not in the default step)
+        self.w7_a, self.w7_b = (workloads.w7_operands(int(8192 / scale), int(8192 / scale))
+                                if ops is not None and need("w7") else (None, None))
         if ops is not None and need("w5c"):
             if self.w5a_dst is None:
                 self.w5a_dst, self.w5a_src = workloads.w5a_tensors(r5a)
@@ -169,6 +172,12 @@ def op_table(h: HostWorkload):
 #     read.
 #   w6.cols2_rt: those images stored back: images read, every sector of the tensor written.
 #   w6.nan: the W4 rank-3 copy with NaN out-of-bounds fill (bytes as w4r3.copy).
+#   w7.gemm: C = A * B^T on the tensor cores, A and B 8192 x 4096 bf16, C 8192 x 8192 fp32 (bytes:
+#     A + B read once, C written; its figure of merit is TFLOP/s, 2 * M * N * K per call).
+def gemm_flops(h: HostWorkload) -> int:
+    return 2 * h.w7_a.shape[0] * h.w7_b.shape[0] * h.w7_a.shape[1] if h.w7_a is not None else 0
+
+
 def extra_ops(h: HostWorkload):
     n = inbounds_bytes(h.r5a) // 4  # elements
     rows2_img = box_count(h.r6_rows2) * box_bytes(h.r6_rows2)
@@ -177,7 +186,9 @@ def extra_ops(h: HostWorkload):
     return [("w5c.add_bf16", 3 * 2 * n), ("w5c.min_s32", 3 * 4 * n), ("w5c.max_f32", 3 * 4 * n),
             ("w6.rows2", 2 * rows2_img), ("w6.cols2", w3 + cols2_img),
             ("w6.cols2_rt", cols2_img + w3),
-            ("w6.nan", inbounds_bytes(h.r6_nan) + box_count(h.r6_nan) * box_bytes(h.r6_nan))]
+            ("w6.nan", inbounds_bytes(h.r6_nan) + box_count(h.r6_nan) * box_bytes(h.r6_nan))] + \
+        ([("w7.gemm", h.w7_a.nbytes + h.w7_b.nbytes + 4 * h.w7_a.shape[0] * h.w7_b.shape[0])]
+         if h.w7_a is not None else [])
 
 
 # ------------------------------------------------------------------------------------------------
@@ -222,6 +233,14 @@ class GpuWorkload:
             self.t["cs_b"] = torch.zeros(n, dtype=torch.float32, device="cuda")
             self.t["bits_a"] = torch.zeros(n, dtype=torch.int64, device="cuda")
             self.t["bits_b"] = torch.zeros(n, dtype=torch.int64, device="cuda")
+        if h.w7_a is not None:
+            (M, K), N = h.w7_a.shape, h.w7_b.shape[0]
+            self.t["w7_a"], self.t["w7_b"] = dev(h.w7_a), dev(h.w7_b)
+            self.t["w7_c"] = torch.empty(M * N, dtype=torch.float32, device="cuda")
+            self.maps["w7_a"] = tm.tmap_encode(bf, self.t["w7_a"], [K, M], [K * 2], [64, 128],
+                                               swizzle=tm.TM_SWIZZLE_128B)
+            self.maps["w7_b"] = tm.tmap_encode(bf, self.t["w7_b"], [K, N], [K * 2], [64, 256],
+                                               swizzle=tm.TM_SWIZZLE_128B)
         if h.w5c_dst is not None:
             self.t["w5c_dst"], self.t["w5c_src"] = dev(h.w5c_dst), dev(h.w5c_src)
             self.maps["w5c_dst"] = enc(tm.TM_BF16, self.t["w5c_dst"], h.r5c)
@@ -260,6 +279,8 @@ class GpuWorkload:
         elif kind == "ring":
             tm.stream_tiles(m["w5b_a"], m["w5b_b"], self.ring_stages, t["cs_a"], t["cs_b"],
                             t["bits_a"], t["bits_b"], s)
+        elif kind == "gemm":
+            tm.stream_gemm(m["w7_a"], m["w7_b"], t["w7_c"], stream=s)
         elif kind in ("rows2", "cols2", "nan"):
             tm.tiled_copy(m[f"w6_{kind}"], None, t[f"w6_{kind}_img"], s)
         elif kind == "cols2_rt":
@@ -462,8 +483,8 @@ def oracle_sample(h: HostWorkload, ops, fraction: float, threads: int):
 
     spent, covered = 0.0, 0
     if not hasattr(h, "scratch3"):  # destinations of the sampled round trips, made once
-        h.scratch3 = np.empty_like(h.w3)
-        h.scratch4 = h.w4.copy()
+        h.scratch3 = np.empty_like(h.w3) if h.w3 is not None else None
+        h.scratch4 = h.w4.copy() if h.w4 is not None else None
     scratch3, scratch4 = h.scratch3, h.scratch4
     for name, nbytes in ops:
         base, kind = name.split(".")
@@ -515,6 +536,13 @@ def oracle_sample(h: HostWorkload, ops, fraction: float, threads: int):
                 return sec
             sec, cov = sample(run, r, nbytes)
             spent, covered = spent + sec, covered + cov
+        elif kind == "gemm":
+            rows = h.w7_a.shape[0]
+            k = max(1, int(rows * fraction))
+            t0 = time.perf_counter()
+            oracle_gemm_rows(h.w7_a, h.w7_b, k, threads)
+            spent += time.perf_counter() - t0
+            covered += nbytes * k // rows
         elif kind == "ring":
             n = box_count(h.r5b_a)
             k = max(1, int(n * fraction))
@@ -524,6 +552,17 @@ def oracle_sample(h: HostWorkload, ops, fraction: float, threads: int):
             spent += time.perf_counter() - t0
             covered += nbytes * k // n
     return spent, covered
+
+
+def oracle_gemm_rows(a, b, rows: int, threads: int):
+    """The oracle's C = A * B^T for the first `rows` rows of A, rows split over threads (ctypes
+    releases the GIL)."""
+    import oracle
+    from concurrent.futures import ThreadPoolExecutor
+    step = -(-rows // threads)
+    with ThreadPoolExecutor(threads) as ex:
+        list(ex.map(lambda r0: oracle.gemm(a, b, r0, min(rows, r0 + step)),
+                    range(0, rows, step)))
 
 
 def calibrated_fraction(h: HostWorkload, ops, threads: int, target_s: float) -> float:
@@ -548,6 +587,15 @@ def measured_hbm_peak():
             return float(json.load(f)["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return 6800.0, "fallback"
+
+
+def measured_bf16_peak():
+    """Dense bf16 TFLOP/s of a cuBLAS GEMM timed alone (burst) on the GB300s."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
 
 
 def tma_kernel_source() -> bytes:
@@ -659,16 +707,29 @@ def main():
     value = weak_scaling_value(step_bytes, step_ms, world)
     peak, peak_kind = measured_hbm_peak()
     breakdown = {}
+    tpeak, tpeak_kind = measured_bf16_peak()
     for name, nbytes in ops:
         ms = statistics.mean(per[name])
         breakdown[name] = {"ms": round(ms, 4), "GB/s": round(nbytes / ms / 1e6, 1),
                            "frac_of_peak": round(nbytes / ms / 1e6 / peak, 3),
                            "bytes": nbytes}
+        if name == "w7.gemm":
+            tflops = gemm_flops(h) / ms / 1e9
+            breakdown[name].update({"TFLOP/s": round(tflops, 1),
+                                    "frac_of_bf16_peak": round(tflops / tpeak, 3)})
     dom = max(ops, key=lambda o: statistics.mean(per[o[0]]))
     dom_name, dom_bytes = dom
     dom_ms = statistics.mean(per[dom_name])
     achieved = dom_bytes / dom_ms / 1e6
-    if any(n.startswith(("w5c", "w6")) for n, _ in ops):
+    roofline = {"kernel": dom_name, "bound": "hbm", "achieved": achieved, "peak": peak,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": recorded_traffic(dom_name) if args.scale == 1 else None}
+    if dom_name == "w7.gemm":  # a dense contraction: against the measured bf16 tensor peak
+        tflops = gemm_flops(h) / dom_ms / 1e9
+        roofline = {"kernel": dom_name, "bound": "tensor", "achieved": tflops, "peak": tpeak,
+                    "peak_kind": tpeak_kind, "unit": "TFLOP/s", "frac": tflops / tpeak,
+                    "traffic": None}
+    if any(n.startswith(("w5c", "w6", "w7")) for n, _ in ops):
         args.e2e_steps = 0  # the widened ops have no end-to-end leg
     if args.e2e_steps > 0:
         e2e_ms, bi, bo = e2e_run(g, h, ops, args.e2e_steps)
@@ -697,9 +758,7 @@ def main():
                    "hbm_frac_of_peak": round(value / world / peak, 3),
                    "paths": {k: ("tma" if p == 1 else "fallback") for k, p in g.paths.items()
                              if not k.endswith("_out")}},
-        "roofline": {"kernel": dom_name, "bound": "hbm", "achieved": achieved, "peak": peak,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": recorded_traffic(dom_name) if args.scale == 1 else None},
+        "roofline": roofline,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": len(ops) * args.steps,

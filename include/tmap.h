@@ -221,6 +221,23 @@ int tile_reduce(const tm_desc* dst, const tm_desc* src, tm_redop op, void* strea
 int stream_tiles(const tm_desc* a, const tm_desc* b, uint32_t stages, float* cs_a, float* cs_b,
                  uint64_t* bits_a, uint64_t* bits_b, void* stream);
 
+/* stream_gemm -- the ring in GEMM order, feeding the tensor cores ([MLSys-TMA] overview: while the
+ *   tensor cores work on the A and B tiles of step k, TMA brings those of step k + 1 into shared
+ *   memory in the swizzled layout the MMA reads; §"把 TMA 放进 pipeline": barriers hand each stage
+ *   between the TMA producer and the MMA consumer).  C = A * B^T: A is M x K and B is N x K, bf16
+ *   with K contiguous, given as rank-2 TM_BF16 maps {K, M} with box {64, 128} and {K, N} with box
+ *   {64, 256}, 128-byte swizzle, TMA path, unit steps, zero fill (else TM_EUNSUPPORTED), equal K
+ *   (else TM_EINVAL); M, N, K below 2^31.  Each 128 x 256 tile of C is computed by one CTA from a
+ *   `stages`-deep ring (2..4) of 48 KiB stages: tcgen05.mma (bf16 in, fp32 accumulated in tensor
+ *   memory), k in steps of 64.  c: device, fp32, row-major M x N with ldc >= N elements between rows,
+ *   16-byte aligned, ldc a multiple of 4 (else TM_EALIGN).  Ragged M, N and K are zero-filled by the
+ *   loads; only in-bounds elements of C are written.  Accuracy: the fp32 result differs from the
+ *   exact sum of the K products by at most K * 2^-23 * sum |A[m][k] * B[n][k]| (any summation order,
+ *   rounding to nearest or toward zero).  A wait that gives up is reported by tm_stream_check();
+ *   C is then undefined. */
+int stream_gemm(const tm_desc* a, const tm_desc* b, float* c, uint64_t ldc, uint32_t stages,
+                void* stream);
+
 /* tiled_copy_noalloc -- tiled_copy for callers that must not allocate device memory.  The pages
  *   have no counterpart: it exists because tiled_copy allocates (its first launching call on a
  *   device cudaMallocs the status word; a list of more than 8 boxes is staged with

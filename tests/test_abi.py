@@ -185,3 +185,30 @@ def test_reduce_and_ring_refuse_strided_or_nan_maps(tm):
         with pytest.raises(tm.TmapError) as e:
             tm.stream_tiles(x, y, 4, out, out, out, out, stream=0)
         assert e.value.code == tm.TM_EUNSUPPORTED
+
+
+def test_stream_gemm_validation(tm):
+    """Checked on the host before any device work (so this runs without a GPU)."""
+    a = tm.tmap_plan(tm.TM_BF16, FAKE, [4096, 512], [8192], [64, 128], swizzle=tm.TM_SWIZZLE_128B)
+    b = tm.tmap_plan(tm.TM_BF16, FAKE, [4096, 768], [8192], [64, 256], swizzle=tm.TM_SWIZZLE_128B)
+    c = 1 << 41  # never dereferenced: every case below fails validation first
+
+    def code(*args, **kw):
+        try:
+            tm.stream_gemm(*args, stream=0, **kw)
+        except tm.TmapError as e:
+            return e.code
+        return tm.TM_OK
+
+    assert code(b, a, c) == tm.TM_EUNSUPPORTED                    # boxes swapped
+    assert code(a, b, c, stages=1) == tm.TM_ERANGE
+    assert code(a, b, c, stages=5) == tm.TM_ERANGE
+    assert code(a, b, c, ldc=700) == tm.TM_EINVAL                 # ldc < N
+    assert code(a, b, c + 8) == tm.TM_EALIGN
+    assert code(a, b, c, ldc=770) == tm.TM_EALIGN
+    b2 = tm.tmap_plan(tm.TM_BF16, FAKE, [4032, 768], [8192], [64, 256], swizzle=tm.TM_SWIZZLE_128B)
+    assert code(a, b2, c) == tm.TM_EINVAL                         # K differs
+    f = tm.tmap_plan(tm.TM_F16, FAKE, [4096, 512], [8192], [64, 128], swizzle=tm.TM_SWIZZLE_128B)
+    assert code(f, b, c) == tm.TM_EUNSUPPORTED
+    n = tm.tmap_plan(tm.TM_BF16, FAKE, [4096, 512], [8192], [64, 128])
+    assert code(n, b, c) == tm.TM_EUNSUPPORTED                    # no swizzle

@@ -202,3 +202,12 @@ def w6_rows2_map(rows: int = 8192, cols: int = 8192):
 
 def w6_cols2_map(rows: int = 8192, cols: int = 8192):
     return dict(w3_map(rows, cols, 0), box=[128, 64], estrides=[2, 1])
+
+
+# The ring in GEMM order (stream_gemm): A 8192 x 4096 and B 8192 x 4096 (B holds B^T: N x K, K
+# contiguous), normal(0,1) rounded to bf16; C = A * B^T is 8192 x 8192 fp32.
+SEEDS_W7 = (71, 72)
+
+
+def w7_operands(m: int = 8192, n: int = 8192, k: int = 4096):
+    return normal_bf16((m, k), SEEDS_W7[0]), normal_bf16((n, k), SEEDS_W7[1])
