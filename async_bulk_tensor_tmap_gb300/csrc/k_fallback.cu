@@ -240,6 +240,24 @@ __device__ __forceinline__ void item_box_start(const BoxWalk& w, const ItemWalk&
     }
 }
 
+// The 16 bytes at offset d (1..15, not a multiple of 4) of the two staged windows at `win`: two
+// aligned 16-byte shared loads and a funnel shift per word (element sizes of 1 or 2 bytes only).
+__device__ __noinline__ uint4 unaligned_chunk(const uint8_t* win, uint32_t d)
+{
+    const uint4 lo = reinterpret_cast<const uint4*>(win)[0];
+    const uint4 hi = reinterpret_cast<const uint4*>(win)[1];
+    const uint32_t qd = d >> 2, sh = (d & 3u) * 8u;
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int t = 0; t < 4; t++) {
+        const uint32_t x0 = sel4(qd, w[t], w[t + 1], w[t + 2], w[t + 3]);
+        const uint32_t y0 = sel4(qd, w[t + 1], w[t + 2], w[t + 3], w[t + 4]);
+        o[t] = __funnelshift_r(x0, y0, sh);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
 // ---- load direction: staged copy ------------------------------------------------------------
 __device__ __forceinline__ void cp_async16(uint32_t dst, uint64_t src)
 {
@@ -258,10 +276,10 @@ __device__ __forceinline__ void cp_async_wait_all()
 // view and the strided W3 copy, although it reads more sectors twice.)  Per block: the row offsets go to a shared table; every thread issues 16-byte
 // cp.async copies of the aligned windows under its share of the rows (only windows holding an
 // in-bounds byte), so a whole block of loads is in flight without occupying registers; after one
-// wait each thread realigns its 16-byte chunks from the staged windows (two aligned shared loads
-// and a word select), fills elements outside the tensor, and stores the chunk to its swizzled
-// place in the global image with one 16-byte store (the swizzle only permutes chunks inside a
-// 128-byte row, so a warp's stores stay coalesced).  An aligned 16-byte window never crosses a
+// wait each thread reads its 16-byte chunks from the staged windows at their byte offset (the
+// widest shared loads the offset allows), fills elements outside the tensor, and stores the chunk
+// to its swizzled place in the global image with one 16-byte store (the swizzle only permutes
+// chunks inside a 128-byte row, so a warp's stores stay coalesced).  An aligned 16-byte window never crosses a
 // page, so no copy touches an unmapped address.  (Measured on GB300: one 1-D bulk copy per image
 // row instead of the per-window cp.async, 80-144 bytes each, was limited by the TMA engine's rate
 // of small requests, 2.2 TB/s against 3.3 on the rank-5 W4 view.)
@@ -360,27 +378,21 @@ __global__ void __launch_bounds__(kThreads, 8) k_fb_copy(const __grid_constant__
                       : es == 4 ? gather_chunk<uint32_t>(row, (int)j, x, step, fillv)
                                 : gather_chunk<unsigned long long>(row, (int)j, x, step, fillv);
             } else {
+                // The chunk is the 16 staged bytes starting d bytes into window j: read them with
+                // the widest shared loads that offset allows (no realignment arithmetic).
                 const uint32_t d = (uint32_t)((gbase + off) & 15);
-                const uint4* src = reinterpret_cast<const uint4*>(stg + (r * wpr + j) * 16);
-                const uint4 lo = src[0];
+                const uint8_t* const src = stg + (r * wpr + j) * 16 + d;
                 if (d == 0) {
-                    out = lo;
+                    out = *reinterpret_cast<const uint4*>(src);
+                } else if ((d & 7) == 0) {
+                    const uint2 a = reinterpret_cast<const uint2*>(src)[0];
+                    const uint2 b = reinterpret_cast<const uint2*>(src)[1];
+                    out = make_uint4(a.x, a.y, b.x, b.y);
+                } else if ((d & 3) == 0) {
+                    const uint32_t* w = reinterpret_cast<const uint32_t*>(src);
+                    out = make_uint4(w[0], w[1], w[2], w[3]);
                 } else {
-                    const uint4 hi = src[1];
-                    if (d == 8) {
-                        out = make_uint4(lo.z, lo.w, hi.x, hi.y);
-                    } else {
-                        const uint32_t qd = d >> 2, sh = (d & 3u) * 8u;
-                        const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-                        uint32_t o[4];
-#pragma unroll
-                        for (int t = 0; t < 4; t++) {
-                            const uint32_t x0 = sel4(qd, w[t], w[t + 1], w[t + 2], w[t + 3]);
-                            const uint32_t y0 = sel4(qd, w[t + 1], w[t + 2], w[t + 3], w[t + 4]);
-                            o[t] = __funnelshift_r(x0, y0, sh);
-                        }
-                        out = make_uint4(o[0], o[1], o[2], o[3]);
-                    }
+                    out = unaligned_chunk(stg + (r * wpr + j) * 16, d);
                 }
                 if (!whole_x && (blo > 0 || bhi < 16)) {  // the chunk holding a row edge
                     uint32_t m = word_mask(blo, bhi, 0);

@@ -7,16 +7,19 @@
 // barriers -- the consumer waits for a stage's bytes, the producer for the consumer to be done
 // with a stage before refilling it.
 //
-// One CTA computes one 128 x 256 tile of C (fp32) from bf16 A (M x K) and B (N x K), both with K
-// contiguous, through an S-stage ring of 48 KiB stages (A 128 x 64 and B 256 x 64, 128-byte
-// swizzled, one mbarrier per stage counting both tiles' bytes):
-//   warp 0  elected lane: TMA loads of step k into stage k % S once the stage is empty
-//   warp 1  owns the tensor memory (tcgen05.alloc / dealloc); its elected lane waits for each stage,
-//           issues four tcgen05.mma (K = 16 each) accumulating into tensor memory, and commits them
-//           to the stage's empty barrier (the stage is free once those MMAs have read it); after the
-//           last step it commits to the done barrier
-//   warps 2-5 wait for done, read the accumulator with tcgen05.ld (each warp the 32 tensor-memory
-//           lanes of its quarter, one row of the tile per lane) and store the in-bounds part of C
+// A persistent CTA (one per SM) computes 128 x 256 tiles of C (fp32) from bf16 A (M x K) and B
+// (N x K), both with K contiguous.  Its (tile, k step) pairs stream through an S-stage ring of
+// 48 KiB stages (A 128 x 64 and B 256 x 64, 128-byte swizzled, one mbarrier per stage counting both
+// tiles' bytes), and two accumulators of 256 tensor-memory columns alternate between tiles, so the
+// epilogue of one tile runs while the tensor cores work on the next:
+//   warp 0  elected lane: TMA loads of each step into the next stage once it is empty
+//   warp 1  owns the tensor memory (tcgen05.alloc / dealloc); its elected lane waits for an empty
+//           accumulator, then for each stage issues four tcgen05.mma (K = 16 each) into it and
+//           commits them to the stage's empty barrier (the stage is free once those MMAs have read
+//           it); after a tile's last step it commits to the accumulator's full barrier
+//   warps 2-5 wait for a full accumulator, read it with tcgen05.ld (each warp the 32 tensor-memory
+//           lanes of its quarter, one row of the tile per lane), store the in-bounds part of C and
+//           arrive on the accumulator's empty barrier
 // Every wait is bounded; after one gives up the CTA still drains what it issued, reaches the final
 // barrier and frees its tensor memory.
 #include "tm_ptx.cuh"
@@ -109,105 +112,136 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kGemmMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kGemmMaxStages];
-    __shared__ __align__(8) uint64_t done_bar;
+    __shared__ __align__(8) uint64_t acc_full[2];   // accumulator b holds a finished tile
+    __shared__ __align__(8) uint64_t acc_empty[2];  // accumulator b has been read out
     __shared__ uint32_t tmem_slot;
 
     const uint32_t base = (smem_u32(smem_raw) + (kStageAlign - 1)) & ~(kStageAlign - 1);
     const uint32_t S = g.stages;
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // consecutive CTAs take consecutive M tiles of one N tile, so a B tile is read from L2 by
-    // the CTAs that run together
-    const uint32_t mt = blockIdx.x % g.mtiles, nt = blockIdx.x / g.mtiles;
+    const uint32_t ntiles = g.mtiles * g.ntiles;
+    // this CTA's tiles: blockIdx.x, blockIdx.x + gridDim.x, ...; tile t is (t % mtiles, t / mtiles),
+    // so the CTAs running together share B tiles through L2
+    const uint32_t my_tiles = blockIdx.x < ntiles ? (ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < S; s++) {
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), 1);
         }
-        mbar_init(smem_u32(&done_bar), 1);
+        for (uint32_t b = 0; b < 2; b++) {
+            mbar_init(smem_u32(&acc_full[b]), 1);
+            mbar_init(smem_u32(&acc_empty[b]), 4);  // one arrival per epilogue warp
+        }
         fence_barrier_init();
     }
-    if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
+    if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), 2 * kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
 
     if (warp == 0) {
-        // ---------------- producer ----------------
+        // ---------------- producer: every (tile, k step) of this CTA through the ring ----------------
         if (elect_one()) {
             prefetch_tmap(&ma);
             prefetch_tmap(&mb);
-            uint32_t s = 0, wraps = 0, kb = 0;
-            for (; kb < g.kblocks; kb++) {
-                if (wraps > 0) {
-                    const uint32_t parity = (wraps - 1) & 1u;
-                    if (!mbar_wait(smem_u32(&empty_bar[s]), parity, g.timeout_ns)) {
-                        record_timeout(g.status, K_GEMM, s, parity, blockIdx.x);
-                        break;
+            uint32_t s = 0, wraps = 0;
+            uint64_t issued = 0;
+            bool failed = false;
+            for (uint32_t i = 0; i < my_tiles && !failed; i++) {
+                const uint32_t t = blockIdx.x + i * gridDim.x;
+                const uint32_t mt = t % g.mtiles, nt = t / g.mtiles;
+                for (uint32_t kb = 0; kb < g.kblocks; kb++) {
+                    if (wraps > 0) {
+                        const uint32_t parity = (wraps - 1) & 1u;
+                        if (!mbar_wait(smem_u32(&empty_bar[s]), parity, g.timeout_ns)) {
+                            record_timeout(g.status, K_GEMM, s, parity, t);
+                            failed = true;
+                            break;
+                        }
+                    }
+                    const uint32_t bar = smem_u32(&full_bar[s]);
+                    const int32_t ca[2] = {(int32_t)(kb * kBK), (int32_t)(mt * kBM)};
+                    const int32_t cb[2] = {(int32_t)(kb * kBK), (int32_t)(nt * kBN)};
+                    mbar_arrive_expect_tx(bar, kGemmStage);
+                    tma_load<2>(base + s * kGemmStage, &ma, ca, bar);
+                    tma_load<2>(base + s * kGemmStage + kTileA, &mb, cb, bar);
+                    issued++;
+                    if (++s == S) {
+                        s = 0;
+                        wraps++;
                     }
                 }
-                const uint32_t bar = smem_u32(&full_bar[s]);
-                const int32_t ca[2] = {(int32_t)(kb * kBK), (int32_t)(mt * kBM)};
-                const int32_t cb[2] = {(int32_t)(kb * kBK), (int32_t)(nt * kBN)};
-                mbar_arrive_expect_tx(bar, kGemmStage);
-                tma_load<2>(base + s * kGemmStage, &ma, ca, bar);
-                tma_load<2>(base + s * kGemmStage + kTileA, &mb, cb, bar);
-                if (++s == S) {
-                    s = 0;
-                    wraps++;
-                }
             }
-            if (kb < g.kblocks) {
-                // After a failure: the last loads issued may still be landing; wait for them.
-                for (uint32_t j = kb > S ? kb - S : 0; j < kb; j++)
-                    mbar_wait(smem_u32(&full_bar[j % S]), (j / S) & 1u, g.timeout_ns);
-            } else {
-                // The MMA warp's last releases of the stages must land before shared memory goes
-                // away: wait for the empty barriers of the last S steps (bounded).
-                for (uint32_t j = kb > S ? kb - S : 0; j < kb; j++)
-                    mbar_wait(smem_u32(&empty_bar[j % S]), (j / S) & 1u, g.timeout_ns);
+            // Drain before shared memory goes away (bounded): after a failure the last loads may
+            // still be landing; otherwise the MMA warp's last releases of the stages must land.
+            for (uint64_t j = issued > S ? issued - S : 0; j < issued; j++) {
+                const uint32_t js = (uint32_t)(j % S), jp = (uint32_t)((j / S) & 1);
+                mbar_wait(smem_u32(failed ? &full_bar[js] : &empty_bar[js]), jp, g.timeout_ns);
             }
         }
     } else if (warp == 1) {
         // ---------------- MMA issuer ----------------
         if (elect_one()) {
             uint32_t s = 0, phase = 0;
-            for (uint32_t kb = 0; kb < g.kblocks; kb++) {
-                if (!mbar_wait(smem_u32(&full_bar[s]), phase, g.timeout_ns)) {
-                    record_timeout(g.status, K_GEMM, s, phase, blockIdx.x);
-                    break;
+            bool failed = false;
+            for (uint32_t i = 0; i < my_tiles && !failed; i++) {
+                const uint32_t b = i & 1u;
+                const uint32_t d = tmem + b * kTmemCols;
+                if (i >= 2) {  // the epilogue has read out accumulator b's previous tile
+                    const uint32_t parity = ((i >> 1) - 1) & 1u;
+                    if (!mbar_wait(smem_u32(&acc_empty[b]), parity, g.timeout_ns)) {
+                        record_timeout(g.status, K_GEMM, 8 + b, parity, i);
+                        break;
+                    }
+                    tc_fence_after();
                 }
-                tc_fence_after();
-                const uint32_t a0 = base + s * kGemmStage, b0 = a0 + kTileA;
+                for (uint32_t kb = 0; kb < g.kblocks; kb++) {
+                    if (!mbar_wait(smem_u32(&full_bar[s]), phase, g.timeout_ns)) {
+                        record_timeout(g.status, K_GEMM, s, phase, i);
+                        failed = true;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = base + s * kGemmStage, b0 = a0 + kTileA;
 #pragma unroll
-                for (uint32_t ks = 0; ks < kBK / kUK; ks++) {
-                    mma_bf16(tmem, sw128_desc(a0 + ks * kUK * 2), sw128_desc(b0 + ks * kUK * 2),
-                             kIdesc, (kb | ks) != 0 ? 1u : 0u);
+                    for (uint32_t ks = 0; ks < kBK / kUK; ks++) {
+                        mma_bf16(d, sw128_desc(a0 + ks * kUK * 2), sw128_desc(b0 + ks * kUK * 2),
+                                 kIdesc, (kb | ks) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(smem_u32(&empty_bar[s]));  // the stage is free once these MMAs read it
+                    if (++s == S) {
+                        s = 0;
+                        phase ^= 1u;
+                    }
                 }
-                tc_commit(smem_u32(&empty_bar[s]));  // the stage is free once these MMAs read it
-                if (++s == S) {
-                    s = 0;
-                    phase ^= 1u;
-                }
+                // accumulator b is complete once every MMA issued so far has (after a failure: the
+                // epilogue still gets its arrival, and the MMAs issued have completed)
+                tc_commit(smem_u32(&acc_full[b]));
             }
-            tc_commit(smem_u32(&done_bar));  // every MMA issued above has completed
         }
         __syncwarp();
     } else {
         // ---------------- epilogue: warps 2-5, tensor-memory lane quarter warp % 4 ----------------
         const uint32_t q = warp & 3u;
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&done_bar), 0, g.timeout_ns));
-        tc_fence_after();
-        if (!ok) {
-            if (lane == 0) record_timeout(g.status, K_GEMM, 0, 0, blockIdx.x);
-        } else {
+        for (uint32_t i = 0; i < my_tiles; i++) {
+            const uint32_t b = i & 1u;
+            const uint32_t t = blockIdx.x + i * gridDim.x;
+            const uint32_t mt = t % g.mtiles, nt = t / g.mtiles;
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&acc_full[b]), (i >> 1) & 1u,
+                                                              g.timeout_ns));
+            tc_fence_after();
+            if (!ok) {
+                if (lane == 0) record_timeout(g.status, K_GEMM, 10 + b, (i >> 1) & 1u, i);
+                break;
+            }
             const uint32_t row = mt * kBM + q * 32 + lane;
             float* const crow = g.c + (uint64_t)row * g.ldc;
             const uint32_t n0 = nt * kBN;
             for (uint32_t c0 = 0; c0 < kBN; c0 += 32) {
                 uint32_t r[32];
-                tmem_ld32(tmem + ((q * 32) << 16) + c0, r);
+                tmem_ld32(tmem + b * kTmemCols + ((q * 32) << 16) + c0, r);
                 if (row < g.m) {
                     const uint32_t n = n0 + c0;
                     if (n + 32 <= g.n) {
@@ -226,16 +260,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                 }
             }
+            // this warp's reads of accumulator b are complete (tcgen05.wait::ld): hand it back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&acc_empty[b]));
         }
     }
 
-    // Every tensor-memory read and every MMA has completed (the done barrier, tcgen05.wait::ld):
-    // free the accumulator.
+    // Every tensor-memory read and every MMA has completed: free the accumulators.
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, 2 * kTmemCols);
     }
 }
 

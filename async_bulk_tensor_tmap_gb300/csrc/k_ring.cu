@@ -87,28 +87,47 @@ __global__ void __launch_bounds__(kRingThreads, 1)
         if (!elect_one()) return;
         prefetch_tmap(&ma);
         prefetch_tmap(&mb);
-        auto coords = [&](uint64_t i, int32_t* ca, int32_t* cb) {
-            const uint64_t t = first + i * gridDim.x;
-            ca[0] = (int32_t)((t % r.a_nb0) * 64);
-            ca[1] = (int32_t)((t / r.a_nb0) * r.rows);
-            cb[0] = (int32_t)((t % r.b_nb0) * 64);
-            cb[1] = (int32_t)((t / r.b_nb0) * r.rows);
+        // Tile counters of A and B (box along dim 0, box along dim 1) of tile `first + i * G`
+        // (G = gridDim.x), stepped by G tiles with a carry: one cursor for the loads and one for the
+        // optional L2 prefetch r.prefetch tiles ahead of them (no completion is tracked for those).
+        struct TileCursor {
+            uint64_t a0, a1, b0, b1;
         };
-        // Optional L2 prefetch r.prefetch tiles ahead of the loads (no completion is tracked).
-        auto prefetch = [&](uint64_t i) {
-            if (i >= n_local) return;
-            int32_t ca[2], cb[2];
-            coords(i, ca, cb);
-            tma_prefetch_l2_2d(&ma, ca[0], ca[1]);
-            tma_prefetch_l2_2d(&mb, cb[0], cb[1]);
-        };
-        for (uint64_t j = S; j < r.prefetch; j++) prefetch(j);
-        // Tile counters of A and B (box along dim 0, box along dim 1), stepped by gridDim.x tiles
-        // with a carry; the stage and the number of times the ring has wrapped are counted too.
         const uint32_t a_d0 = (uint32_t)(gridDim.x % r.a_nb0), b_d0 = (uint32_t)(gridDim.x % r.b_nb0);
         const uint64_t a_d1 = gridDim.x / r.a_nb0, b_d1 = gridDim.x / r.b_nb0;
-        uint64_t a_k0 = first % r.a_nb0, a_k1 = first / r.a_nb0;
-        uint64_t b_k0 = first % r.b_nb0, b_k1 = first / r.b_nb0;
+        auto cursor_at = [&](uint64_t i) {
+            const uint64_t t = first + i * gridDim.x;
+            return TileCursor{t % r.a_nb0, t / r.a_nb0, t % r.b_nb0, t / r.b_nb0};
+        };
+        auto advance = [&](TileCursor& c) {
+            c.a0 += a_d0;
+            c.a1 += a_d1;
+            if (c.a0 >= r.a_nb0) {
+                c.a0 -= r.a_nb0;
+                c.a1++;
+            }
+            c.b0 += b_d0;
+            c.b1 += b_d1;
+            if (c.b0 >= r.b_nb0) {
+                c.b0 -= r.b_nb0;
+                c.b1++;
+            }
+        };
+        TileCursor ld = cursor_at(0);
+        TileCursor pf = ld;
+        uint64_t pf_i = 0;
+        auto prefetch_to = [&](uint64_t upto) {  // prefetch tiles pf_i .. min(upto, n_local) - 1
+            for (; pf_i < upto && pf_i < n_local; pf_i++) {
+                tma_prefetch_l2_2d(&ma, (int32_t)(pf.a0 * 64), (int32_t)(pf.a1 * r.rows));
+                tma_prefetch_l2_2d(&mb, (int32_t)(pf.b0 * 64), (int32_t)(pf.b1 * r.rows));
+                advance(pf);
+            }
+        };
+        if (r.prefetch) {
+            pf = cursor_at(S);
+            pf_i = S;
+            prefetch_to(r.prefetch);
+        }
         uint32_t s = 0, wraps = 0;
         uint64_t i = 0;
         for (; i < n_local; i++) {
@@ -120,24 +139,13 @@ __global__ void __launch_bounds__(kRingThreads, 1)
                 }
             }
             const uint32_t bar = smem_u32(&full_bar[s]);
-            const int32_t ca[2] = {(int32_t)(a_k0 * 64), (int32_t)(a_k1 * r.rows)};
-            const int32_t cb[2] = {(int32_t)(b_k0 * 64), (int32_t)(b_k1 * r.rows)};
+            const int32_t ca[2] = {(int32_t)(ld.a0 * 64), (int32_t)(ld.a1 * r.rows)};
+            const int32_t cb[2] = {(int32_t)(ld.b0 * 64), (int32_t)(ld.b1 * r.rows)};
             mbar_arrive_expect_tx(bar, 2 * tile);
             tma_load<2>(base + s * 2 * tile, &ma, ca, bar);
             tma_load<2>(base + s * 2 * tile + tile, &mb, cb, bar);
-            if (r.prefetch) prefetch(i + r.prefetch);
-            a_k0 += a_d0;
-            a_k1 += a_d1;
-            if (a_k0 >= r.a_nb0) {
-                a_k0 -= r.a_nb0;
-                a_k1++;
-            }
-            b_k0 += b_d0;
-            b_k1 += b_d1;
-            if (b_k0 >= r.b_nb0) {
-                b_k0 -= r.b_nb0;
-                b_k1++;
-            }
+            if (r.prefetch) prefetch_to(i + 1 + r.prefetch);
+            advance(ld);
             if (++s == S) {
                 s = 0;
                 wraps++;

@@ -734,8 +734,10 @@ int stream_gemm(const tm_desc* a, const tm_desc* b, float* c, uint64_t ldc, uint
     g.ldc = ldc;
     g.timeout_ns = wait_limit_ns();
     g.status = ds->status;
-    const uint64_t grid = (uint64_t)g.mtiles * g.ntiles;
-    if (grid >= (1ull << 31)) return fail(TM_ERANGE, "too many tiles");
+    const uint64_t tiles = (uint64_t)g.mtiles * g.ntiles;
+    if (tiles >= (1ull << 31)) return fail(TM_ERANGE, "too many tiles");
+    // persistent: one CTA per SM (the stages and the two 256-column accumulators fill an SM)
+    const uint64_t grid = std::min<uint64_t>(tiles, (uint64_t)ds->sms);
     const size_t smem = (size_t)stages * (16384 + 32768) + kStageAlign;
     if (smem > cta_budget(*ds, 1) + 1024) return fail(TM_ERANGE, "%u stages exceed shared memory", stages);
     return check_launch(launch_gemm((const CUtensorMap*)a->tmap, (const CUtensorMap*)b->tmap, g,
