@@ -390,7 +390,10 @@ def e2e_run(g: GpuWorkload, h: HostWorkload, ops, steps):
     """Same step through the public API with HOST buffers: every step copies its inputs from
     pinned host memory and its results back, inside the timed region.  Three streams pipeline the
     work group by group (inputs of group k+1 go in while group k computes and group k-1's results
-    come out); events keep each tensor's copies and kernels in order across steps."""
+    come out); events keep each tensor's copies and kernels in order across steps.  An input that
+    is also a result (the reduce destination) has two device buffers used by alternate steps, its
+    maps moved between them with tmap_replace_address, so that one step's upload does not wait for
+    the previous step's read-out."""
     torch = g.torch
     names = [n for n, _ in ops]
     groups = [(gn, ins, outs, [n for n in names if n.split(".")[0].startswith(gn)])
@@ -409,22 +412,36 @@ def e2e_run(g: GpuWorkload, h: HostWorkload, ops, steps):
     bi = sum(v.numel() * v.element_size() for v in pin_in.values())
     bo = sum(v.numel() * v.element_size() for v in pin_out.values())
     s_in, s_out, s_run = torch.cuda.Stream(), torch.cuda.Stream(), g.stream
-    outd = {gn: None for gn, *_ in groups}   # results copied out (previous step)
+    dual = {k for _, ins, outs, _ in groups for k in ins if k in outs}
+    bufs = {k: [g.t[k], torch.empty_like(g.t[k])] for k in dual}
+    buf_out = {k: [None, None] for k in dual}       # read-out event of each buffer's last step
+    last_done = {gn: None for gn, *_ in groups}    # the group's kernels of the previous step
+    last_out = {gn: None for gn, *_ in groups}     # the group's read-out of the previous step
+    nstep = [0]
 
     def step():
+        par = nstep[0] & 1
         for gn, ins, outs, gops in groups:
             ev_in = torch.cuda.Event()
             with torch.cuda.stream(s_in):
-                if outd[gn] is not None:
-                    # last step's kernels and read-out are done with these tensors (an input of
-                    # one step may be the previous step's result, e.g. the reduce destination)
-                    s_in.wait_event(outd[gn])
+                for k in ins:  # double-buffered inputs first: they only wait for their buffer
+                    if k in dual:
+                        if buf_out[k][par] is not None:
+                            s_in.wait_event(buf_out[k][par])  # this buffer's last result is out
+                        bufs[k][par].copy_(pin_in[k], non_blocking=True)
+                if last_done[gn] is not None and any(k not in dual for k in ins):
+                    s_in.wait_event(last_done[gn])  # last step's kernels have read the inputs
                 for k in ins:
-                    g.t[k].copy_(pin_in[k], non_blocking=True)
+                    if k not in dual:
+                        g.t[k].copy_(pin_in[k], non_blocking=True)
                 ev_in.record(s_in)
+            for k in ins:
+                if k in dual:
+                    g.t[k] = bufs[k][par]
+                    g.tm.tmap_replace_address(g.maps[k], g.t[k])
             s_run.wait_event(ev_in)
-            if outd[gn] is not None:
-                s_run.wait_event(outd[gn])  # last step's results were read out
+            if last_out[gn] is not None and any(k not in dual for k in outs):
+                s_run.wait_event(last_out[gn])  # last step's results were read out
             for name in gops:
                 g.run_op(name, s_run)
             ev_done = torch.cuda.Event()
@@ -435,7 +452,12 @@ def e2e_run(g: GpuWorkload, h: HostWorkload, ops, steps):
                 for k in outs:
                     pin_out[k].copy_(g.t[k], non_blocking=True)
                 ev_out.record(s_out)
-            outd[gn] = ev_out
+            last_done[gn] = ev_done
+            last_out[gn] = ev_out
+            for k in outs:
+                if k in dual:
+                    buf_out[k][par] = ev_out
+        nstep[0] += 1
 
     step()
     torch.cuda.synchronize()
