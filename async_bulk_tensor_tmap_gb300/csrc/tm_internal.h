@@ -172,7 +172,8 @@ struct RingArgs {
 };
 
 // Tensor-core consumer of the k-ordered ring (stream_gemm): C = A * B^T.
-constexpr uint32_t kGemmMaxStages = 4;
+constexpr uint32_t kGemmMaxStages = 4;      // one-SM form: 48 KiB stages
+constexpr uint32_t kGemmMaxPairStages = 6;  // CTA-pair form: 32 KiB stages per CTA
 struct GemmArgs {
     uint32_t m, n, k;        // C is m x n; A is m x k, B is n x k (bf16, k contiguous)
     uint32_t mtiles, ntiles; // 128-row and 256-column tiles of C
@@ -201,6 +202,8 @@ cudaError_t launch_ring(const CUtensorMap* a, const CUtensorMap* b, const RingAr
 cudaError_t launch_selftest(uint64_t timeout_ns, StatusBlock* status, cudaStream_t s);
 cudaError_t launch_gemm(const CUtensorMap* a, const CUtensorMap* b, const GemmArgs& g,
                         uint32_t grid, size_t smem, cudaStream_t s);
+cudaError_t launch_gemm_pair(const CUtensorMap* a, const CUtensorMap* b, const GemmArgs& g,
+                             uint32_t grid, size_t smem, cudaStream_t s);
 
 // Sets the thread's tm_last_error() text; returns `code`.
 int set_last_error(int code, const char* msg);

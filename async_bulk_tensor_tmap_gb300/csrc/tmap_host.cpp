@@ -716,32 +716,59 @@ int stream_gemm(const tm_desc* a, const tm_desc* b, float* c, uint64_t ldc, uint
                              (unsigned long long)N);
     if ((uintptr_t)c % 16 || ldc % 4)
         return fail(TM_EALIGN, "c must be 16-byte aligned and ldc a multiple of 4");
-    if (stages < 2 || stages > kGemmMaxStages)
-        return fail(TM_ERANGE, "stages %u outside 2..%u", stages, kGemmMaxStages);
+    if (stages < 2 || stages > kGemmMaxPairStages)
+        return fail(TM_ERANGE, "stages %u outside 2..%u", stages, kGemmMaxPairStages);
     DevState* ds = nullptr;
     int rc = device_state(&ds);
     if (rc) return rc;
+    // The CTA-pair form (256-row tiles over two SMs) whenever C has more than one 128-row tile
+    // (TM_GEMM_PAIR=0 keeps the one-SM form).
+    const bool pair = env_u64("TM_GEMM_PAIR", 0) != 0 && M > 128 && ds->sms >= 2;
+    const uint32_t rows = pair ? 256u : 128u;
+    const uint32_t S = std::min<uint32_t>(stages, pair ? kGemmMaxPairStages : kGemmMaxStages);
     GemmArgs g;
     memset(&g, 0, sizeof(g));
     g.m = (uint32_t)M;
     g.n = (uint32_t)N;
     g.k = (uint32_t)K;
-    g.mtiles = (uint32_t)((M + 127) / 128);
+    g.mtiles = (uint32_t)((M + rows - 1) / rows);
     g.ntiles = (uint32_t)((N + 255) / 256);
     g.kblocks = (uint32_t)((K + 63) / 64);
-    g.stages = stages;
+    g.stages = S;
     g.c = c;
     g.ldc = ldc;
     g.timeout_ns = wait_limit_ns();
     g.status = ds->status;
     const uint64_t tiles = (uint64_t)g.mtiles * g.ntiles;
     if (tiles >= (1ull << 31)) return fail(TM_ERANGE, "too many tiles");
+    const size_t smem = (size_t)S * (pair ? 32768 : 49152) + kStageAlign;
+    if (smem > cta_budget(*ds, 1) + 1024) return fail(TM_ERANGE, "%u stages exceed shared memory", S);
+    const CUtensorMap* ma = (const CUtensorMap*)a->tmap;
+    const CUtensorMap* mb = (const CUtensorMap*)b->tmap;
+    if (pair) {
+        // Each CTA of a pair loads a 128-row half of the B tile: a map of B with a 128-row box
+        // (the caller's has 256 rows).  Every stage expects exactly 16 KiB from each map.
+        tm_desc bh;
+        const uint64_t dims[2] = {b->dim[0], b->dim[1]};
+        const uint64_t strides[1] = {b->stride[1]};
+        const uint32_t box[2] = {64, 128};
+        if ((rc = plan_impl(&bh, TM_BF16, 2, (void*)(uintptr_t)b->base, dims, strides, box, nullptr,
+                            TM_SWIZZLE_128B, TM_OOB_ZERO)))
+            return rc;
+        if ((rc = encode_into(&bh))) return rc;
+        if (bh.path != TM_PATH_TMA || bh.box_bytes != 16384 || a->box_bytes != 16384)
+            return fail(TM_EUNSUPPORTED, "stream_gemm could not encode the half-tile map of B");
+        // persistent: one cluster of two CTAs per pair of SMs
+        const uint64_t pairs = std::min<uint64_t>(tiles, (uint64_t)ds->sms / 2);
+        return check_launch(launch_gemm_pair(ma, (const CUtensorMap*)bh.tmap, g,
+                                             (uint32_t)(2 * pairs), smem, (cudaStream_t)stream),
+                            "gemm launch (CTA pairs)");
+    }
+    if (a->box_bytes != 16384 || b->box_bytes != 32768)
+        return fail(TM_EUNSUPPORTED, "stream_gemm: A and B tiles must be 16 and 32 KiB");
     // persistent: one CTA per SM (the stages and the two 256-column accumulators fill an SM)
     const uint64_t grid = std::min<uint64_t>(tiles, (uint64_t)ds->sms);
-    const size_t smem = (size_t)stages * (16384 + 32768) + kStageAlign;
-    if (smem > cta_budget(*ds, 1) + 1024) return fail(TM_ERANGE, "%u stages exceed shared memory", stages);
-    return check_launch(launch_gemm((const CUtensorMap*)a->tmap, (const CUtensorMap*)b->tmap, g,
-                                    (uint32_t)grid, smem, (cudaStream_t)stream),
+    return check_launch(launch_gemm(ma, mb, g, (uint32_t)grid, smem, (cudaStream_t)stream),
                         "gemm launch");
 }
 

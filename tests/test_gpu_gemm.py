@@ -18,10 +18,18 @@ torch = pytest.importorskip("torch")
 
 
 @pytest.fixture(scope="module")
-def tm():
+def tm_lib():
     import async_bulk_tensor_tmap_gb300 as m  # raises if the CUDA library is missing
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     return m
+
+
+@pytest.fixture(params=["pair", "one_sm"])
+def tm(request, tm_lib, monkeypatch):
+    """Both forms of the consumer: CTA pairs (tcgen05 cta_group::2, 256-row tiles over two SMs)
+    and one SM per 128-row tile."""
+    monkeypatch.setenv("TM_GEMM_PAIR", "1" if request.param == "pair" else "0")
+    return tm_lib
 
 
 def check(tm):
@@ -78,7 +86,7 @@ def test_gemm_matches_oracle(tm, M, N, K):
     assert np.isfinite(got).all()
 
 
-@pytest.mark.parametrize("stages", [2, 3, 4])
+@pytest.mark.parametrize("stages", [2, 3, 4, 6])
 def test_gemm_every_ring_depth(tm, stages):
     a, b = bf16_normal(256, 448, 3), bf16_normal(512, 448, 4)
     got = run(tm, a, b, stages=stages)
@@ -120,3 +128,12 @@ def test_gemm_full_size_sampled(tm):
     worst = assert_within_bound(got, a, b, rows, cols)
     print(f"worst error {worst:.3g} of the bound")
     assert np.isfinite(got).all()
+
+
+def test_gemm_one_pair_tile(tm):
+    """The smallest case of each form: one 256 x 256 tile, one k step."""
+    a, b = bf16_normal(256, 64, 11), bf16_normal(256, 64, 12)
+    got = run(tm, a, b)
+    exact = oracle.gemm(a, b)
+    scale = oracle.gemm(a & 0x7FFF, b & 0x7FFF)
+    assert (np.abs(got - exact) <= 64 * 2.0 ** -23 * scale).all()
