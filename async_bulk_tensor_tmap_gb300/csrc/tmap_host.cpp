@@ -721,9 +721,12 @@ int stream_gemm(const tm_desc* a, const tm_desc* b, float* c, uint64_t ldc, uint
     DevState* ds = nullptr;
     int rc = device_state(&ds);
     if (rc) return rc;
-    // The CTA-pair form (256-row tiles over two SMs) whenever C has more than one 128-row tile
-    // (TM_GEMM_PAIR=0 keeps the one-SM form).
+    // Forms: clusters of two one-SM CTAs along M sharing each B tile by TMA multicast (the default
+    // when C has more than one 128-row tile; TM_GEMM_MULTICAST=0 turns it off); one SM per
+    // 128 x 256 tile; TM_GEMM_PAIR=1 the CTA-pair form (256-row tiles over two SMs, tcgen05
+    // cta_group::2; measured slower).
     const bool pair = env_u64("TM_GEMM_PAIR", 0) != 0 && M > 128 && ds->sms >= 2;
+    const bool mcast = !pair && env_u64("TM_GEMM_MULTICAST", 1) != 0 && M > 128 && ds->sms >= 2;
     const uint32_t rows = pair ? 256u : 128u;
     const uint32_t S = std::min<uint32_t>(stages, pair ? kGemmMaxPairStages : kGemmMaxStages);
     GemmArgs g;
@@ -745,9 +748,10 @@ int stream_gemm(const tm_desc* a, const tm_desc* b, float* c, uint64_t ldc, uint
     if (smem > cta_budget(*ds, 1) + 1024) return fail(TM_ERANGE, "%u stages exceed shared memory", S);
     const CUtensorMap* ma = (const CUtensorMap*)a->tmap;
     const CUtensorMap* mb = (const CUtensorMap*)b->tmap;
-    if (pair) {
-        // Each CTA of a pair loads a 128-row half of the B tile: a map of B with a 128-row box
-        // (the caller's has 256 rows).  Every stage expects exactly 16 KiB from each map.
+    if (pair || mcast) {
+        // Each CTA of a cluster loads a 128-row half of the B tile: a map of B with a 128-row box
+        // (the caller's has 256 rows).  Both cluster forms expect exactly 16 KiB per half and per
+        // A tile in every stage.
         tm_desc bh;
         const uint64_t dims[2] = {b->dim[0], b->dim[1]};
         const uint64_t strides[1] = {b->stride[1]};
@@ -758,11 +762,20 @@ int stream_gemm(const tm_desc* a, const tm_desc* b, float* c, uint64_t ldc, uint
         if ((rc = encode_into(&bh))) return rc;
         if (bh.path != TM_PATH_TMA || bh.box_bytes != 16384 || a->box_bytes != 16384)
             return fail(TM_EUNSUPPORTED, "stream_gemm could not encode the half-tile map of B");
-        // persistent: one cluster of two CTAs per pair of SMs
-        const uint64_t pairs = std::min<uint64_t>(tiles, (uint64_t)ds->sms / 2);
-        return check_launch(launch_gemm_pair(ma, (const CUtensorMap*)bh.tmap, g,
-                                             (uint32_t)(2 * pairs), smem, (cudaStream_t)stream),
-                            "gemm launch (CTA pairs)");
+        const CUtensorMap* mbh = (const CUtensorMap*)bh.tmap;
+        if (pair) {
+            // persistent: one cluster of two CTAs per pair of SMs
+            const uint64_t pairs = std::min<uint64_t>(tiles, (uint64_t)ds->sms / 2);
+            return check_launch(launch_gemm_pair(ma, mbh, g, (uint32_t)(2 * pairs), smem,
+                                                 (cudaStream_t)stream),
+                                "gemm launch (CTA pairs)");
+        }
+        // persistent: one cluster of two CTAs (tiles 2m and 2m + 1 of one N tile) per pair of SMs
+        const uint64_t units = (uint64_t)((g.mtiles + 1) / 2) * g.ntiles;
+        const uint64_t clusters = std::min<uint64_t>(units, (uint64_t)ds->sms / 2);
+        return check_launch(launch_gemm_multicast(ma, mbh, g, (uint32_t)(2 * clusters), smem,
+                                                  (cudaStream_t)stream),
+                            "gemm launch (B multicast)");
     }
     if (a->box_bytes != 16384 || b->box_bytes != 32768)
         return fail(TM_EUNSUPPORTED, "stream_gemm: A and B tiles must be 16 and 32 KiB");

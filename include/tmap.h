@@ -230,9 +230,12 @@ int stream_tiles(const tm_desc* a, const tm_desc* b, uint32_t stages, float* cs_
  *   (else TM_EINVAL); M, N, K below 2^31.  Persistent CTAs (one per SM) compute 128 x 256 tiles of
  *   C from a `stages`-deep ring of 48 KiB stages (stages 2..6, at most 4 used): tcgen05.mma (bf16
  *   in, fp32 accumulated in two tensor-memory accumulators, so one tile's epilogue overlaps the
- *   next tile's MMAs), k in steps of 64.  TM_GEMM_PAIR=1 selects the CTA-pair form (tcgen05
- *   cta_group::2, 256-row tiles over two SMs of a cluster, 32 KiB stages, up to 6; measured slower
- *   on GB300, so not the default).  c: device, fp32, row-major M x N with ldc >= N elements between
+ *   next tile's MMAs), k in steps of 64.  When C has more than one 128-row tile, clusters of two
+ *   CTAs along M share each B tile: each CTA loads one 128-row half of it, multicast into both
+ *   CTAs' stages ([H200-TMA] §01: one copy lands in several CTAs' shared memory; one GPU only),
+ *   and each CTA's MMA commits release the stage in both (TM_GEMM_MULTICAST=0 turns this off).
+ *   TM_GEMM_PAIR=1 selects the CTA-pair form (tcgen05 cta_group::2, 256-row tiles over two SMs of a
+ *   cluster, 32 KiB stages, up to 6; measured slower on GB300, so not the default).  c: device, fp32, row-major M x N with ldc >= N elements between
  *   rows, 16-byte aligned, ldc a multiple of 4 (else TM_EALIGN).  Ragged M, N and K are zero-filled by the
  *   loads; only in-bounds elements of C are written.  Accuracy: the fp32 result differs from the
  *   exact sum of the K products by at most K * 2^-23 * sum |A[m][k] * B[n][k]| (any summation order,
