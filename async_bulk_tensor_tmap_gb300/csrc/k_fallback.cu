@@ -138,42 +138,6 @@ __device__ __forceinline__ uint4 gather_chunk(const uint8_t* row, int j, const X
     return u.v;
 }
 
-// Writes the in-bounds elements of chunk j of an image row to the tensor row at `row` (the
-// address of the box's dim-0 start), element k at k * step elements.
-template <typename E>
-__device__ __forceinline__ void scatter_chunk(uint8_t* row, const uint4& v, int j, const XRange& x,
-                                              int step)
-{
-    constexpr int n = 16 / (int)sizeof(E);
-    union {
-        uint4 v;
-        E e[n];
-    } u;
-    u.v = v;
-#pragma unroll
-    for (int t = 0; t < n; t++) {
-        const int k = j * n + t;
-        if (k >= x.i_lo && k < x.i_hi)
-            *reinterpret_cast<E*>(row + (size_t)k * step * sizeof(E)) = u.e[t];
-    }
-}
-
-// In-bounds element range [k0, k1) of chunk j of a row whose element 0 has dim-0 coordinate x0.
-__device__ __forceinline__ void chunk_range(int64_t x0, uint32_t j, uint32_t epc, uint64_t dim0,
-                                            int& k0, int& k1)
-{
-    const int64_t first = x0 + (int64_t)j * epc;
-    if (first >= 0 && first + (int64_t)epc <= (int64_t)dim0) {  // the common case: all inside
-        k0 = 0;
-        k1 = (int)epc;
-        return;
-    }
-    const int64_t lo = first < 0 ? -first : 0;
-    const int64_t hi = (int64_t)dim0 - first;
-    k0 = (int)(lo < (int64_t)epc ? lo : (int64_t)epc);
-    k1 = (int)(hi < 0 ? 0 : hi < (int64_t)epc ? hi : (int64_t)epc);
-}
-
 }  // namespace
 
 constexpr int64_t kRowOutside = INT64_MIN;  // table entry of a row outside the tensor
@@ -487,6 +451,34 @@ __global__ void __launch_bounds__(kThreads, 6) k_fb_store(const __grid_constant_
                 tab[r] = (p.ok && x.i_lo < x.i_hi) ? p.off : kRowOutside;
             }
             __syncthreads();
+            if constexpr (kStep0) {
+                // Element by element, consecutive threads on consecutive image elements of a row,
+                // so that a warp's stores land elementStrides[0] elements apart in one stretch of
+                // the row rather than one element in each of 32 chunks.
+                const uint32_t n0 = a.ibox[0];
+                const uint32_t n0_shift = (n0 & (n0 - 1)) == 0 ? (uint32_t)(__ffs(n0) - 1) : 32u;
+                const int step = (int)a.estride[0];
+                const uint32_t nel = nr * n0;
+                for (uint32_t e = threadIdx.x; e < nel; e += kThreads) {
+                    const uint32_t r = n0_shift < 32 ? e >> n0_shift : e / n0;
+                    const int k = (int)(e - r * n0);
+                    const int64_t off = tab[r];
+                    if (off == kRowOutside || k < x.i_lo || k >= x.i_hi) continue;
+                    const uint8_t* src = img + (size_t)(r0 + r) * a.inner_bytes + (size_t)k * es;
+                    uint8_t* dst = reinterpret_cast<uint8_t*>(a.base + off) + (int64_t)k * step * es;
+                    if (es == 2) {
+                        *reinterpret_cast<uint16_t*>(dst) = __ldg(reinterpret_cast<const uint16_t*>(src));
+                    } else if (es == 4) {
+                        *reinterpret_cast<uint32_t*>(dst) = __ldg(reinterpret_cast<const uint32_t*>(src));
+                    } else if (es == 8) {
+                        *reinterpret_cast<unsigned long long*>(dst) =
+                            __ldg(reinterpret_cast<const unsigned long long*>(src));
+                    } else {
+                        *dst = __ldg(src);
+                    }
+                }
+                continue;  // next item (a strided map is never swizzled: image rows are plain)
+            }
             const uint32_t nch = nr * cpr;
             for (uint32_t it = threadIdx.x; it < nch; it += kThreads * kLoads) {
                 uint4 v[kLoads];
@@ -511,15 +503,6 @@ __global__ void __launch_bounds__(kThreads, 6) k_fb_store(const __grid_constant_
                     split_item(item, cpr, cpr_shift, r, j);
                     const int64_t off = tab[r];
                     if (off == kRowOutside) continue;
-                    if (kStep0) {
-                        uint8_t* const row = reinterpret_cast<uint8_t*>(a.base + off);
-                        const int step = (int)a.estride[0];
-                        if (es == 1) scatter_chunk<uint8_t>(row, v[k], (int)j, x, step);
-                        else if (es == 2) scatter_chunk<uint16_t>(row, v[k], (int)j, x, step);
-                        else if (es == 4) scatter_chunk<uint32_t>(row, v[k], (int)j, x, step);
-                        else scatter_chunk<unsigned long long>(row, v[k], (int)j, x, step);
-                        continue;
-                    }
                     const int pos = whole_x ? 0 : max(lo_byte - 16 * (int)j, 0);
                     const int end = whole_x ? 16 : min(hi_byte - 16 * (int)j, 16);
                     if (pos >= end) continue;
