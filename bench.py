@@ -476,7 +476,22 @@ def e2e_run(g: GpuWorkload, h: HostWorkload, ops, steps):
     torch.cuda.synchronize()
     if g.tm.tm_stream_check(g.stream) != g.tm.TM_OK:
         raise RuntimeError(g.tm.tm_last_error())
+    e2e_verify(h, pin_out)
     return e0.elapsed_time(e1) / steps, bi, bo
+
+
+def e2e_verify(h: HostWorkload, pin_out):
+    """The results the end-to-end leg read back are right: the round trips restored their tensors
+    byte for byte and the reduce destination holds dst + src (each step uploads dst afresh)."""
+    for k, src in (("w3_out", h.w3), ("w4_out", h.w4)):
+        if k in pin_out and not np.array_equal(pin_out[k].numpy(),
+                                                np.ascontiguousarray(src).reshape(-1).view(np.uint8)):
+            raise RuntimeError(f"end-to-end result {k} differs from its input")
+    if "w5a_dst" in pin_out:
+        got = pin_out["w5a_dst"].numpy().view(np.float32)
+        want = (h.w5a_dst.reshape(-1) + h.w5a_src.reshape(-1)).astype(np.float32)
+        if not np.array_equal(got.view(np.uint32), want.view(np.uint32)):
+            raise RuntimeError("end-to-end reduce result differs from dst + src")
 
 
 # ------------------------------------------------------------------------------------------------
