@@ -11,13 +11,17 @@
 // also prefetches tiles a few iterations ahead into L2 (cp.async.bulk.prefetch.tensor), so that
 // each stage's load finds its tiles in L2.
 //
-// CTA = 9 warps.  Warp 0: producer, one elected lane.  Warps 1-4 consume the A tile of each stage,
-// warps 5-8 the B tile (fewer for tiles under 128 rows); each consumer warp takes whole 32-row
-// blocks.  full[s] (count 1) completes when both tiles' bytes have landed; empty[s] (one arrival
-// per consumer warp) when every consumer warp has read the stage.  The per-warp partial sums meet
-// in shared-memory slots guarded by one more mbarrier per slot (S + 1 slots: no warp can be S
-// iterations ahead of another, so a slot is never rewritten before it was read).  Every wait is
-// bounded; no named barrier is used, so a warp that gives up cannot leave the others hanging.
+// CTA = 1 + G x 8 warps.  Warp 0: producer, one elected lane.  The consumers form G groups (G = 2
+// when S is even, else 1); group g takes tiles g, g + G, g + 2G, ..., so it always meets the same
+// S / G stages, and the per-tile chain of one group (reads, ordered sums, cross-warp combine)
+// overlaps the other's.  In a group, 4 warps consume the A tile and 4 the B tile (fewer for tiles
+// under 128 rows); each consumer warp takes whole 32-row blocks.  full[s] (count 1) completes
+// when both tiles' bytes have landed; empty[s] (one arrival per warp of the stage's group) when
+// that group has read the stage.  A group's per-warp partial sums meet in its own shared-memory
+// slots guarded by one more mbarrier per slot (S / G + 1 slots: within a group no warp can be
+// S / G of the group's iterations ahead of another, so a slot is never rewritten before it was
+// read).  Every wait is bounded; no named barrier is used, so a warp that gives up cannot leave
+// the others hanging.
 //
 // Consumer reads follow [MLSys-TMA] §"128-byte swizzle 的分组要求": lane l reads row l of a 32-row
 // block; at any instant eight neighbouring lanes read the same logical sector c of eight
@@ -37,8 +41,9 @@ namespace tmk {
 
 constexpr uint32_t kRingMaxStages = 8;
 constexpr uint32_t kRingMaxWpt = 4;                 // consumer warps per tile
+constexpr uint32_t kRingMaxGroups = 2;              // consumer groups (tiles i % groups)
 constexpr uint32_t kRingSlots = kRingMaxStages + 1;  // reduction slots: one more than the stages
-constexpr uint32_t kRingThreads = 32 * (1 + 2 * kRingMaxWpt);
+constexpr uint32_t kRingThreads = 32 * (1 + kRingMaxGroups * 2 * kRingMaxWpt);
 
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
@@ -50,15 +55,16 @@ __global__ void __launch_bounds__(kRingThreads, 1)
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kRingMaxStages];
     __shared__ __align__(8) uint64_t empty_bar[kRingMaxStages];
-    __shared__ __align__(8) uint64_t red_bar[2][kRingSlots];
-    __shared__ float red_cs[2][kRingSlots][kRingMaxWpt];
-    __shared__ uint32_t red_bits[2][kRingSlots][kRingMaxWpt];
+    __shared__ __align__(8) uint64_t red_bar[kRingMaxGroups][2][kRingSlots];
+    __shared__ float red_cs[kRingMaxGroups][2][kRingSlots][kRingMaxWpt];
+    __shared__ uint32_t red_bits[kRingMaxGroups][2][kRingSlots][kRingMaxWpt];
 
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + (kStageAlign - 1)) & ~(kStageAlign - 1);
     const uint8_t* const stage0 = smem_raw + (base - raw);
     const uint32_t S = r.stages;
-    const uint32_t NS = S + 1;
+    const uint32_t G = r.groups;   // 1, or 2 when S is even
+    const uint32_t NS = S / G + 1;  // reduction slots of a group: one more than its stages
     const uint32_t tile = r.tile_bytes;  // multiple of 1024
     const uint32_t wpt = r.rows >= 32 * kRingMaxWpt ? kRingMaxWpt : r.rows / 32;
     const uint32_t rpl = r.rows / (32 * wpt);  // rows per lane
@@ -74,9 +80,11 @@ __global__ void __launch_bounds__(kRingThreads, 1)
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), 2 * wpt);
         }
-        for (uint32_t s = 0; s < NS; s++) {
-            mbar_init(smem_u32(&red_bar[0][s]), wpt);
-            mbar_init(smem_u32(&red_bar[1][s]), wpt);
+        for (uint32_t g = 0; g < G; g++) {
+            for (uint32_t s = 0; s < NS; s++) {
+                mbar_init(smem_u32(&red_bar[g][0][s]), wpt);
+                mbar_init(smem_u32(&red_bar[g][1][s]), wpt);
+            }
         }
         fence_barrier_init();
     }
@@ -159,21 +167,27 @@ __global__ void __launch_bounds__(kRingThreads, 1)
         return;
     }
 
-    // ---------------- consumers: warps 1..wpt read A, the next wpt read B ----------------
+    // ---------------- consumers: G groups of 2 * wpt warps; group g takes tiles g, g + G, ...;
+    // in a group, wpt warps read A and the next wpt read B ----------------
     const uint32_t cw = warp - 1;
-    if (cw >= 2 * wpt) return;  // launched but idle (small tiles)
-    const uint32_t grp = cw / wpt;   // 0 = A, 1 = B
-    const uint32_t wi = cw % wpt;    // warp index inside the tile
+    if (cw >= G * 2 * wpt) return;  // launched but idle (small tiles)
+    const uint32_t gidx = cw / (2 * wpt);
+    const uint32_t cwg = cw % (2 * wpt);
+    const uint32_t grp = cwg / wpt;  // 0 = A, 1 = B
+    const uint32_t wi = cwg % wpt;   // warp index inside the tile
     float* const cs_out = grp == 0 ? r.cs_a : r.cs_b;
     unsigned long long* const bits_out = grp == 0 ? r.bits_a : r.bits_b;
     const uint32_t xr = r.swizzled ? 7u : 0u;
 
-    uint32_t s = 0, parity = 0;         // stage of tile i and its phase parity
-    uint32_t slot = 0, slot_parity = 0;  // reduction slot of tile i (NS slots) and its parity
-    for (uint64_t i = 0; i < n_local; i++) {
-        if (i) {
-            if (++s == S) {
-                s = 0;
+    // Stage of tile i (i % S; S is a multiple of G, so the group cycles through S / G stages) and
+    // its phase parity; the group's reduction slot (its own iteration count mod NS) and parity.
+    uint32_t s = gidx, parity = 0;
+    uint32_t slot = 0, slot_parity = 0;
+    for (uint64_t i = gidx; i < n_local; i += G) {
+        if (i != gidx) {
+            s += G;
+            if (s >= S) {
+                s -= S;
                 parity ^= 1u;
             }
             if (++slot == NS) {
@@ -258,20 +272,20 @@ __global__ void __launch_bounds__(kRingThreads, 1)
 
         // ... then across the tile's warps, in warp order (slots of iteration i % NS)
         if (lane == 0) {
-            red_cs[grp][slot][wi] = blk[0];
-            red_bits[grp][slot][wi] = bits;
-            mbar_arrive(smem_u32(&red_bar[grp][slot]));
+            red_cs[gidx][grp][slot][wi] = blk[0];
+            red_bits[gidx][grp][slot][wi] = bits;
+            mbar_arrive(smem_u32(&red_bar[gidx][grp][slot]));
         }
         if (wi == 0 && lane == 0) {
-            if (!mbar_wait(smem_u32(&red_bar[grp][slot]), slot_parity, r.timeout_ns)) {
+            if (!mbar_wait(smem_u32(&red_bar[gidx][grp][slot]), slot_parity, r.timeout_ns)) {
                 record_timeout(r.status, K_STREAM, slot, slot_parity, first + i * gridDim.x);
                 break;
             }
             float part[kRingMaxWpt];
             unsigned long long total = 0;
             for (uint32_t w = 0; w < wpt; w++) {
-                part[w] = red_cs[grp][slot][w];
-                total += red_bits[grp][slot][w];
+                part[w] = red_cs[gidx][grp][slot][w];
+                total += red_bits[gidx][grp][slot][w];
             }
             for (uint32_t n = wpt; n > 1; n >>= 1) {
                 for (uint32_t q = 0; q < n / 2; q++) part[q] = __fadd_rn(part[2 * q], part[2 * q + 1]);
@@ -299,7 +313,8 @@ cudaError_t launch_ring(const CUtensorMap* a, const CUtensorMap* b, const RingAr
     cudaError_t e =
         cudaFuncSetAttribute(k_ring, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_ring<<<grid, kRingThreads, smem, s>>>(*a, *b, r);
+    const uint32_t wpt = r.rows >= 32 * kRingMaxWpt ? kRingMaxWpt : r.rows / 32;
+    k_ring<<<grid, 32 * (1 + r.groups * 2 * wpt), smem, s>>>(*a, *b, r);
     return cudaGetLastError();
 }
 

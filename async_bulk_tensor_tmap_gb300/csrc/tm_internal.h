@@ -162,7 +162,7 @@ struct RingArgs {
     uint32_t tile_bytes;     // R * 128
     uint32_t swizzled;       // 1 = 128B, 0 = none
     uint32_t prefetch;       // tiles ahead of the ring prefetched into L2 (0 = none)
-    uint32_t pad;
+    uint32_t groups;         // consumer groups (1, or 2 when stages is even)
     float* cs_a;
     float* cs_b;
     unsigned long long* bits_a;

@@ -672,6 +672,10 @@ int stream_tiles(const tm_desc* a, const tm_desc* b, uint32_t stages, float* cs_
     r.tile_bytes = (uint32_t)a->box_bytes;
     r.swizzled = a->swizzle == TM_SWIZZLE_128B ? 1u : 0u;
     r.prefetch = (uint32_t)std::min<uint64_t>(env_u64("TM_RING_PREFETCH", 0), 64);
+    // Two consumer groups (even and odd tiles) when the stages divide between them
+    // (TM_RING_GROUPS=1 keeps one): a group's per-tile chain of reads, ordered sums and the
+    // cross-warp reduction then overlaps the other group's.
+    r.groups = (stages % 2 == 0 && env_u64("TM_RING_GROUPS", 2) >= 2) ? 2u : 1u;
     r.cs_a = cs_a;
     r.cs_b = cs_b;
     r.bits_a = (unsigned long long*)bits_a;
