@@ -27,7 +27,11 @@
 // block; at any instant eight neighbouring lanes read the same logical sector c of eight
 // consecutive rows, which the 128B swizzle has spread over physical sectors c XOR (row % 8): eight
 // distinct bank sectors, no conflict.  With swizzle NONE the same reads all hit sector c (8-way
-// conflict).
+// conflict).  The same section's ungrouped control (a 256-byte row stride, so that consecutive
+// rows sit two 128-byte swizzle rows apart) is reproduced by the row_pairs read order: lane l
+// reads row 2 (l mod 16) + l / 16, so eight neighbouring lanes meet swizzle rows 0, 2, ..., 14
+// and only four distinct sectors c XOR (2j mod 8) (2-way conflict).  A shuffle then hands each
+// row's sum to lane (row), so the results do not depend on the read order.
 //
 // What the consumer computes (the pages leave it open): per tile, each row is summed in fp32 in
 // logical element order starting from its first element; rows are combined by a pairwise-adjacent
@@ -178,6 +182,7 @@ __global__ void __launch_bounds__(kRingThreads, 1)
     float* const cs_out = grp == 0 ? r.cs_a : r.cs_b;
     unsigned long long* const bits_out = grp == 0 ? r.bits_a : r.bits_b;
     const uint32_t xr = r.swizzled ? 7u : 0u;
+    const uint32_t lrow = r.row_pairs ? 2 * (lane & 15) + (lane >> 4) : lane;  // row read by this lane
 
     // Stage of tile i (i % S; S is a multiple of G, so the group cycles through S / G stages) and
     // its phase parity; the group's reduction slot (its own iteration count mod NS) and parity.
@@ -215,7 +220,7 @@ __global__ void __launch_bounds__(kRingThreads, 1)
                 uint4 v[2][8];
 #pragma unroll
                 for (uint32_t u = 0; u < 2; u++) {
-                    const uint32_t row = 32 * (wi * rpl + q0 + u) + lane;
+                    const uint32_t row = 32 * (wi * rpl + q0 + u) + lrow;
                     const uint8_t* const rp = t_img + row * 128;
 #pragma unroll
                     for (uint32_t c = 0; c < 8; c++) {
@@ -257,6 +262,8 @@ __global__ void __launch_bounds__(kRingThreads, 1)
         for (uint32_t q = 0; q < 8; q++) {
             if (q < rpl) {
                 float v = blk[q];
+                // row_pairs: lane l held row 2 (l mod 16) + l / 16; hand lane l the sum of row l
+                if (r.row_pairs) v = __shfl_sync(0xffffffffu, v, (lane & 1) * 16 + (lane >> 1));
 #pragma unroll
                 for (int m = 1; m < 32; m <<= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, m));
                 blk[q] = v;

@@ -676,6 +676,10 @@ int stream_tiles(const tm_desc* a, const tm_desc* b, uint32_t stages, float* cs_
     // (TM_RING_GROUPS=1 keeps one): a group's per-tile chain of reads, ordered sums and the
     // cross-warp reduction then overlaps the other group's.
     r.groups = (stages % 2 == 0 && env_u64("TM_RING_GROUPS", 2) >= 2) ? 2u : 1u;
+    // Bank-conflict control (TM_RING_ROW_PAIRS=1): the consumers read the rows of each 32-row
+    // block in the order an ungrouped 256-byte row stride would give; same results.
+    r.row_pairs = env_u64("TM_RING_ROW_PAIRS", 0) ? 1u : 0u;
+    r.pad = 0;
     r.cs_a = cs_a;
     r.cs_b = cs_b;
     r.bits_a = (unsigned long long*)bits_a;

@@ -61,9 +61,14 @@ def parse():
                    help="divide every workload's row count by this (small cases for profiling, "
                         "below 1 for larger ones)")
     p.add_argument("--ring-stages", type=int, default=4, help="stages of the W5b ring")
-    p.add_argument("--ring-swizzle", default="128", choices=["128", "none"],
-                   help="swizzle of the ring's tiles (none = the bank-conflict control)")
-    return p.parse_args()
+    p.add_argument("--ring-swizzle", default="128", choices=["128", "none", "ungrouped"],
+                   help="swizzle of the ring's tiles (none = the 8-way bank-conflict control; "
+                        "ungrouped = 128B tiles read in the order of an ungrouped 256-byte row, "
+                        "the 2-way control)")
+    args = p.parse_args()
+    if args.ring_swizzle == "ungrouped":
+        os.environ["TM_RING_ROW_PAIRS"] = "1"  # read by the library at each ring call
+    return args
 
 
 def max_over_ranks(x: float, world: int) -> float:

@@ -217,7 +217,10 @@ int tile_reduce(const tm_desc* dst, const tm_desc* src, tm_redop op, void* strea
  *   are walked in box-grid order.  Per tile t (device outputs,
  *   num_boxes entries each): cs = fp32 checksum (each row summed in order from its first element,
  *   then a pairwise-adjacent tree over the rows), bits = sum of the 16-bit patterns.
- *   stages: 2..8. */
+ *   stages: 2..8.  With an even stage count two consumer groups take the even and the odd tiles
+ *   (TM_RING_GROUPS=1 keeps one); TM_RING_ROW_PAIRS=1 reads each 32-row block in the row order of
+ *   an ungrouped 256-byte row (the 2-way bank-conflict control of [MLSys-TMA] §"128-byte swizzle
+ *   的分组要求").  Neither changes the outputs. */
 int stream_tiles(const tm_desc* a, const tm_desc* b, uint32_t stages, float* cs_a, float* cs_b,
                  uint64_t* bits_a, uint64_t* bits_b, void* stream);
 

@@ -257,6 +257,41 @@ def test_w5b_ring_checksums(tm, span, stages):
     np.testing.assert_array_equal(to_host(bits_b).astype(np.uint64), wbb)
 
 
+# Many laps of the ring on every CTA: tiles of every supported height, ragged in both dims (296
+# columns = 4 full 64-column boxes + 40; rows not a multiple of the tile), with one consumer group,
+# two (even and odd tiles), and the row-pairs read order (the ungrouped bank-conflict control,
+# whose results must not change).  A and B are both M x 296, different seeds.
+RING_LAPS_ROWS = {32: 32000 - 5, 64: 48000 - 7, 128: 32000 - 9, 256: 64000 - 11}
+
+
+@pytest.mark.parametrize("rows", [32, 64, 128, 256])
+@pytest.mark.parametrize("mode", ["two_groups", "one_group", "row_pairs"])
+def test_w5b_ring_many_laps(tm, monkeypatch, rows, mode):
+    stages = 3 if rows == 256 else 4
+    monkeypatch.setenv("TM_RING_GROUPS", "1" if mode == "one_group" else "2")
+    monkeypatch.setenv("TM_RING_ROW_PAIRS", "1" if mode == "row_pairs" else "0")
+    m = RING_LAPS_ROWS[rows]
+    a = workloads.normal_bf16((m, 296), 60 + rows)
+    b = workloads.normal_bf16((m, 296), 61 + rows)
+    r = dict(dims=[296, m], strides=[592], box=[64, rows], span=128, esize=2)
+    ad, bd = to_dev(a), to_dev(b)
+    ma, mb = dev_map(tm, ad, r), dev_map(tm, bd, r)
+    n = ma.num_boxes
+    assert n == 5 * -(-m // rows) and n > 1000
+    cs_a = torch.zeros(n, dtype=torch.float32, device="cuda")
+    cs_b = torch.zeros_like(cs_a)
+    bits_a = torch.zeros(n, dtype=torch.int64, device="cuda")
+    bits_b = torch.zeros_like(bits_a)
+    tm.stream_tiles(ma, mb, stages, cs_a, cs_b, bits_a, bits_b)
+    check(tm)
+    wa, wb, wba, wbb = oracle.stream_checksums(host_map(a, r), host_map(b, r),
+                                               threads=oracle.host_cores())
+    np.testing.assert_array_equal(to_host(cs_a).view(np.uint32), wa.view(np.uint32))
+    np.testing.assert_array_equal(to_host(cs_b).view(np.uint32), wb.view(np.uint32))
+    np.testing.assert_array_equal(to_host(bits_a).astype(np.uint64), wba)
+    np.testing.assert_array_equal(to_host(bits_b).astype(np.uint64), wbb)
+
+
 # ---- brute force: random tiny maps of every rank, swizzle and element size ----------------------
 def random_recipe(rng, span, aligned):
     rank = int(rng.integers(1, 6))
