@@ -13,7 +13,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtmap_gb300.so")
 
-SOURCES = ["tmap_host.cpp", "k_tma.cu", "k_fallback.cu", "k_ring.cu", "k_gemm.cu", "tm_noalloc.cu"]
+SOURCES = ["tmap_host.cpp", "k_tma.cu", "k_fallback.cu", "k_fb_seg.cu", "k_ring.cu", "k_gemm.cu",
+           "tm_noalloc.cu"]
 HEADERS = ["tm_internal.h", "tm_ptx.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,

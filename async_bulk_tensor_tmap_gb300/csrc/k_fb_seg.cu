@@ -1,0 +1,345 @@
+// k_fb_seg.cu -- the segment form of the vector path (load direction): maps the tensor-map
+// hardware cannot take (a stride or base that is not a multiple of 16 bytes), walked over their
+// whole box grid with unit elementStrides.
+//
+// What it computes is the same box image as the tensor-map load ([Book-TMA] §"Tensor descriptor：
+// CUtensorMap": the box at the grid start, elements outside the tensor filled; [MLSys-TMA]
+// §"用 3D TMA 搬运多个 swizzle atoms": 16-byte sectors placed at logical sector XOR (row % 8) in
+// 128-byte rows).  How it moves the bytes follows the same pages' asynchronous-copy design rather
+// than per-thread loads: contiguous tensor bytes are staged by 1-D bulk copies completing on an
+// mbarrier ([MLSys-TMA] §"如何等待 TMA load 完成"), threads realign them into the swizzled image
+// in shared memory, and the image leaves by a bulk store tracked by a bulk group ([MLSys-TMA]
+// §"如何等待 TMA store 完成").
+//
+// Work unit (item): one block of image rows of a RUN, the run being all boxes along dim 0 of one
+// position of the grid in dims 1 and up.  A run covers whole tensor rows, so no tensor byte is
+// read twice; and when dim 1 is contiguous with dim 0 (stride[1] == dim[0] * esize, a reshaped
+// view) the ibox[1] image rows of a box lie back to back in memory and form one SEGMENT of
+// ibox[1] * dim[0] * esize bytes (one bulk copy instead of many 16-byte windows; the W4 rank-5
+// view's segments are 2000 bytes).  Without that contiguity a segment is one tensor row.
+//
+// Pipeline per CTA (items in a contiguous range): S staging buffers and two image buffers.  At
+// the top of item n, warp 0 issues the bulk copies of item n + S - 1 into the staging buffer item
+// n - 1 has released (one lane per segment; lane 0 first posts the total bytes on that buffer's
+// mbarrier), so S - 1 items' bytes are in flight while one is realigned; thread 0
+// waits until the bulk store of item n - 2 has finished reading image buffer n % 2; everyone
+// waits for item n's segments, realigns them (16-byte chunks read at their byte offset with the
+// widest shared loads the offset allows, fill beyond the tensor, written to the swizzled place),
+// fences the generic writes for the async proxy, and thread 0 bulk-stores the block of each box.
+// Every mbarrier wait is bounded; a wait that gives up is reported and ends the CTA after its
+// copies in flight have landed.
+#include "tm_ptx.cuh"
+
+namespace tmk {
+
+constexpr uint32_t kSegConsumerWarps = 8;
+constexpr uint32_t kSegThreads = 32 * (1 + kSegConsumerWarps);
+
+namespace {
+
+// Segment g of the run whose first box starts at c (c[0] = 0): its tensor address, the number of
+// its image rows that lie in the tensor (0: none) and its length in bytes.
+struct Segment {
+    uint64_t src;
+    uint32_t rows;
+    uint32_t bytes;
+};
+
+__device__ __forceinline__ Segment segment_of(const SegArgs& s, const int32_t* c, uint32_t g)
+{
+    const FbArgs& a = s.f;
+    int64_t off = 0;
+    bool ok = true;
+    uint32_t r = g;
+#pragma unroll
+    for (int i = 1; i < 5; i++) {
+        if (i >= (int)s.outer0 && i < (int)a.walk.rank) {
+            const uint32_t bi = a.ibox[i];
+            const uint32_t q = bi == 1 ? r : r / bi;
+            const int64_t x = (int64_t)c[i] + (int64_t)(r - q * bi);
+            r = q;
+            ok = ok && (uint64_t)x < a.dim[i];
+            off += x * a.stride[i];
+        }
+    }
+    Segment sg;
+    sg.rows = 0;
+    sg.bytes = 0;
+    sg.src = 0;
+    if (!ok) return sg;
+    if (s.outer0 == 2) {  // dims 0 and 1 contiguous: the box's rows along dim 1 in the tensor
+        const uint64_t left = a.dim[1] - (uint64_t)c[1];
+        sg.rows = (uint32_t)(left < s.seg_rows ? left : s.seg_rows);
+        off += (int64_t)c[1] * a.stride[1];
+    } else {
+        sg.rows = 1;
+    }
+    sg.bytes = sg.rows * s.row_bytes;
+    sg.src = (uint64_t)((int64_t)a.base + off);
+    return sg;
+}
+
+// Run u, row block q of item m; the run's first box start c.
+__device__ __forceinline__ void item_of(const SegArgs& s, uint64_t m, uint64_t& u, uint32_t& q,
+                                        int32_t* c)
+{
+    u = m / s.nblk;
+    q = (uint32_t)(m - u * s.nblk);
+    uint32_t k[5];
+    grid_counters(s.f.walk, u * s.run, k);
+#pragma unroll
+    for (int i = 0; i < 5; i++) c[i] = i < (int)s.f.walk.rank ? (int32_t)(k[i] * s.f.walk.box[i]) : 0;
+}
+
+// The 16 shared-memory bytes at p, whose address is p_al (p = p_al + d, d = p & 15), read with
+// the widest loads the offset allows; two aligned 16-byte loads and a funnel shift when d is not
+// a multiple of 4.
+__device__ __forceinline__ uint4 load16(const uint8_t* p, uint32_t d)
+{
+    if (d == 0) return *reinterpret_cast<const uint4*>(p);
+    if ((d & 7) == 0) {
+        const uint2 x = reinterpret_cast<const uint2*>(p)[0];
+        const uint2 y = reinterpret_cast<const uint2*>(p)[1];
+        return make_uint4(x.x, x.y, y.x, y.y);
+    }
+    if ((d & 3) == 0) {
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(p);
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    const uint4* al = reinterpret_cast<const uint4*>(p - d);
+    const uint4 lo = al[0], hi = al[1];
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    const uint32_t qd = d >> 2, sh = (d & 3u) * 8u;
+    uint32_t o[4];
+#pragma unroll
+    for (int t = 0; t < 4; t++) {
+        uint32_t x0 = w[t], y0 = w[t + 1];
+#pragma unroll
+        for (uint32_t k = 1; k < 4; k++) {
+            if (qd == k) {
+                x0 = w[t + k];
+                y0 = w[t + k + 1];
+            }
+        }
+        o[t] = __funnelshift_r(x0, y0, sh);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Keeps the first `n` bytes (0 < n < 16) of v and puts fill bytes in the rest.
+__device__ __forceinline__ uint4 keep_head(uint4 v, const uint4& fill, int n)
+{
+    uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+    const uint32_t* f = reinterpret_cast<const uint32_t*>(&fill);
+#pragma unroll
+    for (int t = 0; t < 4; t++) {
+        const int k = n - 4 * t;
+        const uint32_t m = k >= 4 ? 0xffffffffu : k <= 0 ? 0u : ((1u << (8 * k)) - 1u);
+        w[t] = (w[t] & m) | (f[t] & ~m);
+    }
+    return v;
+}
+
+}  // namespace
+
+// 16 bytes of the fill element (zero, or the NaN pattern of a TM_OOB_NAN map).
+__device__ __forceinline__ uint4 seg_fill(const FbArgs& a)
+{
+    if (!a.fill_nan) return make_uint4(0, 0, 0, 0);
+    uint32_t lo, hi;
+    if (a.esize == 2) {
+        lo = hi = (uint32_t)(a.fill & 0xffffu) * 0x10001u;
+    } else if (a.esize == 4) {
+        lo = hi = (uint32_t)a.fill;
+    } else {
+        lo = (uint32_t)a.fill;
+        hi = (uint32_t)(a.fill >> 32);
+    }
+    return make_uint4(lo, hi, lo, hi);
+}
+
+// What the producer leaves beside each staging buffer for the item it staged.
+struct SegItem {
+    uint64_t run;  // run index u: boxes u * run .. u * run + run - 1
+    uint32_t r0;   // first image row of the item in its boxes
+    uint32_t nr;   // image rows of the item in each box
+};
+
+__global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_copy(const __grid_constant__ SegArgs s)
+{
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t full_bar[kSegMaxStages];   // segments landed (count 1 + bytes)
+    __shared__ __align__(8) uint64_t empty_bar[kSegMaxStages];  // consumers done (one per warp)
+    __shared__ SegItem info[kSegMaxStages];
+    const FbArgs& a = s.f;
+    const uint32_t E = s.block_groups;
+    const uint32_t G1 = s.seg_rows;
+    const uint32_t S = s.stages;
+    uint8_t* const sbuf0 = smem_raw;  // S x E segments
+    // per staging buffer, the shared-memory offset of each image row's tensor byte 0 (-1: the
+    // row lies outside the tensor)
+    int32_t* const tabs = reinterpret_cast<int32_t*>(smem_raw + (size_t)S * E * s.seg_stride);
+
+    const uint64_t T = s.nrun * s.nblk;
+    const uint64_t per = T / gridDim.x, extra = T % gridDim.x;
+    const uint64_t m0 = blockIdx.x * per + (blockIdx.x < extra ? blockIdx.x : extra);
+    const uint64_t total = per + (blockIdx.x < extra ? 1 : 0);
+    if (total == 0) return;
+    const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (uint32_t i = 0; i < S; i++) {
+            mbar_init(smem_u32(&full_bar[i]), 1);
+            mbar_init(smem_u32(&empty_bar[i]), kSegConsumerWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == 0) {
+        // ---- producer: walks the CTA's items with a cursor (run u, row block q, counters k of
+        // the run's first box; every lane keeps the same copy) stepped with carries.  Item i
+        // goes to buffer i % S once the consumers have released that buffer's item i - S.
+        uint64_t cu;
+        uint32_t cq;
+        uint32_t ck[5];
+        {
+            int32_t c[5];
+            item_of(s, m0, cu, cq, c);
+            for (int i = 0; i < 5; i++)
+                ck[i] = i < (int)a.walk.rank ? (uint32_t)c[i] / a.walk.box[i] : 0;
+        }
+        // item i: buffer b = i % S, lap = i / S; for i >= S it waits for the release of item
+        // i - S, the buffer's completion number lap - 1
+        uint32_t b = 0, lap = 0;
+        uint64_t i = 0;
+        for (; i < total; i++) {
+            if (lap > 0) {
+                const uint32_t eparity = (lap - 1) & 1u;
+                const bool ok = mbar_wait(smem_u32(&empty_bar[b]), eparity, a.timeout_ns);
+                if (!__all_sync(0xffffffffu, ok)) {
+                    if (lane == 0) record_timeout(a.status, K_FB_SEG_COPY, b, eparity, m0 + i);
+                    break;
+                }
+            }
+            int32_t c[5];
+#pragma unroll
+            for (int d = 0; d < 5; d++) c[d] = (int32_t)(ck[d] * a.walk.box[d]);
+            const uint32_t g0 = cq * E;
+            const uint32_t ng = min(E, s.groups - g0);
+            int32_t* const tab = tabs + (size_t)b * E * G1;
+            const uint32_t sbase = b * E * s.seg_stride;
+            // lane j takes segments j, j + 32, ...: their rows' table entries, then (after lane 0
+            // has posted the item's total bytes) their bulk copies
+            uint32_t bytes = 0;
+            for (uint32_t j = lane; j < ng; j += 32) {
+                const Segment sg = segment_of(s, c, g0 + j);
+                const int32_t at = (int32_t)(sbase + j * s.seg_stride + (uint32_t)(sg.src & 15));
+                for (uint32_t e = 0; e < G1; e++)
+                    tab[j * G1 + e] = e < sg.rows ? at + (int32_t)(e * s.row_bytes) : -1;
+                if (sg.rows) bytes += (uint32_t)(((sg.src & 15) + sg.bytes + 15) & ~15ull);
+            }
+            bytes = __reduce_add_sync(0xffffffffu, bytes);
+            const uint32_t bar = smem_u32(&full_bar[b]);
+            if (lane == 0) {
+                info[b].run = cu;
+                info[b].r0 = g0 * G1;
+                info[b].nr = ng * G1;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(bar, bytes);  // publishes the table and info
+            __syncwarp();
+            const uint32_t dst0 = smem_u32(sbuf0 + sbase);
+            for (uint32_t j = lane; j < ng; j += 32) {
+                const Segment sg = segment_of(s, c, g0 + j);
+                if (sg.rows) {
+                    const uint32_t n = (uint32_t)(((sg.src & 15) + sg.bytes + 15) & ~15ull);
+                    bulk_load(dst0 + j * s.seg_stride, sg.src & ~15ull, n, bar);
+                }
+            }
+            // step the cursor: the next row block, else the next run (odometer over dims 1..)
+            if (++cq == s.nblk) {
+                cq = 0;
+                cu++;
+                uint32_t carry = 1;
+#pragma unroll
+                for (int d = 1; d < 5; d++) {
+                    if (d < (int)a.walk.rank && carry) {
+                        ck[d]++;
+                        carry = ck[d] == a.walk.grid_nb[d] ? 1u : 0u;
+                        if (carry) ck[d] = 0;
+                    }
+                }
+            }
+            if (++b == S) {
+                b = 0;
+                lap++;
+            }
+        }
+        // the copies issued last land before the CTA leaves (the consumers normally saw them)
+        if (lane == 0) {
+            const uint64_t lo = i > S ? i - S : 0;
+            for (uint64_t k = lo; k < i; k++)
+                mbar_wait(smem_u32(&full_bar[k % S]), (uint32_t)((k / S) & 1), a.timeout_ns);
+        }
+        return;
+    }
+
+    // ---- consumers: realign item n's chunks, stored straight to the global images (a warp's 32
+    // chunks are four whole 128-byte image rows, permuted inside each row by the swizzle)
+    const uint32_t inner = a.inner_bytes;
+    const uint32_t cpr = inner >> 4;  // 16-byte chunks per image row
+    const uint32_t cpr_shift = (cpr & (cpr - 1)) == 0 ? (uint32_t)(__ffs(cpr) - 1) : 32u;
+    const uint4 fillv = seg_fill(a);
+    const uint32_t row_bytes = s.row_bytes;
+    const uint32_t ct = threadIdx.x - 32;  // consumer thread index
+    constexpr uint32_t kCT = 32 * kSegConsumerWarps;
+    uint32_t sb = 0, sparity = 0;  // staging buffer of item n (n % S) and its phase parity
+    for (uint64_t n = 0; n < total; n++) {
+        if (n) {
+            if (++sb == S) {
+                sb = 0;
+                sparity ^= 1u;
+            }
+        }
+        const bool ok = mbar_wait(smem_u32(&full_bar[sb]), sparity, a.timeout_ns);
+        if (!__all_sync(0xffffffffu, ok)) {
+            if (lane == 0) record_timeout(a.status, K_FB_SEG_COPY, sb, sparity, m0 + n);
+            break;
+        }
+        const int32_t* const tab = tabs + (size_t)sb * E * G1;
+        const uint32_t r0 = info[sb].r0;
+        const uint32_t nr = info[sb].nr;
+        const uint64_t box0 = info[sb].run * s.run;
+        const uint32_t per_box = nr * cpr;
+        for (uint32_t k = 0; k < s.run; k++) {
+            uint8_t* const img = reinterpret_cast<uint8_t*>(a.images + (box0 + k) * a.box_bytes);
+            for (uint32_t rc = ct; rc < per_box; rc += kCT) {
+                const uint32_t r = cpr_shift < 32 ? rc >> cpr_shift : rc / cpr;
+                const uint32_t j = rc - r * cpr;
+                const int32_t at = tab[r];
+                const int x = (int)(k * inner + 16 * j);  // the chunk's first byte in the tensor row
+                const int left = (int)row_bytes - x;
+                uint4 v = fillv;
+                if (at >= 0 && left > 0) {
+                    const uint32_t p = (uint32_t)at + (uint32_t)x;
+                    v = load16(smem_raw + p, p & 15u);
+                    if (left < 16) v = keep_head(v, fillv, left);
+                }
+                *reinterpret_cast<uint4*>(img + swizzle_offset((r0 + r) * inner + 16 * j, a.span)) = v;
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty_bar[sb]));  // this warp's reads are done
+    }
+}
+
+cudaError_t launch_fb_seg_copy(const SegArgs& a, uint32_t grid, size_t smem, cudaStream_t st)
+{
+    cudaError_t e =
+        cudaFuncSetAttribute(k_fb_seg_copy, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    k_fb_seg_copy<<<grid, kSegThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace tmk

@@ -185,9 +185,15 @@ extern "C" int tiled_copy_noalloc(const tm_desc* src, const int32_t* coords, siz
         a.status = status;
         uint32_t grid = 0;
         size_t smem = 0;
-        fb_shape(a, n, (uint32_t)d->sms, 8u, fb_copy_row_bytes(a.gspan0),
-                 [&](uint32_t per_sm) { return budget(*d, per_sm); }, grid, smem);
-        e = launch_fb_copy(a, grid, smem, st);
+        SegArgs sa;
+        if (seg_plan(a, src, (uint32_t)d->sms, 2u, 2u, 2,
+                     [&](uint32_t per_sm) { return budget(*d, per_sm); }, sa, grid, smem)) {
+            e = launch_fb_seg_copy(sa, grid, smem, st);
+        } else {
+            fb_shape(a, n, (uint32_t)d->sms, 8u, fb_copy_row_bytes(a.gspan0),
+                     [&](uint32_t per_sm) { return budget(*d, per_sm); }, grid, smem);
+            e = launch_fb_copy(a, grid, smem, st);
+        }
     }
     if (e != cudaSuccess) return cuda_err(e, "copy launch");
     // The status word is read back before returning, so the call completes the copy.

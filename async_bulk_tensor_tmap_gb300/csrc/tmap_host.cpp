@@ -328,11 +328,24 @@ int copy_boxes(const tm_desc* src, const int32_t* coords, size_t nbox, void* ima
         FbArgs a = fb_args(src, w, (uint64_t)images, *ds);
         uint32_t grid = 0;
         size_t smem = 0;
-        fb_shape(a, n, (uint32_t)ds->sms,
-                 (uint32_t)std::min<uint64_t>(env_u64("TM_FB_COPY_CTAS_PER_SM", 8), 16),
-                 fb_copy_row_bytes(a.gspan0),
-                 [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); }, grid, smem);
-        rc = check_launch(launch_fb_copy(a, grid, smem, st), "fallback copy launch");
+        SegArgs sa;
+        // TM_FB_SEG: 0 = never the segment form, 1 = whenever the layout allows it, unset = when
+        // its segments are long enough for bulk copies.  Defaults (2 CTAs per SM, 2 staging
+        // buffers: the largest items) measured best on GB300 on the W4 rank-5 view, 5.26 TB/s
+        // against 3.77 for the per-window form; deeper staging with smaller items was slower.
+        if (seg_plan(a, src, (uint32_t)ds->sms,
+                     (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_CTAS_PER_SM", 2), 8),
+                     (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_STAGES", 2), kSegMaxStages),
+                     (int)env_u64("TM_FB_SEG", 2),
+                     [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); }, sa, grid, smem)) {
+            rc = check_launch(launch_fb_seg_copy(sa, grid, smem, st), "fallback segment copy launch");
+        } else {
+            fb_shape(a, n, (uint32_t)ds->sms,
+                     (uint32_t)std::min<uint64_t>(env_u64("TM_FB_COPY_CTAS_PER_SM", 8), 16),
+                     fb_copy_row_bytes(a.gspan0),
+                     [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); }, grid, smem);
+            rc = check_launch(launch_fb_copy(a, grid, smem, st), "fallback copy launch");
+        }
     }
     release_walk(w, st);
     return rc;
@@ -808,8 +821,8 @@ int tm_stream_check(void* stream)
         return cuda_fail(e, "clearing the status word");
     static const char* names[] = {"?", "tiled copy", "round trip", "reduce-add", "ring",
                                   "fallback copy", "fallback store", "fallback reduce", "self-test",
-                                  "gemm"};
-    const char* kn = sb.kernel < 10 ? names[sb.kernel] : "?";
+                                  "gemm", "fallback segment copy"};
+    const char* kn = sb.kernel < sizeof(names) / sizeof(names[0]) ? names[sb.kernel] : "?";
     return fail(sb.code, "%s kernel: wait gave up in block %u, stage %u, parity %u, box %llu", kn,
                 sb.block, sb.stage, sb.phase, (unsigned long long)sb.box);
 }

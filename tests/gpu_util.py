@@ -44,3 +44,24 @@ def host_map(arr: np.ndarray, r, offset=0, dtype=None):
 def empty_images(n_boxes: int, box_bytes: int, fill: int = 0x5A):
     import torch
     return torch.full((n_boxes * box_bytes,), fill, dtype=torch.uint8, device="cuda")
+
+
+U = {1: np.uint8, 2: np.uint16, 4: np.uint32, 8: np.uint64}
+ESIZE = {6: 2, 9: 2, 7: 4, 8: 8}  # library dtype code -> element size
+
+
+def as_float(bits, dtype, tm):
+    if dtype == tm.TM_BF16:
+        return (bits.astype(np.uint32) << 16).view(np.float32)
+    return bits.view({tm.TM_F16: np.float16, tm.TM_F32: np.float32, tm.TM_F64: np.float64}[dtype])
+
+
+def assert_nan_fill(got, want, dtype, tm):
+    """In-bounds elements (finite in the oracle's image) bit-exact; the rest NaN (the pages name
+    no NaN bit pattern: any NaN is a correct fill)."""
+    es = ESIZE[dtype]
+    g, w = got.view(U[es]), want.view(U[es])
+    oob = np.isnan(as_float(w, dtype, tm))
+    assert oob.any() and (~oob).any()
+    np.testing.assert_array_equal(g[~oob], w[~oob])
+    assert np.isnan(as_float(g[oob], dtype, tm)).all()

@@ -10,7 +10,7 @@ import pytest
 
 import oracle
 import workloads
-from gpu_util import dev_map, empty_images, host_map, to_dev, to_host
+from gpu_util import assert_nan_fill, dev_map, empty_images, host_map, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -217,6 +217,45 @@ def test_w4_ragged_and_fallback(tm, variant):
     assert torch.equal(dst, xd)
 
 
+# The vector copy's two forms on the same maps: per-window staging (TM_FB_SEG=0) and segments
+# (TM_FB_SEG=1: one bulk copy per contiguous run of rows, images leave by bulk stores).  Ragged
+# boxes along every dim, NaN fill, a base 2 bytes off alignment, rows of one and of several
+# segments.
+SEG_CASES = {
+    # the W4 rank-5 view (dims 0 and 1 contiguous: 2000-byte segments), ragged along dim 2
+    "w4r5": (workloads.w4_rank5_map(**W4_SMALL, span=128), 0, False),
+    # the same view, box 4 rows along dim 1 (the last box of a group holds 2 rows), NaN fill
+    "w4r5_dim1_ragged": (dict(workloads.w4_rank5_map(**W4_SMALL, span=128), box=[64, 4, 16, 1, 1],
+                              nan=True), 0, True),
+    # one-row segments: rows of 1000 elements at a 2048-byte pitch, the base 2 bytes off
+    "rows_offset": (dict(dims=[1000, 70, 16], strides=[2048, 70 * 2048], box=[64, 32, 2],
+                         span=128, esize=2), 2, False),
+    # dims 0 and 1 contiguous, unswizzled 48-byte image rows, 3 boxes along dim 0
+    "fused_48B": (dict(dims=[60, 9, 70, 16], strides=[120, 1080, 70 * 2048], box=[24, 3, 8, 1],
+                       span=0, esize=2), 0, False),
+}
+
+
+@pytest.mark.parametrize("case", sorted(SEG_CASES))
+@pytest.mark.parametrize("seg", ["0", "1"])
+def test_vector_copy_forms(tm, monkeypatch, case, seg):
+    monkeypatch.setenv("TM_FB_SEG", seg)
+    r, offset, nan = SEG_CASES[case]
+    x = workloads.w4_tensor(**W4_SMALL, seed=43)
+    dt = tm.TM_BF16 if nan else None
+    xd = to_dev(x)
+    m = dev_map(tm, xd, r, offset=offset, dtype=dt)
+    assert m.path == tm.TM_PATH_FALLBACK
+    imgs = empty_images(m.num_boxes, m.box_bytes)
+    tm.tiled_copy(m, None, imgs)
+    check(tm)
+    want = oracle.tiled_copy(host_map(x, r, offset=offset, dtype=dt), threads=8)
+    if nan:
+        assert_nan_fill(to_host(imgs), want, dt, tm)
+    else:
+        np.testing.assert_array_equal(to_host(imgs), want)
+
+
 # ---- W5a (reduced): fp32 reduce-add, [Book-TMA] §"TMA reduce，把“搬运”和“归约”合并" ----------------
 @pytest.mark.parametrize("span", [128, 0])
 @pytest.mark.parametrize("force_fallback", [False, True])
@@ -315,7 +354,10 @@ def random_recipe(rng, span, aligned):
 
 @pytest.mark.parametrize("span", [0, 32, 64, 128])
 @pytest.mark.parametrize("aligned", [True, False])
-def test_brute_force_tiny(tm, span, aligned):
+@pytest.mark.parametrize("seg", ["auto", "forced"])
+def test_brute_force_tiny(tm, monkeypatch, span, aligned, seg):
+    if seg == "forced":  # the vector copy's segment form whenever the layout allows it
+        monkeypatch.setenv("TM_FB_SEG", "1")
     rng = np.random.default_rng(500 + span + aligned)
     for _ in range(25):
         r, nbytes = random_recipe(rng, span, aligned)

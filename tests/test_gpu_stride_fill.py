@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 import oracle
-from gpu_util import dev_map, host_map, to_dev, to_host
+from gpu_util import ESIZE, as_float, assert_nan_fill, dev_map, host_map, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -156,13 +156,6 @@ def finite_floats(dtype, tm, n, seed):
     return v.view(np.uint8)
 
 
-def as_float(bits, dtype, tm):
-    if dtype == tm.TM_BF16:
-        return (bits.astype(np.uint32) << 16).view(np.float32)
-    return bits.view({tm.TM_F16: np.float16, tm.TM_F32: np.float32, tm.TM_F64: np.float64}[dtype])
-
-
-ESIZE = {6: 2, 9: 2, 7: 4, 8: 8}
 
 
 def nan_recipe(dtype, span, steps, cut=5):
@@ -172,16 +165,6 @@ def nan_recipe(dtype, span, steps, cut=5):
     pitch = (dims[0] * es + 15) // 16 * 16
     return dict(esize=es, dims=dims, strides=[pitch, pitch * 37], box=[box0, 8, 2], span=span,
                 estrides=steps, nan=True)
-
-
-def assert_nan_fill(got, want, dtype, tm):
-    """In-bounds elements (finite in the oracle's image) bit-exact; the rest NaN."""
-    es = ESIZE[dtype]
-    g, w = got.view(U[es]), want.view(U[es])
-    oob = np.isnan(as_float(w, dtype, tm))
-    assert oob.any() and (~oob).any()
-    np.testing.assert_array_equal(g[~oob], w[~oob])
-    assert np.isnan(as_float(g[oob], dtype, tm)).all()
 
 
 @pytest.mark.parametrize("force_fb", [False, True])

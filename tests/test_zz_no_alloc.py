@@ -78,3 +78,23 @@ def test_noalloc_rejects_lists_beyond_its_scratch(tm):
         tm.tiled_copy_noalloc(m, coords, images)
     assert e.value.code == tm.TM_ERANGE
     assert "at most" in str(e.value)
+
+
+def test_noalloc_vector_path_whole_grid(tm):
+    """A map the tensor-map hardware cannot take (the W4 rank-5 view, 200-byte stride), its whole
+    grid: the no-allocation copy gives the allocating copy's images."""
+    kw = dict(batch=16, rows=70, cols=1000, pitch=1024)
+    x = workloads.w4_tensor(**kw, seed=45)
+    r = workloads.w4_rank5_map(**kw, span=128)
+    xd = _dev(x)
+    m = tm.tmap_encode(tm.TM_BF16, xd, r["dims"], r["strides"], r["box"],
+                       swizzle=tm.TM_SWIZZLE_128B)
+    assert m.path == tm.TM_PATH_FALLBACK
+    want = torch.zeros(m.num_boxes * m.box_bytes, dtype=torch.uint8, device="cuda")
+    tm.tiled_copy(m, None, want)
+    torch.cuda.synchronize()
+    assert tm.tm_stream_check() == tm.TM_OK, tm.tm_last_error()
+    for _ in range(2):
+        got = torch.full_like(want, 0x44)
+        tm.tiled_copy_noalloc(m, None, got)
+        assert torch.equal(got, want)
