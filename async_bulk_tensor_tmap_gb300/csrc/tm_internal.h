@@ -17,7 +17,7 @@ constexpr uint32_t kStageAlign = 1024; // 128B swizzle is computed on smem addre
 // Kernel ids recorded with a timeout.
 enum KernelId : uint32_t {
     K_COPY = 1, K_ROUNDTRIP = 2, K_REDUCE = 3, K_STREAM = 4, K_FB_COPY = 5, K_FB_STORE = 6,
-    K_FB_REDUCE = 7, K_SELFTEST = 8, K_GEMM = 9, K_FB_SEG_COPY = 10
+    K_FB_REDUCE = 7, K_SELFTEST = 8, K_GEMM = 9, K_FB_SEG_COPY = 10, K_FB_SEG_STORE = 11
 };
 
 // Per-device status word written by a kernel whose bounded wait gave up.
@@ -158,8 +158,8 @@ inline void fb_shape(FbArgs& a, uint64_t nbox, uint32_t sms, uint32_t want, size
 // Segment form of the vector path (grid walks with unit elementStrides): the boxes along dim 0
 // of one block of image rows are handled together as a run, which covers whole tensor rows; when
 // dim 1 is contiguous with dim 0 (stride[1] == dim[0] * esize) the ibox[1] image rows of a box
-// lie back to back in memory and form one segment.  Each segment is staged by one 1-D bulk copy
-// and each box's block of image rows leaves shared memory by one bulk store.
+// lie back to back in memory and form one segment.  The copy stages each segment by one 1-D bulk
+// copy; the store stages each box's block of image rows by one.
 struct SegArgs {
     FbArgs f;
     uint64_t nrun;          // runs = boxes / run
@@ -171,7 +171,7 @@ struct SegArgs {
     uint32_t nblk;          // items per run
     uint32_t seg_stride;    // shared-memory bytes per staged segment
     uint32_t row_bytes;     // dim[0] * esize: tensor bytes of one row
-    uint32_t pad;
+    uint32_t img_stride;    // store: shared-memory bytes per box image block of an item
     uint32_t stages;        // staging buffers (items in flight per CTA)
 };
 constexpr uint32_t kSegMinBytes = 512;  // shorter segments: the per-window copy (request rate)
@@ -182,10 +182,13 @@ constexpr uint32_t kSegMaxStages = 8;
 // map does not take it: segments of ibox[1] rows when dims 0 and 1 are contiguous and such a
 // segment fits, else of one row.  force: 1 = whenever the layout allows (any segment length),
 // 0 = never, other = when segments are at least kSegMinBytes.  budget(n) as for fb_shape.
+// Copy: a stage holds an item's segments (seg_stride bytes each) and a 4-byte shared-memory
+// offset per image row.  Store (store = true): a stage holds the item's image block of each box of
+// the run (img_stride bytes each) and an 8-byte tensor address per image row.
 template <class Budget>
 inline bool seg_plan_rows(const FbArgs& a, uint64_t g1, uint32_t sms, uint32_t want,
-                          uint32_t stages, int force, Budget budget, SegArgs& s, uint32_t& grid,
-                          size_t& smem)
+                          uint32_t stages, int force, bool store, Budget budget, SegArgs& s,
+                          uint32_t& grid, size_t& smem)
 {
     const uint64_t row_bytes = a.dim[0] * a.esize;
     const uint64_t seg_max = g1 * row_bytes;
@@ -194,7 +197,8 @@ inline bool seg_plan_rows(const FbArgs& a, uint64_t g1, uint32_t sms, uint32_t w
     const uint64_t nb0 = a.walk.grid_nb[0];
     const uint64_t seg_stride = (seg_max + 48 + 15) / 16 * 16;
     const uint64_t S = std::min<uint32_t>(std::max<uint32_t>(stages, 2), kSegMaxStages);
-    const uint64_t per_group = S * (seg_stride + 4 * g1);
+    const uint64_t per_group =
+        store ? S * (nb0 * g1 * a.inner_bytes + 8 * g1) : S * (seg_stride + 4 * g1);
     const uint64_t fixed = 64;
     uint32_t per_sm = want < 1 ? 1 : want;
     while (per_sm > 1 && budget(per_sm) < fixed + per_group) per_sm--;
@@ -209,29 +213,30 @@ inline bool seg_plan_rows(const FbArgs& a, uint64_t g1, uint32_t sms, uint32_t w
     s.outer0 = g1 > 1 ? 2u : 1u;
     s.groups = (uint32_t)groups;
     s.row_bytes = (uint32_t)row_bytes;
-    s.seg_stride = (uint32_t)seg_stride;
+    s.seg_stride = store ? 0u : (uint32_t)seg_stride;
     s.nblk = (uint32_t)((groups + e - 1) / e);
     s.block_groups = (s.groups + s.nblk - 1) / s.nblk;
-    s.pad = 0;
+    s.img_stride = store ? (uint32_t)((uint64_t)s.block_groups * g1 * a.inner_bytes) : 0u;
     s.nrun = a.walk.nbox / nb0;
     const uint64_t items = s.nrun * s.nblk;
     const uint64_t ctas = (uint64_t)sms * per_sm;
     grid = (uint32_t)(items < ctas ? items : ctas);
-    smem = (size_t)S * s.block_groups * (s.seg_stride + 4 * g1) + 16;
+    smem = store ? (size_t)S * ((size_t)nb0 * s.img_stride + 8ull * s.block_groups * g1) + 16
+                 : (size_t)S * s.block_groups * (s.seg_stride + 4 * g1) + 16;
     return true;
 }
 
 template <class Budget>
 inline bool seg_plan(const FbArgs& a, const tm_desc* d, uint32_t sms, uint32_t want,
-                     uint32_t stages, int force, Budget budget, SegArgs& s, uint32_t& grid,
-                     size_t& smem)
+                     uint32_t stages, int force, bool store, Budget budget, SegArgs& s,
+                     uint32_t& grid, size_t& smem)
 {
     if (force == 0 || a.walk.mode != WALK_GRID || d->rank < 2 || !unit_steps(d)) return false;
     const bool fused = a.stride[1] == (int64_t)(a.dim[0] * a.esize);
     if (fused && a.ibox[1] > 1 &&
-        seg_plan_rows(a, a.ibox[1], sms, want, stages, force, budget, s, grid, smem))
+        seg_plan_rows(a, a.ibox[1], sms, want, stages, force, store, budget, s, grid, smem))
         return true;
-    return seg_plan_rows(a, 1, sms, want, stages, force, budget, s, grid, smem);
+    return seg_plan_rows(a, 1, sms, want, stages, force, store, budget, s, grid, smem);
 }
 
 // Ring consumer (stream_tiles).
@@ -281,6 +286,7 @@ cudaError_t launch_fb_copy(const FbArgs& a, uint32_t grid, size_t smem, cudaStre
 cudaError_t launch_fb_store(const FbArgs& a, uint32_t grid, size_t smem, cudaStream_t s);
 cudaError_t launch_fb_reduce(const FbArgs& a, uint32_t grid, cudaStream_t s);
 cudaError_t launch_fb_seg_copy(const SegArgs& a, uint32_t grid, size_t smem, cudaStream_t s);
+cudaError_t launch_fb_seg_store(const SegArgs& a, uint32_t grid, size_t smem, cudaStream_t s);
 cudaError_t launch_ring(const CUtensorMap* a, const CUtensorMap* b, const RingArgs& r,
                         uint32_t grid, size_t smem, cudaStream_t s);
 cudaError_t launch_selftest(uint64_t timeout_ns, StatusBlock* status, cudaStream_t s);

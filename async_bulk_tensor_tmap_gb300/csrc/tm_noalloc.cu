@@ -186,7 +186,7 @@ extern "C" int tiled_copy_noalloc(const tm_desc* src, const int32_t* coords, siz
         uint32_t grid = 0;
         size_t smem = 0;
         SegArgs sa;
-        if (seg_plan(a, src, (uint32_t)d->sms, 2u, 2u, 2,
+        if (seg_plan(a, src, (uint32_t)d->sms, 2u, 2u, 2, false,
                      [&](uint32_t per_sm) { return budget(*d, per_sm); }, sa, grid, smem)) {
             e = launch_fb_seg_copy(sa, grid, smem, st);
         } else {

@@ -336,7 +336,7 @@ int copy_boxes(const tm_desc* src, const int32_t* coords, size_t nbox, void* ima
         if (seg_plan(a, src, (uint32_t)ds->sms,
                      (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_CTAS_PER_SM", 2), 8),
                      (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_STAGES", 2), kSegMaxStages),
-                     (int)env_u64("TM_FB_SEG", 2),
+                     (int)env_u64("TM_FB_SEG", 2), false,
                      [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); }, sa, grid, smem)) {
             rc = check_launch(launch_fb_seg_copy(sa, grid, smem, st), "fallback segment copy launch");
         } else {
@@ -573,11 +573,22 @@ int tiled_roundtrip(const tm_desc* dst, const int32_t* coords, size_t nbox, cons
         FbArgs a = fb_args(dst, w, (uint64_t)images, *ds);
         uint32_t grid = 0;
         size_t smem = 0;
-        fb_shape(a, n, (uint32_t)ds->sms,
-                 (uint32_t)std::min<uint64_t>(env_u64("TM_FB_STORE_CTAS_PER_SM", 6), 16),
-                 kFbStoreRowBytes, [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); }, grid,
-                 smem);
-        rc = check_launch(launch_fb_store(a, grid, smem, st), "fallback store launch");
+        SegArgs sa;
+        // The segment form of the store (TM_FB_SEG as for the copy): image blocks staged by bulk
+        // copies, rows written by the consumer warps.
+        if (seg_plan(a, dst, (uint32_t)ds->sms,
+                     (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_CTAS_PER_SM", 2), 8),
+                     (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_STAGES", 2), kSegMaxStages),
+                     (int)env_u64("TM_FB_SEG", 2), true,
+                     [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); }, sa, grid, smem)) {
+            rc = check_launch(launch_fb_seg_store(sa, grid, smem, st), "fallback segment store launch");
+        } else {
+            fb_shape(a, n, (uint32_t)ds->sms,
+                     (uint32_t)std::min<uint64_t>(env_u64("TM_FB_STORE_CTAS_PER_SM", 6), 16),
+                     kFbStoreRowBytes, [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); },
+                     grid, smem);
+            rc = check_launch(launch_fb_store(a, grid, smem, st), "fallback store launch");
+        }
     }
     release_walk(w, st);
     return rc;
@@ -821,7 +832,7 @@ int tm_stream_check(void* stream)
         return cuda_fail(e, "clearing the status word");
     static const char* names[] = {"?", "tiled copy", "round trip", "reduce-add", "ring",
                                   "fallback copy", "fallback store", "fallback reduce", "self-test",
-                                  "gemm", "fallback segment copy"};
+                                  "gemm", "fallback segment copy", "fallback segment store"};
     const char* kn = sb.kernel < sizeof(names) / sizeof(names[0]) ? names[sb.kernel] : "?";
     return fail(sb.code, "%s kernel: wait gave up in block %u, stage %u, parity %u, box %llu", kn,
                 sb.block, sb.stage, sb.phase, (unsigned long long)sb.box);

@@ -217,10 +217,10 @@ def test_w4_ragged_and_fallback(tm, variant):
     assert torch.equal(dst, xd)
 
 
-# The vector copy's two forms on the same maps: per-window staging (TM_FB_SEG=0) and segments
-# (TM_FB_SEG=1: one bulk copy per contiguous run of rows, images leave by bulk stores).  Ragged
-# boxes along every dim, NaN fill, a base 2 bytes off alignment, rows of one and of several
-# segments.
+# The vector path's two forms on the same maps: per-window staging and per-thread image loads
+# (TM_FB_SEG=0) and segments (TM_FB_SEG=1: contiguous runs of tensor rows or image rows moved by
+# bulk copies, realigned by consumer warps).  Ragged boxes along every dim, NaN fill, a base 2
+# bytes off alignment, rows of one and of several segments; copy and store directions.
 SEG_CASES = {
     # the W4 rank-5 view (dims 0 and 1 contiguous: 2000-byte segments), ragged along dim 2
     "w4r5": (workloads.w4_rank5_map(**W4_SMALL, span=128), 0, False),
@@ -254,6 +254,15 @@ def test_vector_copy_forms(tm, monkeypatch, case, seg):
         assert_nan_fill(to_host(imgs), want, dt, tm)
     else:
         np.testing.assert_array_equal(to_host(imgs), want)
+    # store direction: the oracle's images back into a sentinel-filled tensor (only in-bounds
+    # elements are written; padding and everything outside the map keep the sentinel)
+    hin = torch.from_numpy(want.copy()).cuda()
+    dst = torch.full_like(xd, 0xA5)
+    tm.tiled_roundtrip(dev_map(tm, dst, r, offset=offset, dtype=dt), None, hin)
+    check(tm)
+    hdst = np.full(xd.numel(), 0xA5, np.uint8)
+    oracle.tiled_roundtrip(host_map(hdst, r, offset=offset, dtype=dt), want)
+    np.testing.assert_array_equal(to_host(dst), hdst)
 
 
 # ---- W5a (reduced): fp32 reduce-add, [Book-TMA] §"TMA reduce，把“搬运”和“归约”合并" ----------------
