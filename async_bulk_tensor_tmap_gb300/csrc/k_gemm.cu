@@ -449,7 +449,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < S; s++) {
-            mbar_init(smem_u32(&full_bar[s]), 2);   // the leader's expect_tx and the peer's arrival
+            mbar_init(smem_u32(&full_bar[s]), 1);   // the leader's expect_tx (both CTAs' bytes)
             mbar_init(smem_u32(&empty_bar[s]), 1);
         }
         for (uint32_t b = 0; b < 2; b++) {
@@ -486,9 +486,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                             break;
                         }
                     }
+                    // Only the leader arms the stage, for both CTAs' bytes; the peer's loads
+                    // complete on the leader's barrier.  They cannot land on an earlier phase:
+                    // the peer refills stage s only after the MMAs of the previous round, which
+                    // waited for that phase to complete, have released it.  (A peer arrival per
+                    // stage, a cluster-scope release, halved the rate.)
                     const uint32_t fb = leader_full + 8 * s;
                     if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), 2 * kPairStage);
-                    else mbar_arrive_cluster(fb);
                     tma_load_2d_pair(base + s * kPairStage, &ma, (int32_t)(kb * kBK),
                                      (int32_t)(mt * 256 + rank * 128), fb);
                     tma_load_2d_pair(base + s * kPairStage + kPairTileA, &mb, (int32_t)(kb * kBK),

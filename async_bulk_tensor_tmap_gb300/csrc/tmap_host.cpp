@@ -753,11 +753,12 @@ int stream_gemm(const tm_desc* a, const tm_desc* b, float* c, uint64_t ldc, uint
     DevState* ds = nullptr;
     int rc = device_state(&ds);
     if (rc) return rc;
-    // Forms: clusters of two one-SM CTAs along M sharing each B tile by TMA multicast (the default
-    // when C has more than one 128-row tile; TM_GEMM_MULTICAST=0 turns it off); one SM per
-    // 128 x 256 tile; TM_GEMM_PAIR=1 the CTA-pair form (256-row tiles over two SMs, tcgen05
-    // cta_group::2; measured slower).
-    const bool pair = env_u64("TM_GEMM_PAIR", 0) != 0 && M > 128 && ds->sms >= 2;
+    // Forms: the CTA-pair form (256-row tiles over the two SMs of a cluster, tcgen05 cta_group::2,
+    // 32 KiB stages, up to 6), the default when C has more than one 128-row tile (measured on
+    // GB300 at 8192 x 8192 x 4096: 1713 TFLOP/s with 6 stages); TM_GEMM_PAIR=0 gives clusters of
+    // two one-SM CTAs along M sharing each B tile by TMA multicast (1464 TFLOP/s; TM_GEMM_MULTICAST=0
+    // turns the sharing off); one SM per 128 x 256 tile otherwise.
+    const bool pair = env_u64("TM_GEMM_PAIR", 1) != 0 && M > 128 && ds->sms >= 2;
     const bool mcast = !pair && env_u64("TM_GEMM_MULTICAST", 1) != 0 && M > 128 && ds->sms >= 2;
     const uint32_t rows = pair ? 256u : 128u;
     const uint32_t S = std::min<uint32_t>(stages, pair ? kGemmMaxPairStages : kGemmMaxStages);

@@ -61,6 +61,7 @@ def parse():
                    help="divide every workload's row count by this (small cases for profiling, "
                         "below 1 for larger ones)")
     p.add_argument("--ring-stages", type=int, default=4, help="stages of the W5b ring")
+    p.add_argument("--gemm-stages", type=int, default=6, help="ring stages of the W7 GEMM")
     p.add_argument("--ring-swizzle", default="128", choices=["128", "none", "ungrouped"],
                    help="swizzle of the ring's tiles (none = the 8-way bank-conflict control; "
                         "ungrouped = 128B tiles read in the order of an ungrouped 256-byte row, "
@@ -200,12 +201,13 @@ def extra_ops(h: HostWorkload):
 # GPU arm
 # ------------------------------------------------------------------------------------------------
 class GpuWorkload:
-    def __init__(self, h: HostWorkload, stream, ring_stages: int = 4):
+    def __init__(self, h: HostWorkload, stream, ring_stages: int = 4, gemm_stages: int = 6):
         import torch
 
         import async_bulk_tensor_tmap_gb300 as tm
         self.tm, self.torch, self.stream = tm, torch, stream
         self.ring_stages = ring_stages
+        self.gemm_stages = gemm_stages
         dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).reshape(-1).view(np.uint8)).cuda()
         self.t = {k: dev(getattr(h, k)) for k in ("w3", "w4", "w5a_dst", "w5a_src", "w5b_a",
                                                   "w5b_b") if getattr(h, k) is not None}
@@ -285,7 +287,7 @@ class GpuWorkload:
             tm.stream_tiles(m["w5b_a"], m["w5b_b"], self.ring_stages, t["cs_a"], t["cs_b"],
                             t["bits_a"], t["bits_b"], s)
         elif kind == "gemm":
-            tm.stream_gemm(m["w7_a"], m["w7_b"], t["w7_c"], stream=s)
+            tm.stream_gemm(m["w7_a"], m["w7_b"], t["w7_c"], stages=self.gemm_stages, stream=s)
         elif kind in ("rows2", "cols2", "nan"):
             tm.tiled_copy(m[f"w6_{kind}"], None, t[f"w6_{kind}_img"], s)
         elif kind == "cols2_rt":
@@ -727,7 +729,7 @@ def main():
                      0 if args.ring_swizzle == "none" else 128)
     ops = select_ops(h, args.ops)
     stream = torch.cuda.Stream()
-    g = GpuWorkload(h, stream, args.ring_stages)
+    g = GpuWorkload(h, stream, args.ring_stages, args.gemm_stages)
 
     def barrier():
         torch.cuda.synchronize()

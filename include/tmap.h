@@ -230,15 +230,17 @@ int stream_tiles(const tm_desc* a, const tm_desc* b, uint32_t stages, float* cs_
  *   between the TMA producer and the MMA consumer).  C = A * B^T: A is M x K and B is N x K, bf16
  *   with K contiguous, given as rank-2 TM_BF16 maps {K, M} with box {64, 128} and {K, N} with box
  *   {64, 256}, 128-byte swizzle, TMA path, unit steps, zero fill (else TM_EUNSUPPORTED), equal K
- *   (else TM_EINVAL); M, N, K below 2^31.  Persistent CTAs (one per SM) compute 128 x 256 tiles of
- *   C from a `stages`-deep ring of 48 KiB stages (stages 2..6, at most 4 used): tcgen05.mma (bf16
- *   in, fp32 accumulated in two tensor-memory accumulators, so one tile's epilogue overlaps the
- *   next tile's MMAs), k in steps of 64.  When C has more than one 128-row tile, clusters of two
- *   CTAs along M share each B tile: each CTA loads one 128-row half of it, multicast into both
- *   CTAs' stages ([H200-TMA] §01: one copy lands in several CTAs' shared memory; one GPU only),
- *   and each CTA's MMA commits release the stage in both (TM_GEMM_MULTICAST=0 turns this off).
- *   TM_GEMM_PAIR=1 selects the CTA-pair form (tcgen05 cta_group::2, 256-row tiles over two SMs of a
- *   cluster, 32 KiB stages, up to 6; measured slower on GB300, so not the default).  c: device, fp32, row-major M x N with ldc >= N elements between
+ *   (else TM_EINVAL); M, N, K below 2^31.  Persistent CTAs (one per SM) run a `stages`-deep ring
+ *   (stages 2..6): tcgen05.mma (bf16 in, fp32 accumulated in two tensor-memory accumulators, so
+ *   one tile's epilogue overlaps the next tile's MMAs), k in steps of 64.  When C has more than one
+ *   128-row tile, clusters of two CTAs on two SMs compute 256 x 256 tiles with tcgen05
+ *   cta_group::2: each CTA loads its 128-row halves of the A and B tiles into 32 KiB stages (all 6
+ *   usable), the leader issues the MMAs over both; TM_GEMM_PAIR=0 gives instead one SM per
+ *   128 x 256 tile (48 KiB stages, at most 4 used) with clusters of two CTAs along M sharing each
+ *   B tile: each CTA loads one 128-row half of it, multicast into both CTAs' stages ([H200-TMA] §01:
+ *   one copy lands in several CTAs' shared memory; one GPU only), and each CTA's MMA commits
+ *   release the stage in both (TM_GEMM_MULTICAST=0 turns the sharing off).  A C of one 128-row
+ *   tile uses one-SM CTAs.  c: device, fp32, row-major M x N with ldc >= N elements between
  *   rows, 16-byte aligned, ldc a multiple of 4 (else TM_EALIGN).  Ragged M, N and K are zero-filled by the
  *   loads; only in-bounds elements of C are written.  Accuracy: the fp32 result differs from the
  *   exact sum of the K products by at most K * 2^-23 * sum |A[m][k] * B[n][k]| (any summation order,
