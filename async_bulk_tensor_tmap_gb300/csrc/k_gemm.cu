@@ -110,6 +110,9 @@ constexpr uint32_t kPairStage = kPairTileA + kPairTileB;  // 32 KiB per CTA
 // M = 256 (>> 4 in bits 24-28), N = 256, the rest as kIdesc
 constexpr uint32_t kPairIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((kBN >> 3) << 17) |
                                 ((256u >> 4) << 24);
+// the same with N = 128: a 256 x 128 half tile (each CTA holds 64 rows of B)
+constexpr uint32_t kPairIdescHalf = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) |
+                                    ((256u >> 4) << 24);
 
 __device__ __forceinline__ uint32_t cluster_rank()
 {
@@ -430,7 +433,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // and hands the accumulator back with arrivals on the leader's accumulator-empty barrier.
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm_pair(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
-                const __grid_constant__ GemmArgs g)
+                const __grid_constant__ CUtensorMap mbq, const __grid_constant__ GemmArgs g)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kGemmMaxPairStages];   // the leader's are used
@@ -445,7 +448,28 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t rank = cluster_rank();
     const uint32_t pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
     const uint32_t ntiles = g.mtiles * g.ntiles;  // 256 x 256 tiles; tile t = (t % mtiles, t / mtiles)
-    const uint32_t my_tiles = pair < ntiles ? (ntiles - 1 - pair) / npairs + 1 : 0;
+    // Tiles below split_from are done whole, round-robin over the pairs; the rest (a last wave that
+    // would leave pairs idle) as two 256 x 128 halves each, round-robin too.
+    const uint32_t split = g.split_from;
+    const uint32_t halves = 2 * (ntiles - split);
+    const uint32_t nfull = pair < split ? (split - 1 - pair) / npairs + 1 : 0;
+    const uint32_t nhalf = pair < halves ? (halves - 1 - pair) / npairs + 1 : 0;
+    const uint32_t my_tiles = nfull + nhalf;
+    // work item i of this pair: its tile (mt, nt) and half (0 or 1: columns half * 128 .. + 127 of
+    // the tile; 2: the whole tile)
+    auto item = [&](uint32_t i, uint32_t& mt, uint32_t& nt, uint32_t& half) {
+        uint32_t t;
+        if (i < nfull) {
+            t = pair + i * npairs;
+            half = 2;
+        } else {
+            const uint32_t hh = pair + (i - nfull) * npairs;
+            t = split + (hh >> 1);
+            half = hh & 1u;
+        }
+        mt = t % g.mtiles;
+        nt = t / g.mtiles;
+    };
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < S; s++) {
@@ -471,12 +495,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (elect_one()) {
             prefetch_tmap(&ma);
             prefetch_tmap(&mb);
+            prefetch_tmap(&mbq);
             uint32_t s = 0, wraps = 0;
             uint64_t issued = 0;
             bool failed = false;
             for (uint32_t i = 0; i < my_tiles && !failed; i++) {
-                const uint32_t t = pair + i * npairs;
-                const uint32_t mt = t % g.mtiles, nt = t / g.mtiles;
+                uint32_t mt, nt, half;
+                item(i, mt, nt, half);
+                const uint32_t t = i;  // reported with a timeout
+                const uint32_t bytes = half == 2 ? 2 * kPairStage : 2 * (kPairTileA + kPairTileB / 2);
                 for (uint32_t kb = 0; kb < g.kblocks; kb++) {
                     if (wraps > 0) {
                         const uint32_t parity = (wraps - 1) & 1u;
@@ -492,11 +519,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     // waited for that phase to complete, have released it.  (A peer arrival per
                     // stage, a cluster-scope release, halved the rate.)
                     const uint32_t fb = leader_full + 8 * s;
-                    if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), 2 * kPairStage);
+                    if (rank == 0) mbar_arrive_expect_tx(smem_u32(&full_bar[s]), bytes);
                     tma_load_2d_pair(base + s * kPairStage, &ma, (int32_t)(kb * kBK),
                                      (int32_t)(mt * 256 + rank * 128), fb);
-                    tma_load_2d_pair(base + s * kPairStage + kPairTileA, &mb, (int32_t)(kb * kBK),
-                                     (int32_t)(nt * 256 + rank * 128), fb);
+                    if (half == 2) {
+                        tma_load_2d_pair(base + s * kPairStage + kPairTileA, &mb, (int32_t)(kb * kBK),
+                                         (int32_t)(nt * 256 + rank * 128), fb);
+                    } else {  // this CTA's 64 of the half tile's 128 B rows
+                        tma_load_2d_pair(base + s * kPairStage + kPairTileA, &mbq, (int32_t)(kb * kBK),
+                                         (int32_t)(nt * 256 + half * 128 + rank * 64), fb);
+                    }
                     issued++;
                     if (++s == S) {
                         s = 0;
@@ -521,6 +553,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (uint32_t i = 0; i < my_tiles && !failed; i++) {
                 const uint32_t b = i & 1u;
                 const uint32_t d = tmem + b * kTmemCols;
+                uint32_t mt, nt, half;
+                item(i, mt, nt, half);
+                const uint32_t idesc = half == 2 ? kPairIdesc : kPairIdescHalf;
                 if (i >= 2) {  // both CTAs' epilogues have read out accumulator b's previous tile
                     const uint32_t parity = ((i >> 1) - 1) & 1u;
                     if (!mbar_wait(smem_u32(&acc_empty[b]), parity, g.timeout_ns)) {
@@ -540,7 +575,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 #pragma unroll
                     for (uint32_t ks = 0; ks < kBK / kUK; ks++) {
                         mma_bf16_pair(d, sw128_desc(a0 + ks * kUK * 2), sw128_desc(b0 + ks * kUK * 2),
-                                      kPairIdesc, (kb | ks) != 0 ? 1u : 0u);
+                                      idesc, (kb | ks) != 0 ? 1u : 0u);
                     }
                     tc_commit_pair(smem_u32(&empty_bar[s]));  // both CTAs' stage s is free once read
                     if (++s == S) {
@@ -557,8 +592,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t q = warp & 3u;
         for (uint32_t i = 0; i < my_tiles; i++) {
             const uint32_t b = i & 1u;
-            const uint32_t t = pair + i * npairs;
-            const uint32_t mt = t % g.mtiles, nt = t / g.mtiles;
+            uint32_t mt, nt, half;
+            item(i, mt, nt, half);
             const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&acc_full[b]), (i >> 1) & 1u,
                                                               g.timeout_ns));
             tc_fence_after();
@@ -568,8 +603,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             }
             const uint32_t row = mt * 256 + rank * 128 + q * 32 + lane;
             float* const crow = g.c + (uint64_t)row * g.ldc;
-            const uint32_t n0 = nt * kBN;
-            for (uint32_t c0 = 0; c0 < kBN; c0 += 32) {
+            const uint32_t n0 = nt * kBN + (half == 2 ? 0u : half * 128u);
+            const uint32_t ncols = half == 2 ? kBN : 128u;
+            for (uint32_t c0 = 0; c0 < ncols; c0 += 32) {
                 uint32_t r[32];
                 tmem_ld32(tmem + b * kTmemCols + ((q * 32) << 16) + c0, r);
                 if (row < g.m) {
@@ -607,9 +643,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 namespace {
-template <class Kernel>
-cudaError_t launch_cluster2(Kernel k, const CUtensorMap* a, const CUtensorMap* b, const GemmArgs& g,
-                            uint32_t grid, size_t smem, cudaStream_t s)
+template <class Kernel, class... Args>
+cudaError_t launch_cluster2(Kernel k, uint32_t grid, size_t smem, cudaStream_t s, Args... args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid, 1, 1);
@@ -623,7 +658,7 @@ cudaError_t launch_cluster2(Kernel k, const CUtensorMap* a, const CUtensorMap* b
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k, *a, *b, g);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k, args...);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
@@ -645,16 +680,16 @@ cudaError_t launch_gemm_multicast(const CUtensorMap* a, const CUtensorMap* b_hal
     cudaError_t e =
         cudaFuncSetAttribute(k_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_cluster2(k_gemm<true>, a, b_half, g, grid, smem, s);
+    return launch_cluster2(k_gemm<true>, grid, smem, s, *a, *b_half, g);
 }
 
-cudaError_t launch_gemm_pair(const CUtensorMap* a, const CUtensorMap* b, const GemmArgs& g,
-                             uint32_t grid, size_t smem, cudaStream_t s)
+cudaError_t launch_gemm_pair(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* b_quarter,
+                             const GemmArgs& g, uint32_t grid, size_t smem, cudaStream_t s)
 {
     cudaError_t e =
         cudaFuncSetAttribute(k_gemm_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_cluster2(k_gemm_pair, a, b, g, grid, smem, s);
+    return launch_cluster2(k_gemm_pair, grid, smem, s, *a, *b, *b_quarter, g);
 }
 
 }  // namespace tmk

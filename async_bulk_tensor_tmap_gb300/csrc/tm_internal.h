@@ -267,7 +267,7 @@ struct GemmArgs {
     uint32_t mtiles, ntiles; // 128-row and 256-column tiles of C
     uint32_t kblocks;        // 64-wide steps along k
     uint32_t stages;         // 2..kGemmMaxStages
-    uint32_t pad;
+    uint32_t split_from;     // pair form: tiles from here on are done as two 256 x 128 halves
     float* c;                // fp32, row-major
     uint64_t ldc;            // elements between rows of C
     uint64_t timeout_ns;
@@ -292,7 +292,8 @@ cudaError_t launch_ring(const CUtensorMap* a, const CUtensorMap* b, const RingAr
 cudaError_t launch_selftest(uint64_t timeout_ns, StatusBlock* status, cudaStream_t s);
 cudaError_t launch_gemm(const CUtensorMap* a, const CUtensorMap* b, const GemmArgs& g,
                         uint32_t grid, size_t smem, cudaStream_t s);
-cudaError_t launch_gemm_pair(const CUtensorMap* a, const CUtensorMap* b, const GemmArgs& g,
+cudaError_t launch_gemm_pair(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* b_quarter,
+                             const GemmArgs& g,
                              uint32_t grid, size_t smem, cudaStream_t s);
 cudaError_t launch_gemm_multicast(const CUtensorMap* a, const CUtensorMap* b_half,
                                   const GemmArgs& g, uint32_t grid, size_t smem, cudaStream_t s);

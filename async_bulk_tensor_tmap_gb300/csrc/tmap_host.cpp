@@ -771,6 +771,7 @@ int stream_gemm(const tm_desc* a, const tm_desc* b, float* c, uint64_t ldc, uint
     g.ntiles = (uint32_t)((N + 255) / 256);
     g.kblocks = (uint32_t)((K + 63) / 64);
     g.stages = S;
+    g.split_from = 0;
     g.c = c;
     g.ldc = ldc;
     g.timeout_ns = wait_limit_ns();
@@ -797,10 +798,25 @@ int stream_gemm(const tm_desc* a, const tm_desc* b, float* c, uint64_t ldc, uint
             return fail(TM_EUNSUPPORTED, "stream_gemm could not encode the half-tile map of B");
         const CUtensorMap* mbh = (const CUtensorMap*)bh.tmap;
         if (pair) {
-            // persistent: one cluster of two CTAs per pair of SMs
+            // persistent: one cluster of two CTAs per pair of SMs.  A last wave of r < pairs tiles
+            // would leave pairs idle; when 2r <= pairs its tiles are done as 256 x 128 halves (each
+            // CTA loading 64 B rows through a 64-row map of B), so that the wave takes half a tile
+            // (TM_GEMM_TAIL_SPLIT=0 keeps whole tiles).
             const uint64_t pairs = std::min<uint64_t>(tiles, (uint64_t)ds->sms / 2);
-            return check_launch(launch_gemm_pair(ma, mbh, g, (uint32_t)(2 * pairs), smem,
-                                                 (cudaStream_t)stream),
+            const uint64_t rem = tiles % pairs;
+            const bool split = env_u64("TM_GEMM_TAIL_SPLIT", 1) != 0 && tiles > pairs && rem > 0 &&
+                               2 * rem <= pairs;
+            g.split_from = (uint32_t)(split ? tiles - rem : tiles);
+            tm_desc bq;
+            const uint32_t qbox[2] = {64, 64};
+            if ((rc = plan_impl(&bq, TM_BF16, 2, (void*)(uintptr_t)b->base, dims, strides, qbox,
+                                nullptr, TM_SWIZZLE_128B, TM_OOB_ZERO)))
+                return rc;
+            if ((rc = encode_into(&bq))) return rc;
+            if (bq.path != TM_PATH_TMA || bq.box_bytes != 8192)
+                return fail(TM_EUNSUPPORTED, "stream_gemm could not encode the quarter-tile map of B");
+            return check_launch(launch_gemm_pair(ma, mbh, (const CUtensorMap*)bq.tmap, g,
+                                                 (uint32_t)(2 * pairs), smem, (cudaStream_t)stream),
                                 "gemm launch (CTA pairs)");
         }
         // persistent: one cluster of two CTAs (tiles 2m and 2m + 1 of one N tile) per pair of SMs

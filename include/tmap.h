@@ -235,7 +235,8 @@ int stream_tiles(const tm_desc* a, const tm_desc* b, uint32_t stages, float* cs_
  *   one tile's epilogue overlaps the next tile's MMAs), k in steps of 64.  When C has more than one
  *   128-row tile, clusters of two CTAs on two SMs compute 256 x 256 tiles with tcgen05
  *   cta_group::2: each CTA loads its 128-row halves of the A and B tiles into 32 KiB stages (all 6
- *   usable), the leader issues the MMAs over both; TM_GEMM_PAIR=0 gives instead one SM per
+ *   usable), the leader issues the MMAs over both; a last wave that would leave at least half the
+ *   pairs idle is done as 256 x 128 half tiles (TM_GEMM_TAIL_SPLIT=0 keeps whole tiles); TM_GEMM_PAIR=0 gives instead one SM per
  *   128 x 256 tile (48 KiB stages, at most 4 used) with clusters of two CTAs along M sharing each
  *   B tile: each CTA loads one 128-row half of it, multicast into both CTAs' stages ([H200-TMA] §01:
  *   one copy lands in several CTAs' shared memory; one GPU only), and each CTA's MMA commits

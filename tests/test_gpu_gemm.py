@@ -117,6 +117,23 @@ def test_gemm_padded_ldc_and_ragged_edges_leave_the_rest(tm):
     assert (np.abs(got[:, :N] - exact) <= K * 2.0 ** -23 * scale).all()
 
 
+def test_gemm_last_wave_in_half_tiles(tm):
+    """A C of 2 x 43 tiles of 256 x 256 (86 tiles over the 76 SM pairs of a 152-SM GB300): the pair
+    form does the last 10 tiles as 256 x 128 halves; ragged M, N and K.  Every column of the split
+    tiles (and their neighbours) for rows of both CTAs of both row tiles."""
+    M, N, K = 500, 11000, 200
+    a, b = bf16_normal(M, K, 11), bf16_normal(N, K, 12)
+    got = run(tm, a, b, stages=6)
+    rows = [0, 1, 127, 128, 255, 256, 300, 383, 384, 499]
+    cols = list(range(9600, N))
+    exact = oracle.gemm(a[rows], b[cols])
+    scale = oracle.gemm(a[rows] & 0x7FFF, b[cols] & 0x7FFF)
+    bound = K * 2.0 ** -23 * scale
+    err = np.abs(got[rows][:, cols].astype(np.float64) - exact)
+    assert (err <= bound).all(), float((err / np.maximum(bound, 1e-300)).max())
+    assert np.isfinite(got).all()
+
+
 def test_gemm_full_size_sampled(tm):
     """The benchmark's shape (M = N = 8192, K = 4096) in its launch configuration; sampled
     elements against the oracle, one by one (rows and columns of every tile position class)."""
