@@ -94,6 +94,43 @@ __device__ __forceinline__ void item_of(const SegArgs& s, uint64_t m, uint64_t& 
     for (int i = 0; i < 5; i++) c[i] = i < (int)s.f.walk.rank ? (int32_t)(k[i] * s.f.walk.box[i]) : 0;
 }
 
+// The producer's walk over its CTA's items: run u, row block q and the grid counters k of the
+// run's first box (k[0] = 0), stepped with carries (divisions only to start).
+struct ItemCursor {
+    uint64_t u;
+    uint32_t q;
+    uint32_t k[5];
+
+    __device__ __forceinline__ void init(const SegArgs& s, uint64_t m)
+    {
+        int32_t c[5];
+        item_of(s, m, u, q, c);
+        for (int i = 0; i < 5; i++) k[i] = i < (int)s.f.walk.rank ? (uint32_t)c[i] / s.f.walk.box[i] : 0;
+    }
+    // start coordinates of the run's first box
+    __device__ __forceinline__ void start(const SegArgs& s, int32_t* c) const
+    {
+#pragma unroll
+        for (int i = 0; i < 5; i++) c[i] = (int32_t)(k[i] * s.f.walk.box[i]);
+    }
+    // the next row block, else the next run (odometer over dims 1..)
+    __device__ __forceinline__ void next(const SegArgs& s)
+    {
+        if (++q < s.nblk) return;
+        q = 0;
+        u++;
+        uint32_t carry = 1;
+#pragma unroll
+        for (int i = 1; i < 5; i++) {
+            if (i < (int)s.f.walk.rank && carry) {
+                k[i]++;
+                carry = k[i] == s.f.walk.grid_nb[i] ? 1u : 0u;
+                if (carry) k[i] = 0;
+            }
+        }
+    }
+};
+
 // The 16 shared-memory bytes at p, whose address is p_al (p = p_al + d, d = p & 15), read with
 // the widest loads the offset allows; two aligned 16-byte loads and a funnel shift when d is not
 // a multiple of 4.
@@ -143,8 +180,6 @@ __device__ __forceinline__ uint4 keep_head(uint4 v, const uint4& fill, int n)
     return v;
 }
 
-}  // namespace
-
 // 16 bytes of the fill element (zero, or the NaN pattern of a TM_OOB_NAN map).
 __device__ __forceinline__ uint4 seg_fill(const FbArgs& a)
 {
@@ -160,6 +195,48 @@ __device__ __forceinline__ uint4 seg_fill(const FbArgs& a)
     }
     return make_uint4(lo, hi, lo, hi);
 }
+
+// Word t (0..3) of v, selected without indexing memory.
+__device__ __forceinline__ uint32_t word_of(const uint4& v, uint32_t t)
+{
+    return t == 0 ? v.x : t == 1 ? v.y : t == 2 ? v.z : v.w;
+}
+
+// Writes the first n bytes (0 < n <= 16) of v to global address p with the widest stores the
+// address and the byte count allow (nothing past p + n is touched).
+__device__ __forceinline__ void put_head(uint8_t* p, const uint4& v, int n)
+{
+    const uintptr_t at = reinterpret_cast<uintptr_t>(p);
+    if (n == 16 && (at & 15) == 0) {
+        *reinterpret_cast<uint4*>(p) = v;
+        return;
+    }
+    if (n == 16 && (at & 7) == 0) {
+        *reinterpret_cast<uint2*>(p) = make_uint2(v.x, v.y);
+        *reinterpret_cast<uint2*>(p + 8) = make_uint2(v.z, v.w);
+        return;
+    }
+    int pos = 0;
+    while (pos < n) {
+        const uintptr_t q = at + (uintptr_t)pos;
+        const uint32_t t = (uint32_t)pos >> 2;
+        if ((q & 7) == 0 && (pos & 7) == 0 && pos + 8 <= n) {
+            *reinterpret_cast<uint2*>(p + pos) = make_uint2(word_of(v, t), word_of(v, t + 1));
+            pos += 8;
+        } else if ((q & 3) == 0 && (pos & 3) == 0 && pos + 4 <= n) {
+            *reinterpret_cast<uint32_t*>(p + pos) = word_of(v, t);
+            pos += 4;
+        } else if ((q & 1) == 0 && (pos & 1) == 0 && pos + 2 <= n) {
+            *reinterpret_cast<uint16_t*>(p + pos) = (uint16_t)(word_of(v, t) >> (8 * (pos & 3)));
+            pos += 2;
+        } else {
+            p[pos] = (uint8_t)(word_of(v, t) >> (8 * (pos & 3)));
+            pos += 1;
+        }
+    }
+}
+
+}  // namespace
 
 // What the producer leaves beside each staging buffer for the item it staged.
 struct SegItem {
@@ -199,18 +276,10 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_copy(const __grid_con
     __syncthreads();
 
     if (warp == 0) {
-        // ---- producer: walks the CTA's items with a cursor (run u, row block q, counters k of
-        // the run's first box; every lane keeps the same copy) stepped with carries.  Item i
-        // goes to buffer i % S once the consumers have released that buffer's item i - S.
-        uint64_t cu;
-        uint32_t cq;
-        uint32_t ck[5];
-        {
-            int32_t c[5];
-            item_of(s, m0, cu, cq, c);
-            for (int i = 0; i < 5; i++)
-                ck[i] = i < (int)a.walk.rank ? (uint32_t)c[i] / a.walk.box[i] : 0;
-        }
+        // ---- producer: walks the CTA's items with a cursor (every lane keeps the same copy).
+        // Item i goes to buffer i % S once the consumers have released that buffer's item i - S.
+        ItemCursor cur;
+        cur.init(s, m0);
         // item i: buffer b = i % S, lap = i / S; for i >= S it waits for the release of item
         // i - S, the buffer's completion number lap - 1
         uint32_t b = 0, lap = 0;
@@ -225,9 +294,8 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_copy(const __grid_con
                 }
             }
             int32_t c[5];
-#pragma unroll
-            for (int d = 0; d < 5; d++) c[d] = (int32_t)(ck[d] * a.walk.box[d]);
-            const uint32_t g0 = cq * E;
+            cur.start(s, c);
+            const uint32_t g0 = cur.q * E;
             const uint32_t ng = min(E, s.groups - g0);
             int32_t* const tab = tabs + (size_t)b * E * G1;
             const uint32_t sbase = b * E * s.seg_stride;
@@ -244,7 +312,7 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_copy(const __grid_con
             bytes = __reduce_add_sync(0xffffffffu, bytes);
             const uint32_t bar = smem_u32(&full_bar[b]);
             if (lane == 0) {
-                info[b].run = cu;
+                info[b].run = cur.u;
                 info[b].r0 = g0 * G1;
                 info[b].nr = ng * G1;
             }
@@ -259,20 +327,7 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_copy(const __grid_con
                     bulk_load(dst0 + j * s.seg_stride, sg.src & ~15ull, n, bar);
                 }
             }
-            // step the cursor: the next row block, else the next run (odometer over dims 1..)
-            if (++cq == s.nblk) {
-                cq = 0;
-                cu++;
-                uint32_t carry = 1;
-#pragma unroll
-                for (int d = 1; d < 5; d++) {
-                    if (d < (int)a.walk.rank && carry) {
-                        ck[d]++;
-                        carry = ck[d] == a.walk.grid_nb[d] ? 1u : 0u;
-                        if (carry) ck[d] = 0;
-                    }
-                }
-            }
+            cur.next(s);
             if (++b == S) {
                 b = 0;
                 lap++;
@@ -336,46 +391,6 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_copy(const __grid_con
     }
 }
 
-// Word t (0..3) of v, selected without indexing memory.
-__device__ __forceinline__ uint32_t word_of(const uint4& v, uint32_t t)
-{
-    return t == 0 ? v.x : t == 1 ? v.y : t == 2 ? v.z : v.w;
-}
-
-// Writes the first n bytes (0 < n <= 16) of v to global address p with the widest stores the
-// address and the byte count allow (nothing past p + n is touched).
-__device__ __forceinline__ void put_head(uint8_t* p, const uint4& v, int n)
-{
-    const uintptr_t at = reinterpret_cast<uintptr_t>(p);
-    if (n == 16 && (at & 15) == 0) {
-        *reinterpret_cast<uint4*>(p) = v;
-        return;
-    }
-    if (n == 16 && (at & 7) == 0) {
-        *reinterpret_cast<uint2*>(p) = make_uint2(v.x, v.y);
-        *reinterpret_cast<uint2*>(p + 8) = make_uint2(v.z, v.w);
-        return;
-    }
-    int pos = 0;
-    while (pos < n) {
-        const uintptr_t q = at + (uintptr_t)pos;
-        const uint32_t t = (uint32_t)pos >> 2;
-        if ((q & 7) == 0 && (pos & 7) == 0 && pos + 8 <= n) {
-            *reinterpret_cast<uint2*>(p + pos) = make_uint2(word_of(v, t), word_of(v, t + 1));
-            pos += 8;
-        } else if ((q & 3) == 0 && (pos & 3) == 0 && pos + 4 <= n) {
-            *reinterpret_cast<uint32_t*>(p + pos) = word_of(v, t);
-            pos += 4;
-        } else if ((q & 1) == 0 && (pos & 1) == 0 && pos + 2 <= n) {
-            *reinterpret_cast<uint16_t*>(p + pos) = (uint16_t)(word_of(v, t) >> (8 * (pos & 3)));
-            pos += 2;
-        } else {
-            p[pos] = (uint8_t)(word_of(v, t) >> (8 * (pos & 3)));
-            pos += 1;
-        }
-    }
-}
-
 // Store direction (tiled_roundtrip): the inverse walk.  The producer warp bulk-loads, per item,
 // the block of image rows of each box of the run (contiguous in the images) into a staging buffer
 // and writes each row's tensor address beside it; the consumer warps read each 16-byte chunk at
@@ -417,15 +432,8 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_store(const __grid_co
 
     if (warp == 0) {
         // ---- producer (the same item cursor as the copy)
-        uint64_t cu;
-        uint32_t cq;
-        uint32_t ck[5];
-        {
-            int32_t c[5];
-            item_of(s, m0, cu, cq, c);
-            for (int i = 0; i < 5; i++)
-                ck[i] = i < (int)a.walk.rank ? (uint32_t)c[i] / a.walk.box[i] : 0;
-        }
+        ItemCursor cur;
+        cur.init(s, m0);
         uint32_t b = 0, lap = 0;
         uint64_t i = 0;
         for (; i < total; i++) {
@@ -438,9 +446,8 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_store(const __grid_co
                 }
             }
             int32_t c[5];
-#pragma unroll
-            for (int d = 0; d < 5; d++) c[d] = (int32_t)(ck[d] * a.walk.box[d]);
-            const uint32_t g0 = cq * E;
+            cur.start(s, c);
+            const uint32_t g0 = cur.q * E;
             const uint32_t ng = min(E, s.groups - g0);
             const uint32_t nr = ng * G1;
             uint64_t* const tab = tabs + (size_t)b * E * G1;
@@ -451,7 +458,7 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_store(const __grid_co
             }
             const uint32_t bar = smem_u32(&full_bar[b]);
             if (lane == 0) {
-                info[b].run = cu;
+                info[b].run = cur.u;
                 info[b].r0 = g0 * G1;
                 info[b].nr = nr;
             }
@@ -460,23 +467,11 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_store(const __grid_co
             __syncwarp();
             const uint32_t dst0 = smem_u32(sbuf0 + b * stage_bytes);
             for (uint32_t k = lane; k < s.run; k += 32) {
-                const uint64_t box = cu * s.run + k;
+                const uint64_t box = cur.u * s.run + k;
                 bulk_load(dst0 + k * s.img_stride, a.images + box * a.box_bytes + (uint64_t)g0 * G1 * inner,
                           nr * inner, bar);
             }
-            if (++cq == s.nblk) {
-                cq = 0;
-                cu++;
-                uint32_t carry = 1;
-#pragma unroll
-                for (int d = 1; d < 5; d++) {
-                    if (d < (int)a.walk.rank && carry) {
-                        ck[d]++;
-                        carry = ck[d] == a.walk.grid_nb[d] ? 1u : 0u;
-                        if (carry) ck[d] = 0;
-                    }
-                }
-            }
+            cur.next(s);
             if (++b == S) {
                 b = 0;
                 lap++;
