@@ -276,7 +276,7 @@ def stream_tiles(a: TensorMap, b: TensorMap, stages, cs_a, cs_b, bits_a, bits_b,
                            _addr(bits_b), _stream(stream)), "stream_tiles")
 
 
-def stream_gemm(a: TensorMap, b: TensorMap, c, ldc=None, stages: int = 6, stream=None) -> None:
+def stream_gemm(a: TensorMap, b: TensorMap, c, ldc=None, stages: int = 7, stream=None) -> None:
     """C = A * B^T on the tensor cores: A map {K, M} box {64, 128}, B map {K, N} box {64, 256},
     c an fp32 device buffer of M rows, ldc elements apart (default N)."""
     ldc = b.dims[1] if ldc is None else ldc

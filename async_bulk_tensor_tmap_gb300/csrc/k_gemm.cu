@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 // The CTA-pair form: a cluster of two CTAs (ranks 0 and 1, two SMs) computes 256 x 256 tiles of C.
 // Per k step each CTA loads its 128-row half of the A tile and its 128-row half of the B tile into
-// its own 32 KiB stage (so 6 stages fit), both CTAs' loads completing on the leader's (rank 0) full
+// its own 32 KiB stage (so 7 stages fit), both CTAs' loads completing on the leader's (rank 0) full
 // barrier.  The leader's elected lane issues tcgen05.mma.cta_group::2 (M = 256: A rows 0-127 from
 // the leader's shared memory, 128-255 from the peer's at the same offset, B split the same way;
 // each CTA's 128 rows of the accumulator land in its own tensor memory), and its commits arrive

@@ -261,7 +261,7 @@ struct RingArgs {
 
 // Tensor-core consumer of the k-ordered ring (stream_gemm): C = A * B^T.
 constexpr uint32_t kGemmMaxStages = 4;      // one-SM form: 48 KiB stages
-constexpr uint32_t kGemmMaxPairStages = 6;  // CTA-pair form: 32 KiB stages per CTA
+constexpr uint32_t kGemmMaxPairStages = 7;  // CTA-pair form: 32 KiB stages per CTA
 struct GemmArgs {
     uint32_t m, n, k;        // C is m x n; A is m x k, B is n x k (bf16, k contiguous)
     uint32_t mtiles, ntiles; // 128-row and 256-column tiles of C

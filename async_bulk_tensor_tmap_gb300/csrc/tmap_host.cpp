@@ -754,8 +754,8 @@ int stream_gemm(const tm_desc* a, const tm_desc* b, float* c, uint64_t ldc, uint
     int rc = device_state(&ds);
     if (rc) return rc;
     // Forms: the CTA-pair form (256-row tiles over the two SMs of a cluster, tcgen05 cta_group::2,
-    // 32 KiB stages, up to 6), the default when C has more than one 128-row tile (measured on
-    // GB300 at 8192 x 8192 x 4096: 1713 TFLOP/s with 6 stages); TM_GEMM_PAIR=0 gives clusters of
+    // 32 KiB stages, up to 7), the default when C has more than one 128-row tile (measured on
+    // GB300 at 8192 x 8192 x 4096: 1738-1821 TFLOP/s with 7 stages); TM_GEMM_PAIR=0 gives clusters of
     // two one-SM CTAs along M sharing each B tile by TMA multicast (1464 TFLOP/s; TM_GEMM_MULTICAST=0
     // turns the sharing off); one SM per 128 x 256 tile otherwise.
     const bool pair = env_u64("TM_GEMM_PAIR", 1) != 0 && M > 128 && ds->sms >= 2;

@@ -61,7 +61,7 @@ def parse():
                    help="divide every workload's row count by this (small cases for profiling, "
                         "below 1 for larger ones)")
     p.add_argument("--ring-stages", type=int, default=4, help="stages of the W5b ring")
-    p.add_argument("--gemm-stages", type=int, default=6, help="ring stages of the W7 GEMM")
+    p.add_argument("--gemm-stages", type=int, default=7, help="ring stages of the W7 GEMM")
     p.add_argument("--ring-swizzle", default="128", choices=["128", "none", "ungrouped"],
                    help="swizzle of the ring's tiles (none = the 8-way bank-conflict control; "
                         "ungrouped = 128B tiles read in the order of an ungrouped 256-byte row, "
@@ -201,7 +201,7 @@ def extra_ops(h: HostWorkload):
 # GPU arm
 # ------------------------------------------------------------------------------------------------
 class GpuWorkload:
-    def __init__(self, h: HostWorkload, stream, ring_stages: int = 4, gemm_stages: int = 6):
+    def __init__(self, h: HostWorkload, stream, ring_stages: int = 4, gemm_stages: int = 7):
         import torch
 
         import async_bulk_tensor_tmap_gb300 as tm

@@ -231,10 +231,10 @@ int stream_tiles(const tm_desc* a, const tm_desc* b, uint32_t stages, float* cs_
  *   with K contiguous, given as rank-2 TM_BF16 maps {K, M} with box {64, 128} and {K, N} with box
  *   {64, 256}, 128-byte swizzle, TMA path, unit steps, zero fill (else TM_EUNSUPPORTED), equal K
  *   (else TM_EINVAL); M, N, K below 2^31.  Persistent CTAs (one per SM) run a `stages`-deep ring
- *   (stages 2..6): tcgen05.mma (bf16 in, fp32 accumulated in two tensor-memory accumulators, so
+ *   (stages 2..7, else TM_ERANGE): tcgen05.mma (bf16 in, fp32 accumulated in two tensor-memory accumulators, so
  *   one tile's epilogue overlaps the next tile's MMAs), k in steps of 64.  When C has more than one
  *   128-row tile, clusters of two CTAs on two SMs compute 256 x 256 tiles with tcgen05
- *   cta_group::2: each CTA loads its 128-row halves of the A and B tiles into 32 KiB stages (all 6
+ *   cta_group::2: each CTA loads its 128-row halves of the A and B tiles into 32 KiB stages (all 7
  *   usable), the leader issues the MMAs over both; a last wave that would leave at least half the
  *   pairs idle is done as 256 x 128 half tiles (TM_GEMM_TAIL_SPLIT=0 keeps whole tiles); TM_GEMM_PAIR=0 gives instead one SM per
  *   128 x 256 tile (48 KiB stages, at most 4 used) with clusters of two CTAs along M sharing each

@@ -202,7 +202,7 @@ def test_stream_gemm_validation(tm):
 
     assert code(b, a, c) == tm.TM_EUNSUPPORTED                    # boxes swapped
     assert code(a, b, c, stages=1) == tm.TM_ERANGE
-    assert code(a, b, c, stages=7) == tm.TM_ERANGE
+    assert code(a, b, c, stages=8) == tm.TM_ERANGE
     assert code(a, b, c, ldc=700) == tm.TM_EINVAL                 # ldc < N
     assert code(a, b, c + 8) == tm.TM_EALIGN
     assert code(a, b, c, ldc=770) == tm.TM_EALIGN

@@ -87,7 +87,7 @@ def test_gemm_matches_oracle(tm, M, N, K):
     assert np.isfinite(got).all()
 
 
-@pytest.mark.parametrize("stages", [2, 3, 4, 6])
+@pytest.mark.parametrize("stages", [2, 3, 4, 6, 7])
 def test_gemm_every_ring_depth(tm, stages):
     a, b = bf16_normal(256, 448, 3), bf16_normal(512, 448, 4)
     got = run(tm, a, b, stages=stages)
@@ -123,7 +123,7 @@ def test_gemm_last_wave_in_half_tiles(tm):
     tiles (and their neighbours) for rows of both CTAs of both row tiles."""
     M, N, K = 500, 11000, 200
     a, b = bf16_normal(M, K, 11), bf16_normal(N, K, 12)
-    got = run(tm, a, b, stages=6)
+    got = run(tm, a, b, stages=7)
     rows = [0, 1, 127, 128, 255, 256, 300, 383, 384, 499]
     cols = list(range(9600, N))
     exact = oracle.gemm(a[rows], b[cols])
@@ -139,7 +139,7 @@ def test_gemm_full_size_sampled(tm):
     elements against the oracle, one by one (rows and columns of every tile position class)."""
     import workloads
     a, b = workloads.w7_operands()
-    got = run(tm, a, b, stages=6)  # the bench's ring depth
+    got = run(tm, a, b, stages=7)  # the bench's ring depth
     rng = np.random.default_rng(7)
     rows = sorted(set(rng.integers(0, 8192, 6).tolist()) | {0, 127, 128, 255, 256, 8191})
     cols = sorted(set(rng.integers(0, 8192, 6).tolist()) | {0, 255, 256, 8191})
