@@ -57,6 +57,10 @@ CASES = {
     "bf16_rows3_64B": (2, [64, 33], 128, [32, 16], [1, 3], 64),
     "bf16_rows2_unaligned_pitch": (2, [120, 40], 250, [64, 8], [1, 2], 0),
     "f32_cols3_unaligned_pitch": (4, [50, 12], 212, [24, 4], [3, 2], 0),
+    # every other element of 4-byte rows on a 16-byte pitch (the step-2 fast path; ragged last box)
+    "f32_cols2": (4, [130, 20], 528, [32, 8], [2, 1], 0),
+    # every other element of 2-byte rows whose starts are off 16 bytes (the general gather)
+    "bf16_cols2_unaligned_pitch": (2, [200, 30], 418, [64, 8], [2, 1], 0),
 }
 
 
