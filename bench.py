@@ -393,14 +393,23 @@ E2E_GROUPS = (
 )
 
 
+# maps over each device buffer of the step (all start at the buffer's base)
+E2E_MAPS = {
+    "w3": ("w3",), "w3_out": ("w3_out",),
+    "w4": ("w4r3", "w4r3n", "w4r5"), "w4_out": ("w4r3_out", "w4r3n_out", "w4r5_out"),
+    "w5a_dst": ("w5a_dst",), "w5a_src": ("w5a_src",),
+    "w5b_a": ("w5b_a",), "w5b_b": ("w5b_b",),
+}
+
+
 def e2e_run(g: GpuWorkload, h: HostWorkload, ops, steps):
     """Same step through the public API with HOST buffers: every step copies its inputs from
     pinned host memory and its results back, inside the timed region.  Three streams pipeline the
     work group by group (inputs of group k+1 go in while group k computes and group k-1's results
-    come out); events keep each tensor's copies and kernels in order across steps.  An input that
-    is also a result (the reduce destination) has two device buffers used by alternate steps, its
-    maps moved between them with tmap_replace_address, so that one step's upload does not wait for
-    the previous step's read-out."""
+    come out).  Every input and result has two device buffers used by alternate steps (the maps
+    over them moved with tmap_replace_address), so that a step's uploads wait only for the kernels
+    (or read-out) of the step before last, and its kernels only for that step's read-out: the
+    host link is the only thing that orders consecutive steps."""
     torch = g.torch
     names = [n for n, _ in ops]
     groups = [(gn, ins, outs, [n for n in names if n.split(".")[0].startswith(gn)])
@@ -419,36 +428,34 @@ def e2e_run(g: GpuWorkload, h: HostWorkload, ops, steps):
     bi = sum(v.numel() * v.element_size() for v in pin_in.values())
     bo = sum(v.numel() * v.element_size() for v in pin_out.values())
     s_in, s_out, s_run = torch.cuda.Stream(), torch.cuda.Stream(), g.stream
-    dual = {k for _, ins, outs, _ in groups for k in ins if k in outs}
-    bufs = {k: [g.t[k], torch.empty_like(g.t[k])] for k in dual}
-    buf_out = {k: [None, None] for k in dual}       # read-out event of each buffer's last step
-    last_done = {gn: None for gn, *_ in groups}    # the group's kernels of the previous step
-    last_out = {gn: None for gn, *_ in groups}     # the group's read-out of the previous step
+    keys = {k for _, ins, outs, _ in groups for k in ins + outs}
+    # the second buffer of a result starts as a copy of the first, so that bytes a round trip
+    # does not write (padding) match on both
+    bufs = {k: [g.t[k], g.t[k].clone()] for k in keys}
+    free = {k: [None, None] for k in keys}  # the event after which buffer [par] may be rewritten
     nstep = [0]
+
+    def use(k, par):
+        g.t[k] = bufs[k][par]
+        for mk in E2E_MAPS.get(k, ()):
+            g.tm.tmap_replace_address(g.maps[mk], g.t[k])
 
     def step():
         par = nstep[0] & 1
         for gn, ins, outs, gops in groups:
             ev_in = torch.cuda.Event()
             with torch.cuda.stream(s_in):
-                for k in ins:  # double-buffered inputs first: they only wait for their buffer
-                    if k in dual:
-                        if buf_out[k][par] is not None:
-                            s_in.wait_event(buf_out[k][par])  # this buffer's last result is out
-                        bufs[k][par].copy_(pin_in[k], non_blocking=True)
-                if last_done[gn] is not None and any(k not in dual for k in ins):
-                    s_in.wait_event(last_done[gn])  # last step's kernels have read the inputs
                 for k in ins:
-                    if k not in dual:
-                        g.t[k].copy_(pin_in[k], non_blocking=True)
+                    if free[k][par] is not None:
+                        s_in.wait_event(free[k][par])  # the step before last is done with it
+                    bufs[k][par].copy_(pin_in[k], non_blocking=True)
                 ev_in.record(s_in)
-            for k in ins:
-                if k in dual:
-                    g.t[k] = bufs[k][par]
-                    g.tm.tmap_replace_address(g.maps[k], g.t[k])
+            for k in set(ins) | set(outs):
+                use(k, par)
             s_run.wait_event(ev_in)
-            if last_out[gn] is not None and any(k not in dual for k in outs):
-                s_run.wait_event(last_out[gn])  # last step's results were read out
+            for k in outs:
+                if k not in ins and free[k][par] is not None:
+                    s_run.wait_event(free[k][par])  # its result of the step before last is out
             for name in gops:
                 g.run_op(name, s_run)
             ev_done = torch.cuda.Event()
@@ -459,11 +466,10 @@ def e2e_run(g: GpuWorkload, h: HostWorkload, ops, steps):
                 for k in outs:
                     pin_out[k].copy_(g.t[k], non_blocking=True)
                 ev_out.record(s_out)
-            last_done[gn] = ev_done
-            last_out[gn] = ev_out
+            for k in ins:
+                free[k][par] = ev_out if k in outs else ev_done
             for k in outs:
-                if k in dual:
-                    buf_out[k][par] = ev_out
+                free[k][par] = ev_out
         nstep[0] += 1
 
     step()
