@@ -343,7 +343,12 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_copy(const __grid_con
     }
 
     // ---- consumers: realign item n's chunks, stored straight to the global images (a warp's 32
-    // chunks are four whole 128-byte image rows, permuted inside each row by the swizzle)
+    // chunks cover whole 128-byte image rows, permuted inside each by the swizzle).  Box-major
+    // when each box's block has at least one chunk per consumer thread (its images are then
+    // written in order; measured on GB300 4 % faster than the row-major walk on the W4 rank-5
+    // view), else row-major: the chunks of one image row of every box of the run are the 16-byte
+    // chunks of one tensor row, so the item is nr rows x (run x cpr) chunks and no thread idles
+    // on a run of many boxes with few rows; each thread steps its (row, chunk) with carries.
     const uint32_t inner = a.inner_bytes;
     const uint32_t cpr = inner >> 4;  // 16-byte chunks per image row
     const uint32_t cpr_shift = (cpr & (cpr - 1)) == 0 ? (uint32_t)(__ffs(cpr) - 1) : 32u;
@@ -351,6 +356,9 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_copy(const __grid_con
     const uint32_t row_bytes = s.row_bytes;
     const uint32_t ct = threadIdx.x - 32;  // consumer thread index
     constexpr uint32_t kCT = 32 * kSegConsumerWarps;
+    const uint32_t rc = s.run * cpr;  // chunks per tensor row of the run
+    const uint32_t r_start = ct / rc, c_start = ct - r_start * rc;
+    const uint32_t r_step = kCT / rc, c_step = kCT - r_step * rc;
     uint32_t sb = 0, sparity = 0;  // staging buffer of item n (n % S) and its phase parity
     for (uint64_t n = 0; n < total; n++) {
         if (n) {
@@ -367,15 +375,32 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_copy(const __grid_con
         const int32_t* const tab = tabs + (size_t)sb * E * G1;
         const uint32_t r0 = info[sb].r0;
         const uint32_t nr = info[sb].nr;
-        const uint64_t box0 = info[sb].run * s.run;
+        uint8_t* const img0 = reinterpret_cast<uint8_t*>(a.images + info[sb].run * s.run * a.box_bytes);
         const uint32_t per_box = nr * cpr;
-        for (uint32_t k = 0; k < s.run; k++) {
-            uint8_t* const img = reinterpret_cast<uint8_t*>(a.images + (box0 + k) * a.box_bytes);
-            for (uint32_t rc = ct; rc < per_box; rc += kCT) {
-                const uint32_t r = cpr_shift < 32 ? rc >> cpr_shift : rc / cpr;
-                const uint32_t j = rc - r * cpr;
+        if (per_box >= kCT) {
+            for (uint32_t k = 0; k < s.run; k++) {
+                uint8_t* const img = img0 + (size_t)k * a.box_bytes;
+                for (uint32_t q = ct; q < per_box; q += kCT) {
+                    const uint32_t r = cpr_shift < 32 ? q >> cpr_shift : q / cpr;
+                    const uint32_t j = q - r * cpr;
+                    const int32_t at = tab[r];
+                    const int x = (int)(k * inner + 16 * j);  // the chunk's first tensor-row byte
+                    const int left = (int)row_bytes - x;
+                    uint4 v = fillv;
+                    if (at >= 0 && left > 0) {
+                        const uint32_t p = (uint32_t)at + (uint32_t)x;
+                        v = load16(smem_raw + p, p & 15u);
+                        if (left < 16) v = keep_head(v, fillv, left);
+                    }
+                    *reinterpret_cast<uint4*>(img + swizzle_offset((r0 + r) * inner + 16 * j, a.span)) = v;
+                }
+            }
+        } else {
+            for (uint32_t r = r_start, c = c_start; r < nr;) {
+                const uint32_t k = cpr_shift < 32 ? c >> cpr_shift : c / cpr;  // box of the run
+                const uint32_t j = c - k * cpr;                                  // chunk of its row
                 const int32_t at = tab[r];
-                const int x = (int)(k * inner + 16 * j);  // the chunk's first byte in the tensor row
+                const int x = (int)(16 * c);  // the chunk's first byte in the tensor row
                 const int left = (int)row_bytes - x;
                 uint4 v = fillv;
                 if (at >= 0 && left > 0) {
@@ -383,7 +408,14 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_copy(const __grid_con
                     v = load16(smem_raw + p, p & 15u);
                     if (left < 16) v = keep_head(v, fillv, left);
                 }
-                *reinterpret_cast<uint4*>(img + swizzle_offset((r0 + r) * inner + 16 * j, a.span)) = v;
+                *reinterpret_cast<uint4*>(img0 + (size_t)k * a.box_bytes +
+                                          swizzle_offset((r0 + r) * inner + 16 * j, a.span)) = v;
+                r += r_step;
+                c += c_step;
+                if (c >= rc) {
+                    c -= rc;
+                    r++;
+                }
             }
         }
         __syncwarp();
@@ -485,12 +517,16 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_store(const __grid_co
         return;
     }
 
-    // ---- consumers
+    // ---- consumers: the copy's row-major chunk walk, always (the tensor's rows are then written
+    // in order; measured on GB300 10 % faster than box-major on the W4 rank-5 view)
     const uint32_t cpr = inner >> 4;
     const uint32_t cpr_shift = (cpr & (cpr - 1)) == 0 ? (uint32_t)(__ffs(cpr) - 1) : 32u;
     const uint32_t row_bytes = s.row_bytes;
     const uint32_t ct = threadIdx.x - 32;
     constexpr uint32_t kCT = 32 * kSegConsumerWarps;
+    const uint32_t rc = s.run * cpr;  // chunks per tensor row of the run
+    const uint32_t r_start = ct / rc, c_start = ct - r_start * rc;
+    const uint32_t r_step = kCT / rc, c_step = kCT - r_step * rc;
     uint32_t sb = 0, sparity = 0;
     for (uint64_t n = 0; n < total; n++) {
         if (n) {
@@ -507,21 +543,25 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_store(const __grid_co
         const uint64_t* const tab = tabs + (size_t)sb * E * G1;
         const uint32_t r0 = info[sb].r0;
         const uint32_t nr = info[sb].nr;
-        const uint32_t per_box = nr * cpr;
         const uint8_t* const blk0 = sbuf0 + sb * stage_bytes;
-        for (uint32_t k = 0; k < s.run; k++) {
-            const uint8_t* const blk = blk0 + k * s.img_stride;
-            for (uint32_t rc = ct; rc < per_box; rc += kCT) {
-                const uint32_t r = cpr_shift < 32 ? rc >> cpr_shift : rc / cpr;
-                const uint32_t j = rc - r * cpr;
-                const uint64_t row = tab[r];
-                const int x = (int)(k * inner + 16 * j);
-                const int left = (int)row_bytes - x;
-                if (row == ~0ull || left <= 0) continue;
+        for (uint32_t r = r_start, c = c_start; r < nr;) {
+            const uint32_t k = cpr_shift < 32 ? c >> cpr_shift : c / cpr;  // box of the run
+            const uint32_t j = c - k * cpr;                                  // chunk of its row
+            const uint64_t row = tab[r];
+            const int x = (int)(16 * c);
+            const int left = (int)row_bytes - x;
+            if (row != ~0ull && left > 0) {
                 // the block starts at image row r0; the swizzle permutes inside a row
                 const uint4 v = *reinterpret_cast<const uint4*>(
-                    blk + swizzle_offset((r0 + r) * inner + 16 * j, a.span) - r0 * inner);
+                    blk0 + k * s.img_stride + swizzle_offset((r0 + r) * inner + 16 * j, a.span) -
+                    r0 * inner);
                 put_head(reinterpret_cast<uint8_t*>(row + (uint64_t)x), v, left < 16 ? left : 16);
+            }
+            r += r_step;
+            c += c_step;
+            if (c >= rc) {
+                c -= rc;
+                r++;
             }
         }
         __syncwarp();
