@@ -7,7 +7,7 @@ stream.  There is no CPU fallback: if the library was not built this module refu
 Function names and argument order follow the C ABI:
     tmap_plan / tmap_encode(dtype, base, global_dim, global_strides, box_dim, element_strides=None,
                             swizzle=TM_SWIZZLE_NONE, oob=TM_OOB_ZERO) -> TensorMap
-    tmap_replace_address(map, new_base), tmap_force_fallback(map)
+    tmap_replace_address(map, new_base), tmap_force_fallback(map), tmap_set_l2_promotion(map, promo)
     tile_load_image(src, coords, image, stream=None)
     tiled_copy(src, coords, images, stream=None)            coords None = whole box grid
     tiled_roundtrip(dst, coords, images, stream=None)
@@ -24,7 +24,8 @@ import os
 
 __all__ = [
     "TmapError", "TensorMap", "tmap_plan", "tmap_encode", "tmap_replace_address",
-    "tmap_force_fallback", "tile_load_image", "tiled_copy", "tiled_roundtrip", "tile_reduce_add",
+    "tmap_force_fallback", "tmap_set_l2_promotion", "TM_L2_NONE", "TM_L2_64B", "TM_L2_128B",
+    "TM_L2_256B", "tile_load_image", "tiled_copy", "tiled_roundtrip", "tile_reduce_add",
     "tile_reduce", "TM_RED_ADD", "TM_RED_MIN", "TM_RED_MAX",
     "stream_tiles", "stream_gemm", "tiled_copy_noalloc", "TM_NOALLOC_MAX_BOXES", "tm_stream_check",
     "tm_selftest_wait_timeout", "tm_pick_swizzle", "tm_last_error",
@@ -42,6 +43,7 @@ TM_OOB_ZERO, TM_OOB_NAN = 0, 1
 TM_PATH_TMA, TM_PATH_FALLBACK = 1, 2
 TM_RED_ADD, TM_RED_MIN, TM_RED_MAX = 0, 1, 2
 TM_WHY_STRIDE, TM_WHY_BASE, TM_WHY_DRIVER, TM_WHY_FORCED, TM_WHY_STEP0 = 1, 2, 4, 8, 16
+TM_L2_NONE, TM_L2_64B, TM_L2_128B, TM_L2_256B = range(4)
 DESC_SIZE = 384
 TM_NOALLOC_MAX_BOXES = 16384
 
@@ -66,6 +68,7 @@ _SIGS = {
                     ctypes.c_int, ctypes.c_int],
     "tmap_replace_address": [_vp, _vp],
     "tmap_force_fallback": [_vp],
+    "tmap_set_l2_promotion": [_vp, ctypes.c_int],
     "tile_load_image": [_vp, _P(_i32), _vp, _vp],
     "tiled_copy": [_vp, _P(_i32), ctypes.c_size_t, _vp, _vp],
     "tiled_roundtrip": [_vp, _P(_i32), ctypes.c_size_t, _vp, _vp],
@@ -131,7 +134,8 @@ class _Desc(ctypes.Structure):
         ("oob", _u32), ("path", _u32), ("why_fallback", _u32), ("base", _u64),
         ("dim", _u64 * 5), ("stride", _u64 * 5), ("box", _u32 * 5), ("estride", _u32 * 5),
         ("nbox", _u64 * 5), ("box_bytes", _u64), ("num_boxes", _u64),
-        ("reserved", ctypes.c_uint8 * 40), ("tmap", ctypes.c_uint8 * 128),
+        ("l2_promotion", ctypes.c_uint32), ("reserved", ctypes.c_uint8 * 36),
+        ("tmap", ctypes.c_uint8 * 128),
     ]
 
 
@@ -179,6 +183,10 @@ class TensorMap:
     def why_fallback(self) -> int:
         return int(self.d.why_fallback)
 
+    @property
+    def l2_promotion(self) -> int:
+        return int(self.d.l2_promotion)
+
 
 def _arr(ctype, vals):
     vals = list(vals)
@@ -216,6 +224,10 @@ def tmap_replace_address(m: TensorMap, new_base) -> None:
 
 def tmap_force_fallback(m: TensorMap) -> None:
     _check(_L.tmap_force_fallback(m.ptr), "tmap_force_fallback")
+
+
+def tmap_set_l2_promotion(m: TensorMap, promo: int) -> None:
+    _check(_L.tmap_set_l2_promotion(m.ptr, int(promo)), "tmap_set_l2_promotion")
 
 
 def _coords(coords, rank):

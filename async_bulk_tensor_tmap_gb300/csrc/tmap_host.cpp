@@ -27,6 +27,7 @@ static_assert(offsetof(tm_desc, box) == 120, "tm_desc layout");
 static_assert(offsetof(tm_desc, nbox) == 160, "tm_desc layout");
 static_assert(offsetof(tm_desc, box_bytes) == 200, "tm_desc layout");
 static_assert(offsetof(tm_desc, tmap) == 256, "tm_desc layout");
+static_assert(offsetof(tm_desc, l2_promotion) == 216, "tm_desc layout");
 static_assert(sizeof(CUtensorMap) == 128, "CUtensorMap is 128 bytes");
 
 namespace {
@@ -415,6 +416,7 @@ int plan_impl(tm_desc* out, int dtype, uint32_t rank, void* base, const uint64_t
     out->rank = rank;
     out->swizzle = (uint32_t)sw;
     out->oob = (uint32_t)oob;
+    out->l2_promotion = (uint32_t)std::min<uint64_t>(env_u64("TM_L2_PROMOTION", TM_L2_128B), TM_L2_256B);
     out->path = why ? TM_PATH_FALLBACK : TM_PATH_TMA;
     out->why_fallback = why;
     out->base = b;
@@ -450,8 +452,7 @@ int encode_into(tm_desc* d)
         estr[i] = d->estride[i];
         if (i > 0) strides[i - 1] = d->stride[i];
     }
-    const CUtensorMapL2promotion promo =
-        (CUtensorMapL2promotion)std::min<uint64_t>(env_u64("TM_L2_PROMOTION", 2), 3);
+    const CUtensorMapL2promotion promo = (CUtensorMapL2promotion)std::min<uint32_t>(d->l2_promotion, 3);
     const CUresult r = enc((CUtensorMap*)d->tmap, (CUtensorMapDataType)d->dtype, d->rank,
                            (void*)(uintptr_t)d->base, dims, strides, boxd, estr,
                            CU_TENSOR_MAP_INTERLEAVE_NONE, (CUtensorMapSwizzle)d->swizzle, promo,
@@ -518,11 +519,26 @@ int tmap_replace_address(tm_desc* d, void* new_base)
     int rc = tmap_encode(&t, (tm_dtype)d->dtype, d->rank, new_base, gdim, gstr, box, estr,
                          (tm_swizzle)d->swizzle, (tm_oob)d->oob);
     if (rc) return rc;
+    if (t.l2_promotion != d->l2_promotion) {  // keep the map's own promotion
+        t.l2_promotion = d->l2_promotion;
+        if (t.path == TM_PATH_TMA && (rc = encode_into(&t))) return rc;
+    }
     if (forced) {
         t.path = TM_PATH_FALLBACK;
         t.why_fallback |= TM_WHY_FORCED;
     }
     *d = t;
+    return TM_OK;
+}
+
+int tmap_set_l2_promotion(tm_desc* d, tm_l2_promotion promo)
+{
+    if (!valid_desc(d)) return fail(TM_EINVAL, "descriptor is not filled");
+    if ((uint32_t)promo > TM_L2_256B) return fail(TM_EINVAL, "bad L2 promotion %d", (int)promo);
+    d->l2_promotion = (uint32_t)promo;
+    bool encoded = false;  // a planned map has an all-zero tensor map
+    for (size_t i = 0; i < sizeof(d->tmap); i++) encoded = encoded || d->tmap[i] != 0;
+    if (d->path == TM_PATH_TMA && encoded) return encode_into(d);
     return TM_OK;
 }
 

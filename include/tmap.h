@@ -108,7 +108,8 @@ typedef struct __attribute__((aligned(64))) tm_desc {
     uint64_t nbox[5];       /* boxes along each dim: ceil(dim / box)                           */
     uint64_t box_bytes;     /* bytes of one box image: esize * prod(ceil(box / estride))        */
     uint64_t num_boxes;     /* prod(nbox)                                                       */
-    uint8_t reserved[40];
+    uint32_t l2_promotion;  /* tm_l2_promotion of the TMA loads (tmap_set_l2_promotion)          */
+    uint8_t reserved[36];
     uint8_t tmap[128];      /* CUtensorMap (driver-encoded) when path == TM_PATH_TMA            */
 } tm_desc;
 
@@ -155,6 +156,18 @@ int tmap_encode(tm_desc* out, tm_dtype dtype, uint32_t rank, void* base,
  *   device).  A new base that is not 16-byte aligned moves the map to the fallback path; one that
  *   is not a multiple of the element size gives TM_EALIGN. */
 int tmap_replace_address(tm_desc* d, void* new_base);
+
+/* tmap_set_l2_promotion -- the L2 promotion the tensor map asks of its loads, a field of the
+ *   driver's tensor map ([H200-TMA] §04 ① and [Book-TMA] §"单 block、单 lane、单 tile 的 TMA
+ *   load" pass CU_TENSOR_MAP_L2_PROMOTION_NONE to cuTensorMapEncodeTiled).  Performance only: no
+ *   result depends on it, and the oracle has no counterpart.  Maps start at TM_L2_128B (or the
+ *   value of the environment variable TM_L2_PROMOTION, 0..3, when it is set).  An encoded
+ *   tensor-map-path map is re-encoded with the new value; a planned or fallback-path map keeps it
+ *   for a later encode.  promo above TM_L2_256B, or an unfilled descriptor: TM_EINVAL. */
+typedef enum tm_l2_promotion {
+    TM_L2_NONE = 0, TM_L2_64B = 1, TM_L2_128B = 2, TM_L2_256B = 3
+} tm_l2_promotion;
+int tmap_set_l2_promotion(tm_desc* d, tm_l2_promotion promo);
 
 /* tmap_force_fallback -- put a valid map on the fallback path (why_fallback |= TM_WHY_FORCED).
  *   Used to check that both paths produce identical bytes. */

@@ -212,3 +212,23 @@ def test_stream_gemm_validation(tm):
     assert code(f, b, c) == tm.TM_EUNSUPPORTED
     n = tm.tmap_plan(tm.TM_BF16, FAKE, [4096, 512], [8192], [64, 128])
     assert code(n, b, c) == tm.TM_EUNSUPPORTED                    # no swizzle
+
+
+def test_l2_promotion_field(tm, monkeypatch):
+    """The map's L2 promotion: 128B unless TM_L2_PROMOTION says otherwise, set per map, values
+    above TM_L2_256B and unfilled descriptors refused (no GPU: a planned map keeps the value for a
+    later encode)."""
+    monkeypatch.delenv("TM_L2_PROMOTION", raising=False)
+    m = plan(tm)
+    assert m.l2_promotion == tm.TM_L2_128B
+    for p in (tm.TM_L2_NONE, tm.TM_L2_64B, tm.TM_L2_256B):
+        tm.tmap_set_l2_promotion(m, p)
+        assert m.l2_promotion == p
+    with pytest.raises(tm.TmapError) as e:
+        tm.tmap_set_l2_promotion(m, 4)
+    assert e.value.code == tm.TM_EINVAL
+    with pytest.raises(tm.TmapError) as e:
+        tm.tmap_set_l2_promotion(tm.TensorMap(), tm.TM_L2_NONE)
+    assert e.value.code == tm.TM_EINVAL
+    monkeypatch.setenv("TM_L2_PROMOTION", "0")
+    assert plan(tm).l2_promotion == tm.TM_L2_NONE

@@ -116,6 +116,28 @@ def test_w3_copy_and_roundtrip(tm, span, force_fallback):
     assert torch.equal(dst, xd)
 
 
+def test_l2_promotion_changes_no_byte(tm):
+    """Every L2 promotion of the tensor map gives the oracle's images, and a rebase keeps it."""
+    x, r = w3_small(128, rows=520, cols=392)
+    xd = to_dev(x)
+    want = oracle.tiled_copy(host_map(x, r), threads=8)
+    m = dev_map(tm, xd, r)
+    for p in (tm.TM_L2_NONE, tm.TM_L2_64B, tm.TM_L2_128B, tm.TM_L2_256B):
+        tm.tmap_set_l2_promotion(m, p)
+        assert m.path == tm.TM_PATH_TMA and m.l2_promotion == p
+        imgs = empty_images(m.num_boxes, m.box_bytes)
+        tm.tiled_copy(m, None, imgs)
+        check(tm)
+        np.testing.assert_array_equal(to_host(imgs), want, err_msg=f"promotion {p}")
+    x2 = to_dev(x)
+    tm.tmap_replace_address(m, x2)
+    assert m.l2_promotion == tm.TM_L2_256B
+    imgs = empty_images(m.num_boxes, m.box_bytes)
+    tm.tiled_copy(m, None, imgs)
+    check(tm)
+    np.testing.assert_array_equal(to_host(imgs), want)
+
+
 def test_w3_fallback_and_tma_images_identical(tm):
     x, r = w3_small(128, rows=520, cols=392)
     xd = to_dev(x)
