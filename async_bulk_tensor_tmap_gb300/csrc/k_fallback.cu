@@ -621,18 +621,30 @@ __device__ void fb_reduce_rows(const FbArgs& a)
 {
     using E = typename std::conditional<(T == 1 || T == 2), uint16_t, uint32_t>::type;
     constexpr int es = (int)sizeof(E);
-    constexpr uint32_t kVecPerThread = 4;
-    constexpr uint64_t kSegBytes = (uint64_t)kThreads * kVecPerThread * 16;
-    const uint64_t row_bytes = a.dim[0] * es;
+    constexpr uint32_t kVecPerLane = 4;
+    constexpr uint64_t kSegBytes = 8192;  // one warp's item: 8 KiB of a row (4 passes of vectors)
+    // A row is dim 0 and every following dim that is contiguous with it in both tensors (a view
+    // that splits a row, like the rank-5 W4 view's 10 x 100, is walked as its whole rows).
+    uint32_t f = 1;
+    uint64_t row_elems = a.dim[0];
+    while (f < a.walk.rank && a.stride[f] == (int64_t)(row_elems * es) &&
+           a.src_stride[f] == (int64_t)(row_elems * es)) {
+        row_elems *= a.dim[f];
+        f++;
+    }
+    const uint64_t row_bytes = row_elems * es;
     const uint64_t segs = (row_bytes + kSegBytes - 1) / kSegBytes;
     uint64_t nrows = 1;
-    for (uint32_t i = 1; i < a.walk.rank; i++) nrows *= a.dim[i];
+    for (uint32_t i = f; i < a.walk.rank; i++) nrows *= a.dim[i];
     const uint64_t items = nrows * segs;
-    for (uint64_t it = blockIdx.x; it < items; it += gridDim.x) {
+    const uint32_t lane = threadIdx.x & 31;
+    const uint64_t w0 = (uint64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    const uint64_t nw = (uint64_t)gridDim.x * (kThreads / 32);
+    for (uint64_t it = w0; it < items; it += nw) {
         const uint64_t row = it / segs, seg = it - row * segs;
         int64_t od = 0, os = 0;
         uint64_t q = row;
-        for (uint32_t i = 1; i < a.walk.rank; i++) {
+        for (uint32_t i = f; i < a.walk.rank; i++) {
             const uint64_t nxt = q / a.dim[i];
             const int64_t g = (int64_t)(q - nxt * a.dim[i]);
             q = nxt;
@@ -644,42 +656,38 @@ __device__ void fb_reduce_rows(const FbArgs& a)
         const uint64_t b0 = seg * kSegBytes;
         const uint64_t b1 = min(b0 + kSegBytes, row_bytes);
         const uint32_t phase = (uint32_t)((uintptr_t)d & 15);
+        uint64_t vs = b1, ve = b1;  // whole 16-byte vectors in [vs, ve) when both phases agree
         if (phase == ((uintptr_t)sp & 15)) {
-            // head [b0, vs) and tail [ve, b1) element by element, whole vectors in [vs, ve)
             const uint64_t first_vec = ((uint64_t)((uintptr_t)d + b0) + 15) / 16 * 16 - (uintptr_t)d;
-            const uint64_t vs = min(first_vec, b1);
-            const uint64_t ve = vs + (b1 - vs) / 16 * 16;
-            for (uint64_t x = b0 + threadIdx.x * es; x < vs; x += kThreads * es) {
-                E* p = reinterpret_cast<E*>(d + x);
-                *p = (E)combine<T, OP>((uint32_t)*p, (uint32_t)*reinterpret_cast<const E*>(sp + x));
-            }
-            const uint64_t nv = (ve - vs) / 16;
-            for (uint64_t v = threadIdx.x; v < nv; v += kThreads * kVecPerThread) {
-                uint4 dv[kVecPerThread], sv[kVecPerThread];
+            vs = min(first_vec, b1);
+            ve = vs + (b1 - vs) / 16 * 16;
+        }
+        // head [b0, vs) and tail [ve, b1) element by element
+        for (uint64_t x = b0 + lane * es; x < vs; x += 32 * es) {
+            E* p = reinterpret_cast<E*>(d + x);
+            *p = (E)combine<T, OP>((uint32_t)*p, (uint32_t)*reinterpret_cast<const E*>(sp + x));
+        }
+        const uint64_t nv = (ve - vs) / 16;
+        for (uint64_t v = lane; v < nv; v += 32 * kVecPerLane) {
+            uint4 dv[kVecPerLane], sv[kVecPerLane];
 #pragma unroll
-                for (uint32_t u = 0; u < kVecPerThread; u++) {
-                    const uint64_t vi = v + u * kThreads;
-                    if (vi < nv) {
-                        dv[u] = *reinterpret_cast<const uint4*>(d + vs + vi * 16);
-                        sv[u] = __ldg(reinterpret_cast<const uint4*>(sp + vs + vi * 16));
-                    }
-                }
-#pragma unroll
-                for (uint32_t u = 0; u < kVecPerThread; u++) {
-                    const uint64_t vi = v + u * kThreads;
-                    if (vi < nv)
-                        *reinterpret_cast<uint4*>(d + vs + vi * 16) = combine_vec<T, OP>(dv[u], sv[u]);
+            for (uint32_t u = 0; u < kVecPerLane; u++) {
+                const uint64_t vi = v + u * 32;
+                if (vi < nv) {
+                    dv[u] = *reinterpret_cast<const uint4*>(d + vs + vi * 16);
+                    sv[u] = __ldg(reinterpret_cast<const uint4*>(sp + vs + vi * 16));
                 }
             }
-            for (uint64_t x = ve + threadIdx.x * es; x < b1; x += kThreads * es) {
-                E* p = reinterpret_cast<E*>(d + x);
-                *p = (E)combine<T, OP>((uint32_t)*p, (uint32_t)*reinterpret_cast<const E*>(sp + x));
+#pragma unroll
+            for (uint32_t u = 0; u < kVecPerLane; u++) {
+                const uint64_t vi = v + u * 32;
+                if (vi < nv)
+                    *reinterpret_cast<uint4*>(d + vs + vi * 16) = combine_vec<T, OP>(dv[u], sv[u]);
             }
-        } else {
-            for (uint64_t x = b0 + threadIdx.x * es; x < b1; x += kThreads * es) {
-                E* p = reinterpret_cast<E*>(d + x);
-                *p = (E)combine<T, OP>((uint32_t)*p, (uint32_t)*reinterpret_cast<const E*>(sp + x));
-            }
+        }
+        for (uint64_t x = ve + lane * es; x < b1; x += 32 * es) {
+            E* p = reinterpret_cast<E*>(d + x);
+            *p = (E)combine<T, OP>((uint32_t)*p, (uint32_t)*reinterpret_cast<const E*>(sp + x));
         }
     }
 }

@@ -656,10 +656,11 @@ int tile_reduce(const tm_desc* dst, const tm_desc* src, tm_redop op, void* strea
         for (int i = 0; i < 5; i++) a.src_stride[i] = (int64_t)src->stride[i];
         a.red_type = (uint16_t)red_type;
         a.red_op = (uint16_t)op;
-        // work items of the element-wise kernel: 16 KiB segments of the tensor's rows
-        uint64_t items = (dst->dim[0] * dst->esize + 16383) / 16384;
-        for (uint32_t i = 1; i < dst->rank; i++) items *= dst->dim[i];
-        const uint32_t grid = (uint32_t)std::min<uint64_t>(items, (uint64_t)ds->sms * 3);
+        // the element-wise kernel's warps take 8 KiB pieces of the tensor's rows, grid-strided;
+        // 3 CTAs of 8 warps per SM (fewer CTAs for a small tensor)
+        uint64_t pieces = (dst->dim[0] * dst->esize + 8191) / 8192;
+        for (uint32_t i = 1; i < dst->rank; i++) pieces *= dst->dim[i];
+        const uint32_t grid = (uint32_t)std::min<uint64_t>((pieces + 7) / 8, (uint64_t)ds->sms * 3);
         rc = check_launch(launch_fb_reduce(a, std::max<uint32_t>(grid, 1), st),
                           "fallback reduce launch");
     }

@@ -117,8 +117,12 @@ class HostWorkload:
                 self.w5a_dst, self.w5a_src = workloads.w5a_tensors(r5a)
             self.w5c_dst = workloads.normal_bf16((r5a, 16384), 55)
             self.w5c_src = workloads.normal_bf16((r5a, 16384), 56)
+            # bf16 add through the W4 rank-5 view (a 200-byte stride: the vector path)
+            self.w5c_r5_dst = workloads.w4_tensor(rows=r4, seed=57)
+            self.w5c_r5_src = workloads.w4_tensor(rows=r4, seed=58)
         else:
             self.w5c_dst = self.w5c_src = None
+            self.w5c_r5_dst = self.w5c_r5_src = None
         self.gen_s = time.time() - t0
         self.r3 = workloads.w3_map(r3, 8192)
         self.r4_128 = workloads.w4_rank3_map(64, rows=r4, span=128)
@@ -171,7 +175,8 @@ def op_table(h: HostWorkload):
 
 
 # Widened ops, timed only when named with --ops: (name, algorithmic bytes per call).
-#   w5c: reduces of other types and ops: dst read + src read + dst written.
+#   w5c: reduces of other types and ops: dst read + src read + dst written (add_bf16_r5: through
+#     the W4 rank-5 view, whose 200-byte stride puts it on the vector path).
 #   w6.rows2: the image takes every other row: the taken rows are read, the images written.
 #   w6.cols2: every other column (vector path: an innermost step above 1); the taken elements
 #     are 4 bytes apart, so every 32-byte sector of the tensor holds some and the whole tensor is
@@ -190,6 +195,7 @@ def extra_ops(h: HostWorkload):
     cols2_img = box_count(h.r6_cols2) * box_bytes(h.r6_cols2)
     w3 = inbounds_bytes(h.r3)
     return [("w5c.add_bf16", 3 * 2 * n), ("w5c.min_s32", 3 * 4 * n), ("w5c.max_f32", 3 * 4 * n),
+            ("w5c.add_bf16_r5", 3 * inbounds_bytes(h.r4_r5)),
             ("w6.rows2", 2 * rows2_img), ("w6.cols2", w3 + cols2_img),
             ("w6.cols2_rt", cols2_img + w3),
             ("w6.nan", inbounds_bytes(h.r6_nan) + box_count(h.r6_nan) * box_bytes(h.r6_nan))] + \
@@ -252,6 +258,9 @@ class GpuWorkload:
             self.t["w5c_dst"], self.t["w5c_src"] = dev(h.w5c_dst), dev(h.w5c_src)
             self.maps["w5c_dst"] = enc(tm.TM_BF16, self.t["w5c_dst"], h.r5c)
             self.maps["w5c_src"] = enc(tm.TM_BF16, self.t["w5c_src"], h.r5c)
+            self.t["w5c_r5_dst"], self.t["w5c_r5_src"] = dev(h.w5c_r5_dst), dev(h.w5c_r5_src)
+            self.maps["w5c_r5_dst"] = enc(tm.TM_BF16, self.t["w5c_r5_dst"], h.r4_r5)
+            self.maps["w5c_r5_src"] = enc(tm.TM_BF16, self.t["w5c_r5_src"], h.r4_r5)
             self.maps["w5a_dst_s32"] = enc(tm.TM_S32, self.t["w5a_dst"], h.r5a)
             self.maps["w5a_src_s32"] = enc(tm.TM_S32, self.t["w5a_src"], h.r5a)
         if "w3" in self.t and "w4" in self.t:
@@ -279,6 +288,8 @@ class GpuWorkload:
             tm.tile_reduce_add(m["w5a_dst"], m["w5a_src"], s)
         elif kind == "add_bf16":
             tm.tile_reduce(m["w5c_dst"], m["w5c_src"], tm.TM_RED_ADD, s)
+        elif kind == "add_bf16_r5":
+            tm.tile_reduce(m["w5c_r5_dst"], m["w5c_r5_src"], tm.TM_RED_ADD, s)
         elif kind == "min_s32":
             tm.tile_reduce(m["w5a_dst_s32"], m["w5a_src_s32"], tm.TM_RED_MIN, s)
         elif kind == "max_f32":
@@ -566,6 +577,8 @@ def oracle_sample(h: HostWorkload, ops, fraction: float, threads: int):
         elif base == "w5c":
             if kind == "add_bf16":
                 d, sr, r, ty, op = h.w5c_dst, h.w5c_src, h.r5c, oracle.BF16, oracle.ADD
+            elif kind == "add_bf16_r5":
+                d, sr, r, ty, op = h.w5c_r5_dst, h.w5c_r5_src, h.r4_r5, oracle.BF16, oracle.ADD
             else:
                 d, sr, r = h.w5a_dst, h.w5a_src, h.r5a
                 ty, op = (oracle.S32, oracle.MIN) if kind == "min_s32" else (oracle.F32, oracle.MAX)

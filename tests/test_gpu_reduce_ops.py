@@ -78,3 +78,35 @@ def test_reduce_rejects_mixed_types(tm):
     with pytest.raises(tm.TmapError) as e:
         tm.tile_reduce(c, c, tm.TM_RED_MAX)
     assert e.value.code == tm.TM_EUNSUPPORTED
+
+
+# Views whose two innermost dims are contiguous (a row split into G groups of c0 elements, the
+# group stride c0 * esize not a multiple of 16: the vector path, which walks such a view by whole
+# rows), ragged boxes along every dim, padding after each row that must stay untouched; `shifted`
+# moves the destination one element along so that the two tensors' 16-byte phases differ (the
+# element-by-element path); `src_gaps` gives the source a gap between groups (no fusion).
+@pytest.mark.parametrize("kind,op,c0", [("bf16", 0, 60), ("f16", 0, 60), ("f32", 2, 50),
+                                        ("s32", 1, 50)])
+@pytest.mark.parametrize("layout", ["same", "shifted", "src_gaps"])
+def test_reduce_unaligned_view_by_rows(tm, kind, op, c0, layout):
+    es = 2 if kind in ("f16", "bf16") else 4
+    R, G = 37, 5
+    P = G * (c0 + 4) + 8  # row pitch in elements, room for the source's gaps and padding
+    d, s = workloads.reduce_operands(kind, R, P, 400 + op + KINDS.index(kind))
+    box = [64 // es, G, 8]
+    rd = dict(dims=[c0, G, R], strides=[c0 * es, P * es], box=box, span=0, esize=es)
+    rs = dict(rd, strides=[(c0 + 4) * es, P * es]) if layout == "src_gaps" else rd
+    off = es if layout == "shifted" else 0
+    dd, sd = to_dev(d), to_dev(s)
+    dt = tm_dtype(tm, kind)
+    md = tm.tmap_encode(dt, dd.data_ptr() + off, rd["dims"], rd["strides"], rd["box"])
+    ms = tm.tmap_encode(dt, sd, rs["dims"], rs["strides"], rs["box"])
+    assert md.path == tm.TM_PATH_FALLBACK
+    tm.tile_reduce(md, ms, op)
+    torch.cuda.synchronize()
+    assert tm.tm_stream_check() == tm.TM_OK, tm.tm_last_error()
+    hd = np.ascontiguousarray(d).copy()
+    oracle.tile_reduce(host_map(hd, rd, offset=off), host_map(np.ascontiguousarray(s), rs),
+                       ORC_TYPE[kind], op)
+    np.testing.assert_array_equal(to_host(dd), hd.reshape(-1).view(np.uint8),
+                                  err_msg=f"{kind} op {op} {layout}")
