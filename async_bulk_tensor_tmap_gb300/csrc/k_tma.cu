@@ -3,8 +3,9 @@
 // One CTA is one warp; its elected lane issues everything ([MLSys-TMA] = mlc.ai "Modern GPU
 // Programming for MLSys", chapter "异步数据搬运：TMA", §"一个 thread 如何描述整个 tile": a single
 // thread submits the copy, the engine does the addressing).  Boxes are taken in groups of G
-// consecutive boxes (G > 1 only for small boxes whose size is a multiple of 1024 bytes, so that
-// each image in a stage keeps the swizzle phase it has in its own image); the lane walks the
+// consecutive boxes sharing a stage (G > 1 for boxes well under a stage), each in a slot that
+// starts on its swizzle period (1024 / 512 / 256 bytes for 128B / 64B / 32B, 128 without), so that
+// each image in a stage keeps the swizzle phase it has in its own image; the lane walks the
 // groups blockIdx.x, blockIdx.x + gridDim.x, ... through an S-stage ring of 1024-byte aligned
 // shared-memory stages:
 //
@@ -109,17 +110,27 @@ __global__ void __launch_bounds__(32, 1)
         }
     };
 
+    // Box j of a stage sits at j * slot_bytes: boxes smaller than their swizzle period get padded
+    // slots so that each image starts its own swizzle phase; then the images are not contiguous
+    // in the stage and move one bulk copy per box.
+    const uint32_t slot = a.slot_bytes;
+    const bool dense = slot == a.box_bytes;
     auto issue = [&](const Cursor& c) {
         const uint32_t bar = smem_u32(&full_bar[c.s]);
         const uint32_t dst = base + c.s * a.stage_bytes;
         const uint64_t g = group_of(c.i);
-        const uint32_t bytes = count_of(g) * a.box_bytes;
-        mbar_arrive_expect_tx(bar, bytes);
+        const uint32_t cnt = count_of(g);
+        mbar_arrive_expect_tx(bar, cnt * a.box_bytes);
         if constexpr (KIND == KIND_ROUNDTRIP) {
-            bulk_load(dst, a.images + g * G * a.box_bytes, bytes, bar);
+            if (dense) {
+                bulk_load(dst, a.images + g * G * a.box_bytes, cnt * a.box_bytes, bar);
+            } else {
+                for (uint32_t j = 0; j < cnt; j++)
+                    bulk_load(dst + j * slot, a.images + (g * G + j) * a.box_bytes, a.box_bytes, bar);
+            }
         } else {
             for_boxes(c, [&](uint32_t j, const int32_t* co) {
-                tma_load<R>(dst + j * a.box_bytes, &in_map, co, bar);
+                tma_load<R>(dst + j * slot, &in_map, co, bar);
             });
         }
     };
@@ -128,13 +139,19 @@ __global__ void __launch_bounds__(32, 1)
         const uint32_t src = base + c.s * a.stage_bytes;
         const uint64_t g = group_of(c.i);
         if constexpr (KIND == KIND_COPY) {
-            bulk_store(a.images + g * G * a.box_bytes, src, count_of(g) * a.box_bytes);
+            if (dense) {
+                bulk_store(a.images + g * G * a.box_bytes, src, count_of(g) * a.box_bytes);
+            } else {
+                const uint32_t cnt = count_of(g);
+                for (uint32_t j = 0; j < cnt; j++)
+                    bulk_store(a.images + (g * G + j) * a.box_bytes, src + j * slot, a.box_bytes);
+            }
         } else {
             for_boxes(c, [&](uint32_t j, const int32_t* co) {
                 if constexpr (KIND == KIND_ROUNDTRIP) {
-                    tma_store<R>(&out_map, co, src + j * a.box_bytes);
+                    tma_store<R>(&out_map, co, src + j * slot);
                 } else {
-                    tma_reduce<R, KIND - KIND_REDUCE>(&out_map, co, src + j * a.box_bytes);
+                    tma_reduce<R, KIND - KIND_REDUCE>(&out_map, co, src + j * slot);
                 }
             });
         }

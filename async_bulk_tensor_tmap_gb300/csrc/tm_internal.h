@@ -52,7 +52,9 @@ struct StreamArgs {
     uint32_t box_bytes;
     uint32_t stage_bytes;  // group * box_bytes rounded up to kStageAlign
     uint32_t stages;
-    uint32_t group;        // consecutive boxes per stage (1, or more when box_bytes % 1024 == 0)
+    uint32_t group;        // consecutive boxes per stage
+    uint32_t slot_bytes;   // stage bytes per box: box_bytes rounded up to its swizzle period
+    uint32_t pad;
     uint64_t timeout_ns;
     StatusBlock* status;
 };

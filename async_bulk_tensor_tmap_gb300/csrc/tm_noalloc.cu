@@ -167,6 +167,7 @@ extern "C" int tiled_copy_noalloc(const tm_desc* src, const int32_t* coords, siz
         a.box_bytes = (uint32_t)src->box_bytes;
         a.stage_bytes = stage;
         a.group = 1;
+        a.slot_bytes = (uint32_t)src->box_bytes;
         a.stages = (uint32_t)std::max<size_t>(1, std::min<size_t>(b / stage, TM_MAX_STAGES));
         a.timeout_ns = limit_ns();
         a.status = status;

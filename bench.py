@@ -136,6 +136,7 @@ class HostWorkload:
         self.r6_rows2 = workloads.w6_rows2_map(r3, 8192)
         self.r6_cols2 = workloads.w6_cols2_map(r3, 8192)
         self.r6_nan = dict(self.r4_128, nan=True)
+        self.r6_box512 = dict(self.r3, box=[64, 4])  # 512-byte boxes, 128B swizzle
 
 
 def box_count(r):
@@ -183,6 +184,7 @@ def op_table(h: HostWorkload):
 #     read.
 #   w6.cols2_rt: those images stored back: images read, every sector of the tensor written.
 #   w6.nan: the W4 rank-3 copy with NaN out-of-bounds fill (bytes as w4r3.copy).
+#   w6.box512: the W3 copy through 64 x 4 boxes (512-byte images, 128B swizzle; bytes as w3.copy).
 #   w7.gemm: C = A * B^T on the tensor cores, A and B 8192 x 4096 bf16, C 8192 x 8192 fp32 (bytes:
 #     A + B read once, C written; its figure of merit is TFLOP/s, 2 * M * N * K per call).
 def gemm_flops(h: HostWorkload) -> int:
@@ -198,7 +200,8 @@ def extra_ops(h: HostWorkload):
             ("w5c.add_bf16_r5", 3 * inbounds_bytes(h.r4_r5)),
             ("w6.rows2", 2 * rows2_img), ("w6.cols2", w3 + cols2_img),
             ("w6.cols2_rt", cols2_img + w3),
-            ("w6.nan", inbounds_bytes(h.r6_nan) + box_count(h.r6_nan) * box_bytes(h.r6_nan))] + \
+            ("w6.nan", inbounds_bytes(h.r6_nan) + box_count(h.r6_nan) * box_bytes(h.r6_nan)),
+            ("w6.box512", w3 + box_count(h.r6_box512) * box_bytes(h.r6_box512))] + \
         ([("w7.gemm", h.w7_a.nbytes + h.w7_b.nbytes + 4 * h.w7_a.shape[0] * h.w7_b.shape[0])]
          if h.w7_a is not None else [])
 
@@ -268,7 +271,8 @@ class GpuWorkload:
             self.maps["w6_cols2"] = enc(bf, self.t["w3"], h.r6_cols2)
             self.maps["w6_cols2_out"] = enc(bf, self.t["w3_out"], h.r6_cols2)
             self.maps["w6_nan"] = enc(bf, self.t["w4"], h.r6_nan)
-        for k in ("w3", "w4r3", "w4r3n", "w4r5", "w6_rows2", "w6_cols2", "w6_nan"):
+            self.maps["w6_box512"] = enc(bf, self.t["w3"], h.r6_box512)
+        for k in ("w3", "w4r3", "w4r3n", "w4r5", "w6_rows2", "w6_cols2", "w6_nan", "w6_box512"):
             if k in self.maps:
                 m = self.maps[k]
                 self.t[f"{k}_img"] = torch.empty(m.num_boxes * m.box_bytes, dtype=torch.uint8,
@@ -299,7 +303,7 @@ class GpuWorkload:
                             t["bits_a"], t["bits_b"], s)
         elif kind == "gemm":
             tm.stream_gemm(m["w7_a"], m["w7_b"], t["w7_c"], stages=self.gemm_stages, stream=s)
-        elif kind in ("rows2", "cols2", "nan"):
+        elif kind in ("rows2", "cols2", "nan", "box512"):
             tm.tiled_copy(m[f"w6_{kind}"], None, t[f"w6_{kind}_img"], s)
         elif kind == "cols2_rt":
             tm.tiled_roundtrip(m["w6_cols2_out"], None, t["w6_cols2_img"], s)
@@ -586,7 +590,7 @@ def oracle_sample(h: HostWorkload, ops, fraction: float, threads: int):
                                               threads=threads, b0=0, b1=k), r, nbytes)
             spent, covered = spent + sec, covered + cov
         elif base == "w6":
-            r = {"rows2": h.r6_rows2, "nan": h.r6_nan}.get(kind, h.r6_cols2)
+            r = {"rows2": h.r6_rows2, "nan": h.r6_nan, "box512": h.r6_box512}.get(kind, h.r6_cols2)
             src = h.w4 if kind == "nan" else h.w3
 
             def run(k):

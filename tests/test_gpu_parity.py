@@ -138,6 +138,42 @@ def test_l2_promotion_changes_no_byte(tm):
     np.testing.assert_array_equal(to_host(imgs), want)
 
 
+# Small boxes share a stage, each in a slot starting on its swizzle period (1024 / 512 / 256 bytes
+# for 128B / 64B / 32B, 128 without): padded slots (box smaller than its period) move one bulk copy
+# per box; dense ones one per stage.  Copy, round trip and reduce-add on the tensor-map path.
+@pytest.mark.parametrize("box,span", [([64, 4], 128), ([32, 4], 64), ([16, 4], 32), ([8, 3], 0),
+                                      ([64, 8], 0), ([32, 8], 64)])
+def test_small_boxes_share_stages(tm, box, span):
+    x, r = w3_small(span, rows=203, cols=392)
+    r = dict(r, box=box)
+    xd = to_dev(x)
+    m = dev_map(tm, xd, r)
+    assert m.path == tm.TM_PATH_TMA and m.box_bytes == box[0] * box[1] * 2
+    imgs = empty_images(m.num_boxes, m.box_bytes)
+    tm.tiled_copy(m, None, imgs)
+    check(tm)
+    want = oracle.tiled_copy(host_map(x, r), threads=8)
+    np.testing.assert_array_equal(to_host(imgs), want)
+    dst = torch.full_like(xd, 0x77)
+    tm.tiled_roundtrip(dev_map(tm, dst, r), None, imgs)
+    check(tm)
+    assert torch.equal(dst, xd)
+
+
+@pytest.mark.parametrize("box,span", [([32, 4], 128), ([4, 3], 0)])
+def test_small_boxes_reduce_add(tm, box, span):
+    d, s = workloads.w5a_tensors(rows=130, cols=96, seed_dst=15, seed_src=16)
+    r = dict(workloads.w5a_map(rows=130, cols=96, span=span), box=box)
+    dd, sd = to_dev(d), to_dev(s)
+    md, ms = dev_map(tm, dd, r), dev_map(tm, sd, r)
+    assert md.path == tm.TM_PATH_TMA
+    tm.tile_reduce_add(md, ms)
+    check(tm)
+    hd = d.copy()
+    oracle.tile_reduce_add(host_map(hd, r), host_map(s, r))
+    np.testing.assert_array_equal(to_host(dd).view(np.uint32), hd.reshape(-1).view(np.uint32))
+
+
 def test_w3_fallback_and_tma_images_identical(tm):
     x, r = w3_small(128, rows=520, cols=392)
     xd = to_dev(x)
