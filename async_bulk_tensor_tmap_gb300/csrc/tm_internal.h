@@ -86,6 +86,22 @@ struct FbArgs {
     StatusBlock* status;
 };
 
+// Boxes per stage of the TMA streaming kernels and the stage bytes each takes: small boxes share a
+// stage of about `target` bytes, each in a slot starting on its swizzle period (the hardware
+// swizzles on shared-memory address bits 4..9: 1024 / 512 / 256 bytes for a 128 / 64 / 32-byte
+// span; 128 bytes, the tensor copy's alignment, without), so that every image keeps the phase it
+// has in its own image.  (One box per 1 KiB stage was measured on GB300 at 1 TB/s for 512-byte
+// boxes, against 5.5 TB/s for packed 2 KiB boxes.)
+inline void tma_group(uint64_t box_bytes, uint32_t span, uint64_t target, uint32_t& group,
+                      uint32_t& slot)
+{
+    const uint64_t period = span == 128 ? 1024 : span == 64 ? 512 : span == 32 ? 256 : 128;
+    const uint64_t sl = (box_bytes + period - 1) / period * period;
+    const uint64_t g = target / sl;
+    group = (uint32_t)(g < 1 ? 1 : g > 64 ? 64 : g);
+    slot = group > 1 ? (uint32_t)sl : (uint32_t)box_bytes;
+}
+
 // NaN written for out-of-bounds elements of a map with TM_OOB_NAN on the vector path: the pattern
 // GB300's tensor-map NaN-request fill was measured to write, 0x7FF7 repeated over the element.
 inline uint64_t nan_fill_bits(uint32_t dtype)

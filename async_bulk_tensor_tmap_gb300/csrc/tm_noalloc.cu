@@ -154,24 +154,26 @@ extern "C" int tiled_copy_noalloc(const tm_desc* src, const int32_t* coords, siz
     } else {
         w.mode = WALK_GRID;
     }
-    const uint32_t stage = stage_of(src->box_bytes);
     const bool tma = src->path == TM_PATH_TMA && (!coords || list_on_tma(src, coords, n));
     if (tma) {
+        StreamArgs a;
+        memset(&a, 0, sizeof(a));
+        const uint32_t span = src->swizzle == TM_SWIZZLE_128B ? 128u : src->swizzle == TM_SWIZZLE_64B ? 64u
+                              : src->swizzle == TM_SWIZZLE_32B ? 32u : 0u;
+        tma_group(src->box_bytes, span, 32768, a.group, a.slot_bytes);
+        const uint32_t stage = stage_of((uint64_t)a.group * a.slot_bytes);
         uint32_t per_sm = 2;
         size_t b = budget(*d, per_sm);
         while (per_sm > 1 && b < stage) b = budget(*d, --per_sm);
-        StreamArgs a;
-        memset(&a, 0, sizeof(a));
         a.walk = w;
         a.images = (uint64_t)images;
         a.box_bytes = (uint32_t)src->box_bytes;
         a.stage_bytes = stage;
-        a.group = 1;
-        a.slot_bytes = (uint32_t)src->box_bytes;
         a.stages = (uint32_t)std::max<size_t>(1, std::min<size_t>(b / stage, TM_MAX_STAGES));
         a.timeout_ns = limit_ns();
         a.status = status;
-        const uint32_t grid = (uint32_t)std::min<uint64_t>(n, (uint64_t)d->sms * per_sm);
+        const uint64_t groups = (n + a.group - 1) / a.group;
+        const uint32_t grid = (uint32_t)std::min<uint64_t>(groups, (uint64_t)d->sms * per_sm);
         const CUtensorMap* m = (const CUtensorMap*)src->tmap;
         e = launch_tma_stream(KIND_COPY, src->rank, m, m, a, grid,
                               (size_t)a.stages * stage + kStageAlign, st);

@@ -164,21 +164,6 @@ struct Geometry {
     size_t smem;
 };
 
-// Boxes per stage of the TMA streaming kernels and the stage bytes each takes: small boxes share a
-// stage of about TM_GROUP_BYTES (32 KiB), each in a slot starting on its swizzle period (the
-// hardware swizzles on shared-memory address bits 4..9: 1024 / 512 / 256 bytes for a 128 / 64 /
-// 32-byte span; 128 bytes, the tensor copy's alignment, without), so that every image keeps the
-// phase it has in its own image.  (One box per 1 KiB stage was measured on GB300 at 1 TB/s for
-// 512-byte boxes, against 5.5 TB/s for packed 2 KiB boxes.)
-void tma_group(uint64_t box_bytes, uint32_t span, uint32_t& group, uint32_t& slot)
-{
-    const uint64_t period = span == 128 ? 1024 : span == 64 ? 512 : span == 32 ? 256 : 128;
-    const uint64_t sl = (box_bytes + period - 1) / period * period;
-    const uint64_t target = std::max<uint64_t>(env_u64("TM_GROUP_BYTES", 32768), 1024);
-    group = (uint32_t)std::min<uint64_t>(std::max<uint64_t>(target / sl, 1), 64);
-    slot = group > 1 ? (uint32_t)sl : (uint32_t)box_bytes;
-}
-
 // The TMA streaming kernels: `per_sm` one-warp CTAs per SM (TM_CTAS_PER_SM, default 2), each with
 // as many stages as fit (TM_STAGES caps it); `nbox` counts work units (box groups).
 Geometry tma_geometry(const DevState& ds, uint64_t nbox, uint32_t stage_bytes)
@@ -293,7 +278,8 @@ StreamArgs stream_args(const tm_desc* d, const BoxWalk& w, uint64_t images, cons
     a.walk = w;
     a.images = images;
     a.box_bytes = (uint32_t)d->box_bytes;
-    tma_group(d->box_bytes, span_of(d->swizzle), a.group, a.slot_bytes);
+    tma_group(d->box_bytes, span_of(d->swizzle),
+              std::max<uint64_t>(env_u64("TM_GROUP_BYTES", 32768), 1024), a.group, a.slot_bytes);
     a.stage_bytes = stage_bytes_of((uint64_t)a.group * a.slot_bytes);
     g = tma_geometry(ds, (w.nbox + a.group - 1) / a.group, a.stage_bytes);
     a.stages = g.stages;

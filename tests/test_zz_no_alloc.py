@@ -98,3 +98,19 @@ def test_noalloc_vector_path_whole_grid(tm):
         got = torch.full_like(want, 0x44)
         tm.tiled_copy_noalloc(m, None, got)
         assert torch.equal(got, want)
+
+
+def test_noalloc_small_boxes_share_stages(tm):
+    """512-byte boxes (128B swizzle), packed several to a stage in slots on their swizzle period:
+    the no-allocation copy gives the allocating copy's images."""
+    x = workloads.w3_tensor(300, 392, seed=46)
+    xd = _dev(x)
+    m = tm.tmap_encode(tm.TM_BF16, xd, [392, 300], [784], [64, 4], swizzle=tm.TM_SWIZZLE_128B)
+    assert m.path == tm.TM_PATH_TMA and m.box_bytes == 512
+    want = torch.zeros(m.num_boxes * m.box_bytes, dtype=torch.uint8, device="cuda")
+    tm.tiled_copy(m, None, want)
+    torch.cuda.synchronize()
+    assert tm.tm_stream_check() == tm.TM_OK, tm.tm_last_error()
+    got = torch.full_like(want, 0x55)
+    tm.tiled_copy_noalloc(m, None, got)
+    assert torch.equal(got, want)
