@@ -15,6 +15,8 @@ SRC = os.path.join(ROOT, "oracle", "tmap_oracle.c")
 
 MUTANTS = {
     "swizzle_row_bits_shifted": ("(off >> 7)", "(off >> 8)"),
+    "swizzle_64b_takes_three_row_bits": ("xor_bits = 2;", "xor_bits = 3;"),
+    "swizzle_32b_takes_two_row_bits": ("xor_bits = 1;", "xor_bits = 2;"),
     "swizzle_sector_bits_shifted": ("return off ^ (line << 4);", "return off ^ (line << 5);"),
     "oob_upper_off_by_one": ("(uint64_t)g[i] >= m->dim[i]", "(uint64_t)g[i] > m->dim[i]"),
     "oob_negative_dropped": ("if (g[i] < 0 || (uint64_t)g[i]", "if ((uint64_t)g[i] + 0 == 0 && (uint64_t)g[i]"),

@@ -94,6 +94,39 @@ def test_w2_narrow_swizzles_permute_whole_sectors(span, gcols):
             assert got == sorted(map(bytes, none[a:a + atom]))
 
 
+@pytest.mark.parametrize("span,gcols", [(64, 32), (32, 16)])
+def test_narrow_swizzles_spread_a_column_over_eight_bank_sectors(span, gcols):
+    """64B / 32B, still PARITY UNPINNED: the pages fix no permutation for them.  They fix its
+    purpose ([MLSys-TMA] "128-byte swizzle 的分组要求": eight rows reading the same column should
+    hit eight distinct bank sectors, and a narrower atom is the fallback when 128 B do not fit),
+    and, by the 128B rule of "TMA 如何写入 swizzled layout", that sectors move inside their own
+    row by a pattern that depends on row % 8 only.  Checked on the W2 images against the
+    unswizzled image: each 16-byte unit stays in its span-byte row, its new place depends on
+    (row % 8, column) alone, and any eight consecutive rows put a column in eight distinct bank
+    sectors.  Unswizzled rows of this width reach only 16 * 8 / span distinct sectors."""
+    x = workloads.w2_tensor()
+    ng = 128 // gcols
+    units = span // 16
+    for start in [(0, 0, 0), (0, 0, ng)]:
+        none = oracle.image(w2_map(x, 0, gcols, groups=256 // gcols), start).reshape(-1, units, 16)
+        sw = oracle.image(w2_map(x, span, gcols, groups=256 // gcols), start).reshape(-1, units, 16)
+        rows = none.shape[0]
+        place = np.empty((rows, units), np.int64)
+        for r in range(rows):
+            for c in range(units):
+                hit = [k for k in range(units) if bytes(sw[r, k]) == bytes(none[r, c])]
+                assert len(hit) == 1  # the unit is found in its own row, exactly once
+                place[r, c] = hit[0]
+        for r in range(8, rows):
+            np.testing.assert_array_equal(place[r], place[r % 8])
+        for r0 in range(rows - 7):
+            for c in range(units):
+                sectors = {((r * span + place[r, c] * 16) >> 4) & 7 for r in range(r0, r0 + 8)}
+                plain = {((r * span + c * 16) >> 4) & 7 for r in range(r0, r0 + 8)}
+                assert len(sectors) == 8
+                assert len(plain) == 16 * 8 // span
+
+
 # ---- swizzle function invariants ------------------------------------------------------------
 @pytest.mark.parametrize("span", [32, 64, 128])
 def test_swizzle_is_involution_and_bijection(span):
