@@ -116,8 +116,6 @@ extern "C" int tiled_copy_noalloc(const tm_desc* src, const int32_t* coords, siz
     using namespace tmk;
     if (!src || src->magic != TM_DESC_MAGIC)
         return set_last_error(TM_EINVAL, "source descriptor is not filled");
-    if (!images) return set_last_error(TM_EINVAL, "images is NULL");
-    if ((uintptr_t)images % 16) return set_last_error(TM_EALIGN, "images must be 16-byte aligned");
     if (!coords && nbox != 0 && nbox != src->num_boxes)
         return set_last_error(TM_EINVAL, "nbox is neither 0 nor the grid's box count");
     if (coords && nbox > kMaxBoxes) {
@@ -127,7 +125,9 @@ extern "C" int tiled_copy_noalloc(const tm_desc* src, const int32_t* coords, siz
         return set_last_error(TM_ERANGE, msg);
     }
     const uint64_t n = coords ? nbox : src->num_boxes;
-    if (n == 0) return TM_OK;
+    if (n == 0) return TM_OK;  // an empty box list moves nothing and needs no image buffer
+    if (!images) return set_last_error(TM_EINVAL, "images is NULL");
+    if ((uintptr_t)images % 16) return set_last_error(TM_EALIGN, "images must be 16-byte aligned");
     Dev* d = nullptr;
     int rc = setup(&d);
     if (rc) return rc;

@@ -297,13 +297,13 @@ int check_launch(cudaError_t e, const char* what)
 int copy_boxes(const tm_desc* src, const int32_t* coords, size_t nbox, void* images, void* stream)
 {
     if (!valid_desc(src)) return fail(TM_EINVAL, "source descriptor is not filled");
-    if (!images) return fail(TM_EINVAL, "images is NULL");
-    if ((uintptr_t)images % 16) return fail(TM_EALIGN, "images must be 16-byte aligned");
     if (!coords && nbox != 0 && nbox != src->num_boxes)
         return fail(TM_EINVAL, "nbox %zu is neither 0 nor the grid's %llu boxes", nbox,
                     (unsigned long long)src->num_boxes);
     const uint64_t n = coords ? nbox : src->num_boxes;
-    if (n == 0) return TM_OK;
+    if (n == 0) return TM_OK;  // an empty box list moves nothing and needs no image buffer
+    if (!images) return fail(TM_EINVAL, "images is NULL");
+    if ((uintptr_t)images % 16) return fail(TM_EALIGN, "images must be 16-byte aligned");
     DevState* ds = nullptr;
     int rc = device_state(&ds);
     if (rc) return rc;
@@ -557,13 +557,13 @@ int tiled_roundtrip(const tm_desc* dst, const int32_t* coords, size_t nbox, cons
                     void* stream)
 {
     if (!valid_desc(dst)) return fail(TM_EINVAL, "destination descriptor is not filled");
-    if (!images) return fail(TM_EINVAL, "images is NULL");
-    if ((uintptr_t)images % 16) return fail(TM_EALIGN, "images must be 16-byte aligned");
     if (!coords && nbox != 0 && nbox != dst->num_boxes)
         return fail(TM_EINVAL, "nbox %zu is neither 0 nor the grid's %llu boxes", nbox,
                     (unsigned long long)dst->num_boxes);
     const uint64_t n = coords ? nbox : dst->num_boxes;
-    if (n == 0) return TM_OK;
+    if (n == 0) return TM_OK;  // an empty box list moves nothing and needs no image buffer
+    if (!images) return fail(TM_EINVAL, "images is NULL");
+    if ((uintptr_t)images % 16) return fail(TM_EALIGN, "images must be 16-byte aligned");
     DevState* ds = nullptr;
     int rc = device_state(&ds);
     if (rc) return rc;

@@ -186,7 +186,8 @@ int tile_load_image(const tm_desc* src, const int32_t* coords, void* image, void
  *   k[i] * box[i]; nbox must be 0 or num_boxes.  Otherwise coords holds nbox * rank int32 (host).
  *   Each box is one TMA load completed through an mbarrier byte count ([MLSys-TMA] §"如何等待 TMA
  *   load 完成") and one bulk store of the image completed through a bulk async group.  `images`:
- *   device, nbox * box_bytes, 16-byte aligned. */
+ *   device, nbox * box_bytes, 16-byte aligned.  An empty list (coords != NULL, nbox == 0)
+ *   returns TM_OK at once, launches nothing and may pass images == NULL. */
 int tiled_copy(const tm_desc* src, const int32_t* coords, size_t nbox, void* images,
                void* stream);
 
@@ -198,7 +199,8 @@ int tiled_copy(const tm_desc* src, const int32_t* coords, size_t nbox, void* ima
  *   globalDim[0] * esize is not a multiple of 16 (or a box list starting off the 16-byte grid or
  *   outside the tensor) is stored by the vector path instead, which writes exactly the in-bounds
  *   bytes.  So is a map with an elementStride other than 1: image element e goes back to tensor
- *   coordinate start + e * elementStrides, and no other element is written. */
+ *   coordinate start + e * elementStrides, and no other element is written.  An empty list
+ *   (coords != NULL, nbox == 0) returns TM_OK at once and may pass images == NULL. */
 int tiled_roundtrip(const tm_desc* dst, const int32_t* coords, size_t nbox, const void* images,
                     void* stream);
 

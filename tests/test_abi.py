@@ -154,6 +154,22 @@ def test_calls_reject_unfilled_descriptors(tm):
     assert e.value.code == tm.TM_ERANGE
 
 
+def test_empty_box_list_is_a_no_op(tm):
+    """An empty box list (coords given, nbox 0) returns at once without touching the device, so
+    it needs no image buffer; a non-empty list still needs one."""
+    m = plan(tm)
+    tm.tiled_copy(m, [], None, stream=0)
+    tm.tiled_roundtrip(m, [], None, stream=0)
+    tm.tiled_copy_noalloc(m, [], None, stream=0)
+    for call in (tm.tiled_copy, tm.tiled_roundtrip, tm.tiled_copy_noalloc):
+        with pytest.raises(tm.TmapError) as e:
+            call(m, [[0, 0]], None, stream=0)
+        assert e.value.code == tm.TM_EINVAL
+    with pytest.raises(tm.TmapError) as e:  # the whole grid is never empty
+        tm.tiled_copy(m, None, None, stream=0)
+    assert e.value.code == tm.TM_EINVAL
+
+
 def test_plan_element_strides_and_nan_fill(tm):
     """Image extents are ceil(box / elementStrides); the box grid keeps stepping by the box."""
     m = plan(tm, element_strides=[1, 3], oob=tm.TM_OOB_NAN)
