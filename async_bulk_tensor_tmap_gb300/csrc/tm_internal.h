@@ -276,7 +276,7 @@ struct RingArgs {
     uint32_t prefetch;       // tiles ahead of the ring prefetched into L2 (0 = none)
     uint32_t groups;         // consumer groups (1, or 2 when stages is even)
     uint32_t row_pairs;      // 1: lanes read rows two apart (the ungrouped 256-byte-row control)
-    uint32_t pad;
+    uint32_t evict_first;    // 1: tile loads carry an L2 evict-first policy (each tile is read once)
     float* cs_a;
     float* cs_b;
     unsigned long long* bits_a;

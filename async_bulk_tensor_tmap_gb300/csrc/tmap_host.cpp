@@ -712,7 +712,10 @@ int stream_tiles(const tm_desc* a, const tm_desc* b, uint32_t stages, float* cs_
     // Bank-conflict control (TM_RING_ROW_PAIRS=1): the consumers read the rows of each 32-row
     // block in the order an ungrouped 256-byte row stride would give; same results.
     r.row_pairs = env_u64("TM_RING_ROW_PAIRS", 0) ? 1u : 0u;
-    r.pad = 0;
+    // Each tile is read once: its loads carry an L2 evict-first policy, so the stream recycles its
+    // own L2 lines rather than evicting (and forcing the write-back of) other data
+    // (TM_RING_EVICT_FIRST=0 drops the policy).
+    r.evict_first = env_u64("TM_RING_EVICT_FIRST", 1) ? 1u : 0u;
     r.cs_a = cs_a;
     r.cs_b = cs_b;
     r.bits_a = (unsigned long long*)bits_a;

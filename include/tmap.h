@@ -235,7 +235,9 @@ int tile_reduce(const tm_desc* dst, const tm_desc* src, tm_redop op, void* strea
  *   stages: 2..8.  With an even stage count two consumer groups take the even and the odd tiles
  *   (TM_RING_GROUPS=1 keeps one); TM_RING_ROW_PAIRS=1 reads each 32-row block in the row order of
  *   an ungrouped 256-byte row (the 2-way bank-conflict control of [MLSys-TMA] §"128-byte swizzle
- *   的分组要求").  Neither changes the outputs. */
+ *   的分组要求").  Each tile is read once, so the tile loads carry an L2 evict-first policy: the
+ *   stream recycles its own L2 lines instead of evicting other data (TM_RING_EVICT_FIRST=0 drops
+ *   the policy).  None of these changes the outputs. */
 int stream_tiles(const tm_desc* a, const tm_desc* b, uint32_t stages, float* cs_a, float* cs_b,
                  uint64_t* bits_a, uint64_t* bits_b, void* stream);
 
