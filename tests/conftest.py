@@ -8,6 +8,15 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+@pytest.fixture(autouse=True)
+def _guard_bands():
+    """After each test, the guard bands around the device buffers it made are intact."""
+    yield
+    gpu_util = sys.modules.get("gpu_util")
+    if gpu_util is not None and gpu_util._guarded:
+        gpu_util.check_guards()
+
+
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a GB300 (sm_103a) and the built CUDA library")
 

@@ -10,10 +10,49 @@ SPAN_TO_SW = {0: 0, 32: 1, 64: 2, 128: 3}
 ESIZE_TO_DTYPE = {1: 0, 2: 9, 4: 7, 8: 4}  # u8, bf16, f32, u64: copies are bitwise
 
 
+# Canary guard bands: every device buffer a test hands to the library (inputs, images, sentinel
+# destinations) sits between two GUARD-byte bands of CANARY bytes; check_guards() (run after every
+# test by the autouse fixture in conftest.py) fails the test if a kernel wrote into one.
+GUARD = 4096
+CANARY = 0xE7
+_guarded = []
+
+
+def guarded(nbytes: int, fill: int):
+    """A uint8 device tensor of nbytes (16-byte aligned: the bands are 4 KiB) filled with `fill`,
+    inside a larger buffer whose GUARD bytes on each side hold CANARY."""
+    import torch
+    buf = torch.full((GUARD + nbytes + GUARD,), CANARY, dtype=torch.uint8, device="cuda")
+    body = buf[GUARD:GUARD + nbytes]
+    body.fill_(fill)
+    _guarded.append((buf, nbytes))
+    return body
+
+
+def check_guards():
+    """Every guard band still holds its canary bytes; forgets the buffers afterwards."""
+    import torch
+    try:
+        for buf, nbytes in _guarded:
+            lo, hi = buf[:GUARD], buf[GUARD + nbytes:]
+            assert bool((lo == CANARY).all()) and bool((hi == CANARY).all()), (
+                f"a kernel wrote into the guard band of a {nbytes}-byte buffer")
+    finally:
+        _guarded.clear()
+        torch.cuda.synchronize()
+
+
 def to_dev(arr: np.ndarray):
     import torch
     flat = np.ascontiguousarray(arr).reshape(-1).view(np.uint8)
-    return torch.from_numpy(flat.copy()).cuda()
+    t = guarded(flat.size, 0)
+    t.copy_(torch.from_numpy(flat))
+    return t
+
+
+def full_like(t, fill: int):
+    """A guarded device buffer of t's byte size filled with `fill` (a sentinel destination)."""
+    return guarded(t.numel() * t.element_size(), fill)
 
 
 def to_host(t) -> np.ndarray:
@@ -42,8 +81,7 @@ def host_map(arr: np.ndarray, r, offset=0, dtype=None):
 
 
 def empty_images(n_boxes: int, box_bytes: int, fill: int = 0x5A):
-    import torch
-    return torch.full((n_boxes * box_bytes,), fill, dtype=torch.uint8, device="cuda")
+    return guarded(n_boxes * box_bytes, fill)
 
 
 U = {1: np.uint8, 2: np.uint16, 4: np.uint32, 8: np.uint64}

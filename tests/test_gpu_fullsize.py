@@ -8,7 +8,7 @@ import pytest
 
 import oracle
 import workloads
-from gpu_util import dev_map, host_map, to_dev, to_host
+from gpu_util import dev_map, full_like, guarded, host_map, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -50,7 +50,7 @@ def test_w3_full_copy_and_roundtrip(tm):
     tm.tiled_copy(m, None, imgs)
     check(tm)
     assert_sampled_images(imgs, host_map(x, r), sample_boxes(m.num_boxes, 64, 3))
-    dst = torch.full_like(xd, 0x5C)
+    dst = full_like(xd, 0x5C)
     tm.tiled_roundtrip(dev_map(tm, dst, r), None, imgs)
     check(tm)
     assert torch.equal(dst, xd)
@@ -106,10 +106,10 @@ def test_w5b_full_ring_every_tile(tm):
     ad, bd = to_dev(a), to_dev(b)
     ma, mb = dev_map(tm, ad, ra), dev_map(tm, bd, rb)
     n = ma.num_boxes
-    cs_a = torch.zeros(n, dtype=torch.float32, device="cuda")
-    cs_b = torch.zeros_like(cs_a)
-    bits_a = torch.zeros(n, dtype=torch.int64, device="cuda")
-    bits_b = torch.zeros_like(bits_a)
+    cs_a = guarded(4 * n, 0).view(torch.float32)
+    cs_b = guarded(4 * n, 0).view(torch.float32)
+    bits_a = guarded(8 * n, 0).view(torch.int64)
+    bits_b = guarded(8 * n, 0).view(torch.int64)
     tm.stream_tiles(ma, mb, 4, cs_a, cs_b, bits_a, bits_b)
     check(tm)
     wa, wb, wba, wbb = oracle.stream_checksums(host_map(a, ra), host_map(b, rb),

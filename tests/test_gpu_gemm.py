@@ -10,7 +10,7 @@ import numpy as np
 import pytest
 
 import oracle
-from gpu_util import to_host
+from gpu_util import guarded, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -50,7 +50,7 @@ def run(tm, a, b, stages=4, ldc=None):
     ad = torch.from_numpy(a.reshape(-1).view(np.uint8).copy()).cuda()
     bd = torch.from_numpy(b.reshape(-1).view(np.uint8).copy()).cuda()
     ldc = N if ldc is None else ldc
-    c = torch.full((M * ldc,), float("nan"), dtype=torch.float32, device="cuda")
+    c = guarded(4 * M * ldc, 0xFF).view(torch.float32)  # all-ones bytes: a NaN in every float
     ma = tm.tmap_encode(tm.TM_BF16, ad, [K, M], [K * 2], [64, 128], swizzle=tm.TM_SWIZZLE_128B)
     mb = tm.tmap_encode(tm.TM_BF16, bd, [K, N], [K * 2], [64, 256], swizzle=tm.TM_SWIZZLE_128B)
     tm.stream_gemm(ma, mb, c, ldc=ldc, stages=stages)

@@ -10,7 +10,8 @@ import pytest
 
 import oracle
 import workloads
-from gpu_util import assert_nan_fill, dev_map, empty_images, host_map, to_dev, to_host
+from gpu_util import (assert_nan_fill, dev_map, empty_images, full_like, guarded, host_map, to_dev,
+                      to_host)
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +50,7 @@ def test_w1_image_and_roundtrip(tm, span, start):
     want = oracle.image(host_map(x, r), start)
     np.testing.assert_array_equal(to_host(img), want)
     # round trip into a sentinel-filled tensor: only the box's elements change
-    dst = torch.full((16 * 128 * 2,), 0xEE, dtype=torch.uint8, device="cuda")
+    dst = guarded(16 * 128 * 2, 0xEE)
     md = dev_map(tm, dst, r, dtype=tm.TM_F16)
     tm.tiled_roundtrip(md, [list(start)], img)
     check(tm)
@@ -107,7 +108,7 @@ def test_w3_copy_and_roundtrip(tm, span, force_fallback):
     check(tm)
     want = oracle.tiled_copy(host_map(x, r), threads=8)
     np.testing.assert_array_equal(to_host(imgs), want)
-    dst = torch.full_like(xd, 0x77)
+    dst = full_like(xd, 0x77)
     md = dev_map(tm, dst, r)
     if force_fallback:
         tm.tmap_force_fallback(md)
@@ -154,7 +155,7 @@ def test_small_boxes_share_stages(tm, box, span):
     check(tm)
     want = oracle.tiled_copy(host_map(x, r), threads=8)
     np.testing.assert_array_equal(to_host(imgs), want)
-    dst = torch.full_like(xd, 0x77)
+    dst = full_like(xd, 0x77)
     tm.tiled_roundtrip(dev_map(tm, dst, r), None, imgs)
     check(tm)
     assert torch.equal(dst, xd)
@@ -198,7 +199,7 @@ def test_unaligned_base_takes_fallback(tm):
     check(tm)
     want = oracle.tiled_copy(host_map(raw, r, offset=8))
     np.testing.assert_array_equal(to_host(imgs), want)
-    out = torch.full_like(rd, 0x33)
+    out = full_like(rd, 0x33)
     mo = dev_map(tm, out, r, offset=8)
     tm.tiled_roundtrip(mo, None, imgs)
     check(tm)
@@ -227,7 +228,7 @@ def test_box_lists(tm, nbox, kind):
     want = oracle.tiled_copy(host_map(x, r), coords=coords)
     np.testing.assert_array_equal(to_host(imgs), want)
     # write the images back through the list into a sentinel tensor (boxes do not overlap)
-    dst = torch.full_like(xd, 0x44)
+    dst = full_like(xd, 0x44)
     md = dev_map(tm, dst, r)
     tm.tiled_roundtrip(md, coords, imgs)
     check(tm)
@@ -315,7 +316,7 @@ def test_vector_copy_forms(tm, monkeypatch, case, seg):
     # store direction: the oracle's images back into a sentinel-filled tensor (only in-bounds
     # elements are written; padding and everything outside the map keep the sentinel)
     hin = torch.from_numpy(want.copy()).cuda()
-    dst = torch.full_like(xd, 0xA5)
+    dst = full_like(xd, 0xA5)
     tm.tiled_roundtrip(dev_map(tm, dst, r, offset=offset, dtype=dt), None, hin)
     check(tm)
     hdst = np.full(xd.numel(), 0xA5, np.uint8)
@@ -350,10 +351,10 @@ def test_w5b_ring_checksums(tm, span, stages):
     ma, mb = dev_map(tm, ad, ra), dev_map(tm, bd, rb)
     n = ma.num_boxes
     assert n == mb.num_boxes == 12
-    cs_a = torch.zeros(n, dtype=torch.float32, device="cuda")
-    cs_b = torch.zeros_like(cs_a)
-    bits_a = torch.zeros(n, dtype=torch.int64, device="cuda")
-    bits_b = torch.zeros_like(bits_a)
+    cs_a = guarded(4 * n, 0).view(torch.float32)
+    cs_b = guarded(4 * n, 0).view(torch.float32)
+    bits_a = guarded(8 * n, 0).view(torch.int64)
+    bits_b = guarded(8 * n, 0).view(torch.int64)
     tm.stream_tiles(ma, mb, stages, cs_a, cs_b, bits_a, bits_b)
     check(tm)
     wa, wb, wba, wbb = oracle.stream_checksums(host_map(a, ra), host_map(b, rb))
@@ -384,10 +385,10 @@ def test_w5b_ring_many_laps(tm, monkeypatch, rows, mode):
     ma, mb = dev_map(tm, ad, r), dev_map(tm, bd, r)
     n = ma.num_boxes
     assert n == 5 * -(-m // rows) and n > 1000
-    cs_a = torch.zeros(n, dtype=torch.float32, device="cuda")
-    cs_b = torch.zeros_like(cs_a)
-    bits_a = torch.zeros(n, dtype=torch.int64, device="cuda")
-    bits_b = torch.zeros_like(bits_a)
+    cs_a = guarded(4 * n, 0).view(torch.float32)
+    cs_b = guarded(4 * n, 0).view(torch.float32)
+    bits_a = guarded(8 * n, 0).view(torch.int64)
+    bits_b = guarded(8 * n, 0).view(torch.int64)
     tm.stream_tiles(ma, mb, stages, cs_a, cs_b, bits_a, bits_b)
     check(tm)
     wa, wb, wba, wbb = oracle.stream_checksums(host_map(a, r), host_map(b, r),
@@ -441,7 +442,7 @@ def test_brute_force_tiny(tm, monkeypatch, span, aligned, seg):
         # whole grid, then back into a sentinel copy
         g = empty_images(m.num_boxes, m.box_bytes)
         tm.tiled_copy(m, None, g)
-        dst = torch.full_like(xd, 0xC3)
+        dst = full_like(xd, 0xC3)
         md = dev_map(tm, dst, r)
         tm.tiled_roundtrip(md, None, g)
         check(tm)
@@ -463,7 +464,7 @@ def test_store_keeps_padding_after_a_ragged_row_end(tm):
             m = dev_map(tm, xd, r)
             g = empty_images(m.num_boxes, m.box_bytes)
             tm.tiled_copy(m, None, g)
-            dst = torch.full_like(xd, 0xC3)
+            dst = full_like(xd, 0xC3)
             tm.tiled_roundtrip(dev_map(tm, dst, r), None, g)
             check(tm)
             hdst = np.full_like(x, 0xC3)
@@ -501,7 +502,7 @@ def test_big_boxes_single_stage(tm, force_fallback):
     check(tm)
     want = oracle.tiled_copy(host_map(x, r))
     np.testing.assert_array_equal(to_host(imgs), want)
-    dst = torch.full_like(xd, 0x66)
+    dst = full_like(xd, 0x66)
     md = dev_map(tm, dst, r)
     if force_fallback:
         tm.tmap_force_fallback(md)
@@ -519,6 +520,20 @@ def test_big_boxes_single_stage(tm, force_fallback):
     hd = d.copy()
     oracle.tile_reduce_add(host_map(hd, rr), host_map(s, rr))
     np.testing.assert_array_equal(to_host(dd).view(np.uint32), hd.reshape(-1).view(np.uint32))
+
+
+def test_guard_bands_catch_a_stray_byte():
+    """The guard check that runs after every GPU test sees a byte written just past a buffer (and
+    just before one).  The stray bytes are written by torch into the guard band itself, which is
+    allocated memory, so nothing here accesses memory out of bounds."""
+    import gpu_util
+    for where in ("after", "before"):
+        body = gpu_util.guarded(64, 0)
+        buf = gpu_util._guarded[-1][0]
+        buf[gpu_util.GUARD + 64 if where == "after" else gpu_util.GUARD - 1] = 1
+        with pytest.raises(AssertionError):
+            gpu_util.check_guards()
+        assert not gpu_util._guarded and int(body.sum()) == 0
 
 
 # ---- bounded waits: a wait that nothing completes gives up and reports, the GPU stays usable -----

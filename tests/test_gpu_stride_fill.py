@@ -12,7 +12,8 @@ import numpy as np
 import pytest
 
 import oracle
-from gpu_util import ESIZE, as_float, assert_nan_fill, dev_map, host_map, to_dev, to_host
+from gpu_util import (ESIZE, as_float, assert_nan_fill, dev_map, guarded, host_map, to_dev,
+                      to_host)
 
 pytestmark = pytest.mark.gpu
 
@@ -90,7 +91,7 @@ def test_strided_grid_copy(tm, name, force_fb):
         tm.tmap_force_fallback(m)
     om = host_map(buf, r)
     assert m.box_bytes == om.box_bytes and m.num_boxes == om.num_boxes
-    imgs = torch.full((m.num_boxes * m.box_bytes,), 0x5A, dtype=torch.uint8, device="cuda")
+    imgs = guarded(m.num_boxes * m.box_bytes, 0x5A)
     tm.tiled_copy(m, None, imgs)
     check(tm)
     np.testing.assert_array_equal(to_host(imgs), oracle.tiled_copy(om))
@@ -113,7 +114,7 @@ def test_strided_box_list(tm, name):
                 q = 16 // r["esize"]
                 c[0] = c[0] // q * q
             coords.append(c)
-        imgs = torch.zeros(len(coords) * m.box_bytes, dtype=torch.uint8, device="cuda")
+        imgs = guarded(len(coords) * m.box_bytes, 0)
         tm.tiled_copy(m, coords, imgs)
         check(tm)
         np.testing.assert_array_equal(to_host(imgs), oracle.tiled_copy(om, coords=coords),
@@ -139,11 +140,11 @@ def test_strided_noalloc_copy(tm, name):
     buf, r = setup_case(tm, name, seed=6)
     m = dev_map(tm, to_dev(buf), r)
     om = host_map(buf, r)
-    imgs = torch.zeros(m.num_boxes * m.box_bytes, dtype=torch.uint8, device="cuda")
+    imgs = guarded(m.num_boxes * m.box_bytes, 0)
     tm.tiled_copy_noalloc(m, None, imgs)
     np.testing.assert_array_equal(to_host(imgs), oracle.tiled_copy(om))
     coords = [[-2, 1] + [0] * (len(r["dims"]) - 2), [3, -1] + [1] * (len(r["dims"]) - 2)]
-    imgs2 = torch.zeros(2 * m.box_bytes, dtype=torch.uint8, device="cuda")
+    imgs2 = guarded(2 * m.box_bytes, 0)
     tm.tiled_copy_noalloc(m, coords, imgs2)
     np.testing.assert_array_equal(to_host(imgs2), oracle.tiled_copy(om, coords=coords))
 
@@ -184,7 +185,7 @@ def test_nan_fill_copy(tm, dt_name, span, steps, force_fb):
     assert m.path == tm.TM_PATH_TMA
     if force_fb:
         tm.tmap_force_fallback(m)
-    imgs = torch.zeros(m.num_boxes * m.box_bytes, dtype=torch.uint8, device="cuda")
+    imgs = guarded(m.num_boxes * m.box_bytes, 0)
     tm.tiled_copy(m, None, imgs)
     check(tm)
     want = oracle.tiled_copy(host_map(buf, r, dtype=dtype))
@@ -204,7 +205,7 @@ def test_nan_fill_pattern_same_on_both_paths(tm, dt_name):
         m = dev_map(tm, bd, r, dtype=dtype)
         if force_fb:
             tm.tmap_force_fallback(m)
-        imgs = torch.zeros(m.num_boxes * m.box_bytes, dtype=torch.uint8, device="cuda")
+        imgs = guarded(m.num_boxes * m.box_bytes, 0)
         q = 16 // r["esize"]  # starts on the 16-byte grid: the tensor-map path takes the list
         tm.tiled_copy(m, [[-q, -1, 0], [(r["dims"][0] - 3) // q * q, 30, 2]], imgs)
         check(tm)
@@ -230,7 +231,7 @@ def test_nan_fill_map_stores_and_reduces_in_bounds_only(tm, cut):
                        oracle.ADD)
     np.testing.assert_array_equal(to_host(dd), dst)
     m = dev_map(tm, sd, r, dtype=dtype)
-    imgs = torch.zeros(m.num_boxes * m.box_bytes, dtype=torch.uint8, device="cuda")
+    imgs = guarded(m.num_boxes * m.box_bytes, 0)
     tm.tiled_copy(m, None, imgs)
     out = np.full_like(src, 0x3C)
     od = to_dev(out)
