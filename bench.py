@@ -41,6 +41,7 @@ import workloads  # noqa: E402
 
 METRIC = "tiled copy / round-trip / reduce-add HBM GB/s on 1 GB300 and % of HBM peak"
 GB = 1e9
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e nominal bandwidth (about 8 TB/s), beside the measured peak
 FLUSH_BYTES = 512 << 20
 WORKLOAD = ("tmap hot path: W3 bf16 8192x8192 copy+roundtrip (128x64, 128B); W4 bf16 "
             "16x4095x1000 pitch 1024 rank-3 (1x64x64 128B, 1x64x32 64B) and rank-5 fallback view "
@@ -779,6 +780,7 @@ def main():
         ms = statistics.mean(per[name])
         breakdown[name] = {"ms": round(ms, 4), "GB/s": round(nbytes / ms / 1e6, 1),
                            "frac_of_peak": round(nbytes / ms / 1e6 / peak, 3),
+                           "frac_of_nominal": round(nbytes / ms / 1e6 / NOMINAL_HBM_GBS, 3),
                            "bytes": nbytes}
         if name == "w7.gemm":
             tflops = gemm_flops(h) / ms / 1e9
@@ -823,6 +825,7 @@ def main():
         "config": {"workload": WORKLOAD, "step_bytes": step_bytes,
                    "l2": "flushed by a 512 MiB device write before every kernel (not timed)",
                    "hbm_frac_of_peak": round(value / world / peak, 3),
+                   "hbm_frac_of_nominal": round(value / world / NOMINAL_HBM_GBS, 3),
                    "paths": {k: ("tma" if p == 1 else "fallback") for k, p in g.paths.items()
                              if not k.endswith("_out")}},
         "roofline": roofline,
