@@ -55,7 +55,9 @@ def parse():
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", default="tmap", choices=["tmap", "reference"])
-    p.add_argument("--e2e-steps", type=int, default=3)
+    p.add_argument("--e2e-steps", type=int, default=None,
+                   help="steps of the end-to-end leg (default: --steps, the same K as the device "
+                        "timing; 0 skips the leg)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--ops", default="", help="comma list of op names to run (default: all)")
     p.add_argument("--scale", type=float, default=1.0,
@@ -418,7 +420,7 @@ E2E_MAPS = {
 }
 
 
-def e2e_run(g: GpuWorkload, h: HostWorkload, ops, steps):
+def e2e_run(g: GpuWorkload, h: HostWorkload, ops, steps, warmup=1):
     """Same step through the public API with HOST buffers: every step copies its inputs from
     pinned host memory and its results back, inside the timed region.  Three streams pipeline the
     work group by group (inputs of group k+1 go in while group k computes and group k-1's results
@@ -488,7 +490,8 @@ def e2e_run(g: GpuWorkload, h: HostWorkload, ops, steps):
                 free[k][par] = ev_out
         nstep[0] += 1
 
-    step()
+    for _ in range(max(warmup, 1)):
+        step()
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
@@ -800,8 +803,10 @@ def main():
                     "traffic": None}
     if any(n.startswith(("w5c", "w6", "w7")) for n, _ in ops):
         args.e2e_steps = 0  # the widened ops have no end-to-end leg
+    if args.e2e_steps is None:
+        args.e2e_steps = args.steps
     if args.e2e_steps > 0:
-        e2e_ms, bi, bo = e2e_run(g, h, ops, args.e2e_steps)
+        e2e_ms, bi, bo = e2e_run(g, h, ops, args.e2e_steps, args.warmup)
         e2e = {"value": world * step_bytes / (e2e_ms * 1e-3) / GB, "unit": "GB/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
     else:
