@@ -367,16 +367,18 @@ def test_w5b_ring_checksums(tm, span, stages):
 # Many laps of the ring on every CTA: tiles of every supported height, ragged in both dims (296
 # columns = 4 full 64-column boxes + 40; rows not a multiple of the tile), with one consumer group,
 # two (even and odd tiles), and the row-pairs read order (the ungrouped bank-conflict control,
-# whose results must not change).  A and B are both M x 296, different seeds.
+# whose results must not change), and with the tile loads' L2 evict-first policy dropped (a cache
+# policy cannot change the bytes read).  A and B are both M x 296, different seeds.
 RING_LAPS_ROWS = {32: 32000 - 5, 64: 48000 - 7, 128: 32000 - 9, 256: 64000 - 11}
 
 
 @pytest.mark.parametrize("rows", [32, 64, 128, 256])
-@pytest.mark.parametrize("mode", ["two_groups", "one_group", "row_pairs"])
+@pytest.mark.parametrize("mode", ["two_groups", "one_group", "row_pairs", "no_evict_first"])
 def test_w5b_ring_many_laps(tm, monkeypatch, rows, mode):
     stages = 3 if rows == 256 else 4
     monkeypatch.setenv("TM_RING_GROUPS", "1" if mode == "one_group" else "2")
     monkeypatch.setenv("TM_RING_ROW_PAIRS", "1" if mode == "row_pairs" else "0")
+    monkeypatch.setenv("TM_RING_EVICT_FIRST", "0" if mode == "no_evict_first" else "1")
     m = RING_LAPS_ROWS[rows]
     a = workloads.normal_bf16((m, 296), 60 + rows)
     b = workloads.normal_bf16((m, 296), 61 + rows)
