@@ -781,7 +781,9 @@ def main():
     tpeak, tpeak_kind = measured_bf16_peak()
     for name, nbytes in ops:
         ms = statistics.mean(per[name])
-        breakdown[name] = {"ms": round(ms, 4), "GB/s": round(nbytes / ms / 1e6, 1),
+        breakdown[name] = {"ms": round(ms, 4), "ms_median": round(statistics.median(per[name]), 4),
+                           "ms_best": round(min(per[name]), 4),
+                           "GB/s": round(nbytes / ms / 1e6, 1),
                            "frac_of_peak": round(nbytes / ms / 1e6 / peak, 3),
                            "frac_of_nominal": round(nbytes / ms / 1e6 / NOMINAL_HBM_GBS, 3),
                            "bytes": nbytes}
@@ -823,6 +825,14 @@ def main():
         cpu = None if covered == 0 else {"value": covered / spent / GB, "unit": "GB/s", "cores": cores, "kind": "oracle",
                "sample": f"first {frac:.2%} of the boxes of every op ({covered} algorithmic "
                          f"bytes, {spent:.1f} s on {cores} threads)"}
+        if cpu is not None:  # the same oracle on one thread, beside the box-parallel figure
+            frac1 = calibrated_fraction(h, ops, 1, target_s=1.5)
+            spent1, covered1 = oracle_sample(h, ops, frac1, 1)
+            if covered1:
+                cpu["single_thread"] = {
+                    "value": covered1 / spent1 / GB, "cores": 1,
+                    "sample": f"first {frac1:.3%} of the boxes of every op ({covered1} algorithmic "
+                              f"bytes, {spent1:.1f} s on 1 thread)"}
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
