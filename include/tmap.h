@@ -73,7 +73,9 @@ typedef enum tm_oob { TM_OOB_ZERO = 0, TM_OOB_NAN = 1 } tm_oob;
 
 /* ---- execution paths ------------------------------------------------------------------------ */
 #define TM_PATH_TMA 1      /* cp.async.bulk.tensor with a driver-encoded tensor map               */
-#define TM_PATH_FALLBACK 2 /* 16-byte vector loads/stores + warp shuffles where TMA cannot go     */
+#define TM_PATH_FALLBACK 2 /* the vector path where TMA cannot go: aligned 16-byte windows or
+                            * bulk-copied row segments staged in shared memory, realigned
+                            * there, written with 16-byte vector stores                      */
 /* why a descriptor is on the fallback path (bit set in tm_desc.why_fallback) */
 #define TM_WHY_STRIDE 1u   /* a global stride is not a multiple of 16 bytes ([H200-TMA] §03)     */
 #define TM_WHY_BASE 2u     /* the base address is not 16-byte aligned ([H200-TMA] §03)           */
