@@ -40,6 +40,20 @@ def test_library_exports_every_declared_call(tm):
         assert hasattr(lib, n), n
 
 
+def test_package_refuses_to_import_without_the_library(tmp_path):
+    """No CPU fallback: a copy of the package without its CUDA library fails at import."""
+    import shutil
+    import subprocess
+    import sys
+    pkg = tmp_path / "async_bulk_tensor_tmap_gb300"
+    pkg.mkdir()
+    shutil.copy(os.path.join(ROOT, "async_bulk_tensor_tmap_gb300", "__init__.py"), pkg)
+    r = subprocess.run([sys.executable, "-c", "import async_bulk_tensor_tmap_gb300"],
+                       cwd=tmp_path, capture_output=True, text=True)
+    assert r.returncode != 0
+    assert "ImportError" in r.stderr and "is missing" in r.stderr
+
+
 def test_desc_layout(tm):
     assert tm._L.tm_desc_size() == 384
     m = tm.TensorMap()
