@@ -524,7 +524,9 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_store(const __grid_co
     const uint32_t row_bytes = s.row_bytes;
     const uint32_t ct = threadIdx.x - 32;
     constexpr uint32_t kCT = 32 * kSegConsumerWarps;
-    const uint32_t rc = s.run * cpr;  // chunks per tensor row of the run
+    // Chunks per tensor row of the run that hold tensor bytes: the run's images cover the whole
+    // row and more (its last box may reach past the tensor), and a store writes only the row.
+    const uint32_t rc = min(s.run * cpr, (row_bytes + 15) / 16);
     const uint32_t r_start = ct / rc, c_start = ct - r_start * rc;
     const uint32_t r_step = kCT / rc, c_step = kCT - r_step * rc;
     uint32_t sb = 0, sparity = 0;
