@@ -276,6 +276,55 @@ def test_w4_ragged_and_fallback(tm, variant):
     assert torch.equal(dst, xd)
 
 
+# Tensor-map path at ranks 3-5, sizes that give every CTA several box groups: fp32 maps whose
+# strides carry padding between dims (all multiples of 16 bytes, so TMA takes them), ragged along
+# every dim.  Copy, round trip into a sentinel tensor (padding and the gaps between dims keep their
+# bytes), and reduce-add, each against the oracle.
+def _high_rank(dims, box, pads):
+    strides, st = [], dims[0] * 4
+    for i in range(1, len(dims)):
+        st += pads[i - 1]
+        strides.append(st)
+        st *= dims[i]
+    return dict(dims=dims, strides=strides, box=box, esize=4), st
+
+
+HIGH_RANK = {
+    "r3": _high_rank([100, 3000, 21], [32, 16, 3], [16, 32]),
+    "r4": _high_rank([100, 33, 17, 50], [32, 8, 4, 2], [16, 64, 16]),
+    "r5": _high_rank([200, 9, 13, 11, 40], [32, 2, 2, 2, 2], [16, 32, 48, 16]),
+}
+
+
+@pytest.mark.parametrize("case", sorted(HIGH_RANK))
+@pytest.mark.parametrize("span", [0, 128])
+def test_high_rank_tensor_maps(tm, case, span):
+    recipe, nbytes = HIGH_RANK[case]
+    r = dict(recipe, span=span)
+    d, src = workloads.w5a_tensors(1, nbytes // 4, seed_dst=200 + len(r["dims"]),
+                                   seed_src=210 + len(r["dims"]))
+    xd = to_dev(d)
+    m = dev_map(tm, xd, r)
+    assert m.path == tm.TM_PATH_TMA and m.num_boxes > 2000
+    imgs = empty_images(m.num_boxes, m.box_bytes)
+    tm.tiled_copy(m, None, imgs)
+    check(tm)
+    want = oracle.tiled_copy(host_map(d, r), threads=8)
+    np.testing.assert_array_equal(to_host(imgs), want)
+    dst = full_like(xd, 0xC3)
+    tm.tiled_roundtrip(dev_map(tm, dst, r), None, imgs)
+    check(tm)
+    host_dst = np.full(nbytes, 0xC3, np.uint8)
+    oracle.tiled_roundtrip(host_map(host_dst, r), want, threads=8)
+    np.testing.assert_array_equal(to_host(dst), host_dst)
+    sd = to_dev(src)
+    tm.tile_reduce_add(m, dev_map(tm, sd, r))
+    check(tm)
+    hd = d.copy()
+    oracle.tile_reduce_add(host_map(hd, r), host_map(src, r), threads=8)
+    np.testing.assert_array_equal(to_host(xd), hd.reshape(-1).view(np.uint8))
+
+
 # The vector path's two forms on the same maps: per-window staging and per-thread image loads
 # (TM_FB_SEG=0) and segments (TM_FB_SEG=1: contiguous runs of tensor rows or image rows moved by
 # bulk copies, realigned by consumer warps).  Ragged boxes along every dim, NaN fill, a base 2
