@@ -32,6 +32,31 @@
 
 namespace tmk {
 
+// Counters of box b of the grid (as grid_counters), with 32-bit divisions whenever b and the box
+// counts fit in 32 bits: this runs before a CTA's first load.
+__device__ __forceinline__ void first_counters(const BoxWalk& w, uint64_t b, uint32_t* k)
+{
+    bool narrow = b <= 0xffffffffull;
+#pragma unroll
+    for (int i = 0; i < 5; i++) narrow = narrow && w.grid_nb[i] <= 0xffffffffull;
+    if (!narrow) {
+        grid_counters(w, b, k);
+        return;
+    }
+    uint32_t x = (uint32_t)b;
+#pragma unroll
+    for (int i = 0; i < 5; i++) {
+        if (i < (int)w.rank) {
+            const uint32_t nb = (uint32_t)w.grid_nb[i];
+            const uint32_t q = x / nb;
+            k[i] = x - q * nb;
+            x = q;
+        } else {
+            k[i] = 0;
+        }
+    }
+}
+
 template <int R, int KIND>
 __global__ void __launch_bounds__(32, 1)
     k_tma_stream(const __grid_constant__ CUtensorMap in_map,
@@ -45,10 +70,9 @@ __global__ void __launch_bounds__(32, 1)
     // Work unit: a group of `a.group` consecutive boxes sharing one stage (their images are
     // consecutive in the tile-major buffer as well).
     const uint64_t G = a.group;
-    const uint64_t ngroups = (a.walk.nbox + G - 1) / G;
     const uint64_t first = blockIdx.x;
-    if (ngroups <= first) return;
-    const uint64_t n_local = (ngroups - 1 - first) / gridDim.x + 1;
+    if (a.ngroups <= first) return;
+    const uint64_t n_local = a.n_base + (first < a.n_rem ? 1u : 0u);
     const uint32_t S = a.stages;
     const uint32_t base = (smem_u32(smem_raw) + (kStageAlign - 1)) & ~(kStageAlign - 1);
 
@@ -71,12 +95,9 @@ __global__ void __launch_bounds__(32, 1)
         uint32_t s, phase;
         uint32_t k[5];
     };
-    uint32_t dstep[5] = {0, 0, 0, 0, 0};  // digits of G * gridDim.x boxes
+    const uint32_t* const dstep = a.dstep;  // digits of G * gridDim.x boxes (from the host)
     Cursor ld{0, 0, 0, {0, 0, 0, 0, 0}};
-    if (grid) {
-        grid_counters(a.walk, first * G, ld.k);
-        grid_counters(a.walk, (uint64_t)gridDim.x * G, dstep);
-    }
+    if (grid) first_counters(a.walk, first * G, ld.k);
     Cursor wr = ld;
     auto advance = [&](Cursor& c) {
         c.i++;

@@ -54,10 +54,33 @@ struct StreamArgs {
     uint32_t stages;
     uint32_t group;        // consecutive boxes per stage
     uint32_t slot_bytes;   // stage bytes per box: box_bytes rounded up to its swizzle period
-    uint32_t pad;
+    uint32_t n_rem;        // CTAs below n_rem take n_base + 1 groups, the others n_base
     uint64_t timeout_ns;
     StatusBlock* status;
+    // The launch-wide schedule, computed once on the host (stream_schedule) so that no CTA runs
+    // 64-bit divisions before its first load.
+    uint64_t ngroups;      // ceil(walk.nbox / group)
+    uint64_t n_base;       // ngroups / grid
+    uint32_t dstep[5];     // digits (radix: the grid's box counts) of grid * group boxes
+    uint32_t pad;
 };
+
+// Fills the schedule fields of a streaming launch over `grid` CTAs (walk and group already set).
+inline void stream_schedule(StreamArgs& a, uint32_t grid)
+{
+    a.ngroups = (a.walk.nbox + a.group - 1) / a.group;
+    a.n_base = a.ngroups / grid;
+    a.n_rem = (uint32_t)(a.ngroups % grid);
+    uint64_t b = (uint64_t)grid * a.group;
+    for (uint32_t i = 0; i < 5; i++) {
+        if (i < a.walk.rank) {
+            a.dstep[i] = (uint32_t)(b % a.walk.grid_nb[i]);
+            b /= a.walk.grid_nb[i];
+        } else {
+            a.dstep[i] = 0;
+        }
+    }
+}
 
 // Generic fallback kernels.
 struct FbArgs {

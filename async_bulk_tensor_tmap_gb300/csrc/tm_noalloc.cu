@@ -174,6 +174,7 @@ extern "C" int tiled_copy_noalloc(const tm_desc* src, const int32_t* coords, siz
         a.status = status;
         const uint64_t groups = (n + a.group - 1) / a.group;
         const uint32_t grid = (uint32_t)std::min<uint64_t>(groups, (uint64_t)d->sms * per_sm);
+        stream_schedule(a, grid);
         const CUtensorMap* m = (const CUtensorMap*)src->tmap;
         e = launch_tma_stream(KIND_COPY, src->rank, m, m, a, grid,
                               (size_t)a.stages * stage + kStageAlign, st);

@@ -283,6 +283,7 @@ StreamArgs stream_args(const tm_desc* d, const BoxWalk& w, uint64_t images, cons
     a.stage_bytes = stage_bytes_of((uint64_t)a.group * a.slot_bytes);
     g = tma_geometry(ds, (w.nbox + a.group - 1) / a.group, a.stage_bytes);
     a.stages = g.stages;
+    stream_schedule(a, g.grid);
     a.timeout_ns = wait_limit_ns();
     a.status = ds.status;
     return a;
