@@ -82,16 +82,29 @@ __device__ __forceinline__ Segment segment_of(const SegArgs& s, const int32_t* c
     return sg;
 }
 
-// Run u, row block q of item m; the run's first box start c.
-__device__ __forceinline__ void item_of(const SegArgs& s, uint64_t m, uint64_t& u, uint32_t& q,
-                                        int32_t* c)
+// Grid counters of box b (as grid_counters), in 32-bit divisions when b and the box counts fit:
+// this runs before a CTA's first bulk copy.
+__device__ __forceinline__ void item_counters(const BoxWalk& w, uint64_t b, uint32_t* k)
 {
-    u = m / s.nblk;
-    q = (uint32_t)(m - u * s.nblk);
-    uint32_t k[5];
-    grid_counters(s.f.walk, u * s.run, k);
+    bool narrow = b <= 0xffffffffull;
 #pragma unroll
-    for (int i = 0; i < 5; i++) c[i] = i < (int)s.f.walk.rank ? (int32_t)(k[i] * s.f.walk.box[i]) : 0;
+    for (int i = 0; i < 5; i++) narrow = narrow && w.grid_nb[i] <= 0xffffffffull;
+    if (!narrow) {
+        grid_counters(w, b, k);
+        return;
+    }
+    uint32_t x = (uint32_t)b;
+#pragma unroll
+    for (int i = 0; i < 5; i++) {
+        if (i < (int)w.rank) {
+            const uint32_t nb = (uint32_t)w.grid_nb[i];
+            const uint32_t q = x / nb;
+            k[i] = x - q * nb;
+            x = q;
+        } else {
+            k[i] = 0;
+        }
+    }
 }
 
 // The producer's walk over its CTA's items: run u, row block q and the grid counters k of the
@@ -101,11 +114,16 @@ struct ItemCursor {
     uint32_t q;
     uint32_t k[5];
 
+    // item m: run u = m / nblk, row block q = m % nblk, and the counters of the run's first box
     __device__ __forceinline__ void init(const SegArgs& s, uint64_t m)
     {
-        int32_t c[5];
-        item_of(s, m, u, q, c);
-        for (int i = 0; i < 5; i++) k[i] = i < (int)s.f.walk.rank ? (uint32_t)c[i] / s.f.walk.box[i] : 0;
+        if (m <= 0xffffffffull) {
+            u = (uint32_t)m / s.nblk;
+        } else {
+            u = m / s.nblk;
+        }
+        q = (uint32_t)(m - u * s.nblk);
+        item_counters(s.f.walk, u * s.run, k);
     }
     // start coordinates of the run's first box
     __device__ __forceinline__ void start(const SegArgs& s, int32_t* c) const
@@ -260,8 +278,7 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_copy(const __grid_con
     // row lies outside the tensor)
     int32_t* const tabs = reinterpret_cast<int32_t*>(smem_raw + (size_t)S * E * s.seg_stride);
 
-    const uint64_t T = s.nrun * s.nblk;
-    const uint64_t per = T / gridDim.x, extra = T % gridDim.x;
+    const uint64_t per = s.per, extra = s.extra;  // the item split, from the host
     const uint64_t m0 = blockIdx.x * per + (blockIdx.x < extra ? blockIdx.x : extra);
     const uint64_t total = per + (blockIdx.x < extra ? 1 : 0);
     if (total == 0) return;
@@ -446,8 +463,7 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_store(const __grid_co
     // per staging buffer, the tensor address of each image row's element 0 (~0: outside)
     uint64_t* const tabs = reinterpret_cast<uint64_t*>(smem_raw + S * stage_bytes);
 
-    const uint64_t T = s.nrun * s.nblk;
-    const uint64_t per = T / gridDim.x, extra = T % gridDim.x;
+    const uint64_t per = s.per, extra = s.extra;  // the item split, from the host
     const uint64_t m0 = blockIdx.x * per + (blockIdx.x < extra ? blockIdx.x : extra);
     const uint64_t total = per + (blockIdx.x < extra ? 1 : 0);
     if (total == 0) return;

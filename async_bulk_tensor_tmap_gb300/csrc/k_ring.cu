@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kRingThreads, 1)
 
     const uint64_t first = blockIdx.x;
     if (r.ntiles <= first) return;
-    const uint64_t n_local = (r.ntiles - 1 - first) / gridDim.x + 1;
+    const uint64_t n_local = r.n_base + (first < r.n_rem ? 1u : 0u);
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
 
@@ -125,8 +125,8 @@ __global__ void __launch_bounds__(kRingThreads, 1)
         struct TileCursor {
             uint64_t a0, a1, b0, b1;
         };
-        const uint32_t a_d0 = (uint32_t)(gridDim.x % r.a_nb0), b_d0 = (uint32_t)(gridDim.x % r.b_nb0);
-        const uint64_t a_d1 = gridDim.x / r.a_nb0, b_d1 = gridDim.x / r.b_nb0;
+        const uint32_t a_d0 = r.a_d0, b_d0 = r.b_d0;  // the grid step, from the host
+        const uint64_t a_d1 = r.a_d1, b_d1 = r.b_d1;
         auto cursor_at = [&](uint64_t i) {
             const uint64_t t = first + i * gridDim.x;
             return TileCursor{t % r.a_nb0, t / r.a_nb0, t % r.b_nb0, t / r.b_nb0};
@@ -145,7 +145,15 @@ __global__ void __launch_bounds__(kRingThreads, 1)
                 c.b1++;
             }
         };
-        TileCursor ld = cursor_at(0);
+        // The first tile (t = blockIdx.x) in 32-bit divisions when the box counts fit: this runs
+        // before the first load.
+        TileCursor ld;
+        if (r.a_nb0 <= 0xffffffffull && r.b_nb0 <= 0xffffffffull) {
+            const uint32_t t = blockIdx.x, na = (uint32_t)r.a_nb0, nb = (uint32_t)r.b_nb0;
+            ld = TileCursor{t % na, t / na, t % nb, t / nb};
+        } else {
+            ld = cursor_at(0);
+        }
         TileCursor pf = ld;
         uint64_t pf_i = 0;
         auto prefetch_to = [&](uint64_t upto) {  // prefetch tiles pf_i .. min(upto, n_local) - 1

@@ -214,6 +214,9 @@ struct SegArgs {
     uint32_t row_bytes;     // dim[0] * esize: tensor bytes of one row
     uint32_t img_stride;    // store: shared-memory bytes per box image block of an item
     uint32_t stages;        // staging buffers (items in flight per CTA)
+    uint64_t per;           // items per CTA: items / grid (CTAs below `extra` take one more),
+    uint32_t extra;         // computed on the host with the grid
+    uint32_t pad;
 };
 constexpr uint32_t kSegMinBytes = 512;  // shorter segments: the per-window copy (request rate)
 constexpr uint32_t kSegMaxGroups = 64;
@@ -262,6 +265,8 @@ inline bool seg_plan_rows(const FbArgs& a, uint64_t g1, uint32_t sms, uint32_t w
     const uint64_t items = s.nrun * s.nblk;
     const uint64_t ctas = (uint64_t)sms * per_sm;
     grid = (uint32_t)(items < ctas ? items : ctas);
+    s.per = items / grid;
+    s.extra = (uint32_t)(items % grid);
     smem = store ? (size_t)S * ((size_t)nb0 * s.img_stride + 8ull * s.block_groups * g1) + 16
                  : (size_t)S * s.block_groups * (s.seg_stride + 4 * g1) + 16;
     return true;
@@ -306,7 +311,23 @@ struct RingArgs {
     unsigned long long* bits_b;
     uint64_t timeout_ns;
     StatusBlock* status;
+    // The launch-wide schedule over `grid` CTAs, computed once on the host (ring_schedule).
+    uint64_t n_base;         // tiles per CTA: ntiles / grid (CTAs below n_rem take one more)
+    uint64_t a_d1, b_d1;     // grid / a_nb0, grid / b_nb0: a CTA's step in rows of boxes ...
+    uint32_t a_d0, b_d0;     // ... and grid % a_nb0, grid % b_nb0 in boxes along dim 0
+    uint32_t n_rem;
+    uint32_t pad2;
 };
+
+inline void ring_schedule(RingArgs& r, uint32_t grid)
+{
+    r.n_base = r.ntiles / grid;
+    r.n_rem = (uint32_t)(r.ntiles % grid);
+    r.a_d0 = (uint32_t)(grid % r.a_nb0);
+    r.a_d1 = grid / r.a_nb0;
+    r.b_d0 = (uint32_t)(grid % r.b_nb0);
+    r.b_d1 = grid / r.b_nb0;
+}
 
 // Tensor-core consumer of the k-ordered ring (stream_gemm): C = A * B^T.
 constexpr uint32_t kGemmMaxStages = 4;      // one-SM form: 48 KiB stages

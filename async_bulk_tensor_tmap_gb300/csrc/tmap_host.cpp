@@ -728,6 +728,7 @@ int stream_tiles(const tm_desc* a, const tm_desc* b, uint32_t stages, float* cs_
     uint32_t per_sm = 1;
     while (per_sm < 4 && cta_budget(*ds, per_sm + 1) >= smem) per_sm++;
     const uint32_t grid = (uint32_t)std::min<uint64_t>(r.ntiles, (uint64_t)ds->sms * per_sm);
+    ring_schedule(r, grid);
     return check_launch(launch_ring((const CUtensorMap*)a->tmap, (const CUtensorMap*)b->tmap, r, grid,
                                     smem, (cudaStream_t)stream),
                         "ring launch");
