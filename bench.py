@@ -809,14 +809,15 @@ def main():
         args.e2e_steps = args.steps
     if args.e2e_steps > 0:
         e2e_ms, bi, bo = e2e_run(g, h, ops, args.e2e_steps, args.warmup)
+        e2e_ms = max_over_ranks(e2e_ms, world)  # the whole job lasts as long as its slowest rank
         e2e = {"value": world * step_bytes / (e2e_ms * 1e-3) / GB, "unit": "GB/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo}
     else:
         e2e = None
     if rank != 0:
         return
-    if args.scale != 1:
-        args.no_cpu_baseline = True
+    if args.scale != 1 or world > 1:
+        args.no_cpu_baseline = True  # the oracle is timed at N = 1 on the full-size workload only
     cpu = None
     if not args.no_cpu_baseline:
         cores = cpu_cores()
