@@ -640,20 +640,63 @@ __device__ void fb_reduce_rows(const FbArgs& a)
     const uint32_t lane = threadIdx.x & 31;
     const uint64_t w0 = (uint64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const uint64_t nw = (uint64_t)gridDim.x * (kThreads / 32);
+    // The warp's items are w0, w0 + nw, ...: item it is piece seg of row `row`, whose counters
+    // over dims f.. are g[].  They are found by division once; each step then adds nw items as
+    // (rows dr, pieces ds) and the row step's digits dg[], with carries.
+    // (Loops run over the fixed 5 dims, guarded, so that g[] and dg[] stay in registers.)
+    const int rank = (int)a.walk.rank, f0 = (int)f;
+    uint64_t seg = w0 % segs;
+    uint64_t g[5] = {0, 0, 0, 0, 0}, dg[5] = {0, 0, 0, 0, 0};
+    {
+        uint64_t q = w0 / segs, qs = nw / segs;
+#pragma unroll
+        for (int i = 1; i < 5; i++) {
+            if (i >= f0 && i < rank) {
+                if (i + 1 < rank) {
+                    g[i] = q % a.dim[i];
+                    q /= a.dim[i];
+                    dg[i] = qs % a.dim[i];
+                    qs /= a.dim[i];
+                } else {  // the top digits take what is left (past the end: never used)
+                    g[i] = q;
+                    dg[i] = qs;
+                }
+            }
+        }
+    }
+    const uint64_t ds = nw % segs;
     for (uint64_t it = w0; it < items; it += nw) {
-        const uint64_t row = it / segs, seg = it - row * segs;
         int64_t od = 0, os = 0;
-        uint64_t q = row;
-        for (uint32_t i = f; i < a.walk.rank; i++) {
-            const uint64_t nxt = q / a.dim[i];
-            const int64_t g = (int64_t)(q - nxt * a.dim[i]);
-            q = nxt;
-            od += g * a.stride[i];
-            os += g * a.src_stride[i];
+#pragma unroll
+        for (int i = 1; i < 5; i++) {
+            if (i >= f0 && i < rank) {
+                od += (int64_t)g[i] * a.stride[i];
+                os += (int64_t)g[i] * a.src_stride[i];
+            }
+        }
+        const uint64_t cur_seg = seg;
+        // step to item it + nw
+        seg += ds;
+        uint64_t carry = 0;
+        if (seg >= segs) {
+            seg -= segs;
+            carry = 1;
+        }
+#pragma unroll
+        for (int i = 1; i < 5; i++) {
+            if (i >= f0 && i < rank) {
+                uint64_t v = g[i] + dg[i] + carry;
+                carry = 0;
+                if (i + 1 < rank && v >= a.dim[i]) {
+                    v -= a.dim[i];
+                    carry = 1;
+                }
+                g[i] = v;
+            }
         }
         uint8_t* const d = reinterpret_cast<uint8_t*>(a.base + od);
         const uint8_t* const sp = reinterpret_cast<const uint8_t*>(a.src_base + os);
-        const uint64_t b0 = seg * kSegBytes;
+        const uint64_t b0 = cur_seg * kSegBytes;
         const uint64_t b1 = min(b0 + kSegBytes, row_bytes);
         const uint32_t phase = (uint32_t)((uintptr_t)d & 15);
         uint64_t vs = b1, ve = b1;  // whole 16-byte vectors in [vs, ve) when both phases agree

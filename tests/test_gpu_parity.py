@@ -325,6 +325,27 @@ def test_high_rank_tensor_maps(tm, case, span):
     np.testing.assert_array_equal(to_host(xd), hd.reshape(-1).view(np.uint8))
 
 
+@pytest.mark.parametrize("case", sorted(HIGH_RANK))
+@pytest.mark.parametrize("op", ["add", "max"])
+def test_high_rank_vector_reduce(tm, case, op):
+    """The vector path's reduce over the same rank 3-5 maps (forced off the tensor reduce): its
+    rows are walked with counters over the outer dims stepped with carries."""
+    recipe, nbytes = HIGH_RANK[case]
+    r = dict(recipe, span=128)
+    d, src = workloads.w5a_tensors(1, nbytes // 4, seed_dst=220 + len(r["dims"]),
+                                   seed_src=230 + len(r["dims"]))
+    dd, sd = to_dev(d), to_dev(src)
+    md, ms = dev_map(tm, dd, r), dev_map(tm, sd, r)
+    tm.tmap_force_fallback(md)
+    code = tm.TM_RED_ADD if op == "add" else tm.TM_RED_MAX
+    tm.tile_reduce(md, ms, code)
+    check(tm)
+    hd = d.copy()
+    oracle.tile_reduce(host_map(hd, r), host_map(src, r), oracle.F32,
+                       oracle.ADD if op == "add" else oracle.MAX)
+    np.testing.assert_array_equal(to_host(dd), hd.reshape(-1).view(np.uint8))
+
+
 # The vector path's two forms on the same maps: per-window staging and per-thread image loads
 # (TM_FB_SEG=0) and segments (TM_FB_SEG=1: contiguous runs of tensor rows or image rows moved by
 # bulk copies, realigned by consumer warps).  Ragged boxes along every dim, NaN fill, a base 2
