@@ -192,36 +192,8 @@ __device__ __forceinline__ void tc_commit_pair(uint32_t bar_saddr)
         : "memory");
 }
 
-// ---- cluster multicast of the B tile (one-SM MMAs, two CTAs along M sharing B) ----------------
-// TMA tensor load of a box into the same shared-memory offset of every CTA in `mask`, completing on
-// the mbarrier at offset `bar` in each of them.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap* m, int32_t c0,
-                                                      int32_t c1, uint32_t bar, uint16_t mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar), "h"(mask)
-        : "memory");
-}
-
-// Arrives on the mbarrier at offset bar_saddr in every CTA of `mask` once every tcgen05 operation
-// this thread issued before has completed.
-__device__ __forceinline__ void tc_commit_multicast(uint32_t bar_saddr, uint16_t mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(bar_saddr),
-        "h"(mask)
-        : "memory");
-}
-
 }  // namespace
 
-// kMC: clusters of two CTAs along M share each B tile -- each CTA loads one 128-row half of it
-// (mb is then a map with a 128-row box) multicast into both CTAs' stages, and each CTA's MMA
-// commits release the stage in both CTAs (so neither refills a stage the other still reads).
-template <bool kMC>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm(const __grid_constant__ CUtensorMap ma, const __grid_constant__ CUtensorMap mb,
            const __grid_constant__ GemmArgs g)
@@ -236,25 +208,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const uint32_t base = (smem_u32(smem_raw) + (kStageAlign - 1)) & ~(kStageAlign - 1);
     const uint32_t S = g.stages;
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Work units: tiles, or with kMC pairs of tiles (2 m, m + 1 ; n) taken by the two CTAs of a
-    // cluster.  Unit u, u + units, ...: unit t is (t % mgroups, t / mgroups), so the CTAs running
-    // together share B tiles (through L2, or with kMC by multicast as well).
-    const uint32_t rank = kMC ? cluster_rank() : 0u;
-    const uint32_t unit = kMC ? blockIdx.x >> 1 : blockIdx.x;
-    const uint32_t units = kMC ? gridDim.x >> 1 : gridDim.x;
-    const uint32_t mgroups = kMC ? (g.mtiles + 1) / 2 : g.mtiles;
-    const uint32_t nunits = mgroups * g.ntiles;
+    // Tiles u, u + units, ...: tile t is (t % mtiles, t / mtiles), so the CTAs running together
+    // share B tiles through L2.
+    const uint32_t unit = blockIdx.x, units = gridDim.x;
+    const uint32_t nunits = g.mtiles * g.ntiles;
     const uint32_t my_tiles = unit < nunits ? (nunits - 1 - unit) / units + 1 : 0;
     auto tile_of = [&](uint32_t i, uint32_t& mt, uint32_t& nt) {
         const uint32_t t = unit + i * units;
-        mt = kMC ? 2 * (t % mgroups) + rank : t % mgroups;
-        nt = t / mgroups;
+        mt = t % g.mtiles;
+        nt = t / g.mtiles;
     };
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < S; s++) {
             mbar_init(smem_u32(&full_bar[s]), 1);
-            mbar_init(smem_u32(&empty_bar[s]), kMC ? 2 : 1);  // kMC: both CTAs' MMAs release it
+            mbar_init(smem_u32(&empty_bar[s]), 1);
         }
         for (uint32_t b = 0; b < 2; b++) {
             mbar_init(smem_u32(&acc_full[b]), 1);
@@ -264,11 +232,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     if (warp == 1) tmem_alloc(smem_u32(&tmem_slot), 2 * kTmemCols);
     tc_fence_before();
-    if constexpr (kMC) {
-        cluster_sync();  // both CTAs' barriers exist before any multicast or commit reaches them
-    } else {
-        __syncthreads();
-    }
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem = tmem_slot;
 
@@ -294,16 +258,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     const uint32_t bar = smem_u32(&full_bar[s]);
                     const int32_t ca[2] = {(int32_t)(kb * kBK), (int32_t)(mt * kBM)};
-                    mbar_arrive_expect_tx(bar, kGemmStage);  // A and both halves of B
+                    const int32_t cb[2] = {(int32_t)(kb * kBK), (int32_t)(nt * kBN)};
+                    mbar_arrive_expect_tx(bar, kGemmStage);  // the A and B tiles
                     tma_load<2>(base + s * kGemmStage, &ma, ca, bar);
-                    if constexpr (kMC) {
-                        tma_load_2d_multicast(base + s * kGemmStage + kTileA + rank * (kTileB / 2), &mb,
-                                              (int32_t)(kb * kBK), (int32_t)(nt * kBN + rank * (kBN / 2)),
-                                              bar, (uint16_t)0x3);
-                    } else {
-                        const int32_t cb[2] = {(int32_t)(kb * kBK), (int32_t)(nt * kBN)};
-                        tma_load<2>(base + s * kGemmStage + kTileA, &mb, cb, bar);
-                    }
+                    tma_load<2>(base + s * kGemmStage + kTileA, &mb, cb, bar);
                     issued++;
                     if (++s == S) {
                         s = 0;
@@ -347,12 +305,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         mma_bf16(d, sw128_desc(a0 + ks * kUK * 2), sw128_desc(b0 + ks * kUK * 2),
                                  kIdesc, (kb | ks) != 0 ? 1u : 0u);
                     }
-                    // the stage is free once these MMAs read it (with kMC: in both CTAs)
-                    if constexpr (kMC) {
-                        tc_commit_multicast(smem_u32(&empty_bar[s]), (uint16_t)0x3);
-                    } else {
-                        tc_commit(smem_u32(&empty_bar[s]));
-                    }
+                    // the stage is free once these MMAs read it
+                    tc_commit(smem_u32(&empty_bar[s]));
                     if (++s == S) {
                         s = 0;
                         phase ^= 1u;
@@ -409,14 +363,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
     }
 
-    // Every tensor-memory read and every MMA has completed (with kMC in both CTAs, and no
-    // multicast or commit of either CTA is still to reach the other): free the accumulators.
+    // Every tensor-memory read and every MMA has completed: free the accumulators.
     tc_fence_before();
-    if constexpr (kMC) {
-        cluster_sync();
-    } else {
-        __syncthreads();
-    }
+    __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, 2 * kTmemCols);
@@ -668,19 +617,10 @@ cudaError_t launch_gemm(const CUtensorMap* a, const CUtensorMap* b, const GemmAr
                         uint32_t grid, size_t smem, cudaStream_t s)
 {
     cudaError_t e =
-        cudaFuncSetAttribute(k_gemm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        cudaFuncSetAttribute(k_gemm, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k_gemm<false><<<grid, kGemmThreads, smem, s>>>(*a, *b, g);
+    k_gemm<<<grid, kGemmThreads, smem, s>>>(*a, *b, g);
     return cudaGetLastError();
-}
-
-cudaError_t launch_gemm_multicast(const CUtensorMap* a, const CUtensorMap* b_half,
-                                  const GemmArgs& g, uint32_t grid, size_t smem, cudaStream_t s)
-{
-    cudaError_t e =
-        cudaFuncSetAttribute(k_gemm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return launch_cluster2(k_gemm<true>, grid, smem, s, *a, *b_half, g);
 }
 
 cudaError_t launch_gemm_pair(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* b_quarter,

@@ -365,8 +365,6 @@ cudaError_t launch_gemm(const CUtensorMap* a, const CUtensorMap* b, const GemmAr
 cudaError_t launch_gemm_pair(const CUtensorMap* a, const CUtensorMap* b, const CUtensorMap* b_quarter,
                              const GemmArgs& g,
                              uint32_t grid, size_t smem, cudaStream_t s);
-cudaError_t launch_gemm_multicast(const CUtensorMap* a, const CUtensorMap* b_half,
-                                  const GemmArgs& g, uint32_t grid, size_t smem, cudaStream_t s);
 
 // Sets the thread's tm_last_error() text; returns `code`.
 int set_last_error(int code, const char* msg);

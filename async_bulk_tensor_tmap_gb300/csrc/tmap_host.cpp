@@ -769,11 +769,9 @@ int stream_gemm(const tm_desc* a, const tm_desc* b, float* c, uint64_t ldc, uint
     if (rc) return rc;
     // Forms: the CTA-pair form (256-row tiles over the two SMs of a cluster, tcgen05 cta_group::2,
     // 32 KiB stages, up to 7), the default when C has more than one 128-row tile (measured on
-    // GB300 at 8192 x 8192 x 4096: 1738-1821 TFLOP/s with 7 stages); TM_GEMM_PAIR=0 gives clusters of
-    // two one-SM CTAs along M sharing each B tile by TMA multicast (1464 TFLOP/s; TM_GEMM_MULTICAST=0
-    // turns the sharing off); one SM per 128 x 256 tile otherwise.
+    // GB300 at 8192 x 8192 x 4096: 1738-1821 TFLOP/s with 7 stages); one SM per 128 x 256 tile
+    // otherwise, or with TM_GEMM_PAIR=0 (1392-1405 TFLOP/s).
     const bool pair = env_u64("TM_GEMM_PAIR", 1) != 0 && M > 128 && ds->sms >= 2;
-    const bool mcast = !pair && env_u64("TM_GEMM_MULTICAST", 1) != 0 && M > 128 && ds->sms >= 2;
     const uint32_t rows = pair ? 256u : 128u;
     const uint32_t S = std::min<uint32_t>(stages, pair ? kGemmMaxPairStages : kGemmMaxStages);
     GemmArgs g;
@@ -796,10 +794,9 @@ int stream_gemm(const tm_desc* a, const tm_desc* b, float* c, uint64_t ldc, uint
     if (smem > cta_budget(*ds, 1) + 1024) return fail(TM_ERANGE, "%u stages exceed shared memory", S);
     const CUtensorMap* ma = (const CUtensorMap*)a->tmap;
     const CUtensorMap* mb = (const CUtensorMap*)b->tmap;
-    if (pair || mcast) {
-        // Each CTA of a cluster loads a 128-row half of the B tile: a map of B with a 128-row box
-        // (the caller's has 256 rows).  Both cluster forms expect exactly 16 KiB per half and per
-        // A tile in every stage.
+    if (pair) {
+        // Each CTA of a pair loads a 128-row half of the B tile: a map of B with a 128-row box
+        // (the caller's has 256 rows).  Every stage expects exactly 16 KiB per half and per A tile.
         tm_desc bh;
         const uint64_t dims[2] = {b->dim[0], b->dim[1]};
         const uint64_t strides[1] = {b->stride[1]};
@@ -811,34 +808,26 @@ int stream_gemm(const tm_desc* a, const tm_desc* b, float* c, uint64_t ldc, uint
         if (bh.path != TM_PATH_TMA || bh.box_bytes != 16384 || a->box_bytes != 16384)
             return fail(TM_EUNSUPPORTED, "stream_gemm could not encode the half-tile map of B");
         const CUtensorMap* mbh = (const CUtensorMap*)bh.tmap;
-        if (pair) {
-            // persistent: one cluster of two CTAs per pair of SMs.  A last wave of r < pairs tiles
-            // would leave pairs idle; when 2r <= pairs its tiles are done as 256 x 128 halves (each
-            // CTA loading 64 B rows through a 64-row map of B), so that the wave takes half a tile
-            // (TM_GEMM_TAIL_SPLIT=0 keeps whole tiles).
-            const uint64_t pairs = std::min<uint64_t>(tiles, (uint64_t)ds->sms / 2);
-            const uint64_t rem = tiles % pairs;
-            const bool split = env_u64("TM_GEMM_TAIL_SPLIT", 1) != 0 && tiles > pairs && rem > 0 &&
-                               2 * rem <= pairs;
-            g.split_from = (uint32_t)(split ? tiles - rem : tiles);
-            tm_desc bq;
-            const uint32_t qbox[2] = {64, 64};
-            if ((rc = plan_impl(&bq, TM_BF16, 2, (void*)(uintptr_t)b->base, dims, strides, qbox,
-                                nullptr, TM_SWIZZLE_128B, TM_OOB_ZERO)))
-                return rc;
-            if ((rc = encode_into(&bq))) return rc;
-            if (bq.path != TM_PATH_TMA || bq.box_bytes != 8192)
-                return fail(TM_EUNSUPPORTED, "stream_gemm could not encode the quarter-tile map of B");
-            return check_launch(launch_gemm_pair(ma, mbh, (const CUtensorMap*)bq.tmap, g,
-                                                 (uint32_t)(2 * pairs), smem, (cudaStream_t)stream),
-                                "gemm launch (CTA pairs)");
-        }
-        // persistent: one cluster of two CTAs (tiles 2m and 2m + 1 of one N tile) per pair of SMs
-        const uint64_t units = (uint64_t)((g.mtiles + 1) / 2) * g.ntiles;
-        const uint64_t clusters = std::min<uint64_t>(units, (uint64_t)ds->sms / 2);
-        return check_launch(launch_gemm_multicast(ma, mbh, g, (uint32_t)(2 * clusters), smem,
-                                                  (cudaStream_t)stream),
-                            "gemm launch (B multicast)");
+        // persistent: one cluster of two CTAs per pair of SMs.  A last wave of r < pairs tiles
+        // would leave pairs idle; when 2r <= pairs its tiles are done as 256 x 128 halves (each
+        // CTA loading 64 B rows through a 64-row map of B), so that the wave takes half a tile
+        // (TM_GEMM_TAIL_SPLIT=0 keeps whole tiles).
+        const uint64_t pairs = std::min<uint64_t>(tiles, (uint64_t)ds->sms / 2);
+        const uint64_t rem = tiles % pairs;
+        const bool split = env_u64("TM_GEMM_TAIL_SPLIT", 1) != 0 && tiles > pairs && rem > 0 &&
+                           2 * rem <= pairs;
+        g.split_from = (uint32_t)(split ? tiles - rem : tiles);
+        tm_desc bq;
+        const uint32_t qbox[2] = {64, 64};
+        if ((rc = plan_impl(&bq, TM_BF16, 2, (void*)(uintptr_t)b->base, dims, strides, qbox,
+                            nullptr, TM_SWIZZLE_128B, TM_OOB_ZERO)))
+            return rc;
+        if ((rc = encode_into(&bq))) return rc;
+        if (bq.path != TM_PATH_TMA || bq.box_bytes != 8192)
+            return fail(TM_EUNSUPPORTED, "stream_gemm could not encode the quarter-tile map of B");
+        return check_launch(launch_gemm_pair(ma, mbh, (const CUtensorMap*)bq.tmap, g,
+                                             (uint32_t)(2 * pairs), smem, (cudaStream_t)stream),
+                            "gemm launch (CTA pairs)");
     }
     if (a->box_bytes != 16384 || b->box_bytes != 32768)
         return fail(TM_EUNSUPPORTED, "stream_gemm: A and B tiles must be 16 and 32 KiB");

@@ -256,11 +256,7 @@ int stream_tiles(const tm_desc* a, const tm_desc* b, uint32_t stages, float* cs_
  *   cta_group::2: each CTA loads its 128-row halves of the A and B tiles into 32 KiB stages (all 7
  *   usable), the leader issues the MMAs over both; a last wave that would leave at least half the
  *   pairs idle is done as 256 x 128 half tiles (TM_GEMM_TAIL_SPLIT=0 keeps whole tiles); TM_GEMM_PAIR=0 gives instead one SM per
- *   128 x 256 tile (48 KiB stages, at most 4 used) with clusters of two CTAs along M sharing each
- *   B tile: each CTA loads one 128-row half of it, multicast into both CTAs' stages ([H200-TMA] §01:
- *   one copy lands in several CTAs' shared memory; one GPU only), and each CTA's MMA commits
- *   release the stage in both (TM_GEMM_MULTICAST=0 turns the sharing off).  A C of one 128-row
- *   tile uses one-SM CTAs.  c: device, fp32, row-major M x N with ldc >= N elements between
+ *   128 x 256 tile (48 KiB stages, at most 4 used).  A C of one 128-row tile uses one-SM CTAs.  c: device, fp32, row-major M x N with ldc >= N elements between
  *   rows, 16-byte aligned, ldc a multiple of 4 (else TM_EALIGN).  Ragged M, N and K are zero-filled by the
  *   loads; only in-bounds elements of C are written.  Accuracy: the fp32 result differs from the
  *   exact sum of the K products by at most K * 2^-23 * sum |A[m][k] * B[n][k]| (any summation order,

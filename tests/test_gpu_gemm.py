@@ -24,12 +24,11 @@ def tm_lib():
     return m
 
 
-@pytest.fixture(params=["one_sm", "multicast", "pair"])
+@pytest.fixture(params=["one_sm", "pair"])
 def tm(request, tm_lib, monkeypatch):
-    """The three forms of the consumer: one SM per 128-row tile; clusters of two such CTAs sharing
-    each B tile by TMA multicast; CTA pairs (tcgen05 cta_group::2, 256-row tiles over two SMs)."""
+    """The two forms of the consumer: one SM per 128-row tile; CTA pairs (tcgen05 cta_group::2,
+    256-row tiles over two SMs)."""
     monkeypatch.setenv("TM_GEMM_PAIR", "1" if request.param == "pair" else "0")
-    monkeypatch.setenv("TM_GEMM_MULTICAST", "1" if request.param == "multicast" else "0")
     return tm_lib
 
 
