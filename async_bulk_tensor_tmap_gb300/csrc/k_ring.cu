@@ -43,26 +43,6 @@
 
 namespace tmk {
 
-// An L2 cache policy whose lines are the first candidates for eviction, for bytes read once: a
-// stream of such loads recycles its own lines instead of pushing other data out of L2.
-__device__ __forceinline__ uint64_t l2_policy_evict_first()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-// 2-D global -> shared box load as tma_load<2>, with an L2 cache policy on the global reads.
-__device__ __forceinline__ void tma_load_2d_policy(uint32_t dst, const CUtensorMap* m, int32_t c0,
-                                                   int32_t c1, uint32_t bar, uint64_t policy)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1), "r"(bar), "l"(policy)
-        : "memory");
-}
-
 constexpr uint32_t kRingMaxStages = 8;
 constexpr uint32_t kRingMaxWpt = 4;                 // consumer warps per tile
 constexpr uint32_t kRingMaxGroups = 2;              // consumer groups (tiles i % groups)
@@ -168,7 +148,9 @@ __global__ void __launch_bounds__(kRingThreads, 1)
             pf_i = S;
             prefetch_to(r.prefetch);
         }
-        const uint64_t policy = l2_policy_evict_first();
+        // each tile is read once: an evict-first policy lets the stream recycle its own L2 lines
+        // instead of pushing other data out of L2
+        const uint64_t policy = l2_policy(kL2EvictFirst);
         uint32_t s = 0, wraps = 0;
         uint64_t i = 0;
         for (; i < n_local; i++) {
@@ -184,8 +166,8 @@ __global__ void __launch_bounds__(kRingThreads, 1)
             const int32_t cb[2] = {(int32_t)(ld.b0 * 64), (int32_t)(ld.b1 * r.rows)};
             mbar_arrive_expect_tx(bar, 2 * tile);
             if (r.evict_first) {
-                tma_load_2d_policy(base + s * 2 * tile, &ma, ca[0], ca[1], bar, policy);
-                tma_load_2d_policy(base + s * 2 * tile + tile, &mb, cb[0], cb[1], bar, policy);
+                tma_load<2, true>(base + s * 2 * tile, &ma, ca, bar, policy);
+                tma_load<2, true>(base + s * 2 * tile + tile, &mb, cb, bar, policy);
             } else {
                 tma_load<2>(base + s * 2 * tile, &ma, ca, bar);
                 tma_load<2>(base + s * 2 * tile + tile, &mb, cb, bar);

@@ -2,25 +2,27 @@
 //
 // One CTA is one warp; its elected lane issues everything ([MLSys-TMA] = mlc.ai "Modern GPU
 // Programming for MLSys", chapter "异步数据搬运：TMA", §"一个 thread 如何描述整个 tile": a single
-// thread submits the copy, the engine does the addressing).  Boxes are taken in groups of G
+// thread submits the copy, the engine does the addressing).  Boxes are taken in items of up to G
 // consecutive boxes sharing a stage (G > 1 for boxes well under a stage), each in a slot that
 // starts on its swizzle period (1024 / 512 / 256 bytes for 128B / 64B / 32B, 128 without), so that
-// each image in a stage keeps the swizzle phase it has in its own image; the lane walks the
-// groups blockIdx.x, blockIdx.x + gridDim.x, ... through an S-stage ring of 1024-byte aligned
-// shared-memory stages:
+// each image in a stage keeps the swizzle phase it has in its own image.  CTA c takes item c of
+// every full wave of gridDim.x x G boxes, then its share of the tail, dealt out box by box
+// (stream_item), through an S-stage ring of 1024-byte aligned shared-memory stages:
 //
-//   load   group i into stage i % S     (one mbarrier, arrive.expect_tx of the group's bytes, one
-//                                         complete_tx per box, §"如何等待 TMA load 完成")
+//   load   item i into stage i % S     (one mbarrier, arrive.expect_tx of the item's bytes, one
+//                                        complete_tx per box, §"如何等待 TMA load 完成")
 //   wait   full[i % S] for parity (i / S) & 1           -- bounded
 //   write  stage i % S out, commit a bulk group          (§"如何等待 TMA store 完成")
-//   refill stage (i - 1) % S with group i - 1 + S once the bulk group of group i - 1 has finished
-//          READING shared memory (wait_group.read 1): the write of group i stays in flight
-//          (with a single stage, the stage of group i once its own write has read it).
+//   refill stage (i - 1) % S with item i - 1 + S once the bulk group of item i - 1 has finished
+//          READING shared memory (wait_group.read 1): the write of item i stays in flight
+//          (with a single stage, the stage of item i once its own write has read it).
 //
-// The lane keeps two cursors over its groups, one for loads (running up to S groups ahead) and
-// one for writes: each holds the stage, its phase parity and, for a grid walk, the box counters of
-// the group's first box, stepped by G * gridDim.x boxes with carries; the boxes inside a group are
-// stepped with an odometer.  No 64-bit division is left on the issue path.
+// The lane keeps two cursors over its items, one for loads (running up to S items ahead) and one
+// for writes: each holds the stage, its phase parity and, for a grid walk, the box counters of
+// the item's first box, stepped by G * gridDim.x boxes with carries (the tail item's counters are
+// found once, before the first load); the boxes inside an item are stepped with an odometer.  No
+// 64-bit division is left on the issue path.  The loads and the writes may carry an L2 eviction
+// policy (StreamArgs::hints).
 //
 // The three kinds differ only in the two copy instructions:
 //   copy       load = tensor load of the box;  write = 1-D bulk store of the image (tile-major)
@@ -67,12 +69,11 @@ __global__ void __launch_bounds__(32, 1)
 
     if (!elect_one()) return;
 
-    // Work unit: a group of `a.group` consecutive boxes sharing one stage (their images are
-    // consecutive in the tile-major buffer as well).
-    const uint64_t G = a.group;
-    const uint64_t first = blockIdx.x;
-    if (a.ngroups <= first) return;
-    const uint64_t n_local = a.n_base + (first < a.n_rem ? 1u : 0u);
+    // Work unit: an item of up to G consecutive boxes sharing one stage (their images are
+    // consecutive in the tile-major buffer as well): the full waves, then this CTA's tail boxes.
+    const uint32_t cta = blockIdx.x, grid_ctas = gridDim.x;
+    const uint64_t n_local = stream_items(a, cta);
+    if (n_local == 0) return;
     const uint32_t S = a.stages;
     const uint32_t base = (smem_u32(smem_raw) + (kStageAlign - 1)) & ~(kStageAlign - 1);
 
@@ -81,23 +82,34 @@ __global__ void __launch_bounds__(32, 1)
     for (uint32_t s = 0; s < S; s++) mbar_init(smem_u32(&full_bar[s]), 1);
     fence_barrier_init();
 
-    const bool grid = a.walk.mode == WALK_GRID;
-    auto group_of = [&](uint64_t i) -> uint64_t { return first + i * gridDim.x; };
-    auto count_of = [&](uint64_t g) -> uint32_t {
-        const uint64_t b0 = g * G;
-        return (uint32_t)(a.walk.nbox - b0 < G ? a.walk.nbox - b0 : G);
-    };
+    const uint32_t hint_ld = a.hints & 3u, hint_wr = (a.hints >> 2) & 3u;
+    const uint64_t pol_ld = l2_policy(hint_ld), pol_wr = l2_policy(hint_wr);
 
-    // Group i of this CTA: its stage, the phase parity of that stage's barrier, and (grid walks)
-    // the counters of its first box.
+    const bool grid = a.walk.mode == WALK_GRID;
+
+    // Item i of this CTA: its stage, the phase parity of that stage's barrier, its first box and
+    // box count, and (grid walks) the counters of its first box.
     struct Cursor {
-        uint64_t i;
-        uint32_t s, phase;
+        uint64_t i, b0;
+        uint32_t s, phase, cnt;
         uint32_t k[5];
     };
     const uint32_t* const dstep = a.dstep;  // digits of G * gridDim.x boxes (from the host)
-    Cursor ld{0, 0, 0, {0, 0, 0, 0, 0}};
-    if (grid) first_counters(a.walk, first * G, ld.k);
+    Cursor ld;
+    ld.i = 0;
+    ld.s = 0;
+    ld.phase = 0;
+    stream_item(a, cta, grid_ctas, 0, ld.b0, ld.cnt);
+    uint32_t tail_k[5] = {0, 0, 0, 0, 0};  // counters of the tail item's first box
+    if (grid) {
+        first_counters(a.walk, ld.b0, ld.k);
+        if (a.waves > 0 && a.waves < n_local) {
+            uint64_t tb;
+            uint32_t tc;
+            stream_item(a, cta, grid_ctas, a.waves, tb, tc);
+            first_counters(a.walk, tb, tail_k);
+        }
+    }
     Cursor wr = ld;
     auto advance = [&](Cursor& c) {
         c.i++;
@@ -105,27 +117,34 @@ __global__ void __launch_bounds__(32, 1)
             c.s = 0;
             c.phase ^= 1u;
         }
-        if (grid) grid_add(a.walk, c.k, dstep);
+        if (c.i >= n_local) return;
+        stream_item(a, cta, grid_ctas, c.i, c.b0, c.cnt);
+        if (grid) {
+            if (c.i < a.waves) {
+                grid_add(a.walk, c.k, dstep);
+            } else {
+#pragma unroll
+                for (int d = 0; d < 5; d++) c.k[d] = tail_k[d];
+            }
+        }
     };
 
-    // Calls fn(j, coords) for the boxes of the cursor's group, in order.
+    // Calls fn(j, coords) for the boxes of the cursor's item, in order.
     auto for_boxes = [&](const Cursor& c, auto&& fn) {
-        const uint64_t g = group_of(c.i);
-        const uint32_t cnt = count_of(g);
         int32_t co[5];
         if (grid) {
             uint32_t k[5];
 #pragma unroll
             for (int d = 0; d < 5; d++) k[d] = c.k[d];
-            for (uint32_t j = 0; j < cnt; j++) {
+            for (uint32_t j = 0; j < c.cnt; j++) {
 #pragma unroll
                 for (int d = 0; d < 5; d++) co[d] = (int32_t)(k[d] * a.walk.box[d]);
                 fn(j, co);
                 grid_next(a.walk, k);
             }
         } else {
-            for (uint32_t j = 0; j < cnt; j++) {
-                box_start(a.walk, g * G + j, co);
+            for (uint32_t j = 0; j < c.cnt; j++) {
+                box_start(a.walk, c.b0 + j, co);
                 fn(j, co);
             }
         }
@@ -139,40 +158,47 @@ __global__ void __launch_bounds__(32, 1)
     auto issue = [&](const Cursor& c) {
         const uint32_t bar = smem_u32(&full_bar[c.s]);
         const uint32_t dst = base + c.s * a.stage_bytes;
-        const uint64_t g = group_of(c.i);
-        const uint32_t cnt = count_of(g);
-        mbar_arrive_expect_tx(bar, cnt * a.box_bytes);
+        mbar_arrive_expect_tx(bar, c.cnt * a.box_bytes);
         if constexpr (KIND == KIND_ROUNDTRIP) {
+            const uint64_t src = a.images + c.b0 * a.box_bytes;
             if (dense) {
-                bulk_load(dst, a.images + g * G * a.box_bytes, cnt * a.box_bytes, bar);
+                if (hint_ld) bulk_load<true>(dst, src, c.cnt * a.box_bytes, bar, pol_ld);
+                else bulk_load(dst, src, c.cnt * a.box_bytes, bar);
             } else {
-                for (uint32_t j = 0; j < cnt; j++)
-                    bulk_load(dst + j * slot, a.images + (g * G + j) * a.box_bytes, a.box_bytes, bar);
+                for (uint32_t j = 0; j < c.cnt; j++) {
+                    if (hint_ld) bulk_load<true>(dst + j * slot, src + j * a.box_bytes, a.box_bytes, bar, pol_ld);
+                    else bulk_load(dst + j * slot, src + j * a.box_bytes, a.box_bytes, bar);
+                }
             }
         } else {
             for_boxes(c, [&](uint32_t j, const int32_t* co) {
-                tma_load<R>(dst + j * slot, &in_map, co, bar);
+                if (hint_ld) tma_load<R, true>(dst + j * slot, &in_map, co, bar, pol_ld);
+                else tma_load<R>(dst + j * slot, &in_map, co, bar);
             });
         }
     };
 
     auto write_out = [&](const Cursor& c) {
         const uint32_t src = base + c.s * a.stage_bytes;
-        const uint64_t g = group_of(c.i);
         if constexpr (KIND == KIND_COPY) {
+            const uint64_t dst = a.images + c.b0 * a.box_bytes;
             if (dense) {
-                bulk_store(a.images + g * G * a.box_bytes, src, count_of(g) * a.box_bytes);
+                if (hint_wr) bulk_store<true>(dst, src, c.cnt * a.box_bytes, pol_wr);
+                else bulk_store(dst, src, c.cnt * a.box_bytes);
             } else {
-                const uint32_t cnt = count_of(g);
-                for (uint32_t j = 0; j < cnt; j++)
-                    bulk_store(a.images + (g * G + j) * a.box_bytes, src + j * slot, a.box_bytes);
+                for (uint32_t j = 0; j < c.cnt; j++) {
+                    if (hint_wr) bulk_store<true>(dst + j * a.box_bytes, src + j * slot, a.box_bytes, pol_wr);
+                    else bulk_store(dst + j * a.box_bytes, src + j * slot, a.box_bytes);
+                }
             }
         } else {
             for_boxes(c, [&](uint32_t j, const int32_t* co) {
                 if constexpr (KIND == KIND_ROUNDTRIP) {
-                    tma_store<R>(&out_map, co, src + j * slot);
+                    if (hint_wr) tma_store<R, true>(&out_map, co, src + j * slot, pol_wr);
+                    else tma_store<R>(&out_map, co, src + j * slot);
                 } else {
-                    tma_reduce<R, KIND - KIND_REDUCE>(&out_map, co, src + j * slot);
+                    if (hint_wr) tma_reduce<R, KIND - KIND_REDUCE, true>(&out_map, co, src + j * slot, pol_wr);
+                    else tma_reduce<R, KIND - KIND_REDUCE>(&out_map, co, src + j * slot);
                 }
             });
         }
@@ -183,7 +209,7 @@ __global__ void __launch_bounds__(32, 1)
         issue(ld);
         advance(ld);
     }
-    // Stage refilled after writing group i: the one group i - 1 used (its write may still be
+    // Stage refilled after writing item i: the one item i - 1 used (its write may still be
     // reading), or with a single stage the one just written.
     const uint64_t lag = S > 1 ? 1 : 0;
 
@@ -191,7 +217,7 @@ __global__ void __launch_bounds__(32, 1)
         if (!mbar_wait(smem_u32(&full_bar[wr.s]), wr.phase, a.timeout_ns)) {
             const uint32_t kid = KIND == KIND_COPY ? K_COPY : KIND == KIND_ROUNDTRIP ? K_ROUNDTRIP
                                                                                     : K_REDUCE;
-            record_timeout(a.status, kid, wr.s, wr.phase, group_of(wr.i) * G);
+            record_timeout(a.status, kid, wr.s, wr.phase, wr.b0);
             // Let every load still in flight land (bounded) before the stages go away.
             for (uint64_t j = wr.i + 1; j < ld.i; j++) {
                 mbar_wait(smem_u32(&full_bar[j % S]), (uint32_t)((j / S) & 1), a.timeout_ns);
@@ -201,9 +227,9 @@ __global__ void __launch_bounds__(32, 1)
         write_out(wr);
         if (wr.i >= lag && ld.i < n_local) {
             if (lag) {
-                bulk_wait_read<1>();  // group i - 1's write has read its stage
+                bulk_wait_read<1>();  // item i - 1's write has read its stage
             } else {
-                bulk_wait_read<0>();  // the only stage: group i's write has read it
+                bulk_wait_read<0>();  // the only stage: item i's write has read it
             }
             issue(ld);
             advance(ld);

@@ -4,12 +4,23 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include <algorithm>
 
 #include "tmap.h"
 
 namespace tmk {
+
+// A non-negative integer from the environment (library tunables), or dflt when unset or malformed.
+inline uint64_t env_u64(const char* name, uint64_t dflt)
+{
+    const char* v = getenv(name);
+    if (!v || !*v) return dflt;
+    char* end = nullptr;
+    const unsigned long long x = strtoull(v, &end, 10);
+    return (end && *end == 0) ? (uint64_t)x : dflt;
+}
 
 constexpr uint32_t kInlineBoxes = 8;   // explicit box lists up to this size travel in parameters
 constexpr uint32_t kStageAlign = 1024; // 128B swizzle is computed on smem address bits 4..9
@@ -45,33 +56,54 @@ struct BoxWalk {
     int32_t inl[kInlineBoxes * 5];
 };
 
+#if defined(__CUDACC__)
+#define TM_HD __host__ __device__
+#else
+#define TM_HD
+#endif
+
 // TMA-path streaming kernels (copy, round trip, reduce).
+//
+// Work split over a grid of `grid` CTAs: the boxes are taken in full waves of grid x G consecutive
+// boxes (G = group, the boxes sharing one stage), CTA c taking boxes (j * grid + c) * G .. + G - 1
+// of wave j; the R < grid x G boxes after the last full wave form the tail, dealt out at box
+// granularity: CTA c takes q + (c < r ? 1 : 0) consecutive boxes of it (q = R / grid, r = R % grid;
+// at most G, so they fit one stage).  No CTA has more than one box above the mean.
 struct StreamArgs {
     BoxWalk walk;
     uint64_t images;       // copy: destination images; round trip: source images
     uint32_t box_bytes;
     uint32_t stage_bytes;  // group * box_bytes rounded up to kStageAlign
     uint32_t stages;
-    uint32_t group;        // consecutive boxes per stage
+    uint32_t group;        // G: consecutive boxes per stage
     uint32_t slot_bytes;   // stage bytes per box: box_bytes rounded up to its swizzle period
-    uint32_t n_rem;        // CTAs below n_rem take n_base + 1 groups, the others n_base
+    uint32_t hints;        // L2 policies: bits 0-1 the loads', bits 2-3 the writes' (0 none,
+                           // 1 evict-first, 2 evict-last)
     uint64_t timeout_ns;
     StatusBlock* status;
     // The launch-wide schedule, computed once on the host (stream_schedule) so that no CTA runs
     // 64-bit divisions before its first load.
-    uint64_t ngroups;      // ceil(walk.nbox / group)
-    uint64_t n_base;       // ngroups / grid
-    uint32_t dstep[5];     // digits (radix: the grid's box counts) of grid * group boxes
+    uint64_t waves;        // full waves of grid x G boxes
+    uint64_t tail0;        // first box of the tail: waves x grid x G
+    uint32_t tail_q;       // tail boxes per CTA: tail_q, one more below tail_r
+    uint32_t tail_r;
+    uint32_t dstep[5];     // digits (radix: the grid's box counts) of grid x G boxes
     uint32_t pad;
 };
+
+// Default L2 policies of the streaming copies' loads and writes (see stream_plan).
+constexpr uint32_t kDefaultHintLoad = 0, kDefaultHintWrite = 0;
 
 // Fills the schedule fields of a streaming launch over `grid` CTAs (walk and group already set).
 inline void stream_schedule(StreamArgs& a, uint32_t grid)
 {
-    a.ngroups = (a.walk.nbox + a.group - 1) / a.group;
-    a.n_base = a.ngroups / grid;
-    a.n_rem = (uint32_t)(a.ngroups % grid);
-    uint64_t b = (uint64_t)grid * a.group;
+    const uint64_t wave = (uint64_t)grid * a.group;
+    a.waves = a.walk.nbox / wave;
+    a.tail0 = a.waves * wave;
+    const uint64_t rest = a.walk.nbox - a.tail0;
+    a.tail_q = (uint32_t)(rest / grid);
+    a.tail_r = (uint32_t)(rest % grid);
+    uint64_t b = wave;
     for (uint32_t i = 0; i < 5; i++) {
         if (i < a.walk.rank) {
             a.dstep[i] = (uint32_t)(b % a.walk.grid_nb[i]);
@@ -79,6 +111,25 @@ inline void stream_schedule(StreamArgs& a, uint32_t grid)
         } else {
             a.dstep[i] = 0;
         }
+    }
+}
+
+// Items (stages' worth of boxes) CTA c handles: the full waves, plus one if it has tail boxes.
+TM_HD inline uint64_t stream_items(const StreamArgs& a, uint32_t c)
+{
+    return a.waves + ((a.tail_q > 0 || c < a.tail_r) ? 1u : 0u);
+}
+
+// First box and box count of item i of CTA c in a grid of `grid` CTAs.
+TM_HD inline void stream_item(const StreamArgs& a, uint32_t c, uint32_t grid, uint64_t i,
+                              uint64_t& b0, uint32_t& cnt)
+{
+    if (i < a.waves) {
+        b0 = (i * grid + c) * a.group;
+        cnt = a.group;
+    } else {
+        b0 = a.tail0 + (uint64_t)c * a.tail_q + (c < a.tail_r ? c : a.tail_r);
+        cnt = a.tail_q + (c < a.tail_r ? 1u : 0u);
     }
 }
 
@@ -123,6 +174,37 @@ inline void tma_group(uint64_t box_bytes, uint32_t span, uint64_t target, uint32
     const uint64_t g = target / sl;
     group = (uint32_t)(g < 1 ? 1 : g > 64 ? 64 : g);
     slot = group > 1 ? (uint32_t)sl : (uint32_t)box_bytes;
+}
+
+// Launch plan of a TMA streaming kernel over the boxes of a.walk, shared by every entry point that
+// launches one: boxes per stage (tma_group, stages of about TM_GROUP_BYTES = 32 KiB), CTAs per SM
+// (TM_CTAS_PER_SM, default 2; fewer when two stages would not fit), as many stages as fit
+// (at most TM_STAGES when set), the L2 policies of the loads and the writes (TM_L2_HINT_LOAD /
+// TM_L2_HINT_WRITE: 0 none, 1 evict-first, 2 evict-last), the grid, the schedule and the dynamic
+// shared memory.  budget(n) is the shared memory one of n CTAs on an SM may use.
+template <class Budget>
+inline void stream_plan(StreamArgs& a, uint64_t box_bytes, uint32_t span, uint32_t sms,
+                        Budget budget, uint32_t& grid, size_t& smem)
+{
+    a.box_bytes = (uint32_t)box_bytes;
+    tma_group(box_bytes, span, std::max<uint64_t>(env_u64("TM_GROUP_BYTES", 32768), 1024), a.group,
+              a.slot_bytes);
+    const uint64_t stage = (uint64_t)a.group * a.slot_bytes;
+    a.stage_bytes = (uint32_t)((stage + kStageAlign - 1) / kStageAlign * kStageAlign);
+    uint32_t per_sm = (uint32_t)std::min<uint64_t>(std::max<uint64_t>(env_u64("TM_CTAS_PER_SM", 2), 1), 16);
+    size_t b = budget(per_sm);
+    while (per_sm > 1 && b < 2ull * a.stage_bytes) b = budget(--per_sm);
+    uint32_t stages = (uint32_t)std::min<size_t>(b / a.stage_bytes, TM_MAX_STAGES);
+    const uint64_t cap = env_u64("TM_STAGES", 0);
+    if (cap > 0) stages = (uint32_t)std::min<uint64_t>(stages, cap);
+    a.stages = std::max<uint32_t>(stages, 1);
+    const uint32_t hl = (uint32_t)std::min<uint64_t>(env_u64("TM_L2_HINT_LOAD", kDefaultHintLoad), 2);
+    const uint32_t hw = (uint32_t)std::min<uint64_t>(env_u64("TM_L2_HINT_WRITE", kDefaultHintWrite), 2);
+    a.hints = hl | (hw << 2);
+    const uint64_t units = (a.walk.nbox + a.group - 1) / a.group;
+    grid = (uint32_t)std::min<uint64_t>(units, (uint64_t)sms * per_sm);
+    stream_schedule(a, grid);
+    smem = (size_t)a.stages * a.stage_bytes + kStageAlign;
 }
 
 // NaN written for out-of-bounds elements of a map with TM_OOB_NAN on the vector path: the pattern
@@ -291,6 +373,26 @@ inline bool seg_plan(const FbArgs& a, const tm_desc* d, uint32_t sms, uint32_t w
         seg_plan_rows(a, a.ibox[1], sms, want, stages, force, store, budget, s, grid, smem))
         return true;
     return seg_plan_rows(a, 1, sms, want, stages, force, store, budget, s, grid, smem);
+}
+
+// Launch shape of the vector path's copy (load direction), shared by every entry point that
+// launches one: the segment form when the map takes it (TM_FB_SEG: 0 never, 1 whenever the layout
+// allows, unset when its segments are long enough for bulk copies; TM_FB_SEG_CTAS_PER_SM and
+// TM_FB_SEG_STAGES, defaults 2 and 2: the largest items, measured best on GB300 on the W4 rank-5
+// view), else the per-window form (TM_FB_COPY_CTAS_PER_SM, default 8).  Returns true for the
+// segment form (s filled), false for the per-window form (a.block_rows set).  budget(n) as for
+// fb_shape.
+template <class Budget>
+inline bool fb_copy_plan(FbArgs& a, const tm_desc* d, uint64_t nbox, uint32_t sms, Budget budget,
+                         SegArgs& s, uint32_t& grid, size_t& smem)
+{
+    if (seg_plan(a, d, sms, (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_CTAS_PER_SM", 2), 8),
+                 (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_STAGES", 2), kSegMaxStages),
+                 (int)env_u64("TM_FB_SEG", 2), false, budget, s, grid, smem))
+        return true;
+    fb_shape(a, nbox, sms, (uint32_t)std::min<uint64_t>(env_u64("TM_FB_COPY_CTAS_PER_SM", 8), 16),
+             fb_copy_row_bytes(a.gspan0), budget, grid, smem);
+    return false;
 }
 
 // Ring consumer (stream_tiles).

@@ -100,13 +100,7 @@ bool list_on_tma(const tm_desc* d, const int32_t* c, size_t n)
     return true;
 }
 
-uint64_t limit_ns()
-{
-    const char* v = getenv("TM_WAIT_TIMEOUT_NS");
-    char* end = nullptr;
-    const unsigned long long x = v && *v ? strtoull(v, &end, 10) : 0;
-    return (v && *v && end && *end == 0) ? (uint64_t)x : 1000000000ull;
-}
+uint64_t limit_ns() { return tmk::env_u64("TM_WAIT_TIMEOUT_NS", 1000000000ull); }
 
 }  // namespace
 
@@ -160,24 +154,17 @@ extern "C" int tiled_copy_noalloc(const tm_desc* src, const int32_t* coords, siz
         memset(&a, 0, sizeof(a));
         const uint32_t span = src->swizzle == TM_SWIZZLE_128B ? 128u : src->swizzle == TM_SWIZZLE_64B ? 64u
                               : src->swizzle == TM_SWIZZLE_32B ? 32u : 0u;
-        tma_group(src->box_bytes, span, 32768, a.group, a.slot_bytes);
-        const uint32_t stage = stage_of((uint64_t)a.group * a.slot_bytes);
-        uint32_t per_sm = 2;
-        size_t b = budget(*d, per_sm);
-        while (per_sm > 1 && b < stage) b = budget(*d, --per_sm);
         a.walk = w;
         a.images = (uint64_t)images;
-        a.box_bytes = (uint32_t)src->box_bytes;
-        a.stage_bytes = stage;
-        a.stages = (uint32_t)std::max<size_t>(1, std::min<size_t>(b / stage, TM_MAX_STAGES));
+        uint32_t grid = 0;
+        size_t smem = 0;
+        // the launch shape of tiled_copy (same rule, same tunables)
+        stream_plan(a, src->box_bytes, span, (uint32_t)d->sms,
+                    [&](uint32_t per_sm) { return budget(*d, per_sm); }, grid, smem);
         a.timeout_ns = limit_ns();
         a.status = status;
-        const uint64_t groups = (n + a.group - 1) / a.group;
-        const uint32_t grid = (uint32_t)std::min<uint64_t>(groups, (uint64_t)d->sms * per_sm);
-        stream_schedule(a, grid);
         const CUtensorMap* m = (const CUtensorMap*)src->tmap;
-        e = launch_tma_stream(KIND_COPY, src->rank, m, m, a, grid,
-                              (size_t)a.stages * stage + kStageAlign, st);
+        e = launch_tma_stream(KIND_COPY, src->rank, m, m, a, grid, smem, st);
     } else {
         FbArgs a;
         memset(&a, 0, sizeof(a));
@@ -190,12 +177,11 @@ extern "C" int tiled_copy_noalloc(const tm_desc* src, const int32_t* coords, siz
         uint32_t grid = 0;
         size_t smem = 0;
         SegArgs sa;
-        if (seg_plan(a, src, (uint32_t)d->sms, 2u, 2u, 2, false,
-                     [&](uint32_t per_sm) { return budget(*d, per_sm); }, sa, grid, smem)) {
+        // the launch shape of tiled_copy's vector path (same rule, same tunables)
+        if (fb_copy_plan(a, src, n, (uint32_t)d->sms,
+                         [&](uint32_t per_sm) { return budget(*d, per_sm); }, sa, grid, smem)) {
             e = launch_fb_seg_copy(sa, grid, smem, st);
         } else {
-            fb_shape(a, n, (uint32_t)d->sms, 8u, fb_copy_row_bytes(a.gspan0),
-                     [&](uint32_t per_sm) { return budget(*d, per_sm); }, grid, smem);
             e = launch_fb_copy(a, grid, smem, st);
         }
     }

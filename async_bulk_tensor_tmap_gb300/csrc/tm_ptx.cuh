@@ -117,98 +117,136 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
-// Global -> shared box load completing `box_bytes` on mbarrier `bar`.
-template <int R>
-__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* m, const int32_t* c,
-                                         uint32_t bar)
+// L2 cache policies for the streaming copies (createpolicy; the 64-bit policy rides on the copy's
+// .L2::cache_hint operand).  kL2Keep: no hint; kL2EvictFirst: the lines are the first candidates for
+// eviction (bytes touched once: a stream then recycles its own lines instead of evicting other
+// data); kL2EvictLast: the last.
+enum L2Hint : uint32_t { kL2Keep = 0, kL2EvictFirst = 1, kL2EvictLast = 2 };
+
+__device__ __forceinline__ uint64_t l2_policy(uint32_t hint)
 {
-    const uint64_t mp = reinterpret_cast<uint64_t>(m);
-    if constexpr (R == 1) {
-        asm volatile(
-            "cp.async.bulk.tensor.1d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2}], [%3];" ::"r"(dst), "l"(mp), "r"(c[0]), "r"(bar) : "memory");
-    } else if constexpr (R == 2) {
-        asm volatile(
-            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst), "l"(mp), "r"(c[0]), "r"(c[1]), "r"(bar)
-            : "memory");
-    } else if constexpr (R == 3) {
-        asm volatile(
-            "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst), "l"(mp), "r"(c[0]), "r"(c[1]),
-            "r"(c[2]), "r"(bar) : "memory");
-    } else if constexpr (R == 4) {
-        asm volatile(
-            "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst), "l"(mp), "r"(c[0]), "r"(c[1]),
-            "r"(c[2]), "r"(c[3]), "r"(bar) : "memory");
-    } else {
-        asm volatile(
-            "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-            " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst), "l"(mp), "r"(c[0]),
-            "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4]), "r"(bar) : "memory");
+    uint64_t p = 0;
+    if (hint == kL2EvictFirst) {
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    } else if (hint == kL2EvictLast) {
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     }
+    return p;
 }
 
-// Shared -> global box store (only in-bounds elements are written), tracked by a bulk group.
-template <int R>
-__device__ __forceinline__ void tma_store(const CUtensorMap* m, const int32_t* c, uint32_t src)
+// Global -> shared box load completing `box_bytes` on mbarrier `bar`; with H, its global reads
+// carry the L2 policy `pol`.
+#define TMK_LOAD_ASM(RANK, COORDS, BAR, ...)                                                     \
+    if constexpr (H) {                                                                           \
+        asm volatile("cp.async.bulk.tensor." RANK ".shared::cluster.global.tile"                 \
+                     ".mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {" COORDS "}], [" \
+                     BAR "], %" BAR_NEXT ";" ::"r"(dst), "l"(mp), __VA_ARGS__, "r"(bar),         \
+                     "l"(pol) : "memory");                                                       \
+    } else {                                                                                     \
+        asm volatile("cp.async.bulk.tensor." RANK ".shared::cluster.global.tile"                 \
+                     ".mbarrier::complete_tx::bytes [%0], [%1, {" COORDS "}], [" BAR "];"       \
+                     ::"r"(dst), "l"(mp), __VA_ARGS__, "r"(bar) : "memory");                     \
+    }
+
+template <int R, bool H = false>
+__device__ __forceinline__ void tma_load(uint32_t dst, const CUtensorMap* m, const int32_t* c,
+                                         uint32_t bar, uint64_t pol = 0)
 {
     const uint64_t mp = reinterpret_cast<uint64_t>(m);
     if constexpr (R == 1) {
-        asm volatile("cp.async.bulk.tensor.1d.global.shared::cta.tile.bulk_group [%0, {%2}], [%1];"
-                     ::"l"(mp), "r"(src), "r"(c[0]) : "memory");
+#define BAR_NEXT "4"
+        TMK_LOAD_ASM("1d", "%2", "%3", "r"(c[0]))
+#undef BAR_NEXT
     } else if constexpr (R == 2) {
-        asm volatile(
-            "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];"
-            ::"l"(mp), "r"(src), "r"(c[0]), "r"(c[1]) : "memory");
+#define BAR_NEXT "5"
+        TMK_LOAD_ASM("2d", "%2, %3", "%4", "r"(c[0]), "r"(c[1]))
+#undef BAR_NEXT
     } else if constexpr (R == 3) {
-        asm volatile(
-            "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];"
-            ::"l"(mp), "r"(src), "r"(c[0]), "r"(c[1]), "r"(c[2]) : "memory");
+#define BAR_NEXT "6"
+        TMK_LOAD_ASM("3d", "%2, %3, %4", "%5", "r"(c[0]), "r"(c[1]), "r"(c[2]))
+#undef BAR_NEXT
     } else if constexpr (R == 4) {
-        asm volatile(
-            "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group"
-            " [%0, {%2, %3, %4, %5}], [%1];"
-            ::"l"(mp), "r"(src), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]) : "memory");
+#define BAR_NEXT "7"
+        TMK_LOAD_ASM("4d", "%2, %3, %4, %5", "%6", "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]))
+#undef BAR_NEXT
     } else {
-        asm volatile(
-            "cp.async.bulk.tensor.5d.global.shared::cta.tile.bulk_group"
-            " [%0, {%2, %3, %4, %5, %6}], [%1];"
-            ::"l"(mp), "r"(src), "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]), "r"(c[4])
-            : "memory");
+#define BAR_NEXT "8"
+        TMK_LOAD_ASM("5d", "%2, %3, %4, %5, %6", "%7", "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]),
+                     "r"(c[4]))
+#undef BAR_NEXT
     }
 }
+#undef TMK_LOAD_ASM
+
+// Shared -> global box store (only in-bounds elements are written), tracked by a bulk group; with
+// H, its global writes carry the L2 policy `pol`.
+#define TMK_STORE_ASM(RANK, COORDS, POL, ...)                                                    \
+    if constexpr (H) {                                                                           \
+        asm volatile("cp.async.bulk.tensor." RANK ".global.shared::cta.tile.bulk_group"          \
+                     ".L2::cache_hint [%0, {" COORDS "}], [%1], " POL ";"                        \
+                     ::"l"(mp), "r"(src), __VA_ARGS__, "l"(pol) : "memory");                     \
+    } else {                                                                                     \
+        asm volatile("cp.async.bulk.tensor." RANK ".global.shared::cta.tile.bulk_group"          \
+                     " [%0, {" COORDS "}], [%1];" ::"l"(mp), "r"(src), __VA_ARGS__ : "memory");  \
+    }
+
+template <int R, bool H = false>
+__device__ __forceinline__ void tma_store(const CUtensorMap* m, const int32_t* c, uint32_t src,
+                                          uint64_t pol = 0)
+{
+    const uint64_t mp = reinterpret_cast<uint64_t>(m);
+    if constexpr (R == 1) {
+        TMK_STORE_ASM("1d", "%2", "%3", "r"(c[0]))
+    } else if constexpr (R == 2) {
+        TMK_STORE_ASM("2d", "%2, %3", "%4", "r"(c[0]), "r"(c[1]))
+    } else if constexpr (R == 3) {
+        TMK_STORE_ASM("3d", "%2, %3, %4", "%5", "r"(c[0]), "r"(c[1]), "r"(c[2]))
+    } else if constexpr (R == 4) {
+        TMK_STORE_ASM("4d", "%2, %3, %4, %5", "%6", "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]))
+    } else {
+        TMK_STORE_ASM("5d", "%2, %3, %4, %5, %6", "%7", "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]),
+                      "r"(c[4]))
+    }
+}
+#undef TMK_STORE_ASM
 
 // Shared -> global element-wise reduction into the tensor, op OP = 0 add, 1 min, 2 max; the map's
-// element type decides the arithmetic.
-#define TMK_RED_ASM(RANK, OPS, COORDS)                                                           \
-    asm volatile("cp.reduce.async.bulk.tensor." RANK ".global.shared::cta." OPS                 \
-                 ".tile.bulk_group [%0, {" COORDS "}], [%1];"
+// element type decides the arithmetic.  With H the global accesses carry the L2 policy `pol`.
+#define TMK_RED_ASM(RANK, OPS, COORDS, POL, ...)                                                 \
+    if constexpr (H) {                                                                           \
+        asm volatile("cp.reduce.async.bulk.tensor." RANK ".global.shared::cta." OPS             \
+                     ".tile.bulk_group.L2::cache_hint [%0, {" COORDS "}], [%1], " POL ";"        \
+                     ::"l"(mp), "r"(src), __VA_ARGS__, "l"(pol) : "memory");                     \
+    } else {                                                                                     \
+        asm volatile("cp.reduce.async.bulk.tensor." RANK ".global.shared::cta." OPS             \
+                     ".tile.bulk_group [%0, {" COORDS "}], [%1];"                                \
+                     ::"l"(mp), "r"(src), __VA_ARGS__ : "memory");                               \
+    }
 
-template <int R, int OP>
-__device__ __forceinline__ void tma_reduce(const CUtensorMap* m, const int32_t* c, uint32_t src)
+template <int R, int OP, bool H = false>
+__device__ __forceinline__ void tma_reduce(const CUtensorMap* m, const int32_t* c, uint32_t src,
+                                           uint64_t pol = 0)
 {
     const uint64_t mp = reinterpret_cast<uint64_t>(m);
     constexpr bool add = OP == 0, mn = OP == 1;
-#define TMK_RED_OP(RANK, COORDS, ...)                                                            \
+#define TMK_RED_OP(RANK, COORDS, POL, ...)                                                       \
     if constexpr (add) {                                                                         \
-        TMK_RED_ASM(RANK, "add", COORDS)::"l"(mp), "r"(src), __VA_ARGS__ : "memory");           \
+        TMK_RED_ASM(RANK, "add", COORDS, POL, __VA_ARGS__)                                       \
     } else if constexpr (mn) {                                                                   \
-        TMK_RED_ASM(RANK, "min", COORDS)::"l"(mp), "r"(src), __VA_ARGS__ : "memory");           \
+        TMK_RED_ASM(RANK, "min", COORDS, POL, __VA_ARGS__)                                       \
     } else {                                                                                     \
-        TMK_RED_ASM(RANK, "max", COORDS)::"l"(mp), "r"(src), __VA_ARGS__ : "memory");           \
+        TMK_RED_ASM(RANK, "max", COORDS, POL, __VA_ARGS__)                                       \
     }
     if constexpr (R == 1) {
-        TMK_RED_OP("1d", "%2", "r"(c[0]))
+        TMK_RED_OP("1d", "%2", "%3", "r"(c[0]))
     } else if constexpr (R == 2) {
-        TMK_RED_OP("2d", "%2, %3", "r"(c[0]), "r"(c[1]))
+        TMK_RED_OP("2d", "%2, %3", "%4", "r"(c[0]), "r"(c[1]))
     } else if constexpr (R == 3) {
-        TMK_RED_OP("3d", "%2, %3, %4", "r"(c[0]), "r"(c[1]), "r"(c[2]))
+        TMK_RED_OP("3d", "%2, %3, %4", "%5", "r"(c[0]), "r"(c[1]), "r"(c[2]))
     } else if constexpr (R == 4) {
-        TMK_RED_OP("4d", "%2, %3, %4, %5", "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]))
+        TMK_RED_OP("4d", "%2, %3, %4, %5", "%6", "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]))
     } else {
-        TMK_RED_OP("5d", "%2, %3, %4, %5, %6", "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]),
+        TMK_RED_OP("5d", "%2, %3, %4, %5, %6", "%7", "r"(c[0]), "r"(c[1]), "r"(c[2]), "r"(c[3]),
                    "r"(c[4]))
     }
 #undef TMK_RED_OP
@@ -222,18 +260,35 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* m, int32_t
                  ::"l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1) : "memory");
 }
 
-// ---- untiled bulk copies (contiguous bytes; both addresses 16-byte aligned, size % 16 == 0) ---
-__device__ __forceinline__ void bulk_load(uint32_t dst, uint64_t src, uint32_t bytes, uint32_t bar)
+// ---- untiled bulk copies (contiguous bytes; both addresses 16-byte aligned, size % 16 == 0;
+//      with H the global accesses carry the L2 policy `pol`) ---------------------------------------
+template <bool H = false>
+__device__ __forceinline__ void bulk_load(uint32_t dst, uint64_t src, uint32_t bytes, uint32_t bar,
+                                          uint64_t pol = 0)
 {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+    if constexpr (H) {
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+            " [%0], [%1], %2, [%3], %4;"
+            ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(pol) : "memory");
+    } else {
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+            ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+    }
 }
 
-__device__ __forceinline__ void bulk_store(uint64_t dst, uint32_t src, uint32_t bytes)
+template <bool H = false>
+__device__ __forceinline__ void bulk_store(uint64_t dst, uint32_t src, uint32_t bytes,
+                                           uint64_t pol = 0)
 {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
-                 ::"l"(dst), "r"(src), "r"(bytes) : "memory");
+    if constexpr (H) {
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;"
+                     ::"l"(dst), "r"(src), "r"(bytes), "l"(pol) : "memory");
+    } else {
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                     ::"l"(dst), "r"(src), "r"(bytes) : "memory");
+    }
 }
 
 // ---- bulk async groups ([MLSys-TMA] §"如何等待 TMA store 完成": commit, then wait until the

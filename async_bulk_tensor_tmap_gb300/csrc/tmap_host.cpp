@@ -64,15 +64,6 @@ uint32_t span_of(uint32_t sw)
     return sw == TM_SWIZZLE_128B ? 128u : sw == TM_SWIZZLE_64B ? 64u : sw == TM_SWIZZLE_32B ? 32u : 0u;
 }
 
-uint64_t env_u64(const char* name, uint64_t dflt)
-{
-    const char* v = getenv(name);
-    if (!v || !*v) return dflt;
-    char* end = nullptr;
-    unsigned long long x = strtoull(v, &end, 10);
-    return (end && *end == 0) ? (uint64_t)x : dflt;
-}
-
 bool valid_desc(const tm_desc* d) { return d && d->magic == TM_DESC_MAGIC; }
 
 // ---- driver entry points (no link-time dependency on libcuda) ---------------------------------
@@ -157,30 +148,6 @@ size_t cta_budget(const DevState& ds, uint32_t per_sm)
     const size_t share = (size_t)ds.smem_per_sm / per_sm;
     const size_t cap = std::min<size_t>((size_t)ds.smem_optin, share > 1024 ? share - 1024 : 0);
     return cap > 2048 + 256 ? cap - 1024 - 256 : 0;
-}
-
-struct Geometry {
-    uint32_t grid, stages;
-    size_t smem;
-};
-
-// The TMA streaming kernels: `per_sm` one-warp CTAs per SM (TM_CTAS_PER_SM, default 2), each with
-// as many stages as fit (TM_STAGES caps it); `nbox` counts work units (box groups).
-Geometry tma_geometry(const DevState& ds, uint64_t nbox, uint32_t stage_bytes)
-{
-    uint32_t per_sm = (uint32_t)std::min<uint64_t>(std::max<uint64_t>(env_u64("TM_CTAS_PER_SM", 2), 1), 16);
-    size_t budget = cta_budget(ds, per_sm);
-    while (per_sm > 1 && budget < 2ull * stage_bytes) budget = cta_budget(ds, --per_sm);
-    uint32_t stages = (uint32_t)std::min<size_t>(budget / stage_bytes, TM_MAX_STAGES);
-    const uint64_t cap = env_u64("TM_STAGES", 0);
-    if (cap > 0) stages = (uint32_t)std::min<uint64_t>(stages, cap);
-    stages = std::max<uint32_t>(stages, 1);
-    const uint64_t ctas = (uint64_t)ds.sms * per_sm;
-    Geometry g;
-    g.grid = (uint32_t)std::min<uint64_t>(nbox, ctas);
-    g.stages = stages;
-    g.smem = (size_t)stages * stage_bytes + kStageAlign;
-    return g;
 }
 
 uint32_t stage_bytes_of(uint64_t box_bytes)
@@ -270,6 +237,11 @@ FbArgs fb_args(const tm_desc* d, const BoxWalk& w, uint64_t images, const DevSta
 }
 
 // Arguments and launch geometry of a TMA streaming kernel over the walk's boxes.
+struct Geometry {
+    uint32_t grid;
+    size_t smem;
+};
+
 StreamArgs stream_args(const tm_desc* d, const BoxWalk& w, uint64_t images, const DevState& ds,
                        Geometry& g)
 {
@@ -277,13 +249,8 @@ StreamArgs stream_args(const tm_desc* d, const BoxWalk& w, uint64_t images, cons
     memset(&a, 0, sizeof(a));
     a.walk = w;
     a.images = images;
-    a.box_bytes = (uint32_t)d->box_bytes;
-    tma_group(d->box_bytes, span_of(d->swizzle),
-              std::max<uint64_t>(env_u64("TM_GROUP_BYTES", 32768), 1024), a.group, a.slot_bytes);
-    a.stage_bytes = stage_bytes_of((uint64_t)a.group * a.slot_bytes);
-    g = tma_geometry(ds, (w.nbox + a.group - 1) / a.group, a.stage_bytes);
-    a.stages = g.stages;
-    stream_schedule(a, g.grid);
+    stream_plan(a, d->box_bytes, span_of(d->swizzle), (uint32_t)ds.sms,
+                [&](uint32_t per_sm) { return cta_budget(ds, per_sm); }, g.grid, g.smem);
     a.timeout_ns = wait_limit_ns();
     a.status = ds.status;
     return a;
@@ -323,21 +290,10 @@ int copy_boxes(const tm_desc* src, const int32_t* coords, size_t nbox, void* ima
         uint32_t grid = 0;
         size_t smem = 0;
         SegArgs sa;
-        // TM_FB_SEG: 0 = never the segment form, 1 = whenever the layout allows it, unset = when
-        // its segments are long enough for bulk copies.  Defaults (2 CTAs per SM, 2 staging
-        // buffers: the largest items) measured best on GB300 on the W4 rank-5 view, 5.26 TB/s
-        // against 3.77 for the per-window form; deeper staging with smaller items was slower.
-        if (seg_plan(a, src, (uint32_t)ds->sms,
-                     (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_CTAS_PER_SM", 2), 8),
-                     (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_STAGES", 2), kSegMaxStages),
-                     (int)env_u64("TM_FB_SEG", 2), false,
-                     [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); }, sa, grid, smem)) {
+        if (fb_copy_plan(a, src, n, (uint32_t)ds->sms,
+                         [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); }, sa, grid, smem)) {
             rc = check_launch(launch_fb_seg_copy(sa, grid, smem, st), "fallback segment copy launch");
         } else {
-            fb_shape(a, n, (uint32_t)ds->sms,
-                     (uint32_t)std::min<uint64_t>(env_u64("TM_FB_COPY_CTAS_PER_SM", 8), 16),
-                     fb_copy_row_bytes(a.gspan0),
-                     [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); }, grid, smem);
             rc = check_launch(launch_fb_copy(a, grid, smem, st), "fallback copy launch");
         }
     }

@@ -4,8 +4,9 @@ TEST INFRASTRUCTURE ONLY.  The oracle defines what the GPU path must compute and
 the pages' definitions; only the test suite, the smoke check and the benchmark's CPU-baseline leg
 may import it.  It shares no code with the GPU library and never imports it.
 
-Pin status per function is listed in tmap_oracle.h; the 64-byte and 32-byte swizzle layouts are
-PARITY UNPINNED (the pages name those modes without defining them).
+Pin status per function is listed in tmap_oracle.h; the 64-byte and 32-byte swizzle layouts, which
+the pages name without defining, are pinned by the chunk patterns NVIDIA's public CUDA
+documentation gives for those modes.
 
 All dimension lists here are innermost first.  A map views a numpy buffer: `buf` (any dtype, used
 as raw bytes), a byte offset of element (0, ..., 0), dims, byte strides of dims 1..rank-1, the box

@@ -2,7 +2,8 @@
  * tmap_oracle.c -- plain, slow CPU oracle for descriptor-driven tiled tensor movement.
  *
  * TEST INFRASTRUCTURE ONLY: see tmap_oracle.h for who may use it, the page tags and the pin status
- * of every function (the 64-byte and 32-byte swizzle layouts are "parity unpinned").
+ * of every function (the 64-byte and 32-byte swizzle layouts, which the pages do not define, are
+ * pinned by NVIDIA's published chunk patterns for those modes).
  *
  * Everything here walks one element (or one byte) at a time in the order the definitions state.
  * There is no blocking, vectorisation or reordering, so that each function can be checked against
@@ -26,7 +27,8 @@
  * 4..6.  For the 64-byte and 32-byte modes, which the pages name but do not define, this library
  * reads the same rule with two and one XOR bits (bits 7..8 into 4..5, bit 7 into 4): an atom of
  * 8 x 64 bytes resp. 8 x 32 bytes whose 16-byte chunks are permuted by the row bits above the 128-byte
- * line.  PARITY UNPINNED for those two modes.
+ * line.  That reading is the chunk pattern NVIDIA's public CUDA documentation draws for the two
+ * modes (repeating after 512 and 256 bytes), against which the tests check it.
  * ------------------------------------------------------------------------------------------- */
 uint64_t orc_swz(uint64_t off, uint32_t span)
 {

@@ -21,10 +21,13 @@
  *                             physical_sector = col XOR row, §"用 3D TMA 搬运多个 swizzle atoms"
  *                             physical_sector = logical_sector XOR (row % 8), and the bank-sector
  *                             formulas of §"128-byte swizzle 的分组要求".
- *   orc_swz span 64 / 32 .... PARITY UNPINNED: the pages name these modes (§"128-byte swizzle 的分组
- *                             要求", last paragraph) but never define their layout.  Read here as
- *                             the same address-bit rule with 2 / 1 XOR bits; only invariants
- *                             (bijection, involution, 16-byte units kept whole) are checked.
+ *   orc_swz span 64 / 32 .... pinned outside the pages: the pages name these modes (§"128-byte
+ *                             swizzle 的分组要求", last paragraph) but never define their layout.
+ *                             Read here as the same address-bit rule with 2 / 1 XOR bits, and
+ *                             checked byte by byte against the chunk patterns NVIDIA's public CUDA
+ *                             documentation draws for the 32B / 64B / 128B modes (a table in the
+ *                             tests' golden files, cited there); plus the invariants (bijection,
+ *                             involution, 16-byte units kept whole, eight bank sectors per column).
  *   orc_image / orc_store ... pinned: NONE mode equals numpy strided slicing of a zero-padded
  *                             tensor; 128B mode equals the page's sector-XOR-row rule applied to
  *                             that slice; store(image(x)) restores x with sentinels intact.

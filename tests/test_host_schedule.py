@@ -1,12 +1,14 @@
 """Host-side launch schedules, without a GPU.
 
-The streaming kernels read their launch-wide schedule from their arguments: the group (or tile)
-count, each CTA's share of it, and the box-counter step of one grid-wide advance.  The library
-computes these once on the host (stream_schedule, ring_schedule in csrc/tm_internal.h).  This test
-compiles those functions into a small host program and checks them on random shapes against the
-per-CTA definitions: CTA b of a grid of G takes groups b, b + G, ..., so it has
-(ngroups - 1 - b) // G + 1 of them, and one advance moves G * group boxes, written in the mixed
-radix of the grid's box counts (dim 0 fastest)."""
+The streaming kernels read their launch-wide schedule from their arguments: the full waves, the
+tail split, and the box-counter step of one grid-wide advance.  The library computes these once on
+the host (stream_schedule, ring_schedule in csrc/tm_internal.h), and the streaming kernel finds each
+item's boxes with stream_item, which compiles for the host as well.  This test builds those
+functions into a small host program and checks them on random shapes against the per-CTA
+definitions: with grid CTAs and G boxes per stage, CTA c takes boxes (j * grid + c) * G .. + G - 1
+of each full wave j, then q + (c < r) consecutive boxes of the R boxes left over (q = R // grid,
+r = R % grid); one advance moves grid * G boxes, written in the mixed radix of the grid's box
+counts (dim 0 fastest).  The program also checks that the items cover every box exactly once."""
 import os
 import random
 import shutil
@@ -20,6 +22,7 @@ CUDA_INC = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include
 PROGRAM = r"""
 #include <cstdio>
 #include <cstring>
+#include <vector>
 #include "tm_internal.h"
 using namespace tmk;
 int main() {
@@ -37,9 +40,29 @@ int main() {
             for (int i = 0; i < 5; i++) a.walk.grid_nb[i] = nb[i];
             a.group = group;
             stream_schedule(a, grid);
-            printf("%llu %llu %u %u %u %u %u %u\n", (unsigned long long)a.ngroups,
-                   (unsigned long long)a.n_base, a.n_rem, a.dstep[0], a.dstep[1], a.dstep[2],
-                   a.dstep[3], a.dstep[4]);
+            printf("%llu %llu %u %u %u %u %u %u %u\n", (unsigned long long)a.waves,
+                   (unsigned long long)a.tail0, a.tail_q, a.tail_r, a.dstep[0], a.dstep[1],
+                   a.dstep[2], a.dstep[3], a.dstep[4]);
+            // every CTA's items: count, boxes, first and last box; coverage of [0, nbox)
+            std::vector<unsigned char> seen(nbox, 0);
+            bool ok = true;
+            for (unsigned c = 0; c < grid; c++) {
+                const unsigned long long n = stream_items(a, c);
+                unsigned long long boxes = 0, first = 0, last = 0;
+                for (unsigned long long i = 0; i < n; i++) {
+                    uint64_t b0;
+                    uint32_t cnt;
+                    stream_item(a, c, grid, i, b0, cnt);
+                    if (cnt < 1 || cnt > group || b0 + cnt > nbox) { ok = false; break; }
+                    for (uint32_t j = 0; j < cnt; j++) ok = ok && seen[b0 + j]++ == 0;
+                    if (i == 0) first = b0;
+                    last = b0 + cnt - 1;
+                    boxes += cnt;
+                }
+                printf("%llu %llu %llu %llu\n", n, boxes, first, last);
+            }
+            for (unsigned long long b = 0; b < nbox; b++) ok = ok && seen[b] == 1;
+            printf("%d\n", ok ? 1 : 0);
         } else {
             unsigned long long ntiles, anb, bnb;
             unsigned grid;
@@ -90,26 +113,60 @@ def digits(value, radix, rank):
     return out
 
 
+def expected_items(nbox, group, grid, c):
+    """CTA c's items by the definition: (first box, box count) of each."""
+    wave = grid * group
+    waves = nbox // wave
+    items = [((j * grid + c) * group, group) for j in range(waves)]
+    rest = nbox - waves * wave
+    q, r = divmod(rest, grid)
+    cnt = q + (1 if c < r else 0)
+    if cnt:
+        items.append((waves * wave + c * q + min(c, r), cnt))
+    return items
+
+
 def test_stream_schedule_matches_the_per_cta_definitions(program):
     rng = random.Random(7)
     cases = []
-    for _ in range(400):
+    for _ in range(300):
         rank = rng.randint(1, 5)
-        nb = [rng.randint(1, 300) if i < rank else 1 for i in range(5)]
+        nb = [rng.randint(1, 40) if i < rank else 1 for i in range(5)]
         nbox = 1
         for v in nb:
             nbox *= v
+        if nbox > 60000:
+            continue
         group = rng.choice([1, 2, 3, 4, 8, 16, 64])
         ngroups = -(-nbox // group)
         grid = rng.randint(1, min(ngroups, 1216))
         cases.append((nbox, group, rank, nb, grid))
+    # the bench's shapes: W3 (8192 boxes of 16 KiB, 2 a stage), W4 rank-3 (16384 and 32768 boxes,
+    # 4 and 8 a stage), W5a (65536 boxes, 2 a stage), over 304 CTAs
+    cases += [(8192, 2, 2, [128, 64, 1, 1, 1], 304), (16384, 4, 3, [16, 64, 16, 1, 1], 304),
+              (32768, 8, 3, [32, 64, 16, 1, 1], 304), (65536, 2, 2, [128, 512, 1, 1, 1], 304)]
     got = run(program, ["S %d %d %d %s %d" % (n, g, r, " ".join(map(str, nb)), gr)
                         for n, g, r, nb, gr in cases])
-    for (nbox, group, rank, nb, grid), (ngroups, n_base, n_rem, *dstep) in zip(cases, got):
-        assert ngroups == -(-nbox // group)
-        for b in range(grid):
-            assert n_base + (1 if b < n_rem else 0) == (ngroups - 1 - b) // grid + 1
+    pos = 0
+    for nbox, group, rank, nb, grid in cases:
+        waves, tail0, q, r, *dstep = got[pos]
+        per_cta = got[pos + 1:pos + 1 + grid]
+        ok = got[pos + 1 + grid][0]
+        pos += grid + 2
+        assert ok == 1, (nbox, group, grid)
+        assert (waves, tail0) == (nbox // (grid * group), nbox // (grid * group) * grid * group)
+        assert (q, r) == divmod(nbox - tail0, grid)
         assert dstep == digits(grid * group, nb, rank)
+        counts = []
+        for c, (n, boxes, first, last) in enumerate(per_cta):
+            want = expected_items(nbox, group, grid, c)
+            assert n == len(want)
+            assert boxes == sum(k for _, k in want)
+            if want:
+                assert (first, last) == (want[0][0], want[-1][0] + want[-1][1] - 1)
+            counts.append(boxes)
+        assert sum(counts) == nbox
+        assert max(counts) - min(counts) <= 1  # no CTA has more than one box above another
 
 
 def test_ring_schedule_matches_the_per_cta_definitions(program):

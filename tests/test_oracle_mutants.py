@@ -18,6 +18,16 @@ MUTANTS = {
     "swizzle_64b_takes_three_row_bits": ("xor_bits = 2;", "xor_bits = 3;"),
     "swizzle_32b_takes_two_row_bits": ("xor_bits = 1;", "xor_bits = 2;"),
     "swizzle_sector_bits_shifted": ("return off ^ (line << 4);", "return off ^ (line << 5);"),
+    # other valid-looking XOR patterns for the narrow modes (involutions that keep every chunk in
+    # its row, depend on row % 8 and still spread a column over eight bank sectors)
+    "swizzle_64b_row_bits_reversed": (
+        "uint64_t line = (off >> 7) & ((1u << xor_bits) - 1u);",
+        "uint64_t line = xor_bits == 2 ? (((off >> 8) & 1u) | (((off >> 7) & 1u) << 1))\n"
+        "                                : (off >> 7) & ((1u << xor_bits) - 1u);"),
+    "swizzle_32b_mixes_row_bits": (
+        "uint64_t line = (off >> 7) & ((1u << xor_bits) - 1u);",
+        "uint64_t line = xor_bits == 1 ? (((off >> 7) ^ (off >> 6)) & 1u)\n"
+        "                                : (off >> 7) & ((1u << xor_bits) - 1u);"),
     "oob_upper_off_by_one": ("(uint64_t)g[i] >= m->dim[i]", "(uint64_t)g[i] > m->dim[i]"),
     "oob_negative_dropped": ("if (g[i] < 0 || (uint64_t)g[i]", "if ((uint64_t)g[i] + 0 == 0 && (uint64_t)g[i]"),
     "image_axes_transposed": (

@@ -80,9 +80,9 @@ def test_w2_128b_image_is_four_swizzled_atoms(slice_no):
 
 @pytest.mark.parametrize("span,gcols", [(64, 32), (32, 16)])
 def test_w2_narrow_swizzles_permute_whole_sectors(span, gcols):
-    """64B / 32B: PARITY UNPINNED by the pages.  Invariants only: same 16-byte units as the
-    unswizzled image, each unit moved whole within its atom, and the units of one row stay
-    inside that row's atom span."""
+    """64B / 32B (the pages name them without defining them; their pin is the published pattern
+    test above): the same 16-byte units as the unswizzled image, each unit moved whole within its
+    atom."""
     x = workloads.w2_tensor()
     ng = 128 // gcols
     for start in [(0, 0, 0), (0, 0, ng)]:
@@ -96,8 +96,8 @@ def test_w2_narrow_swizzles_permute_whole_sectors(span, gcols):
 
 @pytest.mark.parametrize("span,gcols", [(64, 32), (32, 16)])
 def test_narrow_swizzles_spread_a_column_over_eight_bank_sectors(span, gcols):
-    """64B / 32B, still PARITY UNPINNED: the pages fix no permutation for them.  They fix its
-    purpose ([MLSys-TMA] "128-byte swizzle 的分组要求": eight rows reading the same column should
+    """64B / 32B: the pages fix no permutation for them (the published pattern test above pins
+    it).  They fix its purpose ([MLSys-TMA] "128-byte swizzle 的分组要求": eight rows reading the same column should
     hit eight distinct bank sectors, and a narrower atom is the fallback when 128 B do not fit),
     and, by the 128B rule of "TMA 如何写入 swizzled layout", that sectors move inside their own
     row by a pattern that depends on row % 8 only.  Checked on the W2 images against the
@@ -125,6 +125,28 @@ def test_narrow_swizzles_spread_a_column_over_eight_bank_sectors(span, gcols):
                 plain = {((r * span + c * 16) >> 4) & 7 for r in range(r0, r0 + 8)}
                 assert len(sectors) == 8
                 assert len(plain) == 16 * 8 // span
+
+
+# ---- all three swizzle modes against NVIDIA's published patterns -----------------------------
+def test_swizzle_modes_match_the_published_chunk_patterns():
+    """orc_swz for 32B, 64B and 128B against the chunk permutations NVIDIA's CUDA documentation
+    draws for the three modes (tests/golden/cuda_tma_swizzle_modes.txt, cited there), over four
+    repeats of each pattern, byte by byte: a 16-byte chunk moves whole, to the physical chunk the
+    table gives for its 128-byte line inside the repeat period.  This is the pin of the 64B and
+    32B modes, which the pages name but do not define."""
+    rows = read_golden("cuda_tma_swizzle_modes.txt")
+    table = {}
+    for r in rows:
+        mode, period, line, *phys = map(int, r)
+        table.setdefault((mode, period), {})[line] = phys
+    assert set(table) == {(32, 256), (64, 512), (128, 1024)}
+    for (mode, period), lines in table.items():
+        assert sorted(lines) == list(range(period // 128))
+        for off in range(4 * period):
+            line = (off % period) // 128
+            chunk, byte = (off % 128) // 16, off % 16
+            want = off - off % 128 + lines[line][chunk] * 16 + byte
+            assert oracle.swz(off, mode) == want, (mode, off)
 
 
 # ---- swizzle function invariants ------------------------------------------------------------
@@ -237,7 +259,7 @@ def test_brute_force_image_and_store(span):
         elif span == 128:
             np.testing.assert_array_equal(img, apply_page_swizzle128(
                 np.ascontiguousarray(none).reshape(-1).view(np.uint8)))
-        else:  # unpinned modes: same bytes per 16-byte unit, permuted inside each atom
+        else:  # narrow modes (pinned by the published patterns): same 16-byte units, permuted in each atom
             u_img = img.reshape(-1, 16)
             u_none = np.ascontiguousarray(none).reshape(-1).view(np.uint8).reshape(-1, 16)
             atom = 8 * span // 16

@@ -114,3 +114,26 @@ def test_noalloc_small_boxes_share_stages(tm):
     got = torch.full_like(want, 0x55)
     tm.tiled_copy_noalloc(m, None, got)
     assert torch.equal(got, want)
+
+
+def test_noalloc_on_a_non_default_stream(tm):
+    """The caller's own non-blocking stream: the status word is cleared and the box list uploaded
+    on that stream, the copy runs there, and the call reads the status back before returning.
+    Images as tiled_copy's, for a listed-box call (list staged in the scratch) and the whole grid."""
+    x = workloads.w3_tensor(520, 700, seed=78)
+    xd = _dev(x)
+    m = _map(tm, xd, 520, 700)
+    coords = [[int(64 * (b % m.d.nbox[0])), int(128 * (b // m.d.nbox[0]))]
+              for b in np.random.default_rng(9).permutation(m.num_boxes)[:29]]
+    s = torch.cuda.Stream()
+    for lst in (coords, None):
+        n = len(lst) if lst is not None else m.num_boxes
+        want = torch.zeros(n * m.box_bytes, dtype=torch.uint8, device="cuda")
+        tm.tiled_copy(m, lst, want)
+        torch.cuda.synchronize()
+        assert tm.tm_stream_check() == tm.TM_OK, tm.tm_last_error()
+        for _ in range(2):
+            got = torch.full_like(want, 0x66)
+            torch.cuda.synchronize()  # the fill is done before the other stream writes
+            tm.tiled_copy_noalloc(m, lst, got, stream=s)
+            assert torch.equal(got, want)
