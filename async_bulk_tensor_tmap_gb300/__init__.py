@@ -48,7 +48,9 @@ DESC_SIZE = 384
 TM_NOALLOC_MAX_BOXES = 16384
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-library_path = os.path.join(_HERE, "libtmap_gb300.so")
+# TMAP_GB300_TRACE=1 loads the tracing build (per-CTA timelines, async_bulk_tensor_tmap_gb300.timeline)
+_TRACE = os.environ.get("TMAP_GB300_TRACE") == "1"
+library_path = os.path.join(_HERE, "libtmap_gb300_trace.so" if _TRACE else "libtmap_gb300.so")
 
 if not os.path.exists(library_path):
     raise ImportError(
@@ -178,6 +180,11 @@ class TensorMap:
     @property
     def path(self) -> int:
         return int(_L.tm_path(self.ptr))
+
+    @property
+    def base(self) -> int:
+        """Device address of the tensor's element (0, ..., 0)."""
+        return int(self.d.base)
 
     @property
     def why_fallback(self) -> int:

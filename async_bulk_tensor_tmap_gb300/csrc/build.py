@@ -1,5 +1,9 @@
 """Build libtmap_gb300.so (sm_103a) in-tree with nvcc: one object per source, compiled in
-parallel, linked with the static CUDA runtime (no link-time dependency on libcuda)."""
+parallel, linked with the static CUDA runtime (no link-time dependency on libcuda).
+
+build(trace=True) builds the tracing variant instead, libtmap_gb300_trace.so (-DTM_TRACE: the
+streaming kernels and the ring write a %globaltimer stamp per CTA at fixed points; see
+async_bulk_tensor_tmap_gb300/timeline.py).  The default build never makes or loads it."""
 import os
 import shutil
 import subprocess
@@ -12,6 +16,7 @@ ROOT = os.path.dirname(PKG)
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtmap_gb300.so")
+TRACE_LIB = os.path.join(PKG, "libtmap_gb300_trace.so")
 
 SOURCES = ["tmap_host.cpp", "k_tma.cu", "k_fallback.cu", "k_fb_seg.cu", "k_ring.cu", "k_gemm.cu",
            "tm_noalloc.cu"]
@@ -35,14 +40,18 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), trace: bool = False) -> str:
+    build_dir = os.path.join(BUILD, "trace") if trace else BUILD
+    lib = TRACE_LIB if trace else LIB
+    if trace:
+        extra_flags = (*extra_flags, "-DTM_TRACE")
+    os.makedirs(build_dir, exist_ok=True)
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "tmap.h")]
     objs = []
     jobs = []
     for src in SOURCES:
         path = os.path.join(CSRC, src)
-        obj = os.path.join(BUILD, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         objs.append(obj)
         if force or _stale(obj, [path] + hdrs):
             cmd = [nvcc(), *ARCH, *FLAGS, *extra_flags, "-c", path, "-o", obj]
@@ -57,13 +66,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with ThreadPoolExecutor(max(1, min(len(jobs), os.cpu_count() or 1))) as ex:
         list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
-                extra_flags=["-Xptxas", "-v"] if "--ptxas" in sys.argv else []))
+                extra_flags=["-Xptxas", "-v"] if "--ptxas" in sys.argv else [],
+                trace="--trace" in sys.argv))

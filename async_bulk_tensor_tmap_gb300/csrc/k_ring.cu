@@ -43,6 +43,11 @@
 
 namespace tmk {
 
+// Timeline of the tracing build (see TM_TRACE_BUFFER), per CTA: slot 0 entry, 1 the producer's
+// first tile pair issued, 2 + i the consumers done with tile i (its A checksum written; i < 56),
+// 60 the producer's last tile issued, 63 the CTA's last checksum written.
+TM_TRACE_BUFFER(ring)
+
 constexpr uint32_t kRingMaxStages = 8;
 constexpr uint32_t kRingMaxWpt = 4;                 // consumer warps per tile
 constexpr uint32_t kRingMaxGroups = 2;              // consumer groups (tiles i % groups)
@@ -78,6 +83,7 @@ __global__ void __launch_bounds__(kRingThreads, 1)
     const uint64_t n_local = r.n_base + (first < r.n_rem ? 1u : 0u);
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) TM_STAMP(ring, 0);
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < S; s++) {
@@ -173,6 +179,8 @@ __global__ void __launch_bounds__(kRingThreads, 1)
                 tma_load<2>(base + s * 2 * tile + tile, &mb, cb, bar);
             }
             if (r.prefetch) prefetch_to(i + 1 + r.prefetch);
+            if (i == 0) TM_STAMP(ring, 1);
+            if (i + 1 == n_local) TM_STAMP(ring, 60);
             advance(ld);
             if (++s == S) {
                 s = 0;
@@ -316,6 +324,10 @@ __global__ void __launch_bounds__(kRingThreads, 1)
             const uint64_t t = first + i * gridDim.x;
             cs_out[t] = part[0];
             bits_out[t] = total;
+            if (grp == 0) {
+                if (i < 56) TM_STAMP(ring, 2 + i);
+                if (i + 1 == n_local) TM_STAMP(ring, 63);
+            }
         }
     }
 }

@@ -34,6 +34,11 @@
 
 namespace tmk {
 
+// Timeline of the tracing build (see TM_TRACE_BUFFER), per CTA: slot 0 entry, 1 the first S items
+// issued, 2 + i item i's stage complete (i < 58), 62 the last write issued, 63 exit (every write
+// done).
+TM_TRACE_BUFFER(stream)
+
 // Counters of box b of the grid (as grid_counters), with 32-bit divisions whenever b and the box
 // counts fit in 32 bits: this runs before a CTA's first load.
 __device__ __forceinline__ void first_counters(const BoxWalk& w, uint64_t b, uint32_t* k)
@@ -68,6 +73,7 @@ __global__ void __launch_bounds__(32, 1)
     __shared__ __align__(8) uint64_t full_bar[TM_MAX_STAGES];
 
     if (!elect_one()) return;
+    TM_STAMP(stream, 0);
 
     // Work unit: an item of up to G consecutive boxes sharing one stage (their images are
     // consecutive in the tile-major buffer as well): the full waves, then this CTA's tail boxes.
@@ -212,6 +218,7 @@ __global__ void __launch_bounds__(32, 1)
     // Stage refilled after writing item i: the one item i - 1 used (its write may still be
     // reading), or with a single stage the one just written.
     const uint64_t lag = S > 1 ? 1 : 0;
+    TM_STAMP(stream, 1);
 
     for (; wr.i < n_local; advance(wr)) {
         if (!mbar_wait(smem_u32(&full_bar[wr.s]), wr.phase, a.timeout_ns)) {
@@ -224,6 +231,8 @@ __global__ void __launch_bounds__(32, 1)
             }
             break;
         }
+        if (wr.i < 58) TM_STAMP(stream, 2 + wr.i);
+        if (wr.i + 1 == n_local) TM_STAMP(stream, 62);
         write_out(wr);
         if (wr.i >= lag && ld.i < n_local) {
             if (lag) {
@@ -236,6 +245,7 @@ __global__ void __launch_bounds__(32, 1)
         }
     }
     bulk_wait_all<0>();
+    TM_STAMP(stream, 63);
 }
 
 template <int R>

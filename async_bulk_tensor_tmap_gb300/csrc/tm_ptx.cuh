@@ -28,6 +28,37 @@ __device__ __forceinline__ uint64_t gtimer_ns()
     return t;
 }
 
+// ---- per-CTA timeline (only in the tracing build, libtmap_gb300_trace.so, compiled with
+//      -DTM_TRACE; in the library itself the stamps compile to nothing) --------------------------
+// A kernel file declares its buffer with TM_TRACE_BUFFER(name): kTraceSlots %globaltimer stamps
+// per CTA for the first kTraceCtas CTAs, read and cleared from the host through
+// tm_trace_fetch_<name>() and tm_trace_clear_<name>().  TM_STAMP(name, slot) writes one stamp.
+#ifdef TM_TRACE
+constexpr uint32_t kTraceCtas = 2048, kTraceSlots = 64;
+#define TM_TRACE_BUFFER(NAME)                                                                     \
+    static __device__ unsigned long long g_trace_##NAME[kTraceCtas * kTraceSlots];                \
+    extern "C" int tm_trace_fetch_##NAME(void* host, size_t bytes)                                \
+    {                                                                                             \
+        const size_t n = bytes < sizeof(g_trace_##NAME) ? bytes : sizeof(g_trace_##NAME);         \
+        return (int)cudaMemcpyFromSymbol(host, g_trace_##NAME, n);                                \
+    }                                                                                             \
+    extern "C" int tm_trace_clear_##NAME(void)                                                    \
+    {                                                                                             \
+        void* p = nullptr;                                                                        \
+        cudaError_t e = cudaGetSymbolAddress(&p, g_trace_##NAME);                                 \
+        return (int)(e != cudaSuccess ? e : cudaMemset(p, 0, sizeof(g_trace_##NAME)));            \
+    }
+#define TM_STAMP(NAME, SLOT)                                                                      \
+    do {                                                                                          \
+        if (blockIdx.x < kTraceCtas) g_trace_##NAME[blockIdx.x * kTraceSlots + (SLOT)] = gtimer_ns(); \
+    } while (0)
+#else
+#define TM_TRACE_BUFFER(NAME)
+#define TM_STAMP(NAME, SLOT) \
+    do {                     \
+    } while (0)
+#endif
+
 // One thread of a full warp is chosen to issue ([MLSys-TMA] §"一个 thread 如何描述整个 tile": the
 // other lanes are masked while the request is submitted; [H200-TMA] §03: one issuing thread).
 __device__ __forceinline__ bool elect_one()

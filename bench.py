@@ -212,15 +212,28 @@ def extra_ops(h: HostWorkload):
 # ------------------------------------------------------------------------------------------------
 # GPU arm
 # ------------------------------------------------------------------------------------------------
+def bind_device(world: int, local: int):
+    """The one device this process uses: cuda:LOCAL_RANK under torchrun (one rank per GPU), cuda:0
+    alone.  Every buffer of the workload is allocated on it, and no rank touches another's."""
+    import torch
+    index = local if world > 1 else 0
+    torch.cuda.set_device(index)
+    return torch.device("cuda", index)
+
+
 class GpuWorkload:
-    def __init__(self, h: HostWorkload, stream, ring_stages: int = 4, gemm_stages: int = 7):
+    def __init__(self, h: HostWorkload, stream, ring_stages: int = 4, gemm_stages: int = 7,
+                 device=None, tm=None):
         import torch
 
-        import async_bulk_tensor_tmap_gb300 as tm
+        if tm is None:
+            import async_bulk_tensor_tmap_gb300 as tm
         self.tm, self.torch, self.stream = tm, torch, stream
+        self.device = device if device is not None else torch.device("cuda", torch.cuda.current_device())
         self.ring_stages = ring_stages
         self.gemm_stages = gemm_stages
-        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).reshape(-1).view(np.uint8)).cuda()
+        on = self.device
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).reshape(-1).view(np.uint8)).to(on)
         self.t = {k: dev(getattr(h, k)) for k in ("w3", "w4", "w5a_dst", "w5a_src", "w5b_a",
                                                   "w5b_b") if getattr(h, k) is not None}
         sw = {0: 0, 32: 1, 64: 2, 128: 3}
@@ -248,14 +261,14 @@ class GpuWorkload:
             self.maps["w5b_a"] = enc(bf, self.t["w5b_a"], h.r5b_a)
             self.maps["w5b_b"] = enc(bf, self.t["w5b_b"], h.r5b_b)
             n = self.maps["w5b_a"].num_boxes
-            self.t["cs_a"] = torch.zeros(n, dtype=torch.float32, device="cuda")
-            self.t["cs_b"] = torch.zeros(n, dtype=torch.float32, device="cuda")
-            self.t["bits_a"] = torch.zeros(n, dtype=torch.int64, device="cuda")
-            self.t["bits_b"] = torch.zeros(n, dtype=torch.int64, device="cuda")
+            self.t["cs_a"] = torch.zeros(n, dtype=torch.float32, device=on)
+            self.t["cs_b"] = torch.zeros(n, dtype=torch.float32, device=on)
+            self.t["bits_a"] = torch.zeros(n, dtype=torch.int64, device=on)
+            self.t["bits_b"] = torch.zeros(n, dtype=torch.int64, device=on)
         if h.w7_a is not None:
             (M, K), N = h.w7_a.shape, h.w7_b.shape[0]
             self.t["w7_a"], self.t["w7_b"] = dev(h.w7_a), dev(h.w7_b)
-            self.t["w7_c"] = torch.empty(M * N, dtype=torch.float32, device="cuda")
+            self.t["w7_c"] = torch.empty(M * N, dtype=torch.float32, device=on)
             self.maps["w7_a"] = tm.tmap_encode(bf, self.t["w7_a"], [K, M], [K * 2], [64, 128],
                                                swizzle=tm.TM_SWIZZLE_128B)
             self.maps["w7_b"] = tm.tmap_encode(bf, self.t["w7_b"], [K, N], [K * 2], [64, 256],
@@ -279,9 +292,23 @@ class GpuWorkload:
             if k in self.maps:
                 m = self.maps[k]
                 self.t[f"{k}_img"] = torch.empty(m.num_boxes * m.box_bytes, dtype=torch.uint8,
-                                                 device="cuda")
-        self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+                                                 device=on)
+        self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=on)
         self.paths = {k: m.path for k, m in self.maps.items()}
+        self.check_rank_local()
+
+    def check_rank_local(self):
+        """Every tensor of the workload lives on this process's device and every map describes
+        one of them: a kernel of this rank is never given another GPU's memory (no peer
+        operands; the ranks share nothing but the timing reduction)."""
+        spans = []
+        for k, t in self.t.items():
+            if t.device != self.device:
+                raise RuntimeError(f"buffer {k} is on {t.device}, not on this rank's {self.device}")
+            spans.append((t.data_ptr(), t.data_ptr() + t.numel() * t.element_size()))
+        for k, m in self.maps.items():
+            if not any(lo <= m.base < hi for lo, hi in spans):
+                raise RuntimeError(f"map {k} does not describe a buffer of this rank")
 
     def run_op(self, name, stream=None):
         tm, t, m = self.tm, self.t, self.maps
@@ -670,8 +697,9 @@ def measured_bf16_peak():
 
 
 def tma_kernel_source() -> bytes:
-    """What defines the tensor-map streaming kernels: k_tma.cu, tm_ptx.cuh and the BoxWalk /
-    StreamArgs structs of tm_internal.h."""
+    """What defines the tensor-map streaming kernels: k_tma.cu, tm_ptx.cuh and, of tm_internal.h,
+    everything from the BoxWalk struct to the end of stream_plan (the arguments, the work split,
+    the default L2 policies and the launch shape)."""
     csrc = os.path.join(ROOT, "async_bulk_tensor_tmap_gb300", "csrc")
     out = b""
     for f in ("k_tma.cu", "tm_ptx.cuh"):
@@ -680,7 +708,7 @@ def tma_kernel_source() -> bytes:
     with open(os.path.join(csrc, "tm_internal.h"), "rb") as fh:
         hdr = fh.read()
     i = hdr.index(b"struct BoxWalk")
-    j = hdr.index(b"};", hdr.index(b"struct StreamArgs")) + 2
+    j = hdr.index(b"\n}\n", hdr.index(b"inline void stream_plan(")) + 3
     return out + hdr[i:j]
 
 
@@ -746,17 +774,15 @@ def main():
         return run_reference(args)
     import torch
     rank, world, local = dist_env()
+    device = bind_device(world, local)
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    else:
-        torch.cuda.set_device(0)
+        dist.init_process_group("nccl", device_id=device)
     h = HostWorkload(args.scale, args.ops.split(",") if args.ops else None,
                      0 if args.ring_swizzle == "none" else 128)
     ops = select_ops(h, args.ops)
     stream = torch.cuda.Stream()
-    g = GpuWorkload(h, stream, args.ring_stages, args.gemm_stages)
+    g = GpuWorkload(h, stream, args.ring_stages, args.gemm_stages, device=device)
 
     def barrier():
         torch.cuda.synchronize()

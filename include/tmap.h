@@ -81,9 +81,10 @@ typedef enum tm_oob { TM_OOB_ZERO = 0, TM_OOB_NAN = 1 } tm_oob;
 #define TM_WHY_BASE 2u     /* the base address is not 16-byte aligned ([H200-TMA] §03)           */
 #define TM_WHY_DRIVER 4u   /* the driver's encoder refused the map                               */
 #define TM_WHY_FORCED 8u   /* tmap_force_fallback() was called                                   */
-#define TM_WHY_STEP0 16u   /* elementStrides[0] > 1: measured on GB300, a tensor-map load of such a
-                            * map does not deliver rows of ceil(boxDim[0] / elementStrides[0])
-                            * packed elements (its byte count never completes)                  */
+#define TM_WHY_STEP0 16u   /* elementStrides[0] > 1: the tensor-map hardware ignores the step of
+                            * dim 0 in a non-interleaved map (NVIDIA's driver documentation of
+                            * cuTensorMapEncodeTiled says so) and delivers boxDim[0] elements per
+                            * row, not the ceil(boxDim[0] / elementStrides[0]) the image holds */
 
 /* ---- the descriptor -------------------------------------------------------------------------
  * [MLSys-TMA] §"一个 thread 如何描述整个 tile": the descriptor says how the whole tensor is laid
