@@ -73,7 +73,7 @@ def analyse(stamps: np.ndarray, event_us: float, nbytes: int, item_slots, share:
         "issue_us": round(float(np.median(rel[:, 1])), 2),
         "first_us": round(float(np.median(rel[:, item_slots[0]])), 2),
         "steady_GBps": round(steady),
-        "tail_us": round(span - q(0.9), 2),
+        "tail_us": round(span - q(0.9), 2) if share >= 1.0 else None,  # needs every stage stamped
         "spread_us": round(float(exit_.max() - exit_[exit_ >= 0].min()), 2),
         "ctas": int(len(t)),
         "GBps": round(nbytes / (event_us * 1e-6) / 1e9),
