@@ -20,7 +20,7 @@ TRACE_LIB = os.path.join(PKG, "libtmap_gb300_trace.so")
 
 SOURCES = ["tmap_host.cpp", "k_tma.cu", "k_fallback.cu", "k_fb_seg.cu", "k_ring.cu", "k_gemm.cu",
            "tm_noalloc.cu"]
-HEADERS = ["tm_internal.h", "tm_ptx.cuh"]
+HEADERS = ["tm_internal.h", "tm_ptx.cuh", "tm_gemm.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
          "--expt-relaxed-constexpr"]
