@@ -35,8 +35,16 @@
 
 namespace tmk {
 
-constexpr uint32_t kSegConsumerWarps = 8;
-constexpr uint32_t kSegThreads = 32 * (1 + kSegConsumerWarps);
+// Timeline of the tracing build (see TM_TRACE_BUFFER), per CTA: slot 0 entry, 1 the producer's
+// first item staged, 2 + n the first consumer warp done with item n (n < 58), 61 the CTA's item
+// count (a number), 63 that warp done with its last item.  Shared by the copy and the store (one
+// of them runs at a time).
+TM_TRACE_BUFFER(seg)
+
+// Consumer warps per CTA: W (SegArgs::cwarps picks 8, 12 or 16; 8 unless TM_FB_SEG_WARPS says
+// otherwise), plus one producer warp.
+template <uint32_t W>
+constexpr uint32_t seg_threads() { return 32 * (1 + W); }
 
 namespace {
 
@@ -263,7 +271,9 @@ struct SegItem {
     uint32_t nr;   // image rows of the item in each box
 };
 
-__global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_copy(const __grid_constant__ SegArgs s)
+template <uint32_t kSegConsumerWarps>
+__global__ void __launch_bounds__(seg_threads<kSegConsumerWarps>(), 2)
+    k_fb_seg_copy(const __grid_constant__ SegArgs s)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kSegMaxStages];   // segments landed (count 1 + bytes)
@@ -283,6 +293,10 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_copy(const __grid_con
     const uint64_t total = per + (blockIdx.x < extra ? 1 : 0);
     if (total == 0) return;
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        TM_STAMP(seg, 0);
+        TM_TRACE_PUT(seg, 61, total);
+    }
     if (threadIdx.x == 0) {
         for (uint32_t i = 0; i < S; i++) {
             mbar_init(smem_u32(&full_bar[i]), 1);
@@ -345,6 +359,7 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_copy(const __grid_con
                 }
             }
             cur.next(s);
+            if (i == 0 && lane == 0) TM_STAMP(seg, 1);
             if (++b == S) {
                 b = 0;
                 lap++;
@@ -437,6 +452,10 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_copy(const __grid_con
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty_bar[sb]));  // this warp's reads are done
+        if (warp == 1 && lane == 0) {
+            if (n < 58) TM_STAMP(seg, 2 + n);
+            if (n + 1 == total) TM_STAMP(seg, 63);
+        }
     }
 }
 
@@ -448,7 +467,9 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_copy(const __grid_con
 // (Measured on GB300 and dropped: assembling each segment in shared memory and writing it back
 // with one bulk store, 71.9 against 64.9 us on the W4 rank-5 view -- a stage can then only be
 // reloaded after its write-back has read it, which serialises the pipeline.)
-__global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_store(const __grid_constant__ SegArgs s)
+template <uint32_t kSegConsumerWarps>
+__global__ void __launch_bounds__(seg_threads<kSegConsumerWarps>(), 2)
+    k_fb_seg_store(const __grid_constant__ SegArgs s)
 {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t full_bar[kSegMaxStages];
@@ -468,6 +489,10 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_store(const __grid_co
     const uint64_t total = per + (blockIdx.x < extra ? 1 : 0);
     if (total == 0) return;
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        TM_STAMP(seg, 0);
+        TM_TRACE_PUT(seg, 61, total);
+    }
     const uint32_t inner = a.inner_bytes;
     if (threadIdx.x == 0) {
         for (uint32_t i = 0; i < S; i++) {
@@ -520,6 +545,7 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_store(const __grid_co
                           nr * inner, bar);
             }
             cur.next(s);
+            if (i == 0 && lane == 0) TM_STAMP(seg, 1);
             if (++b == S) {
                 b = 0;
                 lap++;
@@ -584,25 +610,47 @@ __global__ void __launch_bounds__(kSegThreads, 2) k_fb_seg_store(const __grid_co
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty_bar[sb]));
+        if (warp == 1 && lane == 0) {
+            if (n < 58) TM_STAMP(seg, 2 + n);
+            if (n + 1 == total) TM_STAMP(seg, 63);
+        }
     }
 }
 
+namespace {
+template <uint32_t W>
+cudaError_t launch_store_w(const SegArgs& a, uint32_t grid, size_t smem, cudaStream_t st)
+{
+    cudaError_t e = cudaFuncSetAttribute(k_fb_seg_store<W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    k_fb_seg_store<W><<<grid, seg_threads<W>(), smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <uint32_t W>
+cudaError_t launch_copy_w(const SegArgs& a, uint32_t grid, size_t smem, cudaStream_t st)
+{
+    cudaError_t e = cudaFuncSetAttribute(k_fb_seg_copy<W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    k_fb_seg_copy<W><<<grid, seg_threads<W>(), smem, st>>>(a);
+    return cudaGetLastError();
+}
+}  // namespace
+
 cudaError_t launch_fb_seg_store(const SegArgs& a, uint32_t grid, size_t smem, cudaStream_t st)
 {
-    cudaError_t e =
-        cudaFuncSetAttribute(k_fb_seg_store, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k_fb_seg_store<<<grid, kSegThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    return a.cwarps == 16 ? launch_store_w<16>(a, grid, smem, st)
+           : a.cwarps == 12 ? launch_store_w<12>(a, grid, smem, st)
+                            : launch_store_w<8>(a, grid, smem, st);
 }
 
 cudaError_t launch_fb_seg_copy(const SegArgs& a, uint32_t grid, size_t smem, cudaStream_t st)
 {
-    cudaError_t e =
-        cudaFuncSetAttribute(k_fb_seg_copy, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    k_fb_seg_copy<<<grid, kSegThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    return a.cwarps == 16 ? launch_copy_w<16>(a, grid, smem, st)
+           : a.cwarps == 12 ? launch_copy_w<12>(a, grid, smem, st)
+                            : launch_copy_w<8>(a, grid, smem, st);
 }
 
 }  // namespace tmk

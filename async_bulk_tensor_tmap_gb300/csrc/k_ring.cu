@@ -45,7 +45,8 @@ namespace tmk {
 
 // Timeline of the tracing build (see TM_TRACE_BUFFER), per CTA: slot 0 entry, 1 the producer's
 // first tile pair issued, 2 + i the consumers done with tile i (its A checksum written; i < 56),
-// 60 the producer's last tile issued, 63 the CTA's last checksum written.
+// 60 the producer's last tile issued, 61 the CTA's tile count (a number), 63 the CTA's last
+// checksum written.
 TM_TRACE_BUFFER(ring)
 
 constexpr uint32_t kRingMaxStages = 8;
@@ -83,7 +84,10 @@ __global__ void __launch_bounds__(kRingThreads, 1)
     const uint64_t n_local = r.n_base + (first < r.n_rem ? 1u : 0u);
     const uint32_t warp = threadIdx.x >> 5;
     const uint32_t lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) TM_STAMP(ring, 0);
+    if (threadIdx.x == 0) {
+        TM_STAMP(ring, 0);
+        TM_TRACE_PUT(ring, 61, n_local);
+    }
 
     if (threadIdx.x == 0) {
         for (uint32_t s = 0; s < S; s++) {

@@ -35,8 +35,8 @@
 namespace tmk {
 
 // Timeline of the tracing build (see TM_TRACE_BUFFER), per CTA: slot 0 entry, 1 the first S items
-// issued, 2 + i item i's stage complete (i < 58), 62 the last write issued, 63 exit (every write
-// done).
+// issued, 2 + i item i's stage complete (i < 58), 61 the CTA's item count (a number), 62 the last
+// write issued, 63 exit (every write done).
 TM_TRACE_BUFFER(stream)
 
 // Counters of box b of the grid (as grid_counters), with 32-bit divisions whenever b and the box
@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(32, 1)
 
     if (!elect_one()) return;
     TM_STAMP(stream, 0);
+    TM_TRACE_PUT(stream, 61, stream_items(a, blockIdx.x));
 
     // Work unit: an item of up to G consecutive boxes sharing one stage (their images are
     // consecutive in the tile-major buffer as well): the full waves, then this CTA's tail boxes.

@@ -298,7 +298,7 @@ struct SegArgs {
     uint32_t stages;        // staging buffers (items in flight per CTA)
     uint64_t per;           // items per CTA: items / grid (CTAs below `extra` take one more),
     uint32_t extra;         // computed on the host with the grid
-    uint32_t pad;
+    uint32_t cwarps;        // consumer warps per CTA: 8, 12 or 16 (TM_FB_SEG_WARPS, default 8)
 };
 constexpr uint32_t kSegMinBytes = 512;  // shorter segments: the per-window copy (request rate)
 constexpr uint32_t kSegMaxGroups = 64;
@@ -349,6 +349,8 @@ inline bool seg_plan_rows(const FbArgs& a, uint64_t g1, uint32_t sms, uint32_t w
     grid = (uint32_t)(items < ctas ? items : ctas);
     s.per = items / grid;
     s.extra = (uint32_t)(items % grid);
+    const uint64_t w = env_u64("TM_FB_SEG_WARPS", 8);
+    s.cwarps = w >= 16 ? 16u : w >= 12 ? 12u : 8u;
     smem = store ? (size_t)S * ((size_t)nb0 * s.img_stride + 8ull * s.block_groups * g1) + 16
                  : (size_t)S * s.block_groups * (s.seg_stride + 4 * g1) + 16;
     return true;

@@ -32,7 +32,8 @@ __device__ __forceinline__ uint64_t gtimer_ns()
 //      -DTM_TRACE; in the library itself the stamps compile to nothing) --------------------------
 // A kernel file declares its buffer with TM_TRACE_BUFFER(name): kTraceSlots %globaltimer stamps
 // per CTA for the first kTraceCtas CTAs, read and cleared from the host through
-// tm_trace_fetch_<name>() and tm_trace_clear_<name>().  TM_STAMP(name, slot) writes one stamp.
+// tm_trace_fetch_<name>() and tm_trace_clear_<name>().  TM_STAMP(name, slot) writes one stamp,
+// TM_TRACE_PUT(name, slot, value) a plain number (a CTA's item count, say).
 #ifdef TM_TRACE
 constexpr uint32_t kTraceCtas = 2048, kTraceSlots = 64;
 #define TM_TRACE_BUFFER(NAME)                                                                     \
@@ -48,14 +49,18 @@ constexpr uint32_t kTraceCtas = 2048, kTraceSlots = 64;
         cudaError_t e = cudaGetSymbolAddress(&p, g_trace_##NAME);                                 \
         return (int)(e != cudaSuccess ? e : cudaMemset(p, 0, sizeof(g_trace_##NAME)));            \
     }
-#define TM_STAMP(NAME, SLOT)                                                                      \
+#define TM_STAMP(NAME, SLOT) TM_TRACE_PUT(NAME, SLOT, gtimer_ns())
+#define TM_TRACE_PUT(NAME, SLOT, VALUE)                                                           \
     do {                                                                                          \
-        if (blockIdx.x < kTraceCtas) g_trace_##NAME[blockIdx.x * kTraceSlots + (SLOT)] = gtimer_ns(); \
+        if (blockIdx.x < kTraceCtas) g_trace_##NAME[blockIdx.x * kTraceSlots + (SLOT)] = (VALUE); \
     } while (0)
 #else
 #define TM_TRACE_BUFFER(NAME)
 #define TM_STAMP(NAME, SLOT) \
     do {                     \
+    } while (0)
+#define TM_TRACE_PUT(NAME, SLOT, VALUE) \
+    do {                                \
     } while (0)
 #endif
 

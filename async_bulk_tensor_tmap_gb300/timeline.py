@@ -53,10 +53,12 @@ def _stamps(lib, name: str) -> np.ndarray:
     return buf
 
 
-def analyse(stamps: np.ndarray, event_us: float, nbytes: int, item_slots, share: float = 1.0) -> dict:
-    """The decomposition above for one launch; nbytes: algorithmic bytes of the launch; share: the
-    part of the launch's stages that have a stamp (each CTA stamps its first len(item_slots))."""
+def analyse(stamps: np.ndarray, event_us: float, nbytes: int, item_slots) -> dict:
+    """The decomposition above for one launch; nbytes: algorithmic bytes of the launch.  Each CTA
+    stamps its first len(item_slots) stages and records its stage count in slot 61."""
     t = stamps[stamps[:, 0] > 0].astype(np.int64)
+    counts = t[:, 61]
+    share = float(np.minimum(counts, len(item_slots)).sum() / max(1, counts.sum()))
     t0 = t[:, 0].min()
     rel = np.where(t > 0, t - t0, -1) / 1000.0
     exit_ = rel[:, SLOTS - 1]
@@ -98,7 +100,7 @@ def main():
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).reshape(-1).view(np.uint8)).cuda()
 
-    def timed(fn, kname, nbytes, item_slots, reps, share=1.0):
+    def timed(fn, kname, nbytes, item_slots, reps):
         for _ in range(3):
             flush.fill_(1)
             fn()
@@ -120,7 +122,7 @@ def main():
             raise RuntimeError(tm.tm_last_error())
         runs.sort(key=lambda r: r[0])
         ev, st = runs[len(runs) // 2]
-        out = analyse(st, ev, nbytes, item_slots, share) if kname else {"event_us": round(ev, 2)}
+        out = analyse(st, ev, nbytes, item_slots) if kname else {"event_us": round(ev, 2)}
         out["event_us_all"] = [round(r[0], 2) for r in runs]
         return out
 
@@ -153,7 +155,18 @@ def main():
     img4 = torch.empty(m4.num_boxes * m4.box_bytes, dtype=torch.uint8, device="cuda")
     nb4 = 2 * 16 * 4095 * 1000 * 2
     res["w4r3.copy"] = timed(lambda: tm.tiled_copy(m4, None, img4), "stream", nb4, stream_items, args.reps)
-    del x4d, img4
+    # the rank-5 view (200-byte stride): the vector path's segment kernels
+    r5 = workloads.w4_rank5_map(span=128)
+    m5 = tm.tmap_encode(tm.TM_BF16, x4d, r5["dims"], r5["strides"], r5["box"], swizzle=sw)
+    out4 = x4d.clone()
+    m5o = tm.tmap_encode(tm.TM_BF16, out4, r5["dims"], r5["strides"], r5["box"], swizzle=sw)
+    img5 = torch.empty(m5.num_boxes * m5.box_bytes, dtype=torch.uint8, device="cuda")
+    nb5 = 16 * 4095 * 1000 * 2 + m5.num_boxes * m5.box_bytes
+    seg_items = list(range(2, 60))
+    res["w4r5.copy"] = timed(lambda: tm.tiled_copy(m5, None, img5), "seg", nb5, seg_items, args.reps)
+    res["w4r5.roundtrip"] = timed(lambda: tm.tiled_roundtrip(m5o, None, img5), "seg", nb5, seg_items,
+                                  args.reps)
+    del x4d, img4, out4, img5
 
     a, b = workloads.w5b_tensors()
     ra, rb = workloads.w5b_maps()
@@ -172,10 +185,8 @@ def main():
     dd, sd = dev(d), dev(s)
     md = tm.tmap_encode(tm.TM_F32, dd, r5["dims"], r5["strides"], r5["box"], swizzle=sw)
     ms = tm.tmap_encode(tm.TM_F32, sd, r5["dims"], r5["strides"], r5["box"], swizzle=sw)
-    # 65536 boxes, two a stage, over 304 CTAs: 108 stages each, of which the first 58 are stamped
     res["w5a.reduce"] = timed(lambda: tm.tile_reduce_add(md, ms), "stream", 3 * 4 * d.size,
-                              stream_items, max(3, args.reps // 2), share=58 / 108)
-    res["w5a.reduce"]["note"] = "stamps cover the first 58 of each CTA's 108 stages"
+                              stream_items, max(3, args.reps // 2))
 
     cols = ["event_us", "outside_us", "span_us", "issue_us", "first_us", "steady_GBps", "tail_us",
             "spread_us", "GBps"]
