@@ -74,14 +74,15 @@ __global__ void __launch_bounds__(32, 1)
 
     if (!elect_one()) return;
     TM_STAMP(stream, 0);
-    TM_TRACE_PUT(stream, 61, stream_items(a, blockIdx.x));
 
     // Work unit: an item of up to G consecutive boxes sharing one stage (their images are
-    // consecutive in the tile-major buffer as well): the full waves, then this CTA's tail boxes.
+    // consecutive in the tile-major buffer as well).
     const uint32_t cta = blockIdx.x, grid_ctas = gridDim.x;
-    const uint64_t n_local = stream_items(a, cta);
-    if (n_local == 0) return;
+    const bool dyn = a.sched != nullptr;
+    const uint64_t n_local = dyn ? 0 : stream_items(a, cta);  // static schedule only
+    if (!dyn && n_local == 0) return;
     const uint32_t S = a.stages;
+    const uint32_t G = a.group;
     const uint32_t base = (smem_u32(smem_raw) + (kStageAlign - 1)) & ~(kStageAlign - 1);
 
     if constexpr (KIND != KIND_ROUNDTRIP) prefetch_tmap(&in_map);
@@ -94,64 +95,92 @@ __global__ void __launch_bounds__(32, 1)
 
     const bool grid = a.walk.mode == WALK_GRID;
 
-    // Item i of this CTA: its stage, the phase parity of that stage's barrier, its first box and
-    // box count, and (grid walks) the counters of its first box.
-    struct Cursor {
-        uint64_t i, b0;
-        uint32_t s, phase, cnt;
+    // An item: its first box, its box count and (grid walks) the counters of its first box.  rec[s]
+    // is the item stage s holds, written when its loads are issued, read when it is written out.
+    struct Item {
+        uint64_t b0;
+        uint32_t cnt;
         uint32_t k[5];
     };
-    const uint32_t* const dstep = a.dstep;  // digits of G * gridDim.x boxes (from the host)
-    Cursor ld;
-    ld.i = 0;
-    ld.s = 0;
-    ld.phase = 0;
-    stream_item(a, cta, grid_ctas, 0, ld.b0, ld.cnt);
-    uint32_t tail_k[5] = {0, 0, 0, 0, 0};  // counters of the tail item's first box
-    if (grid) {
-        first_counters(a.walk, ld.b0, ld.k);
-        if (a.waves > 0 && a.waves < n_local) {
-            uint64_t tb;
-            uint32_t tc;
-            stream_item(a, cta, grid_ctas, a.waves, tb, tc);
-            first_counters(a.walk, tb, tail_k);
-        }
+    Item rec[TM_MAX_STAGES];
+
+    // The loads' source of items.  Static: this CTA's items of the host's schedule (stream_item),
+    // their counters stepped by G * gridDim.x boxes with carries (the tail item's found once).
+    // Dynamic: items g = 0 .. nitems - 1 of G boxes each (the last one short); CTA c first takes
+    // c, c + gridDim.x, ... for its first S stages, then each further item from the launch's
+    // counter (S * gridDim.x + atomicAdd), fetched one item ahead so that the atomic's round trip
+    // overlaps the wait for a stage.  A CTA that runs faster than others takes more items.
+    uint64_t si = 0;                        // static: the next item index of this CTA
+    uint32_t sk[5] = {0, 0, 0, 0, 0};       // static: counters of item si - 1
+    uint32_t tail_k[5] = {0, 0, 0, 0, 0};   // static: counters of the tail item's first box
+    uint64_t dj = 0;                        // dynamic: items of the static prefix taken
+    unsigned long long pend = 0;            // dynamic: the counter value fetched ahead
+    const uint64_t prefix = (uint64_t)S * grid_ctas;
+    if (dyn) {
+        if (prefix < a.nitems) pend = atomicAdd(a.sched, 1ull);
+    } else if (grid && a.waves > 0 && a.waves < n_local) {
+        uint64_t tb;
+        uint32_t tc;
+        stream_item(a, cta, grid_ctas, a.waves, tb, tc);
+        first_counters(a.walk, tb, tail_k);
     }
-    Cursor wr = ld;
-    auto advance = [&](Cursor& c) {
-        c.i++;
-        if (++c.s == S) {
-            c.s = 0;
-            c.phase ^= 1u;
+    auto next_item = [&](Item& it) -> bool {
+        if (dyn) {
+            uint64_t g;
+            if (dj < S) {
+                g = cta + dj * grid_ctas;
+                dj++;
+                if (g >= a.nitems) {
+                    dj = S;  // the prefix has no more items for this CTA
+                    g = prefix + pend;
+                    if (g >= a.nitems) return false;
+                    pend = atomicAdd(a.sched, 1ull);
+                }
+            } else {
+                g = prefix + pend;
+                if (g >= a.nitems) return false;
+                pend = atomicAdd(a.sched, 1ull);
+            }
+            it.b0 = g * G;
+            const uint64_t left = a.walk.nbox - it.b0;
+            it.cnt = left < G ? (uint32_t)left : G;
+            if (grid) first_counters(a.walk, it.b0, it.k);
+            return true;
         }
-        if (c.i >= n_local) return;
-        stream_item(a, cta, grid_ctas, c.i, c.b0, c.cnt);
+        if (si >= n_local) return false;
+        stream_item(a, cta, grid_ctas, si, it.b0, it.cnt);
         if (grid) {
-            if (c.i < a.waves) {
-                grid_add(a.walk, c.k, dstep);
+            if (si == 0) {
+                first_counters(a.walk, it.b0, sk);
+            } else if (si < a.waves) {
+                grid_add(a.walk, sk, a.dstep);
             } else {
 #pragma unroll
-                for (int d = 0; d < 5; d++) c.k[d] = tail_k[d];
+                for (int d = 0; d < 5; d++) sk[d] = tail_k[d];
             }
+#pragma unroll
+            for (int d = 0; d < 5; d++) it.k[d] = sk[d];
         }
+        si++;
+        return true;
     };
 
-    // Calls fn(j, coords) for the boxes of the cursor's item, in order.
-    auto for_boxes = [&](const Cursor& c, auto&& fn) {
+    // Calls fn(j, coords) for the boxes of an item, in order.
+    auto for_boxes = [&](const Item& it, auto&& fn) {
         int32_t co[5];
         if (grid) {
             uint32_t k[5];
 #pragma unroll
-            for (int d = 0; d < 5; d++) k[d] = c.k[d];
-            for (uint32_t j = 0; j < c.cnt; j++) {
+            for (int d = 0; d < 5; d++) k[d] = it.k[d];
+            for (uint32_t j = 0; j < it.cnt; j++) {
 #pragma unroll
                 for (int d = 0; d < 5; d++) co[d] = (int32_t)(k[d] * a.walk.box[d]);
                 fn(j, co);
                 grid_next(a.walk, k);
             }
         } else {
-            for (uint32_t j = 0; j < c.cnt; j++) {
-                box_start(a.walk, c.b0 + j, co);
+            for (uint32_t j = 0; j < it.cnt; j++) {
+                box_start(a.walk, it.b0 + j, co);
                 fn(j, co);
             }
         }
@@ -162,44 +191,44 @@ __global__ void __launch_bounds__(32, 1)
     // in the stage and move one bulk copy per box.
     const uint32_t slot = a.slot_bytes;
     const bool dense = slot == a.box_bytes;
-    auto issue = [&](const Cursor& c) {
-        const uint32_t bar = smem_u32(&full_bar[c.s]);
-        const uint32_t dst = base + c.s * a.stage_bytes;
-        mbar_arrive_expect_tx(bar, c.cnt * a.box_bytes);
+    auto issue = [&](const Item& it, uint32_t s) {
+        const uint32_t bar = smem_u32(&full_bar[s]);
+        const uint32_t dst = base + s * a.stage_bytes;
+        mbar_arrive_expect_tx(bar, it.cnt * a.box_bytes);
         if constexpr (KIND == KIND_ROUNDTRIP) {
-            const uint64_t src = a.images + c.b0 * a.box_bytes;
+            const uint64_t src = a.images + it.b0 * a.box_bytes;
             if (dense) {
-                if (hint_ld) bulk_load<true>(dst, src, c.cnt * a.box_bytes, bar, pol_ld);
-                else bulk_load(dst, src, c.cnt * a.box_bytes, bar);
+                if (hint_ld) bulk_load<true>(dst, src, it.cnt * a.box_bytes, bar, pol_ld);
+                else bulk_load(dst, src, it.cnt * a.box_bytes, bar);
             } else {
-                for (uint32_t j = 0; j < c.cnt; j++) {
+                for (uint32_t j = 0; j < it.cnt; j++) {
                     if (hint_ld) bulk_load<true>(dst + j * slot, src + j * a.box_bytes, a.box_bytes, bar, pol_ld);
                     else bulk_load(dst + j * slot, src + j * a.box_bytes, a.box_bytes, bar);
                 }
             }
         } else {
-            for_boxes(c, [&](uint32_t j, const int32_t* co) {
+            for_boxes(it, [&](uint32_t j, const int32_t* co) {
                 if (hint_ld) tma_load<R, true>(dst + j * slot, &in_map, co, bar, pol_ld);
                 else tma_load<R>(dst + j * slot, &in_map, co, bar);
             });
         }
     };
 
-    auto write_out = [&](const Cursor& c) {
-        const uint32_t src = base + c.s * a.stage_bytes;
+    auto write_out = [&](const Item& it, uint32_t s) {
+        const uint32_t src = base + s * a.stage_bytes;
         if constexpr (KIND == KIND_COPY) {
-            const uint64_t dst = a.images + c.b0 * a.box_bytes;
+            const uint64_t dst = a.images + it.b0 * a.box_bytes;
             if (dense) {
-                if (hint_wr) bulk_store<true>(dst, src, c.cnt * a.box_bytes, pol_wr);
-                else bulk_store(dst, src, c.cnt * a.box_bytes);
+                if (hint_wr) bulk_store<true>(dst, src, it.cnt * a.box_bytes, pol_wr);
+                else bulk_store(dst, src, it.cnt * a.box_bytes);
             } else {
-                for (uint32_t j = 0; j < c.cnt; j++) {
+                for (uint32_t j = 0; j < it.cnt; j++) {
                     if (hint_wr) bulk_store<true>(dst + j * a.box_bytes, src + j * slot, a.box_bytes, pol_wr);
                     else bulk_store(dst + j * a.box_bytes, src + j * slot, a.box_bytes);
                 }
             }
         } else {
-            for_boxes(c, [&](uint32_t j, const int32_t* co) {
+            for_boxes(it, [&](uint32_t j, const int32_t* co) {
                 if constexpr (KIND == KIND_ROUNDTRIP) {
                     if (hint_wr) tma_store<R, true>(&out_map, co, src + j * slot, pol_wr);
                     else tma_store<R>(&out_map, co, src + j * slot);
@@ -212,40 +241,67 @@ __global__ void __launch_bounds__(32, 1)
         bulk_commit();
     };
 
-    while (ld.i < n_local && ld.i < S) {
-        issue(ld);
-        advance(ld);
+    // Loads run up to S items ahead of the writes; the stage refilled after writing item w is the
+    // one item w - 1 used (its write may still be reading), or with a single stage the one just
+    // written.
+    uint64_t issued = 0;
+    uint32_t ls = 0;  // stage of the next load
+    Item nx;
+    bool have = next_item(nx);
+    while (have && issued < S) {
+        issue(nx, ls);
+        rec[ls] = nx;
+        issued++;
+        ls = ls + 1 == S ? 0 : ls + 1;
+        have = next_item(nx);
     }
-    // Stage refilled after writing item i: the one item i - 1 used (its write may still be
-    // reading), or with a single stage the one just written.
-    const uint64_t lag = S > 1 ? 1 : 0;
     TM_STAMP(stream, 1);
+    const uint64_t lag = S > 1 ? 1 : 0;
 
-    for (; wr.i < n_local; advance(wr)) {
-        if (!mbar_wait(smem_u32(&full_bar[wr.s]), wr.phase, a.timeout_ns)) {
+    uint32_t ws = 0, wphase = 0;  // stage and phase parity of item w
+    for (uint64_t w = 0; w < issued; w++) {
+        if (!mbar_wait(smem_u32(&full_bar[ws]), wphase, a.timeout_ns)) {
             const uint32_t kid = KIND == KIND_COPY ? K_COPY : KIND == KIND_ROUNDTRIP ? K_ROUNDTRIP
                                                                                     : K_REDUCE;
-            record_timeout(a.status, kid, wr.s, wr.phase, wr.b0);
+            record_timeout(a.status, kid, ws, wphase, rec[ws].b0);
             // Let every load still in flight land (bounded) before the stages go away.
-            for (uint64_t j = wr.i + 1; j < ld.i; j++) {
+            for (uint64_t j = w + 1; j < issued; j++) {
                 mbar_wait(smem_u32(&full_bar[j % S]), (uint32_t)((j / S) & 1), a.timeout_ns);
             }
             break;
         }
-        if (wr.i < 58) TM_STAMP(stream, 2 + wr.i);
-        if (wr.i + 1 == n_local) TM_STAMP(stream, 62);
-        write_out(wr);
-        if (wr.i >= lag && ld.i < n_local) {
+        if (w < 58) TM_STAMP(stream, 2 + w);
+        write_out(rec[ws], ws);
+        if (w >= lag && have) {
             if (lag) {
-                bulk_wait_read<1>();  // item i - 1's write has read its stage
+                bulk_wait_read<1>();  // item w - 1's write has read its stage
             } else {
-                bulk_wait_read<0>();  // the only stage: item i's write has read it
+                bulk_wait_read<0>();  // the only stage: item w's write has read it
             }
-            issue(ld);
-            advance(ld);
+            issue(nx, ls);
+            rec[ls] = nx;
+            issued++;
+            ls = ls + 1 == S ? 0 : ls + 1;
+            have = next_item(nx);
+        }
+        if (++ws == S) {
+            ws = 0;
+            wphase ^= 1u;
         }
     }
+    TM_STAMP(stream, 62);
+    TM_TRACE_PUT(stream, 61, issued);
     bulk_wait_all<0>();
+    if (dyn) {
+        // The launch's counter goes back to zero for the next launch on this stream: the last CTA
+        // to get here knows that every CTA has made its last fetch.
+        __threadfence();
+        if (atomicAdd(a.sched + 1, 1ull) == (unsigned long long)grid_ctas - 1) {
+            atomicExch(a.sched, 0ull);
+            atomicExch(a.sched + 1, 0ull);
+            __threadfence();
+        }
+    }
     TM_STAMP(stream, 63);
 }
 

@@ -89,6 +89,12 @@ struct StreamArgs {
     uint32_t tail_r;
     uint32_t dstep[5];     // digits (radix: the grid's box counts) of grid x G boxes
     uint32_t pad;
+    // Dynamic work split (when sched is set): items g = 0 .. nitems - 1 of G boxes (the last one
+    // short); CTA c takes c, c + grid, ... for its first `stages` items, then the next free item
+    // from sched[0] (a counter of this launch's stream, zero at launch; sched[1] counts the CTAs
+    // that are done, and the last one sets both back to zero).
+    unsigned long long* sched;
+    uint64_t nitems;
 };
 
 // Default L2 policies of the streaming copies' loads and writes (see stream_plan).
@@ -204,6 +210,8 @@ inline void stream_plan(StreamArgs& a, uint64_t box_bytes, uint32_t span, uint32
     const uint64_t units = (a.walk.nbox + a.group - 1) / a.group;
     grid = (uint32_t)std::min<uint64_t>(units, (uint64_t)sms * per_sm);
     stream_schedule(a, grid);
+    a.nitems = units;
+    a.sched = nullptr;  // the static schedule unless the caller hands the launch a counter
     smem = (size_t)a.stages * a.stage_bytes + kStageAlign;
 }
 
@@ -325,7 +333,11 @@ inline bool seg_plan_rows(const FbArgs& a, uint64_t g1, uint32_t sms, uint32_t w
     const uint64_t S = std::min<uint32_t>(std::max<uint32_t>(stages, 2), kSegMaxStages);
     const uint64_t per_group =
         store ? S * (nb0 * g1 * a.inner_bytes + 8 * g1) : S * (seg_stride + 4 * g1);
-    const uint64_t fixed = 64;
+    // store: each box's image block is staged 16 bytes past a multiple of its image size, so that
+    // the blocks of a run start at different bank phases (chunk j of one box and chunk j of the
+    // next, read by neighbouring threads, would otherwise share a bank sector)
+    const uint64_t pad = store && nb0 > 1 ? 16 : 0;
+    const uint64_t fixed = 64 + S * nb0 * pad;
     uint32_t per_sm = want < 1 ? 1 : want;
     while (per_sm > 1 && budget(per_sm) < fixed + per_group) per_sm--;
     if (budget(per_sm) < fixed + per_group) return false;
@@ -342,7 +354,7 @@ inline bool seg_plan_rows(const FbArgs& a, uint64_t g1, uint32_t sms, uint32_t w
     s.seg_stride = store ? 0u : (uint32_t)seg_stride;
     s.nblk = (uint32_t)((groups + e - 1) / e);
     s.block_groups = (s.groups + s.nblk - 1) / s.nblk;
-    s.img_stride = store ? (uint32_t)((uint64_t)s.block_groups * g1 * a.inner_bytes) : 0u;
+    s.img_stride = store ? (uint32_t)((uint64_t)s.block_groups * g1 * a.inner_bytes + pad) : 0u;
     s.nrun = a.walk.nbox / nb0;
     const uint64_t items = s.nrun * s.nblk;
     const uint64_t ctas = (uint64_t)sms * per_sm;

@@ -102,12 +102,21 @@ ReplaceAddressFn replace_fn()
 }
 
 // ---- per-device state ---------------------------------------------------------------------------
+// Counters of the streaming kernels' dynamic work split: one per stream, never reassigned to
+// another stream (a stream's launches run in order, so they can share one; launches on different
+// streams may overlap, so they must not).  Each slot has its own 128-byte line.
+constexpr uint32_t kSchedSlots = 256;
+constexpr size_t kSchedSlotBytes = 128;
+
 struct DevState {
     bool ready = false;
     int sms = 0;
     int smem_per_sm = 0;
     int smem_optin = 0;
     StatusBlock* status = nullptr;
+    unsigned char* sched = nullptr;          // kSchedSlots counter slots, zero between launches
+    unsigned long long sched_stream[kSchedSlots] = {};  // stream id of each slot (0: free)
+    uint32_t sched_used = 0;
 };
 
 std::mutex g_mu;
@@ -132,6 +141,10 @@ int device_state(DevState** out)
             return cuda_fail(e, "cudaMalloc(status word)");
         if ((e = cudaMemset(d.status, 0, sizeof(StatusBlock))) != cudaSuccess)
             return cuda_fail(e, "cudaMemset(status word)");
+        if ((e = cudaMalloc((void**)&d.sched, kSchedSlots * kSchedSlotBytes)) != cudaSuccess)
+            return cuda_fail(e, "cudaMalloc(work counters)");
+        if ((e = cudaMemset(d.sched, 0, kSchedSlots * kSchedSlotBytes)) != cudaSuccess)
+            return cuda_fail(e, "cudaMemset(work counters)");
         d.ready = true;
     }
     *out = &d;
@@ -139,6 +152,34 @@ int device_state(DevState** out)
 }
 
 uint64_t wait_limit_ns() { return env_u64("TM_WAIT_TIMEOUT_NS", 1000000000ull); }
+
+// The work counter of `stream` for a streaming launch, or nullptr for the static split: while the
+// stream is being captured into a graph (a graph may later run beside direct launches on the
+// stream), when every slot belongs to another stream, or with TM_DYNAMIC=0.
+unsigned long long* sched_slot(DevState& ds, cudaStream_t stream)
+{
+    if (env_u64("TM_DYNAMIC", 1) == 0) return nullptr;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    if (cs != cudaStreamCaptureStatusNone) return nullptr;
+    unsigned long long id = 0;
+    if (cudaStreamGetId(stream, &id) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    id += 1;  // 0 marks a free slot
+    std::lock_guard<std::mutex> lk(g_mu);
+    for (uint32_t i = 0; i < ds.sched_used; i++)
+        if (ds.sched_stream[i] == id)
+            return reinterpret_cast<unsigned long long*>(ds.sched + (size_t)i * kSchedSlotBytes);
+    if (ds.sched_used == kSchedSlots) return nullptr;
+    const uint32_t i = ds.sched_used++;
+    ds.sched_stream[i] = id;
+    return reinterpret_cast<unsigned long long*>(ds.sched + (size_t)i * kSchedSlotBytes);
+}
 
 // ---- launch geometry ------------------------------------------------------------------------
 // Shared memory a CTA may use when `per_sm` CTAs share an SM (1 KiB per CTA is reserved by the
@@ -242,8 +283,8 @@ struct Geometry {
     size_t smem;
 };
 
-StreamArgs stream_args(const tm_desc* d, const BoxWalk& w, uint64_t images, const DevState& ds,
-                       Geometry& g)
+StreamArgs stream_args(const tm_desc* d, const BoxWalk& w, uint64_t images, DevState& ds,
+                       Geometry& g, cudaStream_t stream)
 {
     StreamArgs a;
     memset(&a, 0, sizeof(a));
@@ -251,6 +292,7 @@ StreamArgs stream_args(const tm_desc* d, const BoxWalk& w, uint64_t images, cons
     a.images = images;
     stream_plan(a, d->box_bytes, span_of(d->swizzle), (uint32_t)ds.sms,
                 [&](uint32_t per_sm) { return cta_budget(ds, per_sm); }, g.grid, g.smem);
+    a.sched = sched_slot(ds, stream);
     a.timeout_ns = wait_limit_ns();
     a.status = ds.status;
     return a;
@@ -281,7 +323,7 @@ int copy_boxes(const tm_desc* src, const int32_t* coords, size_t nbox, void* ima
     if ((rc = make_walk(src, coords, n, st, w))) return rc;
     if (tma) {
         Geometry g;
-        const StreamArgs a = stream_args(src, w, (uint64_t)images, *ds, g);
+        const StreamArgs a = stream_args(src, w, (uint64_t)images, *ds, g, st);
         const CUtensorMap* m = (const CUtensorMap*)src->tmap;
         rc = check_launch(launch_tma_stream(KIND_COPY, src->rank, m, m, a, g.grid, g.smem, st),
                           "tensor copy launch");
@@ -530,7 +572,7 @@ int tiled_roundtrip(const tm_desc* dst, const int32_t* coords, size_t nbox, cons
     if ((rc = make_walk(dst, coords, n, st, w))) return rc;
     if (tma) {
         Geometry g;
-        const StreamArgs a = stream_args(dst, w, (uint64_t)images, *ds, g);
+        const StreamArgs a = stream_args(dst, w, (uint64_t)images, *ds, g, st);
         const CUtensorMap* m = (const CUtensorMap*)dst->tmap;
         rc = check_launch(launch_tma_stream(KIND_ROUNDTRIP, dst->rank, m, m, a, g.grid, g.smem, st),
                           "tensor store launch");
@@ -594,7 +636,7 @@ int tile_reduce(const tm_desc* dst, const tm_desc* src, tm_redop op, void* strea
     const bool tma_op = op == TM_RED_ADD || red_type >= 3;
     if (tma_op && store_fits_tma(dst) && src->path == TM_PATH_TMA) {
         Geometry g;
-        const StreamArgs a = stream_args(dst, w, 0, *ds, g);
+        const StreamArgs a = stream_args(dst, w, 0, *ds, g, st);
         rc = check_launch(launch_tma_stream(KIND_REDUCE + (int)op, dst->rank,
                                             (const CUtensorMap*)src->tmap,
                                             (const CUtensorMap*)dst->tmap, a, g.grid, g.smem, st),
