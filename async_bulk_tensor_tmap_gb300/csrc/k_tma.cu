@@ -107,18 +107,20 @@ __global__ void __launch_bounds__(32, 1)
     // The loads' source of items.  Static: this CTA's items of the host's schedule (stream_item),
     // their counters stepped by G * gridDim.x boxes with carries (the tail item's found once).
     // Dynamic: items g = 0 .. nitems - 1 of G boxes each (the last one short); CTA c first takes
-    // c, c + gridDim.x, ... for its first S stages, then each further item from the launch's
-    // counter (S * gridDim.x + atomicAdd), fetched one item ahead so that the atomic's round trip
-    // overlaps the wait for a stage.  A CTA that runs faster than others takes more items.
+    // c, c + gridDim.x, ... for its first S stages, then batches of B consecutive items from the
+    // launch's counter (item S * gridDim.x + B * atomicAdd).  Each batch is fetched one batch
+    // ahead, right after a stage's loads are issued: the producer's next arrive (a release) then
+    // finds the atomic long done.  A CTA that runs faster than others takes more items.
     uint64_t si = 0;                        // static: the next item index of this CTA
     uint32_t sk[5] = {0, 0, 0, 0, 0};       // static: counters of item si - 1
     uint32_t tail_k[5] = {0, 0, 0, 0, 0};   // static: counters of the tail item's first box
     uint64_t dj = 0;                        // dynamic: items of the static prefix taken
-    unsigned long long pend = 0;            // dynamic: the counter value fetched ahead
+    unsigned long long pend = 0;            // dynamic: the batch fetched ahead
+    uint64_t bg = 0, bend = 0;              // dynamic: items bg .. bend - 1 of the current batch
+    bool refetch = false;                   // dynamic: the batch ahead was taken: fetch another
     const uint64_t prefix = (uint64_t)S * grid_ctas;
-    if (dyn) {
-        if (prefix < a.nitems) pend = atomicAdd(a.sched, 1ull);
-    } else if (grid && a.waves > 0 && a.waves < n_local) {
+    const uint32_t B = a.batch ? a.batch : 1u;
+    if (!dyn && grid && a.waves > 0 && a.waves < n_local) {
         uint64_t tb;
         uint32_t tc;
         stream_item(a, cta, grid_ctas, a.waves, tb, tc);
@@ -128,18 +130,18 @@ __global__ void __launch_bounds__(32, 1)
         if (dyn) {
             uint64_t g;
             if (dj < S) {
+                // the static prefix (if it ends early, so do the items: nitems < prefix)
                 g = cta + dj * grid_ctas;
                 dj++;
-                if (g >= a.nitems) {
-                    dj = S;  // the prefix has no more items for this CTA
-                    g = prefix + pend;
-                    if (g >= a.nitems) return false;
-                    pend = atomicAdd(a.sched, 1ull);
-                }
-            } else {
-                g = prefix + pend;
                 if (g >= a.nitems) return false;
-                pend = atomicAdd(a.sched, 1ull);
+            } else {
+                if (bg == bend) {  // the current batch is done: take the one fetched ahead
+                    bg = prefix + (uint64_t)pend * B;
+                    if (bg >= a.nitems) return false;
+                    bend = bg + B < a.nitems ? bg + B : a.nitems;
+                    refetch = true;
+                }
+                g = bg++;
             }
             it.b0 = g * G;
             const uint64_t left = a.walk.nbox - it.b0;
@@ -247,14 +249,15 @@ __global__ void __launch_bounds__(32, 1)
     uint64_t issued = 0;
     uint32_t ls = 0;  // stage of the next load
     Item nx;
-    bool have = next_item(nx);
-    while (have && issued < S) {
+    bool have = true;
+    while (issued < S && (have = next_item(nx))) {
         issue(nx, ls);
         rec[ls] = nx;
         issued++;
         ls = ls + 1 == S ? 0 : ls + 1;
-        have = next_item(nx);
     }
+    // dynamic: the first batch beyond the prefix, fetched while the first stages load
+    if (dyn && have && prefix < a.nitems) pend = atomicAdd(a.sched, 1ull);
     TM_STAMP(stream, 1);
     const uint64_t lag = S > 1 ? 1 : 0;
 
@@ -272,7 +275,7 @@ __global__ void __launch_bounds__(32, 1)
         }
         if (w < 58) TM_STAMP(stream, 2 + w);
         write_out(rec[ws], ws);
-        if (w >= lag && have) {
+        if (w >= lag && have && (have = next_item(nx))) {
             if (lag) {
                 bulk_wait_read<1>();  // item w - 1's write has read its stage
             } else {
@@ -282,7 +285,10 @@ __global__ void __launch_bounds__(32, 1)
             rec[ls] = nx;
             issued++;
             ls = ls + 1 == S ? 0 : ls + 1;
-            have = next_item(nx);
+            if (refetch) {  // after the issue: the next batch, fetched while this item loads
+                pend = atomicAdd(a.sched, 1ull);
+                refetch = false;
+            }
         }
         if (++ws == S) {
             ws = 0;

@@ -95,6 +95,8 @@ struct StreamArgs {
     // that are done, and the last one sets both back to zero).
     unsigned long long* sched;
     uint64_t nitems;
+    uint32_t batch;        // items per fetch from the counter
+    uint32_t pad2;
 };
 
 // Default L2 policies of the streaming copies' loads and writes (see stream_plan).
@@ -212,6 +214,7 @@ inline void stream_plan(StreamArgs& a, uint64_t box_bytes, uint32_t span, uint32
     stream_schedule(a, grid);
     a.nitems = units;
     a.sched = nullptr;  // the static schedule unless the caller hands the launch a counter
+    a.batch = 1;        // items per fetch of the dynamic split (the caller may raise it)
     smem = (size_t)a.stages * a.stage_bytes + kStageAlign;
 }
 

@@ -106,6 +106,7 @@ ReplaceAddressFn replace_fn()
 // another stream (a stream's launches run in order, so they can share one; launches on different
 // streams may overlap, so they must not).  Each slot has its own 128-byte line.
 constexpr uint32_t kSchedSlots = 256;
+constexpr uint64_t kReduceBatch = 4;
 constexpr size_t kSchedSlotBytes = 128;
 
 struct DevState {
@@ -283,8 +284,18 @@ struct Geometry {
     size_t smem;
 };
 
+// Items per fetch of the dynamic split.  Copies and round trips take one (measured on GB300 on
+// the 128 MiB W3 / W4 maps: 2-4 % faster than the static split, with 2 or 4 a fetch no better
+// than static).  Reductions take several: their counter sits in the L2 that also performs the
+// bulk reductions, and one fetch per item cost the W5a reduce-add 15 % (four: +3 % over static).
+uint32_t fetch_batch(bool reduce)
+{
+    const uint64_t b = reduce ? env_u64("TM_DYN_BATCH_REDUCE", kReduceBatch) : env_u64("TM_DYN_BATCH", 1);
+    return (uint32_t)std::min<uint64_t>(std::max<uint64_t>(b, 1), 64);
+}
+
 StreamArgs stream_args(const tm_desc* d, const BoxWalk& w, uint64_t images, DevState& ds,
-                       Geometry& g, cudaStream_t stream)
+                       Geometry& g, cudaStream_t stream, bool reduce)
 {
     StreamArgs a;
     memset(&a, 0, sizeof(a));
@@ -293,6 +304,7 @@ StreamArgs stream_args(const tm_desc* d, const BoxWalk& w, uint64_t images, DevS
     stream_plan(a, d->box_bytes, span_of(d->swizzle), (uint32_t)ds.sms,
                 [&](uint32_t per_sm) { return cta_budget(ds, per_sm); }, g.grid, g.smem);
     a.sched = sched_slot(ds, stream);
+    a.batch = fetch_batch(reduce);
     a.timeout_ns = wait_limit_ns();
     a.status = ds.status;
     return a;
@@ -323,7 +335,7 @@ int copy_boxes(const tm_desc* src, const int32_t* coords, size_t nbox, void* ima
     if ((rc = make_walk(src, coords, n, st, w))) return rc;
     if (tma) {
         Geometry g;
-        const StreamArgs a = stream_args(src, w, (uint64_t)images, *ds, g, st);
+        const StreamArgs a = stream_args(src, w, (uint64_t)images, *ds, g, st, false);
         const CUtensorMap* m = (const CUtensorMap*)src->tmap;
         rc = check_launch(launch_tma_stream(KIND_COPY, src->rank, m, m, a, g.grid, g.smem, st),
                           "tensor copy launch");
@@ -572,7 +584,7 @@ int tiled_roundtrip(const tm_desc* dst, const int32_t* coords, size_t nbox, cons
     if ((rc = make_walk(dst, coords, n, st, w))) return rc;
     if (tma) {
         Geometry g;
-        const StreamArgs a = stream_args(dst, w, (uint64_t)images, *ds, g, st);
+        const StreamArgs a = stream_args(dst, w, (uint64_t)images, *ds, g, st, false);
         const CUtensorMap* m = (const CUtensorMap*)dst->tmap;
         rc = check_launch(launch_tma_stream(KIND_ROUNDTRIP, dst->rank, m, m, a, g.grid, g.smem, st),
                           "tensor store launch");
@@ -636,7 +648,7 @@ int tile_reduce(const tm_desc* dst, const tm_desc* src, tm_redop op, void* strea
     const bool tma_op = op == TM_RED_ADD || red_type >= 3;
     if (tma_op && store_fits_tma(dst) && src->path == TM_PATH_TMA) {
         Geometry g;
-        const StreamArgs a = stream_args(dst, w, 0, *ds, g, st);
+        const StreamArgs a = stream_args(dst, w, 0, *ds, g, st, true);
         rc = check_launch(launch_tma_stream(KIND_REDUCE + (int)op, dst->rank,
                                             (const CUtensorMap*)src->tmap,
                                             (const CUtensorMap*)dst->tmap, a, g.grid, g.smem, st),
