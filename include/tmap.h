@@ -24,9 +24,15 @@
  *     inside a kernel (every mbarrier wait is bounded, default 1 s, TM_WAIT_TIMEOUT_NS overrides)
  *     is recorded in a per-device status word and reported by tm_stream_check().
  *   - The first call that launches work on a device allocates that device's 64-byte status word
- *     (cudaMalloc) and reads its attributes; make that first call before capturing a stream.
- *     A call given an explicit list of more than 8 boxes stages the list in device memory with
- *     cudaMallocAsync/cudaFreeAsync on `stream`.
+ *     and 32 KiB of work counters (cudaMalloc) and reads its attributes; make that first call
+ *     before capturing a stream.  A call given an explicit list of more than 8 boxes stages the
+ *     list in device memory with cudaMallocAsync/cudaFreeAsync on `stream`.
+ *   - The tensor-map copies, round trips and reduces split their boxes between CTAs dynamically:
+ *     a launch takes items from a work counter of its stream (one per stream, up to 256 streams a
+ *     device; zero between launches, reset by the launch itself), so a stream's launches must not
+ *     run on another stream's counter -- the library keys them by cudaStreamGetId.  A launch made
+ *     while its stream is being captured, launches on streams beyond the 256th, and TM_DYNAMIC=0
+ *     use a fixed split instead; the bytes written are the same either way.
  */
 #ifndef TMAP_GB300_H
 #define TMAP_GB300_H
