@@ -338,8 +338,10 @@ inline bool seg_plan_rows(const FbArgs& a, uint64_t g1, uint32_t sms, uint32_t w
         store ? S * (nb0 * g1 * a.inner_bytes + 8 * g1) : S * (seg_stride + 4 * g1);
     // store: each box's image block is staged 16 bytes past a multiple of its image size, so that
     // the blocks of a run start at different bank phases (chunk j of one box and chunk j of the
-    // next, read by neighbouring threads, would otherwise share a bank sector)
-    const uint64_t pad = store && nb0 > 1 ? 16 : 0;
+    // next, read by neighbouring threads, would otherwise share a bank sector: 29 % of the shared
+    // load wavefronts conflicted on the W4 rank-5 view).  Measured on GB300: no change in time
+    // either way, within run-to-run noise (TM_FB_SEG_PAD=0 drops the pad).
+    const uint64_t pad = store && nb0 > 1 && env_u64("TM_FB_SEG_PAD", 1) ? 16 : 0;
     const uint64_t fixed = 64 + S * nb0 * pad;
     uint32_t per_sm = want < 1 ? 1 : want;
     while (per_sm > 1 && budget(per_sm) < fixed + per_group) per_sm--;
