@@ -266,9 +266,84 @@ __device__ __forceinline__ void put_head(uint8_t* p, const uint4& v, int n)
 
 // What the producer leaves beside each staging buffer for the item it staged.
 struct SegItem {
-    uint64_t run;  // run index u: boxes u * run .. u * run + run - 1
+    uint64_t run;  // run index u: boxes u * run .. u * run + run - 1; kEndOfItems: no more items
     uint32_t r0;   // first image row of the item in its boxes
     uint32_t nr;   // image rows of the item in each box
+};
+constexpr uint64_t kEndOfItems = ~0ull;
+
+// Where the producer warp takes its items from (every lane runs it in step).  Static: the CTA's
+// contiguous share m0 .. m0 + total - 1 of the host's split.  Dynamic (s.sched set): CTA c first
+// takes items c, c + gridDim.x, ... for its S staging buffers, then batches of s.batch
+// consecutive items from the stream's counter (item S * gridDim.x + s.batch * atomicAdd), each
+// batch fetched one ahead, right after an item's bulk copies are issued (the next arrive is a
+// release and would otherwise wait for the atomic); a CTA that runs faster takes more items.
+struct SegSource {
+    bool dyn, first_fetch, refetch;
+    uint32_t S, B;
+    uint64_t m0, total, si, dj, prefix, bg, bend;
+    unsigned long long pend;  // lane 0: the batch fetched ahead
+
+    __device__ __forceinline__ void init(const SegArgs& s, uint64_t m0_, uint64_t total_)
+    {
+        dyn = s.sched != nullptr;
+        S = s.stages;
+        B = s.batch ? s.batch : 1u;
+        m0 = m0_;
+        total = total_;
+        si = dj = bg = bend = 0;
+        pend = 0;
+        prefix = (uint64_t)S * gridDim.x;
+        first_fetch = dyn && prefix < s.nitems;
+        refetch = false;
+    }
+    // The next item, or false when this CTA has none left.
+    __device__ __forceinline__ bool next(const SegArgs& s, uint64_t& m)
+    {
+        if (!dyn) {
+            if (si >= total) return false;
+            m = m0 + si++;
+            return true;
+        }
+        if (dj < S) {
+            m = blockIdx.x + dj * gridDim.x;
+            dj++;
+            return m < s.nitems;  // past the end of the prefix there is nothing left either
+        }
+        if (bg == bend) {
+            const unsigned long long p = __shfl_sync(0xffffffffu, pend, 0);
+            bg = prefix + p * B;
+            if (bg >= s.nitems) return false;
+            bend = bg + B < s.nitems ? bg + B : s.nitems;
+            refetch = true;
+        }
+        m = bg++;
+        return true;
+    }
+    // After an item's bulk copies: the first batch once the prefix is issued, then the next batch
+    // once the one fetched ahead has been taken.
+    __device__ __forceinline__ void after_issue(const SegArgs& s, uint32_t lane)
+    {
+        if (first_fetch && dj == S) {
+            if (lane == 0) pend = atomicAdd(s.sched, 1ull);
+            first_fetch = false;
+        } else if (refetch) {
+            if (lane == 0) pend = atomicAdd(s.sched, 1ull);
+            refetch = false;
+        }
+    }
+    // The launch's counter back to zero for the next launch of the stream: the last CTA to finish
+    // knows that every CTA has made its last fetch.
+    __device__ __forceinline__ void finish(const SegArgs& s, uint32_t lane)
+    {
+        if (!dyn || lane != 0) return;
+        __threadfence();
+        if (atomicAdd(s.sched + 1, 1ull) == (unsigned long long)gridDim.x - 1) {
+            atomicExch(s.sched, 0ull);
+            atomicExch(s.sched + 1, 0ull);
+            __threadfence();
+        }
+    }
 };
 
 template <uint32_t kSegConsumerWarps>
@@ -288,15 +363,12 @@ __global__ void __launch_bounds__(seg_threads<kSegConsumerWarps>(), 2)
     // row lies outside the tensor)
     int32_t* const tabs = reinterpret_cast<int32_t*>(smem_raw + (size_t)S * E * s.seg_stride);
 
-    const uint64_t per = s.per, extra = s.extra;  // the item split, from the host
+    const uint64_t per = s.per, extra = s.extra;  // the static item split, from the host
     const uint64_t m0 = blockIdx.x * per + (blockIdx.x < extra ? blockIdx.x : extra);
     const uint64_t total = per + (blockIdx.x < extra ? 1 : 0);
-    if (total == 0) return;
+    if (s.sched == nullptr && total == 0) return;
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        TM_STAMP(seg, 0);
-        TM_TRACE_PUT(seg, 61, total);
-    }
+    if (threadIdx.x == 0) TM_STAMP(seg, 0);
     if (threadIdx.x == 0) {
         for (uint32_t i = 0; i < S; i++) {
             mbar_init(smem_u32(&full_bar[i]), 1);
@@ -309,21 +381,29 @@ __global__ void __launch_bounds__(seg_threads<kSegConsumerWarps>(), 2)
     if (warp == 0) {
         // ---- producer: walks the CTA's items with a cursor (every lane keeps the same copy).
         // Item i goes to buffer i % S once the consumers have released that buffer's item i - S.
+        SegSource src;
+        src.init(s, m0, total);
         ItemCursor cur;
-        cur.init(s, m0);
+        if (!src.dyn) cur.init(s, m0);
         // item i: buffer b = i % S, lap = i / S; for i >= S it waits for the release of item
-        // i - S, the buffer's completion number lap - 1
+        // i - S, the buffer's completion number lap - 1.  After the last item, buffer b gets the
+        // end marker.
         uint32_t b = 0, lap = 0;
-        uint64_t i = 0;
-        for (; i < total; i++) {
+        uint64_t i = 0, m = 0;
+        bool failed = false;
+        for (;; i++) {
+            const bool more = src.next(s, m);
             if (lap > 0) {
                 const uint32_t eparity = (lap - 1) & 1u;
                 const bool ok = mbar_wait(smem_u32(&empty_bar[b]), eparity, a.timeout_ns);
                 if (!__all_sync(0xffffffffu, ok)) {
                     if (lane == 0) record_timeout(a.status, K_FB_SEG_COPY, b, eparity, m0 + i);
+                    failed = true;
                     break;
                 }
             }
+            if (!more) break;
+            if (src.dyn) cur.init(s, m);
             int32_t c[5];
             cur.start(s, c);
             const uint32_t g0 = cur.q * E;
@@ -358,19 +438,29 @@ __global__ void __launch_bounds__(seg_threads<kSegConsumerWarps>(), 2)
                     bulk_load(dst0 + j * s.seg_stride, sg.src & ~15ull, n, bar);
                 }
             }
-            cur.next(s);
+            src.after_issue(s, lane);
+            if (!src.dyn) cur.next(s);
             if (i == 0 && lane == 0) TM_STAMP(seg, 1);
             if (++b == S) {
                 b = 0;
                 lap++;
             }
         }
+        if (!failed) {  // the end marker in buffer b (released by the consumers, waited for above)
+            if (lane == 0) info[b].run = kEndOfItems;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&full_bar[b]));
+        }
         // the copies issued last land before the CTA leaves (the consumers normally saw them)
         if (lane == 0) {
-            const uint64_t lo = i > S ? i - S : 0;
+            TM_TRACE_PUT(seg, 61, i);
+            // (item i - S shares buffer i % S with the end marker, whose phase followed its own;
+            // the consumers released that buffer before the marker went in, so it has landed)
+            const uint64_t lo = failed ? (i > S ? i - S : 0) : (i >= S ? i - S + 1 : 0);
             for (uint64_t k = lo; k < i; k++)
                 mbar_wait(smem_u32(&full_bar[k % S]), (uint32_t)((k / S) & 1), a.timeout_ns);
         }
+        src.finish(s, lane);
         return;
     }
 
@@ -392,7 +482,7 @@ __global__ void __launch_bounds__(seg_threads<kSegConsumerWarps>(), 2)
     const uint32_t r_start = ct / rc, c_start = ct - r_start * rc;
     const uint32_t r_step = kCT / rc, c_step = kCT - r_step * rc;
     uint32_t sb = 0, sparity = 0;  // staging buffer of item n (n % S) and its phase parity
-    for (uint64_t n = 0; n < total; n++) {
+    for (uint64_t n = 0;; n++) {
         if (n) {
             if (++sb == S) {
                 sb = 0;
@@ -404,6 +494,7 @@ __global__ void __launch_bounds__(seg_threads<kSegConsumerWarps>(), 2)
             if (lane == 0) record_timeout(a.status, K_FB_SEG_COPY, sb, sparity, m0 + n);
             break;
         }
+        if (info[sb].run == kEndOfItems) break;
         const int32_t* const tab = tabs + (size_t)sb * E * G1;
         const uint32_t r0 = info[sb].r0;
         const uint32_t nr = info[sb].nr;
@@ -452,11 +543,9 @@ __global__ void __launch_bounds__(seg_threads<kSegConsumerWarps>(), 2)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty_bar[sb]));  // this warp's reads are done
-        if (warp == 1 && lane == 0) {
-            if (n < 58) TM_STAMP(seg, 2 + n);
-            if (n + 1 == total) TM_STAMP(seg, 63);
-        }
+        if (warp == 1 && lane == 0 && n < 58) TM_STAMP(seg, 2 + n);
     }
+    if (warp == 1 && lane == 0) TM_STAMP(seg, 63);
 }
 
 // Store direction (tiled_roundtrip): the inverse walk.  The producer warp bulk-loads, per item,
@@ -484,15 +573,12 @@ __global__ void __launch_bounds__(seg_threads<kSegConsumerWarps>(), 2)
     // per staging buffer, the tensor address of each image row's element 0 (~0: outside)
     uint64_t* const tabs = reinterpret_cast<uint64_t*>(smem_raw + S * stage_bytes);
 
-    const uint64_t per = s.per, extra = s.extra;  // the item split, from the host
+    const uint64_t per = s.per, extra = s.extra;  // the static item split, from the host
     const uint64_t m0 = blockIdx.x * per + (blockIdx.x < extra ? blockIdx.x : extra);
     const uint64_t total = per + (blockIdx.x < extra ? 1 : 0);
-    if (total == 0) return;
+    if (s.sched == nullptr && total == 0) return;
     const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    if (threadIdx.x == 0) {
-        TM_STAMP(seg, 0);
-        TM_TRACE_PUT(seg, 61, total);
-    }
+    if (threadIdx.x == 0) TM_STAMP(seg, 0);
     const uint32_t inner = a.inner_bytes;
     if (threadIdx.x == 0) {
         for (uint32_t i = 0; i < S; i++) {
@@ -504,20 +590,27 @@ __global__ void __launch_bounds__(seg_threads<kSegConsumerWarps>(), 2)
     __syncthreads();
 
     if (warp == 0) {
-        // ---- producer (the same item cursor as the copy)
+        // ---- producer (the same item source, cursor and end marker as the copy)
+        SegSource src;
+        src.init(s, m0, total);
         ItemCursor cur;
-        cur.init(s, m0);
+        if (!src.dyn) cur.init(s, m0);
         uint32_t b = 0, lap = 0;
-        uint64_t i = 0;
-        for (; i < total; i++) {
+        uint64_t i = 0, m = 0;
+        bool failed = false;
+        for (;; i++) {
+            const bool more = src.next(s, m);
             if (lap > 0) {
                 const uint32_t eparity = (lap - 1) & 1u;
                 const bool ok = mbar_wait(smem_u32(&empty_bar[b]), eparity, a.timeout_ns);
                 if (!__all_sync(0xffffffffu, ok)) {
                     if (lane == 0) record_timeout(a.status, K_FB_SEG_STORE, b, eparity, m0 + i);
+                    failed = true;
                     break;
                 }
             }
+            if (!more) break;
+            if (src.dyn) cur.init(s, m);
             int32_t c[5];
             cur.start(s, c);
             const uint32_t g0 = cur.q * E;
@@ -544,18 +637,28 @@ __global__ void __launch_bounds__(seg_threads<kSegConsumerWarps>(), 2)
                 bulk_load(dst0 + k * s.img_stride, a.images + box * a.box_bytes + (uint64_t)g0 * G1 * inner,
                           nr * inner, bar);
             }
-            cur.next(s);
+            src.after_issue(s, lane);
+            if (!src.dyn) cur.next(s);
             if (i == 0 && lane == 0) TM_STAMP(seg, 1);
             if (++b == S) {
                 b = 0;
                 lap++;
             }
         }
+        if (!failed) {  // the end marker in buffer b
+            if (lane == 0) info[b].run = kEndOfItems;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&full_bar[b]));
+        }
         if (lane == 0) {
-            const uint64_t lo = i > S ? i - S : 0;
+            TM_TRACE_PUT(seg, 61, i);
+            // (item i - S shares buffer i % S with the end marker, whose phase followed its own;
+            // the consumers released that buffer before the marker went in, so it has landed)
+            const uint64_t lo = failed ? (i > S ? i - S : 0) : (i >= S ? i - S + 1 : 0);
             for (uint64_t k = lo; k < i; k++)
                 mbar_wait(smem_u32(&full_bar[k % S]), (uint32_t)((k / S) & 1), a.timeout_ns);
         }
+        src.finish(s, lane);
         return;
     }
 
@@ -572,7 +675,7 @@ __global__ void __launch_bounds__(seg_threads<kSegConsumerWarps>(), 2)
     const uint32_t r_start = ct / rc, c_start = ct - r_start * rc;
     const uint32_t r_step = kCT / rc, c_step = kCT - r_step * rc;
     uint32_t sb = 0, sparity = 0;
-    for (uint64_t n = 0; n < total; n++) {
+    for (uint64_t n = 0;; n++) {
         if (n) {
             if (++sb == S) {
                 sb = 0;
@@ -584,6 +687,7 @@ __global__ void __launch_bounds__(seg_threads<kSegConsumerWarps>(), 2)
             if (lane == 0) record_timeout(a.status, K_FB_SEG_STORE, sb, sparity, m0 + n);
             break;
         }
+        if (info[sb].run == kEndOfItems) break;
         const uint64_t* const tab = tabs + (size_t)sb * E * G1;
         const uint32_t r0 = info[sb].r0;
         const uint32_t nr = info[sb].nr;
@@ -610,11 +714,9 @@ __global__ void __launch_bounds__(seg_threads<kSegConsumerWarps>(), 2)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty_bar[sb]));
-        if (warp == 1 && lane == 0) {
-            if (n < 58) TM_STAMP(seg, 2 + n);
-            if (n + 1 == total) TM_STAMP(seg, 63);
-        }
+        if (warp == 1 && lane == 0 && n < 58) TM_STAMP(seg, 2 + n);
     }
+    if (warp == 1 && lane == 0) TM_STAMP(seg, 63);
 }
 
 namespace {

@@ -310,6 +310,12 @@ struct SegArgs {
     uint64_t per;           // items per CTA: items / grid (CTAs below `extra` take one more),
     uint32_t extra;         // computed on the host with the grid
     uint32_t cwarps;        // consumer warps per CTA: 8, 12 or 16 (TM_FB_SEG_WARPS, default 8)
+    // Dynamic item split (when sched is set; see SegSource in k_fb_seg.cu): a counter of the
+    // launch's stream, zero at launch, reset by the launch's last CTA; batch items per fetch.
+    unsigned long long* sched;
+    uint64_t nitems;        // items of the launch: nrun * nblk
+    uint32_t batch;
+    uint32_t pad;
 };
 constexpr uint32_t kSegMinBytes = 512;  // shorter segments: the per-window copy (request rate)
 constexpr uint32_t kSegMaxGroups = 64;
@@ -366,6 +372,9 @@ inline bool seg_plan_rows(const FbArgs& a, uint64_t g1, uint32_t sms, uint32_t w
     grid = (uint32_t)(items < ctas ? items : ctas);
     s.per = items / grid;
     s.extra = (uint32_t)(items % grid);
+    s.nitems = items;
+    s.sched = nullptr;  // the static split unless the caller hands the launch a counter
+    s.batch = 1;
     const uint64_t w = env_u64("TM_FB_SEG_WARPS", 8);
     s.cwarps = w >= 16 ? 16u : w >= 12 ? 12u : 8u;
     smem = store ? (size_t)S * ((size_t)nb0 * s.img_stride + 8ull * s.block_groups * g1) + 16

@@ -346,6 +346,7 @@ int copy_boxes(const tm_desc* src, const int32_t* coords, size_t nbox, void* ima
         SegArgs sa;
         if (fb_copy_plan(a, src, n, (uint32_t)ds->sms,
                          [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); }, sa, grid, smem)) {
+            sa.sched = sched_slot(*ds, st);
             rc = check_launch(launch_fb_seg_copy(sa, grid, smem, st), "fallback segment copy launch");
         } else {
             rc = check_launch(launch_fb_copy(a, grid, smem, st), "fallback copy launch");
@@ -600,6 +601,7 @@ int tiled_roundtrip(const tm_desc* dst, const int32_t* coords, size_t nbox, cons
                      (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_STAGES", 2), kSegMaxStages),
                      (int)env_u64("TM_FB_SEG", 2), true,
                      [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); }, sa, grid, smem)) {
+            sa.sched = sched_slot(*ds, st);
             rc = check_launch(launch_fb_seg_store(sa, grid, smem, st), "fallback segment store launch");
         } else {
             fb_shape(a, n, (uint32_t)ds->sms,

@@ -119,3 +119,38 @@ def test_static_and_dynamic_split_agree(tm, monkeypatch, dynamic):
     assert torch.equal(back, xd)
     np.testing.assert_array_equal(to_host(dd).view(np.uint32),
                                   oracle_sum(d, s, rr, 1).reshape(-1).view(np.uint32))
+
+
+def test_vector_path_segments_on_three_streams_and_in_a_row(tm):
+    """The vector path's segment kernels (the W4 rank-5 view, a 200-byte stride) take their items
+    the same way: copies and round trips on three streams at once, twice each, then four copies in
+    a row on one stream; every image and every restored tensor against the oracle."""
+    kw = dict(batch=16, rows=70, cols=1000, pitch=1024)
+    x = workloads.w4_tensor(**kw, seed=73)
+    r = workloads.w4_rank5_map(**kw, span=128)
+    xd = to_dev(x)
+    m = dev_map(tm, xd, r)
+    assert m.path == tm.TM_PATH_FALLBACK
+    want = oracle.tiled_copy(host_map(x, r), threads=oracle.host_cores())
+    sent = np.full(x.size, workloads.SENTINEL_U16, np.uint16)
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    imgs = [torch.empty(m.num_boxes * m.box_bytes, dtype=torch.uint8, device="cuda") for _ in streams]
+    backs = [torch.from_numpy(sent.view(np.uint8).copy()).cuda() for _ in streams]
+    bmaps = [dev_map(tm, bk, r) for bk in backs]
+    torch.cuda.synchronize()
+    for _ in range(2):
+        for st, im, bm in zip(streams, imgs, bmaps):
+            tm.tiled_copy(m, None, im, st)
+            tm.tiled_roundtrip(bm, None, im, st)
+    torch.cuda.synchronize()
+    assert tm.tm_stream_check() == tm.TM_OK, tm.tm_last_error()
+    for im, bk in zip(imgs, backs):
+        assert np.array_equal(to_host(im), want)
+        assert torch.equal(bk, xd)
+    outs = [torch.empty_like(imgs[0]) for _ in range(4)]
+    for o in outs:
+        tm.tiled_copy(m, None, o)
+    torch.cuda.synchronize()
+    assert tm.tm_stream_check() == tm.TM_OK, tm.tm_last_error()
+    for o in outs:
+        assert np.array_equal(to_host(o), want)
