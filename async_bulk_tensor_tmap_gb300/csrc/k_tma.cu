@@ -107,10 +107,13 @@ __global__ void __launch_bounds__(32, 1)
     // The loads' source of items.  Static: this CTA's items of the host's schedule (stream_item),
     // their counters stepped by G * gridDim.x boxes with carries (the tail item's found once).
     // Dynamic: items g = 0 .. nitems - 1 of G boxes each (the last one short); CTA c first takes
-    // c, c + gridDim.x, ... for its first S stages, then batches of B consecutive items from the
-    // launch's counter (item S * gridDim.x + B * atomicAdd).  Each batch is fetched one batch
-    // ahead, right after a stage's loads are issued: the producer's next arrive (a release) then
-    // finds the atomic long done.  A CTA that runs faster than others takes more items.
+    // c, c + gridDim.x, ... for its first S + 1 items (its first stages and their first refill),
+    // then batches of B consecutive items from the launch's counter (item (S + 1) * gridDim.x +
+    // B * atomicAdd).  The first batch is fetched right after that first refill is issued, not
+    // before the first loads (304 CTAs fetching at once made every first stage 1.5 us late), and
+    // each further batch one batch ahead, right after a stage's loads are issued: the producer's
+    // next arrive (a release) then finds the atomic long done.  A CTA that runs faster than
+    // others takes more items.
     uint64_t si = 0;                        // static: the next item index of this CTA
     uint32_t sk[5] = {0, 0, 0, 0, 0};       // static: counters of item si - 1
     uint32_t tail_k[5] = {0, 0, 0, 0, 0};   // static: counters of the tail item's first box
@@ -118,7 +121,9 @@ __global__ void __launch_bounds__(32, 1)
     unsigned long long pend = 0;            // dynamic: the batch fetched ahead
     uint64_t bg = 0, bend = 0;              // dynamic: items bg .. bend - 1 of the current batch
     bool refetch = false;                   // dynamic: the batch ahead was taken: fetch another
-    const uint64_t prefix = (uint64_t)S * grid_ctas;
+    const uint64_t npre = (uint64_t)S + 1;  // static items per CTA before the counter
+    const uint64_t prefix = npre * grid_ctas;
+    bool first_fetch = dyn && prefix < a.nitems;
     const uint32_t B = a.batch ? a.batch : 1u;
     if (!dyn && grid && a.waves > 0 && a.waves < n_local) {
         uint64_t tb;
@@ -129,7 +134,7 @@ __global__ void __launch_bounds__(32, 1)
     auto next_item = [&](Item& it) -> bool {
         if (dyn) {
             uint64_t g;
-            if (dj < S) {
+            if (dj < npre) {
                 // the static prefix (if it ends early, so do the items: nitems < prefix)
                 g = cta + dj * grid_ctas;
                 dj++;
@@ -256,8 +261,6 @@ __global__ void __launch_bounds__(32, 1)
         issued++;
         ls = ls + 1 == S ? 0 : ls + 1;
     }
-    // dynamic: the first batch beyond the prefix, fetched while the first stages load
-    if (dyn && have && prefix < a.nitems) pend = atomicAdd(a.sched, 1ull);
     TM_STAMP(stream, 1);
     const uint64_t lag = S > 1 ? 1 : 0;
 
@@ -285,7 +288,10 @@ __global__ void __launch_bounds__(32, 1)
             rec[ls] = nx;
             issued++;
             ls = ls + 1 == S ? 0 : ls + 1;
-            if (refetch) {  // after the issue: the next batch, fetched while this item loads
+            if (first_fetch && dj == npre) {  // after the prefix's last issue: the first batch
+                pend = atomicAdd(a.sched, 1ull);
+                first_fetch = false;
+            } else if (refetch) {  // after the issue: the next batch, fetched while this item loads
                 pend = atomicAdd(a.sched, 1ull);
                 refetch = false;
             }

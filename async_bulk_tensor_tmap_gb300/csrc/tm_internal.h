@@ -342,13 +342,7 @@ inline bool seg_plan_rows(const FbArgs& a, uint64_t g1, uint32_t sms, uint32_t w
     const uint64_t S = std::min<uint32_t>(std::max<uint32_t>(stages, 2), kSegMaxStages);
     const uint64_t per_group =
         store ? S * (nb0 * g1 * a.inner_bytes + 8 * g1) : S * (seg_stride + 4 * g1);
-    // store: each box's image block is staged 16 bytes past a multiple of its image size, so that
-    // the blocks of a run start at different bank phases (chunk j of one box and chunk j of the
-    // next, read by neighbouring threads, would otherwise share a bank sector: 29 % of the shared
-    // load wavefronts conflicted on the W4 rank-5 view).  Measured on GB300: no change in time
-    // either way, within run-to-run noise (TM_FB_SEG_PAD=0 drops the pad).
-    const uint64_t pad = store && nb0 > 1 && env_u64("TM_FB_SEG_PAD", 1) ? 16 : 0;
-    const uint64_t fixed = 64 + S * nb0 * pad;
+    const uint64_t fixed = 64;
     uint32_t per_sm = want < 1 ? 1 : want;
     while (per_sm > 1 && budget(per_sm) < fixed + per_group) per_sm--;
     if (budget(per_sm) < fixed + per_group) return false;
@@ -365,7 +359,7 @@ inline bool seg_plan_rows(const FbArgs& a, uint64_t g1, uint32_t sms, uint32_t w
     s.seg_stride = store ? 0u : (uint32_t)seg_stride;
     s.nblk = (uint32_t)((groups + e - 1) / e);
     s.block_groups = (s.groups + s.nblk - 1) / s.nblk;
-    s.img_stride = store ? (uint32_t)((uint64_t)s.block_groups * g1 * a.inner_bytes + pad) : 0u;
+    s.img_stride = store ? (uint32_t)((uint64_t)s.block_groups * g1 * a.inner_bytes) : 0u;
     s.nrun = a.walk.nbox / nb0;
     const uint64_t items = s.nrun * s.nblk;
     const uint64_t ctas = (uint64_t)sms * per_sm;
