@@ -158,7 +158,8 @@ extern "C" int tiled_copy_noalloc(const tm_desc* src, const int32_t* coords, siz
         a.images = (uint64_t)images;
         uint32_t grid = 0;
         size_t smem = 0;
-        // the launch shape of tiled_copy (same rule, same tunables)
+        // the launch shape of tiled_copy (same rule, same tunables); stream_plan leaves the work
+        // split static (no counter: the dynamic split's counters are allocated memory)
         stream_plan(a, src->box_bytes, span, (uint32_t)d->sms,
                     [&](uint32_t per_sm) { return budget(*d, per_sm); }, grid, smem);
         a.timeout_ns = limit_ns();

@@ -279,7 +279,8 @@ int stream_gemm(const tm_desc* a, const tm_desc* b, float* c, uint64_t ldc, uint
  *   allocator owns all device memory, processes under a hard device-memory cap where a late
  *   allocation may fail, latency-critical loops that cannot afford an allocator call.
  *   Same arguments, the same image bytes and the same launch shape as tiled_copy (one rule and
- *   the same tunables for both).  All scratch (a status word and the
+ *   the same tunables for both), with the fixed split of boxes between CTAs: the dynamic split
+ *   of tiled_copy takes its items from work counters the library allocates.  All scratch (a status word and the
  *   box list, at most TM_NOALLOC_MAX_BOXES boxes; a longer list gives TM_ERANGE) lives in one
  *   fixed __device__ array of 327,936 bytes inside the library, held by every GPU that loads the
  *   library until the process exits.  The first call on a device looks up that array's device
