@@ -28,3 +28,29 @@ def test_reference_arm_prints_one_contract_line():
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1
     assert "workload" in d["config"]
+
+
+def test_recorded_traffic_follows_the_kernel_code(tmp_path, monkeypatch):
+    """bench.py reports a recorded DRAM traffic only while the streaming kernel's code is the one
+    it was captured on: a comment or blank-line edit keeps it, a code edit voids it."""
+    import hashlib
+    import shutil
+    sys.path.insert(0, ROOT)
+    import bench
+    csrc = os.path.join("async_bulk_tensor_tmap_gb300", "csrc")
+    os.makedirs(tmp_path / csrc)
+    os.makedirs(tmp_path / "profiles")
+    for f in ("k_tma.cu", "tm_ptx.cuh", "tm_internal.h"):
+        shutil.copy(os.path.join(ROOT, csrc, f), tmp_path / csrc / f)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    digest = hashlib.sha256(bench.tma_kernel_source()).hexdigest()
+    (tmp_path / "profiles" / "roofline_traffic.txt").write_text(
+        f"# a record\nkernel: w5a.reduce\nsource_sha256: {digest}\ntraffic_bytes: 123\n")
+    assert bench.recorded_traffic("w5a.reduce") == 123
+    assert bench.recorded_traffic("w3.copy") is None
+    k = tmp_path / csrc / "k_tma.cu"
+    src = k.read_text()
+    k.write_text("// a note\n\n" + src.replace("\n", "  // x\n", 3))
+    assert bench.recorded_traffic("w5a.reduce") == 123
+    k.write_text(src.replace("{", "{ ;", 1))
+    assert bench.recorded_traffic("w5a.reduce") is None
