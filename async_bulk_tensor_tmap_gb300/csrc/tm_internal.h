@@ -100,9 +100,15 @@ struct StreamArgs {
 };
 
 // CTAs per SM of the streaming kernels (see stream_plan).  One, with as many 32 KiB stages as fit
-// (six): measured on GB300 with the dynamic work split, 2-3.5 % faster than two CTAs of three
+// (seven): measured on GB300 with the dynamic work split, 2-3.5 % faster than two CTAs of three
 // stages on the 128 MiB copies and round trips and 1 % on the 3.2 GB reduce-add.
 constexpr uint64_t kStreamCtasPerSm = 1;
+
+// Stages of the streaming reductions (tensor loads of src, bulk reduce-adds into dst).  They read
+// two tensors and write one, and keep more DRAM traffic in flight per stage than a copy: measured
+// on GB300, four stages run the 3.2 GB fp32 reduce-add 0.8 % faster than seven (6895-6906 against
+// 6845-6849 GB/s, three interleaved runs each; bf16 add likewise), while the copies lose 1.5 % at four.
+constexpr uint64_t kStreamReduceStages = 4;
 
 // Default L2 policies of the streaming copies' loads and writes (see stream_plan).
 constexpr uint32_t kDefaultHintLoad = 0, kDefaultHintWrite = 0;
@@ -192,12 +198,13 @@ inline void tma_group(uint64_t box_bytes, uint32_t span, uint64_t target, uint32
 // Launch plan of a TMA streaming kernel over the boxes of a.walk, shared by every entry point that
 // launches one: boxes per stage (tma_group, stages of about TM_GROUP_BYTES = 32 KiB), CTAs per SM
 // (TM_CTAS_PER_SM, default kStreamCtasPerSm; fewer when two stages would not fit), as many stages as fit
-// (at most TM_STAGES when set), the L2 policies of the loads and the writes (TM_L2_HINT_LOAD /
-// TM_L2_HINT_WRITE: 0 none, 1 evict-first, 2 evict-last), the grid, the schedule and the dynamic
-// shared memory.  budget(n) is the shared memory one of n CTAs on an SM may use.
+// (at most TM_STAGES when set; a reduction at most TM_STAGES_REDUCE, default kStreamReduceStages),
+// the L2 policies of the loads and the writes (TM_L2_HINT_LOAD / TM_L2_HINT_WRITE: 0 none,
+// 1 evict-first, 2 evict-last), the grid, the schedule and the dynamic shared memory.  budget(n)
+// is the shared memory one of n CTAs on an SM may use.
 template <class Budget>
 inline void stream_plan(StreamArgs& a, uint64_t box_bytes, uint32_t span, uint32_t sms,
-                        Budget budget, uint32_t& grid, size_t& smem)
+                        Budget budget, uint32_t& grid, size_t& smem, bool reduce = false)
 {
     a.box_bytes = (uint32_t)box_bytes;
     tma_group(box_bytes, span, std::max<uint64_t>(env_u64("TM_GROUP_BYTES", 32768), 1024), a.group,
@@ -208,7 +215,7 @@ inline void stream_plan(StreamArgs& a, uint64_t box_bytes, uint32_t span, uint32
     size_t b = budget(per_sm);
     while (per_sm > 1 && b < 2ull * a.stage_bytes) b = budget(--per_sm);
     uint32_t stages = (uint32_t)std::min<size_t>(b / a.stage_bytes, TM_MAX_STAGES);
-    const uint64_t cap = env_u64("TM_STAGES", 0);
+    const uint64_t cap = reduce ? env_u64("TM_STAGES_REDUCE", kStreamReduceStages) : env_u64("TM_STAGES", 0);
     if (cap > 0) stages = (uint32_t)std::min<uint64_t>(stages, cap);
     a.stages = std::max<uint32_t>(stages, 1);
     const uint32_t hl = (uint32_t)std::min<uint64_t>(env_u64("TM_L2_HINT_LOAD", kDefaultHintLoad), 2);
