@@ -41,8 +41,8 @@ namespace tmk {
 // of them runs at a time).
 TM_TRACE_BUFFER(seg)
 
-// Consumer warps per CTA: W (SegArgs::cwarps picks 8, 12 or 16; 8 unless TM_FB_SEG_WARPS says
-// otherwise), plus one producer warp.
+// Consumer warps per CTA: W (SegArgs::cwarps picks 8, 12 or 16; kSegWarps unless TM_FB_SEG_WARPS
+// says otherwise), plus one producer warp.
 template <uint32_t W>
 constexpr uint32_t seg_threads() { return 32 * (1 + W); }
 

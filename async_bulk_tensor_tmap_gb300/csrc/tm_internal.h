@@ -321,7 +321,7 @@ struct SegArgs {
     uint32_t stages;        // staging buffers (items in flight per CTA)
     uint64_t per;           // items per CTA: items / grid (CTAs below `extra` take one more),
     uint32_t extra;         // computed on the host with the grid
-    uint32_t cwarps;        // consumer warps per CTA: 8, 12 or 16 (TM_FB_SEG_WARPS, default 8)
+    uint32_t cwarps;        // consumer warps per CTA: 8, 12 or 16 (TM_FB_SEG_WARPS, default kSegWarps)
     // Dynamic item split (when sched is set; see SegSource in k_fb_seg.cu): a counter of the
     // launch's stream, zero at launch, reset by the launch's last CTA; batch items per fetch.
     unsigned long long* sched;
@@ -340,6 +340,16 @@ constexpr uint32_t kSegMaxStages = 8;
 // Copy: a stage holds an item's segments (seg_stride bytes each) and a 4-byte shared-memory
 // offset per image row.  Store (store = true): a stage holds the item's image block of each box of
 // the run (img_stride bytes each) and an 8-byte tensor address per image row.
+// Launch shape of the segment kernels: CTAs per SM, staging buffers of the copy and of the store,
+// consumer warps.  Measured on GB300 on the W4 rank-5 view with the dynamic item split (two runs
+// of each shape): three buffers took the copy from 5349-5362 to 5577-5618 GB/s (four: 4447-4661),
+// and twelve consumer warps took the store from 5235-5240 to 5379-5405 (its three buffers:
+// 5258-5348); one CTA per SM lost 7-25 % in both directions.
+constexpr uint64_t kSegCtasPerSm = 2;
+constexpr uint64_t kSegCopyStages = 3;
+constexpr uint64_t kSegStoreStages = 2;
+constexpr uint64_t kSegWarps = 12;
+
 template <class Budget>
 inline bool seg_plan_rows(const FbArgs& a, uint64_t g1, uint32_t sms, uint32_t want,
                           uint32_t stages, int force, bool store, Budget budget, SegArgs& s,
@@ -381,7 +391,7 @@ inline bool seg_plan_rows(const FbArgs& a, uint64_t g1, uint32_t sms, uint32_t w
     s.nitems = items;
     s.sched = nullptr;  // the static split unless the caller hands the launch a counter
     s.batch = 1;
-    const uint64_t w = env_u64("TM_FB_SEG_WARPS", 8);
+    const uint64_t w = env_u64("TM_FB_SEG_WARPS", kSegWarps);
     s.cwarps = w >= 16 ? 16u : w >= 12 ? 12u : 8u;
     smem = store ? (size_t)S * ((size_t)nb0 * s.img_stride + 8ull * s.block_groups * g1) + 16
                  : (size_t)S * s.block_groups * (s.seg_stride + 4 * g1) + 16;
@@ -412,16 +422,16 @@ inline bool seg_plan(const FbArgs& a, const tm_desc* d, uint32_t sms, uint32_t w
 // Launch shape of the vector path's copy (load direction), shared by every entry point that
 // launches one: the segment form when the map takes it (TM_FB_SEG: 0 never, 1 whenever the layout
 // allows, unset when its segments are long enough for bulk copies; TM_FB_SEG_CTAS_PER_SM and
-// TM_FB_SEG_STAGES, defaults 2 and 2: the largest items, measured best on GB300 on the W4 rank-5
-// view), else the per-window form (TM_FB_COPY_CTAS_PER_SM, default 8).  Returns true for the
+// TM_FB_SEG_STAGES, defaults kSegCtasPerSm and kSegCopyStages), else the per-window form
+// (TM_FB_COPY_CTAS_PER_SM, default 8).  Returns true for the
 // segment form (s filled), false for the per-window form (a.block_rows set).  budget(n) as for
 // fb_shape.
 template <class Budget>
 inline bool fb_copy_plan(FbArgs& a, const tm_desc* d, uint64_t nbox, uint32_t sms, Budget budget,
                          SegArgs& s, uint32_t& grid, size_t& smem)
 {
-    if (seg_plan(a, d, sms, (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_CTAS_PER_SM", 2), 8),
-                 (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_STAGES", 2), kSegMaxStages),
+    if (seg_plan(a, d, sms, (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_CTAS_PER_SM", kSegCtasPerSm), 8),
+                 (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_STAGES", kSegCopyStages), kSegMaxStages),
                  (int)env_u64("TM_FB_SEG", 2), false, budget, s, grid, smem))
         return true;
     fb_shape(a, nbox, sms, (uint32_t)std::min<uint64_t>(env_u64("TM_FB_COPY_CTAS_PER_SM", 8), 16),

@@ -597,8 +597,8 @@ int tiled_roundtrip(const tm_desc* dst, const int32_t* coords, size_t nbox, cons
         // The segment form of the store (TM_FB_SEG as for the copy): image blocks staged by bulk
         // copies, rows written by the consumer warps.
         if (seg_plan(a, dst, (uint32_t)ds->sms,
-                     (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_CTAS_PER_SM", 2), 8),
-                     (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_STAGES", 2), kSegMaxStages),
+                     (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_CTAS_PER_SM", kSegCtasPerSm), 8),
+                     (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_STAGES", kSegStoreStages), kSegMaxStages),
                      (int)env_u64("TM_FB_SEG", 2), true,
                      [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); }, sa, grid, smem)) {
             sa.sched = sched_slot(*ds, st);

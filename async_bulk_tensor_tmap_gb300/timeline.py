@@ -10,8 +10,10 @@ events on the launching stream.  For each workload it prints the event time and,
 of the median launch, where that time goes:
 
   outside   event time minus the kernel's span (first CTA entry to last CTA exit): launch and
-            event overhead, which the kernel cannot touch; the same flush and events around one
-            trivial torch kernel give the floor of this figure on the machine
+            event overhead, which the kernel cannot touch; the same flush and events with nothing
+            between them, or around one trivial torch kernel, give the floor of this figure on the
+            machine, and a one-box copy with a trivial kernel between the flush and the first
+            event shows what of it the flush leaves behind
   issue     entry to the first S stages issued (median CTA)
   first     entry to the first stage complete (median CTA): the ramp
   steady    the stream's rate between the times 25 % and 75 % of all stages completed
@@ -100,7 +102,7 @@ def main():
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).reshape(-1).view(np.uint8)).cuda()
 
-    def timed(fn, kname, nbytes, item_slots, reps):
+    def timed(fn, kname, nbytes, item_slots, reps, pre=None):
         for _ in range(3):
             flush.fill_(1)
             fn()
@@ -108,6 +110,8 @@ def main():
         runs = []
         for _ in range(reps):
             flush.fill_(1)
+            if pre is not None:
+                pre()
             if kname:
                 assert getattr(tm._L, f"tm_trace_clear_{kname}")() == 0
             e0 = torch.cuda.Event(enable_timing=True)
@@ -130,6 +134,7 @@ def main():
     ring_items = list(range(2, 58))
     res = {}
     tiny = torch.zeros(1, device="cuda")
+    res["events alone (floor)"] = timed(lambda: None, None, 0, None, args.reps)
     res["torch trivial kernel (floor)"] = timed(lambda: tiny.add_(1), None, 0, None, args.reps)
 
     x = workloads.w3_tensor()
@@ -143,6 +148,9 @@ def main():
     nb3 = 2 * xd.numel()
     res["w3.copy one box"] = timed(lambda: tm.tiled_copy(m3, [[0, 0]], img3), "stream",
                                    2 * m3.box_bytes, stream_items, args.reps)
+    res["w3.copy one box, a kernel after the flush"] = timed(
+        lambda: tm.tiled_copy(m3, [[0, 0]], img3), "stream", 2 * m3.box_bytes, stream_items,
+        args.reps, pre=lambda: tiny.add_(1))
     res["w3.copy"] = timed(lambda: tm.tiled_copy(m3, None, img3), "stream", nb3, stream_items, args.reps)
     res["w3.roundtrip"] = timed(lambda: tm.tiled_roundtrip(m3o, None, img3), "stream", nb3,
                                 stream_items, args.reps)
