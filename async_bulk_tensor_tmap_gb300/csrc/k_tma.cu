@@ -21,8 +21,9 @@
 // for writes: each holds the stage, its phase parity and, for a grid walk, the box counters of
 // the item's first box, stepped by G * gridDim.x boxes with carries (the tail item's counters are
 // found once, before the first load); the boxes inside an item are stepped with an odometer.  No
-// 64-bit division is left on the issue path.  The loads and the writes may carry an L2 eviction
-// policy (StreamArgs::hints).
+// 64-bit division is left on the issue path.  The copy instructions carry no L2 policy: evict-first
+// or evict-last policies on the loads or the writes measured no gain on GB300, and choosing between
+// the policy and plain forms box by box cost the 512-byte-box copy a quarter of its issue rate.
 //
 // The three kinds differ only in the two copy instructions:
 //   copy       load = tensor load of the box;  write = 1-D bulk store of the image (tile-major)
@@ -89,9 +90,6 @@ __global__ void __launch_bounds__(32, 1)
     if constexpr (KIND != KIND_COPY) prefetch_tmap(&out_map);
     for (uint32_t s = 0; s < S; s++) mbar_init(smem_u32(&full_bar[s]), 1);
     fence_barrier_init();
-
-    const uint32_t hint_ld = a.hints & 3u, hint_wr = (a.hints >> 2) & 3u;
-    const uint64_t pol_ld = l2_policy(hint_ld), pol_wr = l2_policy(hint_wr);
 
     const bool grid = a.walk.mode == WALK_GRID;
 
@@ -205,19 +203,13 @@ __global__ void __launch_bounds__(32, 1)
         if constexpr (KIND == KIND_ROUNDTRIP) {
             const uint64_t src = a.images + it.b0 * a.box_bytes;
             if (dense) {
-                if (hint_ld) bulk_load<true>(dst, src, it.cnt * a.box_bytes, bar, pol_ld);
-                else bulk_load(dst, src, it.cnt * a.box_bytes, bar);
+                bulk_load(dst, src, it.cnt * a.box_bytes, bar);
             } else {
-                for (uint32_t j = 0; j < it.cnt; j++) {
-                    if (hint_ld) bulk_load<true>(dst + j * slot, src + j * a.box_bytes, a.box_bytes, bar, pol_ld);
-                    else bulk_load(dst + j * slot, src + j * a.box_bytes, a.box_bytes, bar);
-                }
+                for (uint32_t j = 0; j < it.cnt; j++)
+                    bulk_load(dst + j * slot, src + j * a.box_bytes, a.box_bytes, bar);
             }
         } else {
-            for_boxes(it, [&](uint32_t j, const int32_t* co) {
-                if (hint_ld) tma_load<R, true>(dst + j * slot, &in_map, co, bar, pol_ld);
-                else tma_load<R>(dst + j * slot, &in_map, co, bar);
-            });
+            for_boxes(it, [&](uint32_t j, const int32_t* co) { tma_load<R>(dst + j * slot, &in_map, co, bar); });
         }
     };
 
@@ -226,22 +218,17 @@ __global__ void __launch_bounds__(32, 1)
         if constexpr (KIND == KIND_COPY) {
             const uint64_t dst = a.images + it.b0 * a.box_bytes;
             if (dense) {
-                if (hint_wr) bulk_store<true>(dst, src, it.cnt * a.box_bytes, pol_wr);
-                else bulk_store(dst, src, it.cnt * a.box_bytes);
+                bulk_store(dst, src, it.cnt * a.box_bytes);
             } else {
-                for (uint32_t j = 0; j < it.cnt; j++) {
-                    if (hint_wr) bulk_store<true>(dst + j * a.box_bytes, src + j * slot, a.box_bytes, pol_wr);
-                    else bulk_store(dst + j * a.box_bytes, src + j * slot, a.box_bytes);
-                }
+                for (uint32_t j = 0; j < it.cnt; j++)
+                    bulk_store(dst + j * a.box_bytes, src + j * slot, a.box_bytes);
             }
         } else {
             for_boxes(it, [&](uint32_t j, const int32_t* co) {
                 if constexpr (KIND == KIND_ROUNDTRIP) {
-                    if (hint_wr) tma_store<R, true>(&out_map, co, src + j * slot, pol_wr);
-                    else tma_store<R>(&out_map, co, src + j * slot);
+                    tma_store<R>(&out_map, co, src + j * slot);
                 } else {
-                    if (hint_wr) tma_reduce<R, KIND - KIND_REDUCE, true>(&out_map, co, src + j * slot, pol_wr);
-                    else tma_reduce<R, KIND - KIND_REDUCE>(&out_map, co, src + j * slot);
+                    tma_reduce<R, KIND - KIND_REDUCE>(&out_map, co, src + j * slot);
                 }
             });
         }

@@ -77,8 +77,7 @@ struct StreamArgs {
     uint32_t stages;
     uint32_t group;        // G: consecutive boxes per stage
     uint32_t slot_bytes;   // stage bytes per box: box_bytes rounded up to its swizzle period
-    uint32_t hints;        // L2 policies: bits 0-1 the loads', bits 2-3 the writes' (0 none,
-                           // 1 evict-first, 2 evict-last)
+    uint32_t pad0;
     uint64_t timeout_ns;
     StatusBlock* status;
     // The launch-wide schedule, computed once on the host (stream_schedule) so that no CTA runs
@@ -110,8 +109,21 @@ constexpr uint64_t kStreamCtasPerSm = 1;
 // 6845-6849 GB/s, three interleaved runs each; bf16 add likewise), while the copies lose 1.5 % at four.
 constexpr uint64_t kStreamReduceStages = 4;
 
-// Default L2 policies of the streaming copies' loads and writes (see stream_plan).
-constexpr uint32_t kDefaultHintLoad = 0, kDefaultHintWrite = 0;
+// Launch shape for boxes far smaller than a stage (image slots of at most kSmallSlotBytes, 16 or
+// more to a stage).  Their elected lane issues one copy instruction per box in each direction, and
+// its issue rate, not the DRAM, bounds them: more CTAs per SM (more issuing lanes), smaller stages,
+// and the static split, whose items need no index decomposition.  Measured on GB300 on W3 through
+// 64 x 4 boxes (512-byte images, 1 KiB slots): 5497-5544 GB/s with 4 CTAs of 16 KiB stages and the
+// static split, 5206 with the dynamic split, 4726-4794 with 2 CTAs of 32 KiB, 5133-5196 with 6-12
+// CTAs, 2188 with the one CTA of 32 KiB stages that larger boxes take.
+constexpr uint64_t kSmallSlotBytes = 1024;
+constexpr uint64_t kSmallGroupBytes = 16384;
+constexpr uint64_t kSmallCtasPerSm = 4;
+
+inline bool stream_small(const StreamArgs& a)
+{
+    return a.group > 1 && a.slot_bytes <= kSmallSlotBytes;
+}
 
 // Fills the schedule fields of a streaming launch over `grid` CTAs (walk and group already set).
 inline void stream_schedule(StreamArgs& a, uint32_t grid)
@@ -185,42 +197,47 @@ struct FbArgs {
 // span; 128 bytes, the tensor copy's alignment, without), so that every image keeps the phase it
 // has in its own image.  (One box per 1 KiB stage was measured on GB300 at 1 TB/s for 512-byte
 // boxes, against 5.5 TB/s for packed 2 KiB boxes.)
+inline uint64_t slot_of(uint64_t box_bytes, uint32_t span)
+{
+    const uint64_t period = span == 128 ? 1024 : span == 64 ? 512 : span == 32 ? 256 : 128;
+    return (box_bytes + period - 1) / period * period;
+}
+
 inline void tma_group(uint64_t box_bytes, uint32_t span, uint64_t target, uint32_t& group,
                       uint32_t& slot)
 {
-    const uint64_t period = span == 128 ? 1024 : span == 64 ? 512 : span == 32 ? 256 : 128;
-    const uint64_t sl = (box_bytes + period - 1) / period * period;
+    const uint64_t sl = slot_of(box_bytes, span);
     const uint64_t g = target / sl;
     group = (uint32_t)(g < 1 ? 1 : g > 64 ? 64 : g);
     slot = group > 1 ? (uint32_t)sl : (uint32_t)box_bytes;
 }
 
 // Launch plan of a TMA streaming kernel over the boxes of a.walk, shared by every entry point that
-// launches one: boxes per stage (tma_group, stages of about TM_GROUP_BYTES = 32 KiB), CTAs per SM
-// (TM_CTAS_PER_SM, default kStreamCtasPerSm; fewer when two stages would not fit), as many stages as fit
+// launches one: boxes per stage (tma_group, stages of about TM_GROUP_BYTES = 32 KiB, 16 KiB for
+// small slots), CTAs per SM (TM_CTAS_PER_SM, default kStreamCtasPerSm, kSmallCtasPerSm for small
+// slots; fewer when two stages would not fit), as many stages as fit
 // (at most TM_STAGES when set; a reduction at most TM_STAGES_REDUCE, default kStreamReduceStages),
-// the L2 policies of the loads and the writes (TM_L2_HINT_LOAD / TM_L2_HINT_WRITE: 0 none,
-// 1 evict-first, 2 evict-last), the grid, the schedule and the dynamic shared memory.  budget(n)
-// is the shared memory one of n CTAs on an SM may use.
+// the grid, the schedule and the dynamic shared memory.  budget(n) is the shared memory one of n
+// CTAs on an SM may use.
 template <class Budget>
 inline void stream_plan(StreamArgs& a, uint64_t box_bytes, uint32_t span, uint32_t sms,
                         Budget budget, uint32_t& grid, size_t& smem, bool reduce = false)
 {
     a.box_bytes = (uint32_t)box_bytes;
-    tma_group(box_bytes, span, std::max<uint64_t>(env_u64("TM_GROUP_BYTES", 32768), 1024), a.group,
-              a.slot_bytes);
+    const bool small = slot_of(box_bytes, span) <= kSmallSlotBytes;
+    tma_group(box_bytes, span,
+              std::max<uint64_t>(env_u64("TM_GROUP_BYTES", small ? kSmallGroupBytes : 32768), 1024),
+              a.group, a.slot_bytes);
     const uint64_t stage = (uint64_t)a.group * a.slot_bytes;
     a.stage_bytes = (uint32_t)((stage + kStageAlign - 1) / kStageAlign * kStageAlign);
-    uint32_t per_sm = (uint32_t)std::min<uint64_t>(std::max<uint64_t>(env_u64("TM_CTAS_PER_SM", kStreamCtasPerSm), 1), 16);
+    uint32_t per_sm = (uint32_t)std::min<uint64_t>(
+        std::max<uint64_t>(env_u64("TM_CTAS_PER_SM", small ? kSmallCtasPerSm : kStreamCtasPerSm), 1), 16);
     size_t b = budget(per_sm);
     while (per_sm > 1 && b < 2ull * a.stage_bytes) b = budget(--per_sm);
     uint32_t stages = (uint32_t)std::min<size_t>(b / a.stage_bytes, TM_MAX_STAGES);
     const uint64_t cap = reduce ? env_u64("TM_STAGES_REDUCE", kStreamReduceStages) : env_u64("TM_STAGES", 0);
     if (cap > 0) stages = (uint32_t)std::min<uint64_t>(stages, cap);
     a.stages = std::max<uint32_t>(stages, 1);
-    const uint32_t hl = (uint32_t)std::min<uint64_t>(env_u64("TM_L2_HINT_LOAD", kDefaultHintLoad), 2);
-    const uint32_t hw = (uint32_t)std::min<uint64_t>(env_u64("TM_L2_HINT_WRITE", kDefaultHintWrite), 2);
-    a.hints = hl | (hw << 2);
     const uint64_t units = (a.walk.nbox + a.group - 1) / a.group;
     grid = (uint32_t)std::min<uint64_t>(units, (uint64_t)sms * per_sm);
     stream_schedule(a, grid);

@@ -153,10 +153,12 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* m)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
 }
 
-// L2 cache policies for the streaming copies (createpolicy; the 64-bit policy rides on the copy's
-// .L2::cache_hint operand).  kL2Keep: no hint; kL2EvictFirst: the lines are the first candidates for
-// eviction (bytes touched once: a stream then recycles its own lines instead of evicting other
-// data); kL2EvictLast: the last.
+// L2 cache policies (createpolicy; the 64-bit policy rides on the copy's .L2::cache_hint operand).
+// kL2Keep: no hint; kL2EvictFirst: the lines are the first candidates for eviction (bytes touched
+// once: a stream then recycles its own lines instead of evicting other data); kL2EvictLast: the
+// last.  The ring's tile loads use evict-first.  The store, reduce and bulk forms below take a
+// policy as well, but no kernel passes one: on the streaming copies evict-first and evict-last
+// measured no gain on GB300.
 enum L2Hint : uint32_t { kL2Keep = 0, kL2EvictFirst = 1, kL2EvictLast = 2 };
 
 __device__ __forceinline__ uint64_t l2_policy(uint32_t hint)

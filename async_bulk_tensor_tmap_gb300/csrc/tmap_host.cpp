@@ -303,7 +303,7 @@ StreamArgs stream_args(const tm_desc* d, const BoxWalk& w, uint64_t images, DevS
     a.images = images;
     stream_plan(a, d->box_bytes, span_of(d->swizzle), (uint32_t)ds.sms,
                 [&](uint32_t per_sm) { return cta_budget(ds, per_sm); }, g.grid, g.smem, reduce);
-    a.sched = sched_slot(ds, stream);
+    a.sched = stream_small(a) ? nullptr : sched_slot(ds, stream);  // small boxes: static split
     a.batch = fetch_batch(reduce);
     a.timeout_ns = wait_limit_ns();
     a.status = ds.status;
