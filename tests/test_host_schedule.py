@@ -20,6 +20,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 CUDA_INC = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
 
 PROGRAM = r"""
+#include <algorithm>
 #include <cstdio>
 #include <cstring>
 #include <vector>
@@ -63,6 +64,27 @@ int main() {
             }
             for (unsigned long long b = 0; b < nbox; b++) ok = ok && seen[b] == 1;
             printf("%d\n", ok ? 1 : 0);
+        } else if (kind == 'P') {
+            // stream_plan under GB300's shared-memory limits (228 KiB per SM, 227 KiB per CTA;
+            // 1 KiB per CTA reserved, 1 KiB of stage alignment and 256 B of barriers kept back)
+            unsigned long long nbox, box_bytes;
+            unsigned span, reduce;
+            scanf("%llu %llu %u %u", &nbox, &box_bytes, &span, &reduce);
+            auto budget = [](uint32_t per_sm) -> size_t {
+                const size_t share = 233472 / per_sm;
+                const size_t cap = std::min<size_t>(232448, share > 1024 ? share - 1024 : 0);
+                return cap > 2048 + 256 ? cap - 1024 - 256 : 0;
+            };
+            StreamArgs a;
+            memset(&a, 0, sizeof(a));
+            a.walk.nbox = nbox;
+            a.walk.rank = 1;
+            a.walk.grid_nb[0] = nbox;
+            uint32_t grid = 0;
+            size_t smem = 0;
+            stream_plan(a, box_bytes, span, 152, budget, grid, smem, reduce != 0);
+            printf("%u %u %u %u %u %zu %d\n", a.group, a.slot_bytes, a.stage_bytes, a.stages, grid,
+                   smem, stream_small(a) ? 1 : 0);
         } else {
             unsigned long long ntiles, anb, bnb;
             unsigned grid;
@@ -97,8 +119,9 @@ def program(tmp_path_factory):
 
 
 def run(program, lines):
+    env = {k: v for k, v in os.environ.items() if not k.startswith("TM_")}  # the defaults
     r = subprocess.run([program], input="\n".join(lines) + "\n", capture_output=True, text=True,
-                       check=True)
+                       check=True, env=env)
     return [list(map(int, ln.split())) for ln in r.stdout.splitlines()]
 
 
@@ -182,3 +205,46 @@ def test_ring_schedule_matches_the_per_cta_definitions(program):
         for b in range(grid):
             assert n_base + (1 if b < n_rem else 0) == (ntiles - 1 - b) // grid + 1
         assert (a_d0, a_d1, b_d0, b_d1) == (grid % anb, grid // anb, grid % bnb, grid // bnb)
+
+
+def expected_plan(nbox, box_bytes, span, reduce):
+    """The streaming launch shape by its stated rules: image slots rounded up to the swizzle
+    period (1024 / 512 / 256 B, 128 B without); slots of at most 1 KiB take 16 KiB stages and 4 CTAs
+    per SM, others 32 KiB stages and one CTA; as many stages as fit (reductions at most 4)."""
+    period = {128: 1024, 64: 512, 32: 256}.get(span, 128)
+    sl = -(-box_bytes // period) * period
+    small = sl <= 1024
+    group = min(max((16384 if small else 32768) // sl, 1), 64)
+    slot = sl if group > 1 else box_bytes
+    stage = -(-(group * slot) // 1024) * 1024
+
+    def budget(per_sm):
+        share = 233472 // per_sm
+        cap = min(232448, share - 1024 if share > 1024 else 0)
+        return cap - 1280 if cap > 2048 + 256 else 0
+
+    per_sm = 4 if small else 1
+    while per_sm > 1 and budget(per_sm) < 2 * stage:
+        per_sm -= 1
+    stages = min(budget(per_sm) // stage, 16, 4 if reduce else 16)
+    grid = min(-(-nbox // group), 152 * per_sm)
+    return [group, slot, stage, max(stages, 1), grid, max(stages, 1) * stage + 1024,
+            1 if (group > 1 and slot <= 1024) else 0]
+
+
+def test_stream_plan_launch_shapes(program):
+    cases = [(8192, 16384, 128, 0),     # W3: 128 x 64 bf16 boxes, 128B swizzle
+             (65536, 16384, 128, 1),    # W5a reduce-add: 128 x 32 fp32 boxes
+             (262144, 512, 128, 0),     # W3 through 64 x 4 boxes: 512-byte images, 1 KiB slots
+             (32768, 4096, 64, 0),      # W4 rank-3, 64B swizzle: 4 KiB boxes
+             (16384, 8192, 128, 0),     # W4 rank-3, 128B swizzle: 8 KiB boxes
+             (100, 256, 0, 0), (5000, 96, 32, 1), (7, 65536, 128, 0), (3, 200000, 0, 0),
+             (999, 1024, 128, 0), (999, 1040, 128, 0)]
+    got = run(program, ["P %d %d %d %d" % c for c in cases])
+    for c, g in zip(cases, got):
+        assert g == expected_plan(*c), (c, g)
+    # the bench's shapes, spelled out
+    assert got[0][:5] == [2, 16384, 32768, 7, 152] and got[0][6] == 0
+    assert got[1][3] == 4                                  # reductions: four stages
+    assert got[2][:5] == [16, 1024, 16384, 3, 608] and got[2][6] == 1
+    assert got[3][:5] == [8, 4096, 32768, 7, 152] and got[3][6] == 0
