@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(32, 1)
     // c, c + gridDim.x, ... for its first S + 1 items (its first stages and their first refill),
     // then batches of B consecutive items from the launch's counter (item (S + 1) * gridDim.x +
     // B * atomicAdd).  The first batch is fetched right after that first refill is issued, not
-    // before the first loads (304 CTAs fetching at once made every first stage 1.5 us late), and
+    // before the first loads (all CTAs fetching at once made every first stage 1.5 us late), and
     // each further batch one batch ahead, right after a stage's loads are issued: the producer's
     // next arrive (a release) then finds the atomic long done.  A CTA that runs faster than
     // others takes more items.

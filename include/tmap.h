@@ -31,8 +31,10 @@
  *     a launch takes items from a work counter of its stream (one per stream, up to 256 streams a
  *     device; zero between launches, reset by the launch itself), so a stream's launches must not
  *     run on another stream's counter -- the library keys them by cudaStreamGetId.  A launch made
- *     while its stream is being captured, launches on streams beyond the 256th, and TM_DYNAMIC=0
- *     use a fixed split instead; the bytes written are the same either way.
+ *     while its stream is being captured, launches on streams beyond the 256th, maps whose
+ *     images take shared-memory slots of at most 1 KiB (boxes far smaller than a stage, whose
+ *     launches run several CTAs per SM), and TM_DYNAMIC=0 use a fixed split instead; the bytes
+ *     written are the same either way.
  */
 #ifndef TMAP_GB300_H
 #define TMAP_GB300_H

@@ -165,9 +165,12 @@ def test_stream_schedule_matches_the_per_cta_definitions(program):
         grid = rng.randint(1, min(ngroups, 1216))
         cases.append((nbox, group, rank, nb, grid))
     # the bench's shapes: W3 (8192 boxes of 16 KiB, 2 a stage), W4 rank-3 (16384 and 32768 boxes,
-    # 4 and 8 a stage), W5a (65536 boxes, 2 a stage), over 304 CTAs
-    cases += [(8192, 2, 2, [128, 64, 1, 1, 1], 304), (16384, 4, 3, [16, 64, 16, 1, 1], 304),
-              (32768, 8, 3, [32, 64, 16, 1, 1], 304), (65536, 2, 2, [128, 512, 1, 1, 1], 304)]
+    # 4 and 8 a stage), W5a (65536 boxes, 2 a stage) over 152 CTAs (one per SM) and 304; W3 through
+    # 64 x 4 boxes (262144 boxes, 16 a stage) over 608 (four per SM)
+    for grid in (152, 304):
+        cases += [(8192, 2, 2, [128, 64, 1, 1, 1], grid), (16384, 4, 3, [16, 64, 16, 1, 1], grid),
+                  (32768, 8, 3, [32, 64, 16, 1, 1], grid), (65536, 2, 2, [128, 512, 1, 1, 1], grid)]
+    cases.append((262144, 16, 2, [128, 2048, 1, 1, 1], 608))
     got = run(program, ["S %d %d %d %s %d" % (n, g, r, " ".join(map(str, nb)), gr)
                         for n, g, r, nb, gr in cases])
     pos = 0
