@@ -35,10 +35,11 @@
 
 namespace tmk {
 
-// Timeline of the tracing build (see TM_TRACE_BUFFER), per CTA: slot 0 entry, 1 the producer's
-// first item staged, 2 + n the first consumer warp done with item n (n < 58), 61 the CTA's item
-// count (a number), 63 that warp done with its last item.  Shared by the copy and the store (one
-// of them runs at a time).
+// Timeline of the tracing build (see TM_TRACE_BUFFER), per CTA: slot 0 entry, 62 the producer past
+// the CTA's barrier initialisation, 60 its first item's row table written, 1 that item's bulk
+// copies issued, 2 + n the first consumer warp done with item n (n < 58), 61 the CTA's item count
+// (a number), 63 that warp done with its last item.  Shared by the copy and the store (one of
+// them runs at a time).
 TM_TRACE_BUFFER(seg)
 
 // Consumer warps per CTA: W (SegArgs::cwarps picks 8, 12 or 16; kSegWarps unless TM_FB_SEG_WARPS
@@ -379,6 +380,7 @@ __global__ void __launch_bounds__(seg_threads<kSegConsumerWarps>(), 2)
     __syncthreads();
 
     if (warp == 0) {
+        if (lane == 0) TM_STAMP(seg, 62);
         // ---- producer: walks the CTA's items with a cursor (every lane keeps the same copy).
         // Item i goes to buffer i % S once the consumers have released that buffer's item i - S.
         SegSource src;
@@ -421,6 +423,7 @@ __global__ void __launch_bounds__(seg_threads<kSegConsumerWarps>(), 2)
                 if (sg.rows) bytes += (uint32_t)(((sg.src & 15) + sg.bytes + 15) & ~15ull);
             }
             bytes = __reduce_add_sync(0xffffffffu, bytes);
+            if (i == 0 && lane == 0) TM_STAMP(seg, 60);
             const uint32_t bar = smem_u32(&full_bar[b]);
             if (lane == 0) {
                 info[b].run = cur.u;
@@ -590,6 +593,7 @@ __global__ void __launch_bounds__(seg_threads<kSegConsumerWarps>(), 2)
     __syncthreads();
 
     if (warp == 0) {
+        if (lane == 0) TM_STAMP(seg, 62);
         // ---- producer (the same item source, cursor and end marker as the copy)
         SegSource src;
         src.init(s, m0, total);
@@ -622,6 +626,7 @@ __global__ void __launch_bounds__(seg_threads<kSegConsumerWarps>(), 2)
                 for (uint32_t e = 0; e < G1; e++)
                     tab[j * G1 + e] = e < sg.rows ? sg.src + (uint64_t)e * s.row_bytes : ~0ull;
             }
+            if (i == 0 && lane == 0) TM_STAMP(seg, 60);
             const uint32_t bar = smem_u32(&full_bar[b]);
             if (lane == 0) {
                 info[b].run = cur.u;

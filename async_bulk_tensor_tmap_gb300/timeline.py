@@ -20,6 +20,10 @@ of the median launch, where that time goes:
   tail      from 90 % of the stages completed to the last CTA's exit
   spread    first to last CTA exit
 
+and for the vector path's segment kernels, per CTA (medians): `sync` entry to the producer past
+the CTA's barrier initialisation, `table` from there to its first item's row table written,
+`loads` from there to that item's bulk copies issued.
+
 The stamps sit in the tracing build only; the library itself compiles them to nothing.
 """
 from __future__ import annotations
@@ -55,9 +59,10 @@ def _stamps(lib, name: str) -> np.ndarray:
     return buf
 
 
-def analyse(stamps: np.ndarray, event_us: float, nbytes: int, item_slots) -> dict:
+def analyse(stamps: np.ndarray, event_us: float, nbytes: int, item_slots, spans=None) -> dict:
     """The decomposition above for one launch; nbytes: algorithmic bytes of the launch.  Each CTA
-    stamps its first len(item_slots) stages and records its stage count in slot 61."""
+    stamps its first len(item_slots) stages and records its stage count in slot 61.  spans: name ->
+    (slot a, slot b), reported as the median over CTAs of stamp b minus stamp a."""
     t = stamps[stamps[:, 0] > 0].astype(np.int64)
     counts = t[:, 61]
     share = float(np.minimum(counts, len(item_slots)).sum() / max(1, counts.sum()))
@@ -71,7 +76,12 @@ def analyse(stamps: np.ndarray, event_us: float, nbytes: int, item_slots) -> dic
     per_item = nbytes * share / max(1, (items >= 0).sum())
     t25, t75 = q(0.25), q(0.75)
     steady = 0.5 * len(done) * per_item / max(1e-9, (t75 - t25) * 1e-6) / 1e9
+    extra = {}
+    for name, (sa, sb) in (spans or {}).items():
+        ok = (t[:, sa] > 0) & (t[:, sb] > 0)
+        extra[name] = round(float(np.median((t[ok, sb] - t[ok, sa]) / 1000.0)), 2) if ok.any() else None
     return {
+        **extra,
         "event_us": round(event_us, 2), "span_us": round(span, 2),
         "outside_us": round(event_us - span, 2),
         "issue_us": round(float(np.median(rel[:, 1])), 2),
@@ -102,7 +112,7 @@ def main():
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).reshape(-1).view(np.uint8)).cuda()
 
-    def timed(fn, kname, nbytes, item_slots, reps, pre=None):
+    def timed(fn, kname, nbytes, item_slots, reps, pre=None, spans=None):
         for _ in range(3):
             flush.fill_(1)
             fn()
@@ -126,7 +136,7 @@ def main():
             raise RuntimeError(tm.tm_last_error())
         runs.sort(key=lambda r: r[0])
         ev, st = runs[len(runs) // 2]
-        out = analyse(st, ev, nbytes, item_slots) if kname else {"event_us": round(ev, 2)}
+        out = analyse(st, ev, nbytes, item_slots, spans) if kname else {"event_us": round(ev, 2)}
         out["event_us_all"] = [round(r[0], 2) for r in runs]
         return out
 
@@ -171,9 +181,11 @@ def main():
     img5 = torch.empty(m5.num_boxes * m5.box_bytes, dtype=torch.uint8, device="cuda")
     nb5 = 16 * 4095 * 1000 * 2 + m5.num_boxes * m5.box_bytes
     seg_items = list(range(2, 60))
-    res["w4r5.copy"] = timed(lambda: tm.tiled_copy(m5, None, img5), "seg", nb5, seg_items, args.reps)
+    seg_spans = {"sync_us": (0, 62), "table_us": (62, 60), "loads_us": (60, 1)}
+    res["w4r5.copy"] = timed(lambda: tm.tiled_copy(m5, None, img5), "seg", nb5, seg_items, args.reps,
+                             spans=seg_spans)
     res["w4r5.roundtrip"] = timed(lambda: tm.tiled_roundtrip(m5o, None, img5), "seg", nb5, seg_items,
-                                  args.reps)
+                                  args.reps, spans=seg_spans)
     del x4d, img4, out4, img5
 
     a, b = workloads.w5b_tensors()
@@ -197,7 +209,7 @@ def main():
                               stream_items, max(3, args.reps // 2))
 
     cols = ["event_us", "outside_us", "span_us", "issue_us", "first_us", "steady_GBps", "tail_us",
-            "spread_us", "GBps"]
+            "spread_us", "GBps", "sync_us", "table_us", "loads_us"]
     print("| launch | " + " | ".join(cols) + " |")
     print("|---" * (len(cols) + 1) + "|")
     for k, v in res.items():
