@@ -89,13 +89,15 @@ struct StreamArgs {
     uint32_t dstep[5];     // digits (radix: the grid's box counts) of grid x G boxes
     uint32_t pad;
     // Dynamic work split (when sched is set): items g = 0 .. nitems - 1 of G boxes (the last one
-    // short); CTA c takes c, c + grid, ... for its first `stages` items, then the next free item
-    // from sched[0] (a counter of this launch's stream, zero at launch; sched[1] counts the CTAs
-    // that are done, and the last one sets both back to zero).
+    // short); CTA c takes c, c + grid, ... for its first stages + 1 items, then fetches from
+    // sched[0] (a counter of this launch's stream, zero at launch; sched[1] counts the CTAs that
+    // are done, and the last one sets both back to zero).  Fetches 0 .. batched - 1 take `batch`
+    // consecutive items each, later fetches one item: the last items of a launch go out singly.
     unsigned long long* sched;
     uint64_t nitems;
-    uint32_t batch;        // items per fetch from the counter
+    uint32_t batch;        // items per fetch from the counter, for the first `batched` fetches
     uint32_t pad2;
+    uint64_t batched;
 };
 
 // CTAs per SM of the streaming kernels (see stream_plan).  One, with as many 32 KiB stages as fit
@@ -244,6 +246,7 @@ inline void stream_plan(StreamArgs& a, uint64_t box_bytes, uint32_t span, uint32
     a.nitems = units;
     a.sched = nullptr;  // the static schedule unless the caller hands the launch a counter
     a.batch = 1;        // items per fetch of the dynamic split (the caller may raise it)
+    a.batched = 0;
     smem = (size_t)a.stages * a.stage_bytes + kStageAlign;
 }
 
