@@ -1,13 +1,15 @@
-// k_tma.cu -- persistent TMA streaming kernels: tiled copy, round trip and fp32 reduce-add.
+// k_tma.cu -- persistent TMA streaming kernels: tiled copy, round trip and tensor reduce (add, min, max).
 //
 // One CTA is one warp; its elected lane issues everything ([MLSys-TMA] = mlc.ai "Modern GPU
 // Programming for MLSys", chapter "异步数据搬运：TMA", §"一个 thread 如何描述整个 tile": a single
 // thread submits the copy, the engine does the addressing).  Boxes are taken in items of up to G
 // consecutive boxes sharing a stage (G > 1 for boxes well under a stage), each in a slot that
 // starts on its swizzle period (1024 / 512 / 256 bytes for 128B / 64B / 32B, 128 without), so that
-// each image in a stage keeps the swizzle phase it has in its own image.  CTA c takes item c of
-// every full wave of gridDim.x x G boxes, then its share of the tail, dealt out box by box
-// (stream_item), through an S-stage ring of 1024-byte aligned shared-memory stages:
+// each image in a stage keeps the swizzle phase it has in its own image.  The items come from one
+// of two splits: static (CTA c takes item c of every full wave of gridDim.x x G boxes, then its
+// share of the tail, dealt out box by box: stream_item) or dynamic (a static prefix, then items
+// from a counter of the launch's stream, so that faster CTAs take more; see next_item).  They
+// pass through an S-stage ring of 1024-byte aligned shared-memory stages:
 //
 //   load   item i into stage i % S     (one mbarrier, arrive.expect_tx of the item's bytes, one
 //                                        complete_tx per box, §"如何等待 TMA load 完成")
@@ -17,13 +19,14 @@
 //          READING shared memory (wait_group.read 1): the write of item i stays in flight
 //          (with a single stage, the stage of item i once its own write has read it).
 //
-// The lane keeps two cursors over its items, one for loads (running up to S items ahead) and one
-// for writes: each holds the stage, its phase parity and, for a grid walk, the box counters of
-// the item's first box, stepped by G * gridDim.x boxes with carries (the tail item's counters are
-// found once, before the first load); the boxes inside an item are stepped with an odometer.  No
-// 64-bit division is left on the issue path.  The copy instructions carry no L2 policy: evict-first
-// or evict-last policies on the loads or the writes measured no gain on GB300, and choosing between
-// the policy and plain forms box by box cost the 512-byte-box copy a quarter of its issue rate.
+// Each stage records the item it holds (its first box, box count and, for a grid walk, the box
+// counters of its first box), written when the loads are issued and read when the stage is
+// written out.  The static split steps those counters by G * gridDim.x boxes with carries (the
+// tail item's are found once, before the first load); the dynamic split decomposes each item's
+// first box index (32-bit divisions when it fits); the boxes inside an item are stepped with an
+// odometer.  The copy instructions carry no L2 policy: evict-first or evict-last policies on the
+// loads or the writes measured no gain on GB300, and choosing between the policy and plain forms
+// box by box cost the 512-byte-box copy a quarter of its issue rate.
 //
 // The three kinds differ only in the two copy instructions:
 //   copy       load = tensor load of the box;  write = 1-D bulk store of the image (tile-major)
