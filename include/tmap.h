@@ -35,6 +35,23 @@
  *     images take shared-memory slots of at most 1 KiB (boxes far smaller than a stage, whose
  *     launches run several CTAs per SM), and TM_DYNAMIC=0 use a fixed split instead; the bytes
  *     written are the same either way.
+ *   - Environment (read at each launch; none changes the bytes written, only the launch shape;
+ *     the defaults are the shapes measured fastest on GB300):
+ *       TM_WAIT_TIMEOUT_NS        limit of every bounded wait (1e9)
+ *       TM_DYNAMIC                0: fixed split everywhere (1)
+ *       TM_DYN_BATCH, TM_DYN_BATCH_REDUCE   items a fetch for copies, reductions (1, 4)
+ *       TM_DYN_TAPER              last items per CTA handed out singly in batched launches (4)
+ *       TM_GROUP_BYTES            stage size of the tensor-map streaming kernels (32768; 16384
+ *                                 for image slots of at most 1 KiB)
+ *       TM_CTAS_PER_SM            CTAs per SM of those kernels (1; 4 for small slots)
+ *       TM_STAGES, TM_STAGES_REDUCE   stage cap for copies, reductions (none, 4)
+ *       TM_FB_SEG                 vector path segment form: 0 never, 1 whenever possible (auto)
+ *       TM_FB_SEG_CTAS_PER_SM, TM_FB_SEG_STAGES, TM_FB_SEG_WARPS   segment kernels' shape
+ *                                 (2; 3 copy / 2 store; 12 consumer warps: 8, 12 or 16)
+ *       TM_FB_COPY_CTAS_PER_SM, TM_FB_STORE_CTAS_PER_SM   per-window vector kernels (8, 6)
+ *       TM_RING_GROUPS, TM_RING_EVICT_FIRST, TM_RING_ROW_PAIRS, TM_RING_PREFETCH   stream_tiles
+ *                                 (2 consumer groups, evict-first loads on, 0, 0)
+ *       TM_GEMM_PAIR, TM_GEMM_TAIL_SPLIT   stream_gemm: CTA pairs, split last wave (1, 1)
  */
 #ifndef TMAP_GB300_H
 #define TMAP_GB300_H
