@@ -266,14 +266,18 @@ double orc_f16_to_double(uint16_t h)
     return sign * ldexp((double)(1024u + m), (int)e - 25);
 }
 
-/* The value v (finite) rounded to nearest, ties to even, in a binary format with `mbits` stored
+/* The value v rounded to nearest, ties to even, in a binary format with `mbits` stored
  * significand bits and `ebits` exponent bits (bias 2^(ebits-1) - 1, subnormals, overflow to
- * infinity); returns the bits. */
+ * infinity); returns the bits.  An infinite v stays infinite; a NaN v gives the format's quiet NaN
+ * with an empty payload (IEEE 754 leaves the payload of an operation's NaN open). */
 static uint32_t round_to_format(double v, int mbits, int ebits)
 {
     const int emax = (1 << (ebits - 1)) - 1, emin = 1 - emax;
+    const uint32_t all_ones = ((1u << ebits) - 1u) << mbits;
+    if (isnan(v)) return all_ones | (1u << (mbits - 1));
     const uint32_t sign_bit = (signbit(v) ? 1u : 0u) << (mbits + ebits);
     v = fabs(v);
+    if (isinf(v)) return sign_bit | all_ones;
     if (v == 0.0) return sign_bit;
     int e2;
     frexp(v, &e2);

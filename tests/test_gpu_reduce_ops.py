@@ -61,6 +61,51 @@ def test_reduce_ops(tm, kind, op, force_fallback):
     run_case(tm, kind, op, 300, 200, 208, force_fallback, seed=100 + 7 * op + KINDS.index(kind))
 
 
+def _nan_mask(bits, kind):
+    b = bits.astype(np.uint32)
+    if kind == "f32":
+        return ((b & 0x7F800000) == 0x7F800000) & ((b & 0x007FFFFF) != 0)
+    if kind == "f16":
+        return ((b & 0x7C00) == 0x7C00) & ((b & 0x03FF) != 0)
+    if kind == "bf16":
+        return ((b & 0x7F80) == 0x7F80) & ((b & 0x007F) != 0)
+    return np.zeros(b.shape, bool)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("op", [0, 1, 2])
+@pytest.mark.parametrize("force_fallback", [False, True])
+def test_reduce_special_values(tm, kind, op, force_fallback):
+    """Every pair of the formats' special values (zeros of both signs, subnormals, the smallest
+    normal, the largest finite, infinities, NaNs; integer wrap points) and a seeded mix around
+    them, on the bulk tensor reduce and on the vector path.  Bit for bit against the oracle where
+    its result is a number; where it is a NaN, a NaN (the payload of an operation's NaN is open)."""
+    rows, cols, pitch = 64, 96, 96
+    d, s = workloads.special_reduce_operands(kind, rows, pitch, seed=500 + 3 * op + KINDS.index(kind))
+    r = recipe(kind, rows, cols, pitch)
+    dd, sd = to_dev(d), to_dev(s)
+    dt = tm_dtype(tm, kind)
+    md = tm.tmap_encode(dt, dd, r["dims"], r["strides"], r["box"], swizzle=tm.TM_SWIZZLE_128B)
+    ms = tm.tmap_encode(dt, sd, r["dims"], r["strides"], r["box"], swizzle=tm.TM_SWIZZLE_128B)
+    if force_fallback:
+        tm.tmap_force_fallback(md)
+    tm.tile_reduce(md, ms, op)
+    torch.cuda.synchronize()
+    assert tm.tm_stream_check() == tm.TM_OK, tm.tm_last_error()
+    hd = np.ascontiguousarray(d).copy()
+    oracle.tile_reduce(host_map(hd, r), host_map(np.ascontiguousarray(s), r), ORC_TYPE[kind], op)
+    es = r["esize"]
+    ut = np.uint32 if es == 4 else np.uint16
+    want = hd.reshape(-1).view(ut)
+    got = to_host(dd).view(ut)
+    nan = _nan_mask(want, kind)
+    bad = np.flatnonzero(~nan & (got != want))
+    assert bad.size == 0, (f"{kind} op {op} fallback={force_fallback}: {bad.size} mismatches, first "
+                           f"dst {d.reshape(-1).view(ut)[bad[0]]:#x} src {s.reshape(-1).view(ut)[bad[0]]:#x} "
+                           f"got {got[bad[0]]:#x} want {want[bad[0]]:#x}")
+    assert _nan_mask(got[nan], kind).all(), f"{kind} op {op}: a NaN result came back as a number"
+
+
 @pytest.mark.parametrize("kind", ["bf16", "u32"])
 def test_reduce_ragged_row_end_keeps_padding(tm, kind):
     # inner extent not a multiple of 16 bytes: the vector path, padding must survive

@@ -71,6 +71,12 @@ MUTANTS = {
     "float_max_picks_smaller": ("if (op == ORC_MAX) return x > y ? a : (y > x ? b : a);",
                                 "if (op == ORC_MAX) return x < y ? a : (y < x ? b : a);"),
     "half_add_drops_operand": ("    const double sum = x + y;", "    const double sum = x + 0 * y;"),
+    "half_infinity_becomes_max_finite": ("    if (isinf(v)) return sign_bit | all_ones;\n",
+                                         "    if (isinf(v)) return sign_bit | (all_ones - 1u);\n"),
+    "half_nan_becomes_infinity": ("    if (isnan(v)) return all_ones | (1u << (mbits - 1));",
+                                  "    if (isnan(v)) return all_ones;"),
+    "min_takes_nan_src": ("    if (op == ORC_MIN) return x < y ? a : (y < x ? b : a);",
+                          "    if (op == ORC_MIN) return x < y ? a : (x != x || y != y || y < x ? b : a);"),
 }
 
 

@@ -154,3 +154,78 @@ def test_tile_reduce_equals_elementwise(t, op):
     ms = oracle.Map(src, es, r["dims"], r["strides"], r["box"], span)
     oracle.tile_reduce(md, ms, t, op)
     np.testing.assert_array_equal(dst, want)
+
+
+def _is_nan(bits: int, t: int) -> bool:
+    if t == F32:
+        return (bits & 0x7F800000) == 0x7F800000 and (bits & 0x007FFFFF) != 0
+    if t == F16:
+        return (bits & 0x7C00) == 0x7C00 and (bits & 0x03FF) != 0
+    return (bits & 0x7F80) == 0x7F80 and (bits & 0x007F) != 0
+
+
+# IEEE 754 facts of one correctly rounded add (round to nearest): infinities absorb finite values,
+# opposite infinities and NaN operands give a NaN, overflow rounds to infinity, x + (-x) is +0,
+# (-0) + (-0) is -0, and subnormal sums are exact.  NaN stands for any NaN pattern.
+NAN = None
+SPECIAL_ADDS = {
+    F32: [(0x7F800000, 0x3F800000, 0x7F800000), (0xFF800000, 0x3F800000, 0xFF800000),
+          (0x7F800000, 0xFF800000, NAN), (0x7FC00000, 0x3F800000, NAN), (0x3F800000, 0x7FC00000, NAN),
+          (0x7F7FFFFF, 0x7F7FFFFF, 0x7F800000), (0xFF7FFFFF, 0xFF7FFFFF, 0xFF800000),
+          (0x00000001, 0x00000001, 0x00000002), (0x00800000, 0x80000001, 0x007FFFFF),
+          (0x3F800000, 0xBF800000, 0x00000000), (0x80000000, 0x80000000, 0x80000000),
+          (0x00000000, 0x80000000, 0x00000000), (0x807FFFFF, 0x00000001, 0x807FFFFE)],
+    F16: [(0x7C00, 0x3C00, 0x7C00), (0xFC00, 0x3C00, 0xFC00), (0x7C00, 0xFC00, NAN),
+          (0x7E00, 0x3C00, NAN), (0x3C00, 0x7E00, NAN), (0x7BFF, 0x7BFF, 0x7C00),
+          (0xFBFF, 0xFBFF, 0xFC00), (0x0001, 0x0001, 0x0002), (0x0400, 0x8001, 0x03FF),
+          (0x3C00, 0xBC00, 0x0000), (0x8000, 0x8000, 0x8000), (0x0000, 0x8000, 0x0000),
+          (0x03FF, 0x0001, 0x0400)],
+    BF16: [(0x7F80, 0x3F80, 0x7F80), (0xFF80, 0x3F80, 0xFF80), (0x7F80, 0xFF80, NAN),
+           (0x7FC0, 0x3F80, NAN), (0x3F80, 0x7FC0, NAN), (0x7F7F, 0x7F7F, 0x7F80),
+           (0xFF7F, 0xFF7F, 0xFF80), (0x0001, 0x0001, 0x0002), (0x0080, 0x8001, 0x007F),
+           (0x3F80, 0xBF80, 0x0000), (0x8000, 0x8000, 0x8000), (0x0000, 0x8000, 0x0000),
+           (0x007F, 0x0001, 0x0080)],
+}
+
+
+@pytest.mark.parametrize("t", [F32, F16, BF16])
+def test_special_value_adds_follow_ieee(t):
+    for a, b, want in SPECIAL_ADDS[t]:
+        got = oracle.combine(a, b, t, ADD)
+        if want is NAN:
+            assert _is_nan(got, t), (hex(a), hex(b), hex(got))
+        else:
+            assert got == want, (hex(a), hex(b), hex(got), hex(want))
+
+
+@pytest.mark.parametrize("t, one, nan, pz, nz", [(F32, 0x3F800000, 0x7FC00000, 0, 0x80000000),
+                                                (F16, 0x3C00, 0x7E00, 0, 0x8000),
+                                                (BF16, 0x3F80, 0x7FC0, 0, 0x8000)])
+def test_special_value_min_max_keep_dst_unless_src_is_strictly_beyond(t, one, nan, pz, nz):
+    # src replaces dst only when it compares strictly below (min) / above (max): a NaN on either
+    # side and a tie of +0 with -0 keep dst
+    for op in (MIN, MAX):
+        assert oracle.combine(nan, one, t, op) == nan
+        assert oracle.combine(one, nan, t, op) == one
+        assert oracle.combine(pz, nz, t, op) == pz
+        assert oracle.combine(nz, pz, t, op) == nz
+    assert oracle.combine(one, nz, t, MIN) == nz
+    assert oracle.combine(nz, one, t, MAX) == one
+
+
+def test_f16_adds_with_every_special_exponent_match_numpy():
+    """All f16 patterns, infinities and NaNs included, against numpy's half add (the double sum
+    of two halves is exact, so numpy's rounding of it is the reference); NaN results as NaN."""
+    rng = np.random.default_rng(9)
+    specials = np.array([0x7C00, 0xFC00, 0x7E00, 0xFE01, 0x0000, 0x8000, 0x0001, 0x83FF, 0x7BFF,
+                         0xFBFF, 0x0400], np.uint16)
+    a = np.concatenate([np.repeat(specials, len(specials)), rng.integers(0, 1 << 16, 4000).astype(np.uint16)])
+    b = np.concatenate([np.tile(specials, len(specials)), rng.integers(0, 1 << 16, 4000).astype(np.uint16)])
+    with np.errstate(over="ignore", invalid="ignore"):
+        ref = (a.view(np.float16).astype(np.float64) + b.view(np.float16).astype(np.float64)).astype(np.float16)
+    for x, y, r in zip(a, b, ref):
+        got = oracle.combine(int(x), int(y), F16, ADD)
+        if np.isnan(r):
+            assert _is_nan(got, F16), (hex(x), hex(y), hex(got))
+        else:
+            assert got == int(r.view(np.uint16)), (hex(x), hex(y), hex(got))

@@ -164,6 +164,43 @@ def reduce_operands(kind: str, rows: int, cols: int, seed: int):
         d[bad], s[bad] = draw(n), draw(n)
 
 
+# Bit patterns of the special values of each float format: zeros, the smallest and largest
+# subnormals, the smallest normal, one, the largest finite, infinities and quiet NaNs, both signs.
+SPECIAL_BITS = {
+    "f32": [0x00000000, 0x80000000, 0x00000001, 0x80000001, 0x007FFFFF, 0x807FFFFF, 0x00800000,
+            0x80800000, 0x3F800000, 0xBF800000, 0x7F7FFFFF, 0xFF7FFFFF, 0x7F800000, 0xFF800000,
+            0x7FC00000, 0xFFC00001],
+    "f16": [0x0000, 0x8000, 0x0001, 0x8001, 0x03FF, 0x83FF, 0x0400, 0x8400, 0x3C00, 0xBC00,
+            0x7BFF, 0xFBFF, 0x7C00, 0xFC00, 0x7E00, 0xFE01],
+    "bf16": [0x0000, 0x8000, 0x0001, 0x8001, 0x007F, 0x807F, 0x0080, 0x8080, 0x3F80, 0xBF80,
+             0x7F7F, 0xFF7F, 0x7F80, 0xFF80, 0x7FC0, 0xFFC1],
+    "u32": [0, 1, 2, 0x7FFFFFFF, 0x80000000, 0x80000001, 0xFFFFFFFE, 0xFFFFFFFF],
+    "s32": [0, 1, 2, 0x7FFFFFFF, 0x80000000, 0x80000001, 0xFFFFFFFE, 0xFFFFFFFF],
+}
+
+
+def special_reduce_operands(kind: str, rows: int, cols: int, seed: int):
+    """Destination and source bit patterns (rows x cols) for the general reduce at the formats'
+    edges: the first len(SPECIAL_BITS[kind])^2 elements hold every (dst, src) pair of special
+    patterns, the rest a seeded mix of special patterns, their neighbours (one unit in the last
+    place up) and uniform random patterns."""
+    rng = np.random.default_rng(seed)
+    sp = np.array(SPECIAL_BITS[kind], dtype=np.uint64)
+    width = 32 if kind in ("f32", "u32", "s32") else 16
+    n = rows * cols
+    pick = rng.integers(0, 3, size=(2, n))
+    cand = np.stack([sp[rng.integers(0, len(sp), size=(2, n))],
+                     (sp[rng.integers(0, len(sp), size=(2, n))] + 1) % (1 << width),
+                     rng.integers(0, 1 << width, size=(2, n), dtype=np.uint64)])
+    v = np.take_along_axis(cand, pick[None], axis=0)[0]
+    k = len(sp)
+    v[0, :k * k] = np.repeat(sp, k)[:n]
+    v[1, :k * k] = np.tile(sp, k)[:n]
+    dt = np.uint32 if width == 32 else np.uint16
+    d, s = v[0].astype(dt).reshape(rows, cols), v[1].astype(dt).reshape(rows, cols)
+    return (d.view(np.int32), s.view(np.int32)) if kind == "s32" else (d, s)
+
+
 # Map recipes, dims innermost first: (dims, byte strides of dims 1.., box, swizzle span)
 def w3_map(rows: int = 8192, cols: int = 8192, span: int = 128):
     return dict(dims=[cols, rows], strides=[cols * 2], box=[64, 128], span=span, esize=2)
