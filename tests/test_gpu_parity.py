@@ -434,6 +434,46 @@ def test_w5b_ring_checksums(tm, span, stages):
     np.testing.assert_array_equal(to_host(bits_b).astype(np.uint64), wbb)
 
 
+@pytest.mark.parametrize("stages", [2, 4])
+def test_w5b_ring_checksums_special_values(tm, stages):
+    """Tiles of arbitrary bf16 patterns (every special pair, their neighbours and uniform random
+    bits: subnormals, infinities, NaNs): the fp32 row sums bit for bit against the oracle where
+    they are numbers and NaN where the oracle's are (the payload of an operation's NaN is open);
+    the sums of the 16-bit patterns exactly."""
+    a0, b0 = workloads.w5b_tensors(m=380, k=248, n=376, seed_a=9, seed_b=10)
+    finite = [0x0000, 0x8000, 0x0001, 0x8001, 0x007F, 0x807F, 0x0080, 0x8080, 0x3F80, 0xBF80]
+
+    def mix(x0, seed, which):
+        # finite special patterns everywhere; the full mix (NaNs, infinities, the largest
+        # finite) in the first 64 rows only, so that some tiles sum to numbers and some do not
+        sp = workloads.special_reduce_operands("bf16", *x0.shape, seed=seed)[which].reshape(x0.shape)
+        x = x0.copy()
+        pick = np.isin(sp, finite)
+        x[pick] = sp[pick]
+        x[:64] = sp[:64]
+        return x
+
+    a, b = mix(a0, 31, 0), mix(b0, 32, 1)
+    ra, rb = workloads.w5b_maps(m=380, k=248, n=376, span=128)
+    ad, bd = to_dev(a), to_dev(b)
+    ma, mb = dev_map(tm, ad, ra), dev_map(tm, bd, rb)
+    n = ma.num_boxes
+    cs_a = guarded(4 * n, 0).view(torch.float32)
+    cs_b = guarded(4 * n, 0).view(torch.float32)
+    bits_a = guarded(8 * n, 0).view(torch.int64)
+    bits_b = guarded(8 * n, 0).view(torch.int64)
+    tm.stream_tiles(ma, mb, stages, cs_a, cs_b, bits_a, bits_b)
+    check(tm)
+    wa, wb, wba, wbb = oracle.stream_checksums(host_map(a, ra), host_map(b, rb))
+    for got, want in ((to_host(cs_a).view(np.float32), wa), (to_host(cs_b).view(np.float32), wb)):
+        nan = np.isnan(want)
+        assert nan.any() and not nan.all()  # the tiles exercise both outcomes
+        np.testing.assert_array_equal(got[~nan].view(np.uint32), want[~nan].view(np.uint32))
+        assert np.isnan(got[nan]).all()
+    np.testing.assert_array_equal(to_host(bits_a).astype(np.uint64), wba)
+    np.testing.assert_array_equal(to_host(bits_b).astype(np.uint64), wbb)
+
+
 # Many laps of the ring on every CTA: tiles of every supported height, ragged in both dims (296
 # columns = 4 full 64-column boxes + 40; rows not a multiple of the tile), with one consumer group,
 # two (even and odd tiles), and the row-pairs read order (the ungrouped bank-conflict control,
