@@ -109,12 +109,12 @@ __global__ void __launch_bounds__(32, 1)
     // their counters stepped by G * gridDim.x boxes with carries (the tail item's found once).
     // Dynamic: items g = 0 .. nitems - 1 of G boxes each (the last one short); CTA c first takes
     // c, c + gridDim.x, ... for its first S + 1 items (its first stages and their first refill),
-    // then batches of B consecutive items from the launch's counter (item (S + 1) * gridDim.x +
-    // B * atomicAdd), and past the first a.batched fetches single items.  The first batch is
-    // fetched right after that first refill is issued, not before the first loads (all CTAs
-    // fetching at once made every first stage 1.5 us late), and each further batch one batch
-    // ahead, right after a stage's loads are issued: the producer's next arrive (a release) then
-    // finds the atomic long done.  A CTA that runs faster than others takes more items.
+    // then the items of the counter's fetches (dyn_fetch: batches of a.batch consecutive items,
+    // single items past the first a.batched fetches).  The first batch is fetched right after
+    // that first refill is issued, not before the first loads (all CTAs fetching at once made
+    // every first stage 1.5 us late), and each further batch one batch ahead, right after a
+    // stage's loads are issued: the producer's next arrive (a release) then finds the atomic long
+    // done.  A CTA that runs faster than others takes more items.
     uint64_t si = 0;                        // static: the next item index of this CTA
     uint32_t sk[5] = {0, 0, 0, 0, 0};       // static: counters of item si - 1
     uint32_t tail_k[5] = {0, 0, 0, 0, 0};   // static: counters of the tail item's first box
@@ -125,7 +125,6 @@ __global__ void __launch_bounds__(32, 1)
     const uint64_t npre = (uint64_t)S + 1;  // static items per CTA before the counter
     const uint64_t prefix = npre * grid_ctas;
     bool first_fetch = dyn && prefix < a.nitems;
-    const uint32_t B = a.batch ? a.batch : 1u;
     if (!dyn && grid && a.waves > 0 && a.waves < n_local) {
         uint64_t tb;
         uint32_t tc;
@@ -142,13 +141,8 @@ __global__ void __launch_bounds__(32, 1)
                 if (g >= a.nitems) return false;
             } else {
                 if (bg == bend) {  // the current batch is done: take the one fetched ahead
-                    uint64_t n = B;
-                    if (pend < a.batched) {
-                        bg = prefix + (uint64_t)pend * B;
-                    } else {  // past the batched fetches: one item a fetch
-                        bg = prefix + a.batched * B + ((uint64_t)pend - a.batched);
-                        n = 1;
-                    }
+                    uint64_t n;
+                    dyn_fetch(a, prefix, (uint64_t)pend, bg, n);
                     if (bg >= a.nitems) return false;
                     bend = bg + n < a.nitems ? bg + n : a.nitems;
                     refetch = true;

@@ -166,6 +166,35 @@ TM_HD inline void stream_item(const StreamArgs& a, uint32_t c, uint32_t grid, ui
     }
 }
 
+// Dynamic split (a.sched set): CTA c of `grid` first takes items c, c + grid, ... for its first
+// stages + 1 items (the static prefix, `prefix` = (stages + 1) * grid items in all), then fetches
+// p = 0, 1, ... from the counter: fetch p covers items first .. first + count - 1 (clipped to
+// nitems; a fetch past the items ends the CTA's work).  The first `batched` fetches take `batch`
+// items each, later ones a single item.
+TM_HD inline void dyn_fetch(const StreamArgs& a, uint64_t prefix, uint64_t p, uint64_t& first,
+                            uint64_t& count)
+{
+    const uint64_t B = a.batch ? a.batch : 1u;
+    if (p < a.batched) {
+        first = prefix + p * B;
+        count = B;
+    } else {
+        first = prefix + a.batched * B + (p - a.batched);
+        count = 1;
+    }
+}
+
+// Fills `batched` for a launch of `grid` CTAs: whole batches until about taper_per_cta x grid items
+// are left, then single items (with several items a fetch, a CTA could otherwise hold a whole batch
+// more than another when the items run out).
+inline void dyn_taper(StreamArgs& a, uint32_t grid, uint64_t taper_per_cta)
+{
+    const uint64_t prefix = (uint64_t)(a.stages + 1) * grid;
+    const uint64_t rest = a.nitems > prefix ? a.nitems - prefix : 0;
+    const uint64_t single = rest < (uint64_t)grid * taper_per_cta ? rest : (uint64_t)grid * taper_per_cta;
+    a.batched = a.batch > 1 ? (rest - single) / a.batch : 0;
+}
+
 // Generic fallback kernels.
 struct FbArgs {
     BoxWalk walk;

@@ -309,12 +309,8 @@ StreamArgs stream_args(const tm_desc* d, const BoxWalk& w, uint64_t images, DevS
                 [&](uint32_t per_sm) { return cta_budget(ds, per_sm); }, g.grid, g.smem, reduce);
     a.sched = stream_small(a) ? nullptr : sched_slot(ds, stream);  // small boxes: static split
     a.batch = fetch_batch(reduce);
-    // The last grid x kTaperPerCta items (TM_DYN_TAPER per CTA) go out one a fetch: with several
-    // items a fetch a CTA can hold a whole batch more than another when the items run out.
-    const uint64_t prefix = (uint64_t)(a.stages + 1) * g.grid;
-    const uint64_t rest = a.nitems > prefix ? a.nitems - prefix : 0;
-    const uint64_t single = std::min<uint64_t>(rest, (uint64_t)g.grid * env_u64("TM_DYN_TAPER", kTaperPerCta));
-    a.batched = a.batch > 1 ? (rest - single) / a.batch : 0;
+    // the last grid x kTaperPerCta items (TM_DYN_TAPER per CTA) go out one a fetch
+    dyn_taper(a, g.grid, env_u64("TM_DYN_TAPER", kTaperPerCta));
     a.timeout_ns = wait_limit_ns();
     a.status = ds.status;
     return a;

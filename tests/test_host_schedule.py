@@ -64,6 +64,37 @@ int main() {
             }
             for (unsigned long long b = 0; b < nbox; b++) ok = ok && seen[b] == 1;
             printf("%d\n", ok ? 1 : 0);
+        } else if (kind == 'D') {
+            // the dynamic split's items: every CTA's static prefix, then fetches p = 0, 1, ...
+            // until one starts past the items; prints whether every item is taken exactly once
+            unsigned long long nitems, batch, taper;
+            unsigned stages, grid;
+            scanf("%llu %u %u %llu %llu", &nitems, &stages, &grid, &batch, &taper);
+            StreamArgs a;
+            memset(&a, 0, sizeof(a));
+            a.nitems = nitems;
+            a.stages = stages;
+            a.batch = (uint32_t)batch;
+            dyn_taper(a, grid, taper);
+            std::vector<unsigned char> seen(nitems, 0);
+            bool ok = true;
+            const uint64_t prefix = (uint64_t)(stages + 1) * grid;
+            for (unsigned c = 0; c < grid; c++)
+                for (uint64_t dj = 0; dj <= stages; dj++) {
+                    const uint64_t g = c + dj * grid;
+                    if (g < nitems) ok = ok && seen[g]++ == 0;
+                }
+            unsigned long long fetches = 0, singles = 0;
+            for (uint64_t p = 0;; p++) {
+                uint64_t first, count;
+                dyn_fetch(a, prefix, p, first, count);
+                if (first >= nitems) break;
+                fetches++;
+                if (count == 1 && batch > 1) singles++;
+                for (uint64_t g = first; g < first + count && g < nitems; g++) ok = ok && seen[g]++ == 0;
+            }
+            for (uint64_t g = 0; g < nitems; g++) ok = ok && seen[g] == 1;
+            printf("%d %llu %llu %llu\n", ok ? 1 : 0, (unsigned long long)a.batched, fetches, singles);
         } else if (kind == 'P') {
             // stream_plan under GB300's shared-memory limits (228 KiB per SM, 227 KiB per CTA;
             // 1 KiB per CTA reserved, 1 KiB of stage alignment and 256 B of barriers kept back)
@@ -251,3 +282,25 @@ def test_stream_plan_launch_shapes(program):
     assert got[1][3] == 4                                  # reductions: four stages
     assert got[2][:5] == [16, 1024, 16384, 3, 608] and got[2][6] == 1
     assert got[3][:5] == [8, 4096, 32768, 7, 152] and got[3][6] == 0
+
+
+def test_dynamic_split_takes_every_item_once(program):
+    """The dynamic split's item map (csrc/tm_internal.h dyn_fetch, dyn_taper), which the streaming
+    kernel follows: every CTA's static prefix of stages + 1 items, then the counter's fetches, whole
+    batches until about taper x grid items are left and single items after, cover every item of
+    the launch exactly once, on random launches and the bench's shapes."""
+    rng = random.Random(13)
+    cases = [(4096, 7, 152, 1, 4), (32768, 4, 152, 4, 4), (16384, 7, 152, 1, 4), (16384, 3, 608, 1, 4),
+             (100, 7, 152, 4, 4), (1, 1, 1, 4, 4), (1065, 7, 152, 4, 0), (5000, 4, 152, 4, 100)]
+    for _ in range(300):
+        cases.append((rng.randint(1, 50000), rng.randint(1, 16), rng.randint(1, 700),
+                      rng.choice([1, 2, 4, 8, 16]), rng.choice([0, 1, 2, 4, 8])))
+    got = run(program, ["D %d %d %d %d %d" % c for c in cases])
+    for (nitems, stages, grid, batch, taper), (ok, batched, fetches, singles) in zip(cases, got):
+        assert ok == 1, (nitems, stages, grid, batch, taper)
+        rest = max(nitems - (stages + 1) * grid, 0)
+        if batch > 1:
+            assert batched == (rest - min(rest, grid * taper)) // batch
+            assert singles == rest - batched * batch  # the items after the batches go out singly
+        else:
+            assert batched == 0 and fetches == rest
