@@ -746,6 +746,31 @@ cudaError_t launch_copy_w(const SegArgs& a, uint32_t grid, size_t smem, cudaStre
 }
 }  // namespace
 
+// CTAs of the segment kernel (store or copy direction, cwarps consumer warps) that one SM holds with
+// `smem` bytes of dynamic shared memory each: the occupancy calculator's answer for the instance
+// that will run (its registers decide as much as its shared memory); 0 if it cannot say.
+int seg_resident_ctas(bool store, uint32_t cwarps, size_t smem)
+{
+    int n = 0;
+    auto ask = [&](auto k, uint32_t threads) {
+        if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, (int)threads, smem) != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 0;
+        }
+    };
+    if (store) {
+        if (cwarps == 16) ask(k_fb_seg_store<16>, seg_threads<16>());
+        else if (cwarps == 12) ask(k_fb_seg_store<12>, seg_threads<12>());
+        else ask(k_fb_seg_store<8>, seg_threads<8>());
+    } else {
+        if (cwarps == 16) ask(k_fb_seg_copy<16>, seg_threads<16>());
+        else if (cwarps == 12) ask(k_fb_seg_copy<12>, seg_threads<12>());
+        else ask(k_fb_seg_copy<8>, seg_threads<8>());
+    }
+    return n;
+}
+
 cudaError_t launch_fb_seg_store(const SegArgs& a, uint32_t grid, size_t smem, cudaStream_t st)
 {
     return a.cwarps == 16 ? launch_store_w<16>(a, grid, smem, st)

@@ -390,14 +390,16 @@ constexpr uint32_t kSegMaxStages = 8;
 // offset per image row.  Store (store = true): a stage holds the item's image block of each box of
 // the run (img_stride bytes each) and an 8-byte tensor address per image row.
 // Launch shape of the segment kernels: CTAs per SM, staging buffers of the copy and of the store,
-// consumer warps.  Measured on GB300 on the W4 rank-5 view with the dynamic item split (two runs
-// of each shape): three buffers took the copy from 5349-5362 to 5577-5618 GB/s (four: 4447-4661),
-// and twelve consumer warps took the store from 5235-5240 to 5379-5405 (its three buffers:
-// 5258-5348); one CTA per SM lost 7-25 % in both directions.
-constexpr uint64_t kSegCtasPerSm = 2;
+// consumer warps.  Measured on GB300 on the W4 rank-5 view with the dynamic item split: two CTAs
+// of eight warps and two buffers gave copy 5349-5362, store 5235-5240 GB/s; three buffers for the
+// copy and twelve warps, 5542-5618 and 5215-5405; three CTAs of eight warps with three buffers
+// each, 5583-5725 and 5430-5565 (five rounds against the previous shape on two boxes).  One CTA
+// per SM lost 7-25 %; more CTAs than the SM can hold (three of twelve warps: their registers allow
+// two) lost a quarter, which seg_fit keeps from happening.
+constexpr uint64_t kSegCtasPerSm = 3;
 constexpr uint64_t kSegCopyStages = 3;
-constexpr uint64_t kSegStoreStages = 2;
-constexpr uint64_t kSegWarps = 12;
+constexpr uint64_t kSegStoreStages = 3;
+constexpr uint64_t kSegWarps = 8;
 
 template <class Budget>
 inline bool seg_plan_rows(const FbArgs& a, uint64_t g1, uint32_t sms, uint32_t want,
@@ -471,21 +473,39 @@ inline bool seg_plan(const FbArgs& a, const tm_desc* d, uint32_t sms, uint32_t w
 // Launch shape of the vector path's copy (load direction), shared by every entry point that
 // launches one: the segment form when the map takes it (TM_FB_SEG: 0 never, 1 whenever the layout
 // allows, unset when its segments are long enough for bulk copies; TM_FB_SEG_CTAS_PER_SM and
-// TM_FB_SEG_STAGES, defaults kSegCtasPerSm and kSegCopyStages), else the per-window form
-// (TM_FB_COPY_CTAS_PER_SM, default 8).  Returns true for the
+// TM_FB_SEG_STAGES, defaults kSegCtasPerSm and kSegCopyStages, at most cap_per_sm CTAs per SM),
+// else the per-window form (TM_FB_COPY_CTAS_PER_SM, default 8).  Returns true for the
 // segment form (s filled), false for the per-window form (a.block_rows set).  budget(n) as for
 // fb_shape.
 template <class Budget>
 inline bool fb_copy_plan(FbArgs& a, const tm_desc* d, uint64_t nbox, uint32_t sms, Budget budget,
-                         SegArgs& s, uint32_t& grid, size_t& smem)
+                         SegArgs& s, uint32_t& grid, size_t& smem, uint64_t cap_per_sm = 8)
 {
-    if (seg_plan(a, d, sms, (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_CTAS_PER_SM", kSegCtasPerSm), 8),
+    const uint64_t want = std::min<uint64_t>(env_u64("TM_FB_SEG_CTAS_PER_SM", kSegCtasPerSm), cap_per_sm);
+    if (seg_plan(a, d, sms, (uint32_t)std::max<uint64_t>(std::min<uint64_t>(want, 8), 1),
                  (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_STAGES", kSegCopyStages), kSegMaxStages),
                  (int)env_u64("TM_FB_SEG", 2), false, budget, s, grid, smem))
         return true;
     fb_shape(a, nbox, sms, (uint32_t)std::min<uint64_t>(env_u64("TM_FB_COPY_CTAS_PER_SM", 8), 16),
              fb_copy_row_bytes(a.gspan0), budget, grid, smem);
     return false;
+}
+
+// A segment launch whose CTAs the SMs hold all at once: plan(cap) plans it with at most cap CTAs
+// per SM and returns false when the segment form does not apply.  seg_plan sizes a CTA's shared
+// memory only, and the kernel's registers can allow fewer CTAs per SM than planned (three CTAs of
+// twelve consumer warps: two); CTAs beyond what the SMs hold would run as a second, short wave.
+// So the planned launch goes to the occupancy calculator and is planned again with its answer.
+int seg_resident_ctas(bool store, uint32_t cwarps, size_t smem);  // k_fb_seg.cu
+
+template <class Plan>
+inline bool seg_fit(bool store, uint32_t sms, const SegArgs& s, const uint32_t& grid,
+                    const size_t& smem, Plan plan)
+{
+    if (!plan(8)) return false;
+    const int fit = seg_resident_ctas(store, s.cwarps, smem);
+    if (fit > 0 && (uint64_t)grid > (uint64_t)sms * (uint64_t)fit) return plan((uint64_t)fit);
+    return true;
 }
 
 // Ring consumer (stream_tiles).

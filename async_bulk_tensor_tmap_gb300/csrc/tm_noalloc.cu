@@ -179,8 +179,11 @@ extern "C" int tiled_copy_noalloc(const tm_desc* src, const int32_t* coords, siz
         size_t smem = 0;
         SegArgs sa;
         // the launch shape of tiled_copy's vector path (same rule, same tunables)
-        if (fb_copy_plan(a, src, n, (uint32_t)d->sms,
-                         [&](uint32_t per_sm) { return budget(*d, per_sm); }, sa, grid, smem)) {
+        const uint32_t sms = (uint32_t)d->sms;
+        auto cta_bytes = [&](uint32_t per_sm) { return budget(*d, per_sm); };
+        if (seg_fit(false, sms, sa, grid, smem, [&](uint64_t cap) {
+                return fb_copy_plan(a, src, n, sms, cta_bytes, sa, grid, smem, cap);
+            })) {
             e = launch_fb_seg_copy(sa, grid, smem, st);
         } else {
             e = launch_fb_copy(a, grid, smem, st);

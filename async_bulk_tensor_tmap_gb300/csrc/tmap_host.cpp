@@ -350,8 +350,11 @@ int copy_boxes(const tm_desc* src, const int32_t* coords, size_t nbox, void* ima
         uint32_t grid = 0;
         size_t smem = 0;
         SegArgs sa;
-        if (fb_copy_plan(a, src, n, (uint32_t)ds->sms,
-                         [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); }, sa, grid, smem)) {
+        const uint32_t sms = (uint32_t)ds->sms;
+        auto budget = [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); };
+        if (seg_fit(false, sms, sa, grid, smem, [&](uint64_t cap) {
+                return fb_copy_plan(a, src, n, sms, budget, sa, grid, smem, cap);
+            })) {
             sa.sched = sched_slot(*ds, st);
             rc = check_launch(launch_fb_seg_copy(sa, grid, smem, st), "fallback segment copy launch");
         } else {
@@ -602,11 +605,15 @@ int tiled_roundtrip(const tm_desc* dst, const int32_t* coords, size_t nbox, cons
         SegArgs sa;
         // The segment form of the store (TM_FB_SEG as for the copy): image blocks staged by bulk
         // copies, rows written by the consumer warps.
-        if (seg_plan(a, dst, (uint32_t)ds->sms,
-                     (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_CTAS_PER_SM", kSegCtasPerSm), 8),
-                     (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_STAGES", kSegStoreStages), kSegMaxStages),
-                     (int)env_u64("TM_FB_SEG", 2), true,
-                     [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); }, sa, grid, smem)) {
+        const uint32_t sms = (uint32_t)ds->sms;
+        auto budget = [&](uint32_t per_sm) { return cta_budget(*ds, per_sm); };
+        auto plan = [&](uint64_t cap) {
+            const uint64_t want = std::min<uint64_t>(env_u64("TM_FB_SEG_CTAS_PER_SM", kSegCtasPerSm), cap);
+            return seg_plan(a, dst, sms, (uint32_t)std::max<uint64_t>(std::min<uint64_t>(want, 8), 1),
+                            (uint32_t)std::min<uint64_t>(env_u64("TM_FB_SEG_STAGES", kSegStoreStages), kSegMaxStages),
+                            (int)env_u64("TM_FB_SEG", 2), true, budget, sa, grid, smem);
+        };
+        if (seg_fit(true, sms, sa, grid, smem, plan)) {
             sa.sched = sched_slot(*ds, st);
             rc = check_launch(launch_fb_seg_store(sa, grid, smem, st), "fallback segment store launch");
         } else {

@@ -47,7 +47,8 @@
  *       TM_STAGES, TM_STAGES_REDUCE   stage cap for copies, reductions (none, 4)
  *       TM_FB_SEG                 vector path segment form: 0 never, 1 whenever possible (auto)
  *       TM_FB_SEG_CTAS_PER_SM, TM_FB_SEG_STAGES, TM_FB_SEG_WARPS   segment kernels' shape
- *                                 (2; 3 copy / 2 store; 12 consumer warps: 8, 12 or 16)
+ *                                 (3, fewer if the SM cannot hold them; 3; 8 consumer warps:
+ *                                 8, 12 or 16)
  *       TM_FB_COPY_CTAS_PER_SM, TM_FB_STORE_CTAS_PER_SM   per-window vector kernels (8, 6)
  *       TM_RING_GROUPS, TM_RING_EVICT_FIRST, TM_RING_ROW_PAIRS, TM_RING_PREFETCH   stream_tiles
  *                                 (2 consumer groups, evict-first loads on, 0, 0)
