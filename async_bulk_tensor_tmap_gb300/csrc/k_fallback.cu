@@ -741,12 +741,31 @@ __global__ void __launch_bounds__(kThreads, 3) k_fb_reduce(const __grid_constant
     fb_reduce_rows<T, OP>(a);
 }
 
+namespace {
+// The grid cut to the CTAs the device's SMs hold at once (the occupancy calculator's answer for
+// this kernel, block size and shared memory): these kernels split their items by gridDim.x, so
+// fewer CTAs only take more items each, while CTAs beyond what the SMs hold would run as a second,
+// short wave (12 CTAs of 256 threads per SM asked for 3072 threads where an SM holds 2048).
+uint32_t resident_grid(void (*k)(const FbArgs), uint32_t grid, size_t smem)
+{
+    int per_sm = 0, dev = 0, sms = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k, kThreads, smem) != cudaSuccess ||
+        cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return grid;
+    }
+    const uint64_t hold = (uint64_t)per_sm * (uint64_t)sms;
+    return hold > 0 && hold < grid ? (uint32_t)hold : grid;
+}
+}  // namespace
+
 cudaError_t launch_fb_copy(const FbArgs& a, uint32_t grid, size_t smem, cudaStream_t s)
 {
     void (*k)(const FbArgs) = a.estride[0] != 1 ? k_fb_copy<true> : k_fb_copy<false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k<<<grid, kThreads, smem, s>>>(a);
+    k<<<resident_grid(k, grid, smem), kThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -755,7 +774,7 @@ cudaError_t launch_fb_store(const FbArgs& a, uint32_t grid, size_t smem, cudaStr
     void (*k)(const FbArgs) = a.estride[0] != 1 ? k_fb_store<true> : k_fb_store<false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    k<<<grid, kThreads, smem, s>>>(a);
+    k<<<resident_grid(k, grid, smem), kThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
